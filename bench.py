@@ -1,0 +1,432 @@
+#!/usr/bin/env python
+"""Benchmark of exact response-replay attention (one GRPO group replay over a
+captured, paged long prompt) on GB300.
+
+One step = capture-side page write of the whole prompt (A1) + serial replay of
+the G group members (A2-A8: forward, preprocess, backward of each member into
+one reused workspace).  Metric: algorithmic replay flops per second
+(forward 4 + backward 6 times R*P*d*Hq for the prompt part, 4 + 10 times
+d*Hq*R(R+1)/2 for the causal response part), with prompt-KV GB/s and replays/s
+alongside.  Default workload: 2,097,152-position prompt in 8192 pages of 256,
+24/4 heads, d=256, G=8 members of 4096 tokens, bf16.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the float64 CPU oracle arm
+
+Under torchrun each rank runs its own replica of the workload (members are
+independent; no data-path collective), the timing is the max over ranks and
+value is the whole-job aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "replay attn fwd+bwd TFLOP/s and prompt-KV GB/s at 2M-token prefix; replays/s"
+DEFAULT_WORKLOAD = "bf16_p2m_r4096_g8"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def replay_flops(P, R, hq, d):
+    return 10.0 * R * P * d * hq + 14.0 * d * hq * R * (R + 1) / 2.0
+
+
+def peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            d = json.loads(p.read_text())
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        self.f.flush()
+        rows = []
+        try:
+            for line in open(self.f.name):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        finally:
+            os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+
+
+def recorded_traffic(kernel: str, workload: str, source_file: Path):
+    """Per-launch DRAM bytes recorded by an ncu capture in profiles/ for this
+    kernel and workload, or None when absent or taken on another source."""
+    p = ROOT / "profiles" / f"{kernel}_{workload}.md"
+    if not p.exists():
+        return None
+    sha = hashlib.sha256(source_file.read_bytes()).hexdigest()[:16]
+    vals = {}
+    for line in p.read_text().splitlines():
+        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_sha")):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha") != sha or "traffic_bytes_per_launch" not in vals:
+        return None
+    return float(vals["traffic_bytes_per_launch"])
+
+
+# --------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import long_context_grpo_replay_gb300.binding as ls
+    from long_context_grpo_replay_gb300 import build, inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    build.build()
+    ls.lib()
+    w = inputs.WORKLOADS[args.workload]
+    G, P, d, hq, hkv = w.group, w.prompt_len, w.head_dim, w.hq, w.hkv
+    tdt = inputs.torch_dtype(w)
+    desc = ls.desc_for(hq, hkv, d, w.page_size, tdt, w.scale)
+
+    # ---- device-resident inputs (seeded synthetic, generated on the device)
+    src = inputs.make_prompt_source(w.with_(seed=w.seed + 1000 * rank), dev)
+    pool_shape = (w.pool_pages, hkv, w.page_size, d)
+    k_pool = torch.empty(pool_shape, dtype=tdt, device=dev)
+    v_pool = torch.empty(pool_shape, dtype=tdt, device=dev)
+    pt = src["page_table"]
+    prompt = ls.prompt_from(k_pool, v_pool, pt, P)
+    members = []
+    for g in range(G):
+        m = inputs.make_member(w.with_(seed=w.seed + 1000 * rank), g, dev)
+        R = m["q"].shape[0]
+        m.update(o=torch.empty_like(m["q"]), lse=torch.empty(R, hq, device=dev, dtype=torch.float32),
+                 delta=torch.empty(R, hq, device=dev, dtype=torch.float32),
+                 dq=torch.empty_like(m["q"]),
+                 dk=torch.empty_like(m["k"]), dv=torch.empty_like(m["v"]))
+        members.append(m)
+    ws = torch.empty(ls.ls_replay_workspace_size(desc, prompt, max(w.resp_lens)),
+                     dtype=torch.uint8, device=dev)
+    ls.ls_clear_device_status(ws)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ls.ls_kv_page_write(desc, k_pool, v_pool, pt, 0, src["k"], src["v"], ws, stream)
+        ls.ls_replay_group(desc, prompt, members, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ls.ls_read_device_status(ws)
+
+    # ---- timed region: K steps, events on the launching stream
+    ls.ls_trace_enable(True)
+    ls.ls_trace_reset()
+    launches0 = ls.ls_launch_count()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    launches = ls.ls_launch_count() - launches0
+    ms_total = e0.elapsed_time(e1)
+    trace = ls.kernel_trace()
+    ls.ls_trace_enable(False)
+    ls.ls_read_device_status(ws)
+    clocks = clk.summary()
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    flops_step = sum(replay_flops(P, R, hq, d) for R in w.resp_lens)
+    value = flops_step * world / (ms_step * 1e-3) / 1e12
+    kv_bytes_pass = P * hkv * d * 2 * (2 if tdt == torch.bfloat16 else 4)
+    kv_gbs = 2 * G * kv_bytes_pass * world / (ms_step * 1e-3) / 1e9
+
+    # ---- roofline of the dominant kernel (time from the traced events)
+    pk, pk_src = peaks()
+    dom = max(("tc_fwd", "tc_bwd_dq", "simt_fwd", "simt_bwd_dq"),
+              key=lambda k: trace.get(k, (0, 0.0))[1])
+    n_l, t_l = trace.get(dom, (0, 0.0))
+    per_launch_ms = t_l / max(1, n_l)
+    coef = 4.0 if dom.endswith("fwd") else 6.0
+    flops_launch = sum(coef * R * P * d * hq for R in w.resp_lens) / G
+    bytes_launch = kv_bytes_pass
+    R_mean = sum(w.resp_lens) / G
+    if R_mean >= 128:
+        achieved = flops_launch / (per_launch_ms * 1e-3) / 1e12
+        peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak}
+    else:
+        achieved = bytes_launch / (per_launch_ms * 1e-3) / 1e9
+        peak = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak}
+    src_file = ROOT / "long_context_grpo_replay_gb300" / "csrc" / (
+        "ls_tc_fwd.cu" if dom == "tc_fwd" else "ls_tc_bwd.cu" if dom == "tc_bwd_dq" else "ls_simt.cu")
+    roof["traffic"] = recorded_traffic(dom, args.workload, src_file)
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{pk_src} ({'bf16_tflops_sustained' if roof['bound'] == 'tensor' else 'hbm_gbs'})"
+    roof["algorithmic_per_launch"] = flops_launch if roof["bound"] == "tensor" else bytes_launch
+    roof["launch_ms"] = per_launch_ms
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, desc, src, members, k_pool, v_pool, pt, prompt, ws, stream, dev,
+                      flops_step, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, k_pool, v_pool, pt, members, budget_s=args.cpu_budget)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic (seeded N(0,1)/sqrt(d) Q/K/V, N(0,1) dO, random page table)",
+            "config": {"workload": args.workload, "prompt_len": P, "resp_lens": list(w.resp_lens),
+                       "group": G, "hq": hq, "hkv": hkv, "head_dim": d,
+                       "page_size": w.page_size, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (prompt K/V %.1f GiB per pass)" %
+                             (kv_bytes_pass / 2**30)},
+            "prompt_kv_gbs": round(kv_gbs, 1),
+            "replays_per_s": round(G * world / (ms_step * 1e-3), 4),
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "kernels_ms_per_step": {k: round(v[1] / args.steps, 3) for k, v in trace.items()},
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, desc, src, members, k_pool, v_pool, pt, prompt, ws, stream, dev, flops_step,
+            world):
+    """Same step through the public API with pinned host inputs: H2D of the
+    prompt K/V, page table and member inputs, the replay, D2H of the outputs."""
+    import torch
+    import long_context_grpo_replay_gb300.binding as ls
+
+    h_src = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in src.items()}
+    for k in h_src:
+        h_src[k].copy_(src[k])
+    in_keys = ("q", "k", "v", "d_o")
+    out_keys = ("o", "lse", "dq", "dk", "dv")
+    h_in = [{k: torch.empty(m[k].shape, dtype=m[k].dtype, pin_memory=True).copy_(m[k])
+             for k in in_keys} for m in members]
+    h_out = [{k: torch.empty(m[k].shape, dtype=m[k].dtype, pin_memory=True) for k in out_keys}
+             for m in members]
+    h2d = sum(t.numel() * t.element_size() for t in h_src.values()) + \
+        sum(t.numel() * t.element_size() for m in h_in for t in m.values())
+    d2h = sum(t.numel() * t.element_size() for m in h_out for t in m.values())
+
+    def step():
+        for k in h_src:
+            src[k].copy_(h_src[k], non_blocking=True)
+        for m, hm in zip(members, h_in):
+            for k in in_keys:
+                m[k].copy_(hm[k], non_blocking=True)
+        ls.ls_kv_page_write(desc, k_pool, v_pool, src["page_table"], 0, src["k"], src["v"], ws,
+                            stream)
+        ls.ls_replay_group(desc, prompt, members, ws, stream)
+        for m, hm in zip(members, h_out):
+            for k in out_keys:
+                hm[k].copy_(m[k], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, 2))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": round(flops_step * world / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 3), "steps": n, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h)}
+
+
+def _oracle_sample(w, k_pool, v_pool, pt, member, rows, kv=0):
+    """Oracle forward+backward of response rows `rows` of the query heads of KV
+    head `kv` (a bounded sample of the workload); returns (seconds, flops)."""
+    import oracle.ref as ref
+
+    gq = w.hq // w.hkv
+    hs = slice(kv * gq, (kv + 1) * gq)
+    t0 = time.perf_counter()
+    ref.replay_member(k_pool[:, kv:kv + 1], v_pool[:, kv:kv + 1], pt, w.prompt_len,
+                      member["q"][:, hs], member["k"][:, kv:kv + 1], member["v"][:, kv:kv + 1],
+                      member["d_o"][:, hs], scale=w.scale, rows=rows)
+    dt = time.perf_counter() - t0
+    d = w.head_dim
+    flops = sum(gq * (10.0 * w.prompt_len * d + 14.0 * d * (int(r) + 1)) for r in rows)
+    return dt, flops
+
+
+def cpu_baseline(w, k_pool, v_pool, pt, members, budget_s=20.0):
+    import numpy as np
+    import torch
+
+    kp = k_pool.cpu()
+    vp = v_pool.cpu()
+    ptc = pt.cpu()
+    m0 = {k: members[0][k].cpu() for k in ("q", "k", "v", "d_o")}
+    R = m0["q"].shape[0]
+    rows = np.array([R - 1])
+    dt, fl = _oracle_sample(w, kp, vp, ptc, m0, rows)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"member 0, response row {R - 1} of the {w.hq // w.hkv} query heads of KV "
+                      f"head 0, forward+backward over all {w.prompt_len} prompt keys "
+                      f"(float64 numpy; {dt:.1f} s)",
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args):
+    """The reference arm: the float64 CPU oracle timed on this host, on a
+    bounded sample of the same workload per step."""
+    import numpy as np
+    import torch
+
+    from long_context_grpo_replay_gb300 import inputs
+
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    w = inputs.WORKLOADS[args.workload]
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    pr = inputs.make_prompt(w, gen_dev)
+    kp, vp, pt = pr["k_pool"].cpu(), pr["v_pool"].cpu(), pr["page_table"].cpu()
+    m0 = {k: v.cpu() for k, v in inputs.make_member(w, 0, gen_dev).items()}
+    del pr
+    R = m0["q"].shape[0]
+    rows = np.array([R - 1])
+    for _ in range(args.warmup):
+        _oracle_sample(w, kp, vp, pt, m0, rows)
+    tot_t, tot_f = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, fl = _oracle_sample(w, kp, vp, pt, m0, rows)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    sample = (f"per step: member 0, response row {R - 1} of the {w.hq // w.hkv} query heads of "
+              f"KV head 0, forward+backward over all {w.prompt_len} prompt keys (float64 numpy)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "prompt_len": w.prompt_len,
+                   "resp_lens": list(w.resp_lens), "group": w.group, "hq": w.hq, "hkv": w.hkv,
+                   "head_dim": w.head_dim, "page_size": w.page_size},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

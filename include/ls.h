@@ -1,0 +1,229 @@
+/*
+ * ls.h -- C ABI of the response-replay attention library (libls).
+ *
+ * The operator: exact response-replay attention for GRPO post-training with a
+ * shared, detached long prompt.  The prompt is run once without gradients and
+ * its full-attention K/V are kept as compact pages ("Capture once", LongStraw
+ * DeepRead summary, section "Method").  Each group member's short response is
+ * then replayed on its own: its queries attend over every prompt key through
+ * the page table and causally over the response's own keys, partial results
+ * are recombined exactly by log-sum-exp (the "global LSE/output merge" of the
+ * Qwen path, same section; "exact attention composition", LongStraw abstract),
+ * and the backward treats the prompt K/V as constants (the stored prompt state
+ * is stop-gradient, DeepRead summary "Method", last paragraph; review mind map
+ * "Equation1到3": the d(loss)/d(z_P) d(z_P)/d(theta) term is omitted).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  Shapes: Hq query heads, Hkv KV heads (Hq % Hkv == 0), head dim d, page
+ *  size S_p; query head h reads KV head h / (Hq/Hkv).  R = response length,
+ *  P = prompt length.  Response row i sees all P prompt keys and response keys
+ *  j <= i.  The softmax scale is a parameter (normally 1/sqrt(d)).
+ *  Layouts (all row-major, contiguous, device memory unless stated):
+ *    prompt pools   k_pool, v_pool : [pool_pages][Hkv][S_p][d]   element dtype
+ *    page table                    : int32 [num_pages], logical page -> slot
+ *    q, d_o, o, dq                 : [R][Hq][d]                  element dtype
+ *    k_resp, v_resp, dk, dv        : [R][Hkv][d]                 element dtype
+ *    lse, delta                    : float32 [R][Hq]; lse is the natural log
+ *                                    of the softmax denominator, scale included
+ *  Element dtype is uniform per call (LS_DTYPE_F32 or LS_DTYPE_BF16);
+ *  accumulation is always float32.
+ *
+ *  Ownership: the caller allocates every buffer.  The library never allocates
+ *  or frees device memory.  It keeps a small host-side cache (tensor-map
+ *  descriptors) and per-process trace counters, nothing else.  The prompt
+ *  pools are read-only for every replay call.
+ *
+ *  Workspace: one caller-owned device buffer of ls_replay_workspace_size()
+ *  bytes, sized for the longest response, reused by every member (the
+ *  workspace does not grow with the group size).  Its first 256 bytes hold a
+ *  device status word that kernels set on device-side errors.
+ *
+ *  Errors: every call validates its arguments on the host before any launch
+ *  and returns a status; nothing aborts.  Device-side problems (a page-table
+ *  entry outside the pool, a bounded wait that ran out) set bits in the
+ *  workspace status word and the affected work is skipped; the call itself has
+ *  already returned LS_OK by then, so read them with ls_read_device_status().
+ *  ls_last_error() gives a one-line reason for the last failing call on the
+ *  calling thread.
+ *
+ *  Streams: every compute call is asynchronous on the given stream
+ *  (a cudaStream_t passed as void*; NULL = legacy default stream).  Calls are
+ *  thread-safe when they use distinct workspaces.
+ */
+#ifndef LS_H_
+#define LS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LS_API __attribute__((visibility("default")))
+#else
+#define LS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LS_OK = 0,
+  LS_ERR_INVALID_ARGUMENT = 1,   /* null pointer, bad size, misaligned buffer */
+  LS_ERR_UNSUPPORTED = 2,        /* valid but unsupported shape or dtype */
+  LS_ERR_WORKSPACE_TOO_SMALL = 3,
+  LS_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed */
+  LS_ERR_DEVICE_BOUNDS = 5,      /* device saw a page id outside the pool */
+  LS_ERR_DEVICE_TIMEOUT = 6      /* a device-side bounded wait ran out */
+} ls_status;
+
+typedef enum { LS_DTYPE_F32 = 0, LS_DTYPE_BF16 = 1 } ls_dtype;
+
+/* Shape and numerics of one attention layer.
+ * dtype: ls_dtype of every element buffer.  head_dim in {64, 128, 256};
+ * page_size >= 1.  softmax_scale > 0 and finite. */
+typedef struct {
+  int32_t dtype;
+  int32_t hq;
+  int32_t hkv;
+  int32_t head_dim;
+  int32_t page_size;
+  float softmax_scale;
+} ls_attn_desc;
+
+/* The captured prompt of one layer: pools plus page table (device pointers).
+ * Logical prompt position t lives in slot page_table[t / page_size] at row
+ * t % page_size.  Requires num_pages * page_size >= prompt_len; rows of the
+ * last page beyond prompt_len are never read as keys (they may hold anything,
+ * NaN included). */
+typedef struct {
+  const void* k_pool;
+  const void* v_pool;
+  int64_t pool_pages;
+  const int32_t* page_table;
+  int64_t num_pages;
+  int64_t prompt_len;
+} ls_prompt_kv;
+
+/* One group member for ls_replay_group.  Inputs q, k, v, d_o; outputs o, lse,
+ * delta (rowsum(dO*O), written as a by-product), dq, dk, dv. */
+typedef struct {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* d_o;
+  int32_t resp_len;
+  int32_t reserved;
+  void* o;
+  float* lse;
+  float* delta;
+  void* dq;
+  void* dk;
+  void* dv;
+} ls_member;
+
+/* A1. Capture-side page write (DeepRead summary, "Method", "Capture once";
+ * review section 二.2: the full-attention layers keep their K/V in pages).
+ * Scatters token t of k, v ([n_tok][Hkv][d]) to
+ *   pool[page_table[(start_pos+t)/S_p]][kv][(start_pos+t)%S_p][:].
+ * page_table holds num_pages entries; requires start_pos + n_tok <=
+ * num_pages * S_p.  Entries outside [0, pool_pages) are skipped on the device
+ * and, if ws is non-NULL, reported through its status word.  Bit-exact copy.
+ * ws may be NULL (then ws_bytes is ignored). */
+LS_API ls_status ls_kv_page_write(const ls_attn_desc* desc, void* k_pool, void* v_pool,
+                           int64_t pool_pages, const int32_t* page_table,
+                           int64_t num_pages, int64_t start_pos, int64_t n_tok,
+                           const void* k, const void* v, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/* Workspace bytes needed by ls_replay_fwd / ls_replay_bwd / ls_replay_group
+ * for responses of up to max_resp_len tokens against this prompt on the
+ * current device.  Host-only; does not touch the device. */
+LS_API ls_status ls_replay_workspace_size(const ls_attn_desc* desc, const ls_prompt_kv* prompt,
+                                   int32_t max_resp_len, size_t* bytes);
+
+/* A2+A3+A4. Replay forward: O [R][Hq][d] (element dtype) and LSE [R][Hq]
+ * (float32, natural log, scale included) of softmax attention over all prompt
+ * keys plus the causal response keys.  The prompt part runs split over page
+ * ranges into float32 partials held in ws, the response part adds one more
+ * partial, and an exact LSE merge writes o and lse (DeepRead summary,
+ * "Method", Qwen path).  resp_len == 0 is a no-op. */
+LS_API ls_status ls_replay_fwd(const ls_attn_desc* desc, const ls_prompt_kv* prompt,
+                        const void* q, const void* k_resp, const void* v_resp,
+                        int32_t resp_len, void* o, float* lse, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/* A4. Exact log-sum-exp merge of partial attention results (the "global
+ * LSE/output merge" of the DeepRead summary, "Method"):
+ *   L[n] = log sum_s exp(Lp[s][n]);  O[n] = sum_s exp(Lp[s][n] - L[n]) Op[s][n].
+ * o_parts float32 [n_parts][n_rows][head_dim], lse_parts float32
+ * [n_parts][n_rows], natural log; a part with Lp = -inf contributes nothing;
+ * a row whose parts are all -inf gets O = 0, L = -inf.  o is written in
+ * out_dtype, lse as float32 (lse may be NULL).  head_dim % 4 == 0. */
+LS_API ls_status ls_lse_merge(int32_t n_parts, int64_t n_rows, int32_t head_dim,
+                       const float* o_parts, const float* lse_parts, int32_t out_dtype,
+                       void* o, float* lse, void* stream);
+
+/* A5. Backward preprocess: delta[r][h] = sum_c dO[r][h][c] * O[r][h][c]
+ * (float32 accumulation of the element-dtype inputs). */
+LS_API ls_status ls_replay_bwd_preprocess(const ls_attn_desc* desc, const void* o, const void* d_o,
+                                   int32_t resp_len, float* delta, void* stream);
+
+/* A6+A7. Replay backward with the prompt state detached (DeepRead summary,
+ * "Method": stored prompt state is stop-gradient; review section 二, last
+ * paragraph: on the Qwen path only the query gradient crosses ranks).
+ * Recomputes P = exp(s - LSE) from the stored lse (no score matrix is kept),
+ * dS = P * (dO.v - delta), and returns
+ *   dq      [R][Hq][d]  = scale * sum over prompt and visible response keys of dS k
+ *   dk_resp [R][Hkv][d] = scale * sum over the group's heads, rows i >= j of dS q
+ *   dv_resp [R][Hkv][d] = sum over the group's heads, rows i >= j of P dO
+ * No gradient is produced for prompt K/V.  lse and delta come from
+ * ls_replay_fwd and ls_replay_bwd_preprocess. */
+LS_API ls_status ls_replay_bwd(const ls_attn_desc* desc, const ls_prompt_kv* prompt,
+                        const void* q, const void* k_resp, const void* v_resp,
+                        const void* d_o, const float* lse, const float* delta,
+                        int32_t resp_len, void* dq, void* dk_resp, void* dv_resp,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/* A8. Serial suffix replay of a group (DeepRead summary, "Method", "Serial
+ * suffix replay"; abstract: "rebuilds one policy response under autograd,
+ * backpropagates, and pops to the prompt boundary").  For each member in order:
+ * forward, preprocess, backward, all on one stream and into the one workspace,
+ * so only one member's intermediates are live and the workspace does not grow
+ * with n_members.  Each member's results equal a standalone replay of it. */
+LS_API ls_status ls_replay_group(const ls_attn_desc* desc, const ls_prompt_kv* prompt,
+                          int32_t n_members, const ls_member* members, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/* Synchronises the stream, then reports the device status word of ws
+ * (LS_OK, LS_ERR_DEVICE_BOUNDS or LS_ERR_DEVICE_TIMEOUT) and clears it. */
+LS_API ls_status ls_read_device_status(void* ws, size_t ws_bytes, void* stream);
+
+/* Zeroes the workspace status word (asynchronous on the stream). */
+LS_API ls_status ls_clear_device_status(void* ws, size_t ws_bytes, void* stream);
+
+LS_API const char* ls_status_string(ls_status status);
+/* One-line reason for the last non-OK status returned on this thread. */
+LS_API const char* ls_last_error(void);
+
+/* Tracing.  When enabled, every kernel launch is bracketed by CUDA events on
+ * its own stream and accumulated per kernel id; ls_trace_read synchronises
+ * those events and reports launches and total milliseconds since the last
+ * reset.  ls_launch_count counts every kernel this library launched in this
+ * process (traced or not). */
+LS_API ls_status ls_trace_enable(int32_t on);
+LS_API ls_status ls_trace_reset(void);
+LS_API ls_status ls_trace_read(int32_t kernel_id, int64_t* launches, double* total_ms);
+LS_API int32_t ls_num_kernel_ids(void);
+LS_API const char* ls_kernel_name(int32_t kernel_id);
+LS_API int64_t ls_launch_count(void);
+
+/* Which prompt-attention implementation the current device and desc select:
+ * 1 = tcgen05/TMEM tensor-core kernels, 0 = CUDA-core kernels. */
+LS_API int32_t ls_uses_tensor_cores(const ls_attn_desc* desc);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LS_H_ */

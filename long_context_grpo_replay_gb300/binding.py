@@ -1,0 +1,297 @@
+"""Thin ctypes binding of libls, one Python function per C entry point, with
+the same names.  Only argument marshalling happens here (torch tensors to
+device pointers, structs, the current CUDA stream); every step of the replay
+path runs in the library's kernels.  A missing library is an error: there is
+no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from pathlib import Path
+
+__all__ = [
+    "LsError", "lib", "library_path", "AttnDesc", "PromptKV", "Member",
+    "LS_DTYPE_F32", "LS_DTYPE_BF16",
+    "ls_kv_page_write", "ls_replay_workspace_size", "ls_replay_fwd", "ls_lse_merge",
+    "ls_replay_bwd_preprocess", "ls_replay_bwd", "ls_replay_group",
+    "ls_read_device_status", "ls_clear_device_status", "ls_status_string", "ls_last_error",
+    "ls_trace_enable", "ls_trace_reset", "ls_trace_read", "ls_num_kernel_ids",
+    "ls_kernel_name", "ls_launch_count", "ls_uses_tensor_cores", "kernel_trace",
+    "desc_for", "prompt_from", "EXPORTED_SYMBOLS",
+]
+
+LS_DTYPE_F32 = 0
+LS_DTYPE_BF16 = 1
+
+EXPORTED_SYMBOLS = [
+    "ls_kv_page_write", "ls_replay_workspace_size", "ls_replay_fwd", "ls_lse_merge",
+    "ls_replay_bwd_preprocess", "ls_replay_bwd", "ls_replay_group", "ls_read_device_status",
+    "ls_clear_device_status", "ls_status_string", "ls_last_error", "ls_trace_enable",
+    "ls_trace_reset", "ls_trace_read", "ls_num_kernel_ids", "ls_kernel_name",
+    "ls_launch_count", "ls_uses_tensor_cores",
+]
+
+
+class LsError(RuntimeError):
+    def __init__(self, status: int, name: str, detail: str):
+        super().__init__(f"{name}: {detail}")
+        self.status = status
+        self.name = name
+
+
+class AttnDesc(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("hq", ctypes.c_int32), ("hkv", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("softmax_scale", ctypes.c_float)]
+
+
+class PromptKV(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("pool_pages", ctypes.c_int64), ("page_table", ctypes.c_void_p),
+                ("num_pages", ctypes.c_int64), ("prompt_len", ctypes.c_int64)]
+
+
+class Member(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("d_o", ctypes.c_void_p), ("resp_len", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("delta", ctypes.c_void_p), ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p),
+                ("dv", ctypes.c_void_p)]
+
+
+def library_path() -> Path:
+    return Path(os.environ.get("LS_LIBRARY",
+                               Path(__file__).resolve().parent / "_lib" / "libls.so"))
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libls; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not path.exists():
+        raise RuntimeError(
+            f"libls not found at {path}; build it first (python -c 'import __graft_entry__ as g; "
+            "g.build()' or python long_context_grpo_replay_gb300/build.py)")
+    L = ctypes.CDLL(str(path))
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    sig = {
+        "ls_kv_page_write": [ctypes.POINTER(AttnDesc), P, P, I64, P, I64, I64, I64, P, P, P, SZ, P],
+        "ls_replay_workspace_size": [ctypes.POINTER(AttnDesc), ctypes.POINTER(PromptKV), I32,
+                                     ctypes.POINTER(SZ)],
+        "ls_replay_fwd": [ctypes.POINTER(AttnDesc), ctypes.POINTER(PromptKV), P, P, P, I32, P, P,
+                          P, SZ, P],
+        "ls_lse_merge": [I32, I64, I32, P, P, I32, P, P, P],
+        "ls_replay_bwd_preprocess": [ctypes.POINTER(AttnDesc), P, P, I32, P, P],
+        "ls_replay_bwd": [ctypes.POINTER(AttnDesc), ctypes.POINTER(PromptKV), P, P, P, P, P, P,
+                          I32, P, P, P, P, SZ, P],
+        "ls_replay_group": [ctypes.POINTER(AttnDesc), ctypes.POINTER(PromptKV), I32,
+                            ctypes.POINTER(Member), P, SZ, P],
+        "ls_read_device_status": [P, SZ, P],
+        "ls_clear_device_status": [P, SZ, P],
+        "ls_trace_enable": [I32],
+        "ls_trace_reset": [],
+        "ls_trace_read": [I32, ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double)],
+        "ls_uses_tensor_cores": [ctypes.POINTER(AttnDesc)],
+    }
+    for name, args in sig.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int32
+    for name, res, args in [("ls_status_string", ctypes.c_char_p, [I32]),
+                            ("ls_last_error", ctypes.c_char_p, []),
+                            ("ls_num_kernel_ids", I32, []),
+                            ("ls_kernel_name", ctypes.c_char_p, [I32]),
+                            ("ls_launch_count", I64, [])]:
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = L
+    return L
+
+
+def _check(status: int):
+    if status != 0:
+        L = lib()
+        raise LsError(status, L.ls_status_string(status).decode(), L.ls_last_error().decode())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(dt) -> int:
+    import torch
+    if dt == torch.float32:
+        return LS_DTYPE_F32
+    if dt == torch.bfloat16:
+        return LS_DTYPE_BF16
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def desc_for(hq, hkv, head_dim, page_size, dtype, softmax_scale=None) -> AttnDesc:
+    """Build an AttnDesc; dtype may be a torch dtype or an LS_DTYPE_* code."""
+    code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
+    scale = softmax_scale if softmax_scale is not None else head_dim ** -0.5
+    return AttnDesc(code, hq, hkv, head_dim, page_size, scale)
+
+
+def prompt_from(k_pool, v_pool, page_table, prompt_len) -> PromptKV:
+    """PromptKV over device tensors (pools [pool_pages, Hkv, S_p, d], int32 table)."""
+    if prompt_len == 0:
+        return PromptKV(None, None, 0, None, 0, 0)
+    return PromptKV(_ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(page_table),
+                    page_table.shape[0], prompt_len)
+
+
+# ------------------------------------------------------------------ entry points
+def ls_kv_page_write(desc, k_pool, v_pool, page_table, start_pos, k, v, ws=None, stream=None):
+    _want_dtype(desc, k_pool, v_pool, k, v)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().ls_kv_page_write(ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool),
+                                  k_pool.shape[0], _ptr(page_table), page_table.shape[0],
+                                  start_pos, k.shape[0], _ptr(k), _ptr(v), _ptr(ws), ws_bytes,
+                                  _stream(stream)))
+
+
+def ls_replay_workspace_size(desc, prompt, max_resp_len) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().ls_replay_workspace_size(ctypes.byref(desc), ctypes.byref(prompt),
+                                          max_resp_len, ctypes.byref(out)))
+    return out.value
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def _want_f32(*ts):
+    import torch
+    for t in ts:
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"lse/delta/partials must be float32 tensors, got {t.dtype}")
+
+
+def _want_dtype(desc, *ts):
+    for t in ts:
+        if t is not None and _dtype_code(t.dtype) != desc.dtype:
+            raise TypeError(f"tensor dtype {t.dtype} does not match the descriptor dtype")
+
+
+def ls_replay_fwd(desc, prompt, q, k_resp, v_resp, o, lse, ws, stream=None):
+    _want_f32(lse)
+    _want_dtype(desc, q, k_resp, v_resp, o)
+    _check(lib().ls_replay_fwd(ctypes.byref(desc), ctypes.byref(prompt), _ptr(q), _ptr(k_resp),
+                               _ptr(v_resp), q.shape[0], _ptr(o), _ptr(lse), _ptr(ws),
+                               _nbytes(ws), _stream(stream)))
+
+
+def ls_lse_merge(o_parts, lse_parts, o, lse=None, stream=None):
+    n_parts, n_rows, d = o_parts.shape
+    _want_f32(o_parts, lse_parts, lse)
+    _check(lib().ls_lse_merge(n_parts, n_rows, d, _ptr(o_parts), _ptr(lse_parts),
+                              _dtype_code(o.dtype), _ptr(o), _ptr(lse), _stream(stream)))
+
+
+def ls_replay_bwd_preprocess(desc, o, d_o, delta, stream=None):
+    _want_f32(delta)
+    _want_dtype(desc, o, d_o)
+    _check(lib().ls_replay_bwd_preprocess(ctypes.byref(desc), _ptr(o), _ptr(d_o), o.shape[0],
+                                          _ptr(delta), _stream(stream)))
+
+
+def ls_replay_bwd(desc, prompt, q, k_resp, v_resp, d_o, lse, delta, dq, dk, dv, ws, stream=None):
+    _want_f32(lse, delta)
+    _want_dtype(desc, q, k_resp, v_resp, d_o, dq, dk, dv)
+    _check(lib().ls_replay_bwd(ctypes.byref(desc), ctypes.byref(prompt), _ptr(q), _ptr(k_resp),
+                               _ptr(v_resp), _ptr(d_o), _ptr(lse), _ptr(delta), q.shape[0],
+                               _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), _nbytes(ws),
+                               _stream(stream)))
+
+
+def ls_replay_group(desc, prompt, members, ws, stream=None):
+    """members: sequence of dicts with tensors q, k, v, d_o, o, lse, delta, dq, dk, dv."""
+    arr = (Member * max(1, len(members)))()
+    for i, m in enumerate(members):
+        _want_f32(m["lse"], m["delta"])
+        _want_dtype(desc, m["q"], m["k"], m["v"], m["d_o"], m["o"], m["dq"], m["dk"], m["dv"])
+        arr[i] = Member(_ptr(m["q"]), _ptr(m["k"]), _ptr(m["v"]), _ptr(m["d_o"]),
+                        m["q"].shape[0], 0, _ptr(m["o"]), _ptr(m["lse"]), _ptr(m["delta"]),
+                        _ptr(m["dq"]), _ptr(m["dk"]), _ptr(m["dv"]))
+    _check(lib().ls_replay_group(ctypes.byref(desc), ctypes.byref(prompt), len(members), arr,
+                                 _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def ls_read_device_status(ws, stream=None):
+    _check(lib().ls_read_device_status(_ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def ls_clear_device_status(ws, stream=None):
+    _check(lib().ls_clear_device_status(_ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def ls_status_string(status: int) -> str:
+    return lib().ls_status_string(status).decode()
+
+
+def ls_last_error() -> str:
+    return lib().ls_last_error().decode()
+
+
+def ls_trace_enable(on: bool = True):
+    _check(lib().ls_trace_enable(1 if on else 0))
+
+
+def ls_trace_reset():
+    _check(lib().ls_trace_reset())
+
+
+def ls_trace_read(kernel_id: int):
+    n = ctypes.c_int64(0)
+    ms = ctypes.c_double(0.0)
+    _check(lib().ls_trace_read(kernel_id, ctypes.byref(n), ctypes.byref(ms)))
+    return n.value, ms.value
+
+
+def ls_num_kernel_ids() -> int:
+    return lib().ls_num_kernel_ids()
+
+
+def ls_kernel_name(kernel_id: int) -> str:
+    return lib().ls_kernel_name(kernel_id).decode()
+
+
+def ls_launch_count() -> int:
+    return lib().ls_launch_count()
+
+
+def ls_uses_tensor_cores(desc) -> bool:
+    return lib().ls_uses_tensor_cores(ctypes.byref(desc)) != 0
+
+
+def kernel_trace() -> dict:
+    """{kernel name: (launches, total ms)} accumulated since the last reset."""
+    out = {}
+    for k in range(ls_num_kernel_ids()):
+        n, ms = ls_trace_read(k)
+        if n:
+            out[ls_kernel_name(k)] = (n, ms)
+    return out

@@ -1,0 +1,123 @@
+// Internal declarations shared by the libls translation units (not installed).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ls.h"
+
+namespace ls {
+
+// Bits of the device status word (first 4 bytes of the workspace).
+enum : uint32_t {
+  kStatusBadPage = 1u,   // a page-table entry pointed outside the pool
+  kStatusTimeout = 2u,   // a bounded device wait gave up
+};
+
+// Bytes at the head of the workspace reserved for the status word.
+constexpr size_t kWsHeader = 256;
+
+// Kernel ids used by tracing (ls_trace_read / ls_kernel_name).
+enum KernelId : int32_t {
+  kKPageWrite = 0,
+  kKSimtFwd,
+  kKTcFwd,
+  kKLseMerge,
+  kKBwdPre,
+  kKSimtBwdDq,
+  kKTcBwdDq,
+  kKSimtDkDv,
+  kKTcDkDv,
+  kKDqReduce,
+  kNumKernelIds
+};
+
+// Launch bookkeeping (ls_api.cu): count every launch, optionally bracket it
+// with events on its stream.
+struct LaunchScope {
+  LaunchScope(int32_t kid, cudaStream_t s);
+  ~LaunchScope();
+  int32_t kid;
+  cudaStream_t stream;
+  void* ev0;
+  void* ev1;
+};
+
+// Rows of one KV group are numbered t = hh * R + r (hh = head within group).
+// Output row index is n = r * Hq + h with h = g * Gq + hh.
+
+// Common geometry of the attention kernels.
+struct AttnGeom {
+  int32_t hq, hkv, gq, d, page_size;
+  int32_t R;             // response length
+  int64_t P;             // prompt length
+  int64_t pool_pages;
+  float scale;           // softmax scale
+  float scale_log2;      // scale * log2(e)
+  int32_t ns;            // prompt splits (part ns is the response part)
+  int64_t split_span;    // prompt keys per split (a multiple of every key tile)
+};
+
+struct FwdParams {
+  AttnGeom g;
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* page_table;
+  const void* k_resp;
+  const void* v_resp;
+  float* o_parts;    // [n_parts][R*Hq][d]
+  float* lse_parts;  // [n_parts][R*Hq]
+  uint32_t* status;
+};
+
+struct BwdParams {
+  AttnGeom g;
+  const void* q;
+  const void* d_o;
+  const float* lse;    // [R][Hq]
+  const float* delta;  // [R][Hq]
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* page_table;
+  const void* k_resp;
+  const void* v_resp;
+  float* dq_parts;     // [n_parts][R*Hq][d], unscaled
+  void* dk;            // [R][Hkv][d] element dtype
+  void* dv;
+  uint32_t* status;
+};
+
+// CUDA-core kernels (ls_simt.cu)
+cudaError_t launch_page_write(int dtype, int hkv, int d, int page_size, void* k_pool,
+                              void* v_pool, int64_t pool_pages, const int32_t* pt,
+                              int64_t start_pos, int64_t n_tok, const void* k,
+                              const void* v, uint32_t* status, cudaStream_t s);
+cudaError_t launch_simt_fwd(int dtype, const FwdParams& p, cudaStream_t s);
+cudaError_t launch_simt_fwd_resp(int dtype, const FwdParams& p, cudaStream_t s);
+cudaError_t launch_lse_merge(int n_parts, int64_t n_rows, int d, const float* o_parts,
+                             const float* lse_parts, int out_dtype, void* o, float* lse,
+                             cudaStream_t s);
+cudaError_t launch_bwd_preprocess(int dtype, int64_t n_rows, int d, const void* o,
+                                  const void* d_o, float* delta, cudaStream_t s);
+cudaError_t launch_simt_bwd_dq(int dtype, const BwdParams& p, cudaStream_t s);
+cudaError_t launch_simt_bwd_dq_resp(int dtype, const BwdParams& p, cudaStream_t s);
+cudaError_t launch_simt_dkdv(int dtype, const BwdParams& p, cudaStream_t s);
+cudaError_t launch_dq_reduce(int n_parts, int64_t n_rows, int d, float scale,
+                             const float* parts, int out_dtype, void* dq, cudaStream_t s);
+
+// Tensor-core kernels (ls_tc_fwd.cu, ls_tc_bwd.cu): bf16, d = 256,
+// page_size % 128 == 0, sm_100-family device.  Query tiles are 128 rows;
+// split spans are multiples of kTcSpanQuantum keys.
+constexpr int kTcRows = 128;
+constexpr int kTcSpanQuantum = 128;
+cudaError_t launch_tc_fwd(const FwdParams& p, cudaStream_t s);
+cudaError_t launch_tc_bwd_dq(const BwdParams& p, cudaStream_t s);
+
+// 2-D TMA map over a bf16 matrix [rows][256] with [box_rows x 64] boxes and
+// the 128-byte swizzle (ls_api.cu; cuTensorMapEncodeTiled resolved once
+// through the runtime, no -lcuda).
+bool encode_pool_map(CUtensorMap* m, const void* base, int64_t rows, int box_rows);
+
+}  // namespace ls

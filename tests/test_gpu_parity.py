@@ -1,0 +1,260 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle on
+the same seeded inputs, element by element (all rows where the oracle is
+fast, seeded sampled rows at multi-million-token prompts).
+
+Tolerances: max|gpu - oracle| / max|oracle| <= 1e-5 (fp32) or 2e-2 (bf16)
+per tensor; |LSE_gpu - LSE_oracle| <= 1e-3."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import long_context_grpo_replay_gb300.binding as ls
+import oracle.ref as ref
+from long_context_grpo_replay_gb300 import inputs
+from gpu_helpers import (DevicePrompt, check_member, rel_err, run_group, sample_rows,
+                         alloc_member, oracle_member)
+
+pytestmark = pytest.mark.gpu
+W = inputs.WORKLOADS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from long_context_grpo_replay_gb300 import build
+
+    build.build()
+    ls.lib()
+
+
+def _members(w, dev="cpu"):
+    return [inputs.make_member(w, g, dev) for g in range(w.group)]
+
+
+# --------------------------------------------------------------------------
+# the five workload configurations
+# --------------------------------------------------------------------------
+def test_tiny_f32_full(cuda_device):
+    w = W["tiny_f32"]
+    dp = DevicePrompt(w, cuda_device)
+    ms = _members(w)
+    out = run_group(dp, ms, dp.workspace(max(w.resp_lens)), cuda_device)
+    for g, (o, m) in enumerate(zip(out, ms)):
+        check_member(dp, o, m, label=f"tiny member {g}")
+
+
+def test_bf16_p32k_r2048_g2(cuda_device):
+    w = W["bf16_p32k_r2048"]
+    dp = DevicePrompt(w, cuda_device)
+    assert ls.ls_uses_tensor_cores(dp.desc)
+    ms = _members(w)
+    out = run_group(dp, ms, dp.workspace(max(w.resp_lens)), cuda_device)
+    check_member(dp, out[0], ms[0], label="p32k member 0 (all rows)")
+    check_member(dp, out[1], ms[1], rows=sample_rows(2048, 21), label="p32k member 1")
+
+
+def test_bf16_p256k_r4096_g8_kscaled(cuda_device):
+    w = W["bf16_p256k_r4096_g8"]
+    dp = DevicePrompt(w, cuda_device, gen_device=cuda_device)
+    ms = [inputs.make_member(w, g, cuda_device) for g in range(w.group)]
+    out = run_group(dp, ms, dp.workspace(max(w.resp_lens)), cuda_device)
+    for g in (0, 7):
+        hm = {k: v.cpu() for k, v in ms[g].items()}
+        check_member(dp, out[g], hm, rows=sample_rows(4096, 30 + g), label=f"p256k member {g}")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["bf16_p2m_r4096_g8", "bf16_p2m_r64_g8"])
+def test_bf16_p2m(cuda_device, name):
+    w = W[name]
+    dp = DevicePrompt(w, cuda_device, gen_device=cuda_device)
+    ms = [inputs.make_member(w, g, cuda_device) for g in range(w.group)]
+    out = run_group(dp, ms, dp.workspace(max(w.resp_lens)), cuda_device)
+    hm = {k: v.cpu() for k, v in ms[0].items()}
+    R = w.resp_lens[0]
+    check_member(dp, out[0], hm, rows=sample_rows(R, 40), label=f"{name} member 0")
+
+
+@pytest.mark.slow
+def test_bf16_stress_p4m_ragged(cuda_device):
+    w = W["bf16_p4m_ragged_g8"]
+    dp = DevicePrompt(w, cuda_device, gen_device=cuda_device)
+    ms = [inputs.make_member(w, g, cuda_device) for g in range(w.group)]
+    out = run_group(dp, ms, dp.workspace(max(w.resp_lens)), cuda_device)
+    g = int(np.argmin(w.resp_lens))
+    hm = {k: v.cpu() for k, v in ms[g].items()}
+    check_member(dp, out[g], hm, rows=sample_rows(w.resp_lens[g], 50),
+                 label=f"stress member {g} (R={w.resp_lens[g]})")
+
+
+# --------------------------------------------------------------------------
+# shapes that span several tiles and splits with ragged tails, both paths
+# --------------------------------------------------------------------------
+SMALL = [
+    # name, hq, hkv, d, page, P, R list, dtype, wide logits
+    ("tc_ragged", 24, 4, 256, 256, 1000, (37, 130), "bf16", False),
+    ("tc_wide_multi_split", 24, 4, 256, 256, 20000, (300,), "bf16", True),
+    ("tc_exact_tiles", 24, 4, 256, 256, 4096, (128, 256), "bf16", True),
+    ("tc_single_row", 24, 4, 256, 256, 777, (1,), "bf16", True),
+    ("tc_prompt_free", 24, 4, 256, 256, 0, (200,), "bf16", True),
+    ("tc_one_key", 24, 4, 256, 256, 1, (5,), "bf16", True),
+    ("simt_bf16_d64", 8, 2, 64, 16, 333, (40,), "bf16", True),
+    ("simt_bf16_d128", 6, 3, 128, 32, 500, (17, 3), "bf16", False),
+    ("simt_f32_d256", 12, 2, 256, 64, 700, (33,), "f32", True),
+    ("simt_f32_page1", 4, 2, 64, 1, 50, (9,), "f32", True),
+    ("simt_f32_gqa1", 3, 3, 64, 16, 100, (20,), "f32", True),
+]
+
+
+def _small_inputs(spec, dev):
+    name, hq, hkv, d, page, P, Rs, dt, wide = spec
+    w = inputs.Workload(name, hq, hkv, d, page, P, Rs, dt, seed=zlib.crc32(name.encode()) % 1000,
+                        pool_factor=2, poison=True)
+    dp = DevicePrompt(w, dev)
+    ms = _members(w)
+    if wide:
+        # logits of standard deviation ~1 (Q and K ~ N(0,1)): a peaked softmax
+        # in which a missing key, tile or split shows up
+        s = float(np.sqrt(d))
+        for m in ms:
+            m["q"] = (m["q"].float() * s).to(m["q"].dtype)
+            m["k"] = (m["k"].float() * s).to(m["k"].dtype)
+        dp.host["k_pool"] = (dp.host["k_pool"].float() * s).to(dp.host["k_pool"].dtype)
+        dp.k_pool.copy_(dp.host["k_pool"].to(dev))
+    return w, dp, ms
+
+
+@pytest.mark.parametrize("spec", SMALL, ids=[s[0] for s in SMALL])
+def test_small_shapes(cuda_device, spec):
+    w, dp, ms = _small_inputs(spec, cuda_device)
+    expect_tc = spec[0].startswith("tc_")
+    assert ls.ls_uses_tensor_cores(dp.desc) == expect_tc
+    out = run_group(dp, ms, dp.workspace(max(w.resp_lens)), cuda_device)
+    for g, (o, m) in enumerate(zip(out, ms)):
+        check_member(dp, o, m, label=f"{spec[0]} member {g}")
+
+
+# --------------------------------------------------------------------------
+# invariants the pages state: physical placement and group schedule do not
+# change the result; kernels are deterministic
+# --------------------------------------------------------------------------
+def _outputs(members):
+    return [{k: m[k].clone() for k in ("o", "lse", "delta", "dq", "dk", "dv")} for m in members]
+
+
+def test_page_permutation_bitwise_invariance(cuda_device):
+    spec = ("tc_perm", 24, 4, 256, 256, 3000, (100,), "bf16", True)
+    w, dp, ms = _small_inputs(spec, cuda_device)
+    ws = dp.workspace(100)
+    a = _outputs(run_group(dp, ms, ws, cuda_device))
+    g = torch.Generator().manual_seed(9)
+    perm = torch.randperm(dp.k_pool.shape[0], generator=g).to(cuda_device)
+    k2 = torch.empty_like(dp.k_pool)
+    v2 = torch.empty_like(dp.v_pool)
+    k2[perm] = dp.k_pool
+    v2[perm] = dp.v_pool
+    pt2 = perm[dp.page_table.long()].to(torch.int32)
+    dp.k_pool, dp.v_pool, dp.page_table = k2, v2, pt2
+    dp.prompt = ls.prompt_from(k2, v2, pt2, w.prompt_len)
+    b = _outputs(run_group(dp, ms, ws, cuda_device))
+    for key in a[0]:
+        assert torch.equal(a[0][key], b[0][key]), key
+
+
+def test_group_equals_standalone_any_order_and_deterministic(cuda_device):
+    spec = ("tc_group", 24, 4, 256, 256, 2500, (64, 200, 129), "bf16", True)
+    w, dp, ms = _small_inputs(spec, cuda_device)
+    ws = dp.workspace(200)
+    grp = _outputs(run_group(dp, ms, ws, cuda_device))
+    grp2 = _outputs(run_group(dp, ms, ws, cuda_device))
+    ws.fill_(0xFF)  # stale workspace contents (NaN pattern) must not matter
+    ls.ls_clear_device_status(ws)
+    for g in (2, 0, 1):
+        m = alloc_member({k: v.to(cuda_device) for k, v in ms[g].items()}, w.hq)
+        ls.ls_replay_fwd(dp.desc, dp.prompt, m["q"], m["k"], m["v"], m["o"], m["lse"], ws)
+        ls.ls_replay_bwd_preprocess(dp.desc, m["o"], m["d_o"], m["delta"])
+        ls.ls_replay_bwd(dp.desc, dp.prompt, m["q"], m["k"], m["v"], m["d_o"], m["lse"],
+                         m["delta"], m["dq"], m["dk"], m["dv"], ws)
+        for key in grp[g]:
+            assert torch.equal(grp[g][key], m[key]), (g, key)
+            assert torch.equal(grp[g][key], grp2[g][key]), (g, key, "run-to-run")
+    ls.ls_read_device_status(ws)
+
+
+# --------------------------------------------------------------------------
+# the individual calls
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_kv_page_write_bit_exact(cuda_device, dt):
+    w = inputs.Workload("pw", 24, 4, 256, 256, 5000, (1,), dt, seed=3, pool_factor=2)
+    src = inputs.make_prompt_source(w, "cpu")
+    tdt = inputs.torch_dtype(w)
+    pool_shape = (w.pool_pages, w.hkv, w.page_size, w.head_dim)
+    kp = torch.full(pool_shape, float("nan"), dtype=tdt)
+    vp = kp.clone()
+    start = 300
+    k, v = src["k"][: w.prompt_len - start], src["v"][: w.prompt_len - start]
+    ref.kv_page_write(kp, vp, src["page_table"], w.page_size, start, k, v)
+    desc = ls.desc_for(w.hq, w.hkv, w.head_dim, w.page_size, tdt)
+    kd = torch.full(pool_shape, float("nan"), dtype=tdt, device=cuda_device)
+    vd = kd.clone()
+    ls.ls_kv_page_write(desc, kd, vd, src["page_table"].to(cuda_device), start,
+                        k.to(cuda_device), v.to(cuda_device))
+    torch.cuda.synchronize()
+    # bit-exact, NaN poison of untouched rows included (compare the raw bits)
+    bits = torch.int16 if dt == "bf16" else torch.int32
+    assert torch.equal(kd.cpu().view(bits), kp.view(bits))
+    assert torch.equal(vd.cpu().view(bits), vp.view(bits))
+
+
+@pytest.mark.parametrize("out_dt", [torch.float32, torch.bfloat16])
+def test_lse_merge_call(cuda_device, out_dt):
+    g = torch.Generator().manual_seed(5)
+    n_parts, n_rows, d = 7, 333, 256
+    o_parts = torch.randn(n_parts, n_rows, d, generator=g)
+    lse_parts = torch.randn(n_parts, n_rows, generator=g) * 20
+    lse_parts[2, :50] = float("-inf")
+    lse_parts[:, 100] = float("-inf")
+    o = torch.empty(n_rows, d, dtype=out_dt, device=cuda_device)
+    lse = torch.empty(n_rows, device=cuda_device, dtype=torch.float32)
+    ls.ls_lse_merge(o_parts.to(cuda_device), lse_parts.to(cuda_device), o, lse)
+    o_ref, l_ref = ref.lse_merge(o_parts, lse_parts)
+    tol = 1e-5 if out_dt == torch.float32 else 8e-3
+    assert rel_err(o.double().cpu().numpy(), o_ref) <= tol
+    lg = lse.double().cpu().numpy()
+    fin = np.isfinite(l_ref)
+    assert np.abs(lg[fin] - l_ref[fin]).max() <= 1e-4
+    assert np.isneginf(lg[100]) and not torch.isnan(o).any()
+
+
+def test_bwd_preprocess_call(cuda_device):
+    g = torch.Generator().manual_seed(6)
+    o = torch.randn(77, 24, 256, generator=g).to(torch.bfloat16)
+    do = torch.randn(77, 24, 256, generator=g).to(torch.bfloat16)
+    desc = ls.desc_for(24, 4, 256, 256, torch.bfloat16)
+    delta = torch.empty(77, 24, device=cuda_device, dtype=torch.float32)
+    ls.ls_replay_bwd_preprocess(desc, o.to(cuda_device), do.to(cuda_device), delta)
+    want = ref.bwd_preprocess(o, do)
+    assert rel_err(delta.double().cpu().numpy(), want) <= 1e-5
+
+
+# --------------------------------------------------------------------------
+# device-side error reporting: a bad page id is reported, never faults
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("tc", [True, False])
+def test_bad_page_id_is_reported(cuda_device, tc):
+    spec = ("bad_page", 24, 4, 256 if tc else 64, 256 if tc else 16, 1500, (40,), "bf16", False)
+    w, dp, ms = _small_inputs(spec, cuda_device)
+    assert ls.ls_uses_tensor_cores(dp.desc) == tc
+    pt = dp.page_table.clone()
+    pt[1] = dp.k_pool.shape[0] + 5  # outside the pool
+    dp.prompt = ls.prompt_from(dp.k_pool, dp.v_pool, pt, w.prompt_len)
+    ws = dp.workspace(40)
+    m = alloc_member({k: v.to(cuda_device) for k, v in ms[0].items()}, w.hq)
+    ls.ls_replay_fwd(dp.desc, dp.prompt, m["q"], m["k"], m["v"], m["o"], m["lse"], ws)
+    with pytest.raises(ls.LsError) as ei:
+        ls.ls_read_device_status(ws)
+    assert ei.value.status == 5
+    ls.ls_read_device_status(ws)  # cleared by the read; the context is still usable
+    torch.cuda.synchronize()

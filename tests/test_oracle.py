@@ -13,7 +13,15 @@ import torch
 
 import oracle.ref as ref
 
-torch.set_default_dtype(torch.float64)
+
+
+@pytest.fixture(autouse=True)
+def _float64_default():
+    """float64 as torch's default dtype inside this module only."""
+    old = torch.get_default_dtype()
+    torch.set_default_dtype(torch.float64)
+    yield
+    torch.set_default_dtype(old)
 
 
 def _case(P=40, R=7, Hq=4, Hkv=2, d=8, page=8, seed=0, pool_extra=3, scale_logits=1.0):
