@@ -254,8 +254,7 @@ ls_status fwd_impl(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const v
   fp.o_parts = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
   fp.lse_parts = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader + pl.o_bytes);
   if (tc) {
-    if (pl.ns > 0) LS_CUDA(launch_tc_fwd(fp, s), "tensor-core forward launch");
-    LS_CUDA(launch_simt_fwd_resp(desc->dtype, fp, s), "response forward launch");
+    LS_CUDA(launch_tc_fwd(fp, s), "tensor-core forward launch");
   } else {
     LS_CUDA(launch_simt_fwd(desc->dtype, fp, s), "forward launch");
   }
@@ -298,15 +297,18 @@ ls_status bwd_impl(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const v
   bp.dv = dv;
   bp.status = reinterpret_cast<uint32_t*>(ws);
   if (tc) {
-    if (pl.ns > 0) LS_CUDA(launch_tc_bwd_dq(bp, s), "tensor-core backward launch");
-    LS_CUDA(launch_simt_bwd_dq_resp(desc->dtype, bp, s), "response backward launch");
+    LS_CUDA(launch_tc_bwd_dq(bp, s), "tensor-core backward launch");
   } else {
     LS_CUDA(launch_simt_bwd_dq(desc->dtype, bp, s), "backward launch");
   }
   LS_CUDA(launch_dq_reduce(pl.n_parts, (int64_t)R * desc->hq, desc->head_dim,
                            desc->softmax_scale, bp.dq_parts, desc->dtype, dq, s),
           "dQ reduce launch");
-  LS_CUDA(launch_simt_dkdv(desc->dtype, bp, s), "response dK/dV launch");
+  if (tc) {
+    LS_CUDA(launch_tc_dkdv(bp, s), "tensor-core response dK/dV launch");
+  } else {
+    LS_CUDA(launch_simt_dkdv(desc->dtype, bp, s), "response dK/dV launch");
+  }
   return LS_OK;
 }
 
@@ -334,11 +336,12 @@ LaunchScope::~LaunchScope() {
 }
 
 // ------------------------------------------------------------------ TMA maps
-bool encode_pool_map(CUtensorMap* m, const void* base, int64_t rows, int box_rows) {
-  typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encoder() {
   static EncodeTiledFn enc = []() -> EncodeTiledFn {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -348,12 +351,30 @@ bool encode_pool_map(CUtensorMap* m, const void* base, int64_t rows, int box_row
       return nullptr;
     return reinterpret_cast<EncodeTiledFn>(fn);
   }();
+  return enc;
+}
+}  // namespace
+
+bool encode_pool_map(CUtensorMap* m, const void* base, int64_t rows, int box_rows) {
+  EncodeTiledFn enc = encoder();
   if (!enc) return false;
   cuuint64_t gdim[2] = {256u, (cuuint64_t)rows};
   cuuint64_t gstr[1] = {256u * 2u};
   cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1u, 1u};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstr, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_rows_map(CUtensorMap* m, const void* base, int heads, int64_t rows, int box_rows) {
+  EncodeTiledFn enc = encoder();
+  if (!enc) return false;
+  cuuint64_t gdim[3] = {256u, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t gstr[2] = {256u * 2u, (cuuint64_t)heads * 256u * 2u};
+  cuuint32_t box[3] = {64u, 1u, (cuuint32_t)box_rows};
+  cuuint32_t es[3] = {1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstr, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -119,5 +119,10 @@ cudaError_t launch_tc_bwd_dq(const BwdParams& p, cudaStream_t s);
 // the 128-byte swizzle (ls_api.cu; cuTensorMapEncodeTiled resolved once
 // through the runtime, no -lcuda).
 bool encode_pool_map(CUtensorMap* m, const void* base, int64_t rows, int box_rows);
+// 3-D TMA map over a bf16 tensor [rows][heads][256] with [box_rows x 1 x 64]
+// boxes and the 128-byte swizzle (response K/V, Q, dO); rows past the end
+// read as zeros.
+bool encode_rows_map(CUtensorMap* m, const void* base, int heads, int64_t rows, int box_rows);
+cudaError_t launch_tc_dkdv(const BwdParams& p, cudaStream_t s);
 
 }  // namespace ls

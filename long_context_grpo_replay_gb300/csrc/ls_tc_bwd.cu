@@ -21,6 +21,7 @@
 #include <math_constants.h>
 
 #include <cstdlib>
+#include <cstring>
 
 #include "ls_internal.h"
 #include "ls_tc.cuh"
@@ -79,7 +80,9 @@ struct BwdKParams {
 template <int BN, int KSK, int KSV>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const BwdKParams p) {
+                     const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmKr,
+                     const __grid_constant__ CUtensorMap tmVr, const BwdKParams p) {
   using L = BwdLayout<BN, KSK, KSV>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_kf[KSK], bar_ke[KSK], bar_vf[KSV], bar_ve[KSV], bar_sd[2],
@@ -92,12 +95,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = sbase + L::kQ, sO = sbase + L::kO, sK = sbase + L::kK, sV = sbase + L::kV;
 
+  // parts 0..ns-1: prompt key ranges; part ns: the causal response keys
   const int mt = blockIdx.x % p.n_mt;
   const int kvh = (blockIdx.x / p.n_mt) % p.hkv;
   const int part = blockIdx.x / (p.n_mt * p.hkv);
-  const int64_t span = p.split_span;
-  const int64_t kb = (int64_t)part * span;
-  const int64_t ke = kb + span < p.P ? kb + span : p.P;
+  const bool resp = part == p.ns;
+  const int64_t rows_g = (int64_t)p.gq * p.R;
+  int64_t kb, ke;
+  if (!resp) {
+    kb = (int64_t)part * p.split_span;
+    ke = kb + p.split_span < p.P ? kb + p.split_span : p.P;
+  } else {
+    const int64_t t0 = (int64_t)mt * kBM;
+    const int64_t t1 = (t0 + kBM < rows_g ? t0 + kBM : rows_g) - 1;
+    kb = 0;
+    ke = (t0 / p.R == t1 / p.R) ? (t1 % p.R) + 1 : p.R;
+  }
   const int ntiles = ke > kb ? (int)((ke - kb + BN - 1) / BN) : 0;
 
   if (tid == 0) {
@@ -146,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && ntiles > 0) {
       const bool isK = warp == 0;
       const int nst = isK ? KSK : KSV;
-      const CUtensorMap* tm = isK ? &tmK : &tmV;
+      const CUtensorMap* tm = resp ? (isK ? &tmKr : &tmVr) : (isK ? &tmK : &tmV);
       uint64_t* full = isK ? bar_kf : bar_vf;
       uint64_t* empty = isK ? bar_ke : bar_ve;
       const uint32_t sdst = isK ? sK : sV;
@@ -158,12 +171,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           fail();
           break;
         }
-        const int32_t row = pool_row(kb + (int64_t)j * BN);
+        const int64_t key0 = kb + (int64_t)j * BN;
         const uint32_t fb = smem_u32(&full[st]);
         mbar_expect_tx(fb, L::kKVBytes);
+        if (resp) {
 #pragma unroll
-        for (int c = 0; c < kD / 64; ++c)
-          tma_load_2d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, row);
+          for (int c = 0; c < kD / 64; ++c)
+            tma_load_3d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, kvh, (int32_t)key0);
+        } else {
+          const int32_t row = pool_row(key0);
+#pragma unroll
+          for (int c = 0; c < kD / 64; ++c)
+            tma_load_2d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, row);
+        }
         issued = j + 1;
       }
       for (int j = issued - nst < 0 ? 0 : issued - nst; j < issued; ++j)
@@ -229,7 +249,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax
     const int i = tid - 128;
     const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
-    const int64_t rows_g = (int64_t)p.gq * p.R;
     const int64_t t = (int64_t)mt * kBM + i;
     const bool row_ok = t < rows_g;
     const int hh = row_ok ? (int)(t / p.R) : 0;
@@ -263,7 +282,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(smem_u32(&bar_sd[b]), (j >> 1) & 1, abortp)) { fail(); ok = false; break; }
       tc_fence_after();
       const int64_t key0 = kb + (int64_t)j * BN;
-      const int nvalid = (int)(ke - key0 < BN ? ke - key0 : BN);
+      const int64_t lim = resp ? (int64_t)r + 1 : ke;  // causal limit for the response part
+      const int nvalid = (int)(lim - key0 < 0 ? 0 : (lim - key0 < BN ? lim - key0 : BN));
+      const int nvalid_tile = (int)(ke - key0 < BN ? ke - key0 : BN);
       uint32_t ds_pk[BN / 2];
 #pragma unroll
       for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -287,13 +308,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c0 = 0; c0 < BN / 2; c0 += 16)
         tmem_st16(tbase + lane_off + L::kTmemS + b * 2 * BN + c0, ds_pk + c0);
       tmem_wait_st();
-      if (nvalid < BN) {
-        // Partial last tile: rows past the prompt end may hold anything; zero
-        // them in K so that dS=0 times K stays 0 in dQ += dS K.
+      if (!resp && nvalid_tile < BN) {
+        // Partial last prompt tile: rows past the prompt end may hold
+        // anything; zero them in K so that dS=0 times K stays 0 in dQ += dS K.
         const int st = j % KSK;
-        const int nz = (BN - nvalid) * (kD / 64) * 8;
+        const int nz = (BN - nvalid_tile) * (kD / 64) * 8;
         for (int z = i; z < nz; z += 128) {
-          const int row = nvalid + z / ((kD / 64) * 8);
+          const int row = nvalid_tile + z / ((kD / 64) * 8);
           const int box = (z / 8) % (kD / 64);
           st_shared_v4(sK + st * L::kKVBytes + box * L::kKVBox + row * 128 + (z & 7) * 16,
                        make_uint4(0u, 0u, 0u, 0u));
@@ -363,17 +384,22 @@ cudaError_t bwd_variant(const BwdParams& a, cudaStream_t s) {
   p.page_table = a.page_table;
   p.dq_parts = a.dq_parts;
   p.status = a.status;
-  CUtensorMap tk, tv;
-  if (!encode_pool_map(&tk, a.k_pool, p.pool_rows, BN) ||
-      !encode_pool_map(&tv, a.v_pool, p.pool_rows, BN))
+  CUtensorMap tk, tv, tkr, tvr;
+  memset(&tk, 0, sizeof(tk));
+  memset(&tv, 0, sizeof(tv));
+  if (g.P > 0 && (!encode_pool_map(&tk, a.k_pool, p.pool_rows, BN) ||
+                  !encode_pool_map(&tv, a.v_pool, p.pool_rows, BN)))
+    return cudaErrorInvalidValue;
+  if (!encode_rows_map(&tkr, a.k_resp, g.hkv, g.R, BN) ||
+      !encode_rows_map(&tvr, a.v_resp, g.hkv, g.R, BN))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_dq_kernel<BN, KSK, KSV>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kSmem);
   if (e != cudaSuccess) return e;
-  const int64_t units = (int64_t)g.ns * g.hkv * p.n_mt;
+  const int64_t units = (int64_t)(g.ns + 1) * g.hkv * p.n_mt;
   if (units == 0) return cudaSuccess;
   LaunchScope ls(kKTcBwdDq, s);
-  tc_bwd_dq_kernel<BN, KSK, KSV><<<(unsigned)units, kThreads, L::kSmem, s>>>(tk, tv, p);
+  tc_bwd_dq_kernel<BN, KSK, KSV><<<(unsigned)units, kThreads, L::kSmem, s>>>(tk, tv, tkr, tvr, p);
   return cudaGetLastError();
 }
 

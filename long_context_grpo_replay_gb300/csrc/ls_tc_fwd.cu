@@ -3,9 +3,10 @@
 // One CTA owns a work unit (KV head g, 128-row query tile, key part):
 //   rows  : t = hh*R + r over the Gq query heads of KV head g (so the K/V tile
 //           staged in shared memory serves all Gq heads of the group),
-//   keys  : a contiguous range of logical prompt positions, streamed page by
-//           page through the page table with TMA (a key tile never crosses a
-//           page), or the response keys with the causal mask.
+//   keys  : part s < ns: a contiguous range of logical prompt positions,
+//           streamed page by page through the page table with TMA (a key tile
+//           never crosses a page); part ns: the response keys with the causal
+//           mask, read through a 3-D map over [R][Hkv][256].
 // Output: float32 partial O (normalised) and partial LSE (natural log) for
 // the part, merged exactly afterwards by the LSE-merge kernel ("global
 // LSE/output merge", LongStraw DeepRead summary, section "Method").
@@ -86,6 +87,7 @@ struct FwdKParams {
 template <int BN, int KST, bool P_TMEM>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmKr, const __grid_constant__ CUtensorMap tmVr,
                   const FwdKParams p) {
   using L = FwdLayout<BN, KST, P_TMEM>;
   extern __shared__ uint8_t smem_raw[];
@@ -99,13 +101,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = sbase + L::kQ, sK = sbase + L::kK, sV = sbase + L::kV, sP = sbase + L::kP;
 
-  // ---- work unit
+  // ---- work unit: parts 0..ns-1 are prompt key ranges, part ns the
+  // response keys (causal; only keys up to the tile's last row are visited)
   const int mt = blockIdx.x % p.n_mt;
   const int kvh = (blockIdx.x / p.n_mt) % p.hkv;
   const int part = blockIdx.x / (p.n_mt * p.hkv);
-  const int64_t span = p.split_span;
-  const int64_t kb = (int64_t)part * span;
-  const int64_t ke = kb + span < p.P ? kb + span : p.P;
+  const bool resp = part == p.ns;
+  const int64_t rows_g = (int64_t)p.gq * p.R;
+  int64_t kb, ke;
+  if (!resp) {
+    kb = (int64_t)part * p.split_span;
+    ke = kb + p.split_span < p.P ? kb + p.split_span : p.P;
+  } else {
+    const int64_t t0 = (int64_t)mt * kBM;
+    const int64_t t1 = (t0 + kBM < rows_g ? t0 + kBM : rows_g) - 1;
+    kb = 0;
+    ke = (t0 / p.R == t1 / p.R) ? (t1 % p.R) + 1 : p.R;
+  }
   const int ntiles = ke > kb ? (int)((ke - kb + BN - 1) / BN) : 0;
 
   if (tid == 0) {
@@ -156,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producers
     if (lane == 0 && ntiles > 0) {
       const bool isK = warp == 0;
-      const CUtensorMap* tm = isK ? &tmK : &tmV;
+      const CUtensorMap* tm = resp ? (isK ? &tmKr : &tmVr) : (isK ? &tmK : &tmV);
       uint64_t* full = isK ? bar_kf : bar_vf;
       uint64_t* empty = isK ? bar_ke : bar_ve;
       const uint32_t sdst = isK ? sK : sV;
@@ -168,12 +180,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           fail();
           break;
         }
-        const int32_t row = pool_row(kb + (int64_t)j * BN);
+        const int64_t key0 = kb + (int64_t)j * BN;
         const uint32_t fb = smem_u32(&full[st]);
         mbar_expect_tx(fb, L::kKVBytes);
+        if (resp) {
+          // response rows past R read as zeros
 #pragma unroll
-        for (int c = 0; c < kD / 64; ++c)
-          tma_load_2d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, row);
+          for (int c = 0; c < kD / 64; ++c)
+            tma_load_3d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, kvh, (int32_t)key0);
+        } else {
+          const int32_t row = pool_row(key0);
+#pragma unroll
+          for (int c = 0; c < kD / 64; ++c)
+            tma_load_2d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, row);
+        }
         issued = j + 1;
       }
       // make sure no copy is still landing in shared memory when the CTA ends
@@ -233,7 +253,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax
     const int i = tid - 128;           // query row in the tile == TMEM lane
     const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
-    const int64_t rows_g = (int64_t)p.gq * p.R;
     const int64_t t = (int64_t)mt * kBM + i;
     const bool row_ok = t < rows_g;
     const int hh = row_ok ? (int)(t / p.R) : 0;
@@ -275,7 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 32; ++c) s[c0 + c] = __uint_as_float(rr[c]);
       }
       const int64_t key0 = kb + (int64_t)j * BN;
-      const int nvalid = (int)(ke - key0 < BN ? ke - key0 : BN);
+      // keys of this tile visible to this row: the prompt range end, or the
+      // causal limit r for the response part (row r sees response keys <= r)
+      const int64_t lim = resp ? (int64_t)r + 1 : ke;
+      const int nvalid = (int)(lim - key0 < 0 ? 0 : (lim - key0 < BN ? lim - key0 : BN));
+      const int nvalid_tile = (int)(ke - key0 < BN ? ke - key0 : BN);
       float mx = -CUDART_INF_F;
 #pragma unroll
       for (int c = 0; c < BN; ++c) {
@@ -327,20 +350,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           st_shared_v4(sP + b * L::kPBytes + (c >> 3) * (kBM * 128) + sw128_offset(i, c & 7), v);
         }
       }
-      if (nvalid < BN) {
-        // Partial last tile: rows past the prompt end may hold anything (NaN
-        // included); zero them in V so that P=0 times V stays 0.
+      if (!resp && nvalid_tile < BN) {
+        // Partial last prompt tile: rows past the prompt end may hold anything
+        // (NaN included); zero them in V so that P=0 times V stays 0.
         const int st = j % KST;
         if (!mbar_wait(smem_u32(&bar_vf[st]), (j / KST) & 1, abortp)) { fail(); ok = false; break; }
-        const int nz = (BN - nvalid) * (kD / 64) * 8;  // 16-byte chunks
+        const int nz = (BN - nvalid_tile) * (kD / 64) * 8;  // 16-byte chunks
         for (int z = i; z < nz; z += 128) {
-          const int row = nvalid + z / ((kD / 64) * 8);
+          const int row = nvalid_tile + z / ((kD / 64) * 8);
           const int box = (z / 8) % (kD / 64);
           st_shared_v4(sV + st * L::kKVBytes + box * L::kKVBox + row * 128 + (z & 7) * 16,
                        make_uint4(0u, 0u, 0u, 0u));
         }
       }
-      if (!P_TMEM || nvalid < BN) fence_proxy_async_smem();
+      if (!P_TMEM || (!resp && nvalid_tile < BN)) fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_pf[b]));
     }
@@ -408,17 +431,22 @@ cudaError_t fwd_variant(const FwdParams& a, cudaStream_t s) {
   p.o_parts = a.o_parts;
   p.lse_parts = a.lse_parts;
   p.status = a.status;
-  CUtensorMap tk, tv;
-  if (!encode_pool_map(&tk, a.k_pool, p.pool_rows, BN) ||
-      !encode_pool_map(&tv, a.v_pool, p.pool_rows, BN))
+  CUtensorMap tk, tv, tkr, tvr;
+  memset(&tk, 0, sizeof(tk));
+  memset(&tv, 0, sizeof(tv));
+  if (g.P > 0 && (!encode_pool_map(&tk, a.k_pool, p.pool_rows, BN) ||
+                  !encode_pool_map(&tv, a.v_pool, p.pool_rows, BN)))
+    return cudaErrorInvalidValue;
+  if (!encode_rows_map(&tkr, a.k_resp, g.hkv, g.R, BN) ||
+      !encode_rows_map(&tvr, a.v_resp, g.hkv, g.R, BN))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel<BN, KST, P_TMEM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kSmem);
   if (e != cudaSuccess) return e;
-  const int64_t units = (int64_t)g.ns * g.hkv * p.n_mt;
+  const int64_t units = (int64_t)(g.ns + 1) * g.hkv * p.n_mt;
   if (units == 0) return cudaSuccess;
   LaunchScope ls(kKTcFwd, s);
-  tc_fwd_kernel<BN, KST, P_TMEM><<<(unsigned)units, kThreads, L::kSmem, s>>>(tk, tv, p);
+  tc_fwd_kernel<BN, KST, P_TMEM><<<(unsigned)units, kThreads, L::kSmem, s>>>(tk, tv, tkr, tvr, p);
   return cudaGetLastError();
 }
 
