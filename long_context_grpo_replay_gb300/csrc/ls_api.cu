@@ -323,7 +323,24 @@ LaunchScope::LaunchScope(int32_t k, cudaStream_t s) : kid(k), stream(s), ev0(nul
   if (e && cudaEventRecord(e, s) == cudaSuccess) ev0 = e;
 }
 
+namespace {
+// LS_DEBUG_SYNC=1: synchronise after every launch and log it to stderr, so
+// that a stall or an error names its kernel.
+bool debug_sync() {
+  static int v = [] {
+    const char* e = getenv("LS_DEBUG_SYNC");
+    return e ? atoi(e) : 0;
+  }();
+  return v != 0;
+}
+}  // namespace
+
 LaunchScope::~LaunchScope() {
+  if (debug_sync()) {
+    fprintf(stderr, "[libls] %s launched\n", kKernelNames[kid]);
+    const cudaError_t e = cudaStreamSynchronize(stream);
+    fprintf(stderr, "[libls] %s done: %s\n", kKernelNames[kid], cudaGetErrorString(e));
+  }
   if (!ev0) return;
   std::lock_guard<std::mutex> lk(g_trace_mu);
   cudaEvent_t e = take_event();
@@ -503,12 +520,18 @@ ls_status ls_replay_group(const ls_attn_desc* desc, const ls_prompt_kv* prompt, 
 ls_status ls_read_device_status(void* ws, size_t ws_bytes, void* stream) {
   LS_CHECK(check_ws(ws, ws_bytes, kWsHeader));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint32_t word = 0;
+  uint32_t words[2] = {0u, 0u};
   LS_CUDA(cudaStreamSynchronize(s), "stream synchronize");
-  LS_CUDA(cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost), "status read");
-  LS_CUDA(cudaMemset(ws, 0, sizeof(word)), "status clear");
-  if (word & kStatusTimeout)
-    return fail(LS_ERR_DEVICE_TIMEOUT, "a device-side bounded wait ran out (status 0x%x)", word);
+  LS_CUDA(cudaMemcpy(words, ws, sizeof(words), cudaMemcpyDeviceToHost), "status read");
+  LS_CUDA(cudaMemset(ws, 0, sizeof(words)), "status clear");
+  const uint32_t word = words[0];
+  if (word & kStatusTimeout) {
+    const int kid = (int)(words[1] >> 16);
+    return fail(LS_ERR_DEVICE_TIMEOUT,
+                "a device-side bounded wait ran out in %s at source line %u (status 0x%x)",
+                (kid >= 0 && kid < kNumKernelIds) ? kKernelNames[kid] : "?", words[1] & 0xFFFFu,
+                word);
+  }
   if (word & kStatusBadPage)
     return fail(LS_ERR_DEVICE_BOUNDS, "a page-table entry was outside the pool (status 0x%x)",
                 word);

@@ -9,7 +9,8 @@
 
 namespace ls {
 
-// Bits of the device status word (first 4 bytes of the workspace).
+// Bits of the device status word (first 4 bytes of the workspace).  The
+// next word records the first bounded wait that gave up: kernel id << 16 | line.
 enum : uint32_t {
   kStatusBadPage = 1u,   // a page-table entry pointed outside the pool
   kStatusTimeout = 2u,   // a bounded device wait gave up

@@ -48,20 +48,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Gives up (returns
-// false) when *abort becomes non-zero or after timeout_ns of wall time, so a
-// broken pipeline ends the kernel instead of hanging the GPU.
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
+// false) when *abort becomes non-zero, or after about 2 s by either the SM
+// cycle counter or the global nanosecond timer, or after 2^30 polls, so a
+// broken pipeline ends the kernel instead of hanging the GPU.  Each bound is
+// independent, so a timer that does not advance cannot make a wait endless.
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;      // 2 s
+constexpr long long kWaitTimeoutCycles = 4000000000ll;  // 2 s at 2 GHz
+constexpr uint32_t kWaitMaxPolls = 1u << 30;
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           const volatile uint32_t* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
+  const long long c0 = clock64();
+  for (uint32_t it = 1; it < kWaitMaxPolls; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (*abort) return false;
+      if (clock64() - c0 > kWaitTimeoutCycles) return false;
       if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
     }
   }
+  return false;
+}
+
+// Warp-collective form for warps that go on to execute .sync.aligned
+// tensor-memory instructions: every lane waits, and the warp agrees on the
+// outcome, so a failure makes the whole warp leave together (a partial warp
+// must never reach a tcgen05.ld/st).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               const volatile uint32_t* abort) {
+  const bool ok = mbar_wait(bar, parity, abort);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // ---------------------------------------------------------------- proxies

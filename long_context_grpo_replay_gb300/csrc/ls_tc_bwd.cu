@@ -141,8 +141,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = tmem_base_s;
   const volatile uint32_t* abortp = &abort_s;
-  auto fail = [&]() {
+  // a wait that gives up records its kernel and source line in status[1]
+  auto fail = [&](int line) {
     atomicOr(p.status, kStatusTimeout);
+    atomicCAS(p.status + 1, 0u, ((uint32_t)kKTcBwdDq << 16) | (uint32_t)line);
     abort_s = 1;
   };
   auto pool_row = [&](int64_t key0) -> int32_t {
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < ntiles; ++j) {
         const int st = j % nst;
         if (j >= nst && !mbar_wait(smem_u32(&empty[st]), ((j / nst) - 1) & 1, abortp)) {
-          fail();
+          fail(__LINE__);
           break;
         }
         const int64_t key0 = kb + (int64_t)j * BN;
@@ -195,12 +197,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_s = idesc_bf16(kBM, BN, false);
       constexpr uint32_t idesc_dq = idesc_bf16(kBM, kD, true);
       bool ok = mbar_wait(smem_u32(&bar_q), 0, abortp);
-      if (!ok) fail();
+      if (!ok) fail(__LINE__);
       for (int j = 0; ok && j <= ntiles; ++j) {
         if (j < ntiles) {
           // S_j = Q K_j^T
           const int st = j % KSK, b = j & 1;
-          if (!mbar_wait(smem_u32(&bar_kf[st]), (j / KSK) & 1, abortp)) { fail(); break; }
+          if (!mbar_wait(smem_u32(&bar_kf[st]), (j / KSK) & 1, abortp)) { fail(__LINE__); break; }
           tc_fence_after();
           const uint32_t dS = tbase + L::kTmemS + b * 2 * BN;
 #pragma unroll
@@ -214,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= 1) {
           // dQ += dS_{j-1} K_{j-1}
           const int i = j - 1, st = i % KSK, b = i & 1;
-          if (!mbar_wait(smem_u32(&bar_ds[b]), (i >> 1) & 1, abortp)) { fail(); break; }
+          if (!mbar_wait(smem_u32(&bar_ds[b]), (i >> 1) & 1, abortp)) { fail(__LINE__); break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j < ntiles) {
           // dP_j = dO V_j^T
           const int st = j % KSV, b = j & 1;
-          if (!mbar_wait(smem_u32(&bar_vf[st]), (j / KSV) & 1, abortp)) { fail(); break; }
+          if (!mbar_wait(smem_u32(&bar_vf[st]), (j / KSV) & 1, abortp)) { fail(__LINE__); break; }
           tc_fence_after();
           const uint32_t dP = tbase + L::kTmemS + b * 2 * BN + BN;
 #pragma unroll
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int b = j & 1;
-      if (!mbar_wait(smem_u32(&bar_sd[b]), (j >> 1) & 1, abortp)) { fail(); ok = false; break; }
+      if (!mbar_wait_warp(smem_u32(&bar_sd[b]), (j >> 1) & 1, abortp)) { fail(__LINE__); ok = false; break; }
       tc_fence_after();
       const int64_t key0 = kb + (int64_t)j * BN;
       const int64_t lim = resp ? (int64_t)r + 1 : ke;  // causal limit for the response part
@@ -327,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- epilogue: unscaled float32 dQ partial
     if (ok && ntiles > 0) {
-      if (!mbar_wait(smem_u32(&bar_fin), 0, abortp)) { fail(); ok = false; }
+      if (!mbar_wait_warp(smem_u32(&bar_fin), 0, abortp)) { fail(__LINE__); ok = false; }
       tc_fence_after();
     }
     const int64_t nrows = (int64_t)p.R * p.hq;
@@ -335,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
     for (int c0 = 0; c0 < kD; c0 += 32) {
       uint32_t rr[32];
+      __syncwarp();  // the row_ok stores of the previous chunk diverge
       if (ok && ntiles > 0) {
         tmem_ld32(tbase + lane_off + c0, rr);
         tmem_wait_ld();

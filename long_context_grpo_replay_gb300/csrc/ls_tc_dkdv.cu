@@ -108,8 +108,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = tmem_base_s;
   const volatile uint32_t* abortp = &abort_s;
-  auto fail = [&]() {
+  // a wait that gives up records its kernel and source line in status[1]
+  auto fail = [&](int line) {
     atomicOr(p.status, kStatusTimeout);
+    atomicCAS(p.status + 1, 0u, ((uint32_t)kKTcDkDv << 16) | (uint32_t)line);
     abort_s = 1;
   };
 
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int issued = 0;
       for (int it = 0; it < nit; ++it) {
-        if (it > 0 && !mbar_wait(smem_u32(&bar_qe), (it - 1) & 1, abortp)) { fail(); break; }
+        if (it > 0 && !mbar_wait(smem_u32(&bar_qe), (it - 1) & 1, abortp)) { fail(__LINE__); break; }
         const int h = g * p.gq + it / nrt;
         const int r0 = j0 + (it % nrt) * kBR;
         const uint32_t bq = smem_u32(&bar_qf);
@@ -147,9 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_s = idesc_bf16(kBK, kBR, false);
       constexpr uint32_t idesc_g = idesc_bf16(kBK, 128, true);
       bool ok = mbar_wait(smem_u32(&bar_kv), 0, abortp);
-      if (!ok) fail();
+      if (!ok) fail(__LINE__);
       for (int it = 0; ok && it < nit; ++it) {
-        if (!mbar_wait(smem_u32(&bar_qf), it & 1, abortp)) { fail(); break; }
+        if (!mbar_wait(smem_u32(&bar_qf), it & 1, abortp)) { fail(__LINE__); break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
@@ -166,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  idesc_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(&bar_sd));
-        if (!mbar_wait(smem_u32(&bar_ds), it & 1, abortp)) { fail(); break; }
+        if (!mbar_wait(smem_u32(&bar_ds), it & 1, abortp)) { fail(__LINE__); break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBR / 16; ++kk) {
@@ -204,8 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_dl[b][i - kBR] = r < p.R ? __ldg(p.delta + (int64_t)r * p.hq + h) : 0.f;
       }
       mbar_arrive(smem_u32(&bar_st[b]));
-      if (!mbar_wait(smem_u32(&bar_st[b]), (it >> 1) & 1, abortp)) { fail(); ok = false; break; }
-      if (!mbar_wait(smem_u32(&bar_sd), it & 1, abortp)) { fail(); ok = false; break; }
+      if (!mbar_wait_warp(smem_u32(&bar_st[b]), (it >> 1) & 1, abortp)) { fail(__LINE__); ok = false; break; }
+      if (!mbar_wait_warp(smem_u32(&bar_sd), it & 1, abortp)) { fail(__LINE__); ok = false; break; }
       tc_fence_after();
       uint32_t pk[kBR / 2], dk[kBR / 2];
 #pragma unroll
@@ -238,18 +240,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- epilogue: rows j < R of dK (scaled) and dV, columns of this half
     if (ok && nit > 0) {
-      if (!mbar_wait(smem_u32(&bar_fin), 0, abortp)) { fail(); ok = false; }
+      if (!mbar_wait_warp(smem_u32(&bar_fin), 0, abortp)) { fail(__LINE__); ok = false; }
       tc_fence_after();
     }
-    if (ok && j < p.R) {
+    // ok is warp-uniform here; the tensor-memory loads run on the whole warp
+    // and only the stores are limited to keys j < R
+    if (ok && nit > 0) {
       __nv_bfloat16* dko = p.dk + ((int64_t)j * p.hkv + g) * kD + hf * 128;
       __nv_bfloat16* dvo = p.dv + ((int64_t)j * p.hkv + g) * kD + hf * 128;
 #pragma unroll 1
       for (int c0 = 0; c0 < 128; c0 += 32) {
         uint32_t rk[32], rv[32];
+        __syncwarp();  // the j < R stores of the previous chunk diverge
         tmem_ld32(tbase + lane_off + L::kTmemDK + c0, rk);
         tmem_ld32(tbase + lane_off + L::kTmemDV + c0, rv);
         tmem_wait_ld();
+        if (j >= p.R) continue;
 #pragma unroll
         for (int c = 0; c < 32; c += 8) {
           uint4 vk, vv;

@@ -148,8 +148,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = tmem_base_s;
   const volatile uint32_t* abortp = &abort_s;
 
-  auto fail = [&]() {
+  // a wait that gives up records its kernel and source line in status[1]
+  auto fail = [&](int line) {
     atomicOr(p.status, kStatusTimeout);
+    atomicCAS(p.status + 1, 0u, ((uint32_t)kKTcFwd << 16) | (uint32_t)line);
     abort_s = 1;
   };
 
@@ -177,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < ntiles; ++j) {
         const int st = j % KST;
         if (j >= KST && !mbar_wait(smem_u32(&empty[st]), ((j / KST) - 1) & 1, abortp)) {
-          fail();
+          fail(__LINE__);
           break;
         }
         const int64_t key0 = kb + (int64_t)j * BN;
@@ -206,11 +208,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_qk = idesc_bf16(kBM, BN, false);
       constexpr uint32_t idesc_pv = idesc_bf16(kBM, kD, true);
       bool ok = mbar_wait(smem_u32(&bar_q), 0, abortp);
-      if (!ok) fail();
+      if (!ok) fail(__LINE__);
       for (int j = 0; ok && j <= ntiles; ++j) {
         if (j < ntiles) {
           const int st = j % KST, b = j & 1;
-          if (!mbar_wait(smem_u32(&bar_kf[st]), (j / KST) & 1, abortp)) { fail(); break; }
+          if (!mbar_wait(smem_u32(&bar_kf[st]), (j / KST) & 1, abortp)) { fail(__LINE__); break; }
           tc_fence_after();
           const uint32_t dS = tbase + L::kTmemS + b * BN;
 #pragma unroll
@@ -225,8 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (j >= 1) {
           const int i = j - 1, st = i % KST, b = i & 1;
-          if (!mbar_wait(smem_u32(&bar_pf[b]), (i >> 1) & 1, abortp)) { fail(); break; }
-          if (!mbar_wait(smem_u32(&bar_vf[st]), (i / KST) & 1, abortp)) { fail(); break; }
+          if (!mbar_wait(smem_u32(&bar_pf[b]), (i >> 1) & 1, abortp)) { fail(__LINE__); break; }
+          if (!mbar_wait(smem_u32(&bar_vf[st]), (i / KST) & 1, abortp)) { fail(__LINE__); break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int b = j & 1;
-      if (!mbar_wait(smem_u32(&bar_sf[b]), (j >> 1) & 1, abortp)) { fail(); ok = false; break; }
+      if (!mbar_wait_warp(smem_u32(&bar_sf[b]), (j >> 1) & 1, abortp)) { fail(__LINE__); ok = false; break; }
       tc_fence_after();
       float s[BN];
 #pragma unroll
@@ -306,27 +308,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         s[c] = x;
         mx = fmaxf(mx, x);
       }
+      // Lazy rescale: a row moves its running max only when the tile max
+      // exceeds it by more than the threshold.  The O rescale uses
+      // warp-collective TMEM loads/stores, so the whole warp does it when any
+      // of its rows needs it (alpha = 1 for the others).
+      float alpha = 1.f;
+      bool rescale_o = false;
       if (mx > m_run + kRescaleThreshold) {
         if (m_run != -CUDART_INF_F) {
-          const float alpha = ex2(m_run - mx);
-          // O holds PV_0..PV_{j-1}; wait for the last one, then rescale in place.
-          // S_j complete implies PV_{j-2} complete (MMAs finish in issue order),
-          // so bar_od has completed j-1 or j phases and the parity is unambiguous.
-          if (!mbar_wait(smem_u32(&bar_od), (j - 1) & 1, abortp)) { fail(); ok = false; break; }
-          tc_fence_after();
-#pragma unroll 1
-          for (int c0 = 0; c0 < kD; c0 += 32) {
-            uint32_t rr[32];
-            tmem_ld32(tbase + lane_off + c0, rr);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * alpha);
-            tmem_st32(tbase + lane_off + c0, rr);
-          }
-          tmem_wait_st();
-          l_run *= alpha;
+          alpha = ex2(m_run - mx);
+          rescale_o = true;
         }
+        l_run *= alpha;
         m_run = mx;
+      }
+      if (__any_sync(0xffffffffu, rescale_o)) {
+        // O holds PV_0..PV_{j-1} (j >= 1 here: a finite running max needs an
+        // earlier tile); wait for the last one, then rescale in place.  S_j
+        // complete implies PV_{j-2} complete (MMAs finish in issue order), so
+        // bar_od has completed j-1 or j phases and the parity is unambiguous.
+        if (!mbar_wait_warp(smem_u32(&bar_od), (j - 1) & 1, abortp)) { fail(__LINE__); ok = false; break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c0 = 0; c0 < kD; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(tbase + lane_off + c0, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * alpha);
+          tmem_st32(tbase + lane_off + c0, rr);
+        }
+        tmem_wait_st();
       }
       float psum = 0.f;
       uint32_t pk[BN / 2];
@@ -354,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Partial last prompt tile: rows past the prompt end may hold anything
         // (NaN included); zero them in V so that P=0 times V stays 0.
         const int st = j % KST;
-        if (!mbar_wait(smem_u32(&bar_vf[st]), (j / KST) & 1, abortp)) { fail(); ok = false; break; }
+        if (!mbar_wait_warp(smem_u32(&bar_vf[st]), (j / KST) & 1, abortp)) { fail(__LINE__); ok = false; break; }
         const int nz = (BN - nvalid_tile) * (kD / 64) * 8;  // 16-byte chunks
         for (int z = i; z < nz; z += 128) {
           const int row = nvalid_tile + z / ((kD / 64) * 8);
@@ -371,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- epilogue: normalised partial O and its LSE
     if (ok && ntiles > 0) {
       // bar_od may lag two phases behind here, so the last PV has its own barrier
-      if (!mbar_wait(smem_u32(&bar_ofin), 0, abortp)) { fail(); ok = false; }
+      if (!mbar_wait_warp(smem_u32(&bar_ofin), 0, abortp)) { fail(__LINE__); ok = false; }
       tc_fence_after();
     }
     const int64_t nrows = (int64_t)p.R * p.hq;
@@ -380,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
     for (int c0 = 0; c0 < kD; c0 += 32) {
       uint32_t rr[32];
+      __syncwarp();  // the row_ok stores of the previous chunk diverge
       if (ok && ntiles > 0) {
         tmem_ld32(tbase + lane_off + c0, rr);
         tmem_wait_ld();
@@ -460,11 +473,14 @@ int fwd_variant_id() {
 
 }  // namespace
 
+// Default: 128-key tiles (N=128 QK^T runs the tensor pipe at full rate, N=64
+// at about two thirds), P kept in tensor memory, one K and one V stage.
+// LS_TC_FWD_VARIANT selects the 64-key-tile variants for comparison.
 cudaError_t launch_tc_fwd(const FwdParams& a, cudaStream_t s) {
   switch (fwd_variant_id()) {
-    case 1: return fwd_variant<128, 1, true>(a, s);
+    case 1: return fwd_variant<64, 2, false>(a, s);
     case 2: return fwd_variant<64, 2, true>(a, s);
-    default: return fwd_variant<64, 2, false>(a, s);
+    default: return fwd_variant<128, 1, true>(a, s);
   }
 }
 
