@@ -195,6 +195,24 @@ LS_API ls_status ls_replay_group(const ls_attn_desc* desc, const ls_prompt_kv* p
                           int32_t n_members, const ls_member* members, void* ws,
                           size_t ws_bytes, void* stream);
 
+/* Replay forward (same arguments and results as ls_replay_fwd) for callers
+ * that cannot allocate device memory: no workspace argument; the library's
+ * own fixed 64 MiB device scratch (held by every GPU that loads the library
+ * until exit) takes the workspace's place.  The pages have no counterpart to
+ * this call; it exists for embedders that own every allocation.
+ * The first call on each device looks up the scratch's device address with
+ * that device current; make it before any stream capture.  All calls share
+ * the one scratch, so calls that overlap on the GPU race.  A call that would
+ * need more scratch than 64 MiB returns LS_ERR_WORKSPACE_TOO_SMALL.  Device
+ * status bits set by this call are not reported (the status word lives in
+ * the scratch). */
+LS_API ls_status ls_replay_fwd_noalloc(const ls_attn_desc* desc, const ls_prompt_kv* prompt,
+                                       const void* q, const void* k_resp, const void* v_resp,
+                                       int32_t resp_len, void* o, float* lse, void* stream);
+
+/* Bytes of the fixed scratch ls_replay_fwd_noalloc uses (64 MiB). */
+LS_API size_t ls_replay_fwd_noalloc_scratch_bytes(void);
+
 /* Synchronises the stream, then reports the device status word of ws
  * (LS_OK, LS_ERR_DEVICE_BOUNDS or LS_ERR_DEVICE_TIMEOUT) and clears it. */
 LS_API ls_status ls_read_device_status(void* ws, size_t ws_bytes, void* stream);

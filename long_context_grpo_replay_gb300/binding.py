@@ -18,7 +18,8 @@ __all__ = [
     "ls_read_device_status", "ls_clear_device_status", "ls_status_string", "ls_last_error",
     "ls_trace_enable", "ls_trace_reset", "ls_trace_read", "ls_num_kernel_ids",
     "ls_kernel_name", "ls_launch_count", "ls_uses_tensor_cores", "kernel_trace",
-    "desc_for", "prompt_from", "EXPORTED_SYMBOLS",
+    "desc_for", "prompt_from", "EXPORTED_SYMBOLS", "ls_replay_fwd_noalloc",
+    "ls_replay_fwd_noalloc_scratch_bytes",
 ]
 
 LS_DTYPE_F32 = 0
@@ -29,7 +30,8 @@ EXPORTED_SYMBOLS = [
     "ls_replay_bwd_preprocess", "ls_replay_bwd", "ls_replay_group", "ls_read_device_status",
     "ls_clear_device_status", "ls_status_string", "ls_last_error", "ls_trace_enable",
     "ls_trace_reset", "ls_trace_read", "ls_num_kernel_ids", "ls_kernel_name",
-    "ls_launch_count", "ls_uses_tensor_cores",
+    "ls_launch_count", "ls_uses_tensor_cores", "ls_replay_fwd_noalloc",
+    "ls_replay_fwd_noalloc_scratch_bytes",
 ]
 
 
@@ -98,6 +100,8 @@ def lib() -> ctypes.CDLL:
         "ls_trace_reset": [],
         "ls_trace_read": [I32, ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double)],
         "ls_uses_tensor_cores": [ctypes.POINTER(AttnDesc)],
+        "ls_replay_fwd_noalloc": [ctypes.POINTER(AttnDesc), ctypes.POINTER(PromptKV), P, P, P,
+                                  I32, P, P, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -107,7 +111,8 @@ def lib() -> ctypes.CDLL:
                             ("ls_last_error", ctypes.c_char_p, []),
                             ("ls_num_kernel_ids", I32, []),
                             ("ls_kernel_name", ctypes.c_char_p, [I32]),
-                            ("ls_launch_count", I64, [])]:
+                            ("ls_launch_count", I64, []),
+                            ("ls_replay_fwd_noalloc_scratch_bytes", SZ, [])]:
         f = getattr(L, name)
         f.argtypes = args
         f.restype = res
@@ -202,6 +207,20 @@ def ls_replay_fwd(desc, prompt, q, k_resp, v_resp, o, lse, ws, stream=None):
     _check(lib().ls_replay_fwd(ctypes.byref(desc), ctypes.byref(prompt), _ptr(q), _ptr(k_resp),
                                _ptr(v_resp), q.shape[0], _ptr(o), _ptr(lse), _ptr(ws),
                                _nbytes(ws), _stream(stream)))
+
+
+def ls_replay_fwd_noalloc(desc, prompt, q, k_resp, v_resp, o, lse, stream=None):
+    """ls_replay_fwd without a workspace: for callers that cannot allocate
+    device memory; uses the library's fixed device scratch (see ls.h)."""
+    _want_f32(lse)
+    _want_dtype(desc, q, k_resp, v_resp, o)
+    _check(lib().ls_replay_fwd_noalloc(ctypes.byref(desc), ctypes.byref(prompt), _ptr(q),
+                                       _ptr(k_resp), _ptr(v_resp), q.shape[0], _ptr(o), _ptr(lse),
+                                       _stream(stream)))
+
+
+def ls_replay_fwd_noalloc_scratch_bytes() -> int:
+    return lib().ls_replay_fwd_noalloc_scratch_bytes()
 
 
 def ls_lse_merge(o_parts, lse_parts, o, lse=None, stream=None):

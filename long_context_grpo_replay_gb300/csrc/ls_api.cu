@@ -352,6 +352,8 @@ LaunchScope::~LaunchScope() {
   g_pending.push_back({kid, static_cast<cudaEvent_t>(ev0), e});
 }
 
+void set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+
 // ------------------------------------------------------------------ TMA maps
 namespace {
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,

@@ -119,6 +119,9 @@ cudaError_t launch_tc_bwd_dq(const BwdParams& p, cudaStream_t s);
 // 2-D TMA map over a bf16 matrix [rows][256] with [box_rows x 64] boxes and
 // the 128-byte swizzle (ls_api.cu; cuTensorMapEncodeTiled resolved once
 // through the runtime, no -lcuda).
+// Sets the message ls_last_error() returns on this thread.
+void set_last_error(const char* msg);
+
 bool encode_pool_map(CUtensorMap* m, const void* base, int64_t rows, int box_rows);
 // 3-D TMA map over a bf16 tensor [rows][heads][256] with [box_rows x 1 x 64]
 // boxes and the 128-byte swizzle (response K/V, Q, dO); rows past the end
