@@ -127,6 +127,23 @@ def recorded_traffic(kernel: str, workload: str, source_file: Path):
     return float(vals["traffic_bytes_per_launch"])
 
 
+def max_over_ranks(ms: float, device) -> float:
+    """Slowest rank's time: the whole job is done when every replica is."""
+    import torch
+    import torch.distributed as dist
+
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank_step: float, world: int, ms_step: float) -> float:
+    """Whole-job TFLOP/s: every rank processes its own replica (weak scaling)."""
+    return flops_per_rank_step * world / (ms_step * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------------------
 def run_ours(args):
     import torch
@@ -200,13 +217,10 @@ def run_ours(args):
     ls.ls_trace_enable(False)
     ls.ls_read_device_status(ws)
     clocks = clk.summary()
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
     flops_step = sum(replay_flops(P, R, hq, d) for R in w.resp_lens)
-    value = flops_step * world / (ms_step * 1e-3) / 1e12
+    value = job_throughput(flops_step, world, ms_step)
     kv_bytes_pass = P * hkv * d * 2 * (2 if tdt == torch.bfloat16 else 4)
     kv_gbs = 2 * G * kv_bytes_pass * world / (ms_step * 1e-3) / 1e9
 
@@ -317,13 +331,8 @@ def run_e2e(args, w, desc, src, members, k_pool, v_pool, pt, prompt, ws, stream,
         step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / n
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": round(flops_step * world / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+    ms = max_over_ranks(e0.elapsed_time(e1) / n, dev)
+    return {"value": round(job_throughput(flops_step, world, ms), 3), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "steps": n, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h)}
 
