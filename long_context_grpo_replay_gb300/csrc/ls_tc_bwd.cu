@@ -6,14 +6,17 @@
 // memory, streams the part's key pages, recomputes P from the stored LSE and
 // accumulates dQ in tensor memory.  No score matrix is kept between tiles.
 //
-// Per key tile j (BN keys):
-//   S_j  = Q K_j^T            (tcgen05, SS)       -> TMEM S[b]
-//   dP_j = dO V_j^T           (tcgen05, SS)       -> TMEM dP[b]
+// Two kernels share that plan.  The default keeps dO in tensor memory as the
+// A operand of dP = dO V^T, which leaves room for three V stages in shared
+// memory; the older one (selected by LS_TC_BWD_VARIANT) keeps Q and dO in
+// shared memory.  Per key tile j (BN keys):
+//   S_j  = Q K_j^T            (tcgen05, SS)        -> TMEM S
+//   dP_j = dO V_j^T           (tcgen05, TS or SS)  -> TMEM dP
 //   softmax warps: P = exp2(S*scale*log2e - LSE*log2e), dS = P * (dP - delta),
-//                  dS (bf16) written over S[b] in tensor memory
+//                  dS (bf16) written back into tensor memory
 //   dQ  += dS_j K_j           (tcgen05, A from TMEM, K as N-major B operand)
-// The MMA issue order S_j, dQ_{j-1}, dP_j keeps the tensor pipe busy while
-// the softmax warps work on tile j-1 and V_j lands.
+// The MMA issue order keeps the tensor pipe busy while the softmax warps work
+// on one tile and the next tile's K/V land.
 // Output: unscaled float32 dQ partial of the part; the reduction kernel sums
 // parts and applies the softmax scale.
 #include <cuda.h>
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto pool_row = [&](int64_t key0) -> int32_t {
     const int32_t slot = __ldg(p.page_table + key0 / p.page_size);
     if (slot < 0 || slot >= p.pool_pages) {
-      atomicOr(p.status, kStatusBadPage);
+      if (lane == 0) atomicOr(p.status, kStatusBadPage);
       return (int32_t)p.pool_rows;
     }
     return (int32_t)(((int64_t)slot * p.hkv + kvh) * p.page_size + key0 % p.page_size);
@@ -158,34 +161,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 || warp == 3) {
     // ------------------------------------------------------------ producers
-    if (lane == 0 && ntiles > 0) {
+    // whole warps: lane 0 posts the expected bytes, lanes 0..3 each issue one
+    // of the tile's four boxes in parallel
+    if (ntiles > 0) {
       const bool isK = warp == 0;
       const int nst = isK ? KSK : KSV;
       const CUtensorMap* tm = resp ? (isK ? &tmKr : &tmVr) : (isK ? &tmK : &tmV);
       uint64_t* full = isK ? bar_kf : bar_vf;
       uint64_t* empty = isK ? bar_ke : bar_ve;
       const uint32_t sdst = isK ? sK : sV;
-      prefetch_tmap(tm);
+      if (lane == 0) prefetch_tmap(tm);
       int issued = 0;
       for (int j = 0; j < ntiles; ++j) {
         const int st = j % nst;
-        if (j >= nst && !mbar_wait(smem_u32(&empty[st]), ((j / nst) - 1) & 1, abortp)) {
+        if (j >= nst && !mbar_wait_warp(smem_u32(&empty[st]), ((j / nst) - 1) & 1, abortp)) {
           fail(__LINE__);
           break;
         }
         const int64_t key0 = kb + (int64_t)j * BN;
         const uint32_t fb = smem_u32(&full[st]);
-        mbar_expect_tx(fb, L::kKVBytes);
-        if (resp) {
-#pragma unroll
-          for (int c = 0; c < kD / 64; ++c)
+        const int32_t row = resp ? 0 : pool_row(key0);
+        if (lane == 0) mbar_expect_tx(fb, L::kKVBytes);
+        __syncwarp();
+        if (lane < kD / 64) {
+          const int c = lane;
+          if (resp)
             tma_load_3d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, kvh, (int32_t)key0);
-        } else {
-          const int32_t row = pool_row(key0);
-#pragma unroll
-          for (int c = 0; c < kD / 64; ++c)
+          else
             tma_load_2d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, row);
         }
+        __syncwarp();
         issued = j + 1;
       }
       for (int j = issued - nst < 0 ? 0 : issued - nst; j < issued; ++j)
@@ -406,6 +411,382 @@ cudaError_t bwd_variant(const BwdParams& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+
+// ===========================================================================
+// Backward with dO held in tensor memory (default).  dP = dO V^T takes dO as
+// the A operand from tensor memory, which frees 64 KB of shared memory for a
+// third V stage (V_j is needed only by dP_j, and its load latency is what the
+// two-stage layout exposes).  Tensor memory: dQ [0,256), dO [256,384) (bf16
+// pairs), S [384,448), dP [448,512).  The softmax warps release S as soon as
+// they have read it and write dS over dP, so S_{j+1} runs while they work:
+//   MMA order: S_0, dP_0, then per tile j: S_{j+1}, dQ_j, dP_{j+1}.
+// ===========================================================================
+struct BwdTmLayout {
+  static constexpr int BN = 64, KSK = 2, KSV = 3;
+  static constexpr uint32_t kRowBox = kBM * 128;        // 16 KB
+  static constexpr uint32_t kKVBytes = BN * kD * 2;     // 32 KB
+  static constexpr uint32_t kKVBox = BN * 128;          // 8 KB
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kK = kQ + 4 * kRowBox;
+  static constexpr uint32_t kV = kK + KSK * kKVBytes;
+  static constexpr uint32_t kEnd = kV + KSV * kKVBytes;
+  static constexpr uint32_t kSmem = kEnd + 1024;
+  static constexpr uint32_t kTmemO = 256, kTmemS = 384, kTmemP = 448;
+  static_assert(kSmem <= 227 * 1024 - 512, "shared memory budget");
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_bwd_dq_tm_kernel(const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV,
+                        const __grid_constant__ CUtensorMap tmKr,
+                        const __grid_constant__ CUtensorMap tmVr, const BwdKParams p) {
+  using L = BwdTmLayout;
+  constexpr int BN = L::BN, KSK = L::KSK, KSV = L::KSV;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_q, bar_kf[KSK], bar_ke[KSK], bar_vf[KSV], bar_ve[KSV], bar_sf,
+      bar_sfree, bar_dpf, bar_dsf, bar_fin, bar_drain;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ uint32_t abort_s;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = sbase + L::kQ, sK = sbase + L::kK, sV = sbase + L::kV;
+
+  const int mt = blockIdx.x % p.n_mt;
+  const int kvh = (blockIdx.x / p.n_mt) % p.hkv;
+  const int part = blockIdx.x / (p.n_mt * p.hkv);
+  const bool resp = part == p.ns;
+  const int64_t rows_g = (int64_t)p.gq * p.R;
+  int64_t kb, ke;
+  if (!resp) {
+    kb = (int64_t)part * p.split_span;
+    ke = kb + p.split_span < p.P ? kb + p.split_span : p.P;
+  } else {
+    const int64_t t0 = (int64_t)mt * kBM;
+    const int64_t t1 = (t0 + kBM < rows_g ? t0 + kBM : rows_g) - 1;
+    kb = 0;
+    ke = (t0 / p.R == t1 / p.R) ? (t1 % p.R) + 1 : p.R;
+  }
+  const int ntiles = ke > kb ? (int)((ke - kb + BN - 1) / BN) : 0;
+
+  if (tid == 0) {
+    abort_s = 0;
+    mbar_init(smem_u32(&bar_q), 128);
+    for (int s = 0; s < KSK; ++s) {
+      mbar_init(smem_u32(&bar_kf[s]), 1);
+      mbar_init(smem_u32(&bar_ke[s]), 1);
+    }
+    for (int s = 0; s < KSV; ++s) {
+      mbar_init(smem_u32(&bar_vf[s]), 1);
+      mbar_init(smem_u32(&bar_ve[s]), 1);
+    }
+    mbar_init(smem_u32(&bar_sf), 1);
+    mbar_init(smem_u32(&bar_sfree), 128);
+    mbar_init(smem_u32(&bar_dpf), 1);
+    mbar_init(smem_u32(&bar_dsf), 128);
+    mbar_init(smem_u32(&bar_fin), 1);
+    mbar_init(smem_u32(&bar_drain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&tmem_base_s), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base_s;
+  const volatile uint32_t* abortp = &abort_s;
+  auto fail = [&](int line) {
+    atomicOr(p.status, kStatusTimeout);
+    atomicCAS(p.status + 1, 0u, ((uint32_t)kKTcBwdDq << 16) | (uint32_t)line);
+    abort_s = 1;
+  };
+  auto pool_row = [&](int64_t key0) -> int32_t {
+    const int32_t slot = __ldg(p.page_table + key0 / p.page_size);
+    if (slot < 0 || slot >= p.pool_pages) {
+      if (lane == 0) atomicOr(p.status, kStatusBadPage);
+      return (int32_t)p.pool_rows;
+    }
+    return (int32_t)(((int64_t)slot * p.hkv + kvh) * p.page_size + key0 % p.page_size);
+  };
+
+  if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------ producers
+    // whole warps; lane 0 posts the bytes, lanes 0..3 issue the four boxes
+    if (ntiles > 0) {
+      const bool isK = warp == 0;
+      const int nst = isK ? KSK : KSV;
+      const CUtensorMap* tm = resp ? (isK ? &tmKr : &tmVr) : (isK ? &tmK : &tmV);
+      uint64_t* full = isK ? bar_kf : bar_vf;
+      uint64_t* empty = isK ? bar_ke : bar_ve;
+      const uint32_t sdst = isK ? sK : sV;
+      if (lane == 0) prefetch_tmap(tm);
+      int issued = 0;
+      for (int j = 0; j < ntiles; ++j) {
+        const int st = j % nst;
+        if (j >= nst && !mbar_wait_warp(smem_u32(&empty[st]), ((j / nst) - 1) & 1, abortp)) {
+          fail(__LINE__);
+          break;
+        }
+        const int64_t key0 = kb + (int64_t)j * BN;
+        const uint32_t fb = smem_u32(&full[st]);
+        const int32_t row = resp ? 0 : pool_row(key0);
+        if (lane == 0) mbar_expect_tx(fb, L::kKVBytes);
+        __syncwarp();
+        if (lane < kD / 64) {
+          const int c = lane;
+          if (resp)
+            tma_load_3d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, kvh, (int32_t)key0);
+          else
+            tma_load_2d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, row);
+        }
+        __syncwarp();
+        issued = j + 1;
+      }
+      for (int j = issued - nst < 0 ? 0 : issued - nst; j < issued; ++j)
+        mbar_wait(smem_u32(&full[j % nst]), (j / nst) & 1, abortp);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(kBM, BN, false);
+      constexpr uint32_t idesc_dq = idesc_bf16(kBM, kD, true);
+      auto issue_s = [&](int j) -> bool {  // S = Q K_j^T
+        const int st = j % KSK;
+        if (!mbar_wait(smem_u32(&bar_kf[st]), (j / KSK) & 1, abortp)) { fail(__LINE__); return false; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tbase + L::kTmemS, sdesc_sw128(sQ + (kk >> 2) * L::kRowBox + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(sK + st * L::kKVBytes + (kk >> 2) * L::kKVBox + (kk & 3) * 32, 16, 1024),
+                 idesc_s, kk > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&bar_sf));
+        return true;
+      };
+      auto issue_dp = [&](int j) -> bool {  // dP = dO V_j^T, dO from tensor memory
+        const int st = j % KSV;
+        if (!mbar_wait(smem_u32(&bar_vf[st]), (j / KSV) & 1, abortp)) { fail(__LINE__); return false; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ts(tbase + L::kTmemP, tbase + L::kTmemO + kk * 8,
+                 sdesc_sw128(sV + st * L::kKVBytes + (kk >> 2) * L::kKVBox + (kk & 3) * 32, 16, 1024),
+                 idesc_s, kk > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&bar_ve[st]));
+        mma_commit(smem_u32(&bar_dpf));
+        return true;
+      };
+      bool ok = mbar_wait(smem_u32(&bar_q), 0, abortp);
+      if (!ok) fail(__LINE__);
+      tc_fence_after();
+      if (ok) ok = issue_s(0) && issue_dp(0);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        if (j + 1 < ntiles) {
+          // S columns are free once the softmax warps have read S_j
+          if (!mbar_wait(smem_u32(&bar_sfree), j & 1, abortp)) { fail(__LINE__); break; }
+          if (!issue_s(j + 1)) break;
+        }
+        // dQ += dS_j K_j, dS read from the dP columns
+        if (!mbar_wait(smem_u32(&bar_dsf), j & 1, abortp)) { fail(__LINE__); break; }
+        tc_fence_after();
+        const int st = j % KSK;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tbase, tbase + L::kTmemP + kk * 8,
+                 sdesc_sw128(sK + st * L::kKVBytes + kk * 16 * 128, L::kKVBox, 1024), idesc_dq,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&bar_ke[st]));
+        if (j == ntiles - 1) mma_commit(smem_u32(&bar_fin));
+        // dP_{j+1} overwrites dS_j, which dQ_j (issued before it) has consumed
+        if (j + 1 < ntiles && !issue_dp(j + 1)) break;
+      }
+      mma_commit(smem_u32(&bar_drain));
+      mbar_wait(smem_u32(&bar_drain), 0, abortp);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int i = tid - 128;
+    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
+    const int64_t t = (int64_t)mt * kBM + i;
+    const bool row_ok = t < rows_g;
+    const int hh = row_ok ? (int)(t / p.R) : 0;
+    const int r = row_ok ? (int)(t % p.R) : 0;
+    const int64_t n = (int64_t)r * p.hq + (int64_t)kvh * p.gq + hh;
+    const float lse2 = row_ok ? __ldg(p.lse + n) * kLog2ef : 0.f;
+    const float dl = row_ok ? __ldg(p.delta + n) : 0.f;
+    {
+      // Q tile into shared memory (warp-cooperative rows, swizzled) ...
+      const int wq = warp - 4;
+      for (int rr = 0; rr < 32; ++rr) {
+        const int row = wq * 32 + rr;
+        const int64_t tt = (int64_t)mt * kBM + row;
+        uint4 vq = make_uint4(0u, 0u, 0u, 0u);
+        if (tt < rows_g) {
+          const int hh2 = (int)(tt / p.R), r2 = (int)(tt % p.R);
+          const int64_t n2 = (int64_t)r2 * p.hq + (int64_t)kvh * p.gq + hh2;
+          vq = __ldg(reinterpret_cast<const uint4*>(p.q + n2 * kD) + lane);
+        }
+        st_shared_v4(sQ + (lane >> 3) * L::kRowBox + sw128_offset(row, lane & 7), vq);
+      }
+      fence_proxy_async_smem();
+      // ... and this thread's dO row into tensor memory lane i (bf16 pairs)
+      const uint4* orow = reinterpret_cast<const uint4*>(p.d_o + n * kD);
+#pragma unroll 1
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t rr[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 v = row_ok ? __ldg(orow + (c0 >> 2) + u) : make_uint4(0u, 0u, 0u, 0u);
+          rr[4 * u] = v.x;
+          rr[4 * u + 1] = v.y;
+          rr[4 * u + 2] = v.z;
+          rr[4 * u + 3] = v.w;
+        }
+        tmem_st32(tbase + lane_off + L::kTmemO + c0, rr);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_q));
+    }
+
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      if (!mbar_wait_warp(smem_u32(&bar_sf), j & 1, abortp)) { fail(__LINE__); ok = false; break; }
+      tc_fence_after();
+      const int64_t key0 = kb + (int64_t)j * BN;
+      const int64_t lim = resp ? (int64_t)r + 1 : ke;
+      const int nvalid = (int)(lim - key0 < 0 ? 0 : (lim - key0 < BN ? lim - key0 : BN));
+      const int nvalid_tile = (int)(ke - key0 < BN ? ke - key0 : BN);
+      float pv[BN];
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t rs[32];
+        tmem_ld32(tbase + lane_off + L::kTmemS + c0, rs);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pv[c0 + c] = __uint_as_float(rs[c]);
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_sfree));  // S_{j+1} may now overwrite S
+#pragma unroll
+      for (int c = 0; c < BN; ++c)
+        pv[c] = c < nvalid ? ex2(pv[c] * p.scale_log2 - lse2) : 0.f;
+      if (!mbar_wait_warp(smem_u32(&bar_dpf), j & 1, abortp)) { fail(__LINE__); ok = false; break; }
+      tc_fence_after();
+      uint32_t ds_pk[BN / 2];
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t rp[32];
+        tmem_ld32(tbase + lane_off + L::kTmemP + c0, rp);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const float d0 = c0 + c < nvalid ? pv[c0 + c] * (__uint_as_float(rp[c]) - dl) : 0.f;
+          const float d1 = c0 + c + 1 < nvalid ? pv[c0 + c + 1] * (__uint_as_float(rp[c + 1]) - dl) : 0.f;
+          ds_pk[(c0 + c) >> 1] = pack_bf16x2(d0, d1);
+        }
+      }
+      // every dP column of this row has been read: dS goes over its first half
+#pragma unroll
+      for (int c0 = 0; c0 < BN / 2; c0 += 16)
+        tmem_st16(tbase + lane_off + L::kTmemP + c0, ds_pk + c0);
+      tmem_wait_st();
+      if (!resp && nvalid_tile < BN) {
+        // partial last prompt tile: rows past the prompt end may hold anything;
+        // zero them in K so that dS = 0 times K stays 0 in dQ += dS K
+        const int st = j % KSK;
+        const int nz = (BN - nvalid_tile) * (kD / 64) * 8;
+        for (int z = i; z < nz; z += 128) {
+          const int row = nvalid_tile + z / ((kD / 64) * 8);
+          const int box = (z / 8) % (kD / 64);
+          st_shared_v4(sK + st * L::kKVBytes + box * L::kKVBox + row * 128 + (z & 7) * 16,
+                       make_uint4(0u, 0u, 0u, 0u));
+        }
+        fence_proxy_async_smem();
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_dsf));
+    }
+
+    if (ok && ntiles > 0) {
+      if (!mbar_wait_warp(smem_u32(&bar_fin), 0, abortp)) { fail(__LINE__); ok = false; }
+      tc_fence_after();
+    }
+    const int64_t nrows = (int64_t)p.R * p.hq;
+    float* out = p.dq_parts + ((int64_t)part * nrows + n) * kD;
+#pragma unroll 1
+    for (int c0 = 0; c0 < kD; c0 += 32) {
+      uint32_t rr[32];
+      __syncwarp();
+      if (ok && ntiles > 0) {
+        tmem_ld32(tbase + lane_off + c0, rr);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) rr[c] = 0u;
+      }
+      if (row_ok) {
+#pragma unroll
+        for (int c = 0; c < 32; c += 4)
+          *reinterpret_cast<float4*>(out + c0 + c) =
+              make_float4(__uint_as_float(rr[c]), __uint_as_float(rr[c + 1]),
+                          __uint_as_float(rr[c + 2]), __uint_as_float(rr[c + 3]));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+cudaError_t bwd_tm(const BwdParams& a, cudaStream_t s) {
+  using L = BwdTmLayout;
+  const AttnGeom& g = a.g;
+  BwdKParams p;
+  p.hq = g.hq;
+  p.hkv = g.hkv;
+  p.gq = g.gq;
+  p.R = g.R;
+  p.P = g.P;
+  p.pool_pages = g.pool_pages;
+  p.pool_rows = g.pool_pages * g.hkv * g.page_size;
+  p.page_size = g.page_size;
+  p.ns = g.ns;
+  p.split_span = g.split_span;
+  p.n_mt = (int)(((int64_t)g.gq * g.R + kBM - 1) / kBM);
+  p.scale_log2 = g.scale_log2;
+  p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
+  p.d_o = reinterpret_cast<const __nv_bfloat16*>(a.d_o);
+  p.lse = a.lse;
+  p.delta = a.delta;
+  p.page_table = a.page_table;
+  p.dq_parts = a.dq_parts;
+  p.status = a.status;
+  CUtensorMap tk, tv, tkr, tvr;
+  memset(&tk, 0, sizeof(tk));
+  memset(&tv, 0, sizeof(tv));
+  if (g.P > 0 && (!encode_pool_map(&tk, a.k_pool, p.pool_rows, L::BN) ||
+                  !encode_pool_map(&tv, a.v_pool, p.pool_rows, L::BN)))
+    return cudaErrorInvalidValue;
+  if (!encode_rows_map(&tkr, a.k_resp, g.hkv, g.R, L::BN) ||
+      !encode_rows_map(&tvr, a.v_resp, g.hkv, g.R, L::BN))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd_dq_tm_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kSmem);
+  if (e != cudaSuccess) return e;
+  const int64_t units = (int64_t)(g.ns + 1) * g.hkv * p.n_mt;
+  if (units == 0) return cudaSuccess;
+  LaunchScope ls(kKTcBwdDq, s);
+  tc_bwd_dq_tm_kernel<<<(unsigned)units, kThreads, L::kSmem, s>>>(tk, tv, tkr, tvr, p);
+  return cudaGetLastError();
+}
+
 int bwd_variant_id() {
   static int v = [] {
     const char* e = getenv("LS_TC_BWD_VARIANT");
@@ -416,10 +797,14 @@ int bwd_variant_id() {
 
 }  // namespace
 
+// Default: dO in tensor memory with three V stages.  LS_TC_BWD_VARIANT
+// selects the shared-memory-dO kernels for comparison: 1 = 64-key tiles (two
+// K stages, one V stage), 2 = 32-key tiles.
 cudaError_t launch_tc_bwd_dq(const BwdParams& a, cudaStream_t s) {
   switch (bwd_variant_id()) {
-    case 1: return bwd_variant<32, 3, 3>(a, s);
-    default: return bwd_variant<64, 2, 1>(a, s);
+    case 1: return bwd_variant<64, 2, 1>(a, s);
+    case 2: return bwd_variant<32, 3, 3>(a, s);
+    default: return bwd_tm(a, s);
   }
 }
 

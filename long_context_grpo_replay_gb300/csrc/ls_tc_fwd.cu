@@ -12,8 +12,9 @@
 // LSE/output merge", LongStraw DeepRead summary, section "Method").
 //
 // Warp roles (256 threads):
-//   warp 0 lane 0 : TMA producer for K tiles
-//   warp 3 lane 0 : TMA producer for V tiles
+//   warp 0        : TMA producer for K tiles (lanes 0..3 issue the four
+//                   64-column boxes of a tile, lane 0 posts the byte count)
+//   warp 3        : TMA producer for V tiles, the same way
 //   warp 1 lane 0 : MMA issuer: S[b] = Q K^T (SS), O += P V (P from shared or
 //                   tensor memory, V as an N-major B operand)
 //   warp 2        : tensor-memory allocation / release
@@ -160,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto pool_row = [&](int64_t key0) -> int32_t {
     const int32_t slot = __ldg(p.page_table + key0 / p.page_size);
     if (slot < 0 || slot >= p.pool_pages) {
-      atomicOr(p.status, kStatusBadPage);
+      if (lane == 0) atomicOr(p.status, kStatusBadPage);
       return (int32_t)p.pool_rows;
     }
     return (int32_t)(((int64_t)slot * p.hkv + kvh) * p.page_size + key0 % p.page_size);
@@ -168,34 +169,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 || warp == 3) {
     // ------------------------------------------------------------ producers
-    if (lane == 0 && ntiles > 0) {
+    // whole warps: lane 0 posts the expected bytes, lanes 0..3 each issue one
+    // of the tile's four boxes (a TMA issue holds its thread for a while, so
+    // the boxes go out in parallel)
+    if (ntiles > 0) {
       const bool isK = warp == 0;
       const CUtensorMap* tm = resp ? (isK ? &tmKr : &tmVr) : (isK ? &tmK : &tmV);
       uint64_t* full = isK ? bar_kf : bar_vf;
       uint64_t* empty = isK ? bar_ke : bar_ve;
       const uint32_t sdst = isK ? sK : sV;
-      prefetch_tmap(tm);
+      if (lane == 0) prefetch_tmap(tm);
       int issued = 0;
       for (int j = 0; j < ntiles; ++j) {
         const int st = j % KST;
-        if (j >= KST && !mbar_wait(smem_u32(&empty[st]), ((j / KST) - 1) & 1, abortp)) {
+        if (j >= KST && !mbar_wait_warp(smem_u32(&empty[st]), ((j / KST) - 1) & 1, abortp)) {
           fail(__LINE__);
           break;
         }
         const int64_t key0 = kb + (int64_t)j * BN;
         const uint32_t fb = smem_u32(&full[st]);
-        mbar_expect_tx(fb, L::kKVBytes);
-        if (resp) {
-          // response rows past R read as zeros
-#pragma unroll
-          for (int c = 0; c < kD / 64; ++c)
+        const int32_t row = resp ? 0 : pool_row(key0);
+        if (lane == 0) mbar_expect_tx(fb, L::kKVBytes);
+        __syncwarp();
+        if (lane < kD / 64) {
+          const int c = lane;
+          if (resp)
             tma_load_3d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, kvh, (int32_t)key0);
-        } else {
-          const int32_t row = pool_row(key0);
-#pragma unroll
-          for (int c = 0; c < kD / 64; ++c)
+          else
             tma_load_2d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, row);
         }
+        __syncwarp();
         issued = j + 1;
       }
       // make sure no copy is still landing in shared memory when the CTA ends
@@ -473,13 +476,13 @@ int fwd_variant_id() {
 
 }  // namespace
 
-// Default: 128-key tiles (N=128 QK^T runs the tensor pipe at full rate, N=64
-// at about two thirds), P kept in tensor memory, one K and one V stage.
-// LS_TC_FWD_VARIANT selects the 64-key-tile variants for comparison.
+// Default: 128-key tiles with one K and one V stage and P in tensor memory.
+// LS_TC_FWD_VARIANT selects the 64-key kernels for comparison: 2 / 3 = two
+// stages with P in shared / tensor memory.
 cudaError_t launch_tc_fwd(const FwdParams& a, cudaStream_t s) {
   switch (fwd_variant_id()) {
-    case 1: return fwd_variant<64, 2, false>(a, s);
-    case 2: return fwd_variant<64, 2, true>(a, s);
+    case 2: return fwd_variant<64, 2, false>(a, s);
+    case 3: return fwd_variant<64, 2, true>(a, s);
     default: return fwd_variant<128, 1, true>(a, s);
   }
 }
