@@ -127,6 +127,9 @@ bool encode_pool_map(CUtensorMap* m, const void* base, int64_t rows, int box_row
 // boxes and the 128-byte swizzle (response K/V, Q, dO); rows past the end
 // read as zeros.
 bool encode_rows_map(CUtensorMap* m, const void* base, int heads, int64_t rows, int box_rows);
+// One-instruction [box_rows x 256] tiles landing as four swizzled column boxes.
+bool encode_pool_tile_map(CUtensorMap* m, const void* base, int64_t rows, int box_rows);
+bool encode_rows_tile_map(CUtensorMap* m, const void* base, int heads, int64_t rows, int box_rows);
 cudaError_t launch_tc_dkdv(const BwdParams& p, cudaStream_t s);
 
 }  // namespace ls

@@ -414,15 +414,25 @@ cudaError_t bwd_variant(const BwdParams& a, cudaStream_t s) {
 
 // ===========================================================================
 // Backward with dO held in tensor memory (default).  dP = dO V^T takes dO as
-// the A operand from tensor memory, which frees 64 KB of shared memory for a
-// third V stage (V_j is needed only by dP_j, and its load latency is what the
-// two-stage layout exposes).  Tensor memory: dQ [0,256), dO [256,384) (bf16
-// pairs), S [384,448), dP [448,512).  The softmax warps release S as soon as
-// they have read it and write dS over dP, so S_{j+1} runs while they work:
-//   MMA order: S_0, dP_0, then per tile j: S_{j+1}, dQ_j, dP_{j+1}.
+// the A operand from tensor memory, which leaves shared memory for two K and
+// three V tile slots.  Tensor memory: dQ [0,256), dO [256,384) (bf16 pairs),
+// S [384,448), dP [448,512).  The softmax warps release S as soon as they
+// have read it and write dS (bf16) over the first half of dP.
+//
+// The MMA thread issues, per key tile j:  S_{j+1}, dQ_j, dP_{j+1}.
+// Its issue blocks at about the rate the tensor pipe executes, and every
+// commit and every barrier test between groups costs pipe time, so the tile
+// carries as few of them as the dependencies allow:
+//   waits   : tile_full (K and V of one tile, one barrier), s_free, ds_full
+//   commits : s_full after S; dp_full and tile_free after dP (dP_{j+1}
+//             follows dQ_j, so it frees V_{j+1} and K_j).
+// A K tile lives from its load to its dQ, so K gets three slots and V two:
+// tile m's K and V go out together once dP_{m-2} is done, about one tile
+// period of MMA work before S_m needs them.  One producer warp loads a whole
+// K or V tile with a single TMA instruction.
 // ===========================================================================
 struct BwdTmLayout {
-  static constexpr int BN = 64, KSK = 2, KSV = 3;
+  static constexpr int BN = 64, KSK = 3, KSV = 2, NT = 3;  // K slots, V slots, tile barriers
   static constexpr uint32_t kRowBox = kBM * 128;        // 16 KB
   static constexpr uint32_t kKVBytes = BN * kD * 2;     // 32 KB
   static constexpr uint32_t kKVBox = BN * 128;          // 8 KB
@@ -433,6 +443,10 @@ struct BwdTmLayout {
   static constexpr uint32_t kSmem = kEnd + 1024;
   static constexpr uint32_t kTmemO = 256, kTmemS = 384, kTmemP = 448;
   static_assert(kSmem <= 227 * 1024 - 512, "shared memory budget");
+  // tile_free of tile m-KSV (committed after dP_{m-KSV}) frees V slot m%KSV
+  // and, since dQ_{m-KSV-1} was issued before that dP, K slot m%KSK
+  static_assert(KSK == KSV + 1, "slot release assumes one more K slot than V slots");
+  static_assert(KSV <= NT, "tile barrier ring too short");
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -441,10 +455,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmKr,
                         const __grid_constant__ CUtensorMap tmVr, const BwdKParams p) {
   using L = BwdTmLayout;
-  constexpr int BN = L::BN, KSK = L::KSK, KSV = L::KSV;
+  constexpr int BN = L::BN, KSK = L::KSK, KSV = L::KSV, NT = L::NT;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_kf[KSK], bar_ke[KSK], bar_vf[KSV], bar_ve[KSV], bar_sf,
-      bar_sfree, bar_dpf, bar_dsf, bar_fin, bar_drain;
+  __shared__ uint64_t bar_q, bar_tf[NT], bar_te[NT], bar_sf, bar_sfree, bar_dpf, bar_dsf, bar_fin,
+      bar_drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ uint32_t abort_s;
 
@@ -473,13 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     abort_s = 0;
     mbar_init(smem_u32(&bar_q), 128);
-    for (int s = 0; s < KSK; ++s) {
-      mbar_init(smem_u32(&bar_kf[s]), 1);
-      mbar_init(smem_u32(&bar_ke[s]), 1);
-    }
-    for (int s = 0; s < KSV; ++s) {
-      mbar_init(smem_u32(&bar_vf[s]), 1);
-      mbar_init(smem_u32(&bar_ve[s]), 1);
+    for (int s = 0; s < NT; ++s) {
+      mbar_init(smem_u32(&bar_tf[s]), 1);
+      mbar_init(smem_u32(&bar_te[s]), 1);
     }
     mbar_init(smem_u32(&bar_sf), 1);
     mbar_init(smem_u32(&bar_sfree), 128);
@@ -503,104 +513,111 @@ __global__ void __launch_bounds__(kThreads, 1)
     atomicCAS(p.status + 1, 0u, ((uint32_t)kKTcBwdDq << 16) | (uint32_t)line);
     abort_s = 1;
   };
-  auto pool_row = [&](int64_t key0) -> int32_t {
-    const int32_t slot = __ldg(p.page_table + key0 / p.page_size);
-    if (slot < 0 || slot >= p.pool_pages) {
-      if (lane == 0) atomicOr(p.status, kStatusBadPage);
-      return (int32_t)p.pool_rows;
-    }
-    return (int32_t)(((int64_t)slot * p.hkv + kvh) * p.page_size + key0 % p.page_size);
-  };
 
-  if (warp == 0 || warp == 3) {
-    // ------------------------------------------------------------ producers
-    // whole warps; lane 0 posts the bytes, lanes 0..3 issue the four boxes
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // whole warp: lane 0 posts the bytes and loads K, lane 1 loads V, each
+    // tile with one instruction
     if (ntiles > 0) {
-      const bool isK = warp == 0;
-      const int nst = isK ? KSK : KSV;
-      const CUtensorMap* tm = resp ? (isK ? &tmKr : &tmVr) : (isK ? &tmK : &tmV);
-      uint64_t* full = isK ? bar_kf : bar_vf;
-      uint64_t* empty = isK ? bar_ke : bar_ve;
-      const uint32_t sdst = isK ? sK : sV;
-      if (lane == 0) prefetch_tmap(tm);
+      if (lane == 0) prefetch_tmap(resp ? &tmKr : &tmK);
+      if (lane == 1) prefetch_tmap(resp ? &tmVr : &tmV);
       int issued = 0;
-      for (int j = 0; j < ntiles; ++j) {
-        const int st = j % nst;
-        if (j >= nst && !mbar_wait_warp(smem_u32(&empty[st]), ((j / nst) - 1) & 1, abortp)) {
-          fail(__LINE__);
+      for (int m = 0; m < ntiles; ++m) {
+        // V slot m%KSV last held tile m-KSV and K slot m%KSK tile m-KSV-1;
+        // both are free once dP_{m-KSV} has completed
+        bool ok = true;
+        if (m >= KSV) {
+          const int o = m - KSV;
+          ok = mbar_wait_warp(smem_u32(&bar_te[o % NT]), (o / NT) & 1, abortp);
+        }
+        if (!ok) {
+          if (lane == 0) fail(__LINE__);
           break;
         }
-        const int64_t key0 = kb + (int64_t)j * BN;
-        const uint32_t fb = smem_u32(&full[st]);
-        const int32_t row = resp ? 0 : pool_row(key0);
-        if (lane == 0) mbar_expect_tx(fb, L::kKVBytes);
+        const int64_t key0 = kb + (int64_t)m * BN;
+        const uint32_t fb = smem_u32(&bar_tf[m % NT]);
+        int32_t row = 0;
+        if (!resp) {
+          const int32_t slot = __ldg(p.page_table + key0 / p.page_size);
+          if (slot < 0 || slot >= p.pool_pages) {
+            if (lane == 0) atomicOr(p.status, kStatusBadPage);
+            row = (int32_t)p.pool_rows;  // out of range: the load reads zeros
+          } else {
+            row = (int32_t)(((int64_t)slot * p.hkv + kvh) * p.page_size + key0 % p.page_size);
+          }
+        }
+        if (lane == 0) mbar_expect_tx(fb, 2 * L::kKVBytes);
         __syncwarp();
-        if (lane < kD / 64) {
-          const int c = lane;
+        if (lane < 2) {
+          const uint32_t dst = lane == 0 ? sK + (m % KSK) * L::kKVBytes : sV + (m % KSV) * L::kKVBytes;
           if (resp)
-            tma_load_3d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, kvh, (int32_t)key0);
+            tma_load_4d(dst, lane == 0 ? &tmKr : &tmVr, fb, 0, (int32_t)key0, 0, kvh);
           else
-            tma_load_2d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, row);
+            tma_load_3d(dst, lane == 0 ? &tmK : &tmV, fb, 0, row, 0);
         }
         __syncwarp();
-        issued = j + 1;
+        issued = m + 1;
       }
-      for (int j = issued - nst < 0 ? 0 : issued - nst; j < issued; ++j)
-        mbar_wait(smem_u32(&full[j % nst]), (j / nst) & 1, abortp);
+      // no copy may still be landing in shared memory when the CTA ends
+      for (int m = issued - NT < 0 ? 0 : issued - NT; m < issued; ++m)
+        mbar_wait(smem_u32(&bar_tf[m % NT]), (m / NT) & 1, abortp);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(kBM, BN, false);
       constexpr uint32_t idesc_dq = idesc_bf16(kBM, kD, true);
-      auto issue_s = [&](int j) -> bool {  // S = Q K_j^T
-        const int st = j % KSK;
-        if (!mbar_wait(smem_u32(&bar_kf[st]), (j / KSK) & 1, abortp)) { fail(__LINE__); return false; }
-        tc_fence_after();
+      auto issue_s = [&](int j) {  // S = Q K_j^T
+        const uint32_t kslot = sK + (j % KSK) * L::kKVBytes;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
           mma_ss(tbase + L::kTmemS, sdesc_sw128(sQ + (kk >> 2) * L::kRowBox + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(sK + st * L::kKVBytes + (kk >> 2) * L::kKVBox + (kk & 3) * 32, 16, 1024),
-                 idesc_s, kk > 0 ? 1u : 0u);
+                 sdesc_sw128(kslot + (kk >> 2) * L::kKVBox + (kk & 3) * 32, 16, 1024), idesc_s,
+                 kk > 0 ? 1u : 0u);
         mma_commit(smem_u32(&bar_sf));
-        return true;
       };
-      auto issue_dp = [&](int j) -> bool {  // dP = dO V_j^T, dO from tensor memory
-        const int st = j % KSV;
-        if (!mbar_wait(smem_u32(&bar_vf[st]), (j / KSV) & 1, abortp)) { fail(__LINE__); return false; }
-        tc_fence_after();
+      auto issue_dp = [&](int j) {  // dP = dO V_j^T, dO from tensor memory
+        const uint32_t vslot = sV + (j % KSV) * L::kKVBytes;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
           mma_ts(tbase + L::kTmemP, tbase + L::kTmemO + kk * 8,
-                 sdesc_sw128(sV + st * L::kKVBytes + (kk >> 2) * L::kKVBox + (kk & 3) * 32, 16, 1024),
-                 idesc_s, kk > 0 ? 1u : 0u);
-        mma_commit(smem_u32(&bar_ve[st]));
+                 sdesc_sw128(vslot + (kk >> 2) * L::kKVBox + (kk & 3) * 32, 16, 1024), idesc_s,
+                 kk > 0 ? 1u : 0u);
         mma_commit(smem_u32(&bar_dpf));
-        return true;
+        mma_commit(smem_u32(&bar_te[j % NT]));  // V_j and K_{j-1} are done
       };
-      bool ok = mbar_wait(smem_u32(&bar_q), 0, abortp);
+      bool ok = mbar_wait(smem_u32(&bar_q), 0, abortp) && mbar_wait(smem_u32(&bar_tf[0]), 0, abortp);
       if (!ok) fail(__LINE__);
       tc_fence_after();
-      if (ok) ok = issue_s(0) && issue_dp(0);
+      if (ok) {
+        issue_s(0);
+        issue_dp(0);
+      }
       for (int j = 0; ok && j < ntiles; ++j) {
         if (j + 1 < ntiles) {
-          // S columns are free once the softmax warps have read S_j
-          if (!mbar_wait(smem_u32(&bar_sfree), j & 1, abortp)) { fail(__LINE__); break; }
-          if (!issue_s(j + 1)) break;
+          // S columns are free once the softmax warps have read S_j; K and V
+          // of tile j+1 arrive on one barrier
+          const int n1 = j + 1;
+          if (!mbar_wait(smem_u32(&bar_sfree), j & 1, abortp) ||
+              !mbar_wait(smem_u32(&bar_tf[n1 % NT]), (n1 / NT) & 1, abortp)) {
+            fail(__LINE__);
+            break;
+          }
+          tc_fence_after();
+          issue_s(n1);
         }
         // dQ += dS_j K_j, dS read from the dP columns
         if (!mbar_wait(smem_u32(&bar_dsf), j & 1, abortp)) { fail(__LINE__); break; }
         tc_fence_after();
-        const int st = j % KSK;
+        const uint32_t kslot = sK + (j % KSK) * L::kKVBytes;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ts(tbase, tbase + L::kTmemP + kk * 8,
-                 sdesc_sw128(sK + st * L::kKVBytes + kk * 16 * 128, L::kKVBox, 1024), idesc_dq,
+                 sdesc_sw128(kslot + kk * 16 * 128, L::kKVBox, 1024), idesc_dq,
                  (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&bar_ke[st]));
         if (j == ntiles - 1) mma_commit(smem_u32(&bar_fin));
         // dP_{j+1} overwrites dS_j, which dQ_j (issued before it) has consumed
-        if (j + 1 < ntiles && !issue_dp(j + 1)) break;
+        if (j + 1 < ntiles) issue_dp(j + 1);
       }
       mma_commit(smem_u32(&bar_drain));
       mbar_wait(smem_u32(&bar_drain), 0, abortp);
@@ -696,13 +713,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!resp && nvalid_tile < BN) {
         // partial last prompt tile: rows past the prompt end may hold anything;
         // zero them in K so that dS = 0 times K stays 0 in dQ += dS K
-        const int st = j % KSK;
+        const uint32_t kslot = sK + (j % KSK) * L::kKVBytes;
         const int nz = (BN - nvalid_tile) * (kD / 64) * 8;
         for (int z = i; z < nz; z += 128) {
           const int row = nvalid_tile + z / ((kD / 64) * 8);
           const int box = (z / 8) % (kD / 64);
-          st_shared_v4(sK + st * L::kKVBytes + box * L::kKVBox + row * 128 + (z & 7) * 16,
-                       make_uint4(0u, 0u, 0u, 0u));
+          st_shared_v4(kslot + box * L::kKVBox + row * 128 + (z & 7) * 16, make_uint4(0u, 0u, 0u, 0u));
         }
         fence_proxy_async_smem();
       }
@@ -771,11 +787,11 @@ cudaError_t bwd_tm(const BwdParams& a, cudaStream_t s) {
   CUtensorMap tk, tv, tkr, tvr;
   memset(&tk, 0, sizeof(tk));
   memset(&tv, 0, sizeof(tv));
-  if (g.P > 0 && (!encode_pool_map(&tk, a.k_pool, p.pool_rows, L::BN) ||
-                  !encode_pool_map(&tv, a.v_pool, p.pool_rows, L::BN)))
+  if (g.P > 0 && (!encode_pool_tile_map(&tk, a.k_pool, p.pool_rows, L::BN) ||
+                  !encode_pool_tile_map(&tv, a.v_pool, p.pool_rows, L::BN)))
     return cudaErrorInvalidValue;
-  if (!encode_rows_map(&tkr, a.k_resp, g.hkv, g.R, L::BN) ||
-      !encode_rows_map(&tvr, a.v_resp, g.hkv, g.R, L::BN))
+  if (!encode_rows_tile_map(&tkr, a.k_resp, g.hkv, g.R, L::BN) ||
+      !encode_rows_tile_map(&tvr, a.v_resp, g.hkv, g.R, L::BN))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_dq_tm_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kSmem);

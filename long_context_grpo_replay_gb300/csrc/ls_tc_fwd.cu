@@ -12,9 +12,8 @@
 // LSE/output merge", LongStraw DeepRead summary, section "Method").
 //
 // Warp roles (256 threads):
-//   warp 0        : TMA producer for K tiles (lanes 0..3 issue the four
-//                   64-column boxes of a tile, lane 0 posts the byte count)
-//   warp 3        : TMA producer for V tiles, the same way
+//   warp 0        : TMA producer for K tiles (one instruction per tile)
+//   warp 3        : TMA producer for V tiles
 //   warp 1 lane 0 : MMA issuer: S[b] = Q K^T (SS), O += P V (P from shared or
 //                   tensor memory, V as an N-major B operand)
 //   warp 2        : tensor-memory allocation / release
@@ -169,9 +168,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 || warp == 3) {
     // ------------------------------------------------------------ producers
-    // whole warps: lane 0 posts the expected bytes, lanes 0..3 each issue one
-    // of the tile's four boxes (a TMA issue holds its thread for a while, so
-    // the boxes go out in parallel)
+    // whole warps; lane 0 posts the expected bytes and loads the whole tile
+    // with one TMA instruction (the per-instruction cost of TMA, not its
+    // bandwidth, limits small boxes)
     if (ntiles > 0) {
       const bool isK = warp == 0;
       const CUtensorMap* tm = resp ? (isK ? &tmKr : &tmVr) : (isK ? &tmK : &tmV);
@@ -191,12 +190,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t row = resp ? 0 : pool_row(key0);
         if (lane == 0) mbar_expect_tx(fb, L::kKVBytes);
         __syncwarp();
-        if (lane < kD / 64) {
-          const int c = lane;
+        if (lane == 0) {
           if (resp)
-            tma_load_3d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, kvh, (int32_t)key0);
+            tma_load_4d(sdst + st * L::kKVBytes, tm, fb, 0, (int32_t)key0, 0, kvh);
           else
-            tma_load_2d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, row);
+            tma_load_3d(sdst + st * L::kKVBytes, tm, fb, 0, row, 0);
         }
         __syncwarp();
         issued = j + 1;
@@ -450,11 +448,11 @@ cudaError_t fwd_variant(const FwdParams& a, cudaStream_t s) {
   CUtensorMap tk, tv, tkr, tvr;
   memset(&tk, 0, sizeof(tk));
   memset(&tv, 0, sizeof(tv));
-  if (g.P > 0 && (!encode_pool_map(&tk, a.k_pool, p.pool_rows, BN) ||
-                  !encode_pool_map(&tv, a.v_pool, p.pool_rows, BN)))
+  if (g.P > 0 && (!encode_pool_tile_map(&tk, a.k_pool, p.pool_rows, BN) ||
+                  !encode_pool_tile_map(&tv, a.v_pool, p.pool_rows, BN)))
     return cudaErrorInvalidValue;
-  if (!encode_rows_map(&tkr, a.k_resp, g.hkv, g.R, BN) ||
-      !encode_rows_map(&tvr, a.v_resp, g.hkv, g.R, BN))
+  if (!encode_rows_tile_map(&tkr, a.k_resp, g.hkv, g.R, BN) ||
+      !encode_rows_tile_map(&tvr, a.v_resp, g.hkv, g.R, BN))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel<BN, KST, P_TMEM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kSmem);
