@@ -398,17 +398,18 @@ bool encode_rows_map(CUtensorMap* m, const void* base, int heads, int64_t rows, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Whole-tile maps: one TMA instruction moves a [box_rows x 256] bf16 tile and
-// lands it as four 128B-swizzled [box_rows x 64] column boxes, one after the
-// other (the layout the MMA descriptors address).  The 256 columns of a row
+// Whole-tile maps: one TMA instruction moves a [box_rows x 64*box_blocks]
+// bf16 tile and lands it as box_blocks 128B-swizzled [box_rows x 64] column
+// boxes, one after the other (the layout the MMA descriptors address).  The 256 columns of a row
 // are viewed as (64 columns) x (4 column blocks): dim 0 = column in block,
 // dim 1 = row, dim 2 = column block (stride 128 bytes).
-bool encode_pool_tile_map(CUtensorMap* m, const void* base, int64_t rows, int box_rows) {
+bool encode_pool_tile_map(CUtensorMap* m, const void* base, int64_t rows, int box_rows,
+                          int box_blocks) {
   EncodeTiledFn enc = encoder();
   if (!enc) return false;
   cuuint64_t gdim[3] = {64u, (cuuint64_t)rows, 4u};
   cuuint64_t gstr[2] = {256u * 2u, 64u * 2u};
-  cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 4u};
+  cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, (cuuint32_t)box_blocks};
   cuuint32_t es[3] = {1u, 1u, 1u};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstr, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -417,12 +418,13 @@ bool encode_pool_tile_map(CUtensorMap* m, const void* base, int64_t rows, int bo
 
 // The same over token-major [rows][heads][256] data: dim 1 = token (stride
 // heads*512 bytes), dim 3 = head; rows past the end read as zero.
-bool encode_rows_tile_map(CUtensorMap* m, const void* base, int heads, int64_t rows, int box_rows) {
+bool encode_rows_tile_map(CUtensorMap* m, const void* base, int heads, int64_t rows, int box_rows,
+                          int box_blocks) {
   EncodeTiledFn enc = encoder();
   if (!enc) return false;
   cuuint64_t gdim[4] = {64u, (cuuint64_t)rows, 4u, (cuuint64_t)heads};
   cuuint64_t gstr[3] = {(cuuint64_t)heads * 256u * 2u, 64u * 2u, 256u * 2u};
-  cuuint32_t box[4] = {64u, (cuuint32_t)box_rows, 4u, 1u};
+  cuuint32_t box[4] = {64u, (cuuint32_t)box_rows, (cuuint32_t)box_blocks, 1u};
   cuuint32_t es[4] = {1u, 1u, 1u, 1u};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), gdim, gstr, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

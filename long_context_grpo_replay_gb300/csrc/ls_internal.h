@@ -127,9 +127,12 @@ bool encode_pool_map(CUtensorMap* m, const void* base, int64_t rows, int box_row
 // boxes and the 128-byte swizzle (response K/V, Q, dO); rows past the end
 // read as zeros.
 bool encode_rows_map(CUtensorMap* m, const void* base, int heads, int64_t rows, int box_rows);
-// One-instruction [box_rows x 256] tiles landing as four swizzled column boxes.
-bool encode_pool_tile_map(CUtensorMap* m, const void* base, int64_t rows, int box_rows);
-bool encode_rows_tile_map(CUtensorMap* m, const void* base, int heads, int64_t rows, int box_rows);
+// One-instruction [box_rows x 64*box_blocks] tiles landing as box_blocks
+// swizzled [box_rows x 64] column boxes (pool rows; token-major rows).
+bool encode_pool_tile_map(CUtensorMap* m, const void* base, int64_t rows, int box_rows,
+                          int box_blocks = 4);
+bool encode_rows_tile_map(CUtensorMap* m, const void* base, int heads, int64_t rows, int box_rows,
+                          int box_blocks = 4);
 cudaError_t launch_tc_dkdv(const BwdParams& p, cudaStream_t s);
 
 }  // namespace ls

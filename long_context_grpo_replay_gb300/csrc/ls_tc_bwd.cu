@@ -298,7 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t rs[32], rp[32];
         tmem_ld32(tbase + lane_off + L::kTmemS + b * 2 * BN + c0, rs);
         tmem_ld32(tbase + lane_off + L::kTmemS + b * 2 * BN + BN + c0, rp);
-        tmem_wait_ld();
+        tmem_wait_ld_r(rs);
+        reg_dep(rp);
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           float ds2[2];
@@ -345,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();  // the row_ok stores of the previous chunk diverge
       if (ok && ntiles > 0) {
         tmem_ld32(tbase + lane_off + c0, rr);
-        tmem_wait_ld();
+        tmem_wait_ld_r(rr);
       } else {
 #pragma unroll
         for (int c = 0; c < 32; ++c) rr[c] = 0u;
@@ -681,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t rs[32];
         tmem_ld32(tbase + lane_off + L::kTmemS + c0, rs);
-        tmem_wait_ld();
+        tmem_wait_ld_r(rs);
 #pragma unroll
         for (int c = 0; c < 32; ++c) pv[c0 + c] = __uint_as_float(rs[c]);
       }
@@ -697,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t rp[32];
         tmem_ld32(tbase + lane_off + L::kTmemP + c0, rp);
-        tmem_wait_ld();
+        tmem_wait_ld_r(rp);
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           const float d0 = c0 + c < nvalid ? pv[c0 + c] * (__uint_as_float(rp[c]) - dl) : 0.f;
@@ -738,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (ok && ntiles > 0) {
         tmem_ld32(tbase + lane_off + c0, rr);
-        tmem_wait_ld();
+        tmem_wait_ld_r(rr);
       } else {
 #pragma unroll
         for (int c = 0; c < 32; ++c) rr[c] = 0u;

@@ -215,7 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t rs[32], rp[32];
         tmem_ld32(tbase + lane_off + L::kTmemS + c0, rs);
         tmem_ld32(tbase + lane_off + L::kTmemP + c0, rp);
-        tmem_wait_ld();
+        tmem_wait_ld_r(rs);
+        reg_dep(rp);
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           float pv[2], dv[2];
@@ -254,7 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();  // the j < R stores of the previous chunk diverge
         tmem_ld32(tbase + lane_off + L::kTmemDK + c0, rk);
         tmem_ld32(tbase + lane_off + L::kTmemDV + c0, rv);
-        tmem_wait_ld();
+        tmem_wait_ld_r(rk);
+        reg_dep(rv);
         if (j >= p.R) continue;
 #pragma unroll
         for (int c = 0; c < 32; c += 8) {
