@@ -586,6 +586,22 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
         prefetch_tmap(resp ? &tmKr : &tmK);
         prefetch_tmap(resp ? &tmVr : &tmV);
       }
+      // Page ids are fetched one K tile ahead, so the page-table load latency
+      // is not on the issue path; a K tile's row is kept until its V tile.
+      auto page_of = [&](int j) -> int32_t {
+        return resp ? 0 : __ldg(p.page_table + (kb + (int64_t)j * BN) / p.page_size);
+      };
+      auto row_of = [&](int32_t slot, int j) -> int32_t {
+        if (resp) return 0;
+        if (slot < 0 || slot >= p.pool_pages) {
+          if (lane == 0) atomicOr(p.status, kStatusBadPage);
+          return (int32_t)p.pool_rows;  // out of range: the load reads zeros
+        }
+        return (int32_t)(((int64_t)slot * p.hkv + kvh) * p.page_size + (kb + (int64_t)j * BN) % p.page_size);
+      };
+      int32_t pf_slot = page_of(0);
+      int32_t rk = 0, rk_prev = 0;  // rows of the last K tile issued (jk) and of jk-1
+      int jk = -1;
       int issued = 0;
       bool ok = true;
       for (int u = 0; ok && u < nunits; ++u) {
@@ -602,15 +618,15 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
           isK = false, j = (u - 2) / 2;
         }
         const int64_t key0 = kb + (int64_t)j * BN;
-        int32_t row = 0;
-        if (!resp) {
-          const int32_t slot = __ldg(p.page_table + key0 / p.page_size);
-          if (slot < 0 || slot >= p.pool_pages) {
-            if (lane == 0) atomicOr(p.status, kStatusBadPage);
-            row = (int32_t)p.pool_rows;  // out of range: the load reads zeros
-          } else {
-            row = (int32_t)(((int64_t)slot * p.hkv + kvh) * p.page_size + key0 % p.page_size);
-          }
+        int32_t row;
+        if (isK) {
+          rk_prev = rk;
+          rk = row_of(pf_slot, j);
+          jk = j;
+          if (j + 1 < ntiles) pf_slot = page_of(j + 1);
+          row = rk;
+        } else {
+          row = j == jk ? rk : rk_prev;  // V_j follows K_{j+1}, or K_j for the last tile
         }
         const uint32_t fb = smem_u32(&bar_uf[u % NU]);
         for (int h = 0; h < 2; ++h) {
