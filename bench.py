@@ -290,15 +290,19 @@ def run_ours(args):
 def run_e2e(args, w, desc, src, members, k_pool, v_pool, pt, prompt, ws, stream, dev, flops_step,
             world):
     """Same step through the public API with pinned host inputs: H2D of the
-    prompt K/V, page table and member inputs, the replay, D2H of the outputs."""
+    prompt K/V, page table and member inputs, the page write and the replay,
+    D2H of the outputs.  Like a data loader, the next step's inputs are
+    copied on a second stream into a second set of device buffers while this
+    step computes, so each step's H2D is inside the timed region but off its
+    critical path (the first step's is not hidden)."""
     import torch
     import long_context_grpo_replay_gb300.binding as ls
 
+    in_keys = ("q", "k", "v", "d_o")
+    out_keys = ("o", "lse", "dq", "dk", "dv")
     h_src = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in src.items()}
     for k in h_src:
         h_src[k].copy_(src[k])
-    in_keys = ("q", "k", "v", "d_o")
-    out_keys = ("o", "lse", "dq", "dk", "dv")
     h_in = [{k: torch.empty(m[k].shape, dtype=m[k].dtype, pin_memory=True).copy_(m[k])
              for k in in_keys} for m in members]
     h_out = [{k: torch.empty(m[k].shape, dtype=m[k].dtype, pin_memory=True) for k in out_keys}
@@ -307,34 +311,57 @@ def run_e2e(args, w, desc, src, members, k_pool, v_pool, pt, prompt, ws, stream,
         sum(t.numel() * t.element_size() for m in h_in for t in m.values())
     d2h = sum(t.numel() * t.element_size() for m in h_out for t in m.values())
 
-    def step():
-        for k in h_src:
-            src[k].copy_(h_src[k], non_blocking=True)
-        for m, hm in zip(members, h_in):
-            for k in in_keys:
-                m[k].copy_(hm[k], non_blocking=True)
-        ls.ls_kv_page_write(desc, k_pool, v_pool, src["page_table"], 0, src["k"], src["v"], ws,
-                            stream)
-        ls.ls_replay_group(desc, prompt, members, ws, stream)
-        for m, hm in zip(members, h_out):
-            for k in out_keys:
-                hm[k].copy_(m[k], non_blocking=True)
+    # two device buffer sets: [0] reuses the bench's tensors, [1] is new
+    d_src = [src, {k: torch.empty_like(v) for k, v in src.items()}]
+    d_mem = [members, [dict(m, **{k: torch.empty_like(m[k]) for k in in_keys + out_keys})
+                       for m in members]]
+    copy_stream = torch.cuda.Stream(dev)
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    released = [torch.cuda.Event(), torch.cuda.Event()]
 
-    step()
+    def h2d_into(b):
+        copy_stream.wait_event(released[b])  # the set's previous step is done with it
+        with torch.cuda.stream(copy_stream):
+            for k in h_src:
+                d_src[b][k].copy_(h_src[k], non_blocking=True)
+            for m, hm in zip(d_mem[b], h_in):
+                for k in in_keys:
+                    m[k].copy_(hm[k], non_blocking=True)
+        copied[b].record(copy_stream)
+
+    def run(n):
+        h2d_into(0)
+        for i in range(n):
+            b = i & 1
+            if i + 1 < n:
+                h2d_into(b ^ 1)
+            stream.wait_event(copied[b])
+            ls.ls_kv_page_write(desc, k_pool, v_pool, d_src[b]["page_table"], 0, d_src[b]["k"],
+                                d_src[b]["v"], ws, stream)
+            ls.ls_replay_group(desc, prompt, d_mem[b], ws, stream)
+            with torch.cuda.stream(stream):
+                for m, hm in zip(d_mem[b], h_out):
+                    for k in out_keys:
+                        hm[k].copy_(m[k], non_blocking=True)
+            released[b].record(stream)
+
+    for b in (0, 1):
+        released[b].record(stream)
+    run(1)
     torch.cuda.synchronize()
-    n = max(1, min(args.steps, 2))
+    n = max(1, min(args.steps, 3))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     e0.record(stream)
-    for _ in range(n):
-        step()
+    run(n)
     e1.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1) / n, dev)
     return {"value": round(job_throughput(flops_step, world, ms), 3), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "steps": n, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h)}
+            "d2h_bytes_per_step": int(d2h),
+            "overlap": "next step's H2D on a copy stream into a second buffer set"}
 
 
 def _oracle_sample(w, k_pool, v_pool, pt, member, rows, kv=0):
