@@ -3,15 +3,16 @@
  *
  * The operator: exact response-replay attention for GRPO post-training with a
  * shared, detached long prompt.  The prompt is run once without gradients and
- * its full-attention K/V are kept as compact pages ("Capture once", LongStraw
- * DeepRead summary, section "Method").  Each group member's short response is
- * then replayed on its own: its queries attend over every prompt key through
- * the page table and causally over the response's own keys, partial results
- * are recombined exactly by log-sum-exp (the "global LSE/output merge" of the
- * Qwen path, same section; "exact attention composition", LongStraw abstract),
- * and the backward treats the prompt K/V as constants (the stored prompt state
- * is stop-gradient, DeepRead summary "Method", last paragraph; review mind map
- * "Equation1到3": the d(loss)/d(z_P) d(z_P)/d(theta) term is omitted).
+ * its full-attention K/V are kept as compact pages (the capture step of the
+ * LongStraw DeepRead summary, section Method).  Each group member's short
+ * response is then replayed on its own: its queries attend over every prompt
+ * key through the page table and causally over the response's own keys,
+ * partial results are recombined exactly by log-sum-exp (the Qwen path's
+ * global merge in the same section; the LongStraw abstract on exact attention
+ * composition), and the backward treats the prompt K/V as constants (the
+ * stored prompt state is stop-gradient, DeepRead summary, Method, last
+ * paragraph; the review's mind map, node on equations 1-3: the
+ * d(loss)/d(z_P) d(z_P)/d(theta) term is omitted).
  *
  * Conventions shared by every call
  * --------------------------------
@@ -122,7 +123,7 @@ typedef struct {
   void* dv;
 } ls_member;
 
-/* A1. Capture-side page write (DeepRead summary, "Method", "Capture once";
+/* A1. Capture-side page write (DeepRead summary, Method, the capture step;
  * review section 二.2: the full-attention layers keep their K/V in pages).
  * Scatters token t of k, v ([n_tok][Hkv][d]) to
  *   pool[page_table[(start_pos+t)/S_p]][kv][(start_pos+t)%S_p][:].
@@ -153,8 +154,8 @@ LS_API ls_status ls_replay_fwd(const ls_attn_desc* desc, const ls_prompt_kv* pro
                         int32_t resp_len, void* o, float* lse, void* ws, size_t ws_bytes,
                         void* stream);
 
-/* A4. Exact log-sum-exp merge of partial attention results (the "global
- * LSE/output merge" of the DeepRead summary, "Method"):
+/* A4. Exact log-sum-exp merge of partial attention results (the global
+ * LSE and output merge of the DeepRead summary, Method):
  *   L[n] = log sum_s exp(Lp[s][n]);  O[n] = sum_s exp(Lp[s][n] - L[n]) Op[s][n].
  * o_parts float32 [n_parts][n_rows][head_dim], lse_parts float32
  * [n_parts][n_rows], natural log; a part with Lp = -inf contributes nothing;
@@ -170,7 +171,7 @@ LS_API ls_status ls_replay_bwd_preprocess(const ls_attn_desc* desc, const void* 
                                    int32_t resp_len, float* delta, void* stream);
 
 /* A6+A7. Replay backward with the prompt state detached (DeepRead summary,
- * "Method": stored prompt state is stop-gradient; review section 二, last
+ * Method: stored prompt state is stop-gradient; review section 二, last
  * paragraph: on the Qwen path only the query gradient crosses ranks).
  * Recomputes P = exp(s - LSE) from the stored lse (no score matrix is kept),
  * dS = P * (dO.v - delta), and returns
@@ -185,9 +186,9 @@ LS_API ls_status ls_replay_bwd(const ls_attn_desc* desc, const ls_prompt_kv* pro
                         int32_t resp_len, void* dq, void* dk_resp, void* dv_resp,
                         void* ws, size_t ws_bytes, void* stream);
 
-/* A8. Serial suffix replay of a group (DeepRead summary, "Method", "Serial
- * suffix replay"; abstract: "rebuilds one policy response under autograd,
- * backpropagates, and pops to the prompt boundary").  For each member in order:
+/* A8. Serial replay of a group's response suffixes (DeepRead summary, Method;
+ * abstract: one response at a time is rebuilt under autograd and
+ * backpropagated, back to the prompt boundary).  For each member in order:
  * forward, preprocess, backward, all on one stream and into the one workspace,
  * so only one member's intermediates are live and the workspace does not grow
  * with n_members.  Each member's results equal a standalone replay of it. */

@@ -1,7 +1,7 @@
 // Tensor-core (tcgen05/TMEM) prompt-attention backward for bf16, head dim 256:
 // the query gradient only.  The prompt K/V are stop-gradient (LongStraw
-// DeepRead summary, section "Method", last paragraph; review mind map
-// "Equation1到3"), so no dK/dV is formed for prompt keys and the kernel is
+// DeepRead summary, section Method, last paragraph; the review's mind map,
+// node on equations 1-3), so no dK/dV is formed for prompt keys and the kernel is
 // query-stationary: a CTA keeps its 128 query rows (Q and dO tiles) in shared
 // memory, streams the part's key pages, recomputes P from the stored LSE and
 // accumulates dQ in tensor memory.  No score matrix is kept between tiles.

@@ -1,7 +1,7 @@
 // Tensor-core (tcgen05/TMEM) response dK/dV for bf16, head dim 256.
 //
 // Only response keys get K/V gradients; prompt K/V are stop-gradient
-// (LongStraw DeepRead summary, section "Method", last paragraph).  The kernel
+// (LongStraw DeepRead summary, section Method, last paragraph).  The kernel
 // is key-stationary: a CTA owns (KV head g, a tile of 128 response keys j0..,
 // one half of the head dimension) and walks the query rows that see those
 // keys (rows r >= j0 of the Gq query heads of g), 64 rows at a time.

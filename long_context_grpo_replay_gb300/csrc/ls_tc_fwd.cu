@@ -8,8 +8,8 @@
 //           never crosses a page); part ns: the response keys with the causal
 //           mask, read through a 3-D map over [R][Hkv][256].
 // Output: float32 partial O (normalised) and partial LSE (natural log) for
-// the part, merged exactly afterwards by the LSE-merge kernel ("global
-// LSE/output merge", LongStraw DeepRead summary, section "Method").
+// the part, merged exactly afterwards by the LSE-merge kernel (the global
+// LSE and output merge of the LongStraw DeepRead summary, section Method).
 //
 // Warp roles (256 threads):
 //   warp 0        : TMA producer for K tiles (one instruction per tile)

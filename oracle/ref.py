@@ -9,21 +9,23 @@ What it computes is the plain definition of the operator the LongStraw pages
 describe, written out in float64 with numpy (library matmuls as the only
 building block).  Sources, cited by page title and section:
 
-* LongStraw DeepRead summary ("LongStraw: Long-Context RL Beyond 2M Tokens under
-  a Fixed GPU Budget", kendrick-stein.github.io), section *Method*: the shared
-  prompt is run once without gradients and only the state later tokens need is
-  kept ("Capture once"); each short response is rebuilt under autograd one at a
-  time ("Serial suffix replay"); the Qwen path keeps compact KV pages for its
-  full-attention layers and does a global LSE/output merge; the stored prompt
-  state is stop-gradient.
+* LongStraw DeepRead summary (page title "LongStraw: Long-Context RL Beyond 2M
+  Tokens under a Fixed GPU Budget", kendrick-stein.github.io), section *Method*:
+  the shared prompt is run once without gradients and only the state later
+  tokens need is kept (the capture step); each short response is rebuilt under
+  autograd one at a time (the serial replay step); the Qwen path keeps compact
+  KV pages for its full-attention layers and merges partial results globally
+  by LSE; the stored prompt state is stop-gradient.
 * LongStraw review ("论文综述：LongStraw：固定GPU预算下突破200万Token的长上下文强化学习",
   paper.oopus.info), section 三 (models): full-attention layers are GQA with
-  24 query heads, 4 KV heads, head dim 256; section 七 (mind map, "Qwen3.6-27B
-  实现"): "全局LSE softmax重组 forward composition"; mind map "Equation1到3":
-  the term d(loss)/d(z_P) * d(z_P)/d(theta) is omitted (prompt state detached).
-* LongStraw abstract (cortexa.online page): "exact attention composition";
-  "rebuilds one policy response under autograd ... and pops to the prompt
-  boundary"; "response-only execution, not full-sequence gradient equivalence".
+  24 query heads, 4 KV heads, head dim 256; section 七 (mind map, node on the
+  Qwen implementation): the forward is composed by a global LSE softmax
+  recombination; mind map, node on equations 1-3: the term
+  d(loss)/d(z_P) * d(z_P)/d(theta) is omitted (prompt state detached).
+* LongStraw abstract (cortexa.online page): attention is composed exactly; one
+  policy response at a time is rebuilt under autograd, backpropagated, and
+  unwound to the prompt boundary; the claim is exactness of response-only
+  execution, not equivalence with full-sequence gradients.
 
 Readings taken where the pages are silent (each is listed in the design notes):
 softmax scale is a parameter (default 1/sqrt(d)); GQA head h reads KV head
@@ -121,7 +123,8 @@ def gather_prompt(pool, page_table, prompt_len, kv) -> np.ndarray:
 # --------------------------------------------------------------------------
 def lse_merge(o_parts, lse_parts):
     """Exact recombination of partial softmax results (DeepRead summary,
-    *Method*: "全局 LSE/output merge"; review mind map: "全局LSE softmax重组").
+    *Method*: the global LSE and output merge; review mind map: the global LSE
+    softmax recombination).
 
     o_parts [n_parts, n_rows, d], lse_parts [n_parts, n_rows] (natural log).
     L = log sum_s exp(L_s);  O = sum_s exp(L_s - L) * O_s.
@@ -155,9 +158,9 @@ def _head_rows(qh, pos, kp, vp, kr, vr, doh, scale):
 
     Softmax attention over the concatenation [prompt keys ; response keys],
     where row i sees every prompt key and the response keys j <= pos[i]
-    (DeepRead summary, *Method*; abstract: "exact attention composition").
+    (DeepRead summary, *Method*; abstract: exact attention composition).
     The backward holds the prompt K/V constant (stop-gradient prompt state,
-    review mind map "Equation1到3"), so only dQ and the response-key dK/dV
+    review mind map, node on equations 1-3), so only dQ and the response-key dK/dV
     exist.  Returns o, lse, delta, dq for the rows and this head's
     contributions to dK_resp and dV_resp from these rows."""
     n = qh.shape[0]
@@ -197,8 +200,8 @@ def replay_member(
     rows=None,
     row_chunk=None,
 ):
-    """One replayed group member (DeepRead summary, *Method*, "Serial suffix
-    replay"): forward O and LSE and, when ``d_o`` is given, the backward with
+    """One replayed group member (DeepRead summary, *Method*, the serial replay
+    step): forward O and LSE and, when ``d_o`` is given, the backward with
     the prompt state detached.
 
     ``rows``: response positions to compute (default: all).  O, LSE, D and dQ
@@ -276,8 +279,8 @@ def paged_split_forward(
     """Forward computed the paged way: one partial (O_s, LSE_s) per group of
     ``pages_per_split`` prompt pages, one more for the causal response keys,
     ``empty_splits`` partials with no keys at all (LSE = -inf, O = 0), then
-    the exact LSE merge (review mind map: "全局LSE softmax重组 forward
-    composition").  Returns o [R, Hq, d], lse [R, Hq]."""
+    the exact LSE merge (review mind map: the forward is composed by a global
+    LSE softmax recombination).  Returns o [R, Hq, d], lse [R, Hq]."""
     q = to_f64(q)
     kr_all = to_f64(k_resp)
     vr_all = to_f64(v_resp)

@@ -61,7 +61,7 @@ def _sdpa_full_sequence(c, scale):
     All P+R positions are queries (prompt queries are random), the mask is
     plain causal over the whole sequence, prompt K/V are constants and dO is
     zero on prompt rows: the conventional full-sequence execution the review
-    recommends as the parity target (review 七, "未来研究方向")."""
+    recommends as the parity target (review 七, the node on future research directions)."""
     P = c["prompt_len"]
     R, Hq, d = c["q"].shape
     Hkv = c["k_resp"].shape[1]
