@@ -471,17 +471,19 @@ cudaError_t fwd_variant(const FwdParams& a, cudaStream_t s) {
 // keys 0-63 and 64-127, all 256 columns); the producer loads units in the
 // order the MMA thread consumes them,
 //   K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1},
-// and a chunk slot is reloaded as soon as the unit that held it is done, so
-// about two and a half tiles of K/V are in flight while S_{j+1} and PV_j run.
-// Per tile the MMA thread waits three times (K unit, P_j, V unit) and
-// commits four (S ready, K unit done, V unit done, O updated).
+// and a chunk slot is reloaded as soon as the MMAs that read its previous
+// chunk are done: each half of a unit is released on its own, half a group
+// before the unit ends, which is what lets K_{j+1} and V_j land before S_{j+1}
+// and PV_j need them with only five chunks.  Per tile the MMA thread waits
+// three times (K unit, P_j, V unit) and commits six (S ready, four chunks
+// done, O updated).
 // Softmax: eight warps, two threads per query row, each taking half of the
 // tile's keys and half of O's columns.  Both threads of a row read all 128
 // S columns for the row maximum (so they agree on it without exchanging
 // anything) and meet on an mbarrier before the P stores that overwrite S.
 // ===========================================================================
 struct FwdRingLayout {
-  static constexpr int BN = 128, NC = 5, NU = 4;
+  static constexpr int BN = 128, NC = 5, NU = 4, NCD = 8;
   static constexpr uint32_t kQBytes = kBM * kD * 2;  // 64 KB
   static constexpr uint32_t kQBox = kBM * 128;       // 16 KB
   static constexpr uint32_t kChunk = 32768;
@@ -494,9 +496,10 @@ struct FwdRingLayout {
   static constexpr uint32_t kTmemS = 256;
   static_assert(kTmemS + 2 * BN <= 512, "tensor memory budget");
   static_assert(kSmem <= 227 * 1024 - 512, "shared memory budget");
-  // a chunk of unit u reuses the slot of a chunk of unit u-3 or u-2; the
-  // barrier rings must tell apart phases that far apart
-  static_assert(NU >= 4 && NC == 5, "unit ring");
+  // a unit's full barrier is reused by unit u+NU, which can only load after
+  // unit u+1 is done; a chunk's done barrier is reused by chunk c+NCD, which
+  // can only load after chunk c+NCD-NC is done
+  static_assert(NU >= 3 && NCD > NC, "barrier rings");
 };
 
 // Position of K_j / V_j in the unit sequence of a part with n tiles.
@@ -516,9 +519,9 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
                        const __grid_constant__ CUtensorMap tmKr, const __grid_constant__ CUtensorMap tmVr,
                        const FwdKParams p) {
   using L = FwdRingLayout;
-  constexpr int BN = L::BN, NC = L::NC, NU = L::NU;
+  constexpr int BN = L::BN, NC = L::NC, NU = L::NU, NCD = L::NCD;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_uf[NU], bar_ud[NU], bar_sf[2], bar_pf[2], bar_sr, bar_od, bar_ofin,
+  __shared__ uint64_t bar_q, bar_uf[NU], bar_cd[NCD], bar_sf[2], bar_pf[2], bar_sr, bar_od, bar_ofin,
       bar_drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ uint32_t abort_s;
@@ -550,10 +553,8 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
     abort_s = 0;
     mbar_init(smem_u32(&bar_q), 256);
     mbar_init(smem_u32(&bar_sr), 256);
-    for (int u = 0; u < NU; ++u) {
-      mbar_init(smem_u32(&bar_uf[u]), 1);
-      mbar_init(smem_u32(&bar_ud[u]), 1);
-    }
+    for (int u = 0; u < NU; ++u) mbar_init(smem_u32(&bar_uf[u]), 1);
+    for (int c = 0; c < NCD; ++c) mbar_init(smem_u32(&bar_cd[c]), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bar_sf[b]), 1);
       mbar_init(smem_u32(&bar_pf[b]), 256);
@@ -631,9 +632,9 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
         const uint32_t fb = smem_u32(&bar_uf[u % NU]);
         for (int h = 0; h < 2; ++h) {
           const int c = 2 * u + h;
-          if (c >= NC) {  // the slot's previous chunk belonged to unit (c-NC)/2
-            const int v = (c - NC) / 2;
-            if (!mbar_wait_warp(smem_u32(&bar_ud[v % NU]), (v / NU) & 1, abortp)) {
+          if (c >= NC) {  // the slot's previous chunk, c-NC, must be done
+            const int v = c - NC;
+            if (!mbar_wait_warp(smem_u32(&bar_cd[v % NCD]), (v / NCD) & 1, abortp)) {
               if (lane == 0) fail(__LINE__);
               ok = false;
               break;
@@ -675,9 +676,10 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
           mma_ss(dS, sdesc_sw128(sQ + (kk >> 2) * L::kQBox + (kk & 3) * 32, 16, 1024),
                  sdesc_sw128(kc + ((kk >> 2) & 1) * L::kKBox + (kk & 3) * 32, 16, 1024), idesc_qk,
                  kk > 0 ? 1u : 0u);
+          if (kk == 7) mma_commit(smem_u32(&bar_cd[(2 * u) % NCD]));  // columns 0-127 read
         }
         mma_commit(smem_u32(&bar_sf[j & 1]));
-        mma_commit(smem_u32(&bar_ud[u % NU]));
+        mma_commit(smem_u32(&bar_cd[(2 * u + 1) % NCD]));
         return true;
       };
       bool ok = mbar_wait(smem_u32(&bar_q), 0, abortp);
@@ -702,8 +704,9 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
           mma_ts(tbase, tbase + L::kTmemS + b * BN + kk * 8,
                  sdesc_sw128(vc + (kk & 3) * 16 * 128, L::kVBox, 1024), idesc_pv,
                  (j > 0 || kk > 0) ? 1u : 0u);
+          if (kk == 3) mma_commit(smem_u32(&bar_cd[(2 * u) % NCD]));  // keys 0-63 read
         }
-        mma_commit(smem_u32(&bar_ud[u % NU]));
+        mma_commit(smem_u32(&bar_cd[(2 * u + 1) % NCD]));
         mma_commit(smem_u32(&bar_od));
         if (j == ntiles - 1) mma_commit(smem_u32(&bar_ofin));
       }
