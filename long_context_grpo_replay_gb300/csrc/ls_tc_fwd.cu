@@ -6,12 +6,15 @@
 //   keys  : part s < ns: a contiguous range of logical prompt positions,
 //           streamed page by page through the page table with TMA (a key tile
 //           never crosses a page); part ns: the response keys with the causal
-//           mask, read through a 3-D map over [R][Hkv][256].
+//           mask, read through a 4-D map over [R][Hkv][256].
 // Output: float32 partial O (normalised) and partial LSE (natural log) for
 // the part, merged exactly afterwards by the LSE-merge kernel (the global
 // LSE and output merge of the LongStraw DeepRead summary, section Method).
 //
-// Warp roles (256 threads):
+// Two kernels share that plan.  tc_fwd_ring_kernel (the default, further
+// down) streams K and V through a ring of 32 KB chunks and runs eight softmax
+// warps.  tc_fwd_kernel (selected by LS_TC_FWD_VARIANT) is the staged design
+// it grew from, with these warp roles (256 threads):
 //   warp 0        : TMA producer for K tiles (one instruction per tile)
 //   warp 3        : TMA producer for V tiles
 //   warp 1 lane 0 : MMA issuer: S[b] = Q K^T (SS), O += P V (P from shared or
@@ -22,7 +25,8 @@
 //                   lazy rescaling (the running max only moves when the tile
 //                   max exceeds it by more than 8, so exp2 stays below 256),
 //                   writes P as bf16 and finally normalises O.
-// Tensor memory: O in columns [0,256), S double-buffered at 256 + b*BN.
+// Tensor memory (both kernels): O in columns [0,256), S double-buffered at
+// 256 + b*BN.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math_constants.h>
