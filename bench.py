@@ -12,6 +12,7 @@ alongside.  Default workload: 2,097,152-position prompt in 8192 pages of 256,
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the float64 CPU oracle arm
+    python bench.py --workload prefill_bf16_p256k   # the capture step, ls_prompt_prefill
 
 Under torchrun each rank runs its own replica of the workload (members are
 independent; no data-path collective), the timing is the max over ranks and
@@ -448,6 +449,155 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+PREFILL_WORKLOADS = {"prefill_bf16_p256k": 262144, "prefill_bf16_p2m": 2097152}
+PREFILL_METRIC = "prompt prefill (page write + causal attention) TFLOP/s"
+
+
+def prefill_flops(N, hq, d):
+    return 4.0 * d * hq * N * (N + 1) / 2.0
+
+
+def run_prefill(args):
+    """The capture step, ls_prompt_prefill: page write of the prompt K/V and
+    causal self-attention of the prompt (24/4 heads, d=256, bf16)."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import long_context_grpo_replay_gb300.binding as ls
+    from long_context_grpo_replay_gb300 import build, inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    build.build()
+    ls.lib()
+    N = PREFILL_WORKLOADS[args.workload]
+    w = inputs.Workload(args.workload, 24, 4, 256, 256, N, (N,), "bf16", seed=31 + 1000 * rank)
+    hq, hkv, d = w.hq, w.hkv, w.head_dim
+    desc = ls.desc_for(hq, hkv, d, w.page_size, torch.bfloat16, w.scale)
+    pr = inputs.make_prompt(w, dev)
+    k_pool, v_pool, pt = pr["k_pool"], pr["v_pool"], pr["page_table"]
+    m = inputs.make_member(w, 0, dev, resp_len=N)
+    q, k, v = m["q"], m["k"], m["v"]
+    del m["d_o"]
+    o = torch.empty_like(q)
+    lse = torch.empty(N, hq, device=dev, dtype=torch.float32)
+    ws = torch.empty(ls.ls_prompt_prefill_workspace_size(desc, N), dtype=torch.uint8, device=dev)
+    ls.ls_clear_device_status(ws)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(qq, kk, vv):
+        ls.ls_prompt_prefill(desc, qq, kk, vv, o, lse, k_pool, v_pool, pt, ws, stream)
+
+    for _ in range(args.warmup):
+        step(q, k, v)
+    torch.cuda.synchronize()
+    ls.ls_read_device_status(ws)
+    ls.ls_trace_enable(True)
+    ls.ls_trace_reset()
+    launches0 = ls.ls_launch_count()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step(q, k, v)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    launches = ls.ls_launch_count() - launches0
+    trace = ls.kernel_trace()
+    ls.ls_trace_enable(False)
+    ls.ls_read_device_status(ws)
+    clocks = clk.summary()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev) / args.steps
+    fl = prefill_flops(N, hq, d)
+    value = job_throughput(fl, world, ms)
+
+    pk, pk_src = peaks()
+    dom = "tc_fwd" if "tc_fwd" in trace else "simt_fwd"
+    n_l, t_l = trace.get(dom, (1, ms * args.steps))
+    launch_ms = t_l / max(1, n_l)
+    peak_t = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    achieved = fl / (launch_ms * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
+            "frac": achieved / peak_t, "traffic": None, "kernel": dom,
+            "peak_source": f"{pk_src} (bf16_tflops_sustained)", "algorithmic_per_launch": fl,
+            "launch_ms": launch_ms}
+
+    e2e = None
+    if not args.no_e2e:
+        hq_, hk_, hv_ = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+                         for t in (q, k, v))
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            dq_.copy_(hq_, non_blocking=True)
+            dk_.copy_(hk_, non_blocking=True)
+            dv_.copy_(hv_, non_blocking=True)
+            step(dq_, dk_, dv_)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        n = max(1, min(args.steps, 3))
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(a0.elapsed_time(a1) / n, dev)
+        e2e = {"value": round(job_throughput(fl, world, ems), 3), "unit": "TFLOP/s",
+               "ms_per_step": round(ems, 3), "steps": n,
+               "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_))),
+               "d2h_bytes_per_step": int(ho.numel() * ho.element_size() + hl.numel() * 4)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle.ref as ref
+        gq = hq // hkv
+        qc = q[:, :gq].cpu()
+        t0 = time.perf_counter()
+        dummy = k_pool[:1, :1].cpu()  # no prompt pages: the prompt is the causal part
+        ref.replay_member(dummy, dummy, pt[:1].cpu(), 0, qc, k[:, :1].cpu(), v[:, :1].cpu(),
+                          scale=w.scale, rows=np.array([N - 1]))
+        dt = time.perf_counter() - t0
+        cpu = {"value": 4.0 * d * gq * N / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+               "kind": "oracle",
+               "sample": f"row {N - 1} of the {gq} query heads of KV head 0 over all {N} keys "
+                         f"(float64 numpy; {dt:.2f} s)", "seconds": round(dt, 2)}
+
+    if rank == 0:
+        print(json.dumps({
+            "metric": PREFILL_METRIC, "value": round(value, 3), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1)/sqrt(d) Q/K/V, random page table)",
+            "config": {"workload": args.workload, "prompt_len": N, "hq": hq, "hkv": hkv,
+                       "head_dim": d, "page_size": w.page_size,
+                       "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (Q %.1f GiB)" % (q.numel() * 2 / 2**30)},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clocks,
+            "kernels_ms_per_step": {kk: round(vv[1] / args.steps, 3) for kk, vv in trace.items()},
+        }), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -463,6 +613,8 @@ def main():
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload in PREFILL_WORKLOADS:
+        run_prefill(args)
     else:
         run_ours(args)
 

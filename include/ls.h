@@ -148,7 +148,7 @@ LS_API ls_status ls_replay_workspace_size(const ls_attn_desc* desc, const ls_pro
  * keys plus the causal response keys.  The prompt part runs split over page
  * ranges into float32 partials held in ws, the response part adds one more
  * partial, and an exact LSE merge writes o and lse (DeepRead summary,
- * "Method", Qwen path).  resp_len == 0 is a no-op. */
+ * Method, Qwen path).  resp_len == 0 is a no-op. */
 LS_API ls_status ls_replay_fwd(const ls_attn_desc* desc, const ls_prompt_kv* prompt,
                         const void* q, const void* k_resp, const void* v_resp,
                         int32_t resp_len, void* o, float* lse, void* ws, size_t ws_bytes,
@@ -195,6 +195,31 @@ LS_API ls_status ls_replay_bwd(const ls_attn_desc* desc, const ls_prompt_kv* pro
 LS_API ls_status ls_replay_group(const ls_attn_desc* desc, const ls_prompt_kv* prompt,
                           int32_t n_members, const ls_member* members, void* ws,
                           size_t ws_bytes, void* stream);
+
+/* Prompt prefill with capture (the capture step of the DeepRead summary,
+ * Method: the shared prompt is run once without gradients and its
+ * full-attention K/V are kept as pages; the summary's Key Results put most
+ * of the wall time in this no-gradient prefill).  Two steps on one stream:
+ *   1. page write, as ls_kv_page_write with start_pos 0: token t of k, v
+ *      ([n_tok][Hkv][d]) goes to pool[page_table[t/S_p]][kv][t%S_p][:];
+ *   2. causal self-attention of the prompt: o [n_tok][Hq][d] (element dtype)
+ *      and lse float32 [n_tok][Hq] (natural log, scale included), row t over
+ *      keys 0..t of k, v (read from the contiguous k, v, not the pages).
+ * Step 2 is the replay forward with an empty prompt and the prompt in the
+ * response's place, so it runs on the same kernels.  ws must hold
+ * ls_prompt_prefill_workspace_size() bytes (float32 partials of n_tok rows);
+ * a page-table entry outside the pool is skipped and reported through the
+ * workspace status word.  n_tok == 0 is a no-op.  No counterpart in the pages
+ * beyond the step itself: the interface is this library's. */
+LS_API ls_status ls_prompt_prefill(const ls_attn_desc* desc, const void* q, const void* k,
+                                   const void* v, int32_t n_tok, void* o, float* lse,
+                                   void* k_pool, void* v_pool, int64_t pool_pages,
+                                   const int32_t* page_table, int64_t num_pages, void* ws,
+                                   size_t ws_bytes, void* stream);
+
+/* Workspace bytes ls_prompt_prefill needs for n_tok tokens.  Host-only. */
+LS_API ls_status ls_prompt_prefill_workspace_size(const ls_attn_desc* desc, int32_t n_tok,
+                                                  size_t* bytes);
 
 /* Replay forward (same arguments and results as ls_replay_fwd) for callers
  * that cannot allocate device memory: no workspace argument; the library's

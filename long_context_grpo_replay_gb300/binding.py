@@ -19,7 +19,7 @@ __all__ = [
     "ls_trace_enable", "ls_trace_reset", "ls_trace_read", "ls_num_kernel_ids",
     "ls_kernel_name", "ls_launch_count", "ls_uses_tensor_cores", "kernel_trace",
     "desc_for", "prompt_from", "EXPORTED_SYMBOLS", "ls_replay_fwd_noalloc",
-    "ls_replay_fwd_noalloc_scratch_bytes",
+    "ls_replay_fwd_noalloc_scratch_bytes", "ls_prompt_prefill", "ls_prompt_prefill_workspace_size",
 ]
 
 LS_DTYPE_F32 = 0
@@ -31,7 +31,7 @@ EXPORTED_SYMBOLS = [
     "ls_clear_device_status", "ls_status_string", "ls_last_error", "ls_trace_enable",
     "ls_trace_reset", "ls_trace_read", "ls_num_kernel_ids", "ls_kernel_name",
     "ls_launch_count", "ls_uses_tensor_cores", "ls_replay_fwd_noalloc",
-    "ls_replay_fwd_noalloc_scratch_bytes",
+    "ls_replay_fwd_noalloc_scratch_bytes", "ls_prompt_prefill", "ls_prompt_prefill_workspace_size",
 ]
 
 
@@ -94,6 +94,9 @@ def lib() -> ctypes.CDLL:
                           I32, P, P, P, P, SZ, P],
         "ls_replay_group": [ctypes.POINTER(AttnDesc), ctypes.POINTER(PromptKV), I32,
                             ctypes.POINTER(Member), P, SZ, P],
+        "ls_prompt_prefill": [ctypes.POINTER(AttnDesc), P, P, P, I32, P, P, P, P, I64, P, I64, P,
+                              SZ, P],
+        "ls_prompt_prefill_workspace_size": [ctypes.POINTER(AttnDesc), I32, ctypes.POINTER(SZ)],
         "ls_read_device_status": [P, SZ, P],
         "ls_clear_device_status": [P, SZ, P],
         "ls_trace_enable": [I32],
@@ -207,6 +210,23 @@ def ls_replay_fwd(desc, prompt, q, k_resp, v_resp, o, lse, ws, stream=None):
     _check(lib().ls_replay_fwd(ctypes.byref(desc), ctypes.byref(prompt), _ptr(q), _ptr(k_resp),
                                _ptr(v_resp), q.shape[0], _ptr(o), _ptr(lse), _ptr(ws),
                                _nbytes(ws), _stream(stream)))
+
+
+def ls_prompt_prefill_workspace_size(desc, n_tok) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().ls_prompt_prefill_workspace_size(ctypes.byref(desc), n_tok, ctypes.byref(out)))
+    return out.value
+
+
+def ls_prompt_prefill(desc, q, k, v, o, lse, k_pool, v_pool, page_table, ws, stream=None):
+    """Capture a prompt: write its K/V into the pool pages and compute its
+    causal self-attention o, lse (see ls.h)."""
+    _want_f32(lse)
+    _want_dtype(desc, q, k, v, o, k_pool, v_pool)
+    _check(lib().ls_prompt_prefill(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), q.shape[0],
+                                   _ptr(o), _ptr(lse), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0],
+                                   _ptr(page_table), page_table.shape[0], _ptr(ws), _nbytes(ws),
+                                   _stream(stream)))
 
 
 def ls_replay_fwd_noalloc(desc, prompt, q, k_resp, v_resp, o, lse, stream=None):

@@ -491,6 +491,33 @@ ls_status ls_replay_fwd(const ls_attn_desc* desc, const ls_prompt_kv* prompt, co
                   static_cast<cudaStream_t>(stream));
 }
 
+ls_status ls_prompt_prefill_workspace_size(const ls_attn_desc* desc, int32_t n_tok, size_t* bytes) {
+  LS_CHECK(check_desc(desc));
+  if (!bytes) return fail(LS_ERR_INVALID_ARGUMENT, "bytes is NULL");
+  if (n_tok < 0) return fail(LS_ERR_INVALID_ARGUMENT, "n_tok < 0");
+  // an empty prompt: one part (the causal one) whatever the route
+  *bytes = make_plan(*desc, 0, n_tok, device_sms(), false).ws_bytes;
+  return LS_OK;
+}
+
+ls_status ls_prompt_prefill(const ls_attn_desc* desc, const void* q, const void* k, const void* v,
+                            int32_t n_tok, void* o, float* lse, void* k_pool, void* v_pool,
+                            int64_t pool_pages, const int32_t* page_table, int64_t num_pages,
+                            void* ws, size_t ws_bytes, void* stream) {
+  LS_CHECK(check_desc(desc));
+  if (n_tok < 0) return fail(LS_ERR_INVALID_ARGUMENT, "n_tok < 0");
+  if (n_tok == 0) return LS_OK;
+  size_t need = 0;
+  LS_CHECK(ls_prompt_prefill_workspace_size(desc, n_tok, &need));
+  LS_CHECK(check_ws(ws, ws_bytes, need));
+  LS_CHECK(ls_kv_page_write(desc, k_pool, v_pool, pool_pages, page_table, num_pages, 0, n_tok, k, v,
+                            ws, ws_bytes, stream));
+  ls_prompt_kv empty{};
+  empty.prompt_len = 0;
+  return fwd_impl(desc, &empty, q, k, v, n_tok, o, lse, ws, ws_bytes,
+                  static_cast<cudaStream_t>(stream));
+}
+
 ls_status ls_lse_merge(int32_t n_parts, int64_t n_rows, int32_t head_dim, const float* o_parts,
                        const float* lse_parts, int32_t out_dtype, void* o, float* lse,
                        void* stream) {
