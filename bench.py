@@ -449,7 +449,8 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-PREFILL_WORKLOADS = {"prefill_bf16_p256k": 262144, "prefill_bf16_p2m": 2097152}
+PREFILL_WORKLOADS = {"prefill_bf16_p32k": 32768, "prefill_bf16_p256k": 262144,
+                     "prefill_bf16_p2m": 2097152}
 PREFILL_METRIC = "prompt prefill (page write + causal attention) TFLOP/s"
 
 
