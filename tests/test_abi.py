@@ -154,3 +154,21 @@ def test_product_path_does_not_import_the_oracle():
     for f in list(pkg.rglob("*.cu")) + list(pkg.rglob("*.h")) + list(pkg.rglob("*.cuh")):
         for line in f.read_text().splitlines():
             assert not (line.strip().startswith("#include") and "oracle" in line), (f, line)
+
+
+def test_prefill_workspace_and_argument_checks(ls):
+    """ls_prompt_prefill: host-side sizing and validation (no launch)."""
+    d = _desc(ls)
+    sizes = [ls.ls_prompt_prefill_workspace_size(d, n) for n in (1, 1000, 32768, 262144)]
+    assert sizes == sorted(sizes)
+    # one float32 partial of O and of LSE for n tokens after the 256-byte header
+    n = 32768
+    assert sizes[2] >= 256 + n * 24 * 256 * 4 + n * 24 * 4
+    L = ls.lib()
+    assert L.ls_prompt_prefill(ctypes.byref(d), None, None, None, 0, None, None, None, None, 0, None,
+                               0, None, 0, None) == 0  # n_tok == 0: no-op
+    st = L.ls_prompt_prefill(ctypes.byref(d), None, None, None, 16, None, None, None, None, 1, None,
+                             1, None, 0, None)
+    assert st == 1 and "workspace" in ls.ls_last_error()  # NULL workspace, before any launch
+    out = ctypes.c_size_t(0)
+    assert L.ls_prompt_prefill_workspace_size(ctypes.byref(d), -1, ctypes.byref(out)) == 1
