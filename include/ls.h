@@ -196,6 +196,36 @@ LS_API ls_status ls_replay_group(const ls_attn_desc* desc, const ls_prompt_kv* p
                           int32_t n_members, const ls_member* members, void* ws,
                           size_t ws_bytes, void* stream);
 
+/* Context parallelism, one rank's share (DeepRead summary, Method, Qwen path:
+ * the prompt pages are sharded over ranks and the partial results are merged
+ * globally by LSE; review section 二: the query gradient is what crosses
+ * ranks).  `prompt` holds the pages this rank owns, in any order: attention
+ * over a set of keys does not depend on their order.  Every rank holds the
+ * whole response (q, k_resp, v_resp, d_o).  Exactly one rank passes
+ * with_response != 0 and adds the causal response keys.
+ *
+ * ls_replay_fwd_part writes the rank's exact partial in float32: o_part
+ * [R][Hq][d], normalised over the rank's keys, and lse_part [R][Hq].  A rank
+ * with no visible key gets O = 0 and LSE = -inf.  The global O, LSE is
+ * ls_lse_merge over all ranks' partials (an all-gather, then the merge).
+ *
+ * ls_replay_bwd_part writes dq_part float32 [R][Hq][d], the rank's share of
+ * dQ with the scale applied.  The global dQ is the sum over ranks (an
+ * all-reduce).  lse and delta must be the global ones (from the merged
+ * forward).  dk_resp and dv_resp are written only with_response, and may be
+ * NULL otherwise.  Workspace: ls_replay_workspace_size for the rank's prompt.
+ * The interface is this library's; the pages describe the split, not a call. */
+LS_API ls_status ls_replay_fwd_part(const ls_attn_desc* desc, const ls_prompt_kv* prompt,
+                                    const void* q, const void* k_resp, const void* v_resp,
+                                    int32_t resp_len, int32_t with_response, float* o_part,
+                                    float* lse_part, void* ws, size_t ws_bytes, void* stream);
+LS_API ls_status ls_replay_bwd_part(const ls_attn_desc* desc, const ls_prompt_kv* prompt,
+                                    const void* q, const void* k_resp, const void* v_resp,
+                                    const void* d_o, const float* lse, const float* delta,
+                                    int32_t resp_len, int32_t with_response, float* dq_part,
+                                    void* dk_resp, void* dv_resp, void* ws, size_t ws_bytes,
+                                    void* stream);
+
 /* Prompt prefill with capture (the capture step of the DeepRead summary,
  * Method: the shared prompt is run once without gradients and its
  * full-attention K/V are kept as pages; the summary's Key Results put most

@@ -20,6 +20,7 @@ __all__ = [
     "ls_kernel_name", "ls_launch_count", "ls_uses_tensor_cores", "kernel_trace",
     "desc_for", "prompt_from", "EXPORTED_SYMBOLS", "ls_replay_fwd_noalloc",
     "ls_replay_fwd_noalloc_scratch_bytes", "ls_prompt_prefill", "ls_prompt_prefill_workspace_size",
+    "ls_replay_fwd_part", "ls_replay_bwd_part",
 ]
 
 LS_DTYPE_F32 = 0
@@ -32,6 +33,7 @@ EXPORTED_SYMBOLS = [
     "ls_trace_reset", "ls_trace_read", "ls_num_kernel_ids", "ls_kernel_name",
     "ls_launch_count", "ls_uses_tensor_cores", "ls_replay_fwd_noalloc",
     "ls_replay_fwd_noalloc_scratch_bytes", "ls_prompt_prefill", "ls_prompt_prefill_workspace_size",
+    "ls_replay_fwd_part", "ls_replay_bwd_part",
 ]
 
 
@@ -97,6 +99,10 @@ def lib() -> ctypes.CDLL:
         "ls_prompt_prefill": [ctypes.POINTER(AttnDesc), P, P, P, I32, P, P, P, P, I64, P, I64, P,
                               SZ, P],
         "ls_prompt_prefill_workspace_size": [ctypes.POINTER(AttnDesc), I32, ctypes.POINTER(SZ)],
+        "ls_replay_fwd_part": [ctypes.POINTER(AttnDesc), ctypes.POINTER(PromptKV), P, P, P, I32, I32,
+                               P, P, P, SZ, P],
+        "ls_replay_bwd_part": [ctypes.POINTER(AttnDesc), ctypes.POINTER(PromptKV), P, P, P, P, P, P,
+                               I32, I32, P, P, P, P, SZ, P],
         "ls_read_device_status": [P, SZ, P],
         "ls_clear_device_status": [P, SZ, P],
         "ls_trace_enable": [I32],
@@ -227,6 +233,29 @@ def ls_prompt_prefill(desc, q, k, v, o, lse, k_pool, v_pool, page_table, ws, str
                                    _ptr(o), _ptr(lse), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0],
                                    _ptr(page_table), page_table.shape[0], _ptr(ws), _nbytes(ws),
                                    _stream(stream)))
+
+
+def ls_replay_fwd_part(desc, prompt, q, k_resp, v_resp, with_response, o_part, lse_part, ws,
+                       stream=None):
+    """One rank's exact float32 partial of the replay forward (see ls.h)."""
+    _want_f32(o_part, lse_part)
+    _want_dtype(desc, q, k_resp, v_resp)
+    _check(lib().ls_replay_fwd_part(ctypes.byref(desc), ctypes.byref(prompt), _ptr(q), _ptr(k_resp),
+                                    _ptr(v_resp), q.shape[0], 1 if with_response else 0,
+                                    _ptr(o_part), _ptr(lse_part), _ptr(ws), _nbytes(ws),
+                                    _stream(stream)))
+
+
+def ls_replay_bwd_part(desc, prompt, q, k_resp, v_resp, d_o, lse, delta, with_response, dq_part,
+                       dk=None, dv=None, ws=None, stream=None):
+    """One rank's float32 share of dQ (and the response dK/dV on the rank
+    that holds the response keys; see ls.h)."""
+    _want_f32(lse, delta, dq_part)
+    _want_dtype(desc, q, k_resp, v_resp, d_o, dk, dv)
+    _check(lib().ls_replay_bwd_part(ctypes.byref(desc), ctypes.byref(prompt), _ptr(q), _ptr(k_resp),
+                                    _ptr(v_resp), _ptr(d_o), _ptr(lse), _ptr(delta), q.shape[0],
+                                    1 if with_response else 0, _ptr(dq_part), _ptr(dk), _ptr(dv),
+                                    _ptr(ws), _nbytes(ws), _stream(stream)))
 
 
 def ls_replay_fwd_noalloc(desc, prompt, q, k_resp, v_resp, o, lse, stream=None):

@@ -227,9 +227,13 @@ AttnGeom make_geom(const ls_attn_desc& d, const ls_prompt_kv& p, int32_t R, cons
   return g;
 }
 
+// with_resp == false leaves the response keys out of the merge (the causal
+// partial, the last of the ns+1, is still computed); out_dtype is the dtype
+// o is written in.
 ls_status fwd_impl(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const void* q,
                    const void* k_resp, const void* v_resp, int32_t R, void* o, float* lse,
-                   void* ws, size_t ws_bytes, cudaStream_t s) {
+                   void* ws, size_t ws_bytes, cudaStream_t s, bool with_resp = true,
+                   int out_dtype = -1) {
   LS_CHECK(check_desc(desc));
   LS_CHECK(check_prompt(desc, prompt));
   if (R < 0) return fail(LS_ERR_INVALID_ARGUMENT, "resp_len < 0");
@@ -258,21 +262,25 @@ ls_status fwd_impl(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const v
   } else {
     LS_CUDA(launch_simt_fwd(desc->dtype, fp, s), "forward launch");
   }
-  LS_CUDA(launch_lse_merge(pl.n_parts, (int64_t)R * desc->hq, desc->head_dim, fp.o_parts,
-                           fp.lse_parts, desc->dtype, o, lse, s),
+  LS_CUDA(launch_lse_merge(with_resp ? pl.n_parts : pl.n_parts - 1, (int64_t)R * desc->hq,
+                           desc->head_dim, fp.o_parts, fp.lse_parts,
+                           out_dtype < 0 ? desc->dtype : out_dtype, o, lse, s),
           "LSE merge launch");
   return LS_OK;
 }
 
+// with_resp == false sums dQ over the prompt parts only and skips the
+// response dK/dV (dk, dv may then be NULL); dq_dtype is the dtype dq is
+// written in.
 ls_status bwd_impl(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const void* q,
                    const void* k_resp, const void* v_resp, const void* d_o, const float* lse,
                    const float* delta, int32_t R, void* dq, void* dk, void* dv, void* ws,
-                   size_t ws_bytes, cudaStream_t s) {
+                   size_t ws_bytes, cudaStream_t s, bool with_resp = true, int dq_dtype = -1) {
   LS_CHECK(check_desc(desc));
   LS_CHECK(check_prompt(desc, prompt));
   if (R < 0) return fail(LS_ERR_INVALID_ARGUMENT, "resp_len < 0");
   if (R == 0) return LS_OK;
-  if (!q || !k_resp || !v_resp || !d_o || !lse || !delta || !dq || !dk || !dv)
+  if (!q || !k_resp || !v_resp || !d_o || !lse || !delta || !dq || (with_resp && (!dk || !dv)))
     return fail(LS_ERR_INVALID_ARGUMENT, "backward buffers must be non-NULL");
   if (!aligned(q, 16) || !aligned(k_resp, 16) || !aligned(v_resp, 16) || !aligned(d_o, 16) ||
       !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) ||
@@ -301,9 +309,11 @@ ls_status bwd_impl(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const v
   } else {
     LS_CUDA(launch_simt_bwd_dq(desc->dtype, bp, s), "backward launch");
   }
-  LS_CUDA(launch_dq_reduce(pl.n_parts, (int64_t)R * desc->hq, desc->head_dim,
-                           desc->softmax_scale, bp.dq_parts, desc->dtype, dq, s),
+  LS_CUDA(launch_dq_reduce(with_resp ? pl.n_parts : pl.n_parts - 1, (int64_t)R * desc->hq,
+                           desc->head_dim, desc->softmax_scale, bp.dq_parts,
+                           dq_dtype < 0 ? desc->dtype : dq_dtype, dq, s),
           "dQ reduce launch");
+  if (!with_resp) return LS_OK;
   if (tc) {
     LS_CUDA(launch_tc_dkdv(bp, s), "tensor-core response dK/dV launch");
   } else {
@@ -516,6 +526,24 @@ ls_status ls_prompt_prefill(const ls_attn_desc* desc, const void* q, const void*
   empty.prompt_len = 0;
   return fwd_impl(desc, &empty, q, k, v, n_tok, o, lse, ws, ws_bytes,
                   static_cast<cudaStream_t>(stream));
+}
+
+ls_status ls_replay_fwd_part(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const void* q,
+                             const void* k_resp, const void* v_resp, int32_t resp_len,
+                             int32_t with_response, float* o_part, float* lse_part, void* ws,
+                             size_t ws_bytes, void* stream) {
+  return fwd_impl(desc, prompt, q, k_resp, v_resp, resp_len, o_part, lse_part, ws, ws_bytes,
+                  static_cast<cudaStream_t>(stream), with_response != 0, LS_DTYPE_F32);
+}
+
+ls_status ls_replay_bwd_part(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const void* q,
+                             const void* k_resp, const void* v_resp, const void* d_o,
+                             const float* lse, const float* delta, int32_t resp_len,
+                             int32_t with_response, float* dq_part, void* dk_resp, void* dv_resp,
+                             void* ws, size_t ws_bytes, void* stream) {
+  return bwd_impl(desc, prompt, q, k_resp, v_resp, d_o, lse, delta, resp_len, dq_part, dk_resp,
+                  dv_resp, ws, ws_bytes, static_cast<cudaStream_t>(stream), with_response != 0,
+                  LS_DTYPE_F32);
 }
 
 ls_status ls_lse_merge(int32_t n_parts, int64_t n_rows, int32_t head_dim, const float* o_parts,
