@@ -226,6 +226,15 @@ LS_API ls_status ls_replay_bwd_part(const ls_attn_desc* desc, const ls_prompt_kv
                                     void* dk_resp, void* dv_resp, void* ws, size_t ws_bytes,
                                     void* stream);
 
+/* Sum of float32 partials: out[i] = sum_s parts[s][i] (float32
+ * accumulation, in part order), written in out_dtype.  parts float32
+ * [n_parts][n_elems], 16-byte aligned; n_elems % 4 == 0; n_parts == 0 writes
+ * zeros.  The dQ reduction of A6 as a call of its own, for callers that hold
+ * several dQ shares (context-parallel ranks without a collective, or prompt
+ * pages streamed from host memory in chunks). */
+LS_API ls_status ls_sum_parts(int32_t n_parts, int64_t n_elems, const float* parts,
+                              int32_t out_dtype, void* out, void* stream);
+
 /* Prompt prefill with capture (the capture step of the DeepRead summary,
  * Method: the shared prompt is run once without gradients and its
  * full-attention K/V are kept as pages; the summary's Key Results put most

@@ -20,7 +20,7 @@ __all__ = [
     "ls_kernel_name", "ls_launch_count", "ls_uses_tensor_cores", "kernel_trace",
     "desc_for", "prompt_from", "EXPORTED_SYMBOLS", "ls_replay_fwd_noalloc",
     "ls_replay_fwd_noalloc_scratch_bytes", "ls_prompt_prefill", "ls_prompt_prefill_workspace_size",
-    "ls_replay_fwd_part", "ls_replay_bwd_part",
+    "ls_replay_fwd_part", "ls_replay_bwd_part", "ls_sum_parts",
 ]
 
 LS_DTYPE_F32 = 0
@@ -33,7 +33,7 @@ EXPORTED_SYMBOLS = [
     "ls_trace_reset", "ls_trace_read", "ls_num_kernel_ids", "ls_kernel_name",
     "ls_launch_count", "ls_uses_tensor_cores", "ls_replay_fwd_noalloc",
     "ls_replay_fwd_noalloc_scratch_bytes", "ls_prompt_prefill", "ls_prompt_prefill_workspace_size",
-    "ls_replay_fwd_part", "ls_replay_bwd_part",
+    "ls_replay_fwd_part", "ls_replay_bwd_part", "ls_sum_parts",
 ]
 
 
@@ -99,6 +99,7 @@ def lib() -> ctypes.CDLL:
         "ls_prompt_prefill": [ctypes.POINTER(AttnDesc), P, P, P, I32, P, P, P, P, I64, P, I64, P,
                               SZ, P],
         "ls_prompt_prefill_workspace_size": [ctypes.POINTER(AttnDesc), I32, ctypes.POINTER(SZ)],
+        "ls_sum_parts": [I32, I64, P, I32, P, P],
         "ls_replay_fwd_part": [ctypes.POINTER(AttnDesc), ctypes.POINTER(PromptKV), P, P, P, I32, I32,
                                P, P, P, SZ, P],
         "ls_replay_bwd_part": [ctypes.POINTER(AttnDesc), ctypes.POINTER(PromptKV), P, P, P, P, P, P,
@@ -256,6 +257,14 @@ def ls_replay_bwd_part(desc, prompt, q, k_resp, v_resp, d_o, lse, delta, with_re
                                     _ptr(v_resp), _ptr(d_o), _ptr(lse), _ptr(delta), q.shape[0],
                                     1 if with_response else 0, _ptr(dq_part), _ptr(dk), _ptr(dv),
                                     _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def ls_sum_parts(parts, out, stream=None):
+    """out = parts.sum(0) in float32 accumulation (parts float32 [n, ...])."""
+    _want_f32(parts)
+    n = parts.shape[0]
+    _check(lib().ls_sum_parts(n, out.numel(), _ptr(parts), _dtype_code(out.dtype), _ptr(out),
+                              _stream(stream)))
 
 
 def ls_replay_fwd_noalloc(desc, prompt, q, k_resp, v_resp, o, lse, stream=None):

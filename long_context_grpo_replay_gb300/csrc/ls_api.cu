@@ -546,6 +546,24 @@ ls_status ls_replay_bwd_part(const ls_attn_desc* desc, const ls_prompt_kv* promp
                   LS_DTYPE_F32);
 }
 
+ls_status ls_sum_parts(int32_t n_parts, int64_t n_elems, const float* parts, int32_t out_dtype,
+                       void* out, void* stream) {
+  if (n_parts < 0 || n_elems < 0 || n_elems % 4 != 0)
+    return fail(LS_ERR_INVALID_ARGUMENT, "need n_parts >= 0 and n_elems a multiple of 4");
+  if (out_dtype != LS_DTYPE_F32 && out_dtype != LS_DTYPE_BF16)
+    return fail(LS_ERR_INVALID_ARGUMENT, "bad out_dtype");
+  if (n_elems == 0) return LS_OK;
+  if ((n_parts > 0 && !parts) || !out)
+    return fail(LS_ERR_INVALID_ARGUMENT, "parts and out must be non-NULL");
+  if (!aligned(parts, 16) || !aligned(out, out_dtype == LS_DTYPE_F32 ? 4 : 2))
+    return fail(LS_ERR_INVALID_ARGUMENT, "parts must be 16-byte aligned");
+  // the dQ partial-sum kernel over rows of 4 elements, scale 1
+  LS_CUDA(launch_dq_reduce(n_parts, n_elems / 4, 4, 1.0f, parts, out_dtype, out,
+                           static_cast<cudaStream_t>(stream)),
+          "partial sum launch");
+  return LS_OK;
+}
+
 ls_status ls_lse_merge(int32_t n_parts, int64_t n_rows, int32_t head_dim, const float* o_parts,
                        const float* lse_parts, int32_t out_dtype, void* o, float* lse,
                        void* stream) {

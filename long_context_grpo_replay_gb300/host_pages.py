@@ -1,0 +1,132 @@
+"""Prompt pages resident in host memory, streamed to the GPU in chunks.
+
+The GLM path of the LongStraw DeepRead summary (section Method) keeps its
+prompt state in CPU memory and stages it per layer.  Here that idea is
+applied to the KV pages of the full-attention replay.  Pages live in pinned
+host memory (on GB300 the Grace memory, reached over NVLink-C2C).  For each
+pass the prompt is cut into chunks of whole logical pages.  Each chunk is
+copied into one of two device staging pools on a copy stream while the
+previous chunk computes.
+
+Every chunk is an exact share of the keys, so the result is exact:
+
+  forward  : ls_replay_fwd_part per chunk (the first chunk adds the causal
+             response keys), then ls_lse_merge of the chunk partials;
+  backward : ls_replay_bwd_part per chunk with the global LSE and D, then
+             ls_sum_parts of the dQ shares; the response dK/dV come from the
+             first chunk.
+
+Device memory holds two chunks of pages plus one float32 partial per chunk,
+however long the prompt.  The page copies are plain transfers and every
+arithmetic step runs in the library.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as ls
+
+
+class HostPagedReplay:
+    """Replay over a prompt whose pages are in pinned host memory.
+
+    k_pool_host, v_pool_host: pinned [pool_pages, Hkv, page_size, d] tensors;
+    page_table: int32 [num_pages] (host), logical page -> pool slot;
+    chunk_pages: pages per staged chunk."""
+
+    def __init__(self, desc, k_pool_host, v_pool_host, page_table, prompt_len, chunk_pages, device):
+        if not (k_pool_host.is_pinned() and v_pool_host.is_pinned()):
+            raise ValueError("host pools must be pinned")
+        if chunk_pages < 1:
+            raise ValueError("chunk_pages must be >= 1")
+        self.desc = desc
+        self.kh, self.vh = k_pool_host, v_pool_host
+        self.pt = page_table.cpu().to(torch.int64)
+        self.P = int(prompt_len)
+        self.page = k_pool_host.shape[2]
+        n_pages = -(-self.P // self.page)
+        if self.pt.shape[0] < n_pages:
+            raise ValueError("page table shorter than the prompt")
+        if n_pages and (int(self.pt[:n_pages].min()) < 0 or int(self.pt[:n_pages].max()) >= k_pool_host.shape[0]):
+            raise ValueError("page table entry outside the host pool")
+        self.chunks = [(c, min(c + chunk_pages, n_pages)) for c in range(0, n_pages, chunk_pages)]
+        shape = (chunk_pages,) + tuple(k_pool_host.shape[1:])
+        self.kst = [torch.empty(shape, dtype=k_pool_host.dtype, device=device) for _ in range(2)]
+        self.vst = [torch.empty(shape, dtype=v_pool_host.dtype, device=device) for _ in range(2)]
+        self.local_pt = torch.arange(chunk_pages, dtype=torch.int32, device=device)
+        self.copy_stream = torch.cuda.Stream(device)
+        self.device = device
+
+    def n_chunks(self) -> int:
+        return max(1, len(self.chunks))
+
+    def _prompt(self, b, c0, c1):
+        n_tok = min(self.P, c1 * self.page) - c0 * self.page
+        return ls.prompt_from(self.kst[b], self.vst[b], self.local_pt[: c1 - c0], n_tok)
+
+    def workspace_bytes(self, max_resp_len) -> int:
+        """Bytes of the one workspace every chunk's calls share."""
+        if not self.chunks:
+            return ls.ls_replay_workspace_size(self.desc, ls.prompt_from(None, None, None, 0),
+                                               max_resp_len)
+        return max(ls.ls_replay_workspace_size(self.desc, self._prompt(0, c0, c1), max_resp_len)
+                   for c0, c1 in {self.chunks[0], self.chunks[-1]})
+
+    def _stream_chunks(self, run_chunk):
+        """Stage every chunk (double-buffered) and call run_chunk(i, prompt)."""
+        stream = torch.cuda.current_stream(self.device)
+        if not self.chunks:
+            run_chunk(0, ls.prompt_from(None, None, None, 0))
+            return
+        copied = [torch.cuda.Event(), torch.cuda.Event()]
+        free = [torch.cuda.Event(), torch.cuda.Event()]
+        for e in free:
+            e.record(stream)
+
+        def stage(i):
+            b = i & 1
+            c0, c1 = self.chunks[i]
+            self.copy_stream.wait_event(free[b])
+            with torch.cuda.stream(self.copy_stream):
+                for j, p in enumerate(range(c0, c1)):
+                    slot = int(self.pt[p])
+                    self.kst[b][j].copy_(self.kh[slot], non_blocking=True)
+                    self.vst[b][j].copy_(self.vh[slot], non_blocking=True)
+            copied[b].record(self.copy_stream)
+
+        stage(0)
+        for i, (c0, c1) in enumerate(self.chunks):
+            b = i & 1
+            if i + 1 < len(self.chunks):
+                stage(i + 1)
+            stream.wait_event(copied[b])
+            run_chunk(i, self._prompt(b, c0, c1))
+            free[b].record(stream)
+
+    def forward(self, q, k, v, o, lse, ws):
+        R, hq, d = q.shape
+        n = self.n_chunks()
+        parts_o = torch.empty((n, R, hq, d), dtype=torch.float32, device=q.device)
+        parts_l = torch.empty((n, R, hq), dtype=torch.float32, device=q.device)
+
+        def run(i, prompt):
+            ls.ls_replay_fwd_part(self.desc, prompt, q, k, v, i == 0, parts_o[i], parts_l[i], ws)
+
+        self._stream_chunks(run)
+        ls.ls_lse_merge(parts_o.view(n, R * hq, d), parts_l.view(n, R * hq), o, lse)
+
+    def backward(self, q, k, v, d_o, o, lse, dq, dk, dv, ws):
+        """dq in its own dtype (the sum of the chunk shares)."""
+        R, hq, d = q.shape
+        n = self.n_chunks()
+        delta = torch.empty((R, hq), dtype=torch.float32, device=q.device)
+        ls.ls_replay_bwd_preprocess(self.desc, o, d_o, delta)
+        dq_parts = torch.empty((n, R, hq, d), dtype=torch.float32, device=q.device)
+
+        def run(i, prompt):
+            first = i == 0
+            ls.ls_replay_bwd_part(self.desc, prompt, q, k, v, d_o, lse, delta, first, dq_parts[i],
+                                  dk if first else None, dv if first else None, ws)
+
+        self._stream_chunks(run)
+        ls.ls_sum_parts(dq_parts, dq)
