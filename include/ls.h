@@ -30,7 +30,9 @@
  *  Element dtype is uniform per call (LS_DTYPE_F32 or LS_DTYPE_BF16);
  *  accumulation is always float32.
  *
- *  Ownership: the caller allocates every buffer.  The library never allocates
+ *  Ownership: the caller allocates every buffer and keeps each one alive
+ *  until the work that reads it has finished on its stream; the structs
+ *  (ls_prompt_kv, ls_member) only hold pointers.  The library never allocates
  *  or frees device memory.  It keeps a small host-side cache (tensor-map
  *  descriptors) and per-process trace counters, nothing else.  The prompt
  *  pools are read-only for every replay call.
