@@ -1,0 +1,124 @@
+"""Pins of the gated-DeltaNet replay oracle (oracle/gdn.py) against facts that
+do not come from the oracle itself: closed forms of the gated delta rule,
+central finite differences, an explicit-matrix brute force, and planted
+mistakes that one of these must reject."""
+import numpy as np
+import pytest
+import torch
+
+from oracle.gdn import gdn_replay
+
+
+def _case(H=2, dk=5, dv=4, R=7, seed=0, g0=None, b0=None, unit_k=True):
+    rng = np.random.default_rng(seed)
+    s0 = rng.standard_normal((H, dv, dk))
+    q = rng.standard_normal((R, H, dk))
+    k = rng.standard_normal((R, H, dk))
+    if unit_k:
+        k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((R, H, dv))
+    g = np.log(rng.uniform(0.7, 1.0, (R, H))) if g0 is None else np.full((R, H), g0)
+    b = rng.uniform(0.1, 0.9, (R, H)) if b0 is None else np.full((R, H), b0)
+    d_o = rng.standard_normal((R, H, dv))
+    return s0, q, k, v, g, b, d_o
+
+
+def test_no_decay_no_write_keeps_the_captured_state():
+    """g = 0, b = 0: S_t = S_0, so o_t = S_0 q_t, dq_t = S_0^T dO_t, dk = dv = 0,
+    dg_t = sum_{s>=t} dO_s^T S_0 q_s, db_t = (v_t - S_0 k_t)^T G_t k_t with
+    G_t = sum_{s>=t} dO_s q_s^T."""
+    s0, q, k, v, g, b, d_o = _case(g0=0.0, b0=0.0)
+    r = gdn_replay(s0, q, k, v, g, b, d_o)
+    R, H = g.shape
+    for h in range(H):
+        S = s0[h]
+        np.testing.assert_allclose(r["o"][:, h], q[:, h] @ S.T, atol=1e-12)
+        np.testing.assert_allclose(r["dq"][:, h], d_o[:, h] @ S, atol=1e-12)
+        for t in range(R):
+            G = sum(np.outer(d_o[s, h], q[s, h]) for s in range(t, R))
+            np.testing.assert_allclose(r["dg"][t, h], np.sum(G * S), atol=1e-10)
+            w = v[t, h] - S @ k[t, h]
+            np.testing.assert_allclose(r["dbeta"][t, h], w @ G @ k[t, h], atol=1e-10)
+    assert np.abs(r["dk"]).max() < 1e-12 and np.abs(r["dv"]).max() < 1e-12
+    np.testing.assert_allclose(r["s_final"], s0, atol=1e-12)
+
+
+def test_full_write_stores_the_value_under_its_key():
+    """b = 1 and |k_t| = 1: S_t k_t = a S_{t-1} (k_t - k_t) + v_t = v_t, whatever
+    the decay; with q_t = k_t the output is v_t."""
+    s0, q, k, v, g, b, d_o = _case(b0=1.0)
+    r = gdn_replay(s0, k, k, v, g, b)
+    np.testing.assert_allclose(r["o"], v, atol=1e-12)
+    H = g.shape[1]
+    for h in range(H):
+        np.testing.assert_allclose(r["s_final"][h] @ k[-1, h], v[-1, h], atol=1e-12)
+
+
+def _brute(s0, q, k, v, g, b):
+    R, H, dk = q.shape
+    o = np.zeros((R, H, v.shape[2]))
+    fin = np.zeros_like(s0)
+    for h in range(H):
+        S = s0[h].copy()
+        for t in range(R):
+            kt = k[t, h][:, None]
+            S = np.exp(g[t, h]) * S @ (np.eye(dk) - b[t, h] * kt @ kt.T) + b[t, h] * v[t, h][:, None] @ kt.T
+            o[t, h] = S @ q[t, h]
+        fin[h] = S
+    return o, fin
+
+
+def test_explicit_matrix_brute_force():
+    s0, q, k, v, g, b, _ = _case(H=3, dk=6, dv=3, R=9, seed=3, unit_k=False)
+    r = gdn_replay(s0, q, k, v, g, b)
+    o, fin = _brute(s0, q, k, v, g, b)
+    np.testing.assert_allclose(r["o"], o, atol=1e-12)
+    np.testing.assert_allclose(r["s_final"], fin, atol=1e-12)
+
+
+@pytest.mark.parametrize("name", ["q", "k", "v", "g", "beta"])
+def test_finite_differences(name):
+    s0, q, k, v, g, b, d_o = _case(H=2, dk=3, dv=4, R=5, seed=7, unit_k=False)
+    args = {"q": q, "k": k, "v": v, "g": g, "beta": b}
+    r = gdn_replay(s0, q, k, v, g, b, d_o)
+    grad = r["d" + name]
+    eps = 1e-6
+    x = args[name]
+    num = np.zeros_like(x)
+    it = np.nditer(x, flags=["multi_index"])
+    for _ in it:
+        i = it.multi_index
+        for sgn in (1, -1):
+            xx = x.copy()
+            xx[i] += sgn * eps
+            a2 = dict(args, **{name: xx})
+            o = gdn_replay(s0, a2["q"], a2["k"], a2["v"], a2["g"], a2["beta"])["o"]
+            num[i] += sgn * np.sum(o * d_o) / (2 * eps)
+    np.testing.assert_allclose(grad, num, rtol=1e-6, atol=1e-7)
+
+
+def test_planted_mistakes_are_caught():
+    """A write scaled by the decay, or a missing decay, breaks one of the pins."""
+    s0, q, k, v, g, b, _ = _case(b0=1.0, seed=11)
+
+    def scaled_write(s0, q, k, v, g, b):  # a_t * b_t v_t k_t^T instead of b_t v_t k_t^T
+        R, H, dk = q.shape
+        o = np.zeros((R, H, v.shape[2]))
+        for h in range(H):
+            S = s0[h].copy()
+            for t in range(R):
+                a = np.exp(g[t, h])
+                S = a * (S - b[t, h] * np.outer(S @ k[t, h], k[t, h]) + b[t, h] * np.outer(v[t, h], k[t, h]))
+                o[t, h] = S @ q[t, h]
+        return o
+
+    assert np.abs(scaled_write(s0, k, k, v, g, b) - v).max() > 1e-3  # fails the full-write pin
+    o_nodecay, _ = _brute(s0, q, k, v, np.zeros_like(g), b)
+    assert np.abs(o_nodecay - gdn_replay(s0, q, k, v, g, b)["o"]).max() > 1e-3
+
+
+def test_empty_response():
+    s0, q, k, v, g, b, d_o = _case(R=0)
+    r = gdn_replay(s0, q, k, v, g, b, d_o)
+    assert r["o"].shape == (0, 2, 4)
+    np.testing.assert_allclose(r["s_final"], s0)
