@@ -624,6 +624,148 @@ def run_prefill(args):
         dist.destroy_process_group()
 
 
+GDN_WORKLOADS = {"gdn_f32_h32_r4096_g8": (8, 32, 4096)}
+GDN_METRIC = "GDN state replay (forward+backward) response tokens/s per layer"
+# fp32 FMA lanes: 152 SMs x 128 lanes x 2 flop x 2.07 GHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+GDN_FWD_FLOP_PER_TOKEN_HEAD = 7   # x dk*dv: S k, the state update, S q
+GDN_BWD_FLOP_PER_TOKEN_HEAD = 20  # x dk*dv: S_t, G, G k, S_t^T dO, <G,S>, dk's two products, G decay
+
+
+def run_gdn(args):
+    """Gated-DeltaNet replay of one layer for a group: ls_gdn_replay_fwd (with
+    the final state) and ls_gdn_replay_bwd, float32, dk = dv = 128."""
+    import torch
+    import torch.distributed as dist
+
+    import long_context_grpo_replay_gb300.binding as ls
+    from long_context_grpo_replay_gb300 import build, inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    build.build()
+    ls.lib()
+    B, H, R = GDN_WORKLOADS[args.workload]
+    D = 128
+    c = inputs.make_gdn_group(B, H, R, seed=55 + 1000 * rank, device=dev)
+    o = torch.empty_like(c["v"])
+    s_final = torch.empty((B, H, D, D), device=dev, dtype=torch.float32)
+    gr = {n: torch.empty_like(c[x]) for n, x in
+          (("dq", "q"), ("dk", "k"), ("dv", "v"), ("dg", "g"), ("dbeta", "beta"))}
+    ws = torch.empty(ls.ls_gdn_workspace_size(ls.GdnDesc(B, H, D, D), R), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(x):
+        ls.ls_gdn_replay_fwd(x["s0"], x["q"], x["k"], x["v"], x["g"], x["beta"], o, s_final, stream)
+        ls.ls_gdn_replay_bwd(x["s0"], x["q"], x["k"], x["v"], x["g"], x["beta"], x["d_o"],
+                             gr["dq"], gr["dk"], gr["dv"], gr["dg"], gr["dbeta"], ws, stream)
+
+    for _ in range(args.warmup):
+        step(c)
+    torch.cuda.synchronize()
+    ls.ls_trace_enable(True)
+    ls.ls_trace_reset()
+    launches0 = ls.ls_launch_count()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step(c)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    launches = ls.ls_launch_count() - launches0
+    trace = ls.kernel_trace()
+    ls.ls_trace_enable(False)
+    clocks = clk.summary()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev) / args.steps
+    tokens = B * R
+    value = tokens * world / (ms * 1e-3)
+    unit_flop = D * D * B * R * H
+    n_l, t_l = trace.get("gdn_bwd", (1, ms * args.steps))
+    launch_ms = t_l / max(1, n_l)
+    fl_bwd = GDN_BWD_FLOP_PER_TOKEN_HEAD * unit_flop
+    achieved = fl_bwd / (launch_ms * 1e-3) / 1e12
+    roof = {"bound": "alu", "achieved": achieved, "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
+            "frac": achieved / FP32_ALU_TFLOPS, "traffic": None, "kernel": "gdn_bwd",
+            "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz",
+            "algorithmic_per_launch": fl_bwd, "launch_ms": launch_ms}
+
+    e2e = None
+    if not args.no_e2e:
+        names_in = ("s0", "q", "k", "v", "g", "beta", "d_o")
+        host = {x: torch.empty(c[x].shape, dtype=torch.float32, pin_memory=True).copy_(c[x])
+                for x in names_in}
+        dbuf = {x: torch.empty_like(c[x]) for x in names_in}
+        outs = [o, s_final] + list(gr.values())
+        hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+
+        def e2e_step():
+            for x in names_in:
+                dbuf[x].copy_(host[x], non_blocking=True)
+            step(dbuf)
+            for h_, d_ in zip(hout, outs):
+                h_.copy_(d_, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        n = max(1, args.steps)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(a0.elapsed_time(a1) / n, dev)
+        e2e = {"value": round(tokens * world / (ems * 1e-3), 1), "unit": "tokens/s",
+               "ms_per_step": round(ems, 3), "steps": n,
+               "h2d_bytes_per_step": int(sum(t.numel() * 4 for t in host.values())),
+               "d2h_bytes_per_step": int(sum(t.numel() * 4 for t in hout))}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle.gdn import gdn_replay
+        n_tok = min(R, 1024)
+        a = {x: c[x].cpu() for x in ("s0", "q", "k", "v", "g", "beta", "d_o")}
+        t0 = time.perf_counter()
+        gdn_replay(a["s0"][:1], a["q"][0, :n_tok, :1], a["k"][0, :n_tok, :1], a["v"][0, :n_tok, :1],
+                   a["g"][0, :n_tok, :1], a["beta"][0, :n_tok, :1], a["d_o"][0, :n_tok, :1])
+        dt = time.perf_counter() - t0
+        cpu = {"value": n_tok / H / dt, "unit": "tokens/s", "cores": torch.get_num_threads(),
+               "kind": "oracle",
+               "sample": f"member 0, head 0 of {H}, first {n_tok} tokens, forward+backward "
+                         f"(float64 torch, autograd; {dt:.2f} s), scaled to all heads",
+               "seconds": round(dt, 2)}
+
+    if rank == 0:
+        print(json.dumps({
+            "metric": GDN_METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded unit-norm q/k, N(0,1) v, decay in [0.85,1), beta in [0.05,0.95))",
+            "config": {"workload": args.workload, "group": B, "heads": H, "resp_len": R, "dk": D,
+                       "dv": D, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (%.1f GiB of q/k/v/dO)"
+                             % (4 * c["q"].numel() * 4 / 2**30)},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clocks,
+            "kernels_ms_per_step": {kk: round(vv[1] / args.steps, 3) for kk, vv in trace.items()},
+        }), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -644,6 +786,8 @@ def main():
         run_reference(args)
     elif args.workload in PREFILL_WORKLOADS:
         run_prefill(args)
+    elif args.workload in GDN_WORKLOADS:
+        run_gdn(args)
     else:
         run_ours(args)
 

@@ -237,6 +237,46 @@ LS_API ls_status ls_replay_bwd_part(const ls_attn_desc* desc, const ls_prompt_kv
 LS_API ls_status ls_sum_parts(int32_t n_parts, int64_t n_elems, const float* parts,
                               int32_t out_dtype, void* out, void* stream);
 
+/* Gated-DeltaNet state replay (the Qwen model's recurrent layers keep a
+ * fixed-size state for the prompt and replay each response from it with that
+ * state detached: DeepRead summary, Method, Qwen path; review sections 二,
+ * 三).  The pages name the layer but not its recurrence.  This library takes
+ * the published gated delta rule, per member and head, with S [dv][dk] and
+ * S_0 the captured state:
+ *   a_t = exp(g_t);  S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T;
+ *   o_t = S_t q_t.
+ * A call replays `batch` members of one group, all of resp_len tokens, from
+ * one shared S_0.  float32 throughout, row-major, device memory:
+ *   s0 [H][dv][dk] (shared);  s_final [B][H][dv][dk];
+ *   q, k [B][R][H][dk];  v, o [B][R][H][dv];  g, beta [B][R][H].
+ * Supported: dk = dv = 128.  s0 and the token buffers are read only.
+ * ls_gdn_replay_fwd writes o and, if s_final is non-NULL, the state after the
+ * last token.  ls_gdn_replay_bwd returns the gradient of sum(d_o * o) for q,
+ * k, v, g and beta (same shapes); none is formed for s0 (the detached prompt
+ * state).  It needs ls_gdn_workspace_size() bytes of workspace (16-byte
+ * aligned, owned by the caller) for its checkpoints of S.  resp_len == 0 or
+ * batch == 0 is a no-op (the forward still copies s0 to s_final when R = 0).
+ * Errors: LS_ERR_UNSUPPORTED for other dk/dv, LS_ERR_INVALID_ARGUMENT for
+ * NULL buffers or negative sizes, LS_ERR_WORKSPACE_TOO_SMALL; all before any
+ * launch. */
+typedef struct {
+  int32_t batch;
+  int32_t heads;
+  int32_t dk;
+  int32_t dv;
+} ls_gdn_desc;
+
+LS_API ls_status ls_gdn_workspace_size(const ls_gdn_desc* desc, int32_t resp_len, size_t* bytes);
+LS_API ls_status ls_gdn_replay_fwd(const ls_gdn_desc* desc, const float* s0, const float* q,
+                                   const float* k, const float* v, const float* g,
+                                   const float* beta, int32_t resp_len, float* o, float* s_final,
+                                   void* stream);
+LS_API ls_status ls_gdn_replay_bwd(const ls_gdn_desc* desc, const float* s0, const float* q,
+                                   const float* k, const float* v, const float* g,
+                                   const float* beta, const float* d_o, int32_t resp_len,
+                                   float* dq, float* dk, float* dv, float* dg, float* dbeta,
+                                   void* ws, size_t ws_bytes, void* stream);
+
 /* Prompt prefill with capture (the capture step of the DeepRead summary,
  * Method: the shared prompt is run once without gradients and its
  * full-attention K/V are kept as pages; the summary's Key Results put most

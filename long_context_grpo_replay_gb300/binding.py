@@ -21,6 +21,7 @@ __all__ = [
     "desc_for", "prompt_from", "EXPORTED_SYMBOLS", "ls_replay_fwd_noalloc",
     "ls_replay_fwd_noalloc_scratch_bytes", "ls_prompt_prefill", "ls_prompt_prefill_workspace_size",
     "ls_replay_fwd_part", "ls_replay_bwd_part", "ls_sum_parts",
+    "GdnDesc", "ls_gdn_workspace_size", "ls_gdn_replay_fwd", "ls_gdn_replay_bwd",
 ]
 
 LS_DTYPE_F32 = 0
@@ -34,6 +35,7 @@ EXPORTED_SYMBOLS = [
     "ls_launch_count", "ls_uses_tensor_cores", "ls_replay_fwd_noalloc",
     "ls_replay_fwd_noalloc_scratch_bytes", "ls_prompt_prefill", "ls_prompt_prefill_workspace_size",
     "ls_replay_fwd_part", "ls_replay_bwd_part", "ls_sum_parts",
+    "ls_gdn_workspace_size", "ls_gdn_replay_fwd", "ls_gdn_replay_bwd",
 ]
 
 
@@ -62,6 +64,11 @@ class Member(ctypes.Structure):
                 ("reserved", ctypes.c_int32), ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
                 ("delta", ctypes.c_void_p), ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p),
                 ("dv", ctypes.c_void_p)]
+
+
+class GdnDesc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("heads", ctypes.c_int32), ("dk", ctypes.c_int32),
+                ("dv", ctypes.c_int32)]
 
 
 def library_path() -> Path:
@@ -104,6 +111,10 @@ def lib() -> ctypes.CDLL:
                                P, P, P, SZ, P],
         "ls_replay_bwd_part": [ctypes.POINTER(AttnDesc), ctypes.POINTER(PromptKV), P, P, P, P, P, P,
                                I32, I32, P, P, P, P, SZ, P],
+        "ls_gdn_workspace_size": [ctypes.POINTER(GdnDesc), I32, ctypes.POINTER(SZ)],
+        "ls_gdn_replay_fwd": [ctypes.POINTER(GdnDesc), P, P, P, P, P, P, I32, P, P, P],
+        "ls_gdn_replay_bwd": [ctypes.POINTER(GdnDesc), P, P, P, P, P, P, P, I32, P, P, P, P, P, P,
+                              SZ, P],
         "ls_read_device_status": [P, SZ, P],
         "ls_clear_device_status": [P, SZ, P],
         "ls_trace_enable": [I32],
@@ -202,7 +213,7 @@ def _want_f32(*ts):
     import torch
     for t in ts:
         if t is not None and t.dtype != torch.float32:
-            raise TypeError(f"lse/delta/partials must be float32 tensors, got {t.dtype}")
+            raise TypeError(f"expected a float32 tensor, got {t.dtype}")
 
 
 def _want_dtype(desc, *ts):
@@ -265,6 +276,40 @@ def ls_sum_parts(parts, out, stream=None):
     n = parts.shape[0]
     _check(lib().ls_sum_parts(n, out.numel(), _ptr(parts), _dtype_code(out.dtype), _ptr(out),
                               _stream(stream)))
+
+
+def _gdn_desc(s0, q):
+    """q [B, R, H, dk] (a group) or [R, H, dk] (one member)."""
+    return GdnDesc(q.shape[0] if q.dim() == 4 else 1, s0.shape[0], s0.shape[2], s0.shape[1])
+
+
+def _resp_len(q):
+    return q.shape[1] if q.dim() == 4 else q.shape[0]
+
+
+def ls_gdn_workspace_size(desc, resp_len) -> int:
+    """desc: GdnDesc(batch, heads, dk, dv)."""
+    out = ctypes.c_size_t(0)
+    _check(lib().ls_gdn_workspace_size(ctypes.byref(desc), resp_len, ctypes.byref(out)))
+    return out.value
+
+
+def ls_gdn_replay_fwd(s0, q, k, v, g, beta, o, s_final=None, stream=None):
+    """Gated-DeltaNet replay from the captured state s0 [H, dv, dk] of one
+    member (q [R, H, dk]) or a group (q [B, R, H, dk]); see ls.h.  float32."""
+    _want_f32(s0, q, k, v, g, beta, o, s_final)
+    _check(lib().ls_gdn_replay_fwd(ctypes.byref(_gdn_desc(s0, q)), _ptr(s0), _ptr(q), _ptr(k),
+                                   _ptr(v), _ptr(g), _ptr(beta), _resp_len(q), _ptr(o), _ptr(s_final),
+                                   _stream(stream)))
+
+
+def ls_gdn_replay_bwd(s0, q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta, ws, stream=None):
+    """Gradients of the replay for q, k, v, g, beta (none for s0; see ls.h)."""
+    _want_f32(s0, q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta)
+    _check(lib().ls_gdn_replay_bwd(ctypes.byref(_gdn_desc(s0, q)), _ptr(s0), _ptr(q), _ptr(k),
+                                   _ptr(v), _ptr(g), _ptr(beta), _ptr(d_o), _resp_len(q), _ptr(dq), _ptr(dk),
+                                   _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(ws), _nbytes(ws),
+                                   _stream(stream)))
 
 
 def ls_replay_fwd_noalloc(desc, prompt, q, k_resp, v_resp, o, lse, stream=None):

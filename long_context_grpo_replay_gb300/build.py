@@ -19,7 +19,8 @@ CSRC = HERE / "csrc"
 INCLUDE = HERE.parent / "include"
 LIBDIR = HERE / "_lib"
 LIB = LIBDIR / "libls.so"
-SOURCES = ["ls_api.cu", "ls_simt.cu", "ls_tc_fwd.cu", "ls_tc_bwd.cu", "ls_tc_dkdv.cu", "ls_noalloc.cu"]
+SOURCES = ["ls_api.cu", "ls_simt.cu", "ls_tc_fwd.cu", "ls_tc_bwd.cu", "ls_tc_dkdv.cu", "ls_noalloc.cu",
+           "ls_gdn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -62,7 +62,8 @@ cudaEvent_t take_event() {
 
 const char* kKernelNames[kNumKernelIds] = {
     "page_write",  "simt_fwd",   "tc_fwd",     "lse_merge", "bwd_preprocess",
-    "simt_bwd_dq", "tc_bwd_dq",  "simt_dkdv",  "tc_dkdv",   "dq_reduce"};
+    "simt_bwd_dq", "tc_bwd_dq",  "simt_dkdv",  "tc_dkdv",   "dq_reduce",
+    "gdn_fwd",     "gdn_bwd"};
 
 // ------------------------------------------------------------------ devices
 int device_sms() {
@@ -561,6 +562,59 @@ ls_status ls_sum_parts(int32_t n_parts, int64_t n_elems, const float* parts, int
   LS_CUDA(launch_dq_reduce(n_parts, n_elems / 4, 4, 1.0f, parts, out_dtype, out,
                            static_cast<cudaStream_t>(stream)),
           "partial sum launch");
+  return LS_OK;
+}
+
+namespace {
+ls_status check_gdn(const ls_gdn_desc* d) {
+  if (!d) return fail(LS_ERR_INVALID_ARGUMENT, "desc is NULL");
+  if (d->heads < 0 || d->batch < 0) return fail(LS_ERR_INVALID_ARGUMENT, "heads or batch < 0");
+  if (d->batch > 65535) return fail(LS_ERR_UNSUPPORTED, "batch %d > 65535", d->batch);
+  if (!gdn_supported(d->dk, d->dv))
+    return fail(LS_ERR_UNSUPPORTED, "dk=%d dv=%d: supported is dk = dv = 128", d->dk, d->dv);
+  return LS_OK;
+}
+}  // namespace
+
+ls_status ls_gdn_workspace_size(const ls_gdn_desc* desc, int32_t resp_len, size_t* bytes) {
+  LS_CHECK(check_gdn(desc));
+  if (!bytes) return fail(LS_ERR_INVALID_ARGUMENT, "bytes is NULL");
+  if (resp_len < 0) return fail(LS_ERR_INVALID_ARGUMENT, "resp_len < 0");
+  *bytes = gdn_workspace_bytes(desc->batch, desc->heads, resp_len);
+  return LS_OK;
+}
+
+ls_status ls_gdn_replay_fwd(const ls_gdn_desc* desc, const float* s0, const float* q,
+                            const float* k, const float* v, const float* g, const float* beta,
+                            int32_t resp_len, float* o, float* s_final, void* stream) {
+  LS_CHECK(check_gdn(desc));
+  if (resp_len < 0) return fail(LS_ERR_INVALID_ARGUMENT, "resp_len < 0");
+  if (desc->batch == 0 || desc->heads == 0 || (resp_len == 0 && !s_final)) return LS_OK;
+  if (!s0 || (resp_len > 0 && (!q || !k || !v || !g || !beta || !o)))
+    return fail(LS_ERR_INVALID_ARGUMENT, "state and token buffers must be non-NULL");
+  LS_CUDA(launch_gdn_fwd(desc->batch, desc->heads, resp_len, s0, q, k, v, g, beta, o, s_final,
+                         static_cast<cudaStream_t>(stream)),
+          "GDN forward launch");
+  return LS_OK;
+}
+
+ls_status ls_gdn_replay_bwd(const ls_gdn_desc* desc, const float* s0, const float* q,
+                            const float* k, const float* v, const float* g, const float* beta,
+                            const float* d_o, int32_t resp_len, float* dq, float* dk, float* dv,
+                            float* dg, float* dbeta, void* ws, size_t ws_bytes, void* stream) {
+  LS_CHECK(check_gdn(desc));
+  if (resp_len < 0) return fail(LS_ERR_INVALID_ARGUMENT, "resp_len < 0");
+  if (desc->batch == 0 || desc->heads == 0 || resp_len == 0) return LS_OK;
+  if (!s0 || !q || !k || !v || !g || !beta || !d_o || !dq || !dk || !dv || !dg || !dbeta)
+    return fail(LS_ERR_INVALID_ARGUMENT, "backward buffers must be non-NULL");
+  const size_t need = gdn_workspace_bytes(desc->batch, desc->heads, resp_len);
+  if (!ws) return fail(LS_ERR_INVALID_ARGUMENT, "workspace is NULL");
+  if (ws_bytes < need)
+    return fail(LS_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes, need %zu", ws_bytes, need);
+  if (!aligned(ws, 16)) return fail(LS_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
+  LS_CUDA(launch_gdn_bwd(desc->batch, desc->heads, resp_len, s0, q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta,
+                         static_cast<float*>(ws), static_cast<cudaStream_t>(stream)),
+          "GDN backward launch");
   return LS_OK;
 }
 

@@ -31,6 +31,8 @@ enum KernelId : int32_t {
   kKSimtDkDv,
   kKTcDkDv,
   kKDqReduce,
+  kKGdnFwd,
+  kKGdnBwd,
   kNumKernelIds
 };
 
@@ -134,5 +136,15 @@ bool encode_pool_tile_map(CUtensorMap* m, const void* base, int64_t rows, int bo
 bool encode_rows_tile_map(CUtensorMap* m, const void* base, int heads, int64_t rows, int box_rows,
                           int box_blocks = 4);
 cudaError_t launch_tc_dkdv(const BwdParams& p, cudaStream_t s);
+// Gated-DeltaNet replay (ls_gdn.cu): dk = dv = 128, one CTA per (head, member).
+bool gdn_supported(int dk, int dv);
+size_t gdn_workspace_bytes(int B, int H, int R);
+cudaError_t launch_gdn_fwd(int B, int H, int R, const float* s0, const float* q, const float* k,
+                           const float* v, const float* g, const float* beta, float* o,
+                           float* s_final, cudaStream_t st);
+cudaError_t launch_gdn_bwd(int B, int H, int R, const float* s0, const float* q, const float* k,
+                           const float* v, const float* g, const float* beta, const float* d_o,
+                           float* dq, float* dk, float* dv, float* dg, float* dbeta, float* ws,
+                           cudaStream_t st);
 
 }  // namespace ls

@@ -192,3 +192,31 @@ def make_member(w: Workload, member: int, device="cpu", resp_len=None) -> dict:
     v = (torch.randn((R, w.hkv, w.head_dim), generator=g, device=device) * mult).to(dt)
     d_o = torch.randn((R, w.hq, w.head_dim), generator=g, device=device).to(dt)
     return {"q": q, "k": k, "v": v, "d_o": d_o}
+
+
+def make_gdn_group(batch: int, heads: int, resp_len: int, seed: int, dk: int = 128,
+                   dv: int = 128, device="cpu") -> dict:
+    """Seeded float32 inputs of one gated-DeltaNet group replay, drawn on
+    `device` (a CUDA generator's stream differs from the CPU one).
+
+    s0 [H, dv, dk]: the captured prompt state shared by the group, N(0, 0.1^2).
+    q, k [B, R, H, dk]: unit-norm rows (the layer normalises q and k before
+    the recurrence), q further scaled by dk^-1/2.  v, d_o [B, R, H, dv]:
+    N(0, 1).  g [B, R, H]: log of a decay in [0.85, 1).  beta [B, R, H]:
+    write strength in [0.05, 0.95)."""
+    gen = _gen(device, seed, 11)
+    B, R, H = batch, resp_len, heads
+    f32 = dict(generator=gen, device=device, dtype=torch.float32)
+
+    def unit(x):
+        return x / x.norm(dim=-1, keepdim=True).clamp_min(1e-6)
+
+    return {
+        "s0": 0.1 * torch.randn((H, dv, dk), **f32),
+        "q": unit(torch.randn((B, R, H, dk), **f32)) * dk ** -0.5,
+        "k": unit(torch.randn((B, R, H, dk), **f32)),
+        "v": torch.randn((B, R, H, dv), **f32),
+        "g": torch.log(0.85 + 0.15 * torch.rand((B, R, H), **f32)),
+        "beta": 0.05 + 0.9 * torch.rand((B, R, H), **f32),
+        "d_o": torch.randn((B, R, H, dv), **f32),
+    }

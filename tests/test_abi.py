@@ -172,3 +172,27 @@ def test_prefill_workspace_and_argument_checks(ls):
     assert st == 1 and "workspace" in ls.ls_last_error()  # NULL workspace, before any launch
     out = ctypes.c_size_t(0)
     assert L.ls_prompt_prefill_workspace_size(ctypes.byref(d), -1, ctypes.byref(out)) == 1
+
+
+def test_gdn_workspace_and_argument_checks(ls):
+    """Gated-DeltaNet entry points: sizing and validation before any launch."""
+    L = ls.lib()
+    d = ls.GdnDesc(8, 32, 128, 128)
+    sizes = [ls.ls_gdn_workspace_size(d, r) for r in (1, 64, 65, 4096)]
+    # per (member, head): one 128x128 float32 state per checkpoint (every 64
+    # tokens) plus one segment of 64 states
+    assert sizes == [8 * 32 * (n + 64) * 128 * 128 * 4 for n in (1, 1, 2, 64)]
+    out = ctypes.c_size_t(0)
+    bad = ls.GdnDesc(8, 32, 64, 128)
+    assert L.ls_gdn_workspace_size(ctypes.byref(bad), 10, ctypes.byref(out)) != 0
+    assert "128" in ls.ls_last_error()
+    assert L.ls_gdn_workspace_size(ctypes.byref(d), -1, ctypes.byref(out)) == 1
+    args = [None] * 6
+    assert L.ls_gdn_replay_fwd(ctypes.byref(d), *args, 0, None, None, None) == 0  # no-op
+    assert L.ls_gdn_replay_fwd(ctypes.byref(d), *args, 8, None, None, None) == 1  # NULL buffers
+    bw = [ctypes.c_void_p(256)] * 7
+    st = L.ls_gdn_replay_bwd(ctypes.byref(d), *bw, 8, *([ctypes.c_void_p(256)] * 5), None, 0, None)
+    assert st == 1 and "workspace" in ls.ls_last_error()
+    st = L.ls_gdn_replay_bwd(ctypes.byref(d), *bw, 8, *([ctypes.c_void_p(256)] * 5),
+                             ctypes.c_void_p(256), 100, None)
+    assert st != 0 and "workspace" in ls.ls_last_error()
