@@ -22,9 +22,11 @@
 //   dk_t  = b_t G_t^T w_t - a_t S_{t-1}^T dw
 //   G_{t-1} = a_t (G_t - dw k_t^T)
 // S_{t-1} is needed in reverse order: the forward is re-run with a
-// checkpoint of S every kSeg steps, and each segment is recomputed into a
-// per-head buffer before it is walked backwards.  The column sums (dq_t,
-// dk_t) go through shared memory; the two scalars through a block reduction.
+// checkpoint of S every kSegB = 8 steps, and each segment is recomputed into
+// a per-(member, head) buffer of 8 states (512 KB, so the buffers of all
+// resident CTAs stay in L2) before it is walked backwards.  The column sums
+// (dq_t, dk_t) go through shared memory; the two scalars through a block
+// reduction.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -36,9 +38,19 @@ namespace {
 
 constexpr int kD = 128;    // dk = dv
 constexpr int kTB = 16;    // tokens staged per block in the forward
-constexpr int kSeg = 64;   // checkpoint interval of the backward
+constexpr int kSegB = 8;   // checkpoint interval of the backward
 constexpr int kThreads = 256;
-constexpr int kRedPitch = kD + 1;  // padded rows of the column-sum buffers
+// Column-sum buffers of the backward: quantity (0: dq, 1: dk) x column half
+// x 128 rows x 64 columns, rows padded to 65 floats and the second half
+// shifted by 16 banks, so that both the row writes (thread (i, half)) and the
+// column reads are free of bank conflicts.
+constexpr int kRedPitch = 65;
+constexpr int kRedHalf = kD * kRedPitch + 16;
+constexpr int kRedQty = 2 * kRedHalf;
+constexpr int kRedFloats = 2 * kRedQty;
+__device__ __forceinline__ int red_at(int qty, int half, int row, int col) {
+  return qty * kRedQty + half * kRedHalf + row * kRedPitch + col;
+}
 
 __device__ __forceinline__ float pair_sum(float x) { return x + __shfl_xor_sync(0xffffffffu, x, 1); }
 
@@ -100,6 +112,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Thread-private state scratch, laid out so that a warp's accesses are
+// coalesced: element c of thread tid sits at float4 (c/4) * kThreads + tid.
+__device__ __forceinline__ void put_state(float* base, int tid, const float (&s)[64]) {
+  float4* p = reinterpret_cast<float4*>(base) + tid;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) p[j * kThreads] = make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]);
+}
+__device__ __forceinline__ void get_state(const float* base, int tid, float (&s)[64]) {
+  const float4* p = reinterpret_cast<const float4*>(base) + tid;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float4 x = p[j * kThreads];
+    s[4 * j] = x.x, s[4 * j + 1] = x.y, s[4 * j + 2] = x.z, s[4 * j + 3] = x.w;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_bwd_kernel(int H, int R, const float* __restrict__ s0, const float* __restrict__ q,
                    const float* __restrict__ k, const float* __restrict__ v,
@@ -107,98 +135,90 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const float* __restrict__ d_o, float* __restrict__ dq, float* __restrict__ dk,
                    float* __restrict__ dv, float* __restrict__ dg, float* __restrict__ dbeta,
                    float* __restrict__ ws) {
-  extern __shared__ float red[];  // [2][kD][kRedPitch]
-  __shared__ float kv_k[kD], kv_q[kD], kv_v[kD], kv_do[kD], sc[2];
-  __shared__ float part[2][kThreads / 32];
+  extern __shared__ float red[];  // column-sum buffers, see red_at
+  __shared__ float tk[kSegB][kD], tv[kSegB][kD], tq[kSegB][kD], tdo[kSegB][kD];
+  __shared__ float tg[kSegB], tb[kSegB], part[2][kThreads / 32];
   const int h = blockIdx.x, tid = threadIdx.x;
   const int i = tid >> 1, half = tid & 1;
   const int lane = tid & 31, wid = tid >> 5;
-  const int nseg = (R + kSeg - 1) / kSeg;
+  const int nseg = (R + kSegB - 1) / kSegB;
   {  // member blockIdx.y
     const int64_t tok = (int64_t)blockIdx.y * R * H;
     q += tok * kD, k += tok * kD, v += tok * kD, d_o += tok * kD, g += tok, beta += tok;
     dq += tok * kD, dk += tok * kD, dv += tok * kD, dg += tok, dbeta += tok;
   }
-  // per (member, head) workspace: nseg checkpoints, then kSeg states of one segment
-  float* ckpt = ws + ((int64_t)blockIdx.y * H + h) * (nseg + kSeg) * kD * kD;
-  float* seg = ckpt + (int64_t)nseg * kD * kD;
-  const int64_t my = (int64_t)i * kD + half * 64;  // this thread's slice of a state
+  // per (member, head) workspace: nseg checkpoints, then the kSegB states of one segment
+  float* ckpt = ws + ((int64_t)blockIdx.y * H + h) * (nseg + kSegB) * kD * kD;
+  float* segs = ckpt + (int64_t)nseg * kD * kD;
 
-  auto stage = [&](int t, bool with_q) {  // vectors of token t into shared memory
+  // tokens t0 .. t0+nt-1 into shared memory (q and dO only for the reverse walk)
+  auto stage = [&](int t0, int nt, bool with_q) {
     __syncthreads();
-    const int64_t row = (int64_t)t * H + h;
-    if (tid < kD) {
-      kv_k[tid] = k[row * kD + tid];
-      kv_v[tid] = v[row * kD + tid];
-    } else if (with_q) {
-      kv_q[tid - kD] = q[row * kD + tid - kD];
-      kv_do[tid - kD] = d_o[row * kD + tid - kD];
+    for (int x = tid; x < nt * kD; x += kThreads) {
+      const int tt = x / kD, j = x % kD;
+      const int64_t e = ((int64_t)(t0 + tt) * H + h) * kD + j;
+      tk[tt][j] = k[e];
+      tv[tt][j] = v[e];
+      if (with_q) {
+        tq[tt][j] = q[e];
+        tdo[tt][j] = d_o[e];
+      }
     }
-    if (tid == 0) {
-      sc[0] = g[row];
-      sc[1] = beta[row];
+    if (tid < nt) {
+      tg[tid] = g[(int64_t)(t0 + tid) * H + h];
+      tb[tid] = beta[(int64_t)(t0 + tid) * H + h];
     }
     __syncthreads();
   };
-  auto step = [&](float (&s)[64]) {  // S <- a S + b w k^T with the staged token
-    const float a = expf(sc[0]);
-    const float* kr = &kv_k[half * 64];
+  auto step = [&](float (&s)[64], int tt) {  // S <- a S + b w k^T with staged token tt
+    const float a = expf(tg[tt]);
+    const float* kr = &tk[tt][half * 64];
     float u = 0.f;
 #pragma unroll
     for (int c = 0; c < 64; ++c) u = fmaf(s[c], kr[c], u);
     u = pair_sum(u);
-    const float bw = sc[1] * (kv_v[i] - a * u);
+    const float bw = tb[tt] * (tv[tt][i] - a * u);
 #pragma unroll
     for (int c = 0; c < 64; ++c) s[c] = fmaf(a, s[c], bw * kr[c]);
   };
 
-  // ---- pass 1: forward, keeping S before every kSeg-th token
+  // ---- pass 1: forward, keeping S at the start of every segment
   float s[64];
 #pragma unroll
-  for (int c = 0; c < 64; ++c) s[c] = s0[(int64_t)h * kD * kD + my + c];
-  for (int t = 0; t < R; ++t) {
-    if (t % kSeg == 0) {
-      float* dst = ckpt + (int64_t)(t / kSeg) * kD * kD + my;
-#pragma unroll
-      for (int c = 0; c < 64; ++c) dst[c] = s[c];
-    }
-    stage(t, false);
-    step(s);
+  for (int c = 0; c < 64; ++c) s[c] = s0[(int64_t)h * kD * kD + (int64_t)i * kD + half * 64 + c];
+  for (int sg = 0; sg < nseg; ++sg) {
+    put_state(ckpt + (int64_t)sg * kD * kD, tid, s);
+    if (sg == nseg - 1) break;  // the last segment is recomputed in pass 2
+    stage(sg * kSegB, kSegB, false);
+    for (int tt = 0; tt < kSegB; ++tt) step(s, tt);
   }
 
   // ---- pass 2: segments in reverse; G = dL/dS in registers
   float gg[64];
 #pragma unroll
   for (int c = 0; c < 64; ++c) gg[c] = 0.f;
-  float* red0 = red;
-  float* red1 = red + kD * kRedPitch;
-  for (int sgi = nseg - 1; sgi >= 0; --sgi) {
-    const int t0 = sgi * kSeg, t1 = (t0 + kSeg < R) ? t0 + kSeg : R;
-    const float* c0 = ckpt + (int64_t)sgi * kD * kD + my;
-#pragma unroll
-    for (int c = 0; c < 64; ++c) s[c] = c0[c];
-    for (int t = t0; t < t1; ++t) {  // S before each token of the segment
-      float* dst = seg + (int64_t)(t - t0) * kD * kD + my;
-#pragma unroll
-      for (int c = 0; c < 64; ++c) dst[c] = s[c];
-      stage(t, false);
-      step(s);
+  float* r0 = red + red_at(0, half, i, 0);  // this thread's row of the dq buffer
+  float* r1 = red + red_at(1, half, i, 0);  // and of the dk buffer
+  for (int sg = nseg - 1; sg >= 0; --sg) {
+    const int t0 = sg * kSegB, nt = (R - t0 < kSegB) ? R - t0 : kSegB;
+    stage(t0, nt, true);
+    get_state(ckpt + (int64_t)sg * kD * kD, tid, s);
+    for (int tt = 0; tt < nt; ++tt) {  // S before each token of the segment
+      put_state(segs + (int64_t)tt * kD * kD, tid, s);
+      step(s, tt);
     }
-    for (int t = t1 - 1; t >= t0; --t) {
-      stage(t, true);  // also orders the previous step's column sums before reuse
-      const float* spp = seg + (int64_t)(t - t0) * kD * kD + my;
+    for (int tt = nt - 1; tt >= 0; --tt) {
       float sp[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) sp[c] = spp[c];
-      const float a = expf(sc[0]), b = sc[1];
-      const float* kr = &kv_k[half * 64];
-      const float* qr = &kv_q[half * 64];
+      get_state(segs + (int64_t)tt * kD * kD, tid, sp);  // S_{t-1}, written by this thread
+      const float a = expf(tg[tt]), b = tb[tt];
+      const float* kr = &tk[tt][half * 64];
+      const float* qr = &tq[tt][half * 64];
       float u = 0.f;
 #pragma unroll
       for (int c = 0; c < 64; ++c) u = fmaf(sp[c], kr[c], u);
       u = pair_sum(u);
-      const float w = kv_v[i] - a * u;
-      const float doi = kv_do[i];
+      const float w = tv[tt][i] - a * u;
+      const float doi = tdo[tt][i];
       float gk = 0.f;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
@@ -208,8 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       gk = pair_sum(gk);
       const float dw = b * gk;
       float gs_dot = 0.f;
-      float* r0 = red0 + i * kRedPitch + half * 64;
-      float* r1 = red1 + i * kRedPitch + half * 64;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float st = fmaf(a, sp[c], b * w * kr[c]);  // S_t
@@ -230,18 +248,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         part[0][wid] = pdb;
         part[1][wid] = pda;
       }
-      if (half == 0) dv[((int64_t)t * H + h) * kD + i] = dw;
+      const int64_t row = (int64_t)(t0 + tt) * H + h;
+      if (half == 0) dv[row * kD + i] = dw;
       __syncthreads();
-      const int64_t row = (int64_t)t * H + h;
-      if (tid < kD) {
-        float acc = 0.f;
-        for (int r = 0; r < kD; ++r) acc += red0[r * kRedPitch + tid];
-        dq[row * kD + tid] = acc;
-      } else {
-        const int j = tid - kD;
-        float acc = 0.f;
-        for (int r = 0; r < kD; ++r) acc += red1[r * kRedPitch + j];
-        dk[row * kD + j] = acc;
+      {  // column j of dq (threads 0..127) or dk (128..255): the sum over the 128 rows
+        const int which = tid >> 7, j = tid & (kD - 1);
+        const float* col = red + red_at(which, j >> 6, 0, j & 63);
+        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll 8
+        for (int r = 0; r < kD; r += 4) {
+          acc0 += col[(r + 0) * kRedPitch];
+          acc1 += col[(r + 1) * kRedPitch];
+          acc2 += col[(r + 2) * kRedPitch];
+          acc3 += col[(r + 3) * kRedPitch];
+        }
+        (which == 0 ? dq : dk)[row * kD + j] = (acc0 + acc1) + (acc2 + acc3);
       }
       if (tid == 0) {
         float sdb = 0.f, sda = 0.f;
@@ -252,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         dbeta[row] = sdb;
         dg[row] = sda * a;
       }
+      __syncthreads();  // the buffers and part[] are rewritten by the next step
     }
   }
 }
@@ -259,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 size_t gdn_workspace_bytes(int B, int H, int R) {
-  const int64_t nseg = (R + kSeg - 1) / kSeg;
-  return (size_t)B * H * (size_t)(nseg + kSeg) * kD * kD * sizeof(float);
+  const int64_t nseg = (R + kSegB - 1) / kSegB;
+  return (size_t)B * H * (size_t)(nseg + kSegB) * kD * kD * sizeof(float);
 }
 
 bool gdn_supported(int dk, int dv) { return dk == kD && dv == kD; }
@@ -279,7 +301,7 @@ cudaError_t launch_gdn_bwd(int B, int H, int R, const float* s0, const float* q,
                            float* dq, float* dk, float* dv, float* dg, float* dbeta, float* ws,
                            cudaStream_t st) {
   if (B == 0 || H == 0 || R == 0) return cudaSuccess;
-  const int smem = 2 * kD * kRedPitch * (int)sizeof(float);
+  const int smem = kRedFloats * (int)sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(gdn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   LaunchScope ls(kKGdnBwd, st);
