@@ -624,7 +624,7 @@ def run_prefill(args):
         dist.destroy_process_group()
 
 
-GDN_WORKLOADS = {"gdn_f32_h32_r4096_g8": (8, 32, 4096)}
+GDN_WORKLOADS = {"gdn_f32_h32_r4096_g8": (8, 32, 4096), "gdn_f32_h32_r1024_g4": (4, 32, 1024)}
 GDN_METRIC = "GDN state replay (forward+backward) response tokens/s per layer"
 # fp32 FMA lanes: 152 SMs x 128 lanes x 2 flop x 2.07 GHz
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
@@ -695,8 +695,10 @@ def run_gdn(args):
     launch_ms = t_l / max(1, n_l)
     fl_bwd = GDN_BWD_FLOP_PER_TOKEN_HEAD * unit_flop
     achieved = fl_bwd / (launch_ms * 1e-3) / 1e12
+    traffic = recorded_traffic("gdn_bwd", args.workload,
+                               ROOT / "long_context_grpo_replay_gb300" / "csrc" / "ls_gdn.cu")
     roof = {"bound": "alu", "achieved": achieved, "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
-            "frac": achieved / FP32_ALU_TFLOPS, "traffic": None, "kernel": "gdn_bwd",
+            "frac": achieved / FP32_ALU_TFLOPS, "traffic": traffic, "kernel": "gdn_bwd",
             "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz",
             "algorithmic_per_launch": fl_bwd, "launch_ms": launch_ms}
 
