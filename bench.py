@@ -440,6 +440,10 @@ def run_reference(args):
     world, rank, local = dist_env()
     if rank != 0:
         return
+    if args.workload in GDN_WORKLOADS:
+        return run_reference_gdn(args, world)
+    if args.workload in PREFILL_WORKLOADS:
+        return run_reference_prefill(args, world)
     w = inputs.WORKLOADS[args.workload]
     gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
     pr = inputs.make_prompt(w, gen_dev)
@@ -471,6 +475,84 @@ def run_reference(args):
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+    print(json.dumps(line), flush=True)
+
+
+def _reference_line(args, world, metric, value, unit, dtype, config, sample, ms):
+    return {
+        "impl": "reference", "metric": metric, "value": value, "unit": unit,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+        "data": "synthetic", "config": config,
+        "cpu_baseline": {"value": value, "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_reference_gdn(args, world):
+    """Oracle arm of a GDN workload: per step the float64 oracle replays the
+    first tokens of one head of one member, forward and backward."""
+    from long_context_grpo_replay_gb300 import inputs
+    from oracle.gdn import gdn_replay
+
+    B, H, R = GDN_WORKLOADS[args.workload]
+    n_tok = min(R, 256)
+    c = inputs.make_gdn_group(1, 1, n_tok, seed=55)  # same distributions, one (member, head)
+    a = {x: t[0] if x != "s0" else t for x, t in c.items()}
+
+    def one():
+        t0 = time.perf_counter()
+        gdn_replay(a["s0"], a["q"], a["k"], a["v"], a["g"], a["beta"], a["d_o"])
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        one()
+    tot = sum(one() for _ in range(args.steps))
+    value = n_tok * args.steps / H / tot  # whole tokens (all H heads) per second
+    line = _reference_line(
+        args, world, GDN_METRIC, value, "tokens/s", "f64",
+        {"workload": args.workload, "group": B, "heads": H, "resp_len": R, "dk": 128, "dv": 128},
+        f"per step: one head of one member, {n_tok} tokens, forward+backward (float64 torch, "
+        f"autograd), scaled to {H} heads", tot / args.steps * 1e3)
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_prefill(args, world):
+    """Oracle arm of a prefill workload: per step the last prompt row of the
+    query heads of one KV head, over all prompt keys."""
+    import torch
+
+    import oracle.ref as ref
+    from long_context_grpo_replay_gb300 import inputs
+
+    N = PREFILL_WORKLOADS[args.workload]
+    w = inputs.Workload(args.workload, 24, 4, 256, 256, N, (N,), "bf16", seed=31)
+    gq = w.hq // w.hkv
+    hs = inputs.make_head_sample(w, N)
+    # The last prompt row sees all N keys: keys 0..N-2 as prompt pages of the
+    # one KV head, key N-1 as its own (causal) key, the query as a single row.
+    pages = N // w.page_size
+    k_pool = hs["k"].view(pages, w.page_size, 1, w.head_dim).transpose(1, 2).contiguous()
+    v_pool = hs["v"].view(pages, w.page_size, 1, w.head_dim).transpose(1, 2).contiguous()
+    table = torch.arange(pages, dtype=torch.int32)
+
+    def one():
+        t0 = time.perf_counter()
+        ref.replay_member(k_pool, v_pool, table, N - 1, hs["q"], hs["k"][N - 1:], hs["v"][N - 1:],
+                          scale=w.scale)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        one()
+    tot = sum(one() for _ in range(args.steps))
+    value = 4.0 * w.head_dim * gq * N * args.steps / tot / 1e12
+    line = _reference_line(
+        args, world, PREFILL_METRIC, value, "TFLOP/s", "f64",
+        {"workload": args.workload, "prompt_len": N, "hq": w.hq, "hkv": w.hkv,
+         "head_dim": w.head_dim, "page_size": w.page_size},
+        f"per step: row {N - 1} of the {gq} query heads of KV head 0 over all {N} keys "
+        "(float64 numpy)", tot / args.steps * 1e3)
     print(json.dumps(line), flush=True)
 
 

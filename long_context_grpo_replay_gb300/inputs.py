@@ -194,6 +194,20 @@ def make_member(w: Workload, member: int, device="cpu", resp_len=None) -> dict:
     return {"q": q, "k": k, "v": v, "d_o": d_o}
 
 
+def make_head_sample(w: Workload, n_tok: int, device="cpu") -> dict:
+    """The inputs one KV head's group of query heads sees, drawn alone with the
+    distributions of make_member (a bounded sample for timing the oracle on a
+    long prompt): q [1, Gq, d] (the last row), k/v [n_tok, 1, d]."""
+    dt = torch_dtype(w)
+    g = _gen(device, w.seed, 900)
+    mult = 1.0 / math.sqrt(w.head_dim)
+    gq = w.hq // w.hkv
+    q = (torch.randn((1, gq, w.head_dim), generator=g, device=device) * mult).to(dt)
+    k = (torch.randn((n_tok, 1, w.head_dim), generator=g, device=device) * mult).to(dt)
+    v = (torch.randn((n_tok, 1, w.head_dim), generator=g, device=device) * mult).to(dt)
+    return {"q": q, "k": k, "v": v}
+
+
 def make_gdn_group(batch: int, heads: int, resp_len: int, seed: int, dk: int = 128,
                    dv: int = 128, device="cpu") -> dict:
     """Seeded float32 inputs of one gated-DeltaNet group replay, drawn on
