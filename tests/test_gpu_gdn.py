@@ -2,8 +2,8 @@
 (oracle/gdn.py) on the same seeded inputs: every output of the forward (o,
 the final state) and of the backward (dq, dk, dv, dg, dbeta) element by
 element at the float32 tolerance, for one member, a group, a single token,
-a response that crosses the backward's 64-token checkpoint boundary, and
-the empty response.  At the group size the benchmark times (8 members, 32
+a response that spans 17 of the backward's 8-token checkpoint segments (the
+last one partial), and the empty response.  At the group size the benchmark times (8 members, 32
 heads, 4096 tokens) two sampled (member, head) pairs are checked in full."""
 import numpy as np
 import pytest

@@ -122,3 +122,42 @@ def test_empty_response():
     r = gdn_replay(s0, q, k, v, g, b, d_o)
     assert r["o"].shape == (0, 2, 4)
     np.testing.assert_allclose(r["s_final"], s0)
+
+
+def _chunkwise(s0, q, k, v, g, b, C):
+    """The same rule in chunkwise form, derived independently of the oracle's
+    loop.  Within a chunk, with gamma_t the running product of the decays and
+    e_t = b_t (v_t - a_t S_{t-1} k_t):
+        S_t = gamma_t S_0 + sum_{s<=t} (gamma_t / gamma_s) e_s k_s^T,
+    so the e_t solve a unit lower-triangular system
+        (I + A) E = diag(b) (V - diag(gamma) K S_0^T),
+        A_ts = b_t (gamma_t / gamma_s) k_t . k_s   (s < t),
+    and O = diag(gamma) Q S_0^T + (tril(Gamma) * Q K^T) E,
+        S_C = gamma_C S_0 + E^T diag(gamma_C / gamma) K."""
+    R, H, _ = q.shape
+    o = np.zeros((R, H, v.shape[2]))
+    fin = np.zeros_like(s0)
+    for h in range(H):
+        S = s0[h].copy()
+        for c0 in range(0, R, C):
+            sl = slice(c0, min(R, c0 + C))
+            Q, K, V = q[sl, h], k[sl, h], v[sl, h]
+            gam = np.exp(np.cumsum(g[sl, h]))
+            bt = b[sl, h]
+            ratio = gam[:, None] / gam[None, :]
+            n = len(gam)
+            A = np.tril(bt[:, None] * ratio * (K @ K.T), -1)
+            E = np.linalg.solve(np.eye(n) + A, bt[:, None] * (V - gam[:, None] * (K @ S.T)))
+            o[sl, h] = gam[:, None] * (Q @ S.T) + (np.tril(ratio) * (Q @ K.T)) @ E
+            S = gam[-1] * S + E.T @ ((gam[-1] / gam)[:, None] * K)
+        fin[h] = S
+    return o, fin
+
+
+@pytest.mark.parametrize("C", [1, 4, 16])
+def test_chunkwise_form_equals_the_recurrence(C):
+    s0, q, k, v, g, b, _ = _case(H=2, dk=6, dv=5, R=13, seed=17, unit_k=False)
+    r = gdn_replay(s0, q, k, v, g, b)
+    o, fin = _chunkwise(s0, q, k, v, g, b, C)
+    np.testing.assert_allclose(r["o"], o, atol=1e-11)
+    np.testing.assert_allclose(r["s_final"], fin, atol=1e-11)
