@@ -238,6 +238,12 @@ def run_ours(args):
     ls.ls_trace_enable(False)
     ls.ls_read_device_status(ws)
     clocks = clk.summary()
+    memory = {  # the workspace is sized for the longest member, not for G
+        "peak_allocated_gib": round(torch.cuda.max_memory_allocated(dev) / 2**30, 2),
+        "workspace_gib": round(ws.numel() / 2**30, 3),
+        "member_io_gib": round(sum(t.numel() * t.element_size() for m in members for t in m.values())
+                               / G / 2**30, 3),
+    }
     ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
     flops_step = sum(replay_flops(P, R, hq, d) for R in w.resp_lens)
@@ -309,6 +315,7 @@ def run_ours(args):
             "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clocks,
+            "memory": memory,
             "kernels_ms_per_step": {k: round(v[1] / args.steps, 3) for k, v in trace.items()},
         }
         print(json.dumps(line), flush=True)
