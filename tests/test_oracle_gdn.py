@@ -161,3 +161,76 @@ def test_chunkwise_form_equals_the_recurrence(C):
     o, fin = _chunkwise(s0, q, k, v, g, b, C)
     np.testing.assert_allclose(r["o"], o, atol=1e-11)
     np.testing.assert_allclose(r["s_final"], fin, atol=1e-11)
+
+
+def _chunk_grads(S, Q, K, V, g, b, dO, G_end):
+    """Backward of one chunk of the chunkwise form, derived by hand: the
+    gradients for Q, K, V, g, b and dL/dS at the chunk's start, given dO and
+    dL/dS at its end.  All products are dense; the one solve is the
+    transposed triangular system of the forward."""
+    n = len(g)
+    c = np.cumsum(g)
+    gam = np.exp(c)
+    Gam = np.exp(c[:, None] - c[None, :])
+    L = np.tril(np.ones((n, n)))
+    KK = K @ K.T
+    A = np.tril(b[:, None] * Gam * KK, -1)
+    X = V - gam[:, None] * (K @ S.T)
+    E = np.linalg.solve(np.eye(n) + A, b[:, None] * X)
+    P = L * Gam * (Q @ K.T)
+    w = np.exp(c[-1] - c)
+    # O = diag(gam) Q S^T + P E;  S_end = gam_n S + E^T diag(w) K
+    dE = P.T @ dO + (w[:, None] * K) @ G_end.T
+    dP = dO @ E.T
+    dW = E @ G_end
+    dS = dO.T @ (gam[:, None] * Q) + gam[-1] * G_end
+    dgam = (dO * (Q @ S.T)).sum(1)
+    LdP = L * Gam * dP
+    dQ = gam[:, None] * (dO @ S) + LdP @ K
+    dK = LdP.T @ Q
+    dGam = L * dP * (Q @ K.T)
+    dU = np.linalg.solve((np.eye(n) + A).T, dE)       # E = (I + A)^-1 U
+    dA = -np.tril(dU @ E.T, -1)
+    db = (dA * Gam * KK).sum(1) + (dU * X).sum(1)
+    dGam += dA * b[:, None] * KK
+    dKK = dA * b[:, None] * Gam
+    dK += (dKK + dKK.T) @ K
+    dX = b[:, None] * dU                               # U = diag(b) X
+    dV = dX
+    dgam -= (dX * (K @ S.T)).sum(1)
+    dK += -gam[:, None] * (dX @ S) + w[:, None] * dW
+    dS -= dX.T @ (gam[:, None] * K)
+    # back to the log-decays through gam, Gam, w and gam_n, then g = diff(c)
+    r = dGam * Gam
+    rw = (dW * K).sum(1) * w
+    dc = dgam * gam + r.sum(1) - r.sum(0) - rw
+    dc[-1] += rw.sum() + (G_end * S).sum() * gam[-1]
+    dg = np.cumsum(dc[::-1])[::-1]
+    return dQ, dK, dV, dg, db, dS
+
+
+@pytest.mark.parametrize("C", [1, 4, 8, 23])
+def test_chunkwise_backward_equals_the_oracle_gradients(C):
+    """The oracle's gradients (autograd of its step loop) against a chunkwise
+    backward derived by hand: forward over the chunks keeping each chunk's
+    starting state, then the chunks in reverse, carrying dL/dS."""
+    s0, q, k, v, g, b, d_o = _case(H=2, dk=6, dv=5, R=23, seed=3, unit_k=False)
+    want = gdn_replay(s0, q, k, v, g, b, d_o)
+    R, H, _ = q.shape
+    got = {x: np.zeros_like(want[x]) for x in ("dq", "dk", "dv", "dg", "dbeta")}
+    for h in range(H):
+        chunks = [(c0, min(R, c0 + C)) for c0 in range(0, R, C)]
+        starts, S = [], s0[h].copy()
+        for c0, c1 in chunks:
+            starts.append(S)
+            S = gdn_replay(S[None], q[c0:c1, h:h + 1], k[c0:c1, h:h + 1], v[c0:c1, h:h + 1],
+                           g[c0:c1, h:h + 1], b[c0:c1, h:h + 1])["s_final"][0]
+        G = np.zeros_like(S)
+        for (c0, c1), S0 in reversed(list(zip(chunks, starts))):
+            sl = slice(c0, c1)
+            dQ, dK, dV, dg, db, G = _chunk_grads(S0, q[sl, h], k[sl, h], v[sl, h], g[sl, h],
+                                                 b[sl, h], d_o[sl, h], G)
+            got["dq"][sl, h], got["dk"][sl, h], got["dv"][sl, h] = dQ, dK, dV
+            got["dg"][sl, h], got["dbeta"][sl, h] = dg, db
+    for x in got:
+        np.testing.assert_allclose(got[x], want[x], atol=1e-10, err_msg=x)
