@@ -142,6 +142,11 @@ size_t gdn_workspace_bytes(int B, int H, int R);
 cudaError_t launch_gdn_fwd(int B, int H, int R, const float* s0, const float* q, const float* k,
                            const float* v, const float* g, const float* beta, float* o,
                            float* s_final, cudaStream_t st);
+// Chunkwise tensor-core forward (ls_gdn_chunk.cu), selected by LS_GDN_VARIANT=chunk.
+bool gdn_chunk_selected();
+cudaError_t launch_gdn_chunk_fwd(int B, int H, int R, const float* s0, const float* q,
+                                 const float* k, const float* v, const float* g, const float* beta,
+                                 float* o, float* s_final, cudaStream_t st);
 cudaError_t launch_gdn_bwd(int B, int H, int R, const float* s0, const float* q, const float* k,
                            const float* v, const float* g, const float* beta, const float* d_o,
                            float* dq, float* dk, float* dv, float* dg, float* dbeta, float* ws,

@@ -1,0 +1,72 @@
+"""The chunkwise tensor-core GDN forward (LS_GDN_VARIANT=chunk) against the
+float64 oracle at the bf16 tolerance: its products take bf16 operands, which
+a CPU simulation of the same rounding points puts near 4e-3.  Cases: three
+chunks with a partial last one, one exact chunk, a single token, the empty
+response, and two sampled heads of the 8 x 32-head x 4096-token group.
+
+The kernel is compiled with the library but has not yet run on a GPU, so
+these tests run only when LS_GDN_CHUNK_TESTS=1."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import long_context_grpo_replay_gb300.binding as ls
+from long_context_grpo_replay_gb300 import inputs
+from oracle.gdn import gdn_replay
+from gpu_helpers import TOL, rel_err
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(os.environ.get("LS_GDN_CHUNK_TESTS") != "1",
+                                 reason="chunkwise GDN forward not yet run on a GPU")]
+
+
+@pytest.fixture(autouse=True)
+def _chunk_variant(monkeypatch):
+    from long_context_grpo_replay_gb300 import build
+
+    build.build()
+    ls.lib()
+    monkeypatch.setenv("LS_GDN_VARIANT", "chunk")
+
+
+def _fwd(c):
+    B, R, H, _ = c["q"].shape
+    o = torch.full_like(c["v"], float("nan"))
+    s_final = torch.empty((B, H, 128, 128), device=c["q"].device)
+    ls.ls_gdn_replay_fwd(c["s0"], c["q"], c["k"], c["v"], c["g"], c["beta"], o, s_final)
+    torch.cuda.synchronize()
+    return o, s_final
+
+
+def _check(c, o, s_final, b, heads):
+    hs = list(heads)
+    a = {x: c[x].cpu() for x in ("s0", "q", "k", "v", "g", "beta")}
+    want = gdn_replay(a["s0"][hs], a["q"][b][:, hs], a["k"][b][:, hs], a["v"][b][:, hs],
+                      a["g"][b][:, hs], a["beta"][b][:, hs])
+    e_o = rel_err(o[b][:, hs].double().cpu().numpy(), want["o"])
+    e_s = rel_err(s_final[b][hs].double().cpu().numpy(), want["s_final"])
+    assert e_o <= TOL["bf16"] and e_s <= TOL["bf16"], (b, hs, e_o, e_s)
+
+
+@pytest.mark.parametrize("B,H,R", [(1, 4, 300), (2, 2, 128), (2, 3, 1)],
+                         ids=["three_chunks_r300", "one_chunk_r128", "one_token"])
+def test_chunk_forward_matches_the_oracle(cuda_device, B, H, R):
+    c = inputs.make_gdn_group(B, H, R, seed=60 + R, device=cuda_device)
+    o, s_final = _fwd(c)
+    for b in range(B):
+        _check(c, o, s_final, b, range(H))
+
+
+def test_chunk_forward_empty_response(cuda_device):
+    c = inputs.make_gdn_group(2, 2, 0, seed=8, device=cuda_device)
+    _, s_final = _fwd(c)
+    assert torch.equal(s_final, c["s0"].expand_as(s_final))
+
+
+def test_chunk_forward_at_bench_size_sampled(cuda_device):
+    c = inputs.make_gdn_group(8, 32, 4096, seed=78, device=cuda_device)
+    o, s_final = _fwd(c)
+    assert torch.isfinite(o).all() and torch.isfinite(s_final).all()
+    _check(c, o, s_final, 6, (1, 30))
