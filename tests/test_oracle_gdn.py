@@ -234,3 +234,24 @@ def test_chunkwise_backward_equals_the_oracle_gradients(C):
             got["dg"][sl, h], got["dbeta"][sl, h] = dg, db
     for x in got:
         np.testing.assert_allclose(got[x], want[x], atol=1e-10, err_msg=x)
+
+
+def test_state_gradient_is_linear_across_a_chunk():
+    """dL/dS at a chunk's start depends on dL/dS at its end through one fixed
+    matrix, G_start = G_end M + C with M = gamma_C I - W^T (I + A)^-1
+    diag(gamma b) K: the chunks' backward can run in parallel, with only
+    this product chained over them."""
+    rng = np.random.default_rng(0)
+    n, dk, dv = 7, 5, 4
+    S, Q, K = rng.standard_normal((dv, dk)), rng.standard_normal((n, dk)), rng.standard_normal((n, dk))
+    V, dO = rng.standard_normal((n, dv)), rng.standard_normal((n, dv))
+    g, b = np.log(rng.uniform(0.7, 1, n)), rng.uniform(0.1, 0.9, n)
+    G1 = rng.standard_normal((dv, dk))
+    dS1 = _chunk_grads(S, Q, K, V, g, b, dO, G1)[5]
+    dS0 = _chunk_grads(S, Q, K, V, g, b, dO, np.zeros((dv, dk)))[5]
+    c = np.cumsum(g)
+    gam = np.exp(c)
+    A = np.tril(b[:, None] * np.exp(c[:, None] - c[None, :]) * (K @ K.T), -1)
+    W = np.exp(c[-1] - c)[:, None] * K
+    M = gam[-1] * np.eye(dk) - W.T @ np.linalg.solve(np.eye(n) + A, np.diag(gam * b) @ K)
+    np.testing.assert_allclose(dS1 - dS0, G1 @ M, atol=1e-12)
