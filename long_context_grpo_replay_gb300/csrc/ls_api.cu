@@ -592,9 +592,14 @@ ls_status ls_gdn_replay_fwd(const ls_gdn_desc* desc, const float* s0, const floa
   if (desc->batch == 0 || desc->heads == 0 || (resp_len == 0 && !s_final)) return LS_OK;
   if (!s0 || (resp_len > 0 && (!q || !k || !v || !g || !beta || !o)))
     return fail(LS_ERR_INVALID_ARGUMENT, "state and token buffers must be non-NULL");
-  LS_CUDA(launch_gdn_fwd(desc->batch, desc->heads, resp_len, s0, q, k, v, g, beta, o, s_final,
-                         static_cast<cudaStream_t>(stream)),
-          "GDN forward launch");
+  if (gdn_chunk_selected())
+    LS_CUDA(launch_gdn_chunk_fwd(desc->batch, desc->heads, resp_len, s0, q, k, v, g, beta, o,
+                                 s_final, static_cast<cudaStream_t>(stream)),
+            "GDN chunk forward launch");
+  else
+    LS_CUDA(launch_gdn_fwd(desc->batch, desc->heads, resp_len, s0, q, k, v, g, beta, o, s_final,
+                           static_cast<cudaStream_t>(stream)),
+            "GDN forward launch");
   return LS_OK;
 }
 

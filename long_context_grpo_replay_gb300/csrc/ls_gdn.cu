@@ -291,8 +291,6 @@ cudaError_t launch_gdn_fwd(int B, int H, int R, const float* s0, const float* q,
                            const float* v, const float* g, const float* beta, float* o,
                            float* s_final, cudaStream_t st) {
   if (B == 0 || H == 0) return cudaSuccess;
-  if (gdn_chunk_selected())
-    return launch_gdn_chunk_fwd(B, H, R, s0, q, k, v, g, beta, o, s_final, st);
   LaunchScope ls(kKGdnFwd, st);
   gdn_fwd_kernel<<<dim3(H, B), kThreads, 0, st>>>(H, R, s0, q, k, v, g, beta, o, s_final);
   return cudaGetLastError();
