@@ -27,6 +27,18 @@ import torch
 from . import binding as ls
 
 
+def page_chunks(prompt_len: int, page_size: int, chunk_pages: int) -> list:
+    """The prompt's logical pages cut into chunks of at most chunk_pages:
+    (first page, end page, keys in the chunk) per chunk; none for an empty
+    prompt.  The last chunk may end in a partial page."""
+    if chunk_pages < 1:
+        raise ValueError("chunk_pages must be >= 1")
+    n_pages = -(-prompt_len // page_size)
+    return [(c0, min(c0 + chunk_pages, n_pages),
+             min(prompt_len, min(c0 + chunk_pages, n_pages) * page_size) - c0 * page_size)
+            for c0 in range(0, n_pages, chunk_pages)]
+
+
 class HostPagedReplay:
     """Replay over a prompt whose pages are in pinned host memory.
 
@@ -49,7 +61,7 @@ class HostPagedReplay:
             raise ValueError("page table shorter than the prompt")
         if n_pages and (int(self.pt[:n_pages].min()) < 0 or int(self.pt[:n_pages].max()) >= k_pool_host.shape[0]):
             raise ValueError("page table entry outside the host pool")
-        self.chunks = [(c, min(c + chunk_pages, n_pages)) for c in range(0, n_pages, chunk_pages)]
+        self.chunks = [(c0, c1) for c0, c1, _ in page_chunks(self.P, self.page, chunk_pages)]
         shape = (chunk_pages,) + tuple(k_pool_host.shape[1:])
         self.kst = [torch.empty(shape, dtype=k_pool_host.dtype, device=device) for _ in range(2)]
         self.vst = [torch.empty(shape, dtype=v_pool_host.dtype, device=device) for _ in range(2)]

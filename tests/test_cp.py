@@ -162,3 +162,21 @@ def test_block_cyclic_ownership_covers_every_page_once():
         assert flat == list(range(n))
         lens = [cp.local_prompt_len(n * PAGE - 3, PAGE, o) for o in owned]
         assert sum(lens) == n * PAGE - 3
+
+
+def test_host_page_chunks_cover_the_prompt_once():
+    """Host-resident pages are streamed in chunks of whole pages: together the
+    chunks hold every key exactly once, in order, with a partial last page."""
+    from long_context_grpo_replay_gb300.host_pages import page_chunks
+
+    assert page_chunks(0, 256, 4) == []
+    assert page_chunks(1, 256, 4) == [(0, 1, 1)]
+    assert page_chunks(1000, 256, 3) == [(0, 3, 768), (3, 4, 232)]
+    assert page_chunks(1024, 256, 8) == [(0, 4, 1024)]
+    for P, S_p, n in [(20 * 16 - 5, 16, 3), (5000, 256, 1), (65536, 256, 64)]:
+        ch = page_chunks(P, S_p, n)
+        assert sum(k for _, _, k in ch) == P
+        assert all(a[1] == b[0] for a, b in zip(ch, ch[1:]))
+        assert all(c1 - c0 <= n for c0, c1, _ in ch)
+    with pytest.raises(ValueError):
+        page_chunks(10, 16, 0)
