@@ -67,19 +67,6 @@ __device__ __forceinline__ uint4 pack8(const float* x) {
   return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
                     pack_bf16x2(x[6], x[7]));
 }
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-__device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
-  __nv_bfloat162 b;
-  *reinterpret_cast<uint32_t*>(&b) = u;
-  return __bfloat1622float2(b);
-}
 
 __global__ void __launch_bounds__(kThr, 1)
     gdn_chunk_fwd_kernel(int H, int R, const float* __restrict__ s0, const float* __restrict__ q,
