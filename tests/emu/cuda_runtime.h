@@ -1,7 +1,11 @@
 // Host stand-in for the CUDA runtime header when a kernel's source is run
-// on the CPU block emulator (emu_core.h): the qualifiers compile away, the
-// vector types are plain structs, and the block built-ins go to the emulator.
+// on the CPU block emulator (emu_core.h): the qualifiers compile away
+// (__shared__ objects become function statics, shared by the block's
+// threads), the vector types are plain structs, and the block built-ins go
+// to the emulator.  A kernel's "extern __shared__" array is declared by the
+// test harness, which rewrites that line to "extern".
 #pragma once
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -13,7 +17,8 @@
 #define __host__
 #define __forceinline__ inline
 #define __restrict__
-#define __shared__
+#define __shared__ static
+#define __grid_constant__
 #define __launch_bounds__(...)
 
 struct dim3 {
@@ -43,24 +48,41 @@ inline float __int_as_float(int i) {
   std::memcpy(&f, &i, 4);
   return f;
 }
+inline unsigned __float_as_uint(float f) {
+  unsigned u;
+  std::memcpy(&u, &f, 4);
+  return u;
+}
+inline float __log2f(float x) { return std::log2(x); }
+template <class T>
+inline T __ldg(const T* p) {
+  return *p;
+}
 inline unsigned atomicExch(unsigned* p, unsigned v) {
-  const unsigned o = *p;
-  *p = v;
-  return o;
+  return std::atomic_ref<unsigned>(*p).exchange(v);
+}
+inline unsigned atomicOr(unsigned* p, unsigned v) { return std::atomic_ref<unsigned>(*p).fetch_or(v); }
+inline unsigned atomicCAS(unsigned* p, unsigned cmp, unsigned v) {
+  std::atomic_ref<unsigned>(*p).compare_exchange_strong(cmp, v);
+  return cmp;
 }
 inline void __syncthreads() { emu::syncthreads(); }
 inline int __syncthreads_or(int p) { return emu::syncthreads_or(p); }
+inline void __syncwarp(unsigned = 0xffffffffu) { emu::syncwarp(); }
 inline float __shfl_up_sync(unsigned, float x, int off) { return emu::shfl_up(x, off); }
 inline int __all_sync(unsigned, int p) { return emu::all_sync(p); }
+inline int __any_sync(unsigned, int p) { return emu::any_sync(p); }
 
 typedef int cudaError_t;
 typedef void* cudaStream_t;
+enum { cudaSuccess = 0, cudaErrorInvalidValue = 1, cudaErrorMisalignedAddress = 74 };
 
 namespace emu {
+// Runs body() on every thread of one block of n threads.
 template <class F>
-void run_block(unsigned bx, unsigned by, int n, F body) {
-  std::unique_ptr<Block> blk(new Block(n));
-  std::memset(blk->tmem, 0xff, sizeof(blk->tmem));  // NaN-like poison: unwritten TMEM shows
+void run_block(unsigned bx, unsigned by, int n, F body, unsigned seed = 1) {
+  std::unique_ptr<Block> blk(new Block(n, seed));
+  std::memset(blk->tmem, 0xff, sizeof(blk->tmem));  // poison: unwritten tensor memory shows
   g_block = blk.get();
   std::vector<std::thread> ts;
   for (int t = 0; t < n; ++t)
@@ -72,6 +94,7 @@ void run_block(unsigned bx, unsigned by, int n, F body) {
     });
   for (auto& t : ts) t.join();
   if (blk->tmem_allocated) die("tensor memory not freed at the end of the block");
+  blk.reset();  // drains the engines while the block is still current
   g_block = nullptr;
 }
 }  // namespace emu

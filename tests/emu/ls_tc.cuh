@@ -3,6 +3,7 @@
 // versions; the descriptor and instruction-descriptor bit layouts are the
 // library's, so the emulator decodes exactly what the kernel encodes.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -43,10 +44,41 @@ inline uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
 }
 inline void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                    uint32_t accumulate) {
-  emu::mma_ss(d_tmem, adesc, bdesc, idesc, accumulate);
+  emu::mma(d_tmem, adesc, -1, bdesc, idesc, accumulate);
 }
-inline void mma_commit(uint32_t bar) { emu::mbar_arrive(bar); }
-inline void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) { emu::tmem_ld32(taddr, r); }
+inline void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                   uint32_t accumulate) {
+  emu::mma(d_tmem, 0, (int64_t)a_tmem, bdesc, idesc, accumulate);
+}
+inline void mma_commit(uint32_t bar) { emu::mma_commit(bar); }
+inline void mbar_arrive(uint32_t bar) { emu::mbar_arrive(bar); }
+inline void mbar_expect_tx(uint32_t bar, uint32_t bytes) { emu::mbar_expect_tx(bar, bytes); }
+inline void prefetch_tmap(const CUtensorMap*) {}
+inline void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t c0, int32_t c1) {
+  const int32_t c[2] = {c0, c1};
+  emu::tma_load(dst, m, bar, c);
+}
+inline void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t c0, int32_t c1,
+                        int32_t c2) {
+  const int32_t c[3] = {c0, c1, c2};
+  emu::tma_load(dst, m, bar, c);
+}
+inline void tma_load_4d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t c0, int32_t c1,
+                        int32_t c2, int32_t c3) {
+  const int32_t c[4] = {c0, c1, c2, c3};
+  emu::tma_load(dst, m, bar, c);
+}
+inline void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) { emu::tmem_ld(taddr, r, 32); }
+inline void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) { emu::tmem_st(taddr, r, 32); }
+inline void tmem_st16(uint32_t taddr, const uint32_t* r) { emu::tmem_st(taddr, r, 16); }
+inline void tmem_st1(uint32_t taddr, uint32_t v) { emu::tmem_st(taddr, &v, 1); }
+inline void tmem_ld1x2(uint32_t a0, uint32_t a1, uint32_t& a, uint32_t& b) {
+  emu::tmem_ld(a0, &a, 1);
+  emu::tmem_ld(a1, &b, 1);
+}
+inline void tmem_wait_ld() {}
+inline void tmem_wait_st() {}
+inline void named_bar_sync(uint32_t, uint32_t) { emu::die("named barriers are not emulated"); }
 inline void tmem_wait_ld_r(uint32_t (&)[32]) {}
 inline void reg_dep(uint32_t (&)[32]) {}
 inline uint32_t sw128_offset(uint32_t row, uint32_t chunk) {

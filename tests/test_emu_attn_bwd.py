@@ -1,0 +1,120 @@
+"""The prompt-attention backward kernel (tc_bwd_dq_tm_kernel in
+csrc/ls_tc_bwd.cu), its own source compiled for the host and run on the CPU
+block emulator (tests/emu/): TMA copies and tcgen05 MMAs run asynchronously
+on engine threads with random delays, so a missing wait or an early slot
+reuse shows as wrong data or a timeout.  Three prompt parts over a scattered,
+NaN-poisoned pool with a partial last page, plus the causal response part,
+for a GQA 12/2 group; the parts' float32 dQ, summed and scaled, must match
+the float64 oracle at the bf16 tolerance.  This checks the kernel's indexing
+and its producer / MMA / softmax protocol without a GPU."""
+import shutil
+import subprocess
+from pathlib import Path
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.ref as ref
+from long_context_grpo_replay_gb300 import inputs
+
+ROOT = Path(__file__).resolve().parents[1]
+EMU = Path(__file__).resolve().parent / "emu"
+SRC = ROOT / "long_context_grpo_replay_gb300" / "csrc" / "ls_tc_bwd.cu"
+TOL_BF16 = 2e-2
+
+
+def kernel_source(mutation=None):
+    """The default kernel's source, cut out of its file: the constants and
+    parameter block, then the kernel; host launchers left out."""
+    src = SRC.read_text()
+    if mutation:  # applied to the last occurrence: the default kernel comes last in the file
+        i = src.rindex(mutation[0])
+        src = src[:i] + mutation[1] + src[i + len(mutation[0]):]
+    pre = src[:src.index("template <int BN, int KSK, int KSV>\n__global__")]
+    body = src[src.index("struct BwdTmLayout"):src.index("cudaError_t bwd_tm(")]
+    text = pre + body + "}  // namespace\n}  // namespace ls\n"
+    text = text.replace("extern __shared__", "extern")
+    ex2 = 'asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));'
+    assert ex2 in text
+    return text.replace(ex2, "y = exp2f(x);")
+
+
+def build(d, mutation=None):
+    if shutil.which("g++") is None:
+        pytest.skip("no host C++ compiler")
+    csrc = d / "x" / "csrc"
+    csrc.mkdir(parents=True)
+    (d / "include").mkdir()
+    (csrc / "kernel.cu").write_text(kernel_source(mutation))
+    shutil.copy(SRC.parent / "ls_internal.h", csrc / "ls_internal.h")
+    shutil.copy(EMU / "ls_tc.cuh", csrc / "ls_tc.cuh")
+    shutil.copy(ROOT / "include" / "ls.h", d / "include" / "ls.h")
+    exe = d / "attn_bwd_emu"
+    r = subprocess.run(["g++", "-std=c++20", "-O2", "-pthread", "-Wno-unknown-pragmas", "-I", str(EMU),
+                        "-I", str(csrc), str(EMU / "attn_bwd_main.cpp"), "-o", str(exe)],
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    return exe
+
+
+def _bf16_bytes(t):
+    return t.to(torch.bfloat16).contiguous().view(torch.int16).numpy().tobytes()
+
+
+def run_case(exe, d, P=600, R=64, seed=5):
+    w = inputs.Workload("emu", 12, 2, 256, 256, P, (R,), "bf16", seed=seed, pool_factor=2,
+                        poison=True)
+    pr = inputs.make_prompt(w, "cpu")
+    m = inputs.make_member(w, 0, "cpu")
+    want = ref.replay_member(pr["k_pool"], pr["v_pool"], pr["page_table"], P, m["q"], m["k"], m["v"],
+                             m["d_o"], scale=w.scale)
+    span = 256
+    ns = -(-P // span)
+    kp, pt = pr["k_pool"], pr["page_table"]
+    hdr = np.array([w.hq, w.hkv, R, P, w.page_size, kp.shape[0], pt.shape[0], ns, span],
+                   dtype=np.int64)
+    with open(d / "in.bin", "wb") as f:
+        f.write(hdr.tobytes())
+        f.write(np.array([w.scale], dtype=np.float32).tobytes())
+        f.write(_bf16_bytes(kp))
+        f.write(_bf16_bytes(pr["v_pool"]))
+        f.write(pt.to(torch.int32).numpy().tobytes())
+        for x in ("q", "d_o", "k", "v"):
+            f.write(_bf16_bytes(m[x]))
+        f.write(want["lse"].astype(np.float32).tobytes())
+        f.write(want["delta"].astype(np.float32).tobytes())
+    r = subprocess.run([str(exe), str(d / "in.bin"), str(d / "out.bin")], capture_output=True,
+                       text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    out = np.fromfile(d / "out.bin", dtype=np.uint32, count=2)
+    parts = np.fromfile(d / "out.bin", dtype=np.float32, offset=8).reshape(ns + 1, R, w.hq, 256)
+    dq = parts.astype(np.float64).sum(0) * w.scale
+    return out, float(np.abs(dq - want["dq"]).max() / np.abs(want["dq"]).max())
+
+
+@pytest.fixture(scope="module")
+def emulator(tmp_path_factory):
+    d = tmp_path_factory.mktemp("emu_attn_bwd")
+    return build(d), d
+
+
+def test_emulated_backward_matches_the_oracle(emulator):
+    exe, d = emulator
+    status, err = run_case(exe, d)
+    assert status[0] == 0, status  # no bad page, no wait that gave up
+    assert err <= TOL_BF16, err
+
+
+@pytest.mark.parametrize("mutation", [
+    ("constexpr uint32_t idesc_dq = idesc_bf16(kBM, kD, true);",
+     "constexpr uint32_t idesc_dq = idesc_bf16(kBM, kD, false);"),
+    ("        if (!mbar_wait(smem_u32(&bar_dsf), j & 1, abortp)) { fail(__LINE__); break; }\n", ""),
+    ("(j > 0 || kk > 0) ? 1u : 0u);", "kk > 0 ? 1u : 0u);"),
+], ids=["K_read_K_major_in_dQ", "dQ_before_dS_is_written", "dQ_reset_every_tile"])
+def test_emulator_rejects_planted_kernel_mistakes(tmp_path, mutation):
+    """A wrong operand layout, a missing wait and a lost accumulation, each
+    planted in a copy of the kernel source, must fail the comparison."""
+    exe = build(tmp_path, mutation)
+    status, err = run_case(exe, tmp_path)
+    assert not err <= TOL_BF16, err  # also true for NaN

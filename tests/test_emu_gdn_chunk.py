@@ -34,7 +34,8 @@ def _build(d, mutation=None):
         src = src.replace(mutation[0], mutation[1], 1)
     start = src.index("gdn_chunk_fwd_kernel(")
     end = src.index("\n}  // namespace\n", start) + len("\n}  // namespace\n")
-    (d / "kernel.cu").write_text(src[:end] + "}  // namespace ls\n")
+    src = src[:end].replace("extern __shared__", "extern")
+    (d / "kernel.cu").write_text(src + "}  // namespace ls\n")
     for name in ("ls_internal.h", "ls_tc.cuh"):
         shutil.copy(EMU / name, d / name)
     exe = d / "gdn_chunk_emu"
