@@ -70,6 +70,7 @@ inline void __syncthreads() { emu::syncthreads(); }
 inline int __syncthreads_or(int p) { return emu::syncthreads_or(p); }
 inline void __syncwarp(unsigned = 0xffffffffu) { emu::syncwarp(); }
 inline float __shfl_up_sync(unsigned, float x, int off) { return emu::shfl_up(x, off); }
+inline float __shfl_xor_sync(unsigned, float x, int mask) { return emu::shfl_xor(x, mask); }
 inline int __all_sync(unsigned, int p) { return emu::all_sync(p); }
 inline int __any_sync(unsigned, int p) { return emu::any_sync(p); }
 

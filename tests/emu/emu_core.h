@@ -175,6 +175,15 @@ inline int all_sync(int p) {
   return r;
 }
 
+inline float shfl_xor(float x, int mask) {
+  Block& b = *g_block;
+  const int w = t_tid >> 5, l = t_tid & 31;
+  b.warp_f[w][l] = x;
+  b.warp_bar[w]->arrive_and_wait();
+  const float y = b.warp_f[w][l ^ mask];
+  b.warp_bar[w]->arrive_and_wait();
+  return y;
+}
 inline int any_sync(int p) {
   Block& b = *g_block;
   const int w = t_tid >> 5, l = t_tid & 31;
