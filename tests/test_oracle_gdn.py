@@ -255,3 +255,86 @@ def test_state_gradient_is_linear_across_a_chunk():
     W = np.exp(c[-1] - c)[:, None] * K
     M = gam[-1] * np.eye(dk) - W.T @ np.linalg.solve(np.eye(n) + A, np.diag(gam * b) @ K)
     np.testing.assert_allclose(dS1 - dS0, G1 @ M, atol=1e-12)
+
+
+def _cp_prep(K, Q, V, dO, g, b):
+    """Chunk-local solves of the chunk-parallel form (no state, no dL/dS):
+    E0 = T diag(b) V, ZK = T diag(b gamma) K, dU0 = T^T P^T dO, ZW = T^T W,
+    with T = (I + A)^-1."""
+    n = len(g)
+    c = np.cumsum(g)
+    gam = np.exp(c)
+    Gam = np.exp(c[:, None] - c[None, :])
+    IA = np.eye(n) + b[:, None] * np.tril(Gam * (K @ K.T), -1)
+    Pt = np.tril(Gam * (Q @ K.T)).T
+    W = np.exp(c[-1] - c)[:, None] * K
+    return (np.linalg.solve(IA, b[:, None] * V), np.linalg.solve(IA, (b * gam)[:, None] * K),
+            np.linalg.solve(IA.T, Pt @ dO), np.linalg.solve(IA.T, W))
+
+
+def _chunk_parallel(s0, q, k, v, g, b, d_o, C):
+    """The replay and its gradients in three stages: chunk-local solves (all
+    chunks independent), then the two linear chains over the chunks (the state
+    forward, E = E0 - ZK S^T, S <- gamma_C S + E^T W; dL/dS backward,
+    dU = dU0 + ZW G^T, G <- gamma_C G + (gamma dO)^T Q - (gamma b dU)^T K),
+    then every output chunk by chunk from its starting state, its final dL/dS,
+    E and dU (independent again)."""
+    R = len(g)
+    chunks = [(a, min(R, a + C)) for a in range(0, R, C)]
+    pre = [_cp_prep(k[a:e], q[a:e], v[a:e], d_o[a:e], g[a:e], b[a:e]) for a, e in chunks]
+    S, S_start, E = s0.copy(), [], []
+    for (a, e), (E0, ZK, _, _) in zip(chunks, pre):
+        S_start.append(S)
+        c = np.cumsum(g[a:e])
+        E.append(E0 - ZK @ S.T)
+        S = np.exp(c[-1]) * S + E[-1].T @ (np.exp(c[-1] - c)[:, None] * k[a:e])
+    out = {"s_final": S}
+    G, G_end, dU = np.zeros_like(S), [None] * len(chunks), [None] * len(chunks)
+    for ci in reversed(range(len(chunks))):
+        a, e = chunks[ci]
+        G_end[ci] = G
+        c = np.cumsum(g[a:e])
+        gam = np.exp(c)
+        dU[ci] = pre[ci][2] + pre[ci][3] @ G.T
+        G = np.exp(c[-1]) * G + (gam[:, None] * d_o[a:e]).T @ q[a:e] - \
+            ((gam * b[a:e])[:, None] * dU[ci]).T @ k[a:e]
+    res = {x: np.zeros_like(t) for x, t in (("o", v), ("dq", q), ("dk", k), ("dv", v),
+                                             ("dg", g), ("dbeta", b))}
+    for ci, (a, e) in enumerate(chunks):
+        S0, Gc, Ec, dUc = S_start[ci], G_end[ci], E[ci], dU[ci]
+        Q, K, V, dO, gg, bb = q[a:e], k[a:e], v[a:e], d_o[a:e], g[a:e], b[a:e]
+        n = e - a
+        c = np.cumsum(gg)
+        gam, w = np.exp(c), np.exp(c[-1] - c)
+        Gam = np.exp(c[:, None] - c[None, :])
+        L = np.tril(np.ones((n, n)))
+        P = L * Gam * (Q @ K.T)
+        GK = np.tril(Gam * (K @ K.T), -1)
+        dP, dW = dO @ Ec.T, Ec @ Gc
+        LdP = L * Gam * dP
+        dA = -np.tril(dUc @ Ec.T, -1)
+        Msym = dA * bb[:, None] * Gam
+        Msym = Msym + Msym.T
+        res["o"][a:e] = gam[:, None] * (Q @ S0.T) + P @ Ec
+        res["dq"][a:e] = gam[:, None] * (dO @ S0) + LdP @ K
+        res["dk"][a:e] = LdP.T @ Q + Msym @ K - ((gam * bb)[:, None] * dUc) @ S0 + w[:, None] * dW
+        res["dv"][a:e] = bb[:, None] * dUc
+        res["dbeta"][a:e] = (dA * GK).sum(1) + (dUc * (V - gam[:, None] * (K @ S0.T))).sum(1)
+        dgam = (dO * (Q @ S0.T)).sum(1) - (bb[:, None] * dUc * (K @ S0.T)).sum(1)
+        r = dP * P + dA * bb[:, None] * GK
+        rw = (dW * K).sum(1) * w
+        dc = dgam * gam + r.sum(1) - r.sum(0) - rw
+        dc[-1] += rw.sum() + (Gc * S0).sum() * gam[-1]
+        res["dg"][a:e] = np.cumsum(dc[::-1])[::-1]
+    out.update(res)
+    return out
+
+
+@pytest.mark.parametrize("C", [1, 4, 8, 23])
+def test_chunk_parallel_form_equals_the_oracle(C):
+    s0, q, k, v, g, b, d_o = _case(H=1, dk=6, dv=5, R=23, seed=2, unit_k=False)
+    want = gdn_replay(s0, q, k, v, g, b, d_o)
+    got = _chunk_parallel(s0[0], q[:, 0], k[:, 0], v[:, 0], g[:, 0], b[:, 0], d_o[:, 0], C)
+    for x in ("o", "dq", "dk", "dv", "dg", "dbeta"):
+        np.testing.assert_allclose(got[x], want[x][:, 0], atol=1e-10, err_msg=x)
+    np.testing.assert_allclose(got["s_final"], want["s_final"][0], atol=1e-10)
