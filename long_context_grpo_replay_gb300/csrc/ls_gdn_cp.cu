@@ -1,0 +1,258 @@
+// Gated-DeltaNet replay in chunk-parallel form (forward and backward).
+//
+// With chunks of C = 128 tokens, per chunk: c_t the running sum of the
+// log-decays, gamma_t = exp(c_t), Gamma_ts = exp(c_t - c_s), w_t = gamma_C /
+// gamma_t, GK = strict_lower(Gamma . K K^T), A = diag(b) GK, T = (I + A)^-1,
+// P = lower(Gamma . Q K^T), W = diag(w) K.  The replay is three stages:
+//   prep  (all chunks at once): E0 = T diag(b) V, ZK = T diag(b gamma) K,
+//         dU0 = T^T P^T dO, ZW = T^T W         (the only triangular solves)
+//   chain (per head and member, over the chunks):
+//         state forward   E = E0 - ZK S^T,  S <- gamma_C S + E^T W
+//         dL/dS backward  dU = dU0 + ZW G^T, G <- gamma_C G + (gamma dO)^T Q - (gamma b dU)^T K
+//   out   (all chunks at once): o = diag(gamma) Q S^T + P E and the gradients
+//         of q, k, v, g, b from S, G, E and dU of the chunk.
+// The chains carry only two 128 x 128 products per chunk; everything else is
+// parallel over chunks.  Products are tcgen05.mma on bf16 operands with fp32
+// accumulators; solves and states are fp32.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ls_gdn_tiles.cuh"
+#include "ls_internal.h"
+
+namespace ls {
+namespace {
+using namespace gdn;
+
+// float32 scratch per (member, head, chunk): the [128 x 128] blocks below,
+// then the packed GK.
+enum : int { kE0 = 0, kZK, kDU0, kZW, kEblk, kDUblk, kSstart, kGend, kGKblk, kScrBlocks };
+constexpr int64_t kScrFloats = (int64_t)kScrBlocks * kTileElems;
+
+__device__ __forceinline__ float* scratch_of(float* scr, int H, int nch, int m, int h, int ch) {
+  return scr + (((int64_t)m * H + h) * nch + ch) * kScrFloats;
+}
+
+// Cumulative log-decay and write strength of the chunk's tokens into sc[],
+// sbt[] (zero past the response); swt[4] is scan scratch.  All threads.
+__device__ __forceinline__ void stage_gates(const float* g, const float* beta, int64_t t0, int nt,
+                                            int H, int h, float* sc, float* sbt, float* swt) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float x = 0.f;
+  if (tid < nt) {
+    x = g[(t0 + tid) * H + h];
+    sbt[tid] = beta[(t0 + tid) * H + h];
+  } else {
+    sbt[tid] = 0.f;
+  }
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) swt[warp] = x;
+  __syncthreads();
+  for (int w = 0; w < warp; ++w) x += swt[w];
+  sc[tid] = x;
+}
+
+// Forward substitution (I + diag(b) GK) y = rhs on column x of the fp32
+// buffer buf (in place), rows 0..nt8-1, eight rows at a time.
+__device__ __forceinline__ void solve_lower(float* buf, const float* gk, const float* sbt, int nt8,
+                                            int x) {
+  for (int t8 = 0; t8 < nt8; t8 += 8) {
+    float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < t8; ++s) {
+      const float e = buf[u_at(s, x)];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) sum[u] = fmaf(gk[a_at(t8 + u, s)], e, sum[u]);
+    }
+    float ev[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+#pragma unroll
+      for (int u2 = 0; u2 < u; ++u2) sum[u] = fmaf(gk[a_at(t8 + u, t8 + u2)], ev[u2], sum[u]);
+      ev[u] = fmaf(-sbt[t8 + u], sum[u], buf[u_at(t8 + u, x)]);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) buf[u_at(t8 + u, x)] = ev[u];
+  }
+}
+// Backward substitution (I + diag(b) GK)^T y = rhs on column x, in place.
+__device__ __forceinline__ void solve_upper(float* buf, const float* gk, const float* sbt, int nt8,
+                                            int x) {
+  for (int t8 = nt8 - 8; t8 >= 0; t8 -= 8) {
+    float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s = t8 + 8; s < nt8; ++s) {
+      const float e = sbt[s] * buf[u_at(s, x)];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) sum[u] = fmaf(gk[a_at(s, t8 + u)], e, sum[u]);
+    }
+    float ev[8];
+#pragma unroll
+    for (int u = 7; u >= 0; --u) {
+#pragma unroll
+      for (int u2 = 7; u2 > u; --u2) sum[u] = fmaf(gk[a_at(t8 + u2, t8 + u)], sbt[t8 + u2] * ev[u2], sum[u]);
+      ev[u] = buf[u_at(t8 + u, x)] - sum[u];
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) buf[u_at(t8 + u, x)] = ev[u];
+  }
+}
+
+// ---------------------------------------------------------------- prep
+// One CTA per (chunk, head, member).
+constexpr uint32_t kPrepK = 0, kPrepQ = kTile, kPrepDO = 2 * kTile, kPrepGK = 3 * kTile;
+constexpr uint32_t kPrepU = 4 * kTile, kPrepMisc = 6 * kTile;
+constexpr uint32_t kPrepSmem = kPrepMisc + 2048 + 1024;
+
+__global__ void __launch_bounds__(kThr, 1)
+    gdn_cp_prep_kernel(int H, int R, int nch, const float* __restrict__ q,
+                       const float* __restrict__ k, const float* __restrict__ v,
+                       const float* __restrict__ g, const float* __restrict__ beta,
+                       const float* __restrict__ d_o, float* __restrict__ scr,
+                       uint32_t* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(sm);
+  float* gk = reinterpret_cast<float*>(sm + kPrepGK);
+  float* buf = reinterpret_cast<float*>(sm + kPrepU);
+  float* sc = reinterpret_cast<float*>(sm + kPrepMisc);
+  float* sbt = sc + kC;
+  float* swt = sbt + kC;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kPrepMisc + 1536);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
+  uint32_t* abort_s = tslot + 1;
+
+  const int ch = blockIdx.x, h = blockIdx.y, m = blockIdx.z, tid = threadIdx.x, warp = tid >> 5;
+  const int64_t t0 = (int64_t)ch * kC;
+  const int nt = R - t0 < kC ? (int)(R - t0) : kC, nt8 = (nt + 7) & ~7;
+  {
+    const int64_t tok = (int64_t)m * R * H;
+    q += tok * kD, k += tok * kD, v += tok * kD, d_o += tok * kD, g += tok, beta += tok;
+  }
+  float* out = scratch_of(scr, H, nch, m, h, ch);
+  if (tid == 0) {
+    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    *abort_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tslot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = *tslot, lane_off = (uint32_t)(warp * 32) << 16;
+  const volatile uint32_t* abortp = abort_s;
+  const int64_t rs = (int64_t)H * kD;  // token stride of q, k, v, d_o
+
+  stage_rows(sb + kPrepK, k + (t0 * H + h) * kD, rs, nt, nullptr);
+  stage_rows(sb + kPrepQ, q + (t0 * H + h) * kD, rs, nt, nullptr);
+  stage_rows(sb + kPrepDO, d_o + (t0 * H + h) * kD, rs, nt, nullptr);
+  stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  if (tid == 0) {  // K K^T -> cols 0..127, K Q^T -> 128..255
+    tc_fence_after();
+    mma_group(tb + 0, sb + kPrepK, sb + kPrepK, false, false);
+    mma_group(tb + 128, sb + kPrepK, sb + kPrepQ, false, false);
+    mma_commit(smem_u32(&bars[0]));
+  }
+  bool ok = mbar_wait_warp(smem_u32(&bars[0]), 0, abortp);
+  if (!__syncthreads_or(!ok)) {
+    tc_fence_after();
+    // thread r: GK row r (s < r); P^T row r: P^T[r][t] = [t >= r] Gamma_tr (K_r . Q_t)
+    const int r = tid;
+    const float cr = sc[r];
+    float* gko = out + (int64_t)kGKblk * kTileElems;
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+      uint32_t t32[32];
+      tmem_ld32(tb + lane_off + 0 + cb * 32, t32);
+      tmem_wait_ld_r(t32);
+#pragma unroll
+      for (int xx = 0; xx < 32; ++xx) {
+        const int s = cb * 32 + xx;
+        if (s < r) {
+          const float val = expf(cr - sc[s]) * __uint_as_float(t32[xx]);
+          gk[a_at(r, s)] = val;
+          gko[a_at(r, s)] = val;
+        }
+      }
+      tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
+      tmem_wait_ld_r(t32);
+      float pv[32];
+#pragma unroll
+      for (int xx = 0; xx < 32; ++xx) {
+        const int t = cb * 32 + xx;
+        pv[xx] = t >= r ? expf(sc[t] - cr) * __uint_as_float(t32[xx]) : 0.f;
+      }
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) st_shared_v4(sb + kPrepQ + tile_off(r, cb * 4 + gg), pack8(&pv[8 * gg]));
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {  // dE0 = P^T dO -> cols 256..383 (dO as an N-major B)
+      tc_fence_after();
+      mma_group(tb + 256, sb + kPrepQ, sb + kPrepDO, true, false);
+      mma_commit(smem_u32(&bars[1]));
+    }
+    // forward solves, thread x = column x: E0 from b V, ZK from b gamma K
+    const int x = tid;
+    for (int which = 0; which < 2; ++which) {
+      const float* src = which == 0 ? v : k;
+      for (int t = 0; t < kC; ++t) {
+        float val = 0.f;
+        if (t < nt) val = sbt[t] * src[(t0 + t) * rs + h * kD + x] * (which == 0 ? 1.f : expf(sc[t]));
+        buf[u_at(t, x)] = val;
+      }
+      solve_lower(buf, gk, sbt, nt8, x);
+      float* dst = out + (int64_t)(which == 0 ? kE0 : kZK) * kTileElems;
+      for (int t = 0; t < kC; ++t) dst[t * kD + x] = buf[u_at(t, x)];
+    }
+    ok = mbar_wait_warp(smem_u32(&bars[1]), 0, abortp);
+    if (!__syncthreads_or(!ok)) {
+      tc_fence_after();
+      // backward solves: dU0 from dE0 (rows from tensor memory), ZW from w K
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t t32[32];
+        tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
+        tmem_wait_ld_r(t32);
+#pragma unroll
+        for (int xx = 0; xx < 32; ++xx) buf[u_at(r, cb * 32 + xx)] = __uint_as_float(t32[xx]);
+      }
+      __syncthreads();
+      solve_upper(buf, gk, sbt, nt8, x);
+      float* dst = out + (int64_t)kDU0 * kTileElems;
+      for (int t = 0; t < kC; ++t) dst[t * kD + x] = buf[u_at(t, x)];
+      const float clast = sc[kC - 1];
+      for (int t = 0; t < kC; ++t)
+        buf[u_at(t, x)] = t < nt ? expf(clast - sc[t]) * k[(t0 + t) * rs + h * kD + x] : 0.f;
+      solve_upper(buf, gk, sbt, nt8, x);
+      dst = out + (int64_t)kZW * kTileElems;
+      for (int t = 0; t < kC; ++t) dst[t * kD + x] = buf[u_at(t, x)];
+    }
+  }
+  if (__syncthreads_or(!ok) && tid == 0 && status) atomicOr(status, kStatusTimeout);
+  if (tid == 0) {  // drain before tensor memory is freed
+    mma_commit(smem_u32(&bars[2]));
+    mbar_wait(smem_u32(&bars[2]), 0, abortp);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tb, 512);
+  }
+}
+
+}  // namespace
+}  // namespace ls

@@ -1,0 +1,82 @@
+// Tile helpers of the chunkwise gated-DeltaNet kernels: [128 x 128] bf16
+// operand tiles in the 128-byte-swizzled K-major layout (two [128 x 64]
+// boxes), their shared-memory descriptors, staging from float32 rows, and
+// 128 x 128 x 128 tcgen05.mma groups.  One CTA of 128 threads.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ls_tc.cuh"
+
+namespace ls {
+namespace gdn {
+using namespace tc;
+
+constexpr int kC = 128;   // tokens per chunk: the MMAs' M
+constexpr int kD = 128;   // dk = dv
+constexpr int kThr = 128;
+constexpr uint32_t kBox = kC * 128;   // [128 rows x 64 bf16] box
+constexpr uint32_t kTile = 2 * kBox;  // [128 x 128] tile
+constexpr int kTileElems = kC * kD;   // also the float32 [128 x 128] block of a chunk
+
+__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int kk) {  // K-major, K step kk of 16
+  return sdesc_sw128(tile + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t mndesc(uint32_t tile, int kk) {  // N-major B: K rows 16kk..
+  return sdesc_sw128(tile + kk * 16 * 128, kBox, 1024);
+}
+// byte offset of the 16-byte group gq (columns 8gq .. 8gq+7) of row r
+__device__ __forceinline__ uint32_t tile_off(int r, int gq) {
+  return (gq >> 3) * kBox + sw128_offset(r, gq & 7);
+}
+// byte offset of element (r, c)
+__device__ __forceinline__ uint32_t elem_off(int r, int c) { return tile_off(r, c >> 3) + (c & 7) * 2; }
+__device__ __forceinline__ uint4 pack8(const float* x) {
+  return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                    pack_bf16x2(x[6], x[7]));
+}
+__device__ __forceinline__ uint16_t bf16_of(float x) { return (uint16_t)(pack_bf16x2(x, 0.f) & 0xffffu); }
+
+// Rows 0..nt-1 of a float32 matrix (row r at src + r * stride, 128 columns)
+// into a tile, each row times scale[r] when scale is given; rows nt..127 zero.
+// All threads.
+__device__ __forceinline__ void stage_rows(uint32_t tile, const float* src, int64_t stride, int nt,
+                                           const float* scale) {
+  const int tid = threadIdx.x;
+#pragma unroll 4
+  for (int it = 0; it < 16; ++it) {
+    const int item = tid + kThr * it, r = item >> 4, gq = item & 15;
+    uint4 pk = make_uint4(0u, 0u, 0u, 0u);
+    if (r < nt) {
+      const float4* p = reinterpret_cast<const float4*>(src + r * stride + gq * 8);
+      const float4 a = p[0], b = p[1];
+      const float f = scale ? scale[r] : 1.f;
+      const float x[8] = {a.x * f, a.y * f, a.z * f, a.w * f, b.x * f, b.y * f, b.z * f, b.w * f};
+      pk = pack8(x);
+    }
+    st_shared_v4(tile + tile_off(r, gq), pk);
+  }
+}
+// One row of a tile from 128 registers (thread = row).
+__device__ __forceinline__ void stage_row_regs(uint32_t tile, int r, const float (&x)[kD]) {
+#pragma unroll
+  for (int gq = 0; gq < 16; ++gq) st_shared_v4(tile + tile_off(r, gq), pack8(&x[8 * gq]));
+}
+// D[tmem] (+)= A B^T over K = 128 (eight K steps); B K-major or N-major.
+__device__ __forceinline__ void mma_group(uint32_t d, uint32_t a, uint32_t b, bool b_mn, bool acc) {
+  const uint32_t id = idesc_bf16(128, 128, b_mn);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ss(d, kdesc(a, kk), b_mn ? mndesc(b, kk) : kdesc(b, kk), id, (acc || kk > 0) ? 1u : 0u);
+}
+// fp32 [128 x 128] shared buffer, columns XOR-swizzled by the row: row
+// writes (thread = row) and column reads (thread = column) are both free of
+// bank conflicts.
+__device__ __forceinline__ int u_at(int t, int j) { return t * kD + (j ^ (t & 31)); }
+// packed strict lower triangle
+__device__ __forceinline__ int a_at(int t, int s) { return t * (t - 1) / 2 + s; }
+
+}  // namespace gdn
+}  // namespace ls

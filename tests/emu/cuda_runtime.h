@@ -98,4 +98,9 @@ void run_block(unsigned bx, unsigned by, int n, F body, unsigned seed = 1) {
   blk.reset();  // drains the engines while the block is still current
   g_block = nullptr;
 }
+// The same for a block with a three-dimensional index.
+template <class F>
+void run_block3(unsigned bx, unsigned by, unsigned bz, int n, F body, unsigned seed = 1) {
+  run_block(bx, by, n, [&] { blockIdx.z = bz; body(); }, seed);
+}
 }  // namespace emu

@@ -94,6 +94,7 @@ inline uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 inline void st_shared_v4(uint32_t addr, uint4 v) { std::memcpy(emu::smem_ptr(addr, 16), &v, 16); }
+inline void st_shared_u16(uint32_t addr, uint16_t v) { std::memcpy(emu::smem_ptr(addr, 2), &v, 2); }
 
 }  // namespace tc
 }  // namespace ls

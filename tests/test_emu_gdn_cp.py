@@ -1,0 +1,94 @@
+"""The chunk-parallel GDN kernels (csrc/ls_gdn_cp.cu), their own source
+compiled for the host and run on the CPU block emulator (tests/emu/), stage
+by stage against the float64 chunk-parallel reference of
+tests/test_oracle_gdn.py (itself pinned to the oracle), at the bf16
+tolerance of their tensor-core products."""
+import shutil
+import subprocess
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+from long_context_grpo_replay_gb300 import inputs
+from test_oracle_gdn import _cp_prep
+
+ROOT = Path(__file__).resolve().parents[1]
+EMU = Path(__file__).resolve().parent / "emu"
+CSRC = ROOT / "long_context_grpo_replay_gb300" / "csrc"
+SRC = CSRC / "ls_gdn_cp.cu"
+TOL_BF16 = 2e-2
+SCR_BLOCKS = 9  # E0, ZK, dU0, ZW, E, dU, S_start, G_end, GK
+
+
+def build(d):
+    if shutil.which("g++") is None:
+        pytest.skip("no host C++ compiler")
+    src = SRC.read_text()
+    end = src.index("\n}  // namespace\n}  // namespace ls") + len("\n}  // namespace\n")
+    text = src[:end] + "}  // namespace ls\n" + (EMU / "gdn_cp_run.inc").read_text()
+    text = text.replace("extern __shared__", "extern")
+    csrc = d / "x" / "csrc"
+    csrc.mkdir(parents=True)
+    (d / "include").mkdir()
+    (csrc / "kernel.cu").write_text(text)
+    shutil.copy(CSRC / "ls_internal.h", csrc / "ls_internal.h")
+    shutil.copy(CSRC / "ls_gdn_tiles.cuh", csrc / "ls_gdn_tiles.cuh")
+    shutil.copy(EMU / "ls_tc.cuh", csrc / "ls_tc.cuh")
+    shutil.copy(ROOT / "include" / "ls.h", d / "include" / "ls.h")
+    exe = d / "gdn_cp_emu"
+    r = subprocess.run(["g++", "-std=c++20", "-O2", "-pthread", "-Wno-unknown-pragmas", "-I", str(EMU),
+                        "-I", str(csrc), str(EMU / "gdn_cp_main.cpp"), "-o", str(exe)],
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    return exe
+
+
+def run(exe, d, c, stage):
+    B, R, H, _ = c["q"].shape
+    with open(d / "in.bin", "wb") as f:
+        np.array([B, H, R], dtype=np.int32).tofile(f)
+        for x in ("s0", "q", "k", "v", "d_o", "g", "beta"):
+            c[x].numpy().astype(np.float32).tofile(f)
+    r = subprocess.run([str(exe), stage, str(d / "in.bin"), str(d / "out.bin")], capture_output=True,
+                       text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    nch = -(-R // 128)
+    out = np.fromfile(d / "out.bin", dtype=np.float32, offset=4)
+    n_scr = B * H * nch * SCR_BLOCKS * 128 * 128
+    status = int(np.fromfile(d / "out.bin", dtype=np.uint32, count=1)[0])
+    scr = out[:n_scr].reshape(B, H, nch, SCR_BLOCKS, 128, 128)
+    return status, scr, out[n_scr:]
+
+
+@pytest.fixture(scope="module")
+def emulator(tmp_path_factory):
+    d = tmp_path_factory.mktemp("emu_gdn_cp")
+    return build(d), d
+
+
+def rel(a, b):
+    return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-30))
+
+
+def test_prep_solves_match_the_reference(emulator):
+    exe, d = emulator
+    B, H, R = 1, 2, 200  # two chunks, the second partial
+    c = inputs.make_gdn_group(B, H, R, seed=31)
+    status, scr, _ = run(exe, d, c, "prep")
+    assert status == 0
+    a = {x: t.numpy().astype(np.float64) for x, t in c.items()}
+    errs = []
+    for h in range(H):
+        for ch, (t0, t1) in enumerate([(0, 128), (128, 200)]):
+            sl = slice(t0, t1)
+            want = _cp_prep(a["k"][0, sl, h], a["q"][0, sl, h], a["v"][0, sl, h], a["d_o"][0, sl, h],
+                            a["g"][0, sl, h], a["beta"][0, sl, h])
+            n = t1 - t0
+            for blk, w in zip(range(4), want):
+                got = scr[0, h, ch, blk, :n]
+                errs.append(rel(got, w))
+                assert rel(got, w) <= TOL_BF16, (h, ch, blk, rel(got, w))
+                if n < 128:
+                    assert np.abs(scr[0, h, ch, blk, n:]).max() == 0.0  # rows past the response
+    print("prep max rel err", max(errs))
