@@ -254,5 +254,232 @@ __global__ void __launch_bounds__(kThr, 1)
   }
 }
 
+// ---------------------------------------------------------------- chain
+// One CTA per (head, member), sequential over the chunks: the state forward,
+// then dL/dS backward.  Per chunk it writes S at the chunk's start, G at its
+// end, E and dU into the scratch.
+constexpr uint32_t kChT0 = 0, kChT1 = kTile, kChT2 = 2 * kTile, kChT3 = 3 * kTile;
+constexpr uint32_t kChT4 = 4 * kTile, kChT5 = 5 * kTile, kChMisc = 6 * kTile;
+constexpr uint32_t kChainSmem = kChMisc + 2048 + 1024;
+
+__global__ void __launch_bounds__(kThr, 1)
+    gdn_cp_chain_kernel(int H, int R, int nch, const float* __restrict__ s0,
+                        const float* __restrict__ q, const float* __restrict__ k,
+                        const float* __restrict__ g, const float* __restrict__ beta,
+                        const float* __restrict__ d_o, float* __restrict__ scr,
+                        float* __restrict__ s_final, uint32_t* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(sm);
+  float* sc = reinterpret_cast<float*>(sm + kChMisc);
+  float* sbt = sc + kC;
+  float* swt = sbt + kC;
+  float* sw = swt + 4;  // w_t (state pass) or gamma_t (gradient pass), zero past the response
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kChMisc + 1536);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
+  uint32_t* abort_s = tslot + 1;
+
+  const int h = blockIdx.x, m = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+  {
+    const int64_t tok = (int64_t)m * R * H;
+    q += tok * kD, k += tok * kD, d_o += tok * kD, g += tok, beta += tok;
+  }
+  if (tid == 0) {
+    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    *abort_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tslot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = *tslot, lane_off = (uint32_t)(warp * 32) << 16;
+  const volatile uint32_t* abortp = abort_s;
+  const int64_t rs = (int64_t)H * kD;
+  const int x = tid;  // state row i / token row t / column, by phase
+  uint32_t n0 = 0, n1 = 0;  // completed phases of bars[0], bars[1]
+  bool ok = true;
+
+  float st[kD];  // S (state pass), then G (gradient pass): row x, fp32
+  {
+    const float* src = s0 + ((int64_t)h * kD + x) * kD;
+#pragma unroll
+    for (int c = 0; c < kD; ++c) st[c] = src[c];
+  }
+  // ---- state forward
+  for (int ch = 0; ok && ch < nch; ++ch) {
+    const int64_t t0 = (int64_t)ch * kC;
+    const int nt = R - t0 < kC ? (int)(R - t0) : kC;
+    float* blk = scratch_of(scr, H, nch, m, h, ch);
+    {
+      float* dst = blk + (int64_t)kSstart * kTileElems + x * kD;
+#pragma unroll
+      for (int c = 0; c < kD; ++c) dst[c] = st[c];
+    }
+    stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
+    __syncthreads();
+    sw[x] = x < nt ? expf(sc[kC - 1] - sc[x]) : 0.f;
+    __syncthreads();
+    stage_row_regs(sb + kChT0, x, st);                                         // S (bf16)
+    stage_rows(sb + kChT1, blk + (int64_t)kZK * kTileElems, kD, kC, nullptr);  // ZK
+    stage_rows(sb + kChT2, k + (t0 * H + h) * kD, rs, nt, sw);                 // W = diag(w) K
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {  // ZK S^T -> cols 0..127
+      tc_fence_after();
+      mma_group(tb + 0, sb + kChT1, sb + kChT0, false, false);
+      mma_commit(smem_u32(&bars[0]));
+    }
+    ok = mbar_wait_warp(smem_u32(&bars[0]), n0++ & 1, abortp);
+    if (__syncthreads_or(!ok)) break;
+    tc_fence_after();
+    {  // E row x = E0 row x - (ZK S^T) row x; E^T column x as bf16
+      const float* e0 = blk + (int64_t)kE0 * kTileElems + x * kD;
+      float* eo = blk + (int64_t)kEblk * kTileElems + x * kD;
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t t32[32];
+        tmem_ld32(tb + lane_off + cb * 32, t32);
+        tmem_wait_ld_r(t32);
+#pragma unroll
+        for (int xx = 0; xx < 32; ++xx) {
+          const int i = cb * 32 + xx;
+          const float e = e0[i] - __uint_as_float(t32[xx]);
+          eo[i] = e;
+          st_shared_u16(sb + kChT3 + elem_off(i, x), bf16_of(e));
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {  // E^T W -> cols 128..255 (W as an N-major B)
+      tc_fence_after();
+      mma_group(tb + 128, sb + kChT3, sb + kChT2, true, false);
+      mma_commit(smem_u32(&bars[1]));
+    }
+    ok = mbar_wait_warp(smem_u32(&bars[1]), n1++ & 1, abortp);
+    if (__syncthreads_or(!ok)) break;
+    tc_fence_after();
+    {
+      const float gl = expf(sc[kC - 1]);
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t t32[32];
+        tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
+        tmem_wait_ld_r(t32);
+#pragma unroll
+        for (int xx = 0; xx < 32; ++xx) st[cb * 32 + xx] = fmaf(gl, st[cb * 32 + xx], __uint_as_float(t32[xx]));
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+  if (ok && s_final) {
+    float* dst = s_final + (((int64_t)m * H + h) * kD + x) * kD;
+#pragma unroll
+    for (int c = 0; c < kD; ++c) dst[c] = st[c];
+  }
+  // ---- dL/dS backward
+#pragma unroll
+  for (int c = 0; c < kD; ++c) st[c] = 0.f;
+  for (int ch = nch - 1; ok && ch >= 0; --ch) {
+    const int64_t t0 = (int64_t)ch * kC;
+    const int nt = R - t0 < kC ? (int)(R - t0) : kC;
+    float* blk = scratch_of(scr, H, nch, m, h, ch);
+    {
+      float* dst = blk + (int64_t)kGend * kTileElems + x * kD;
+#pragma unroll
+      for (int c = 0; c < kD; ++c) dst[c] = st[c];
+    }
+    stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
+    __syncthreads();
+    sw[x] = expf(sc[x]);
+    __syncthreads();
+    stage_row_regs(sb + kChT0, x, st);                                         // G (bf16)
+    stage_rows(sb + kChT1, blk + (int64_t)kZW * kTileElems, kD, kC, nullptr);  // ZW
+    stage_rows(sb + kChT2, q + (t0 * H + h) * kD, rs, nt, nullptr);            // Q
+    stage_rows(sb + kChT3, k + (t0 * H + h) * kD, rs, nt, nullptr);            // K
+#pragma unroll 4
+    for (int gq = 0; gq < 16; ++gq) {  // (gamma dO)^T row x (tokens along K)
+      float f8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int t = 8 * gq + u;
+        f8[u] = t < nt ? sw[t] * d_o[(t0 + t) * rs + h * kD + x] : 0.f;
+      }
+      st_shared_v4(sb + kChT4 + tile_off(x, gq), pack8(f8));
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {  // ZW G^T -> cols 0..127
+      tc_fence_after();
+      mma_group(tb + 0, sb + kChT1, sb + kChT0, false, false);
+      mma_commit(smem_u32(&bars[0]));
+    }
+    ok = mbar_wait_warp(smem_u32(&bars[0]), n0++ & 1, abortp);
+    if (__syncthreads_or(!ok)) break;
+    tc_fence_after();
+    {  // dU row x = dU0 row x + (ZW G^T) row x; -(gamma b dU)^T column x as bf16
+      const float* u0 = blk + (int64_t)kDU0 * kTileElems + x * kD;
+      float* uo = blk + (int64_t)kDUblk * kTileElems + x * kD;
+      const float f = -sw[x] * sbt[x];
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t t32[32];
+        tmem_ld32(tb + lane_off + cb * 32, t32);
+        tmem_wait_ld_r(t32);
+#pragma unroll
+        for (int xx = 0; xx < 32; ++xx) {
+          const int i = cb * 32 + xx;
+          const float du = u0[i] + __uint_as_float(t32[xx]);
+          uo[i] = du;
+          st_shared_u16(sb + kChT5 + elem_off(i, x), bf16_of(f * du));
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {  // (gamma dO)^T Q - (gamma b dU)^T K -> cols 128..255
+      tc_fence_after();
+      mma_group(tb + 128, sb + kChT4, sb + kChT2, true, false);
+      mma_group(tb + 128, sb + kChT5, sb + kChT3, true, true);
+      mma_commit(smem_u32(&bars[1]));
+    }
+    ok = mbar_wait_warp(smem_u32(&bars[1]), n1++ & 1, abortp);
+    if (__syncthreads_or(!ok)) break;
+    tc_fence_after();
+    {
+      const float gl = expf(sc[kC - 1]);
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t t32[32];
+        tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
+        tmem_wait_ld_r(t32);
+#pragma unroll
+        for (int xx = 0; xx < 32; ++xx) st[cb * 32 + xx] = fmaf(gl, st[cb * 32 + xx], __uint_as_float(t32[xx]));
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+  if (!ok && tid == 0 && status) atomicOr(status, kStatusTimeout);
+  if (tid == 0) {
+    mma_commit(smem_u32(&bars[2]));
+    mbar_wait(smem_u32(&bars[2]), 0, abortp);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tb, 512);
+  }
+}
+
 }  // namespace
 }  // namespace ls

@@ -92,3 +92,52 @@ def test_prep_solves_match_the_reference(emulator):
                 if n < 128:
                     assert np.abs(scr[0, h, ch, blk, n:]).max() == 0.0  # rows past the response
     print("prep max rel err", max(errs))
+
+
+def _chains(s0, q, k, v, g, b, d_o):
+    """float64 reference of the two chains over chunks of 128: S at each
+    chunk's start, E, G at each chunk's end, dU, and the final state."""
+    R = len(g)
+    chunks = [(a, min(R, a + 128)) for a in range(0, R, 128)]
+    pre = [_cp_prep(k[a:e], q[a:e], v[a:e], d_o[a:e], g[a:e], b[a:e]) for a, e in chunks]
+    S, S_start, E = s0.copy(), [], []
+    for (a, e), (E0, ZK, _, _) in zip(chunks, pre):
+        S_start.append(S)
+        c = np.cumsum(g[a:e])
+        E.append(E0 - ZK @ S.T)
+        S = np.exp(c[-1]) * S + E[-1].T @ (np.exp(c[-1] - c)[:, None] * k[a:e])
+    G, G_end, dU = np.zeros_like(S), [None] * len(chunks), [None] * len(chunks)
+    for ci in reversed(range(len(chunks))):
+        a, e = chunks[ci]
+        G_end[ci] = G
+        c = np.cumsum(g[a:e])
+        gam = np.exp(c)
+        dU[ci] = pre[ci][2] + pre[ci][3] @ G.T
+        G = np.exp(c[-1]) * G + (gam[:, None] * d_o[a:e]).T @ q[a:e] - \
+            ((gam * b[a:e])[:, None] * dU[ci]).T @ k[a:e]
+    return S_start, E, G_end, dU, S
+
+
+def test_chains_match_the_reference(emulator):
+    exe, d = emulator
+    B, H, R = 2, 1, 300  # three chunks, the last partial; two members share s0
+    c = inputs.make_gdn_group(B, H, R, seed=32)
+    status, scr, _ = run(exe, d, c, "all")
+    assert status == 0
+    a = {x: t.numpy().astype(np.float64) for x, t in c.items()}
+    errs = {}
+    for m in range(B):
+        S_start, E, G_end, dU, S_fin = _chains(a["s0"][0], a["q"][m, :, 0], a["k"][m, :, 0],
+                                               a["v"][m, :, 0], a["g"][m, :, 0], a["beta"][m, :, 0],
+                                               a["d_o"][m, :, 0])
+        for ch in range(3):
+            n = min(128, R - 128 * ch)
+            for name, blk, want in (("S_start", 6, S_start[ch]), ("E", 4, E[ch][:n]),
+                                    ("G_end", 7, G_end[ch]), ("dU", 5, dU[ch][:n])):
+                got = scr[m, 0, ch, blk] if name in ("S_start", "G_end") else scr[m, 0, ch, blk, :n]
+                if np.abs(want).max() == 0:
+                    assert np.abs(got).max() == 0, name
+                    continue
+                errs[name] = max(errs.get(name, 0.0), rel(got, want))
+    print("chain max rel errs", errs)
+    assert all(e <= TOL_BF16 for e in errs.values()), errs
