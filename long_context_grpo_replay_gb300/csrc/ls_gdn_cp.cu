@@ -481,5 +481,355 @@ __global__ void __launch_bounds__(kThr, 1)
   }
 }
 
+// ---------------------------------------------------------------- out
+// One CTA per (chunk, head, member): the output o and the gradients of the
+// chunk's q, k, v, g, b from S (start), G (end), E and dU of the chunk.
+//   o   = diag(gamma) Q S^T + P E
+//   dQ  = diag(gamma) dO S + LdP K,            LdP = lower(Gamma . dP), dP = dO E^T
+//   dK  = LdP^T Q + Msym K - diag(gamma b) dU S + diag(w) E G,
+//         Msym = M + M^T, M = strict_lower(dA . b . Gamma), dA = -strict_lower(dU E^T)
+//   dV  = diag(b) dU
+//   db  = rowsum(dA . GK) + rowsum(dU . X),    X = V - diag(gamma) K S^T
+//   dg  = reverse cumulative sum of dc, with r = dP . P + dA . b . GK,
+//         dc = dgamma . gamma + rowsum(r) - colsum(r) - rw, rw = w . rowsum(E G . K),
+//         dgamma = rowsum(dO . Q S^T) - rowsum(b . dU . K S^T),
+//         and dc_last += sum(rw) + gamma_C <G, S>.
+constexpr uint32_t kOutMisc = 6 * kTile;
+constexpr uint32_t kOutSmem = kOutMisc + 4096 + 1024;
+
+__global__ void __launch_bounds__(kThr, 1)
+    gdn_cp_out_kernel(int H, int R, int nch, const float* __restrict__ q,
+                      const float* __restrict__ k, const float* __restrict__ v,
+                      const float* __restrict__ g, const float* __restrict__ beta,
+                      const float* __restrict__ d_o, float* __restrict__ scr,
+                      float* __restrict__ o, float* __restrict__ dq, float* __restrict__ dk,
+                      float* __restrict__ dv, float* __restrict__ dg, float* __restrict__ dbeta,
+                      uint32_t* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(sm);
+  const uint32_t S0 = sb, S1 = sb + kTile, S2 = sb + 2 * kTile, S3 = sb + 3 * kTile,
+                 S4 = sb + 4 * kTile, S5 = sb + 5 * kTile;
+  float* sc = reinterpret_cast<float*>(sm + kOutMisc);
+  float* sbt = sc + kC;
+  float* sgam = sbt + kC;
+  float* sw = sgam + kC;
+  float* rcol = sw + kC;
+  float* swt = rcol + kC;  // 8 floats of scan and reduction scratch
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOutMisc + 3584);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 5);
+  uint32_t* abort_s = tslot + 1;
+
+  const int ch = blockIdx.x, h = blockIdx.y, m = blockIdx.z, tid = threadIdx.x, warp = tid >> 5;
+  const int lane = tid & 31;
+  const int64_t t0 = (int64_t)ch * kC;
+  const int nt = R - t0 < kC ? (int)(R - t0) : kC;
+  {
+    const int64_t tok = (int64_t)m * R * H;
+    q += tok * kD, k += tok * kD, v += tok * kD, d_o += tok * kD, g += tok, beta += tok;
+    o += tok * kD, dq += tok * kD, dk += tok * kD, dv += tok * kD, dg += tok, dbeta += tok;
+  }
+  float* blk = scratch_of(scr, H, nch, m, h, ch);
+  const float* Sst = blk + (int64_t)kSstart * kTileElems;
+  const float* Gen = blk + (int64_t)kGend * kTileElems;
+  const float* Eb = blk + (int64_t)kEblk * kTileElems;
+  const float* dUb = blk + (int64_t)kDUblk * kTileElems;
+  const float* gkb = blk + (int64_t)kGKblk * kTileElems;
+  float* Pb = blk + (int64_t)kE0 * kTileElems;  // the E0 block is free after the chain: P (fp32)
+  if (tid == 0) {
+    for (int i = 0; i < 5; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    *abort_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tslot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = *tslot, lane_off = (uint32_t)(warp * 32) << 16;
+  const volatile uint32_t* abortp = abort_s;
+  const int64_t rs = (int64_t)H * kD;
+  const int t = tid;  // token row in the epilogues
+  const int64_t row = ((t0 + t) * H + h) * kD;  // row t of q, k, v, d_o, o, dq, dk, dv
+  const bool live = t < nt;
+  bool ok = true;
+
+  // ---- round 1: Q K^T -> T0, Q S^T -> T1, K S^T -> T2
+  stage_rows(S0, q + (t0 * H + h) * kD, rs, nt, nullptr);
+  stage_rows(S1, k + (t0 * H + h) * kD, rs, nt, nullptr);
+  stage_rows(S2, Sst, kD, kD, nullptr);
+  stage_rows(S3, Eb, kD, kC, nullptr);
+  stage_rows(S4, d_o + (t0 * H + h) * kD, rs, nt, nullptr);
+  stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
+  __syncthreads();
+  sgam[t] = expf(sc[t]);
+  sw[t] = live ? expf(sc[kC - 1] - sc[t]) : 0.f;
+  rcol[t] = 0.f;
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    tc_fence_after();
+    mma_group(tb + 0, S0, S1, false, false);
+    mma_group(tb + 128, S0, S2, false, false);
+    mma_group(tb + 256, S1, S2, false, false);
+    mma_commit(smem_u32(&bars[0]));
+  }
+  ok = mbar_wait_warp(smem_u32(&bars[0]), 0, abortp);
+  float dgam = 0.f, dbt = 0.f, rrow = 0.f, rw = 0.f;
+  if (!__syncthreads_or(!ok)) {
+    tc_fence_after();
+    const float ct = sc[t], gt = sgam[t], bt = sbt[t];
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+      uint32_t t32[32];
+      float f32[32];
+      // P row t (bf16 tile S5 for P E, fp32 copy for r)
+      tmem_ld32(tb + lane_off + 0 + cb * 32, t32);
+      tmem_wait_ld_r(t32);
+#pragma unroll
+      for (int xx = 0; xx < 32; ++xx) {
+        const int s = cb * 32 + xx;
+        f32[xx] = s <= t ? expf(ct - sc[s]) * __uint_as_float(t32[xx]) : 0.f;
+        Pb[t * kD + s] = f32[xx];
+      }
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) st_shared_v4(S5 + tile_off(t, cb * 4 + gg), pack8(&f32[8 * gg]));
+      // Q S^T row t: dgamma, and T1 scaled by gamma_t for o = gamma Q S^T + P E
+      tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
+      tmem_wait_ld_r(t32);
+#pragma unroll
+      for (int xx = 0; xx < 32; ++xx) {
+        const float qs = __uint_as_float(t32[xx]);
+        if (live) dgam = fmaf(d_o[row + cb * 32 + xx], qs, dgam);
+        t32[xx] = __float_as_uint(gt * qs);
+      }
+      tmem_st32(tb + lane_off + 128 + cb * 32, t32);
+      // K S^T row t: db (dU . X) and dgamma (- b dU . K S^T)
+      tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
+      tmem_wait_ld_r(t32);
+      if (live) {
+#pragma unroll
+        for (int xx = 0; xx < 32; ++xx) {
+          const int i = cb * 32 + xx;
+          const float ks = __uint_as_float(t32[xx]), du = dUb[t * kD + i];
+          dbt = fmaf(du, v[row + i] - gt * ks, dbt);
+          dgam = fmaf(-bt * du, ks, dgam);
+        }
+      }
+    }
+    tmem_wait_st();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // ---- round 2: P E -> T1 (onto gamma Q S^T), dO E^T -> T0, dU E^T -> T2, E G -> T3
+    stage_rows(S0, dUb, kD, kC, nullptr);
+    stage_rows(S1, Gen, kD, kD, nullptr);
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      mma_group(tb + 128, S5, S3, true, true);
+      mma_group(tb + 0, S4, S3, false, false);
+      mma_group(tb + 256, S0, S3, false, false);
+      mma_group(tb + 384, S3, S1, true, false);
+      mma_commit(smem_u32(&bars[1]));
+    }
+    ok = mbar_wait_warp(smem_u32(&bars[1]), 0, abortp);
+  }
+  if (!__syncthreads_or(!ok)) {
+    tc_fence_after();
+    const float ct = sc[t], bt = sbt[t], gt = sgam[t], wt = sw[t];
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+      uint32_t t32[32];
+      float f32[32];
+      // o row t
+      tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
+      tmem_wait_ld_r(t32);
+      if (live) {
+        float4* op = reinterpret_cast<float4*>(o + row + cb * 32);
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4)
+          op[i4] = make_float4(__uint_as_float(t32[4 * i4]), __uint_as_float(t32[4 * i4 + 1]),
+                               __uint_as_float(t32[4 * i4 + 2]), __uint_as_float(t32[4 * i4 + 3]));
+      }
+      // dP row t: LdP (tile S5, row t; and LdP^T column t into S0), r = dP . P
+      tmem_ld32(tb + lane_off + 0 + cb * 32, t32);
+      tmem_wait_ld_r(t32);
+#pragma unroll
+      for (int xx = 0; xx < 32; ++xx) {
+        const int s = cb * 32 + xx;
+        const float dp = __uint_as_float(t32[xx]);
+        f32[xx] = s <= t ? expf(ct - sc[s]) * dp : 0.f;
+        const float r = dp * Pb[t * kD + s];
+        rrow += r;
+        if (r != 0.f) atomicAdd(&rcol[s], r);
+        st_shared_u16(S0 + elem_off(s, t), bf16_of(f32[xx]));
+      }
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) st_shared_v4(S5 + tile_off(t, cb * 4 + gg), pack8(&f32[8 * gg]));
+      // dA row t = -strict_lower(dU E^T): db, r, and Msym (both triangles) into S3
+      tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
+      tmem_wait_ld_r(t32);
+#pragma unroll
+      for (int xx = 0; xx < 32; ++xx) {
+        const int s = cb * 32 + xx;
+        float mk = 0.f;
+        if (s < t) {
+          const float da = -__uint_as_float(t32[xx]);
+          const float gkv = gkb[a_at(t, s)];
+          dbt = fmaf(da, gkv, dbt);
+          const float r = da * bt * gkv;
+          rrow += r;
+          if (r != 0.f) atomicAdd(&rcol[s], r);
+          mk = da * bt * expf(ct - sc[s]);
+        }
+        if (s <= t) {
+          const uint16_t hb = bf16_of(mk);
+          st_shared_u16(S3 + elem_off(t, s), hb);
+          st_shared_u16(S3 + elem_off(s, t), hb);
+        }
+      }
+      // E G row t: rw = w . rowsum(E G . K)
+      tmem_ld32(tb + lane_off + 384 + cb * 32, t32);
+      tmem_wait_ld_r(t32);
+      if (live) {
+#pragma unroll
+        for (int xx = 0; xx < 32; ++xx) rw = fmaf(__uint_as_float(t32[xx]), k[row + cb * 32 + xx], rw);
+      }
+    }
+    rw *= wt;
+    // dO tile rows scaled by gamma for dQ; K back into S1; dV
+    {
+#pragma unroll
+      for (int gq = 0; gq < 16; ++gq) {
+        const uint32_t ad = S4 + tile_off(t, gq);
+        const uint4 pk = ld_shared_v4(ad);
+        const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
+        float f8[8];
+#pragma unroll
+        for (int i2 = 0; i2 < 4; ++i2) {
+          const float2 f = unpack_bf16x2(w4[i2]);
+          f8[2 * i2] = f.x * gt, f8[2 * i2 + 1] = f.y * gt;
+        }
+        st_shared_v4(ad, pack8(f8));
+      }
+      if (live)
+        for (int i = 0; i < kD; ++i) dv[row + i] = bt * dUb[t * kD + i];
+    }
+    __syncthreads();
+    stage_rows(S1, k + (t0 * H + h) * kD, rs, nt, nullptr);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // ---- round 3a: dQ = (gamma dO) S + LdP K -> T0
+    if (tid == 0) {
+      tc_fence_after();
+      mma_group(tb + 0, S4, S2, true, false);
+      mma_group(tb + 0, S5, S1, true, true);
+      mma_commit(smem_u32(&bars[2]));
+    }
+    ok = mbar_wait_warp(smem_u32(&bars[2]), 0, abortp);
+  }
+  if (!__syncthreads_or(!ok)) {
+    tc_fence_after();
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+      uint32_t t32[32];
+      tmem_ld32(tb + lane_off + 0 + cb * 32, t32);
+      tmem_wait_ld_r(t32);
+      if (live)
+#pragma unroll
+        for (int xx = 0; xx < 32; ++xx) dq[row + cb * 32 + xx] = __uint_as_float(t32[xx]);
+    }
+    // Q into S4, -(gamma b) dU into S5 for dK
+    {
+      const float f = -sgam[t] * sbt[t];
+      float f8[8];
+#pragma unroll 1
+      for (int gq = 0; gq < 16; ++gq) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) f8[u] = f * dUb[t * kD + 8 * gq + u];
+        st_shared_v4(S5 + tile_off(t, gq), pack8(f8));
+      }
+    }
+    stage_rows(S4, q + (t0 * H + h) * kD, rs, nt, nullptr);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // ---- round 3b: dK = LdP^T Q + Msym K - (gamma b dU) S -> T2 (+ w E G from T3)
+    if (tid == 0) {
+      tc_fence_after();
+      mma_group(tb + 256, S0, S4, true, false);
+      mma_group(tb + 256, S3, S1, true, true);
+      mma_group(tb + 256, S5, S2, true, true);
+      mma_commit(smem_u32(&bars[3]));
+    }
+    ok = mbar_wait_warp(smem_u32(&bars[3]), 0, abortp);
+  }
+  if (!__syncthreads_or(!ok)) {
+    tc_fence_after();
+    const float wt = sw[t];
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+      uint32_t a32[32], b32[32];
+      tmem_ld32(tb + lane_off + 256 + cb * 32, a32);
+      tmem_ld32(tb + lane_off + 384 + cb * 32, b32);
+      tmem_wait_ld_r(a32);
+      reg_dep(b32);
+      if (live)
+#pragma unroll
+        for (int xx = 0; xx < 32; ++xx)
+          dk[row + cb * 32 + xx] = fmaf(wt, __uint_as_float(b32[xx]), __uint_as_float(a32[xx]));
+    }
+    // <G, S> over the block, then dc and its reverse cumulative sum
+    float gs = 0.f;
+    for (int j = 0; j < kD; ++j) gs = fmaf(Gen[t * kD + j], Sst[t * kD + j], gs);
+    float rws = rw;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      gs += __shfl_xor_sync(0xffffffffu, gs, off);
+      rws += __shfl_xor_sync(0xffffffffu, rws, off);
+    }
+    __syncthreads();
+    if (lane == 0) {
+      swt[warp] = gs;
+      swt[4 + warp] = rws;
+    }
+    __syncthreads();
+    float dc = dgam * sgam[t] + rrow - rcol[t] - rw;
+    if (t == kC - 1)
+      dc += (swt[4] + swt[5] + swt[6] + swt[7]) + sgam[kC - 1] * (swt[0] + swt[1] + swt[2] + swt[3]);
+    float x = dc;  // suffix sum within the warp
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float y = __shfl_down_sync(0xffffffffu, x, off);
+      if (lane + off < 32) x += y;
+    }
+    __syncthreads();
+    if (lane == 0) swt[warp] = x;  // the warp's total
+    __syncthreads();
+    for (int w = warp + 1; w < 4; ++w) x += swt[w];
+    if (live) {
+      dg[(t0 + t) * H + h] = x;
+      dbeta[(t0 + t) * H + h] = dbt;
+    }
+  }
+  if (!ok && tid == 0 && status) atomicOr(status, kStatusTimeout);
+  if (tid == 0) {
+    mma_commit(smem_u32(&bars[4]));
+    mbar_wait(smem_u32(&bars[4]), 0, abortp);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tb, 512);
+  }
+}
+
 }  // namespace
 }  // namespace ls

@@ -66,11 +66,13 @@ inline unsigned atomicCAS(unsigned* p, unsigned cmp, unsigned v) {
   std::atomic_ref<unsigned>(*p).compare_exchange_strong(cmp, v);
   return cmp;
 }
+inline float atomicAdd(float* p, float v) { return std::atomic_ref<float>(*p).fetch_add(v); }
 inline void __syncthreads() { emu::syncthreads(); }
 inline int __syncthreads_or(int p) { return emu::syncthreads_or(p); }
 inline void __syncwarp(unsigned = 0xffffffffu) { emu::syncwarp(); }
 inline float __shfl_up_sync(unsigned, float x, int off) { return emu::shfl_up(x, off); }
 inline float __shfl_xor_sync(unsigned, float x, int mask) { return emu::shfl_xor(x, mask); }
+inline float __shfl_down_sync(unsigned, float x, int off) { return emu::shfl_down(x, off); }
 inline int __all_sync(unsigned, int p) { return emu::all_sync(p); }
 inline int __any_sync(unsigned, int p) { return emu::any_sync(p); }
 

@@ -175,6 +175,15 @@ inline int all_sync(int p) {
   return r;
 }
 
+inline float shfl_down(float x, int off) {
+  Block& b = *g_block;
+  const int w = t_tid >> 5, l = t_tid & 31;
+  b.warp_f[w][l] = x;
+  b.warp_bar[w]->arrive_and_wait();
+  const float y = l + off < 32 ? b.warp_f[w][l + off] : x;
+  b.warp_bar[w]->arrive_and_wait();
+  return y;
+}
 inline float shfl_xor(float x, int mask) {
   Block& b = *g_block;
   const int w = t_tid >> 5, l = t_tid & 31;

@@ -141,3 +141,32 @@ def test_chains_match_the_reference(emulator):
                 errs[name] = max(errs.get(name, 0.0), rel(got, want))
     print("chain max rel errs", errs)
     assert all(e <= TOL_BF16 for e in errs.values()), errs
+
+
+def test_full_replay_matches_the_oracle(emulator):
+    """prep, chain and out together: the forward (o, final state) and every
+    gradient of a two-member group over three chunks, the last partial,
+    against the float64 oracle."""
+    from oracle.gdn import gdn_replay
+
+    exe, d = emulator
+    B, H, R = 2, 1, 300
+    c = inputs.make_gdn_group(B, H, R, seed=33)
+    status, _, rest = run(exe, d, c, "all")
+    assert status == 0
+    nt, ns, nsc = B * R * H * 128, B * H * 128 * 128, B * R * H
+    got, i = {}, 0
+    for name, n in (("o", nt), ("s_final", ns), ("dq", nt), ("dk", nt), ("dv", nt), ("dg", nsc),
+                    ("dbeta", nsc)):
+        got[name] = rest[i:i + n]
+        i += n
+    a = {x: t.numpy() for x, t in c.items()}
+    errs = {}
+    for m in range(B):
+        want = gdn_replay(a["s0"], a["q"][m], a["k"][m], a["v"][m], a["g"][m], a["beta"][m],
+                          a["d_o"][m])
+        for name in got:
+            gm = got[name].reshape((B,) + want[name].shape)[m]
+            errs[name] = max(errs.get(name, 0.0), rel(gm, want[name]))
+    print("full replay max rel errs", errs)
+    assert all(e <= TOL_BF16 for e in errs.values()), errs
