@@ -259,10 +259,11 @@ LS_API ls_status ls_sum_parts(int32_t n_parts, int64_t n_elems, const float* par
  * Errors: LS_ERR_UNSUPPORTED for other dk/dv, LS_ERR_INVALID_ARGUMENT for
  * NULL buffers or negative sizes, LS_ERR_WORKSPACE_TOO_SMALL; all before any
  * launch.
- * The environment variable LS_GDN_VARIANT=chunk makes ls_gdn_replay_fwd use
- * a chunkwise tensor-core kernel instead (bf16 operands, about 4e-3 relative
- * error; q, k, v and o 16-byte aligned, else LS_ERR_CUDA).  It is
- * experimental: it has not been validated on a GPU. */
+ * The environment variable LS_GDN_VARIANT=chunk makes both calls use the
+ * tensor-core kernels instead: a chunkwise forward and a chunk-parallel
+ * backward (bf16 operands, about 5e-3 relative error; q, k, v, d_o and the
+ * outputs 16-byte aligned, else LS_ERR_CUDA).  ls_gdn_workspace_size covers
+ * either backward.  It is experimental: it has not been validated on a GPU. */
 typedef struct {
   int32_t batch;
   int32_t heads;

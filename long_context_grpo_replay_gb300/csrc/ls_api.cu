@@ -580,7 +580,11 @@ ls_status ls_gdn_workspace_size(const ls_gdn_desc* desc, int32_t resp_len, size_
   LS_CHECK(check_gdn(desc));
   if (!bytes) return fail(LS_ERR_INVALID_ARGUMENT, "bytes is NULL");
   if (resp_len < 0) return fail(LS_ERR_INVALID_ARGUMENT, "resp_len < 0");
-  *bytes = gdn_workspace_bytes(desc->batch, desc->heads, resp_len);
+  // enough for either backward (the recurrent one, or the chunk-parallel one
+  // that LS_GDN_VARIANT=chunk selects)
+  const size_t a = gdn_workspace_bytes(desc->batch, desc->heads, resp_len);
+  const size_t b = gdn_cp_workspace_bytes(desc->batch, desc->heads, resp_len);
+  *bytes = a > b ? a : b;
   return LS_OK;
 }
 
@@ -612,14 +616,22 @@ ls_status ls_gdn_replay_bwd(const ls_gdn_desc* desc, const float* s0, const floa
   if (desc->batch == 0 || desc->heads == 0 || resp_len == 0) return LS_OK;
   if (!s0 || !q || !k || !v || !g || !beta || !d_o || !dq || !dk || !dv || !dg || !dbeta)
     return fail(LS_ERR_INVALID_ARGUMENT, "backward buffers must be non-NULL");
-  const size_t need = gdn_workspace_bytes(desc->batch, desc->heads, resp_len);
+  const bool chunk = gdn_chunk_selected();
+  const size_t need = chunk ? gdn_cp_workspace_bytes(desc->batch, desc->heads, resp_len)
+                            : gdn_workspace_bytes(desc->batch, desc->heads, resp_len);
   if (!ws) return fail(LS_ERR_INVALID_ARGUMENT, "workspace is NULL");
   if (ws_bytes < need)
     return fail(LS_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes, need %zu", ws_bytes, need);
   if (!aligned(ws, 16)) return fail(LS_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
-  LS_CUDA(launch_gdn_bwd(desc->batch, desc->heads, resp_len, s0, q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta,
-                         static_cast<float*>(ws), static_cast<cudaStream_t>(stream)),
-          "GDN backward launch");
+  if (chunk)
+    LS_CUDA(launch_gdn_cp_bwd(desc->batch, desc->heads, resp_len, s0, q, k, v, g, beta, d_o, dq, dk,
+                              dv, dg, dbeta, static_cast<float*>(ws),
+                              static_cast<cudaStream_t>(stream)),
+            "GDN chunk-parallel backward launch");
+  else
+    LS_CUDA(launch_gdn_bwd(desc->batch, desc->heads, resp_len, s0, q, k, v, g, beta, d_o, dq, dk,
+                           dv, dg, dbeta, static_cast<float*>(ws), static_cast<cudaStream_t>(stream)),
+            "GDN backward launch");
   return LS_OK;
 }
 

@@ -528,7 +528,8 @@ __global__ void __launch_bounds__(kThr, 1)
   {
     const int64_t tok = (int64_t)m * R * H;
     q += tok * kD, k += tok * kD, v += tok * kD, d_o += tok * kD, g += tok, beta += tok;
-    o += tok * kD, dq += tok * kD, dk += tok * kD, dv += tok * kD, dg += tok, dbeta += tok;
+    if (o) o += tok * kD;
+    dq += tok * kD, dk += tok * kD, dv += tok * kD, dg += tok, dbeta += tok;
   }
   float* blk = scratch_of(scr, H, nch, m, h, ch);
   const float* Sst = blk + (int64_t)kSstart * kTileElems;
@@ -649,7 +650,7 @@ __global__ void __launch_bounds__(kThr, 1)
       // o row t
       tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
       tmem_wait_ld_r(t32);
-      if (live) {
+      if (live && o) {
         float4* op = reinterpret_cast<float4*>(o + row + cb * 32);
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4)
@@ -832,4 +833,42 @@ __global__ void __launch_bounds__(kThr, 1)
 }
 
 }  // namespace
+
+size_t gdn_cp_workspace_bytes(int B, int H, int R) {
+  const int64_t nch = (R + kC - 1) / kC;
+  return (size_t)B * H * nch * kScrFloats * sizeof(float);
+}
+
+// The backward in chunk-parallel form: prep over all chunks, the two chains
+// per (head, member), then the outputs over all chunks.  ws holds the
+// scratch (gdn_cp_workspace_bytes); q, k, v and d_o must be 16-byte aligned.
+cudaError_t launch_gdn_cp_bwd(int B, int H, int R, const float* s0, const float* q, const float* k,
+                              const float* v, const float* g, const float* beta, const float* d_o,
+                              float* dq, float* dk, float* dv, float* dg, float* dbeta, float* ws,
+                              cudaStream_t st) {
+  if (B == 0 || H == 0 || R == 0) return cudaSuccess;
+  for (const void* p : {(const void*)q, (const void*)k, (const void*)v, (const void*)d_o,
+                        (const void*)dq, (const void*)dk, (const void*)ws})
+    if (reinterpret_cast<uintptr_t>(p) & 15u) return cudaErrorMisalignedAddress;
+  const int nch = (R + kC - 1) / kC;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(gdn_cp_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kPrepSmem)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(gdn_cp_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kChainSmem)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(gdn_cp_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kOutSmem)) != cudaSuccess)
+    return e;
+  LaunchScope ls(kKGdnBwd, st);
+  gdn_cp_prep_kernel<<<dim3(nch, H, B), kThr, kPrepSmem, st>>>(H, R, nch, q, k, v, g, beta, d_o, ws,
+                                                              nullptr);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  gdn_cp_chain_kernel<<<dim3(H, B), kThr, kChainSmem, st>>>(H, R, nch, s0, q, k, g, beta, d_o, ws,
+                                                           nullptr, nullptr);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  gdn_cp_out_kernel<<<dim3(nch, H, B), kThr, kOutSmem, st>>>(H, R, nch, q, k, v, g, beta, d_o, ws,
+                                                            nullptr, dq, dk, dv, dg, dbeta, nullptr);
+  return cudaGetLastError();
+}
+
 }  // namespace ls

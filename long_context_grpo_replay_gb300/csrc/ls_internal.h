@@ -147,6 +147,12 @@ bool gdn_chunk_selected();
 cudaError_t launch_gdn_chunk_fwd(int B, int H, int R, const float* s0, const float* q,
                                  const float* k, const float* v, const float* g, const float* beta,
                                  float* o, float* s_final, cudaStream_t st);
+// Chunk-parallel tensor-core backward (ls_gdn_cp.cu), selected with the chunkwise forward.
+size_t gdn_cp_workspace_bytes(int B, int H, int R);
+cudaError_t launch_gdn_cp_bwd(int B, int H, int R, const float* s0, const float* q, const float* k,
+                              const float* v, const float* g, const float* beta, const float* d_o,
+                              float* dq, float* dk, float* dv, float* dg, float* dbeta, float* ws,
+                              cudaStream_t st);
 cudaError_t launch_gdn_bwd(int B, int H, int R, const float* s0, const float* q, const float* k,
                            const float* v, const float* g, const float* beta, const float* d_o,
                            float* dq, float* dk, float* dv, float* dg, float* dbeta, float* ws,

@@ -179,9 +179,12 @@ def test_gdn_workspace_and_argument_checks(ls):
     L = ls.lib()
     d = ls.GdnDesc(8, 32, 128, 128)
     sizes = [ls.ls_gdn_workspace_size(d, r) for r in (1, 64, 65, 4096)]
-    # per (member, head): one 128x128 float32 state per checkpoint (every 8
-    # tokens) plus one segment of 8 states
-    assert sizes == [8 * 32 * (n + 8) * 128 * 128 * 4 for n in (1, 8, 9, 512)]
+    # enough for either backward: per (member, head) the recurrent one keeps one
+    # 128x128 float32 state per 8-token checkpoint plus a segment of 8 states;
+    # the chunk-parallel one keeps nine 128x128 float32 blocks per 128-token chunk
+    rec = [8 * 32 * (n + 8) * 128 * 128 * 4 for n in (1, 8, 9, 512)]
+    cp = [8 * 32 * -(-R // 128) * 9 * 128 * 128 * 4 for R in (1, 64, 65, 4096)]
+    assert sizes == [max(a, b) for a, b in zip(rec, cp)]
     out = ctypes.c_size_t(0)
     bad = ls.GdnDesc(8, 32, 64, 128)
     assert L.ls_gdn_workspace_size(ctypes.byref(bad), 10, ctypes.byref(out)) != 0

@@ -25,7 +25,8 @@ def build(d):
     if shutil.which("g++") is None:
         pytest.skip("no host C++ compiler")
     src = SRC.read_text()
-    end = src.index("\n}  // namespace\n}  // namespace ls") + len("\n}  // namespace\n")
+    # the kernels, up to the end of their anonymous namespace; launchers stay out
+    end = src.index("\n}  // namespace\n\nsize_t gdn_cp_workspace_bytes") + len("\n}  // namespace\n")
     text = src[:end] + "}  // namespace ls\n" + (EMU / "gdn_cp_run.inc").read_text()
     text = text.replace("extern __shared__", "extern")
     csrc = d / "x" / "csrc"

@@ -1,11 +1,13 @@
-"""The chunkwise tensor-core GDN forward (LS_GDN_VARIANT=chunk) against the
-float64 oracle at the bf16 tolerance: its products take bf16 operands, which
-a CPU simulation of the same rounding points puts near 4e-3.  Cases: three
-chunks with a partial last one, one exact chunk, a single token, the empty
-response, and two sampled heads of the 8 x 32-head x 4096-token group.
+"""The tensor-core GDN path (LS_GDN_VARIANT=chunk: the chunkwise forward and
+the chunk-parallel backward) against the float64 oracle at the bf16
+tolerance: its products take bf16 operands, which the CPU block emulator
+puts near 4e-3 to 5e-3.  Cases: three chunks with a partial last one, one
+exact chunk, a single token, the empty response, and two sampled heads of
+the 8 x 32-head x 4096-token group.
 
-The kernel is compiled with the library but has not yet run on a GPU, so
-these tests run only when LS_GDN_CHUNK_TESTS=1."""
+The kernels are compiled with the library and checked on the CPU emulator,
+but have not yet run on a GPU, so these tests run only when
+LS_GDN_CHUNK_TESTS=1."""
 import os
 
 import numpy as np
@@ -40,23 +42,38 @@ def _fwd(c):
     return o, s_final
 
 
-def _check(c, o, s_final, b, heads):
+def _bwd(c):
+    B, R, H, _ = c["q"].shape
+    grads = {n: torch.empty_like(c[x]) for n, x in
+             (("dq", "q"), ("dk", "k"), ("dv", "v"), ("dg", "g"), ("dbeta", "beta"))}
+    ws = torch.empty(ls.ls_gdn_workspace_size(ls.GdnDesc(B, H, 128, 128), R), dtype=torch.uint8,
+                     device=c["q"].device)
+    ls.ls_gdn_replay_bwd(c["s0"], c["q"], c["k"], c["v"], c["g"], c["beta"], c["d_o"], grads["dq"],
+                         grads["dk"], grads["dv"], grads["dg"], grads["dbeta"], ws)
+    torch.cuda.synchronize()
+    return grads
+
+
+def _check(c, o, s_final, b, heads, grads=None):
     hs = list(heads)
-    a = {x: c[x].cpu() for x in ("s0", "q", "k", "v", "g", "beta")}
+    a = {x: c[x].cpu() for x in ("s0", "q", "k", "v", "g", "beta", "d_o")}
     want = gdn_replay(a["s0"][hs], a["q"][b][:, hs], a["k"][b][:, hs], a["v"][b][:, hs],
-                      a["g"][b][:, hs], a["beta"][b][:, hs])
-    e_o = rel_err(o[b][:, hs].double().cpu().numpy(), want["o"])
-    e_s = rel_err(s_final[b][hs].double().cpu().numpy(), want["s_final"])
-    assert e_o <= TOL["bf16"] and e_s <= TOL["bf16"], (b, hs, e_o, e_s)
+                      a["g"][b][:, hs], a["beta"][b][:, hs], a["d_o"][b][:, hs])
+    errs = {"o": rel_err(o[b][:, hs].double().cpu().numpy(), want["o"]),
+            "s_final": rel_err(s_final[b][hs].double().cpu().numpy(), want["s_final"])}
+    for name, t in (grads or {}).items():
+        errs[name] = rel_err(t[b][:, hs].double().cpu().numpy(), want[name])
+    assert all(e <= TOL["bf16"] for e in errs.values()), (b, hs, errs)
 
 
 @pytest.mark.parametrize("B,H,R", [(1, 4, 300), (2, 2, 128), (2, 3, 1)],
                          ids=["three_chunks_r300", "one_chunk_r128", "one_token"])
-def test_chunk_forward_matches_the_oracle(cuda_device, B, H, R):
+def test_chunk_path_matches_the_oracle(cuda_device, B, H, R):
     c = inputs.make_gdn_group(B, H, R, seed=60 + R, device=cuda_device)
     o, s_final = _fwd(c)
+    grads = _bwd(c)
     for b in range(B):
-        _check(c, o, s_final, b, range(H))
+        _check(c, o, s_final, b, range(H), grads)
 
 
 def test_chunk_forward_empty_response(cuda_device):
@@ -65,8 +82,10 @@ def test_chunk_forward_empty_response(cuda_device):
     assert torch.equal(s_final, c["s0"].expand_as(s_final))
 
 
-def test_chunk_forward_at_bench_size_sampled(cuda_device):
+def test_chunk_path_at_bench_size_sampled(cuda_device):
     c = inputs.make_gdn_group(8, 32, 4096, seed=78, device=cuda_device)
     o, s_final = _fwd(c)
+    grads = _bwd(c)
     assert torch.isfinite(o).all() and torch.isfinite(s_final).all()
-    _check(c, o, s_final, 6, (1, 30))
+    assert all(torch.isfinite(t).all() for t in grads.values())
+    _check(c, o, s_final, 6, (1, 30), grads)
