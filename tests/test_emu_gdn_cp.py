@@ -171,3 +171,27 @@ def test_full_replay_matches_the_oracle(emulator):
             errs[name] = max(errs.get(name, 0.0), rel(gm, want[name]))
     print("full replay max rel errs", errs)
     assert all(e <= TOL_BF16 for e in errs.values()), errs
+
+
+@pytest.mark.parametrize("B,H,R", [(1, 2, 1), (1, 1, 128), (1, 1, 129)],
+                         ids=["one_token_two_heads", "one_exact_chunk", "one_token_past_a_chunk"])
+def test_edge_lengths_match_the_oracle(emulator, B, H, R):
+    from oracle.gdn import gdn_replay
+
+    exe, d = emulator
+    c = inputs.make_gdn_group(B, H, R, seed=40 + R)
+    status, _, rest = run(exe, d, c, "all")
+    assert status == 0
+    nt, ns, nsc = B * R * H * 128, B * H * 128 * 128, B * R * H
+    got, i = {}, 0
+    for name, n in (("o", nt), ("s_final", ns), ("dq", nt), ("dk", nt), ("dv", nt), ("dg", nsc),
+                    ("dbeta", nsc)):
+        got[name] = rest[i:i + n]
+        i += n
+    a = {x: t.numpy() for x, t in c.items()}
+    for m in range(B):
+        want = gdn_replay(a["s0"], a["q"][m], a["k"][m], a["v"][m], a["g"][m], a["beta"][m],
+                          a["d_o"][m])
+        for name in got:
+            gm = got[name].reshape((B,) + want[name].shape)[m]
+            assert rel(gm, want[name]) <= TOL_BF16, (name, rel(gm, want[name]))
