@@ -77,8 +77,9 @@ def _errors(emulator, B, H, R, seed):
     return errs
 
 
-@pytest.mark.parametrize("B,H,R", [(1, 2, 300), (1, 1, 128), (2, 1, 1)],
-                         ids=["three_chunks_r300", "one_chunk_r128", "one_token"])
+@pytest.mark.parametrize("B,H,R", [(1, 2, 300), (1, 1, 128), (2, 1, 1), (2, 2, 129)],
+                         ids=["three_chunks_r300", "one_chunk_r128", "one_token",
+                              "one_token_past_a_chunk"])
 def test_emulated_chunk_forward_matches_the_oracle(emulator, B, H, R):
     for e_o, e_s in _errors(emulator, B, H, R, seed=90 + R):
         assert e_o <= TOL_BF16 and e_s <= TOL_BF16, (e_o, e_s)
