@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import oracle.ref as ref
+from emu_support import compile_harness
 from long_context_grpo_replay_gb300 import inputs
 
 ROOT = Path(__file__).resolve().parents[1]
@@ -39,10 +40,7 @@ def build(d):
     shutil.copy(EMU / "ls_tc.cuh", csrc / "ls_tc.cuh")
     shutil.copy(ROOT / "include" / "ls.h", d / "include" / "ls.h")
     exe = d / "attn_dkdv_emu"
-    r = subprocess.run(["g++", "-std=c++20", "-O2", "-pthread", "-Wno-unknown-pragmas", "-I", str(EMU),
-                        "-I", str(csrc), str(EMU / "attn_dkdv_main.cpp"), "-o", str(exe)],
-                       capture_output=True, text=True, timeout=600)
-    assert r.returncode == 0, r.stderr[-3000:]
+    compile_harness("attn_dkdv_main.cpp", csrc, exe)
     return exe
 
 

@@ -14,6 +14,7 @@ from pathlib import Path
 import numpy as np
 import pytest
 
+from emu_support import compile_harness
 from long_context_grpo_replay_gb300 import inputs
 from oracle.gdn import gdn_replay
 
@@ -39,9 +40,7 @@ def _build(d, mutation=None):
     for name in ("ls_internal.h", "ls_tc.cuh"):
         shutil.copy(EMU / name, d / name)
     exe = d / "gdn_chunk_emu"
-    subprocess.run(["g++", "-std=c++20", "-O2", "-pthread", "-Wno-unknown-pragmas", "-I", str(EMU),
-                    "-I", str(d), str(EMU / "gdn_chunk_main.cpp"), "-o", str(exe)], check=True,
-                   capture_output=True, text=True, timeout=600)
+    compile_harness("gdn_chunk_main.cpp", d, exe)
     return d, exe
 
 

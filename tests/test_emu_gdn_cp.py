@@ -10,6 +10,7 @@ from pathlib import Path
 import numpy as np
 import pytest
 
+from emu_support import compile_harness
 from long_context_grpo_replay_gb300 import inputs
 from test_oracle_gdn import _cp_prep
 
@@ -38,10 +39,7 @@ def build(d):
     shutil.copy(EMU / "ls_tc.cuh", csrc / "ls_tc.cuh")
     shutil.copy(ROOT / "include" / "ls.h", d / "include" / "ls.h")
     exe = d / "gdn_cp_emu"
-    r = subprocess.run(["g++", "-std=c++20", "-O2", "-pthread", "-Wno-unknown-pragmas", "-I", str(EMU),
-                        "-I", str(csrc), str(EMU / "gdn_cp_main.cpp"), "-o", str(exe)],
-                       capture_output=True, text=True, timeout=600)
-    assert r.returncode == 0, r.stderr[-3000:]
+    compile_harness("gdn_cp_main.cpp", csrc, exe)
     return exe
 
 

@@ -12,6 +12,7 @@ from pathlib import Path
 import numpy as np
 import pytest
 
+from emu_support import compile_harness
 from long_context_grpo_replay_gb300 import inputs
 from oracle.gdn import gdn_replay
 
@@ -36,10 +37,7 @@ def build(d, mutation=None):
     for name in ("ls_internal.h", "ls_tc.cuh"):
         shutil.copy(EMU / name, d / name)
     exe = d / "gdn_rec_emu"
-    r = subprocess.run(["g++", "-std=c++20", "-O2", "-pthread", "-Wno-unknown-pragmas", "-I", str(EMU),
-                        "-I", str(d), str(EMU / "gdn_recurrent_main.cpp"), "-o", str(exe)],
-                       capture_output=True, text=True, timeout=600)
-    assert r.returncode == 0, r.stderr[-3000:]
+    compile_harness("gdn_recurrent_main.cpp", d, exe)
     return exe
 
 
