@@ -719,6 +719,7 @@ GDN_METRIC = "GDN state replay (forward+backward) response tokens/s per layer"
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 GDN_FWD_FLOP_PER_TOKEN_HEAD = 7   # x dk*dv: S k, the state update, S q
 GDN_BWD_FLOP_PER_TOKEN_HEAD = 20  # x dk*dv: S_t, G, G k, S_t^T dO, <G,S>, dk's two products, G decay
+GDN_CP_BWD_PRODUCTS = 20  # prep 3, chains 5, outputs 12 (128 x 128 x 128 each, per chunk and head)
 
 
 def run_gdn(args):
@@ -790,6 +791,18 @@ def run_gdn(args):
             "frac": achieved / FP32_ALU_TFLOPS, "traffic": traffic, "kernel": "gdn_bwd",
             "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz",
             "algorithmic_per_launch": fl_bwd, "launch_ms": launch_ms}
+    if os.environ.get("LS_GDN_VARIANT", "").startswith("c"):
+        # tensor-core path: the backward's three kernels execute 20 products of
+        # 128 x 128 x 128 per (chunk, head, member); the solves are not counted
+        nch = -(-R // 128)
+        fl_tc = GDN_CP_BWD_PRODUCTS * 2.0 * 128 ** 3 * nch * H * B
+        pk, pk_src = peaks()
+        peak_t = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        ach = fl_tc / (launch_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peak_t, "unit": "TFLOP/s",
+                "frac": ach / peak_t, "traffic": None, "kernel": "gdn_bwd (chunk-parallel)",
+                "peak_source": f"{pk_src} (bf16_tflops_sustained)",
+                "algorithmic_per_launch": fl_tc, "launch_ms": launch_ms}
 
     e2e = None
     if not args.no_e2e:
