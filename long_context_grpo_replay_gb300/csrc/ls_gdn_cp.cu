@@ -847,6 +847,7 @@ cudaError_t launch_gdn_cp_bwd(int B, int H, int R, const float* s0, const float*
                               float* dq, float* dk, float* dv, float* dg, float* dbeta, float* ws,
                               cudaStream_t st) {
   if (B == 0 || H == 0 || R == 0) return cudaSuccess;
+  if (H > 65535 || B > 65535) return cudaErrorInvalidValue;  // grid y and z
   for (const void* p : {(const void*)q, (const void*)k, (const void*)v, (const void*)d_o,
                         (const void*)dq, (const void*)dk, (const void*)ws})
     if (reinterpret_cast<uintptr_t>(p) & 15u) return cudaErrorMisalignedAddress;
