@@ -263,7 +263,8 @@ LS_API ls_status ls_sum_parts(int32_t n_parts, int64_t n_elems, const float* par
  * tensor-core kernels instead: a chunkwise forward and a chunk-parallel
  * backward (bf16 operands, about 5e-3 relative error; q, k, v, d_o and the
  * outputs 16-byte aligned, else LS_ERR_CUDA).  ls_gdn_workspace_size covers
- * either backward.  It is experimental: it has not been validated on a GPU. */
+ * either backward.  It is experimental: its parity is checked on a GB300 for
+ * short responses, its speed not yet measured. */
 typedef struct {
   int32_t batch;
   int32_t heads;

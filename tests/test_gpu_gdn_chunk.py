@@ -5,9 +5,9 @@ puts near 4e-3 to 5e-3.  Cases: three chunks with a partial last one, one
 exact chunk, a single token, the empty response, and two sampled heads of
 the 8 x 32-head x 4096-token group.
 
-The kernels are compiled with the library and checked on the CPU emulator,
-but have not yet run on a GPU, so these tests run only when
-LS_GDN_CHUNK_TESTS=1."""
+The three-chunk, single-token and empty cases have run green on a GB300 and
+run by default; the exact-chunk and bench-size cases have not yet run on a
+GPU and run only when LS_GDN_CHUNK_TESTS=1."""
 import os
 
 import numpy as np
@@ -19,9 +19,9 @@ from long_context_grpo_replay_gb300 import inputs
 from oracle.gdn import gdn_replay
 from gpu_helpers import TOL, rel_err
 
-pytestmark = [pytest.mark.gpu,
-              pytest.mark.skipif(os.environ.get("LS_GDN_CHUNK_TESTS") != "1",
-                                 reason="chunkwise GDN forward not yet run on a GPU")]
+pytestmark = pytest.mark.gpu
+not_yet_on_gpu = pytest.mark.skipif(os.environ.get("LS_GDN_CHUNK_TESTS") != "1",
+                                    reason="not yet run on a GPU")
 
 
 @pytest.fixture(autouse=True)
@@ -66,7 +66,8 @@ def _check(c, o, s_final, b, heads, grads=None):
     assert all(e <= TOL["bf16"] for e in errs.values()), (b, hs, errs)
 
 
-@pytest.mark.parametrize("B,H,R", [(1, 4, 300), (2, 2, 128), (2, 3, 1)],
+@pytest.mark.parametrize("B,H,R", [(1, 4, 300), pytest.param(2, 2, 128, marks=not_yet_on_gpu),
+                                   (2, 3, 1)],
                          ids=["three_chunks_r300", "one_chunk_r128", "one_token"])
 def test_chunk_path_matches_the_oracle(cuda_device, B, H, R):
     c = inputs.make_gdn_group(B, H, R, seed=60 + R, device=cuda_device)
@@ -82,6 +83,7 @@ def test_chunk_forward_empty_response(cuda_device):
     assert torch.equal(s_final, c["s0"].expand_as(s_final))
 
 
+@not_yet_on_gpu
 def test_chunk_path_at_bench_size_sampled(cuda_device):
     c = inputs.make_gdn_group(8, 32, 4096, seed=78, device=cuda_device)
     o, s_final = _fwd(c)
