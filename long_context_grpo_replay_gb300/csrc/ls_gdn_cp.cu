@@ -1,4 +1,7 @@
-// Gated-DeltaNet replay in chunk-parallel form (forward and backward).
+// Gated-DeltaNet replay in chunk-parallel form (forward and backward): the
+// recurrent layers of the Qwen path replayed from the captured prompt state
+// (LongStraw DeepRead summary, section Method), the gated delta rule of
+// ls_gdn.cu rewritten over chunks.
 //
 // With chunks of C = 128 tokens, per chunk: c_t the running sum of the
 // log-decays, gamma_t = exp(c_t), Gamma_ts = exp(c_t - c_s), w_t = gamma_C /
