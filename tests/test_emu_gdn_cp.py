@@ -193,3 +193,25 @@ def test_edge_lengths_match_the_oracle(emulator, B, H, R):
         for name in got:
             gm = got[name].reshape((B,) + want[name].shape)[m]
             assert rel(gm, want[name]) <= TOL_BF16, (name, rel(gm, want[name]))
+
+
+def test_bench_length_matches_the_oracle(emulator):
+    """One head of one member at the benchmark's 4096 tokens (32 chunks):
+    the chains' rounding does not grow over the chunks."""
+    from oracle.gdn import gdn_replay
+
+    exe, d = emulator
+    B, H, R = 1, 1, 4096
+    c = inputs.make_gdn_group(B, H, R, seed=77)
+    status, _, rest = run(exe, d, c, "all")
+    assert status == 0
+    nt, ns, nsc = B * R * H * 128, B * H * 128 * 128, B * R * H
+    got, i = {}, 0
+    for name, n in (("o", nt), ("s_final", ns), ("dq", nt), ("dk", nt), ("dv", nt), ("dg", nsc),
+                    ("dbeta", nsc)):
+        got[name] = rest[i:i + n]
+        i += n
+    a = {x: t.numpy() for x, t in c.items()}
+    want = gdn_replay(a["s0"], a["q"][0], a["k"][0], a["v"][0], a["g"][0], a["beta"][0], a["d_o"][0])
+    errs = {n: rel(got[n].reshape(want[n].shape), want[n]) for n in got}
+    assert all(e <= TOL_BF16 for e in errs.values()), errs
