@@ -140,6 +140,33 @@ def max_over_ranks(ms: float, device) -> float:
     return float(t.item())
 
 
+def replay_config(workload: str, w, world: int, host_pages: int = 0) -> dict:
+    """The config object of a replay line; both arms print the same one."""
+    kv_bytes_pass = w.prompt_len * w.hkv * w.head_dim * 2 * (2 if w.dtype == "bf16" else 4)
+    return {"workload": workload, "prompt_len": w.prompt_len, "resp_lens": list(w.resp_lens),
+            "group": w.group, "hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim,
+            "page_size": w.page_size, "parallelism": f"replicas x{world}",
+            "pages": ("HBM" if host_pages <= 0 else
+                      f"pinned host memory, streamed in chunks of {host_pages} pages "
+                      "(capture outside the timed steps)"),
+            "l2": "inputs larger than L2 (prompt K/V %.1f GiB per pass)" % (kv_bytes_pass / 2**30)}
+
+
+def clock_matched(roof: dict, pk: dict, clocks: dict) -> None:
+    """Adds to a tensor-bound roofline the peak rescaled from the clock the
+    peak was measured at to the median SM clock of this run (the tensor pipe
+    does a fixed amount of work per clock), and the launch time in clocks."""
+    ref_mhz = (pk.get("clocks_under_load") or {}).get("sm_mhz_median")
+    mhz = clocks.get("sm_mhz")
+    if mhz:
+        roof["launch_kcycles"] = round(roof["launch_ms"] * mhz, 1)
+    if roof.get("bound") != "tensor" or not ref_mhz or not mhz:
+        return
+    peak = roof["peak"] * mhz / ref_mhz
+    roof["clock_matched"] = {"peak": round(peak, 1), "frac": roof["achieved"] / peak,
+                             "sm_mhz": mhz, "peak_sm_mhz": ref_mhz}
+
+
 def job_throughput(flops_per_rank_step: float, world: int, ms_step: float) -> float:
     """Whole-job TFLOP/s: every rank processes its own replica (weak scaling)."""
     return flops_per_rank_step * world / (ms_step * 1e-3) / 1e12
@@ -283,6 +310,7 @@ def run_ours(args):
     roof["peak_source"] = f"{pk_src} ({'bf16_tflops_sustained' if roof['bound'] == 'tensor' else 'hbm_gbs'})"
     roof["algorithmic_per_launch"] = flops_launch if roof["bound"] == "tensor" else bytes_launch
     roof["launch_ms"] = per_launch_ms
+    clock_matched(roof, pk, clocks)
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -294,20 +322,22 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, k_pool, v_pool, pt, members, budget_s=args.cpu_budget)
 
+    # the pages' second regime (short responses over the same 2M prefix) and
+    # their memory property (peak memory nearly flat in G), in this process
+    short = mem_g = None
+    if args.workload == DEFAULT_WORKLOAD and host is None and not args.no_extras:
+        short = short_response_leg(args, desc, prompt, ws, stream, dev, pk, clocks)
+        del src, members
+        mem_g = memory_vs_group(w, desc, prompt, ws, stream, dev)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic (seeded N(0,1)/sqrt(d) Q/K/V, N(0,1) dO, random page table)",
-            "config": {"workload": args.workload, "prompt_len": P, "resp_lens": list(w.resp_lens),
-                       "group": G, "hq": hq, "hkv": hkv, "head_dim": d,
-                       "page_size": w.page_size, "parallelism": f"replicas x{world}",
-                       "pages": ("HBM" if host is None else
-                                 f"pinned host memory, streamed in chunks of {args.host_pages} "
-                                 "pages (capture outside the timed steps)"),
-                       "l2": "inputs larger than L2 (prompt K/V %.1f GiB per pass)" %
-                             (kv_bytes_pass / 2**30)},
+            "config": replay_config(args.workload, w, world,
+                                    args.host_pages if host is not None else 0),
             "prompt_kv_gbs": round(kv_gbs, 1),
             "replays_per_s": round(G * world / (ms_step * 1e-3), 4),
             "roofline": roof,
@@ -318,9 +348,142 @@ def run_ours(args):
             "memory": memory,
             "kernels_ms_per_step": {k: round(v[1] / args.steps, 3) for k, v in trace.items()},
         }
+        if short is not None:
+            line["short_response"] = short
+        if mem_g is not None:
+            line["memory_vs_group"] = mem_g
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+SHORT_WORKLOAD = "bf16_p2m_r64_g8"
+
+
+def short_response_leg(args, desc, prompt, ws, stream, dev, pk, clocks):
+    """The KV-streaming regime: G=8 members of 64 tokens over the 2M-position
+    prompt pages already written, timed (steps x group replay, after the
+    warm-up) with CUDA events on the stream.  Reports the forward's and the
+    backward's prompt-K/V GB/s and their fractions of the HBM and tensor
+    peaks, next to the ceiling the arithmetic intensity allows: at R = 64 a
+    prompt-K/V byte carries 384 flop in the forward and 576 in the backward,
+    above the ridge of the measured peaks, so the tensor pipe, not HBM, is the
+    first limit."""
+    import torch
+
+    import long_context_grpo_replay_gb300.binding as ls
+    from long_context_grpo_replay_gb300 import inputs
+
+    w = inputs.WORKLOADS[SHORT_WORKLOAD]
+    G, P, d, hq, hkv = w.group, w.prompt_len, w.head_dim, w.hq, w.hkv
+    members = []
+    for g in range(G):
+        m = inputs.make_member(w, g, dev)
+        R = m["q"].shape[0]
+        m.update(o=torch.empty_like(m["q"]), lse=torch.empty(R, hq, device=dev, dtype=torch.float32),
+                 delta=torch.empty(R, hq, device=dev, dtype=torch.float32),
+                 dq=torch.empty_like(m["q"]), dk=torch.empty_like(m["k"]), dv=torch.empty_like(m["v"]))
+        members.append(m)
+    for _ in range(args.warmup):
+        ls.ls_replay_group(desc, prompt, members, ws, stream)
+    torch.cuda.synchronize()
+    ls.ls_read_device_status(ws)
+    ls.ls_trace_enable(True)
+    ls.ls_trace_reset()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    n = max(3, args.steps)
+    e0.record(stream)
+    for _ in range(n):
+        ls.ls_replay_group(desc, prompt, members, ws, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    trace = ls.kernel_trace()
+    ls.ls_trace_enable(False)
+    ls.ls_read_device_status(ws)
+    ms = e0.elapsed_time(e1) / n
+    peak_t = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_m = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    kv = P * hkv * d * 2 * 2
+    ridge = peak_t * 1e12 / (peak_m * 1e9)
+    out = {"workload": SHORT_WORKLOAD, "prompt_len": P, "resp_len": w.resp_lens[0], "group": G,
+           "steps": n, "ms_per_step": round(ms, 3),
+           "value": round(sum(replay_flops(P, R, hq, d) for R in w.resp_lens) / (ms * 1e-3) / 1e12, 2),
+           "unit": "TFLOP/s", "replays_per_s": round(G / (ms * 1e-3), 2),
+           "peaks": {"hbm_gbs": peak_m, "bf16_tflops_sustained": peak_t,
+                     "ridge_flop_per_byte": round(ridge, 1)}}
+    R = w.resp_lens[0]
+    legs = {}
+    for name, kern, coef in (("fwd", "tc_fwd", 4.0), ("bwd", "tc_bwd_dq", 6.0)):
+        n_l, t_l = trace.get(kern, (0, 0.0))
+        if n_l == 0:
+            continue
+        lms = t_l / n_l
+        fl = coef * R * P * d * hq
+        gbs = kv / (lms * 1e-3) / 1e9
+        intensity = fl / kv
+        legs[name] = lms
+        out[name] = {"kernel": kern, "launch_ms": round(lms, 3), "prompt_kv_gbs": round(gbs, 1),
+                     "hbm_frac": round(gbs / peak_m, 4),
+                     "tflops": round(fl / (lms * 1e-3) / 1e12, 1),
+                     "tensor_frac": round(fl / (lms * 1e-3) / 1e12 / peak_t, 4),
+                     "flop_per_byte": round(intensity, 1),
+                     "hbm_frac_ceiling": round(min(1.0, ridge / intensity), 4)}
+    if "fwd" in legs and "bwd" in legs:
+        gbs = 2 * kv / ((legs["fwd"] + legs["bwd"]) * 1e-3) / 1e9
+        inten = 10.0 * R * P * d * hq / (2 * kv)
+        out["fwd_bwd"] = {"prompt_kv_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak_m, 4),
+                          "flop_per_byte": round(inten, 1),
+                          "hbm_frac_ceiling": round(min(1.0, ridge / inten), 4)}
+    out["kernels_ms_per_step"] = {k: round(v[1] / n, 3) for k, v in trace.items()}
+    out["target"] = "0.75 of HBM asked; the ceiling above is what the intensity allows"
+    del members
+    return out
+
+
+def memory_vs_group(w, desc, prompt, ws, stream, dev):
+    """Peak device memory of one group replay at G = 2 and G = 8 (the
+    default workload's members: 4096 tokens each) with the prompt pages and
+    the workspace resident: the analogue of the pages' 2M-position G=2 vs G=8
+    peaks.  The workspace is sized for the longest member, so the two peaks
+    should differ by the six extra members' own inputs and outputs alone.
+    'non_torch_gib' is device memory in use outside PyTorch's allocator: the
+    library allocates nothing, so it must not move with G either."""
+    import torch
+
+    import long_context_grpo_replay_gb300.binding as ls
+    from long_context_grpo_replay_gb300 import inputs
+
+    res = {}
+    io = {}
+    for G in (2, 8):
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        torch.cuda.reset_peak_memory_stats(dev)
+        members = []
+        for g in range(G):
+            m = inputs.make_member(w, g, dev)
+            R = m["q"].shape[0]
+            m.update(o=torch.empty_like(m["q"]),
+                     lse=torch.empty(R, w.hq, device=dev, dtype=torch.float32),
+                     delta=torch.empty(R, w.hq, device=dev, dtype=torch.float32),
+                     dq=torch.empty_like(m["q"]), dk=torch.empty_like(m["k"]),
+                     dv=torch.empty_like(m["v"]))
+            members.append(m)
+        ls.ls_replay_group(desc, prompt, members, ws, stream)
+        torch.cuda.synchronize(dev)
+        ls.ls_read_device_status(ws)
+        free, total = torch.cuda.mem_get_info(dev)
+        io[G] = sum(t.numel() * t.element_size() for m in members for t in m.values())
+        res[f"G{G}"] = {"peak_allocated_gib": round(torch.cuda.max_memory_allocated(dev) / 2**30, 3),
+                        "members_io_gib": round(io[G] / 2**30, 3),
+                        "non_torch_gib": round((total - free - torch.cuda.memory_reserved(dev))
+                                               / 2**30, 3)}
+        del members
+    res["peak_delta_gib"] = round(res["G8"]["peak_allocated_gib"] - res["G2"]["peak_allocated_gib"], 3)
+    res["extra_members_io_gib"] = round((io[8] - io[2]) / 2**30, 3)
+    res["workspace_gib"] = round(ws.numel() / 2**30, 3)
+    return res
 
 
 def run_e2e(args, w, desc, src, members, k_pool, v_pool, pt, prompt, ws, stream, dev, flops_step,
@@ -351,6 +514,8 @@ def run_e2e(args, w, desc, src, members, k_pool, v_pool, pt, prompt, ws, stream,
     d_src = [src, {k: torch.empty_like(v) for k, v in src.items()}]
     d_mem = [members, [dict(m, **{k: torch.empty_like(m[k]) for k in in_keys + out_keys})
                        for m in members]]
+    # each set's replay reads the page table that set's step copied in
+    prompts = [prompt, ls.prompt_from(k_pool, v_pool, d_src[1]["page_table"], w.prompt_len)]
     copy_stream = torch.cuda.Stream(dev)
     copied = [torch.cuda.Event(), torch.cuda.Event()]
     released = [torch.cuda.Event(), torch.cuda.Event()]
@@ -374,7 +539,7 @@ def run_e2e(args, w, desc, src, members, k_pool, v_pool, pt, prompt, ws, stream,
             stream.wait_event(copied[b])
             ls.ls_kv_page_write(desc, k_pool, v_pool, d_src[b]["page_table"], 0, d_src[b]["k"],
                                 d_src[b]["v"], ws, stream)
-            ls.ls_replay_group(desc, prompt, d_mem[b], ws, stream)
+            ls.ls_replay_group(desc, prompts[b], d_mem[b], ws, stream)
             with torch.cuda.stream(stream):
                 for m, hm in zip(d_mem[b], h_out):
                     for k in out_keys:
@@ -474,9 +639,7 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "prompt_len": w.prompt_len,
-                   "resp_lens": list(w.resp_lens), "group": w.group, "hq": w.hq, "hkv": w.hkv,
-                   "head_dim": w.head_dim, "page_size": w.page_size},
+        "config": replay_config(args.workload, w, world, args.host_pages),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -503,7 +666,7 @@ def run_reference_gdn(args, world):
     from long_context_grpo_replay_gb300 import inputs
     from oracle.gdn import gdn_replay
 
-    B, H, R = GDN_WORKLOADS[args.workload]
+    B, H, R, _ = GDN_WORKLOADS[args.workload]
     n_tok = min(R, 256)
     c = inputs.make_gdn_group(1, 1, n_tok, seed=55)  # same distributions, one (member, head)
     a = {x: t[0] if x != "s0" else t for x, t in c.items()}
@@ -519,7 +682,7 @@ def run_reference_gdn(args, world):
     value = n_tok * args.steps / H / tot  # whole tokens (all H heads) per second
     line = _reference_line(
         args, world, GDN_METRIC, value, "tokens/s", "f64",
-        {"workload": args.workload, "group": B, "heads": H, "resp_len": R, "dk": 128, "dv": 128},
+        gdn_config(args.workload, world),
         f"per step: one head of one member, {n_tok} tokens, forward+backward (float64 torch, "
         f"autograd), scaled to {H} heads", tot / args.steps * 1e3)
     print(json.dumps(line), flush=True)
@@ -556,8 +719,7 @@ def run_reference_prefill(args, world):
     value = 4.0 * w.head_dim * gq * N * args.steps / tot / 1e12
     line = _reference_line(
         args, world, PREFILL_METRIC, value, "TFLOP/s", "f64",
-        {"workload": args.workload, "prompt_len": N, "hq": w.hq, "hkv": w.hkv,
-         "head_dim": w.head_dim, "page_size": w.page_size},
+        prefill_config(args.workload, world),
         f"per step: row {N - 1} of the {gq} query heads of KV head 0 over all {N} keys "
         "(float64 numpy)", tot / args.steps * 1e3)
     print(json.dumps(line), flush=True)
@@ -566,6 +728,14 @@ def run_reference_prefill(args, world):
 PREFILL_WORKLOADS = {"prefill_bf16_p32k": 32768, "prefill_bf16_p256k": 262144,
                      "prefill_bf16_p2m": 2097152}
 PREFILL_METRIC = "prompt prefill (page write + causal attention) TFLOP/s"
+
+
+def prefill_config(workload: str, world: int) -> dict:
+    """The config object of a prefill line; both arms print the same one."""
+    N = PREFILL_WORKLOADS[workload]
+    return {"workload": workload, "prompt_len": N, "hq": 24, "hkv": 4, "head_dim": 256,
+            "page_size": 256, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (Q %.1f GiB)" % (N * 24 * 256 * 2 / 2**30)}
 
 
 def prefill_flops(N, hq, d):
@@ -701,10 +871,7 @@ def run_prefill(args):
             "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1)/sqrt(d) Q/K/V, random page table)",
-            "config": {"workload": args.workload, "prompt_len": N, "hq": hq, "hkv": hkv,
-                       "head_dim": d, "page_size": w.page_size,
-                       "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2 (Q %.1f GiB)" % (q.numel() * 2 / 2**30)},
+            "config": prefill_config(args.workload, world),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clocks,
             "kernels_ms_per_step": {kk: round(vv[1] / args.steps, 3) for kk, vv in trace.items()},
@@ -713,13 +880,34 @@ def run_prefill(args):
         dist.destroy_process_group()
 
 
-GDN_WORKLOADS = {"gdn_f32_h32_r4096_g8": (8, 32, 4096), "gdn_f32_h32_r1024_g4": (4, 32, 1024)}
+# (members, heads, tokens, precision): f32 = the float32 recurrence
+# (LS_GDN_EXACT), tc = the chunkwise tensor-core path (LS_GDN_TENSOR_CORE)
+GDN_WORKLOADS = {"gdn_f32_h32_r4096_g8": (8, 32, 4096, 0), "gdn_f32_h32_r1024_g4": (4, 32, 1024, 0),
+                 "gdn_tc_h32_r4096_g8": (8, 32, 4096, 1), "gdn_tc_h32_r1024_g4": (4, 32, 1024, 1)}
 GDN_METRIC = "GDN state replay (forward+backward) response tokens/s per layer"
-# fp32 FMA lanes: 152 SMs x 128 lanes x 2 flop x 2.07 GHz
-FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def fp32_alu_tflops(dev, clocks) -> tuple:
+    """fp32 FMA peak of this device: SMs (queried) x 128 lanes x 2 flop x the
+    maximum SM clock nvidia-smi reported (2070 MHz when unsampled)."""
+    import torch
+
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clocks.get("sm_max_mhz") or 2070.0
+    return sms * 128 * 2 * mhz * 1e6 / 1e12, sms, mhz
+
 GDN_FWD_FLOP_PER_TOKEN_HEAD = 7   # x dk*dv: S k, the state update, S q
 GDN_BWD_FLOP_PER_TOKEN_HEAD = 20  # x dk*dv: S_t, G, G k, S_t^T dO, <G,S>, dk's two products, G decay
 GDN_CP_BWD_PRODUCTS = 20  # prep 3, chains 5, outputs 12 (128 x 128 x 128 each, per chunk and head)
+
+
+def gdn_config(workload: str, world: int) -> dict:
+    """The config object of a GDN line; both arms print the same one."""
+    B, H, R, prec = GDN_WORKLOADS[workload]
+    return {"workload": workload, "group": B, "heads": H, "resp_len": R, "dk": 128, "dv": 128,
+            "precision": "LS_GDN_EXACT" if prec == 0 else "LS_GDN_TENSOR_CORE",
+            "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (%.1f GiB of q/k/v/dO)" % (4 * B * R * H * 128 * 4 / 2**30)}
 
 
 def run_gdn(args):
@@ -738,21 +926,24 @@ def run_gdn(args):
         dist.init_process_group("nccl", device_id=dev)
     build.build()
     ls.lib()
-    B, H, R = GDN_WORKLOADS[args.workload]
+    B, H, R, prec = GDN_WORKLOADS[args.workload]
     D = 128
     c = inputs.make_gdn_group(B, H, R, seed=55 + 1000 * rank, device=dev)
     o = torch.empty_like(c["v"])
     s_final = torch.empty((B, H, D, D), device=dev, dtype=torch.float32)
     gr = {n: torch.empty_like(c[x]) for n, x in
           (("dq", "q"), ("dk", "k"), ("dv", "v"), ("dg", "g"), ("dbeta", "beta"))}
-    ws = torch.empty(ls.ls_gdn_workspace_size(ls.GdnDesc(B, H, D, D), R), dtype=torch.uint8,
+    ws = torch.empty(ls.ls_gdn_workspace_size(ls.GdnDesc(B, H, D, D, prec), R), dtype=torch.uint8,
                      device=dev)
+    ls.ls_clear_device_status(ws)
     stream = torch.cuda.current_stream(dev)
 
     def step(x):
-        ls.ls_gdn_replay_fwd(x["s0"], x["q"], x["k"], x["v"], x["g"], x["beta"], o, s_final, stream)
+        ls.ls_gdn_replay_fwd(x["s0"], x["q"], x["k"], x["v"], x["g"], x["beta"], o, s_final, stream,
+                             precision=prec)
         ls.ls_gdn_replay_bwd(x["s0"], x["q"], x["k"], x["v"], x["g"], x["beta"], x["d_o"],
-                             gr["dq"], gr["dk"], gr["dv"], gr["dg"], gr["dbeta"], ws, stream)
+                             gr["dq"], gr["dk"], gr["dv"], gr["dg"], gr["dbeta"], ws, stream,
+                             precision=prec)
 
     for _ in range(args.warmup):
         step(c)
@@ -787,11 +978,13 @@ def run_gdn(args):
     achieved = fl_bwd / (launch_ms * 1e-3) / 1e12
     traffic = recorded_traffic("gdn_bwd", args.workload,
                                ROOT / "long_context_grpo_replay_gb300" / "csrc" / "ls_gdn.cu")
-    roof = {"bound": "alu", "achieved": achieved, "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
-            "frac": achieved / FP32_ALU_TFLOPS, "traffic": traffic, "kernel": "gdn_bwd",
-            "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz",
+    alu_peak, sms, alu_mhz = fp32_alu_tflops(dev, clocks)
+    roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+            "frac": achieved / alu_peak, "traffic": traffic, "kernel": "gdn_bwd",
+            "peak_source": f"derived: {sms} SMs (device query) x 128 fp32 lanes x 2 flop x "
+                           f"{alu_mhz:.0f} MHz (maximum SM clock)",
             "algorithmic_per_launch": fl_bwd, "launch_ms": launch_ms}
-    if os.environ.get("LS_GDN_VARIANT", "").startswith("c"):
+    if prec == 1:
         # tensor-core path: the backward's three kernels execute 20 products of
         # 128 x 128 x 128 per (chunk, head, member); the solves are not counted
         nch = -(-R // 128)
@@ -800,9 +993,13 @@ def run_gdn(args):
         peak_t = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
         ach = fl_tc / (launch_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": peak_t, "unit": "TFLOP/s",
-                "frac": ach / peak_t, "traffic": None, "kernel": "gdn_bwd (chunk-parallel)",
+                "frac": ach / peak_t,
+                "traffic": recorded_traffic("gdn_bwd", args.workload, ROOT / "long_context_grpo_replay_gb300"
+                                            / "csrc" / "ls_gdn_cp.cu"),
+                "kernel": "gdn_bwd (chunk-parallel: prep, chain, out)",
                 "peak_source": f"{pk_src} (bf16_tflops_sustained)",
                 "algorithmic_per_launch": fl_tc, "launch_ms": launch_ms}
+        clock_matched(roof, pk, clocks)
 
     e2e = None
     if not args.no_e2e:
@@ -856,12 +1053,9 @@ def run_gdn(args):
             "metric": GDN_METRIC, "value": round(value, 1), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32",
+            "vs_baseline": None, "dtype": "f32" if prec == 0 else "bf16 operands, f32 accumulation",
             "data": "synthetic (seeded unit-norm q/k, N(0,1) v, decay in [0.85,1), beta in [0.05,0.95))",
-            "config": {"workload": args.workload, "group": B, "heads": H, "resp_len": R, "dk": D,
-                       "dv": D, "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2 (%.1f GiB of q/k/v/dO)"
-                             % (4 * c["q"].numel() * 4 / 2**30)},
+            "config": gdn_config(args.workload, world),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clocks,
             "kernels_ms_per_step": {kk: round(vv[1] / args.steps, 3) for kk, vv in trace.items()},
@@ -879,6 +1073,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the short-response leg and the G=2/G=8 memory check")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--host-pages", type=int, default=0,
                     help="keep the prompt pages in pinned host memory, streamed in chunks of "

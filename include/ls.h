@@ -43,10 +43,12 @@
  *  device status word that kernels set on device-side errors.
  *
  *  Errors: every call validates its arguments on the host before any launch
- *  and returns a status; nothing aborts.  Device-side problems (a page-table
- *  entry outside the pool, a bounded wait that ran out) set bits in the
- *  workspace status word and the affected work is skipped; the call itself has
- *  already returned LS_OK by then, so read them with ls_read_device_status().
+ *  and returns a status; nothing aborts.  Device-side problems set bits in
+ *  the workspace status word: a page-table entry outside the pool (that page
+ *  is then treated as holding no keys: nothing is read from it and it adds
+ *  nothing to the softmax), or a bounded wait that ran out (the affected work
+ *  is skipped).  The call itself has already returned LS_OK by then, so read
+ *  them with ls_read_device_status().
  *  ls_last_error() gives a one-line reason for the last failing call on the
  *  calling thread.
  *
@@ -253,23 +255,36 @@ LS_API ls_status ls_sum_parts(int32_t n_parts, int64_t n_elems, const float* par
  * ls_gdn_replay_fwd writes o and, if s_final is non-NULL, the state after the
  * last token.  ls_gdn_replay_bwd returns the gradient of sum(d_o * o) for q,
  * k, v, g and beta (same shapes); none is formed for s0 (the detached prompt
- * state).  It needs ls_gdn_workspace_size() bytes of workspace (16-byte
- * aligned, owned by the caller) for its checkpoints of S.  resp_len == 0 or
- * batch == 0 is a no-op (the forward still copies s0 to s_final when R = 0).
+ * state).  It needs ls_gdn_workspace_size() bytes of workspace (256-byte
+ * aligned, owned by the caller).  The workspace starts with the same 256-byte
+ * device status word as the attention workspace: a bounded device wait that
+ * ran out in the tensor-core path sets it, and ls_read_device_status(ws)
+ * reports it.  resp_len == 0 or batch == 0 is a no-op (the forward still
+ * copies s0 to s_final when R = 0).
+ *
+ * precision selects the kernels (a zeroed desc selects the exact path):
+ *   LS_GDN_EXACT        float32 recurrence, one token at a time; about 1e-7
+ *                       relative error, held to 1e-5 against the float64
+ *                       oracle.
+ *   LS_GDN_TENSOR_CORE  the chunkwise forward and the chunk-parallel
+ *                       backward on tcgen05 tensor cores with bf16 operands
+ *                       and float32 accumulation; about 5e-3 relative error,
+ *                       held to 2e-2 (the bf16 bar).  q, k, v, d_o and the
+ *                       outputs must be 16-byte aligned (else LS_ERR_CUDA).
+ *                       If a bounded device wait gives up in the forward, o
+ *                       and s_final of that (member, head) are set to NaN.
+ * Float32 callers that need the 1e-5 result keep LS_GDN_EXACT.
  * Errors: LS_ERR_UNSUPPORTED for other dk/dv, LS_ERR_INVALID_ARGUMENT for
- * NULL buffers or negative sizes, LS_ERR_WORKSPACE_TOO_SMALL; all before any
- * launch.
- * The environment variable LS_GDN_VARIANT=chunk makes both calls use the
- * tensor-core kernels instead: a chunkwise forward and a chunk-parallel
- * backward (bf16 operands, about 5e-3 relative error; q, k, v, d_o and the
- * outputs 16-byte aligned, else LS_ERR_CUDA).  ls_gdn_workspace_size covers
- * either backward.  It is experimental: its parity is checked on a GB300 for
- * short responses, its speed not yet measured. */
+ * NULL buffers, negative sizes or an unknown precision,
+ * LS_ERR_WORKSPACE_TOO_SMALL; all before any launch. */
+typedef enum { LS_GDN_EXACT = 0, LS_GDN_TENSOR_CORE = 1 } ls_gdn_precision;
+
 typedef struct {
   int32_t batch;
   int32_t heads;
   int32_t dk;
   int32_t dv;
+  int32_t precision; /* ls_gdn_precision */
 } ls_gdn_desc;
 
 LS_API ls_status ls_gdn_workspace_size(const ls_gdn_desc* desc, int32_t resp_len, size_t* bytes);

@@ -21,7 +21,7 @@ __all__ = [
     "desc_for", "prompt_from", "EXPORTED_SYMBOLS", "ls_replay_fwd_noalloc",
     "ls_replay_fwd_noalloc_scratch_bytes", "ls_prompt_prefill", "ls_prompt_prefill_workspace_size",
     "ls_replay_fwd_part", "ls_replay_bwd_part", "ls_sum_parts",
-    "GdnDesc", "ls_gdn_workspace_size", "ls_gdn_replay_fwd", "ls_gdn_replay_bwd",
+    "GdnDesc", "LS_GDN_EXACT", "LS_GDN_TENSOR_CORE", "ls_gdn_workspace_size", "ls_gdn_replay_fwd", "ls_gdn_replay_bwd",
 ]
 
 LS_DTYPE_F32 = 0
@@ -66,9 +66,13 @@ class Member(ctypes.Structure):
                 ("dv", ctypes.c_void_p)]
 
 
+LS_GDN_EXACT = 0
+LS_GDN_TENSOR_CORE = 1
+
+
 class GdnDesc(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("heads", ctypes.c_int32), ("dk", ctypes.c_int32),
-                ("dv", ctypes.c_int32)]
+                ("dv", ctypes.c_int32), ("precision", ctypes.c_int32)]
 
 
 def library_path() -> Path:
@@ -278,9 +282,10 @@ def ls_sum_parts(parts, out, stream=None):
                               _stream(stream)))
 
 
-def _gdn_desc(s0, q):
+def _gdn_desc(s0, q, precision):
     """q [B, R, H, dk] (a group) or [R, H, dk] (one member)."""
-    return GdnDesc(q.shape[0] if q.dim() == 4 else 1, s0.shape[0], s0.shape[2], s0.shape[1])
+    return GdnDesc(q.shape[0] if q.dim() == 4 else 1, s0.shape[0], s0.shape[2], s0.shape[1],
+                   precision)
 
 
 def _resp_len(q):
@@ -288,25 +293,27 @@ def _resp_len(q):
 
 
 def ls_gdn_workspace_size(desc, resp_len) -> int:
-    """desc: GdnDesc(batch, heads, dk, dv)."""
+    """desc: GdnDesc(batch, heads, dk, dv, precision)."""
     out = ctypes.c_size_t(0)
     _check(lib().ls_gdn_workspace_size(ctypes.byref(desc), resp_len, ctypes.byref(out)))
     return out.value
 
 
-def ls_gdn_replay_fwd(s0, q, k, v, g, beta, o, s_final=None, stream=None):
+def ls_gdn_replay_fwd(s0, q, k, v, g, beta, o, s_final=None, stream=None, precision=LS_GDN_EXACT):
     """Gated-DeltaNet replay from the captured state s0 [H, dv, dk] of one
-    member (q [R, H, dk]) or a group (q [B, R, H, dk]); see ls.h.  float32."""
+    member (q [R, H, dk]) or a group (q [B, R, H, dk]); see ls.h.  float32
+    buffers; precision LS_GDN_EXACT or LS_GDN_TENSOR_CORE."""
     _want_f32(s0, q, k, v, g, beta, o, s_final)
-    _check(lib().ls_gdn_replay_fwd(ctypes.byref(_gdn_desc(s0, q)), _ptr(s0), _ptr(q), _ptr(k),
+    _check(lib().ls_gdn_replay_fwd(ctypes.byref(_gdn_desc(s0, q, precision)), _ptr(s0), _ptr(q), _ptr(k),
                                    _ptr(v), _ptr(g), _ptr(beta), _resp_len(q), _ptr(o), _ptr(s_final),
                                    _stream(stream)))
 
 
-def ls_gdn_replay_bwd(s0, q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta, ws, stream=None):
+def ls_gdn_replay_bwd(s0, q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta, ws, stream=None,
+                      precision=LS_GDN_EXACT):
     """Gradients of the replay for q, k, v, g, beta (none for s0; see ls.h)."""
     _want_f32(s0, q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta)
-    _check(lib().ls_gdn_replay_bwd(ctypes.byref(_gdn_desc(s0, q)), _ptr(s0), _ptr(q), _ptr(k),
+    _check(lib().ls_gdn_replay_bwd(ctypes.byref(_gdn_desc(s0, q, precision)), _ptr(s0), _ptr(q), _ptr(k),
                                    _ptr(v), _ptr(g), _ptr(beta), _ptr(d_o), _resp_len(q), _ptr(dq), _ptr(dk),
                                    _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(ws), _nbytes(ws),
                                    _stream(stream)))

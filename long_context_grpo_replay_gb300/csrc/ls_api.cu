@@ -225,16 +225,17 @@ AttnGeom make_geom(const ls_attn_desc& d, const ls_prompt_kv& p, int32_t R, cons
   g.scale_log2 = d.softmax_scale * 1.4426950408889634f;
   g.ns = pl.ns;
   g.split_span = pl.span;
+  g.resp_part = true;
   return g;
 }
 
-// with_resp == false leaves the response keys out of the merge (the causal
-// partial, the last of the ns+1, is still computed); out_dtype is the dtype
-// o is written in.
-ls_status fwd_impl(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const void* q,
-                   const void* k_resp, const void* v_resp, int32_t R, void* o, float* lse,
-                   void* ws, size_t ws_bytes, cudaStream_t s, bool with_resp = true,
-                   int out_dtype = -1) {
+// with_resp == false leaves the response keys out: the causal part (the
+// last of the ns+1) is neither computed nor merged; out_dtype is the dtype o
+// is written in.
+// The host-side checks of a replay forward (nothing is launched).
+ls_status fwd_check(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const void* q,
+                    const void* k_resp, const void* v_resp, int32_t R, const void* o,
+                    const float* lse) {
   LS_CHECK(check_desc(desc));
   LS_CHECK(check_prompt(desc, prompt));
   if (R < 0) return fail(LS_ERR_INVALID_ARGUMENT, "resp_len < 0");
@@ -244,11 +245,21 @@ ls_status fwd_impl(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const v
   if (!aligned(q, 16) || !aligned(k_resp, 16) || !aligned(v_resp, 16) || !aligned(o, 16) ||
       !aligned(lse, 4))
     return fail(LS_ERR_INVALID_ARGUMENT, "element buffers must be 16-byte aligned");
+  return LS_OK;
+}
+
+ls_status fwd_impl(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const void* q,
+                   const void* k_resp, const void* v_resp, int32_t R, void* o, float* lse,
+                   void* ws, size_t ws_bytes, cudaStream_t s, bool with_resp = true,
+                   int out_dtype = -1) {
+  LS_CHECK(fwd_check(desc, prompt, q, k_resp, v_resp, R, o, lse));
+  if (R == 0) return LS_OK;
   const bool tc = use_tc(*desc);
   const Plan pl = make_plan(*desc, prompt->prompt_len, R, device_sms(), tc);
   LS_CHECK(check_ws(ws, ws_bytes, pl.ws_bytes));
   FwdParams fp{};
   fp.g = make_geom(*desc, *prompt, R, pl);
+  fp.g.resp_part = with_resp;
   fp.q = q;
   fp.k_pool = prompt->k_pool;
   fp.v_pool = prompt->v_pool;
@@ -270,9 +281,9 @@ ls_status fwd_impl(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const v
   return LS_OK;
 }
 
-// with_resp == false sums dQ over the prompt parts only and skips the
-// response dK/dV (dk, dv may then be NULL); dq_dtype is the dtype dq is
-// written in.
+// with_resp == false computes and sums dQ over the prompt parts only and
+// skips the response dK/dV (dk, dv may then be NULL); dq_dtype is the dtype
+// dq is written in.
 ls_status bwd_impl(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const void* q,
                    const void* k_resp, const void* v_resp, const void* d_o, const float* lse,
                    const float* delta, int32_t R, void* dq, void* dk, void* dv, void* ws,
@@ -292,6 +303,7 @@ ls_status bwd_impl(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const v
   LS_CHECK(check_ws(ws, ws_bytes, pl.ws_bytes));
   BwdParams bp{};
   bp.g = make_geom(*desc, *prompt, R, pl);
+  bp.g.resp_part = with_resp;
   bp.q = q;
   bp.d_o = d_o;
   bp.lse = lse;
@@ -324,6 +336,15 @@ ls_status bwd_impl(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const v
 }
 
 }  // namespace
+
+ls_status replay_fwd_validate(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const void* q,
+                              const void* k_resp, const void* v_resp, int32_t R, const void* o,
+                              const float* lse, size_t* ws_need) {
+  LS_CHECK(fwd_check(desc, prompt, q, k_resp, v_resp, R, o, lse));
+  *ws_need = R == 0 ? 0
+                    : make_plan(*desc, prompt->prompt_len, R, device_sms(), use_tc(*desc)).ws_bytes;
+  return LS_OK;
+}
 
 // ------------------------------------------------------------------ LaunchScope
 LaunchScope::LaunchScope(int32_t k, cudaStream_t s) : kid(k), stream(s), ev0(nullptr), ev1(nullptr) {
@@ -570,9 +591,18 @@ ls_status check_gdn(const ls_gdn_desc* d) {
   if (!d) return fail(LS_ERR_INVALID_ARGUMENT, "desc is NULL");
   if (d->heads < 0 || d->batch < 0) return fail(LS_ERR_INVALID_ARGUMENT, "heads or batch < 0");
   if (d->batch > 65535) return fail(LS_ERR_UNSUPPORTED, "batch %d > 65535", d->batch);
+  if (d->precision != LS_GDN_EXACT && d->precision != LS_GDN_TENSOR_CORE)
+    return fail(LS_ERR_INVALID_ARGUMENT, "precision %d is not LS_GDN_EXACT or LS_GDN_TENSOR_CORE",
+                d->precision);
   if (!gdn_supported(d->dk, d->dv))
     return fail(LS_ERR_UNSUPPORTED, "dk=%d dv=%d: supported is dk = dv = 128", d->dk, d->dv);
   return LS_OK;
+}
+
+// Backward workspace: the status header, then the kernels' scratch.
+size_t gdn_ws_need(const ls_gdn_desc& d, int32_t R) {
+  return kWsHeader + (d.precision == LS_GDN_TENSOR_CORE ? gdn_cp_workspace_bytes(d.batch, d.heads, R)
+                                                        : gdn_workspace_bytes(d.batch, d.heads, R));
 }
 }  // namespace
 
@@ -580,11 +610,7 @@ ls_status ls_gdn_workspace_size(const ls_gdn_desc* desc, int32_t resp_len, size_
   LS_CHECK(check_gdn(desc));
   if (!bytes) return fail(LS_ERR_INVALID_ARGUMENT, "bytes is NULL");
   if (resp_len < 0) return fail(LS_ERR_INVALID_ARGUMENT, "resp_len < 0");
-  // enough for either backward (the recurrent one, or the chunk-parallel one
-  // that LS_GDN_VARIANT=chunk selects)
-  const size_t a = gdn_workspace_bytes(desc->batch, desc->heads, resp_len);
-  const size_t b = gdn_cp_workspace_bytes(desc->batch, desc->heads, resp_len);
-  *bytes = a > b ? a : b;
+  *bytes = gdn_ws_need(*desc, resp_len);
   return LS_OK;
 }
 
@@ -596,7 +622,7 @@ ls_status ls_gdn_replay_fwd(const ls_gdn_desc* desc, const float* s0, const floa
   if (desc->batch == 0 || desc->heads == 0 || (resp_len == 0 && !s_final)) return LS_OK;
   if (!s0 || (resp_len > 0 && (!q || !k || !v || !g || !beta || !o)))
     return fail(LS_ERR_INVALID_ARGUMENT, "state and token buffers must be non-NULL");
-  if (gdn_chunk_selected())
+  if (desc->precision == LS_GDN_TENSOR_CORE)
     LS_CUDA(launch_gdn_chunk_fwd(desc->batch, desc->heads, resp_len, s0, q, k, v, g, beta, o,
                                  s_final, static_cast<cudaStream_t>(stream)),
             "GDN chunk forward launch");
@@ -616,21 +642,16 @@ ls_status ls_gdn_replay_bwd(const ls_gdn_desc* desc, const float* s0, const floa
   if (desc->batch == 0 || desc->heads == 0 || resp_len == 0) return LS_OK;
   if (!s0 || !q || !k || !v || !g || !beta || !d_o || !dq || !dk || !dv || !dg || !dbeta)
     return fail(LS_ERR_INVALID_ARGUMENT, "backward buffers must be non-NULL");
-  const bool chunk = gdn_chunk_selected();
-  const size_t need = chunk ? gdn_cp_workspace_bytes(desc->batch, desc->heads, resp_len)
-                            : gdn_workspace_bytes(desc->batch, desc->heads, resp_len);
-  if (!ws) return fail(LS_ERR_INVALID_ARGUMENT, "workspace is NULL");
-  if (ws_bytes < need)
-    return fail(LS_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes, need %zu", ws_bytes, need);
-  if (!aligned(ws, 16)) return fail(LS_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
-  if (chunk)
+  LS_CHECK(check_ws(ws, ws_bytes, gdn_ws_need(*desc, resp_len)));
+  uint32_t* status = static_cast<uint32_t*>(ws);
+  float* scratch = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
+  if (desc->precision == LS_GDN_TENSOR_CORE)
     LS_CUDA(launch_gdn_cp_bwd(desc->batch, desc->heads, resp_len, s0, q, k, v, g, beta, d_o, dq, dk,
-                              dv, dg, dbeta, static_cast<float*>(ws),
-                              static_cast<cudaStream_t>(stream)),
+                              dv, dg, dbeta, scratch, status, static_cast<cudaStream_t>(stream)),
             "GDN chunk-parallel backward launch");
   else
     LS_CUDA(launch_gdn_bwd(desc->batch, desc->heads, resp_len, s0, q, k, v, g, beta, d_o, dq, dk,
-                           dv, dg, dbeta, static_cast<float*>(ws), static_cast<cudaStream_t>(stream)),
+                           dv, dg, dbeta, scratch, static_cast<cudaStream_t>(stream)),
             "GDN backward launch");
   return LS_OK;
 }

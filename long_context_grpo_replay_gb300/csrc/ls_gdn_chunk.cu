@@ -326,6 +326,7 @@ __global__ void __launch_bounds__(kThr, 1)
 
   if (!ok) {  // a wait gave up: mark the results so that no caller takes them for data
     if (tid == 0 && fault) atomicExch(fault, 1u);
+    for (int t = 0; t < R; ++t) o[((int64_t)t * H + h) * kD + tid] = __int_as_float(0x7fc00000);
     if (s_final)
       for (int c = 0; c < kD; ++c) s_final[((int64_t)h * kD + tid) * kD + c] = __int_as_float(0x7fc00000);
   } else if (s_final) {
@@ -347,12 +348,6 @@ __global__ void __launch_bounds__(kThr, 1)
 }
 
 }  // namespace
-
-// LS_GDN_VARIANT=chunk selects this kernel for the forward (read per call).
-bool gdn_chunk_selected() {
-  const char* e = getenv("LS_GDN_VARIANT");
-  return e && e[0] == 'c';
-}
 
 cudaError_t launch_gdn_chunk_fwd(int B, int H, int R, const float* s0, const float* q,
                                  const float* k, const float* v, const float* g, const float* beta,

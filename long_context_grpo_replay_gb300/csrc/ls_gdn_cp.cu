@@ -848,7 +848,7 @@ size_t gdn_cp_workspace_bytes(int B, int H, int R) {
 cudaError_t launch_gdn_cp_bwd(int B, int H, int R, const float* s0, const float* q, const float* k,
                               const float* v, const float* g, const float* beta, const float* d_o,
                               float* dq, float* dk, float* dv, float* dg, float* dbeta, float* ws,
-                              cudaStream_t st) {
+                              uint32_t* status, cudaStream_t st) {
   if (B == 0 || H == 0 || R == 0) return cudaSuccess;
   if (H > 65535 || B > 65535) return cudaErrorInvalidValue;  // grid y and z
   for (const void* p : {(const void*)q, (const void*)k, (const void*)v, (const void*)d_o,
@@ -865,13 +865,13 @@ cudaError_t launch_gdn_cp_bwd(int B, int H, int R, const float* s0, const float*
     return e;
   LaunchScope ls(kKGdnBwd, st);
   gdn_cp_prep_kernel<<<dim3(nch, H, B), kThr, kPrepSmem, st>>>(H, R, nch, q, k, v, g, beta, d_o, ws,
-                                                              nullptr);
+                                                              status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gdn_cp_chain_kernel<<<dim3(H, B), kThr, kChainSmem, st>>>(H, R, nch, s0, q, k, g, beta, d_o, ws,
-                                                           nullptr, nullptr);
+                                                           nullptr, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gdn_cp_out_kernel<<<dim3(nch, H, B), kThr, kOutSmem, st>>>(H, R, nch, q, k, v, g, beta, d_o, ws,
-                                                            nullptr, dq, dk, dv, dg, dbeta, nullptr);
+                                                            nullptr, dq, dk, dv, dg, dbeta, status);
   return cudaGetLastError();
 }
 

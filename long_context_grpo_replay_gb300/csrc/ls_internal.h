@@ -19,6 +19,13 @@ enum : uint32_t {
 // Bytes at the head of the workspace reserved for the status word.
 constexpr size_t kWsHeader = 256;
 
+// Runs every host-side check ls_replay_fwd makes (descriptor, prompt,
+// pointers, alignment) without launching anything, and gives the workspace
+// bytes the call needs on the current device.
+ls_status replay_fwd_validate(const ls_attn_desc* desc, const ls_prompt_kv* prompt, const void* q,
+                              const void* k_resp, const void* v_resp, int32_t resp_len,
+                              const void* o, const float* lse, size_t* ws_need);
+
 // Kernel ids used by tracing (ls_trace_read / ls_kernel_name).
 enum KernelId : int32_t {
   kKPageWrite = 0,
@@ -60,7 +67,13 @@ struct AttnGeom {
   float scale_log2;      // scale * log2(e)
   int32_t ns;            // prompt splits (part ns is the response part)
   int64_t split_span;    // prompt keys per split (a multiple of every key tile)
+  bool resp_part;        // compute part ns; false on a context-parallel rank
+                         // that does not hold the response (parts 0..ns-1 only)
 };
+
+// Parts a forward/backward launch covers: the ns prompt splits plus the
+// causal response part when it is wanted.
+inline int launch_parts(const AttnGeom& g) { return g.ns + (g.resp_part ? 1 : 0); }
 
 struct FwdParams {
   AttnGeom g;
@@ -142,17 +155,17 @@ size_t gdn_workspace_bytes(int B, int H, int R);
 cudaError_t launch_gdn_fwd(int B, int H, int R, const float* s0, const float* q, const float* k,
                            const float* v, const float* g, const float* beta, float* o,
                            float* s_final, cudaStream_t st);
-// Chunkwise tensor-core forward (ls_gdn_chunk.cu), selected by LS_GDN_VARIANT=chunk.
-bool gdn_chunk_selected();
+// Chunkwise tensor-core forward (ls_gdn_chunk.cu), precision LS_GDN_TENSOR_CORE.
 cudaError_t launch_gdn_chunk_fwd(int B, int H, int R, const float* s0, const float* q,
                                  const float* k, const float* v, const float* g, const float* beta,
                                  float* o, float* s_final, cudaStream_t st);
 // Chunk-parallel tensor-core backward (ls_gdn_cp.cu), selected with the chunkwise forward.
 size_t gdn_cp_workspace_bytes(int B, int H, int R);
+// status: the workspace status word a wait that gives up sets.
 cudaError_t launch_gdn_cp_bwd(int B, int H, int R, const float* s0, const float* q, const float* k,
                               const float* v, const float* g, const float* beta, const float* d_o,
                               float* dq, float* dk, float* dv, float* dg, float* dbeta, float* ws,
-                              cudaStream_t st);
+                              uint32_t* status, cudaStream_t st);
 cudaError_t launch_gdn_bwd(int B, int H, int R, const float* s0, const float* q, const float* k,
                            const float* v, const float* g, const float* beta, const float* d_o,
                            float* dq, float* dk, float* dv, float* dg, float* dbeta, float* ws,

@@ -43,6 +43,21 @@ extern "C" {
 LS_API ls_status ls_replay_fwd_noalloc(const ls_attn_desc* desc, const ls_prompt_kv* prompt,
                                        const void* q, const void* k_resp, const void* v_resp,
                                        int32_t resp_len, void* o, float* lse, void* stream) {
+  // Every check comes first: a refused call enqueues nothing and leaves the
+  // scratch (and a status word an earlier call may still be setting) alone.
+  size_t need = 0;
+  const ls_status vs =
+      ls::replay_fwd_validate(desc, prompt, q, k_resp, v_resp, resp_len, o, lse, &need);
+  if (vs != LS_OK) return vs;
+  if (resp_len == 0) return LS_OK;
+  if (need > kScratchBytes) {
+    snprintf(g_noalloc_err, sizeof(g_noalloc_err),
+             "ls_replay_fwd_noalloc: this call needs %zu bytes of scratch, more than the fixed "
+             "%zu-byte (64 MiB) scratch; use ls_replay_fwd with a caller-owned workspace",
+             need, kScratchBytes);
+    ls::set_last_error(g_noalloc_err);
+    return LS_ERR_WORKSPACE_TOO_SMALL;
+  }
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -69,26 +84,16 @@ LS_API ls_status ls_replay_fwd_noalloc(const ls_attn_desc* desc, const ls_prompt
     scratch = g_scratch_addr[dev];
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (resp_len > 0) {
-    e = cudaMemsetAsync(scratch, 0, ls::kWsHeader, s);  // status word starts at zero
-    if (e != cudaSuccess) {
-      snprintf(g_noalloc_err, sizeof(g_noalloc_err),
-               "ls_replay_fwd_noalloc: clearing the scratch status failed (%s)",
-               cudaGetErrorString(e));
-      ls::set_last_error(g_noalloc_err);
-      return LS_ERR_CUDA;
-    }
-  }
-  const ls_status st = ls_replay_fwd(desc, prompt, q, k_resp, v_resp, resp_len, o, lse, scratch,
-                                     kScratchBytes, stream);
-  if (st == LS_ERR_WORKSPACE_TOO_SMALL) {
+  e = cudaMemsetAsync(scratch, 0, ls::kWsHeader, s);  // status word starts at zero
+  if (e != cudaSuccess) {
     snprintf(g_noalloc_err, sizeof(g_noalloc_err),
-             "ls_replay_fwd_noalloc: this call needs more than the fixed %zu-byte (64 MiB) scratch "
-             "(%s); use ls_replay_fwd with a caller-owned workspace",
-             kScratchBytes, ls_last_error());
+             "ls_replay_fwd_noalloc: clearing the scratch status failed (%s)",
+             cudaGetErrorString(e));
     ls::set_last_error(g_noalloc_err);
+    return LS_ERR_CUDA;
   }
-  return st;
+  return ls_replay_fwd(desc, prompt, q, k_resp, v_resp, resp_len, o, lse, scratch, kScratchBytes,
+                       stream);
 }
 
 size_t ls_replay_fwd_noalloc_scratch_bytes(void) { return kScratchBytes; }

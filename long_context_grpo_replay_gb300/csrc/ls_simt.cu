@@ -166,6 +166,14 @@ __device__ __forceinline__ void part_range(const AttnGeom& g, int part, int64_t 
   }
 }
 
+// Whether prompt key `key` (< prompt_len) lies on a page inside the pool; a
+// key on a page outside it is no key at all (its page was skipped and the
+// status word flagged).
+__device__ __forceinline__ bool prompt_key_ok(const AttnGeom& g, const int32_t* pt, int64_t key) {
+  const int32_t slot = __ldg(pt + key / g.page_size);
+  return slot >= 0 && slot < g.pool_pages;
+}
+
 // Stage keys kb..kb+31 of the range into sK/sV ([kKC][D+1] float32).
 template <typename T, int D>
 __device__ __forceinline__ void stage_keys(const AttnGeom& g, bool resp, int kvh, int64_t kb,
@@ -239,7 +247,7 @@ __global__ void __launch_bounds__(kNW * 32) simt_fwd_kernel(FwdParams p, int par
 #pragma unroll 8
     for (int x = 0; x < D; ++x) s = fmaf(sQ[warp * D + x], sK[lane * DP + x], s);
     const int64_t key = kb + lane;
-    const bool valid = key < ke && (!resp || key <= r);
+    const bool valid = key < ke && (resp ? key <= r : prompt_key_ok(g, p.page_table, key));
     const float s2 = valid ? s * g.scale_log2 : -CUDART_INF_F;
     const float m_new = fmaxf(m, warp_max(s2));
     if (m_new == -CUDART_INF_F) continue;
@@ -315,7 +323,7 @@ __global__ void __launch_bounds__(kNW * 32) simt_bwd_dq_kernel(BwdParams p, int 
       dp = fmaf(sO[warp * D + x], sV[lane * DP + x], dp);
     }
     const int64_t key = kb + lane;
-    const bool valid = key < ke && (!resp || key <= r);
+    const bool valid = key < ke && (resp ? key <= r : prompt_key_ok(g, p.page_table, key));
     const float pj = valid ? exp2f(s * g.scale_log2 - lse2) : 0.f;
     const float ds = pj * (dp - dl);
     for (int j = 0; j < kKC; ++j) {
@@ -421,6 +429,7 @@ size_t dkdv_smem() { return sizeof(float) * (2 * 32 * (D + 1) + 2 * kNW * D + 64
 
 template <typename T, int D>
 cudaError_t fwd_impl(const FwdParams& p, int part0, int nparts, cudaStream_t s) {
+  if (nparts <= 0) return cudaSuccess;
   const size_t sm = fwd_smem<T, D>();
   cudaError_t e = cudaFuncSetAttribute(simt_fwd_kernel<T, D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
@@ -434,6 +443,7 @@ cudaError_t fwd_impl(const FwdParams& p, int part0, int nparts, cudaStream_t s) 
 
 template <typename T, int D>
 cudaError_t bwd_impl(const BwdParams& p, int part0, int nparts, cudaStream_t s) {
+  if (nparts <= 0) return cudaSuccess;
   const size_t sm = bwd_smem<T, D>();
   cudaError_t e = cudaFuncSetAttribute(simt_bwd_dq_kernel<T, D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
@@ -544,13 +554,13 @@ cudaError_t launch_dq_reduce(int n_parts, int64_t n_rows, int d, float scale,
 }
 
 cudaError_t launch_simt_fwd(int dtype, const FwdParams& p, cudaStream_t s) {
-  LS_DISPATCH(fwd_impl, dtype, p.g.d, p, 0, p.g.ns + 1, s);
+  LS_DISPATCH(fwd_impl, dtype, p.g.d, p, 0, launch_parts(p.g), s);
 }
 cudaError_t launch_simt_fwd_resp(int dtype, const FwdParams& p, cudaStream_t s) {
   LS_DISPATCH(fwd_impl, dtype, p.g.d, p, p.g.ns, 1, s);
 }
 cudaError_t launch_simt_bwd_dq(int dtype, const BwdParams& p, cudaStream_t s) {
-  LS_DISPATCH(bwd_impl, dtype, p.g.d, p, 0, p.g.ns + 1, s);
+  LS_DISPATCH(bwd_impl, dtype, p.g.d, p, 0, launch_parts(p.g), s);
 }
 cudaError_t launch_simt_bwd_dq_resp(int dtype, const BwdParams& p, cudaStream_t s) {
   LS_DISPATCH(bwd_impl, dtype, p.g.d, p, p.g.ns, 1, s);

@@ -6,12 +6,11 @@
 // memory, streams the part's key pages, recomputes P from the stored LSE and
 // accumulates dQ in tensor memory.  No score matrix is kept between tiles.
 //
-// Two kernels share that plan.  The default keeps dO in tensor memory as the
-// A operand of dP = dO V^T, which leaves room for three V stages in shared
-// memory; the older one (selected by LS_TC_BWD_VARIANT) keeps Q and dO in
-// shared memory.  Per key tile j (BN keys):
+// The kernel keeps dO in tensor memory as the A operand of dP = dO V^T,
+// which leaves room for three K stages in shared memory.  Per key tile j
+// (BN keys):
 //   S_j  = Q K_j^T            (tcgen05, SS)        -> TMEM S
-//   dP_j = dO V_j^T           (tcgen05, TS or SS)  -> TMEM dP
+//   dP_j = dO V_j^T           (tcgen05, TS)        -> TMEM dP
 //   softmax warps: P = exp2(S*scale*log2e - LSE*log2e), dS = P * (dP - delta),
 //                  dS (bf16) written back into tensor memory
 //   dQ  += dS_j K_j           (tcgen05, A from TMEM, K as N-major B operand)
@@ -44,23 +43,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-template <int BN, int KSK, int KSV>
-struct BwdLayout {
-  static constexpr uint32_t kRowTile = kBM * kD * 2;  // 64 KB, 4 boxes [128 x 64]
-  static constexpr uint32_t kRowBox = kBM * 128;
-  static constexpr uint32_t kKVBytes = BN * kD * 2;
-  static constexpr uint32_t kKVBox = BN * 128;
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kO = kQ + kRowTile;  // dO
-  static constexpr uint32_t kK = kO + kRowTile;
-  static constexpr uint32_t kV = kK + KSK * kKVBytes;
-  static constexpr uint32_t kEnd = kV + KSV * kKVBytes;
-  static constexpr uint32_t kSmem = kEnd + 1024;
-  static constexpr uint32_t kTmemS = 256;  // buffer b: S at kTmemS + b*2*BN, dP at +BN
-  static_assert(kTmemS + 4 * BN <= 512, "tensor memory budget");
-  static_assert(kSmem <= 227 * 1024 - 512, "shared memory budget");
-};
-
 struct BwdKParams {
   int32_t hq, hkv, gq, R;
   int64_t P;
@@ -79,339 +61,6 @@ struct BwdKParams {
   float* dq_parts;
   uint32_t* status;
 };
-
-template <int BN, int KSK, int KSV>
-__global__ void __launch_bounds__(kThreads, 1)
-    tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV,
-                     const __grid_constant__ CUtensorMap tmKr,
-                     const __grid_constant__ CUtensorMap tmVr, const BwdKParams p) {
-  using L = BwdLayout<BN, KSK, KSV>;
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_kf[KSK], bar_ke[KSK], bar_vf[KSV], bar_ve[KSV], bar_sd[2],
-      bar_ds[2], bar_fin, bar_drain;
-  __shared__ uint32_t tmem_base_s;
-  __shared__ uint32_t abort_s;
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sQ = sbase + L::kQ, sO = sbase + L::kO, sK = sbase + L::kK, sV = sbase + L::kV;
-
-  // parts 0..ns-1: prompt key ranges; part ns: the causal response keys
-  const int mt = blockIdx.x % p.n_mt;
-  const int kvh = (blockIdx.x / p.n_mt) % p.hkv;
-  const int part = blockIdx.x / (p.n_mt * p.hkv);
-  const bool resp = part == p.ns;
-  const int64_t rows_g = (int64_t)p.gq * p.R;
-  int64_t kb, ke;
-  if (!resp) {
-    kb = (int64_t)part * p.split_span;
-    ke = kb + p.split_span < p.P ? kb + p.split_span : p.P;
-  } else {
-    const int64_t t0 = (int64_t)mt * kBM;
-    const int64_t t1 = (t0 + kBM < rows_g ? t0 + kBM : rows_g) - 1;
-    kb = 0;
-    ke = (t0 / p.R == t1 / p.R) ? (t1 % p.R) + 1 : p.R;
-  }
-  const int ntiles = ke > kb ? (int)((ke - kb + BN - 1) / BN) : 0;
-
-  if (tid == 0) {
-    abort_s = 0;
-    mbar_init(smem_u32(&bar_q), 128);
-    for (int s = 0; s < KSK; ++s) {
-      mbar_init(smem_u32(&bar_kf[s]), 1);
-      mbar_init(smem_u32(&bar_ke[s]), 1);
-    }
-    for (int s = 0; s < KSV; ++s) {
-      mbar_init(smem_u32(&bar_vf[s]), 1);
-      mbar_init(smem_u32(&bar_ve[s]), 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&bar_sd[b]), 1);
-      mbar_init(smem_u32(&bar_ds[b]), 128);
-    }
-    mbar_init(smem_u32(&bar_fin), 1);
-    mbar_init(smem_u32(&bar_drain), 1);
-    fence_mbar_init();
-  }
-  if (warp == 2) {
-    tmem_alloc(smem_u32(&tmem_base_s), 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = tmem_base_s;
-  const volatile uint32_t* abortp = &abort_s;
-  // a wait that gives up records its kernel and source line in status[1]
-  auto fail = [&](int line) {
-    atomicOr(p.status, kStatusTimeout);
-    atomicCAS(p.status + 1, 0u, ((uint32_t)kKTcBwdDq << 16) | (uint32_t)line);
-    abort_s = 1;
-  };
-  auto pool_row = [&](int64_t key0) -> int32_t {
-    const int32_t slot = __ldg(p.page_table + key0 / p.page_size);
-    if (slot < 0 || slot >= p.pool_pages) {
-      if (lane == 0) atomicOr(p.status, kStatusBadPage);
-      return (int32_t)p.pool_rows;
-    }
-    return (int32_t)(((int64_t)slot * p.hkv + kvh) * p.page_size + key0 % p.page_size);
-  };
-
-  if (warp == 0 || warp == 3) {
-    // ------------------------------------------------------------ producers
-    // whole warps: lane 0 posts the expected bytes, lanes 0..3 each issue one
-    // of the tile's four boxes in parallel
-    if (ntiles > 0) {
-      const bool isK = warp == 0;
-      const int nst = isK ? KSK : KSV;
-      const CUtensorMap* tm = resp ? (isK ? &tmKr : &tmVr) : (isK ? &tmK : &tmV);
-      uint64_t* full = isK ? bar_kf : bar_vf;
-      uint64_t* empty = isK ? bar_ke : bar_ve;
-      const uint32_t sdst = isK ? sK : sV;
-      if (lane == 0) prefetch_tmap(tm);
-      int issued = 0;
-      for (int j = 0; j < ntiles; ++j) {
-        const int st = j % nst;
-        if (j >= nst && !mbar_wait_warp(smem_u32(&empty[st]), ((j / nst) - 1) & 1, abortp)) {
-          fail(__LINE__);
-          break;
-        }
-        const int64_t key0 = kb + (int64_t)j * BN;
-        const uint32_t fb = smem_u32(&full[st]);
-        const int32_t row = resp ? 0 : pool_row(key0);
-        if (lane == 0) mbar_expect_tx(fb, L::kKVBytes);
-        __syncwarp();
-        if (lane < kD / 64) {
-          const int c = lane;
-          if (resp)
-            tma_load_3d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, kvh, (int32_t)key0);
-          else
-            tma_load_2d(sdst + st * L::kKVBytes + c * L::kKVBox, tm, fb, c * 64, row);
-        }
-        __syncwarp();
-        issued = j + 1;
-      }
-      for (int j = issued - nst < 0 ? 0 : issued - nst; j < issued; ++j)
-        mbar_wait(smem_u32(&full[j % nst]), (j / nst) & 1, abortp);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && ntiles > 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(kBM, BN, false);
-      constexpr uint32_t idesc_dq = idesc_bf16(kBM, kD, true);
-      bool ok = mbar_wait(smem_u32(&bar_q), 0, abortp);
-      if (!ok) fail(__LINE__);
-      for (int j = 0; ok && j <= ntiles; ++j) {
-        if (j < ntiles) {
-          // S_j = Q K_j^T
-          const int st = j % KSK, b = j & 1;
-          if (!mbar_wait(smem_u32(&bar_kf[st]), (j / KSK) & 1, abortp)) { fail(__LINE__); break; }
-          tc_fence_after();
-          const uint32_t dS = tbase + L::kTmemS + b * 2 * BN;
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * L::kRowBox + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd =
-                sdesc_sw128(sK + st * L::kKVBytes + (kk >> 2) * L::kKVBox + (kk & 3) * 32, 16, 1024);
-            mma_ss(dS, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-          }
-        }
-        if (j >= 1) {
-          // dQ += dS_{j-1} K_{j-1}
-          const int i = j - 1, st = i % KSK, b = i & 1;
-          if (!mbar_wait(smem_u32(&bar_ds[b]), (i >> 1) & 1, abortp)) { fail(__LINE__); break; }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint64_t bd = sdesc_sw128(sK + st * L::kKVBytes + kk * 16 * 128, L::kKVBox, 1024);
-            mma_ts(tbase, tbase + L::kTmemS + b * 2 * BN + kk * 8, bd, idesc_dq,
-                   (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(smem_u32(&bar_ke[st]));
-          if (i == ntiles - 1) mma_commit(smem_u32(&bar_fin));
-        }
-        if (j < ntiles) {
-          // dP_j = dO V_j^T
-          const int st = j % KSV, b = j & 1;
-          if (!mbar_wait(smem_u32(&bar_vf[st]), (j / KSV) & 1, abortp)) { fail(__LINE__); break; }
-          tc_fence_after();
-          const uint32_t dP = tbase + L::kTmemS + b * 2 * BN + BN;
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(sO + (kk >> 2) * L::kRowBox + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd =
-                sdesc_sw128(sV + st * L::kKVBytes + (kk >> 2) * L::kKVBox + (kk & 3) * 32, 16, 1024);
-            mma_ss(dP, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(smem_u32(&bar_ve[st]));
-          mma_commit(smem_u32(&bar_sd[b]));
-        }
-      }
-      mma_commit(smem_u32(&bar_drain));
-      mbar_wait(smem_u32(&bar_drain), 0, abortp);
-    }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax
-    const int i = tid - 128;
-    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
-    const int64_t t = (int64_t)mt * kBM + i;
-    const bool row_ok = t < rows_g;
-    const int hh = row_ok ? (int)(t / p.R) : 0;
-    const int r = row_ok ? (int)(t % p.R) : 0;
-    const int64_t n = (int64_t)r * p.hq + (int64_t)kvh * p.gq + hh;
-    const float lse2 = row_ok ? __ldg(p.lse + n) * kLog2ef : 0.f;
-    const float dl = row_ok ? __ldg(p.delta + n) : 0.f;
-    {
-      const int wq = warp - 4;
-      for (int rr = 0; rr < 32; ++rr) {
-        const int row = wq * 32 + rr;
-        const int64_t tt = (int64_t)mt * kBM + row;
-        uint4 vq = make_uint4(0u, 0u, 0u, 0u), vo = vq;
-        if (tt < rows_g) {
-          const int hh2 = (int)(tt / p.R), r2 = (int)(tt % p.R);
-          const int64_t n2 = (int64_t)r2 * p.hq + (int64_t)kvh * p.gq + hh2;
-          vq = __ldg(reinterpret_cast<const uint4*>(p.q + n2 * kD) + lane);
-          vo = __ldg(reinterpret_cast<const uint4*>(p.d_o + n2 * kD) + lane);
-        }
-        const uint32_t off = (lane >> 3) * L::kRowBox + sw128_offset(row, lane & 7);
-        st_shared_v4(sQ + off, vq);
-        st_shared_v4(sO + off, vo);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&bar_q));
-    }
-
-    bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
-      const int b = j & 1;
-      if (!mbar_wait_warp(smem_u32(&bar_sd[b]), (j >> 1) & 1, abortp)) { fail(__LINE__); ok = false; break; }
-      tc_fence_after();
-      const int64_t key0 = kb + (int64_t)j * BN;
-      const int64_t lim = resp ? (int64_t)r + 1 : ke;  // causal limit for the response part
-      const int nvalid = (int)(lim - key0 < 0 ? 0 : (lim - key0 < BN ? lim - key0 : BN));
-      const int nvalid_tile = (int)(ke - key0 < BN ? ke - key0 : BN);
-      uint32_t ds_pk[BN / 2];
-#pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t rs[32], rp[32];
-        tmem_ld32(tbase + lane_off + L::kTmemS + b * 2 * BN + c0, rs);
-        tmem_ld32(tbase + lane_off + L::kTmemS + b * 2 * BN + BN + c0, rp);
-        tmem_wait_ld_r(rs);
-        reg_dep(rp);
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float ds2[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const bool valid = c0 + c + u < nvalid;
-            const float pv = ex2(__uint_as_float(rs[c + u]) * p.scale_log2 - lse2);
-            ds2[u] = valid ? pv * (__uint_as_float(rp[c + u]) - dl) : 0.f;
-          }
-          ds_pk[(c0 + c) >> 1] = pack_bf16x2(ds2[0], ds2[1]);
-        }
-      }
-#pragma unroll
-      for (int c0 = 0; c0 < BN / 2; c0 += 16)
-        tmem_st16(tbase + lane_off + L::kTmemS + b * 2 * BN + c0, ds_pk + c0);
-      tmem_wait_st();
-      if (!resp && nvalid_tile < BN) {
-        // Partial last prompt tile: rows past the prompt end may hold
-        // anything; zero them in K so that dS=0 times K stays 0 in dQ += dS K.
-        const int st = j % KSK;
-        const int nz = (BN - nvalid_tile) * (kD / 64) * 8;
-        for (int z = i; z < nz; z += 128) {
-          const int row = nvalid_tile + z / ((kD / 64) * 8);
-          const int box = (z / 8) % (kD / 64);
-          st_shared_v4(sK + st * L::kKVBytes + box * L::kKVBox + row * 128 + (z & 7) * 16,
-                       make_uint4(0u, 0u, 0u, 0u));
-        }
-        fence_proxy_async_smem();
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_ds[b]));
-    }
-
-    // ---- epilogue: unscaled float32 dQ partial
-    if (ok && ntiles > 0) {
-      if (!mbar_wait_warp(smem_u32(&bar_fin), 0, abortp)) { fail(__LINE__); ok = false; }
-      tc_fence_after();
-    }
-    const int64_t nrows = (int64_t)p.R * p.hq;
-    float* out = p.dq_parts + ((int64_t)part * nrows + n) * kD;
-#pragma unroll 1
-    for (int c0 = 0; c0 < kD; c0 += 32) {
-      uint32_t rr[32];
-      __syncwarp();  // the row_ok stores of the previous chunk diverge
-      if (ok && ntiles > 0) {
-        tmem_ld32(tbase + lane_off + c0, rr);
-        tmem_wait_ld_r(rr);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) rr[c] = 0u;
-      }
-      if (row_ok) {
-#pragma unroll
-        for (int c = 0; c < 32; c += 4)
-          *reinterpret_cast<float4*>(out + c0 + c) =
-              make_float4(__uint_as_float(rr[c]), __uint_as_float(rr[c + 1]),
-                          __uint_as_float(rr[c + 2]), __uint_as_float(rr[c + 3]));
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 2) {
-    tc_fence_after();
-    tmem_dealloc(tbase, 512);
-  }
-}
-
-template <int BN, int KSK, int KSV>
-cudaError_t bwd_variant(const BwdParams& a, cudaStream_t s) {
-  using L = BwdLayout<BN, KSK, KSV>;
-  const AttnGeom& g = a.g;
-  BwdKParams p;
-  p.hq = g.hq;
-  p.hkv = g.hkv;
-  p.gq = g.gq;
-  p.R = g.R;
-  p.P = g.P;
-  p.pool_pages = g.pool_pages;
-  p.pool_rows = g.pool_pages * g.hkv * g.page_size;
-  p.page_size = g.page_size;
-  p.ns = g.ns;
-  p.split_span = g.split_span;
-  p.n_mt = (int)(((int64_t)g.gq * g.R + kBM - 1) / kBM);
-  p.scale_log2 = g.scale_log2;
-  p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
-  p.d_o = reinterpret_cast<const __nv_bfloat16*>(a.d_o);
-  p.lse = a.lse;
-  p.delta = a.delta;
-  p.page_table = a.page_table;
-  p.dq_parts = a.dq_parts;
-  p.status = a.status;
-  CUtensorMap tk, tv, tkr, tvr;
-  memset(&tk, 0, sizeof(tk));
-  memset(&tv, 0, sizeof(tv));
-  if (g.P > 0 && (!encode_pool_map(&tk, a.k_pool, p.pool_rows, BN) ||
-                  !encode_pool_map(&tv, a.v_pool, p.pool_rows, BN)))
-    return cudaErrorInvalidValue;
-  if (!encode_rows_map(&tkr, a.k_resp, g.hkv, g.R, BN) ||
-      !encode_rows_map(&tvr, a.v_resp, g.hkv, g.R, BN))
-    return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(tc_bwd_dq_kernel<BN, KSK, KSV>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kSmem);
-  if (e != cudaSuccess) return e;
-  const int64_t units = (int64_t)(g.ns + 1) * g.hkv * p.n_mt;
-  if (units == 0) return cudaSuccess;
-  LaunchScope ls(kKTcBwdDq, s);
-  tc_bwd_dq_kernel<BN, KSK, KSV><<<(unsigned)units, kThreads, L::kSmem, s>>>(tk, tv, tkr, tvr, p);
-  return cudaGetLastError();
-}
-
 
 // ===========================================================================
 // Backward with dO held in tensor memory (default).  dP = dO V^T takes dO as
@@ -671,10 +320,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
+      const int64_t key0 = kb + (int64_t)j * BN;
+      // a tile whose page id lies outside the pool holds no keys (zeros were
+      // loaded for it and the status word flagged); read before the wait
+      const int32_t tslot = resp ? 0 : __ldg(p.page_table + key0 / p.page_size);
       if (!mbar_wait_warp(smem_u32(&bar_sf), j & 1, abortp)) { fail(__LINE__); ok = false; break; }
       tc_fence_after();
-      const int64_t key0 = kb + (int64_t)j * BN;
-      const int64_t lim = resp ? (int64_t)r + 1 : ke;
+      const int64_t lim = resp ? (int64_t)r + 1 : (tslot >= 0 && tslot < p.pool_pages ? ke : key0);
       const int nvalid = (int)(lim - key0 < 0 ? 0 : (lim - key0 < BN ? lim - key0 : BN));
       const int nvalid_tile = (int)(ke - key0 < BN ? ke - key0 : BN);
       float pv[BN];
@@ -797,32 +449,15 @@ cudaError_t bwd_tm(const BwdParams& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_dq_tm_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kSmem);
   if (e != cudaSuccess) return e;
-  const int64_t units = (int64_t)(g.ns + 1) * g.hkv * p.n_mt;
+  const int64_t units = (int64_t)launch_parts(g) * g.hkv * p.n_mt;
   if (units == 0) return cudaSuccess;
   LaunchScope ls(kKTcBwdDq, s);
   tc_bwd_dq_tm_kernel<<<(unsigned)units, kThreads, L::kSmem, s>>>(tk, tv, tkr, tvr, p);
   return cudaGetLastError();
 }
 
-int bwd_variant_id() {
-  static int v = [] {
-    const char* e = getenv("LS_TC_BWD_VARIANT");
-    return e ? atoi(e) : 0;
-  }();
-  return v;
-}
-
 }  // namespace
 
-// Default: dO in tensor memory with three V stages.  LS_TC_BWD_VARIANT
-// selects the shared-memory-dO kernels for comparison: 1 = 64-key tiles (two
-// K stages, one V stage), 2 = 32-key tiles.
-cudaError_t launch_tc_bwd_dq(const BwdParams& a, cudaStream_t s) {
-  switch (bwd_variant_id()) {
-    case 1: return bwd_variant<64, 2, 1>(a, s);
-    case 2: return bwd_variant<32, 3, 3>(a, s);
-    default: return bwd_tm(a, s);
-  }
-}
+cudaError_t launch_tc_bwd_dq(const BwdParams& a, cudaStream_t s) { return bwd_tm(a, s); }
 
 }  // namespace ls

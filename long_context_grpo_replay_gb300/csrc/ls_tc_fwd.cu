@@ -11,22 +11,18 @@
 // the part, merged exactly afterwards by the LSE-merge kernel (the global
 // LSE and output merge of the LongStraw DeepRead summary, section Method).
 //
-// Two kernels share that plan.  tc_fwd_ring_kernel (the default, further
-// down) streams K and V through a ring of 32 KB chunks and runs eight softmax
-// warps.  tc_fwd_kernel (selected by LS_TC_FWD_VARIANT) is the staged design
-// it grew from, with these warp roles (256 threads):
-//   warp 0        : TMA producer for K tiles (one instruction per tile)
-//   warp 3        : TMA producer for V tiles
-//   warp 1 lane 0 : MMA issuer: S[b] = Q K^T (SS), O += P V (P from shared or
-//                   tensor memory, V as an N-major B operand)
+// tc_fwd_ring_kernel streams K and V through a ring of 32 KB chunks.  Warp
+// roles (384 threads):
+//   warp 0        : TMA producer for K and V (one instruction per chunk)
+//   warp 1 lane 0 : MMA issuer: S[b] = Q K^T (SS), O += P V (P from tensor
+//                   memory, V as an N-major B operand)
 //   warp 2        : tensor-memory allocation / release
-//   warps 4-7     : softmax; thread i owns query row i (TMEM lane i): reads S,
-//                   masks, keeps the running max/sum in the log2 domain with
+//   warps 4-11    : softmax, two threads per query row (TMEM lane): read S,
+//                   mask, keep the running max/sum in the log2 domain with
 //                   lazy rescaling (the running max only moves when the tile
 //                   max exceeds it by more than 8, so exp2 stays below 256),
-//                   writes P as bf16 and finally normalises O.
-// Tensor memory (both kernels): O in columns [0,256), S double-buffered at
-// 256 + b*BN.
+//                   write P as bf16 and finally normalise O.
+// Tensor memory: O in columns [0,256), S double-buffered at 256 + b*128.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math_constants.h>
@@ -53,24 +49,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-template <int BN, int KST, bool P_TMEM>
-struct FwdLayout {
-  static constexpr uint32_t kQBytes = kBM * kD * 2;   // 64 KB: 4 boxes [128 x 64]
-  static constexpr uint32_t kQBox = kBM * 128;         // 16 KB
-  static constexpr uint32_t kKVBytes = BN * kD * 2;    // one K or V tile
-  static constexpr uint32_t kKVBox = BN * 128;         // [BN x 64] box
-  static constexpr uint32_t kPBytes = kBM * BN * 2;    // P tile [128 x BN]
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + kQBytes;
-  static constexpr uint32_t kV = kK + KST * kKVBytes;
-  static constexpr uint32_t kP = kV + KST * kKVBytes;
-  static constexpr uint32_t kEnd = kP + (P_TMEM ? 0u : 2u * kPBytes);
-  static constexpr uint32_t kSmem = kEnd + 1024;  // slack for 1 KB alignment
-  static constexpr uint32_t kTmemS = 256;
-  static_assert(kTmemS + 2 * BN <= 512, "tensor memory budget");
-  static_assert(kSmem <= 227 * 1024 - 512, "shared memory budget");
-};
-
 struct FwdKParams {
   int32_t hq, hkv, gq, R;
   int64_t P;
@@ -87,386 +65,6 @@ struct FwdKParams {
   float* lse_parts;
   uint32_t* status;
 };
-
-template <int BN, int KST, bool P_TMEM>
-__global__ void __launch_bounds__(kThreads, 1)
-    tc_fwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                  const __grid_constant__ CUtensorMap tmKr, const __grid_constant__ CUtensorMap tmVr,
-                  const FwdKParams p) {
-  using L = FwdLayout<BN, KST, P_TMEM>;
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_kf[KST], bar_ke[KST], bar_vf[KST], bar_ve[KST], bar_sf[2],
-      bar_pf[2], bar_od, bar_ofin, bar_drain;
-  __shared__ uint32_t tmem_base_s;
-  __shared__ uint32_t abort_s;
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sQ = sbase + L::kQ, sK = sbase + L::kK, sV = sbase + L::kV, sP = sbase + L::kP;
-
-  // ---- work unit: parts 0..ns-1 are prompt key ranges, part ns the
-  // response keys (causal; only keys up to the tile's last row are visited)
-  const int mt = blockIdx.x % p.n_mt;
-  const int kvh = (blockIdx.x / p.n_mt) % p.hkv;
-  const int part = blockIdx.x / (p.n_mt * p.hkv);
-  const bool resp = part == p.ns;
-  const int64_t rows_g = (int64_t)p.gq * p.R;
-  int64_t kb, ke;
-  if (!resp) {
-    kb = (int64_t)part * p.split_span;
-    ke = kb + p.split_span < p.P ? kb + p.split_span : p.P;
-  } else {
-    const int64_t t0 = (int64_t)mt * kBM;
-    const int64_t t1 = (t0 + kBM < rows_g ? t0 + kBM : rows_g) - 1;
-    kb = 0;
-    ke = (t0 / p.R == t1 / p.R) ? (t1 % p.R) + 1 : p.R;
-  }
-  const int ntiles = ke > kb ? (int)((ke - kb + BN - 1) / BN) : 0;
-
-  if (tid == 0) {
-    abort_s = 0;
-    mbar_init(smem_u32(&bar_q), 128);
-    for (int s = 0; s < KST; ++s) {
-      mbar_init(smem_u32(&bar_kf[s]), 1);
-      mbar_init(smem_u32(&bar_ke[s]), 1);
-      mbar_init(smem_u32(&bar_vf[s]), 1);
-      mbar_init(smem_u32(&bar_ve[s]), 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&bar_sf[b]), 1);
-      mbar_init(smem_u32(&bar_pf[b]), 128);
-    }
-    mbar_init(smem_u32(&bar_od), 1);
-    mbar_init(smem_u32(&bar_ofin), 1);
-    mbar_init(smem_u32(&bar_drain), 1);
-    fence_mbar_init();
-  }
-  if (warp == 2) {
-    tmem_alloc(smem_u32(&tmem_base_s), 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = tmem_base_s;
-  const volatile uint32_t* abortp = &abort_s;
-
-  // a wait that gives up records its kernel and source line in status[1]
-  auto fail = [&](int line) {
-    atomicOr(p.status, kStatusTimeout);
-    atomicCAS(p.status + 1, 0u, ((uint32_t)kKTcFwd << 16) | (uint32_t)line);
-    abort_s = 1;
-  };
-
-  // Row of the pool that holds key `key0` (a multiple of BN) of KV head kvh;
-  // an out-of-pool page id gives an out-of-range row (TMA fills zeros).
-  auto pool_row = [&](int64_t key0) -> int32_t {
-    const int32_t slot = __ldg(p.page_table + key0 / p.page_size);
-    if (slot < 0 || slot >= p.pool_pages) {
-      if (lane == 0) atomicOr(p.status, kStatusBadPage);
-      return (int32_t)p.pool_rows;
-    }
-    return (int32_t)(((int64_t)slot * p.hkv + kvh) * p.page_size + key0 % p.page_size);
-  };
-
-  if (warp == 0 || warp == 3) {
-    // ------------------------------------------------------------ producers
-    // whole warps; lane 0 posts the expected bytes and loads the whole tile
-    // with one TMA instruction (the per-instruction cost of TMA, not its
-    // bandwidth, limits small boxes)
-    if (ntiles > 0) {
-      const bool isK = warp == 0;
-      const CUtensorMap* tm = resp ? (isK ? &tmKr : &tmVr) : (isK ? &tmK : &tmV);
-      uint64_t* full = isK ? bar_kf : bar_vf;
-      uint64_t* empty = isK ? bar_ke : bar_ve;
-      const uint32_t sdst = isK ? sK : sV;
-      if (lane == 0) prefetch_tmap(tm);
-      int issued = 0;
-      for (int j = 0; j < ntiles; ++j) {
-        const int st = j % KST;
-        if (j >= KST && !mbar_wait_warp(smem_u32(&empty[st]), ((j / KST) - 1) & 1, abortp)) {
-          fail(__LINE__);
-          break;
-        }
-        const int64_t key0 = kb + (int64_t)j * BN;
-        const uint32_t fb = smem_u32(&full[st]);
-        const int32_t row = resp ? 0 : pool_row(key0);
-        if (lane == 0) mbar_expect_tx(fb, L::kKVBytes);
-        __syncwarp();
-        if (lane == 0) {
-          if (resp)
-            tma_load_4d(sdst + st * L::kKVBytes, tm, fb, 0, (int32_t)key0, 0, kvh);
-          else
-            tma_load_3d(sdst + st * L::kKVBytes, tm, fb, 0, row, 0);
-        }
-        __syncwarp();
-        issued = j + 1;
-      }
-      // make sure no copy is still landing in shared memory when the CTA ends
-      for (int j = issued - KST < 0 ? 0 : issued - KST; j < issued; ++j)
-        mbar_wait(smem_u32(&full[j % KST]), (j / KST) & 1, abortp);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && ntiles > 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16(kBM, BN, false);
-      constexpr uint32_t idesc_pv = idesc_bf16(kBM, kD, true);
-      bool ok = mbar_wait(smem_u32(&bar_q), 0, abortp);
-      if (!ok) fail(__LINE__);
-      for (int j = 0; ok && j <= ntiles; ++j) {
-        if (j < ntiles) {
-          const int st = j % KST, b = j & 1;
-          if (!mbar_wait(smem_u32(&bar_kf[st]), (j / KST) & 1, abortp)) { fail(__LINE__); break; }
-          tc_fence_after();
-          const uint32_t dS = tbase + L::kTmemS + b * BN;
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * L::kQBox + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(sK + st * L::kKVBytes + (kk >> 2) * L::kKVBox + (kk & 3) * 32,
-                                            16, 1024);
-            mma_ss(dS, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(smem_u32(&bar_sf[b]));
-          mma_commit(smem_u32(&bar_ke[st]));
-        }
-        if (j >= 1) {
-          const int i = j - 1, st = i % KST, b = i & 1;
-          if (!mbar_wait(smem_u32(&bar_pf[b]), (i >> 1) & 1, abortp)) { fail(__LINE__); break; }
-          if (!mbar_wait(smem_u32(&bar_vf[st]), (i / KST) & 1, abortp)) { fail(__LINE__); break; }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint64_t bd = sdesc_sw128(sV + st * L::kKVBytes + kk * 16 * 128, L::kKVBox, 1024);
-            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-            if (P_TMEM) {
-              mma_ts(tbase, tbase + L::kTmemS + b * BN + kk * 8, bd, idesc_pv, acc);
-            } else {
-              const uint64_t ad =
-                  sdesc_sw128(sP + b * L::kPBytes + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
-              mma_ss(tbase, ad, bd, idesc_pv, acc);
-            }
-          }
-          mma_commit(smem_u32(&bar_ve[st]));
-          mma_commit(smem_u32(&bar_od));
-          if (i == ntiles - 1) mma_commit(smem_u32(&bar_ofin));
-        }
-      }
-      // drain: every MMA issued above is complete before tensor memory is freed
-      mma_commit(smem_u32(&bar_drain));
-      mbar_wait(smem_u32(&bar_drain), 0, abortp);
-    }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax
-    const int i = tid - 128;           // query row in the tile == TMEM lane
-    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
-    const int64_t t = (int64_t)mt * kBM + i;
-    const bool row_ok = t < rows_g;
-    const int hh = row_ok ? (int)(t / p.R) : 0;
-    const int r = row_ok ? (int)(t % p.R) : 0;
-    const int64_t n = (int64_t)r * p.hq + (int64_t)kvh * p.gq + hh;
-
-    // Q tile: warp w loads rows w*32..w*32+31, 16 bytes per lane, into the
-    // 128B-swizzled K-major layout the MMA reads.
-    {
-      const int wq = warp - 4;
-      for (int rr = 0; rr < 32; ++rr) {
-        const int row = wq * 32 + rr;
-        const int64_t tt = (int64_t)mt * kBM + row;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (tt < rows_g) {
-          const int hh2 = (int)(tt / p.R), r2 = (int)(tt % p.R);
-          const int64_t n2 = (int64_t)r2 * p.hq + (int64_t)kvh * p.gq + hh2;
-          v = __ldg(reinterpret_cast<const uint4*>(p.q + n2 * kD) + lane);
-        }
-        st_shared_v4(sQ + (lane >> 3) * L::kQBox + sw128_offset(row, lane & 7), v);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&bar_q));
-    }
-
-    float m_run = -CUDART_INF_F, l_run = 0.f;
-    bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
-      const int b = j & 1;
-      if (!mbar_wait_warp(smem_u32(&bar_sf[b]), (j >> 1) & 1, abortp)) { fail(__LINE__); ok = false; break; }
-      tc_fence_after();
-      float s[BN];
-#pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(tbase + lane_off + L::kTmemS + b * BN + c0, rr);
-        tmem_wait_ld_r(rr);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) s[c0 + c] = __uint_as_float(rr[c]);
-      }
-      const int64_t key0 = kb + (int64_t)j * BN;
-      // keys of this tile visible to this row: the prompt range end, or the
-      // causal limit r for the response part (row r sees response keys <= r)
-      const int64_t lim = resp ? (int64_t)r + 1 : ke;
-      const int nvalid = (int)(lim - key0 < 0 ? 0 : (lim - key0 < BN ? lim - key0 : BN));
-      const int nvalid_tile = (int)(ke - key0 < BN ? ke - key0 : BN);
-      float mx = -CUDART_INF_F;
-#pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        const float x = c < nvalid ? s[c] * p.scale_log2 : -CUDART_INF_F;
-        s[c] = x;
-        mx = fmaxf(mx, x);
-      }
-      // Lazy rescale: a row moves its running max only when the tile max
-      // exceeds it by more than the threshold.  The O rescale uses
-      // warp-collective TMEM loads/stores, so the whole warp does it when any
-      // of its rows needs it (alpha = 1 for the others).
-      float alpha = 1.f;
-      bool rescale_o = false;
-      if (mx > m_run + kRescaleThreshold) {
-        if (m_run != -CUDART_INF_F) {
-          alpha = ex2(m_run - mx);
-          rescale_o = true;
-        }
-        l_run *= alpha;
-        m_run = mx;
-      }
-      if (__any_sync(0xffffffffu, rescale_o)) {
-        // O holds PV_0..PV_{j-1} (j >= 1 here: a finite running max needs an
-        // earlier tile); wait for the last one, then rescale in place.  S_j
-        // complete implies PV_{j-2} complete (MMAs finish in issue order), so
-        // bar_od has completed j-1 or j phases and the parity is unambiguous.
-        if (!mbar_wait_warp(smem_u32(&bar_od), (j - 1) & 1, abortp)) { fail(__LINE__); ok = false; break; }
-        tc_fence_after();
-#pragma unroll 1
-        for (int c0 = 0; c0 < kD; c0 += 32) {
-          uint32_t rr[32];
-          tmem_ld32(tbase + lane_off + c0, rr);
-          tmem_wait_ld_r(rr);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * alpha);
-          tmem_st32(tbase + lane_off + c0, rr);
-        }
-        tmem_wait_st();
-      }
-      float psum = 0.f;
-      uint32_t pk[BN / 2];
-#pragma unroll
-      for (int c = 0; c < BN; c += 2) {
-        const float p0 = s[c] == -CUDART_INF_F ? 0.f : ex2(s[c] - m_run);
-        const float p1 = s[c + 1] == -CUDART_INF_F ? 0.f : ex2(s[c + 1] - m_run);
-        psum += p0 + p1;
-        pk[c >> 1] = pack_bf16x2(p0, p1);
-      }
-      l_run += psum;
-      if (P_TMEM) {
-#pragma unroll
-        for (int c0 = 0; c0 < BN / 2; c0 += 16)
-          tmem_st16(tbase + lane_off + L::kTmemS + b * BN + c0, pk + c0);
-        tmem_wait_st();
-      } else {
-#pragma unroll
-        for (int c = 0; c < BN / 8; ++c) {
-          const uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-          st_shared_v4(sP + b * L::kPBytes + (c >> 3) * (kBM * 128) + sw128_offset(i, c & 7), v);
-        }
-      }
-      if (!resp && nvalid_tile < BN) {
-        // Partial last prompt tile: rows past the prompt end may hold anything
-        // (NaN included); zero them in V so that P=0 times V stays 0.
-        const int st = j % KST;
-        if (!mbar_wait_warp(smem_u32(&bar_vf[st]), (j / KST) & 1, abortp)) { fail(__LINE__); ok = false; break; }
-        const int nz = (BN - nvalid_tile) * (kD / 64) * 8;  // 16-byte chunks
-        for (int z = i; z < nz; z += 128) {
-          const int row = nvalid_tile + z / ((kD / 64) * 8);
-          const int box = (z / 8) % (kD / 64);
-          st_shared_v4(sV + st * L::kKVBytes + box * L::kKVBox + row * 128 + (z & 7) * 16,
-                       make_uint4(0u, 0u, 0u, 0u));
-        }
-      }
-      if (!P_TMEM || (!resp && nvalid_tile < BN)) fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_pf[b]));
-    }
-
-    // ---- epilogue: normalised partial O and its LSE
-    if (ok && ntiles > 0) {
-      // bar_od may lag two phases behind here, so the last PV has its own barrier
-      if (!mbar_wait_warp(smem_u32(&bar_ofin), 0, abortp)) { fail(__LINE__); ok = false; }
-      tc_fence_after();
-    }
-    const int64_t nrows = (int64_t)p.R * p.hq;
-    float* orow = p.o_parts + ((int64_t)part * nrows + n) * kD;
-    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-#pragma unroll 1
-    for (int c0 = 0; c0 < kD; c0 += 32) {
-      uint32_t rr[32];
-      __syncwarp();  // the row_ok stores of the previous chunk diverge
-      if (ok && ntiles > 0) {
-        tmem_ld32(tbase + lane_off + c0, rr);
-        tmem_wait_ld_r(rr);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) rr[c] = 0u;
-      }
-      if (row_ok) {
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          float4 v = make_float4(__uint_as_float(rr[c]) * inv, __uint_as_float(rr[c + 1]) * inv,
-                                 __uint_as_float(rr[c + 2]) * inv, __uint_as_float(rr[c + 3]) * inv);
-          *reinterpret_cast<float4*>(orow + c0 + c) = v;
-        }
-      }
-    }
-    if (row_ok)
-      p.lse_parts[(int64_t)part * nrows + n] =
-          l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2f : -CUDART_INF_F;
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 2) {
-    tc_fence_after();
-    tmem_dealloc(tbase, 512);
-  }
-}
-
-template <int BN, int KST, bool P_TMEM>
-cudaError_t fwd_variant(const FwdParams& a, cudaStream_t s) {
-  using L = FwdLayout<BN, KST, P_TMEM>;
-  const AttnGeom& g = a.g;
-  FwdKParams p;
-  p.hq = g.hq;
-  p.hkv = g.hkv;
-  p.gq = g.gq;
-  p.R = g.R;
-  p.P = g.P;
-  p.pool_pages = g.pool_pages;
-  p.pool_rows = g.pool_pages * g.hkv * g.page_size;
-  p.page_size = g.page_size;
-  p.ns = g.ns;
-  p.split_span = g.split_span;
-  p.n_mt = (int)(((int64_t)g.gq * g.R + kBM - 1) / kBM);
-  p.scale_log2 = g.scale_log2;
-  p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
-  p.page_table = a.page_table;
-  p.o_parts = a.o_parts;
-  p.lse_parts = a.lse_parts;
-  p.status = a.status;
-  CUtensorMap tk, tv, tkr, tvr;
-  memset(&tk, 0, sizeof(tk));
-  memset(&tv, 0, sizeof(tv));
-  if (g.P > 0 && (!encode_pool_tile_map(&tk, a.k_pool, p.pool_rows, BN) ||
-                  !encode_pool_tile_map(&tv, a.v_pool, p.pool_rows, BN)))
-    return cudaErrorInvalidValue;
-  if (!encode_rows_tile_map(&tkr, a.k_resp, g.hkv, g.R, BN) ||
-      !encode_rows_tile_map(&tvr, a.v_resp, g.hkv, g.R, BN))
-    return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel<BN, KST, P_TMEM>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kSmem);
-  if (e != cudaSuccess) return e;
-  const int64_t units = (int64_t)(g.ns + 1) * g.hkv * p.n_mt;
-  if (units == 0) return cudaSuccess;
-  LaunchScope ls(kKTcFwd, s);
-  tc_fwd_kernel<BN, KST, P_TMEM><<<(unsigned)units, kThreads, L::kSmem, s>>>(tk, tv, tkr, tvr, p);
-  return cudaGetLastError();
-}
 
 // ===========================================================================
 // Chunk-ring forward (default), 128-key tiles.  K and V stream through one
@@ -750,10 +348,14 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int b = j & 1;
+      const int64_t tkey0 = kb + (int64_t)j * BN;
+      // a tile whose page id lies outside the pool holds no keys (the
+      // producer loaded zeros for it and flagged the status word); the id is
+      // read before the wait so that its latency hides behind it
+      const int32_t tslot = resp ? 0 : __ldg(p.page_table + tkey0 / p.page_size);
       if (!mbar_wait_warp(smem_u32(&bar_sf[b]), (j >> 1) & 1, abortp)) { fail(__LINE__); ok = false; break; }
       tc_fence_after();
-      const int64_t tkey0 = kb + (int64_t)j * BN;
-      const int64_t lim = resp ? (int64_t)r + 1 : ke;
+      const int64_t lim = resp ? (int64_t)r + 1 : (tslot >= 0 && tslot < p.pool_pages ? ke : tkey0);
       // visible keys of this row in the tile, and in each half
       const int nv_row = (int)(lim - tkey0 < 0 ? 0 : (lim - tkey0 < BN ? lim - tkey0 : BN));
       const bool full = !resp && nv_row == BN;  // the common case skips the masks
@@ -970,34 +572,15 @@ cudaError_t fwd_ring(const FwdParams& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(tc_fwd_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)L::kSmem);
   if (e != cudaSuccess) return e;
-  const int64_t units = (int64_t)(g.ns + 1) * g.hkv * p.n_mt;
+  const int64_t units = (int64_t)launch_parts(g) * g.hkv * p.n_mt;
   if (units == 0) return cudaSuccess;
   LaunchScope ls(kKTcFwd, s);
   tc_fwd_ring_kernel<<<(unsigned)units, kThreadsRing, L::kSmem, s>>>(tk, tv, tkr, tvr, p);
   return cudaGetLastError();
 }
 
-int fwd_variant_id() {
-  static int v = [] {
-    const char* e = getenv("LS_TC_FWD_VARIANT");
-    return e ? atoi(e) : 0;
-  }();
-  return v;
-}
-
 }  // namespace
 
-// Default: the chunk-ring kernel.  LS_TC_FWD_VARIANT selects the staged
-// kernels for comparison: 1 = 128-key tiles with one K and one V stage and P
-// in tensor memory, 2 / 3 = 64-key tiles, two stages, P in shared / tensor
-// memory.
-cudaError_t launch_tc_fwd(const FwdParams& a, cudaStream_t s) {
-  switch (fwd_variant_id()) {
-    case 1: return fwd_variant<128, 1, true>(a, s);
-    case 2: return fwd_variant<64, 2, false>(a, s);
-    case 3: return fwd_variant<64, 2, true>(a, s);
-    default: return fwd_ring(a, s);
-  }
-}
+cudaError_t launch_tc_fwd(const FwdParams& a, cudaStream_t s) { return fwd_ring(a, s); }
 
 }  // namespace ls

@@ -178,17 +178,23 @@ def test_gdn_workspace_and_argument_checks(ls):
     """Gated-DeltaNet entry points: sizing and validation before any launch."""
     L = ls.lib()
     d = ls.GdnDesc(8, 32, 128, 128)
-    sizes = [ls.ls_gdn_workspace_size(d, r) for r in (1, 64, 65, 4096)]
-    # enough for either backward: per (member, head) the recurrent one keeps one
-    # 128x128 float32 state per 8-token checkpoint plus a segment of 8 states;
-    # the chunk-parallel one keeps nine 128x128 float32 blocks per 128-token chunk
-    rec = [8 * 32 * (n + 8) * 128 * 128 * 4 for n in (1, 8, 9, 512)]
-    cp = [8 * 32 * -(-R // 128) * 9 * 128 * 128 * 4 for R in (1, 64, 65, 4096)]
-    assert sizes == [max(a, b) for a, b in zip(rec, cp)]
+    assert d.precision == ls.LS_GDN_EXACT  # a zeroed desc selects the exact float32 path
+    tc = ls.GdnDesc(8, 32, 128, 128, ls.LS_GDN_TENSOR_CORE)
+    # the 256-byte status header, then the precision's own scratch: per (member,
+    # head) the recurrent backward keeps one 128x128 float32 state per 8-token
+    # checkpoint plus a segment of 8 states; the chunk-parallel one keeps nine
+    # 128x128 float32 blocks per 128-token chunk
+    rec = [256 + 8 * 32 * (n + 8) * 128 * 128 * 4 for n in (1, 8, 9, 512)]
+    cp = [256 + 8 * 32 * -(-R // 128) * 9 * 128 * 128 * 4 for R in (1, 64, 65, 4096)]
+    assert [ls.ls_gdn_workspace_size(d, r) for r in (1, 64, 65, 4096)] == rec
+    assert [ls.ls_gdn_workspace_size(tc, r) for r in (1, 64, 65, 4096)] == cp
     out = ctypes.c_size_t(0)
     bad = ls.GdnDesc(8, 32, 64, 128)
     assert L.ls_gdn_workspace_size(ctypes.byref(bad), 10, ctypes.byref(out)) != 0
     assert "128" in ls.ls_last_error()
+    badp = ls.GdnDesc(8, 32, 128, 128, 7)
+    assert L.ls_gdn_workspace_size(ctypes.byref(badp), 10, ctypes.byref(out)) == 1
+    assert "precision" in ls.ls_last_error()
     assert L.ls_gdn_workspace_size(ctypes.byref(d), -1, ctypes.byref(out)) == 1
     args = [None] * 6
     assert L.ls_gdn_replay_fwd(ctypes.byref(d), *args, 0, None, None, None) == 0  # no-op
@@ -199,3 +205,20 @@ def test_gdn_workspace_and_argument_checks(ls):
     st = L.ls_gdn_replay_bwd(ctypes.byref(d), *bw, 8, *([ctypes.c_void_p(256)] * 5),
                              ctypes.c_void_p(256), 100, None)
     assert st != 0 and "workspace" in ls.ls_last_error()
+
+
+def test_noalloc_forward_validates_before_touching_the_device(ls):
+    """ls_replay_fwd_noalloc refuses a bad call before it looks up or clears
+    its fixed scratch: these run without a GPU."""
+    L = ls.lib()
+    d = _desc(ls)
+    prompt = _prompt(ls)
+    A = ctypes.c_void_p(1 << 24)  # aligned, never dereferenced
+    assert L.ls_replay_fwd_noalloc(None, ctypes.byref(prompt), A, A, A, 8, A, A, None) == 1
+    assert L.ls_replay_fwd_noalloc(ctypes.byref(d), ctypes.byref(prompt), ctypes.c_void_p((1 << 24) + 2),
+                                   A, A, 8, A, A, None) == 1
+    assert "aligned" in ls.ls_last_error()
+    assert L.ls_replay_fwd_noalloc(ctypes.byref(d), ctypes.byref(prompt), A, A, A, 0, A, A, None) == 0
+    big = ls.PromptKV(1 << 24, 1 << 24, 8192, 1 << 24, 8192, 2097152)
+    assert L.ls_replay_fwd_noalloc(ctypes.byref(d), ctypes.byref(big), A, A, A, 8192, A, A, None) == 3
+    assert "64 MiB" in ls.ls_last_error()

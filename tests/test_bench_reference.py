@@ -26,5 +26,12 @@ def test_reference_arm_prints_one_contract_line(workload, unit):
         assert key in line, key
     assert line["impl"] == "reference" and line["unit"] == unit and line["value"] > 0
     assert line["config"]["workload"] == workload
+    # the same config object the GPU arm prints for this workload and rank count
+    sys.path.insert(0, str(ROOT))
+    import bench
+
+    cfg = bench.gdn_config(workload, 1) if workload in bench.GDN_WORKLOADS else \
+        bench.prefill_config(workload, 1)
+    assert line["config"] == cfg
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0

@@ -32,7 +32,7 @@ def kernel_source(mutation=None):
     if mutation:  # applied to the last occurrence: the default kernel comes last in the file
         i = src.rindex(mutation[0])
         src = src[:i] + mutation[1] + src[i + len(mutation[0]):]
-    pre = src[:src.index("template <int BN, int KSK, int KSV>\n__global__")]
+    pre = src[:src.index("// ===========================================================================\n// Backward with dO held in tensor memory")]
     body = src[src.index("struct BwdTmLayout"):src.index("cudaError_t bwd_tm(")]
     text = pre + body + "}  // namespace\n}  // namespace ls\n"
     text = text.replace("extern __shared__", "extern")

@@ -31,7 +31,7 @@ def kernel_source(mutation=None):
     if mutation:  # applied to the last occurrence: the ring kernel comes last
         i = src.rindex(mutation[0])
         src = src[:i] + mutation[1] + src[i + len(mutation[0]):]
-    pre = src[:src.index("template <int BN, int KST, bool P_TMEM>\n__global__")]
+    pre = src[:src.index("// ===========================================================================\n// Chunk-ring forward")]
     body = src[src.index("struct FwdRingLayout"):src.index("cudaError_t fwd_ring(")]
     text = pre + body + "}  // namespace\n}  // namespace ls\n"
     text = text.replace("extern __shared__", "extern")

@@ -114,3 +114,64 @@ def test_single_rank_cpreplay_is_the_replay(cuda_device):
     run.backward(q, k, v, d_o, o, lse, dq, dk, dv, ws)
     ls.ls_read_device_status(ws)
     _check(w, pr, m, o, lse, dq, dk, dv)
+
+
+def test_ranks_without_the_response_skip_its_part(cuda_device):
+    """A rank called with with_response = 0 computes no causal response part:
+    against the same call with the response, its workspace has exactly one
+    partial fewer written (R*Hq*(d+1) float32 words in the forward, the
+    partial O and LSE; R*Hq*d in the backward, the dQ share), and its merged
+    share is unchanged."""
+    dev = cuda_device
+    w = inputs.Workload("cp_skip", 24, 4, 256, 256, 3000, (300,), "bf16", seed=23, pool_factor=2,
+                        poison=True)
+    pr = inputs.make_prompt(w, "cpu")
+    m = inputs.make_member(w, 0, "cpu")
+    kp, vp, pt = (pr[x].to(dev) for x in ("k_pool", "v_pool", "page_table"))
+    q, k, v, d_o = (m[x].to(dev) for x in ("q", "k", "v", "d_o"))
+    R, hq, d = q.shape
+    desc = ls.desc_for(w.hq, w.hkv, w.head_dim, w.page_size, torch.bfloat16, w.scale)
+    prompt = ls.prompt_from(kp, vp, pt, w.prompt_len)
+    n = ls.ls_replay_workspace_size(desc, prompt, R)
+    f32 = dict(device=dev, dtype=torch.float32)
+
+    def fresh_ws():
+        ws = torch.full((n,), 0xFF, dtype=torch.uint8, device=dev)  # NaN pattern everywhere
+        ws[:256] = 0  # the status header starts clear
+        return ws
+
+    def written(ws):
+        return int((ws[256:].view(torch.int32) != -1).sum())
+
+    outs, counts = {}, {}
+    for with_resp in (True, False):
+        ws = fresh_ws()
+        o_part = torch.empty(R, hq, d, **f32)
+        l_part = torch.empty(R, hq, **f32)
+        ls.ls_replay_fwd_part(desc, prompt, q, k, v, with_resp, o_part, l_part, ws)
+        ls.ls_read_device_status(ws)
+        counts[("fwd", with_resp)] = written(ws)
+        outs[with_resp] = (o_part, l_part)
+    assert counts[("fwd", True)] - counts[("fwd", False)] == R * hq * (d + 1), counts
+    # the prompt-only share equals the oracle's replay over the prompt keys alone
+    want = ref.replay_member(pr["k_pool"], pr["v_pool"], pr["page_table"], w.prompt_len,
+                             m["q"], m["k"][:0], m["v"][:0], scale=w.scale)
+    o_p, l_p = outs[False]
+    assert rel_err(o_p.double().cpu().numpy(), want["o"]) <= TOL["bf16"]
+    assert float(np.abs(l_p.double().cpu().numpy() - want["lse"]).max()) <= LSE_TOL
+
+    o_full = torch.empty_like(q)
+    lse = torch.empty(R, hq, **f32)
+    ws = fresh_ws()
+    ls.ls_replay_fwd(desc, prompt, q, k, v, o_full, lse, ws)
+    delta = torch.empty(R, hq, **f32)
+    ls.ls_replay_bwd_preprocess(desc, o_full, d_o, delta)
+    for with_resp in (True, False):
+        ws = fresh_ws()
+        dq_part = torch.empty(R, hq, d, **f32)
+        dk, dv = torch.empty_like(k), torch.empty_like(v)
+        ls.ls_replay_bwd_part(desc, prompt, q, k, v, d_o, lse, delta, with_resp, dq_part,
+                              dk if with_resp else None, dv if with_resp else None, ws)
+        ls.ls_read_device_status(ws)
+        counts[("bwd", with_resp)] = written(ws)
+    assert counts[("bwd", True)] - counts[("bwd", False)] == R * hq * d, counts

@@ -1,15 +1,10 @@
-"""The tensor-core GDN path (LS_GDN_VARIANT=chunk: the chunkwise forward and
-the chunk-parallel backward) against the float64 oracle at the bf16
-tolerance: its products take bf16 operands, which the CPU block emulator
-puts near 4e-3 to 5e-3.  Cases: three chunks with a partial last one, one
-exact chunk, a single token, the empty response, and two sampled heads of
-the 8 x 32-head x 4096-token group.
-
-The three-chunk, single-token and empty cases have run green on a GB300 and
-run by default; the exact-chunk and bench-size cases have not yet run on a
-GPU and run only when LS_GDN_CHUNK_TESTS=1."""
-import os
-
+"""The tensor-core GDN path (precision LS_GDN_TENSOR_CORE: the chunkwise
+forward and the chunk-parallel backward) against the float64 oracle at the
+bf16 tolerance: its products take bf16 operands, which the CPU block
+emulator puts near 4e-3 to 5e-3.  Cases: three chunks with a partial last
+one, one exact chunk, a single token, the empty response, and two sampled
+heads of the 8 x 32-head x 4096-token group; the workspace status word must
+stay clear."""
 import numpy as np
 import pytest
 import torch
@@ -20,24 +15,23 @@ from oracle.gdn import gdn_replay
 from gpu_helpers import TOL, rel_err
 
 pytestmark = pytest.mark.gpu
-not_yet_on_gpu = pytest.mark.skipif(os.environ.get("LS_GDN_CHUNK_TESTS") != "1",
-                                    reason="not yet run on a GPU")
+TC = ls.LS_GDN_TENSOR_CORE
 
 
 @pytest.fixture(autouse=True)
-def _chunk_variant(monkeypatch):
+def _built():
     from long_context_grpo_replay_gb300 import build
 
     build.build()
     ls.lib()
-    monkeypatch.setenv("LS_GDN_VARIANT", "chunk")
 
 
 def _fwd(c):
     B, R, H, _ = c["q"].shape
     o = torch.full_like(c["v"], float("nan"))
     s_final = torch.empty((B, H, 128, 128), device=c["q"].device)
-    ls.ls_gdn_replay_fwd(c["s0"], c["q"], c["k"], c["v"], c["g"], c["beta"], o, s_final)
+    ls.ls_gdn_replay_fwd(c["s0"], c["q"], c["k"], c["v"], c["g"], c["beta"], o, s_final,
+                         precision=TC)
     torch.cuda.synchronize()
     return o, s_final
 
@@ -46,11 +40,13 @@ def _bwd(c):
     B, R, H, _ = c["q"].shape
     grads = {n: torch.empty_like(c[x]) for n, x in
              (("dq", "q"), ("dk", "k"), ("dv", "v"), ("dg", "g"), ("dbeta", "beta"))}
-    ws = torch.empty(ls.ls_gdn_workspace_size(ls.GdnDesc(B, H, 128, 128), R), dtype=torch.uint8,
-                     device=c["q"].device)
+    ws = torch.empty(ls.ls_gdn_workspace_size(ls.GdnDesc(B, H, 128, 128, TC), R),
+                     dtype=torch.uint8, device=c["q"].device)
+    ls.ls_clear_device_status(ws)
     ls.ls_gdn_replay_bwd(c["s0"], c["q"], c["k"], c["v"], c["g"], c["beta"], c["d_o"], grads["dq"],
-                         grads["dk"], grads["dv"], grads["dg"], grads["dbeta"], ws)
+                         grads["dk"], grads["dv"], grads["dg"], grads["dbeta"], ws, precision=TC)
     torch.cuda.synchronize()
+    ls.ls_read_device_status(ws)  # raises if a bounded device wait ran out
     return grads
 
 
@@ -66,8 +62,7 @@ def _check(c, o, s_final, b, heads, grads=None):
     assert all(e <= TOL["bf16"] for e in errs.values()), (b, hs, errs)
 
 
-@pytest.mark.parametrize("B,H,R", [(1, 4, 300), pytest.param(2, 2, 128, marks=not_yet_on_gpu),
-                                   (2, 3, 1)],
+@pytest.mark.parametrize("B,H,R", [(1, 4, 300), (2, 2, 128), (2, 3, 1)],
                          ids=["three_chunks_r300", "one_chunk_r128", "one_token"])
 def test_chunk_path_matches_the_oracle(cuda_device, B, H, R):
     c = inputs.make_gdn_group(B, H, R, seed=60 + R, device=cuda_device)
@@ -83,7 +78,6 @@ def test_chunk_forward_empty_response(cuda_device):
     assert torch.equal(s_final, c["s0"].expand_as(s_final))
 
 
-@not_yet_on_gpu
 def test_chunk_path_at_bench_size_sampled(cuda_device):
     c = inputs.make_gdn_group(8, 32, 4096, seed=78, device=cuda_device)
     o, s_final = _fwd(c)

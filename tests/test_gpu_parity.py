@@ -246,6 +246,9 @@ def test_bwd_preprocess_call(cuda_device):
 # --------------------------------------------------------------------------
 @pytest.mark.parametrize("tc", [True, False])
 def test_bad_page_id_is_reported(cuda_device, tc):
+    """A page-table entry outside the pool (planted on the host) is reported
+    through the status word and its page holds no keys: O, LSE, dQ, dK and dV
+    equal the oracle's on the prompt with that page taken out."""
     spec = ("bad_page", 24, 4, 256 if tc else 64, 256 if tc else 16, 1500, (40,), "bf16", False)
     w, dp, ms = _small_inputs(spec, cuda_device)
     assert ls.ls_uses_tensor_cores(dp.desc) == tc
@@ -259,4 +262,24 @@ def test_bad_page_id_is_reported(cuda_device, tc):
         ls.ls_read_device_status(ws)
     assert ei.value.status == 5
     ls.ls_read_device_status(ws)  # cleared by the read; the context is still usable
+    ls.ls_replay_bwd_preprocess(dp.desc, m["o"], m["d_o"], m["delta"])
+    ls.ls_replay_bwd(dp.desc, dp.prompt, m["q"], m["k"], m["v"], m["d_o"], m["lse"], m["delta"],
+                     m["dq"], m["dk"], m["dv"], ws)
+    with pytest.raises(ls.LsError) as ei:
+        ls.ls_read_device_status(ws)
+    assert ei.value.status == 5
     torch.cuda.synchronize()
+    # the oracle on the prompt without logical page 1 (a full page): keys are
+    # a set, so the remaining pages keep their order and the partial last page
+    # stays last
+    h = dict(dp.host)
+    keep = [i for i in range(h["page_table"].shape[0]) if i != 1]
+    h["page_table"] = h["page_table"][keep]
+    h["prompt_len"] = w.prompt_len - w.page_size
+    hm = ms[0]
+    r = ref.replay_member(h["k_pool"], h["v_pool"], h["page_table"], h["prompt_len"], hm["q"],
+                          hm["k"], hm["v"], hm["d_o"], scale=w.scale)
+    for key in ("o", "dq", "dk", "dv"):
+        err = rel_err(m[key].double().cpu().numpy(), r[key])
+        assert err <= 2e-2, (key, err)
+    assert float(np.abs(m["lse"].double().cpu().numpy() - r["lse"]).max()) <= 1e-3
