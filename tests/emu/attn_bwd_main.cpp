@@ -1,4 +1,5 @@
-// Runs the prompt-attention backward kernel's source (tc_bwd_dq_tm_kernel) on
+// Runs a prompt-attention backward kernel's source (tc_bwd_dq_ring_kernel with
+// LS_EMU_RING defined, else tc_bwd_dq_tm_kernel) on
 // the CPU block emulator:  attn_bwd_emu <in.bin> <out.bin>
 // in.bin: int64 hq, hkv, R, P, page_size, pool_pages, num_pages, ns,
 // split_span; float32 scale; then bf16 k_pool, v_pool [pool_pages][hkv][page][256],
@@ -20,27 +21,40 @@ alignas(1024) unsigned char smem_raw[emu::kSmemBytes];
 
 namespace ls {
 namespace {
-// The tensor maps the library encodes for this kernel (whole [64 x 256] tiles
-// landing as four swizzled [64 x 64] column boxes).
-emu::TensorMap pool_tile_map(const void* base, int64_t rows, int box_rows) {
-  return {base, 3, {64, (uint64_t)rows, 4}, {2, 512, 128}, {64, (uint32_t)box_rows, 4}};
+// The tensor maps the library encodes for these kernels (whole [rows x 64*blocks]
+// tiles landing as `blocks` swizzled [rows x 64] column boxes).
+emu::TensorMap pool_tile_map(const void* base, int64_t rows, int box_rows, int blocks) {
+  return {base, 3, {64, (uint64_t)rows, 4}, {2, 512, 128}, {64, (uint32_t)box_rows, (uint32_t)blocks}};
 }
-emu::TensorMap rows_tile_map(const void* base, int heads, int64_t rows, int box_rows) {
+emu::TensorMap rows_tile_map(const void* base, int heads, int64_t rows, int box_rows, int blocks) {
   return {base, 4, {64, (uint64_t)rows, 4, (uint64_t)heads}, {2, (uint64_t)heads * 512, 128, 512},
-          {64, (uint32_t)box_rows, 4, 1}};
+          {64, (uint32_t)box_rows, (uint32_t)blocks, 1}};
 }
+
+#ifdef LS_EMU_RING
+// the 128-key ring kernel: K and V chunks of [128 keys x 128 columns]
+constexpr int kBoxBlocks = 2;
+#define LS_EMU_KERNEL tc_bwd_dq_ring_kernel
+#define LS_EMU_THREADS kThreadsRing
+using EmuLayout = BwdRingLayout;
+#else
+constexpr int kBoxBlocks = 4;
+#define LS_EMU_KERNEL tc_bwd_dq_tm_kernel
+#define LS_EMU_THREADS kThreads
+using EmuLayout = BwdTmLayout;
+#endif
 
 void emulate(BwdKParams p, const void* k_pool, const void* v_pool, const void* k_resp,
              const void* v_resp) {
-  using L = BwdTmLayout;
-  const CUtensorMap tk = pool_tile_map(k_pool, p.pool_rows, L::BN);
-  const CUtensorMap tv = pool_tile_map(v_pool, p.pool_rows, L::BN);
-  const CUtensorMap tkr = rows_tile_map(k_resp, p.hkv, p.R, L::BN);
-  const CUtensorMap tvr = rows_tile_map(v_resp, p.hkv, p.R, L::BN);
+  using L = EmuLayout;
+  const CUtensorMap tk = pool_tile_map(k_pool, p.pool_rows, L::BN, kBoxBlocks);
+  const CUtensorMap tv = pool_tile_map(v_pool, p.pool_rows, L::BN, kBoxBlocks);
+  const CUtensorMap tkr = rows_tile_map(k_resp, p.hkv, p.R, L::BN, kBoxBlocks);
+  const CUtensorMap tvr = rows_tile_map(v_resp, p.hkv, p.R, L::BN, kBoxBlocks);
   emu::g_smem = smem_raw;
   const int units = (p.ns + 1) * p.hkv * p.n_mt;
   for (int u = 0; u < units; ++u)
-    emu::run_block((unsigned)u, 0, kThreads, [&] { tc_bwd_dq_tm_kernel(tk, tv, tkr, tvr, p); },
+    emu::run_block((unsigned)u, 0, LS_EMU_THREADS, [&] { LS_EMU_KERNEL(tk, tv, tkr, tvr, p); },
                    (unsigned)(u + 1));
 }
 }  // namespace

@@ -25,29 +25,39 @@ SRC = ROOT / "long_context_grpo_replay_gb300" / "csrc" / "ls_tc_bwd.cu"
 TOL_BF16 = 2e-2
 
 
-def kernel_source(mutation=None):
-    """The default kernel's source, cut out of its file: the constants and
-    parameter block, then the kernel; host launchers left out."""
+KERNELS = {  # kernel: (first line of its block, line after it)
+    "tm": ("struct BwdTmLayout", "cudaError_t bwd_tm("),
+    "ring": ("struct BwdRingLayout", "cudaError_t bwd_ring("),
+}
+
+
+def kernel_source(mutation=None, kernel="ring"):
+    """A kernel's source, cut out of its file: the constants and parameter
+    block, then the kernel; host launchers left out.  A mutation is applied
+    inside the kernel's own block."""
     src = SRC.read_text()
-    if mutation:  # applied to the last occurrence: the default kernel comes last in the file
-        i = src.rindex(mutation[0])
-        src = src[:i] + mutation[1] + src[i + len(mutation[0]):]
+    start, end = KERNELS[kernel]
+    body = src[src.index(start):src.index(end)]
+    if mutation:
+        assert mutation[0] in body, mutation[0]
+        i = body.rindex(mutation[0])
+        body = body[:i] + mutation[1] + body[i + len(mutation[0]):]
     pre = src[:src.index("// ===========================================================================\n// Backward with dO held in tensor memory")]
-    body = src[src.index("struct BwdTmLayout"):src.index("cudaError_t bwd_tm(")]
-    text = pre + body + "}  // namespace\n}  // namespace ls\n"
+    text = ("#define LS_EMU_RING 1\n" if kernel == "ring" else "") + pre + body + \
+        "}  // namespace\n}  // namespace ls\n"
     text = text.replace("extern __shared__", "extern")
     ex2 = 'asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));'
     assert ex2 in text
     return text.replace(ex2, "y = exp2f(x);")
 
 
-def build(d, mutation=None):
+def build(d, mutation=None, kernel="ring"):
     if shutil.which("g++") is None:
         pytest.skip("no host C++ compiler")
     csrc = d / "x" / "csrc"
     csrc.mkdir(parents=True)
     (d / "include").mkdir()
-    (csrc / "kernel.cu").write_text(kernel_source(mutation))
+    (csrc / "kernel.cu").write_text(kernel_source(mutation, kernel))
     shutil.copy(SRC.parent / "ls_internal.h", csrc / "ls_internal.h")
     shutil.copy(EMU / "ls_tc.cuh", csrc / "ls_tc.cuh")
     shutil.copy(ROOT / "include" / "ls.h", d / "include" / "ls.h")
@@ -60,14 +70,13 @@ def _bf16_bytes(t):
     return t.to(torch.bfloat16).contiguous().view(torch.int16).numpy().tobytes()
 
 
-def run_case(exe, d, P=600, R=64, seed=5):
+def run_case(exe, d, P=600, R=64, seed=5, span=256):
     w = inputs.Workload("emu", 12, 2, 256, 256, P, (R,), "bf16", seed=seed, pool_factor=2,
                         poison=True)
     pr = inputs.make_prompt(w, "cpu")
     m = inputs.make_member(w, 0, "cpu")
     want = ref.replay_member(pr["k_pool"], pr["v_pool"], pr["page_table"], P, m["q"], m["k"], m["v"],
                              m["d_o"], scale=w.scale)
-    span = 256
     ns = -(-P // span)
     kp, pt = pr["k_pool"], pr["page_table"]
     hdr = np.array([w.hq, w.hkv, R, P, w.page_size, kp.shape[0], pt.shape[0], ns, span],
@@ -91,10 +100,10 @@ def run_case(exe, d, P=600, R=64, seed=5):
     return out, float(np.abs(dq - want["dq"]).max() / np.abs(want["dq"]).max())
 
 
-@pytest.fixture(scope="module")
-def emulator(tmp_path_factory):
-    d = tmp_path_factory.mktemp("emu_attn_bwd")
-    return build(d), d
+@pytest.fixture(scope="module", params=["ring", "tm"])
+def emulator(tmp_path_factory, request):
+    d = tmp_path_factory.mktemp("emu_attn_bwd_" + request.param)
+    return build(d, kernel=request.param), d
 
 
 def test_emulated_backward_matches_the_oracle(emulator):
@@ -104,15 +113,27 @@ def test_emulated_backward_matches_the_oracle(emulator):
     assert err <= TOL_BF16, err
 
 
+def test_emulated_backward_over_many_tiles(emulator):
+    """One 1500-key part (12 tiles, 48 chunks: the ring's slot pattern runs
+    through more than two periods) with a partial last tile."""
+    exe, d = emulator
+    status, err = run_case(exe, d, P=1500, R=40, seed=6, span=1536)
+    assert status[0] == 0, status
+    assert err <= TOL_BF16, err
+
+
 @pytest.mark.parametrize("mutation", [
-    ("constexpr uint32_t idesc_dq = idesc_bf16(kBM, kD, true);",
-     "constexpr uint32_t idesc_dq = idesc_bf16(kBM, kD, false);"),
+    ("constexpr uint32_t idesc_q = idesc_bf16(kBM, 128, true);",
+     "constexpr uint32_t idesc_q = idesc_bf16(kBM, 128, false);"),
     ("        if (!mbar_wait(smem_u32(&bar_dsf), j & 1, abortp)) { fail(__LINE__); break; }\n", ""),
     ("(j > 0 || kk > 0) ? 1u : 0u);", "kk > 0 ? 1u : 0u);"),
-], ids=["K_read_K_major_in_dQ", "dQ_before_dS_is_written", "dQ_reset_every_tile"])
+    ("tbase + L::kTmemX + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8)", "tbase + L::kTmemX + kk * 8"),
+], ids=["K_read_K_major_in_dQ", "dQ_before_dS_is_written", "dQ_reset_every_tile",
+        "dS_of_the_second_half_misplaced"])
 def test_emulator_rejects_planted_kernel_mistakes(tmp_path, mutation):
-    """A wrong operand layout, a missing wait and a lost accumulation, each
-    planted in a copy of the kernel source, must fail the comparison."""
+    """A wrong operand layout, a missing wait, a lost accumulation and a
+    misplaced operand, each planted in a copy of the ring kernel's source,
+    must fail the comparison."""
     exe = build(tmp_path, mutation)
     status, err = run_case(exe, tmp_path)
     assert not err <= TOL_BF16, err  # also true for NaN
