@@ -477,13 +477,15 @@ cudaError_t bwd_tm(const BwdParams& a, cudaStream_t s) {
 // (dq_done).  Chunk n reuses the slot of chunk n-7 (n = 0, 3 mod 4) or n-3
 // (n = 1, 2 mod 4): the slot freed earliest that keeps every load about a
 // thousand cycles ahead of its first MMA.  That rule is periodic in 20
-// chunks (five tiles), so the slot of chunk n is a table entry.
+// chunks (five tiles), so the slot of chunk n is a table entry.  The two
+// chunks of one K or V tile land on one full barrier, so the MMA thread
+// tests two barriers per tile for its operands.
 // Softmax: eight warps, two threads per query row; half hf owns keys
 // 64hf..64hf+63 of each tile and writes their dS (bf16 pairs) over the first
 // half of its own dP columns, so the halves never touch each other's data.
 // ===========================================================================
 struct BwdRingLayout {
-  static constexpr int BN = 128, NC = 5, NF = 8;
+  static constexpr int BN = 128, NC = 5, NF = 4;  // NF: full barriers, one per chunk pair
   static constexpr uint32_t kRowBox = kBM * 128;  // Q box [128 rows x 64 columns], 16 KB
   static constexpr uint32_t kBox = BN * 128;      // K/V box [128 keys x 64 columns], 16 KB
   static constexpr uint32_t kChunk = 2 * kBox;    // 32 KB
@@ -595,9 +597,14 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
       int dp_seen = -1, dq_seen = -1;  // last tile whose dP / dQ completion was awaited
       int32_t row = 0;
       int issued = 0;
+      bool failed = false;
       for (int n = 0; n < nch; ++n) {
         const int j = n >> 2, kind = n & 3;
-        if (n >= 5) {
+        // after a wait gave up, only the second chunk of a pair already begun
+        // is still loaded, so that its full barrier completes and the drain
+        // below can account for every copy in flight
+        if (failed && (n & 1) == 0) break;
+        if (n >= 5 && !failed) {
           // the slot's previous chunk must be done with: a V chunk after dP
           // of its tile, a K chunk after dQ of its tile
           const int pr = ring_pred(n), t = pr >> 2;
@@ -609,7 +616,8 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
           }
           if (!ok) {
             if (lane == 0) fail(__LINE__);
-            break;
+            failed = true;
+            if ((n & 1) == 0) break;
           }
         }
         const int64_t key0 = kb + (int64_t)j * BN;
@@ -623,8 +631,11 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
           }
         }
         if (lane == 0) {
-          const uint32_t fb = smem_u32(&bar_full[n % NF]);
-          mbar_expect_tx(fb, L::kChunk);
+          // chunks 2g and 2g+1 (the two column halves of one K or V tile)
+          // land on full barrier g: armed for both with the first
+          const int g = n >> 1;
+          const uint32_t fb = smem_u32(&bar_full[g % NF]);
+          if ((n & 1) == 0) mbar_expect_tx(fb, 2 * L::kChunk);
           const uint32_t dst = chunk_addr(n);
           if (resp)
             tma_load_4d(dst, kind < 2 ? &tmKr : &tmVr, fb, 0, (int32_t)key0, 2 * (kind & 1), kvh);
@@ -635,16 +646,18 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
         issued = n + 1;
       }
       // no copy may still be landing in shared memory when the CTA ends
-      for (int n = issued - NF < 0 ? 0 : issued - NF; n < issued; ++n)
-        mbar_wait(smem_u32(&bar_full[n % NF]), (n / NF) & 1, abortp);
+      // (issued is even: pairs are always completed)
+      const int gend = issued >> 1;
+      for (int g = gend - NF < 0 ? 0 : gend - NF; g < gend; ++g)
+        mbar_wait(smem_u32(&bar_full[g % NF]), (g / NF) & 1, abortp);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(kBM, BN, false);  // S, dP: K-major B
       constexpr uint32_t idesc_q = idesc_bf16(kBM, 128, true);  // dQ halves: N-major B
-      auto wait_full = [&](int n) {
-        return mbar_wait(smem_u32(&bar_full[n % NF]), (n / NF) & 1, abortp);
+      auto wait_full = [&](int g) {  // chunk pair g: K_j is pair 2j, V_j pair 2j+1
+        return mbar_wait(smem_u32(&bar_full[g % NF]), (g / NF) & 1, abortp);
       };
       bool ok = mbar_wait(smem_u32(&bar_q), 0, abortp);
       if (!ok) fail(__LINE__);
@@ -652,7 +665,7 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
       for (int j = 0; ok && j < ntiles; ++j) {
         const int n0 = 4 * j;
         // S_j = Q K_j^T into X (X last held dS_{j-1}, read by dQ_{j-1} before)
-        if (!wait_full(n0) || !wait_full(n0 + 1)) { fail(__LINE__); break; }
+        if (!wait_full(2 * j)) { fail(__LINE__); break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
@@ -663,8 +676,7 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
         }
         mma_commit(smem_u32(&bar_sf));
         // dP_j = dO V_j^T into X, once the softmax warps have read S_j
-        if (!mbar_wait(smem_u32(&bar_sfree), j & 1, abortp) || !wait_full(n0 + 2) ||
-            !wait_full(n0 + 3)) {
+        if (!mbar_wait(smem_u32(&bar_sfree), j & 1, abortp) || !wait_full(2 * j + 1)) {
           fail(__LINE__);
           break;
         }
