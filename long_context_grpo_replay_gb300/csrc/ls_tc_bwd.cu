@@ -480,9 +480,10 @@ cudaError_t bwd_tm(const BwdParams& a, cudaStream_t s) {
 // chunks (five tiles), so the slot of chunk n is a table entry.  The two
 // chunks of one K or V tile land on one full barrier, so the MMA thread
 // tests two barriers per tile for its operands.
-// Softmax: eight warps, two threads per query row; half hf owns keys
-// 64hf..64hf+63 of each tile and writes their dS (bf16 pairs) over the first
-// half of its own dP columns, so the halves never touch each other's data.
+// Softmax: sixteen warps, four threads per query row (two warps per
+// scheduler leave the dS arithmetic, which sits on the critical path,
+// latency-bound); quarter qq owns keys 32qq..32qq+31 of each tile and writes
+// their dS (bf16 pairs) over the first half of its own dP columns.
 // ===========================================================================
 struct BwdRingLayout {
   static constexpr int BN = 128, NC = 5, NF = 4;  // NF: full barriers, one per chunk pair
@@ -519,7 +520,8 @@ __device__ __forceinline__ uint32_t ring_slot(int n) {
   return (uint32_t)(kRingTable >> (3 * (n % 20))) & 7u;
 }
 
-constexpr int kThreadsRing = 384;  // 4 control warps + 8 softmax warps
+constexpr int kThreadsRing = 640;  // 4 control warps + 16 softmax warps
+constexpr int kSoftWarps = 16;
 
 __global__ void __launch_bounds__(kThreadsRing, 1)
     tc_bwd_dq_ring_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -558,12 +560,12 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
 
   if (tid == 0) {
     abort_s = 0;
-    mbar_init(smem_u32(&bar_q), 256);
+    mbar_init(smem_u32(&bar_q), kSoftWarps);
     for (int f = 0; f < NF; ++f) mbar_init(smem_u32(&bar_full[f]), 1);
     mbar_init(smem_u32(&bar_sf), 1);
-    mbar_init(smem_u32(&bar_sfree), 256);
+    mbar_init(smem_u32(&bar_sfree), kSoftWarps);
     mbar_init(smem_u32(&bar_dpf), 1);
-    mbar_init(smem_u32(&bar_dsf), 256);
+    mbar_init(smem_u32(&bar_dsf), kSoftWarps);
     mbar_init(smem_u32(&bar_dqd), 1);
     mbar_init(smem_u32(&bar_fin), 1);
     mbar_init(smem_u32(&bar_drain), 1);
@@ -689,7 +691,7 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
                  kk > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(&bar_dpf));  // dP_j ready; V_j's chunks free
-        // dQ += dS_j K_j; dS of keys 0-63 in X columns 0-31, keys 64-127 in 64-95
+        // dQ += dS_j K_j; dS of keys 32q..32q+31 in X columns 32q..32q+15
         if (!mbar_wait(smem_u32(&bar_dsf), j & 1, abortp)) { fail(__LINE__); break; }
         tc_fence_after();
 #pragma unroll
@@ -697,7 +699,7 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
           const uint32_t kc = chunk_addr(n0 + h);
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tbase + h * 128, tbase + L::kTmemX + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+            mma_ts(tbase + h * 128, tbase + L::kTmemX + 32 * (kk >> 1) + 8 * (kk & 1),
                    sdesc_sw128(kc + kk * 16 * 128, L::kBox, 1024), idesc_q,
                    (j > 0 || kk > 0) ? 1u : 0u);
         }
@@ -709,13 +711,16 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    // warp 4+q and warp 8+q both reach tensor-memory lanes 32q..32q+31;
-    // half hf = 0 / 1 owns keys 0-63 / 64-127 of a tile, dO and dQ columns
-    // 0-127 / 128-255
-    const int sw = warp - 4, q4 = sw & 3, hf = sw >> 2;
+    // Sixteen warps, four threads per query row: warp 4 + 4qq + q reaches
+    // tensor-memory lanes 32q..32q+31 (its rows) and owns quarter qq of every
+    // key tile (keys 32qq..32qq+31), dO columns 64qq..64qq+63 and dQ columns
+    // 64qq..64qq+63.  Each quarter writes its dS (bf16 pairs) over the first
+    // half of its own dP columns, so quarters never touch each other's data.
+    // One lane per warp arrives on the MMA thread's barriers.
+    const int sw = warp - 4, q4 = sw & 3, qq = sw >> 2;
     const int i = q4 * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const uint32_t tX = tbase + lane_off + L::kTmemX + hf * 64;
+    const uint32_t tX = tbase + lane_off + L::kTmemX + qq * 32;
     const int64_t t = (int64_t)mt * kBM + i;
     const bool row_ok = t < rows_g;
     const int hh = row_ok ? (int)(t / p.R) : 0;
@@ -723,10 +728,14 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
     const int64_t n = (int64_t)r * p.hq + (int64_t)kvh * p.gq + hh;
     const float lse2 = row_ok ? __ldg(p.lse + n) * kLog2ef : 0.f;
     const float dl = row_ok ? __ldg(p.delta + n) : 0.f;
+    auto warp_arrive = [&](uint32_t bar) {  // after each lane's own ordering
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar);
+    };
     {
-      // Q tile into shared memory (16 rows per warp, swizzled) ...
-      for (int rr = 0; rr < 16; ++rr) {
-        const int row = sw * 16 + rr;
+      // Q tile into shared memory (8 rows per warp, swizzled) ...
+      for (int rr = 0; rr < 8; ++rr) {
+        const int row = sw * 8 + rr;
         const int64_t tt = (int64_t)mt * kBM + row;
         uint4 vq = make_uint4(0u, 0u, 0u, 0u);
         if (tt < rows_g) {
@@ -737,24 +746,21 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
         st_shared_v4(sQ + (lane >> 3) * L::kRowBox + sw128_offset(row, lane & 7), vq);
       }
       fence_proxy_async_smem();
-      // ... and this half of the row's dO into tensor memory (bf16 pairs)
-      const uint4* orow = reinterpret_cast<const uint4*>(p.d_o + n * kD) + hf * 16;
-#pragma unroll 1
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t rr[32];
+      // ... and this quarter of the row's dO into tensor memory (bf16 pairs)
+      const uint4* orow = reinterpret_cast<const uint4*>(p.d_o + n * kD) + qq * 8;
+      uint32_t rr[32];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 v = row_ok ? __ldg(orow + (c0 >> 2) + u) : make_uint4(0u, 0u, 0u, 0u);
-          rr[4 * u] = v.x;
-          rr[4 * u + 1] = v.y;
-          rr[4 * u + 2] = v.z;
-          rr[4 * u + 3] = v.w;
-        }
-        tmem_st32(tbase + lane_off + L::kTmemO + hf * 64 + c0, rr);
+      for (int u = 0; u < 8; ++u) {
+        const uint4 v = row_ok ? __ldg(orow + u) : make_uint4(0u, 0u, 0u, 0u);
+        rr[4 * u] = v.x;
+        rr[4 * u + 1] = v.y;
+        rr[4 * u + 2] = v.z;
+        rr[4 * u + 3] = v.w;
       }
+      tmem_st32(tbase + lane_off + L::kTmemO + qq * 32, rr);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bar_q));
+      warp_arrive(smem_u32(&bar_q));
     }
 
     bool ok = true;
@@ -766,52 +772,59 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
       if (!mbar_wait_warp(smem_u32(&bar_sf), j & 1, abortp)) { fail(__LINE__); ok = false; break; }
       tc_fence_after();
       const int64_t lim = resp ? (int64_t)r + 1 : (tslot >= 0 && tslot < p.pool_pages ? ke : key0);
-      const int64_t nvh = lim - key0 - hf * 64;
-      const int nv = (int)(nvh < 0 ? 0 : (nvh < 64 ? nvh : 64));  // visible keys of this half
+      const int64_t nvq = lim - key0 - qq * 32;
+      const int nv = (int)(nvq < 0 ? 0 : (nvq < 32 ? nvq : 32));  // visible keys of this quarter
+      const bool full = nv == 32;  // every key visible: no masks
       const int nvalid_tile = (int)(ke - key0 < BN ? ke - key0 : BN);
-      float pv[64];
+      float pv[32];
       {
-        uint32_t r0[32], r1[32];
+        uint32_t r0[32];
         tmem_ld32(tX, r0);
-        tmem_ld32(tX + 32, r1);
         tmem_wait_ld_r(r0);
-        reg_dep(r1);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          pv[c] = __uint_as_float(r0[c]);
-          pv[32 + c] = __uint_as_float(r1[c]);
-        }
+        for (int c = 0; c < 32; ++c) pv[c] = __uint_as_float(r0[c]);
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&bar_sfree));  // dP_j may now overwrite X
+      warp_arrive(smem_u32(&bar_sfree));  // dP_j may now overwrite X
+      if (full) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) pv[c] = c < nv ? ex2(pv[c] * p.scale_log2 - lse2) : 0.f;
+        for (int c = 0; c < 32; ++c) pv[c] = ex2(fmaf(pv[c], p.scale_log2, -lse2));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pv[c] = c < nv ? ex2(fmaf(pv[c], p.scale_log2, -lse2)) : 0.f;
+      }
       if (!mbar_wait_warp(smem_u32(&bar_dpf), j & 1, abortp)) { fail(__LINE__); ok = false; break; }
       tc_fence_after();
-      uint32_t ds_pk[32];
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
+      uint32_t ds_pk[16];
+      {
         uint32_t rp[32];
-        tmem_ld32(tX + c0, rp);
+        tmem_ld32(tX, rp);
         tmem_wait_ld_r(rp);
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float d0 = c0 + c < nv ? pv[c0 + c] * (__uint_as_float(rp[c]) - dl) : 0.f;
-          const float d1 = c0 + c + 1 < nv ? pv[c0 + c + 1] * (__uint_as_float(rp[c + 1]) - dl) : 0.f;
-          ds_pk[(c0 + c) >> 1] = pack_bf16x2(d0, d1);
+          for (int c = 0; c < 32; c += 2)
+            ds_pk[c >> 1] = pack_bf16x2(pv[c] * (__uint_as_float(rp[c]) - dl),
+                                        pv[c + 1] * (__uint_as_float(rp[c + 1]) - dl));
+        } else {
+          // masked keys give dS = 0 exactly, whatever dP holds (NaN included)
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float d0 = c < nv ? pv[c] * (__uint_as_float(rp[c]) - dl) : 0.f;
+            const float d1 = c + 1 < nv ? pv[c + 1] * (__uint_as_float(rp[c + 1]) - dl) : 0.f;
+            ds_pk[c >> 1] = pack_bf16x2(d0, d1);
+          }
         }
       }
-      // every dP column of this half has been read: its dS goes over the
+      // every dP column of this quarter has been read: its dS goes over the
       // first half of those columns
-#pragma unroll
-      for (int c0 = 0; c0 < 32; c0 += 16) tmem_st16(tX + c0, ds_pk + c0);
+      tmem_st16(tX, ds_pk);
       tmem_wait_st();
       if (!resp && nvalid_tile < BN) {
         // partial last prompt tile: rows past the prompt end may hold anything
         // (NaN included); zero them in both K chunks so that dS = 0 times K
         // stays 0 in dQ += dS K
         const int nz = (BN - nvalid_tile) * 32;  // 16-byte pieces: 2 chunks x 2 boxes x 8
-        for (int z = sw * 32 + lane; z < nz; z += 256) {
+        for (int z = sw * 32 + lane; z < nz; z += 32 * kSoftWarps) {
           const int row = nvalid_tile + z / 32;
           const int rem = z & 31;
           st_shared_v4(chunk_addr(4 * j + (rem >> 4)) + ((rem >> 3) & 1) * L::kBox + row * 128 +
@@ -821,7 +834,7 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
         fence_proxy_async_smem();
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&bar_dsf));
+      warp_arrive(smem_u32(&bar_dsf));
     }
 
     if (ok && ntiles > 0) {
@@ -831,7 +844,7 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
     const int64_t nrows = (int64_t)p.R * p.hq;
     float* out = p.dq_parts + ((int64_t)part * nrows + n) * kD;
 #pragma unroll 1
-    for (int c0 = hf * 128; c0 < hf * 128 + 128; c0 += 32) {
+    for (int c0 = qq * 64; c0 < qq * 64 + 64; c0 += 32) {
       uint32_t rr[32];
       __syncwarp();
       if (ok && ntiles > 0) {

@@ -127,7 +127,7 @@ def test_emulated_backward_over_many_tiles(emulator):
      "constexpr uint32_t idesc_q = idesc_bf16(kBM, 128, false);"),
     ("        if (!mbar_wait(smem_u32(&bar_dsf), j & 1, abortp)) { fail(__LINE__); break; }\n", ""),
     ("(j > 0 || kk > 0) ? 1u : 0u);", "kk > 0 ? 1u : 0u);"),
-    ("tbase + L::kTmemX + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8)", "tbase + L::kTmemX + kk * 8"),
+    ("tbase + L::kTmemX + 32 * (kk >> 1) + 8 * (kk & 1)", "tbase + L::kTmemX + kk * 8"),
 ], ids=["K_read_K_major_in_dQ", "dQ_before_dS_is_written", "dQ_reset_every_tile",
         "dS_of_the_second_half_misplaced"])
 def test_emulator_rejects_planted_kernel_mistakes(tmp_path, mutation):
