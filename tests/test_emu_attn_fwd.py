@@ -62,14 +62,13 @@ def _bf16_bytes(t):
     return t.to(torch.bfloat16).contiguous().view(torch.int16).numpy().tobytes()
 
 
-def run_case(exe, d, P=600, R=64, seed=6):
+def run_case(exe, d, P=600, R=64, seed=6, span=256):
     w = inputs.Workload("emu", 12, 2, 256, 256, P, (R,), "bf16", seed=seed, pool_factor=2,
                         poison=True)
     pr = inputs.make_prompt(w, "cpu")
     m = inputs.make_member(w, 0, "cpu")
     want = ref.replay_member(pr["k_pool"], pr["v_pool"], pr["page_table"], P, m["q"], m["k"], m["v"],
                              scale=w.scale)
-    span = 256
     ns = -(-P // span)
     kp, pt = pr["k_pool"], pr["page_table"]
     hdr = np.array([w.hq, w.hkv, R, P, w.page_size, kp.shape[0], pt.shape[0], ns, span],
@@ -110,10 +109,25 @@ def test_emulated_forward_matches_the_oracle(emulator):
     assert e_o <= TOL_BF16 and e_l <= LSE_TOL, (e_o, e_l)
 
 
-def test_emulator_rejects_a_planted_kernel_mistake(tmp_path):
-    """V read as a K-major operand in P V, planted in a copy of the kernel
+def test_emulated_forward_over_many_tiles(emulator):
+    """One 1500-key part: 12 tiles, 24 ring units, the slot releases wrap the
+    five-chunk ring many times; partial last tile."""
+    exe, d = emulator
+    status, e_o, e_l = run_case(exe, d, P=1500, R=40, seed=7, span=1536)
+    assert status[0] == 0, status
+    assert e_o <= TOL_BF16 and e_l <= LSE_TOL, (e_o, e_l)
+
+
+@pytest.mark.parametrize("mutation", [
+    ("constexpr uint32_t idesc_pv = idesc_bf16(kBM, kD, true);",
+     "constexpr uint32_t idesc_pv = idesc_bf16(kBM, kD, false);"),
+    ("            if (!mbar_wait_warp(smem_u32(&bar_cd[v % NCD]), (v / NCD) & 1, abortp)) {",
+     "            if (false) {"),
+], ids=["V_read_K_major", "K_slot_reused_before_S_is_done"])
+def test_emulator_rejects_planted_kernel_mistakes(tmp_path, mutation):
+    """V read as a K-major operand in P V, or a K chunk's slot refilled
+    before the S that reads it is complete, planted in a copy of the kernel
     source, must fail the comparison."""
-    exe = build(tmp_path, ("constexpr uint32_t idesc_pv = idesc_bf16(kBM, kD, true);",
-                           "constexpr uint32_t idesc_pv = idesc_bf16(kBM, kD, false);"))
-    status, e_o, e_l = run_case(exe, tmp_path)
-    assert not e_o <= TOL_BF16, e_o
+    exe = build(tmp_path, mutation)
+    status, e_o, e_l = run_case(exe, tmp_path, P=1500, R=40, seed=7, span=1536)
+    assert not (e_o <= TOL_BF16 and e_l <= LSE_TOL), (e_o, e_l)
