@@ -6,16 +6,14 @@
 // memory, streams the part's key pages, recomputes P from the stored LSE and
 // accumulates dQ in tensor memory.  No score matrix is kept between tiles.
 //
-// The kernel keeps dO in tensor memory as the A operand of dP = dO V^T,
-// which leaves room for three K stages in shared memory.  Per key tile j
-// (BN keys):
-//   S_j  = Q K_j^T            (tcgen05, SS)        -> TMEM S
-//   dP_j = dO V_j^T           (tcgen05, TS)        -> TMEM dP
+// Per key tile j (128 keys), with dO held in tensor memory as the A operand
+// of dP = dO V^T:
+//   S_j  = Q K_j^T            (tcgen05, SS)        -> TMEM X
+//   dP_j = dO V_j^T           (tcgen05, TS)        -> TMEM X (after S_j is read)
 //   softmax warps: P = exp2(S*scale*log2e - LSE*log2e), dS = P * (dP - delta),
-//                  dS (bf16) written back into tensor memory
+//                  dS (bf16) written back over X
 //   dQ  += dS_j K_j           (tcgen05, A from TMEM, K as N-major B operand)
-// The MMA issue order keeps the tensor pipe busy while the softmax warps work
-// on one tile and the next tile's K/V land.
+// (details and the shared-memory ring below, at the kernel).
 // Output: unscaled float32 dQ partial of the part; the reduction kernel sums
 // parts and applies the softmax scale.
 #include <cuda.h>
@@ -34,7 +32,6 @@ using namespace tc;
 
 constexpr int kD = 256;
 constexpr int kBM = 128;
-constexpr int kThreads = 256;
 constexpr float kLog2ef = 1.4426950408889634f;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -63,402 +60,7 @@ struct BwdKParams {
 };
 
 // ===========================================================================
-// Backward with dO held in tensor memory (default).  dP = dO V^T takes dO as
-// the A operand from tensor memory, which leaves shared memory for two K and
-// three V tile slots.  Tensor memory: dQ [0,256), dO [256,384) (bf16 pairs),
-// S [384,448), dP [448,512).  The softmax warps release S as soon as they
-// have read it and write dS (bf16) over the first half of dP.
-//
-// The MMA thread issues, per key tile j:  S_{j+1}, dQ_j, dP_{j+1}.
-// Its issue blocks at about the rate the tensor pipe executes, and every
-// commit and every barrier test between groups costs pipe time, so the tile
-// carries as few of them as the dependencies allow:
-//   waits   : tile_full (K and V of one tile, one barrier), s_free, ds_full
-//   commits : s_full after S; dp_full and tile_free after dP (dP_{j+1}
-//             follows dQ_j, so it frees V_{j+1} and K_j).
-// A K tile lives from its load to its dQ, so K gets three slots and V two:
-// tile m's K and V go out together once dP_{m-2} is done, about one tile
-// period of MMA work before S_m needs them.  One producer warp loads a whole
-// K or V tile with a single TMA instruction.
-// ===========================================================================
-struct BwdTmLayout {
-  static constexpr int BN = 64, KSK = 3, KSV = 2, NT = 3;  // K slots, V slots, tile barriers
-  static constexpr uint32_t kRowBox = kBM * 128;        // 16 KB
-  static constexpr uint32_t kKVBytes = BN * kD * 2;     // 32 KB
-  static constexpr uint32_t kKVBox = BN * 128;          // 8 KB
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + 4 * kRowBox;
-  static constexpr uint32_t kV = kK + KSK * kKVBytes;
-  static constexpr uint32_t kEnd = kV + KSV * kKVBytes;
-  static constexpr uint32_t kSmem = kEnd + 1024;
-  static constexpr uint32_t kTmemO = 256, kTmemS = 384, kTmemP = 448;
-  static_assert(kSmem <= 227 * 1024 - 512, "shared memory budget");
-  // tile_free of tile m-KSV (committed after dP_{m-KSV}) frees V slot m%KSV
-  // and, since dQ_{m-KSV-1} was issued before that dP, K slot m%KSK
-  static_assert(KSK == KSV + 1, "slot release assumes one more K slot than V slots");
-  static_assert(KSV <= NT, "tile barrier ring too short");
-};
-
-__global__ void __launch_bounds__(kThreads, 1)
-    tc_bwd_dq_tm_kernel(const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV,
-                        const __grid_constant__ CUtensorMap tmKr,
-                        const __grid_constant__ CUtensorMap tmVr, const BwdKParams p) {
-  using L = BwdTmLayout;
-  constexpr int BN = L::BN, KSK = L::KSK, KSV = L::KSV, NT = L::NT;
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_tf[NT], bar_te[NT], bar_sf, bar_sfree, bar_dpf, bar_dsf, bar_fin,
-      bar_drain;
-  __shared__ uint32_t tmem_base_s;
-  __shared__ uint32_t abort_s;
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sQ = sbase + L::kQ, sK = sbase + L::kK, sV = sbase + L::kV;
-
-  const int mt = blockIdx.x % p.n_mt;
-  const int kvh = (blockIdx.x / p.n_mt) % p.hkv;
-  const int part = blockIdx.x / (p.n_mt * p.hkv);
-  const bool resp = part == p.ns;
-  const int64_t rows_g = (int64_t)p.gq * p.R;
-  int64_t kb, ke;
-  if (!resp) {
-    kb = (int64_t)part * p.split_span;
-    ke = kb + p.split_span < p.P ? kb + p.split_span : p.P;
-  } else {
-    const int64_t t0 = (int64_t)mt * kBM;
-    const int64_t t1 = (t0 + kBM < rows_g ? t0 + kBM : rows_g) - 1;
-    kb = 0;
-    ke = (t0 / p.R == t1 / p.R) ? (t1 % p.R) + 1 : p.R;
-  }
-  const int ntiles = ke > kb ? (int)((ke - kb + BN - 1) / BN) : 0;
-
-  if (tid == 0) {
-    abort_s = 0;
-    mbar_init(smem_u32(&bar_q), 128);
-    for (int s = 0; s < NT; ++s) {
-      mbar_init(smem_u32(&bar_tf[s]), 1);
-      mbar_init(smem_u32(&bar_te[s]), 1);
-    }
-    mbar_init(smem_u32(&bar_sf), 1);
-    mbar_init(smem_u32(&bar_sfree), 128);
-    mbar_init(smem_u32(&bar_dpf), 1);
-    mbar_init(smem_u32(&bar_dsf), 128);
-    mbar_init(smem_u32(&bar_fin), 1);
-    mbar_init(smem_u32(&bar_drain), 1);
-    fence_mbar_init();
-  }
-  if (warp == 2) {
-    tmem_alloc(smem_u32(&tmem_base_s), 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = tmem_base_s;
-  const volatile uint32_t* abortp = &abort_s;
-  auto fail = [&](int line) {
-    atomicOr(p.status, kStatusTimeout);
-    atomicCAS(p.status + 1, 0u, ((uint32_t)kKTcBwdDq << 16) | (uint32_t)line);
-    abort_s = 1;
-  };
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // whole warp: lane 0 posts the bytes and loads K, lane 1 loads V, each
-    // tile with one instruction
-    if (ntiles > 0) {
-      if (lane == 0) prefetch_tmap(resp ? &tmKr : &tmK);
-      if (lane == 1) prefetch_tmap(resp ? &tmVr : &tmV);
-      int issued = 0;
-      for (int m = 0; m < ntiles; ++m) {
-        // V slot m%KSV last held tile m-KSV and K slot m%KSK tile m-KSV-1;
-        // both are free once dP_{m-KSV} has completed
-        bool ok = true;
-        if (m >= KSV) {
-          const int o = m - KSV;
-          ok = mbar_wait_warp(smem_u32(&bar_te[o % NT]), (o / NT) & 1, abortp);
-        }
-        if (!ok) {
-          if (lane == 0) fail(__LINE__);
-          break;
-        }
-        const int64_t key0 = kb + (int64_t)m * BN;
-        const uint32_t fb = smem_u32(&bar_tf[m % NT]);
-        int32_t row = 0;
-        if (!resp) {
-          const int32_t slot = __ldg(p.page_table + key0 / p.page_size);
-          if (slot < 0 || slot >= p.pool_pages) {
-            if (lane == 0) atomicOr(p.status, kStatusBadPage);
-            row = (int32_t)p.pool_rows;  // out of range: the load reads zeros
-          } else {
-            row = (int32_t)(((int64_t)slot * p.hkv + kvh) * p.page_size + key0 % p.page_size);
-          }
-        }
-        if (lane == 0) mbar_expect_tx(fb, 2 * L::kKVBytes);
-        __syncwarp();
-        if (lane < 2) {
-          const uint32_t dst = lane == 0 ? sK + (m % KSK) * L::kKVBytes : sV + (m % KSV) * L::kKVBytes;
-          if (resp)
-            tma_load_4d(dst, lane == 0 ? &tmKr : &tmVr, fb, 0, (int32_t)key0, 0, kvh);
-          else
-            tma_load_3d(dst, lane == 0 ? &tmK : &tmV, fb, 0, row, 0);
-        }
-        __syncwarp();
-        issued = m + 1;
-      }
-      // no copy may still be landing in shared memory when the CTA ends
-      for (int m = issued - NT < 0 ? 0 : issued - NT; m < issued; ++m)
-        mbar_wait(smem_u32(&bar_tf[m % NT]), (m / NT) & 1, abortp);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && ntiles > 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(kBM, BN, false);
-      constexpr uint32_t idesc_dq = idesc_bf16(kBM, kD, true);
-      auto issue_s = [&](int j) {  // S = Q K_j^T
-        const uint32_t kslot = sK + (j % KSK) * L::kKVBytes;
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ss(tbase + L::kTmemS, sdesc_sw128(sQ + (kk >> 2) * L::kRowBox + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(kslot + (kk >> 2) * L::kKVBox + (kk & 3) * 32, 16, 1024), idesc_s,
-                 kk > 0 ? 1u : 0u);
-        mma_commit(smem_u32(&bar_sf));
-      };
-      auto issue_dp = [&](int j) {  // dP = dO V_j^T, dO from tensor memory
-        const uint32_t vslot = sV + (j % KSV) * L::kKVBytes;
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ts(tbase + L::kTmemP, tbase + L::kTmemO + kk * 8,
-                 sdesc_sw128(vslot + (kk >> 2) * L::kKVBox + (kk & 3) * 32, 16, 1024), idesc_s,
-                 kk > 0 ? 1u : 0u);
-        mma_commit(smem_u32(&bar_dpf));
-        mma_commit(smem_u32(&bar_te[j % NT]));  // V_j and K_{j-1} are done
-      };
-      bool ok = mbar_wait(smem_u32(&bar_q), 0, abortp) && mbar_wait(smem_u32(&bar_tf[0]), 0, abortp);
-      if (!ok) fail(__LINE__);
-      tc_fence_after();
-      if (ok) {
-        issue_s(0);
-        issue_dp(0);
-      }
-      for (int j = 0; ok && j < ntiles; ++j) {
-        if (j + 1 < ntiles) {
-          // S columns are free once the softmax warps have read S_j; K and V
-          // of tile j+1 arrive on one barrier
-          const int n1 = j + 1;
-          if (!mbar_wait(smem_u32(&bar_sfree), j & 1, abortp) ||
-              !mbar_wait(smem_u32(&bar_tf[n1 % NT]), (n1 / NT) & 1, abortp)) {
-            fail(__LINE__);
-            break;
-          }
-          tc_fence_after();
-          issue_s(n1);
-        }
-        // dQ += dS_j K_j, dS read from the dP columns
-        if (!mbar_wait(smem_u32(&bar_dsf), j & 1, abortp)) { fail(__LINE__); break; }
-        tc_fence_after();
-        const uint32_t kslot = sK + (j % KSK) * L::kKVBytes;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tbase, tbase + L::kTmemP + kk * 8,
-                 sdesc_sw128(kslot + kk * 16 * 128, L::kKVBox, 1024), idesc_dq,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        if (j == ntiles - 1) mma_commit(smem_u32(&bar_fin));
-        // dP_{j+1} overwrites dS_j, which dQ_j (issued before it) has consumed
-        if (j + 1 < ntiles) issue_dp(j + 1);
-      }
-      mma_commit(smem_u32(&bar_drain));
-      mbar_wait(smem_u32(&bar_drain), 0, abortp);
-    }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax
-    const int i = tid - 128;
-    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
-    const int64_t t = (int64_t)mt * kBM + i;
-    const bool row_ok = t < rows_g;
-    const int hh = row_ok ? (int)(t / p.R) : 0;
-    const int r = row_ok ? (int)(t % p.R) : 0;
-    const int64_t n = (int64_t)r * p.hq + (int64_t)kvh * p.gq + hh;
-    const float lse2 = row_ok ? __ldg(p.lse + n) * kLog2ef : 0.f;
-    const float dl = row_ok ? __ldg(p.delta + n) : 0.f;
-    {
-      // Q tile into shared memory (warp-cooperative rows, swizzled) ...
-      const int wq = warp - 4;
-      for (int rr = 0; rr < 32; ++rr) {
-        const int row = wq * 32 + rr;
-        const int64_t tt = (int64_t)mt * kBM + row;
-        uint4 vq = make_uint4(0u, 0u, 0u, 0u);
-        if (tt < rows_g) {
-          const int hh2 = (int)(tt / p.R), r2 = (int)(tt % p.R);
-          const int64_t n2 = (int64_t)r2 * p.hq + (int64_t)kvh * p.gq + hh2;
-          vq = __ldg(reinterpret_cast<const uint4*>(p.q + n2 * kD) + lane);
-        }
-        st_shared_v4(sQ + (lane >> 3) * L::kRowBox + sw128_offset(row, lane & 7), vq);
-      }
-      fence_proxy_async_smem();
-      // ... and this thread's dO row into tensor memory lane i (bf16 pairs)
-      const uint4* orow = reinterpret_cast<const uint4*>(p.d_o + n * kD);
-#pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t rr[32];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 v = row_ok ? __ldg(orow + (c0 >> 2) + u) : make_uint4(0u, 0u, 0u, 0u);
-          rr[4 * u] = v.x;
-          rr[4 * u + 1] = v.y;
-          rr[4 * u + 2] = v.z;
-          rr[4 * u + 3] = v.w;
-        }
-        tmem_st32(tbase + lane_off + L::kTmemO + c0, rr);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_q));
-    }
-
-    bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
-      const int64_t key0 = kb + (int64_t)j * BN;
-      // a tile whose page id lies outside the pool holds no keys (zeros were
-      // loaded for it and the status word flagged); read before the wait
-      const int32_t tslot = resp ? 0 : __ldg(p.page_table + key0 / p.page_size);
-      if (!mbar_wait_warp(smem_u32(&bar_sf), j & 1, abortp)) { fail(__LINE__); ok = false; break; }
-      tc_fence_after();
-      const int64_t lim = resp ? (int64_t)r + 1 : (tslot >= 0 && tslot < p.pool_pages ? ke : key0);
-      const int nvalid = (int)(lim - key0 < 0 ? 0 : (lim - key0 < BN ? lim - key0 : BN));
-      const int nvalid_tile = (int)(ke - key0 < BN ? ke - key0 : BN);
-      float pv[BN];
-#pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t rs[32];
-        tmem_ld32(tbase + lane_off + L::kTmemS + c0, rs);
-        tmem_wait_ld_r(rs);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) pv[c0 + c] = __uint_as_float(rs[c]);
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_sfree));  // S_{j+1} may now overwrite S
-#pragma unroll
-      for (int c = 0; c < BN; ++c)
-        pv[c] = c < nvalid ? ex2(pv[c] * p.scale_log2 - lse2) : 0.f;
-      if (!mbar_wait_warp(smem_u32(&bar_dpf), j & 1, abortp)) { fail(__LINE__); ok = false; break; }
-      tc_fence_after();
-      uint32_t ds_pk[BN / 2];
-#pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t rp[32];
-        tmem_ld32(tbase + lane_off + L::kTmemP + c0, rp);
-        tmem_wait_ld_r(rp);
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float d0 = c0 + c < nvalid ? pv[c0 + c] * (__uint_as_float(rp[c]) - dl) : 0.f;
-          const float d1 = c0 + c + 1 < nvalid ? pv[c0 + c + 1] * (__uint_as_float(rp[c + 1]) - dl) : 0.f;
-          ds_pk[(c0 + c) >> 1] = pack_bf16x2(d0, d1);
-        }
-      }
-      // every dP column of this row has been read: dS goes over its first half
-#pragma unroll
-      for (int c0 = 0; c0 < BN / 2; c0 += 16)
-        tmem_st16(tbase + lane_off + L::kTmemP + c0, ds_pk + c0);
-      tmem_wait_st();
-      if (!resp && nvalid_tile < BN) {
-        // partial last prompt tile: rows past the prompt end may hold anything;
-        // zero them in K so that dS = 0 times K stays 0 in dQ += dS K
-        const uint32_t kslot = sK + (j % KSK) * L::kKVBytes;
-        const int nz = (BN - nvalid_tile) * (kD / 64) * 8;
-        for (int z = i; z < nz; z += 128) {
-          const int row = nvalid_tile + z / ((kD / 64) * 8);
-          const int box = (z / 8) % (kD / 64);
-          st_shared_v4(kslot + box * L::kKVBox + row * 128 + (z & 7) * 16, make_uint4(0u, 0u, 0u, 0u));
-        }
-        fence_proxy_async_smem();
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_dsf));
-    }
-
-    if (ok && ntiles > 0) {
-      if (!mbar_wait_warp(smem_u32(&bar_fin), 0, abortp)) { fail(__LINE__); ok = false; }
-      tc_fence_after();
-    }
-    const int64_t nrows = (int64_t)p.R * p.hq;
-    float* out = p.dq_parts + ((int64_t)part * nrows + n) * kD;
-#pragma unroll 1
-    for (int c0 = 0; c0 < kD; c0 += 32) {
-      uint32_t rr[32];
-      __syncwarp();
-      if (ok && ntiles > 0) {
-        tmem_ld32(tbase + lane_off + c0, rr);
-        tmem_wait_ld_r(rr);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) rr[c] = 0u;
-      }
-      if (row_ok) {
-#pragma unroll
-        for (int c = 0; c < 32; c += 4)
-          *reinterpret_cast<float4*>(out + c0 + c) =
-              make_float4(__uint_as_float(rr[c]), __uint_as_float(rr[c + 1]),
-                          __uint_as_float(rr[c + 2]), __uint_as_float(rr[c + 3]));
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 2) {
-    tc_fence_after();
-    tmem_dealloc(tbase, 512);
-  }
-}
-
-cudaError_t bwd_tm(const BwdParams& a, cudaStream_t s) {
-  using L = BwdTmLayout;
-  const AttnGeom& g = a.g;
-  BwdKParams p;
-  p.hq = g.hq;
-  p.hkv = g.hkv;
-  p.gq = g.gq;
-  p.R = g.R;
-  p.P = g.P;
-  p.pool_pages = g.pool_pages;
-  p.pool_rows = g.pool_pages * g.hkv * g.page_size;
-  p.page_size = g.page_size;
-  p.ns = g.ns;
-  p.split_span = g.split_span;
-  p.n_mt = (int)(((int64_t)g.gq * g.R + kBM - 1) / kBM);
-  p.scale_log2 = g.scale_log2;
-  p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
-  p.d_o = reinterpret_cast<const __nv_bfloat16*>(a.d_o);
-  p.lse = a.lse;
-  p.delta = a.delta;
-  p.page_table = a.page_table;
-  p.dq_parts = a.dq_parts;
-  p.status = a.status;
-  CUtensorMap tk, tv, tkr, tvr;
-  memset(&tk, 0, sizeof(tk));
-  memset(&tv, 0, sizeof(tv));
-  if (g.P > 0 && (!encode_pool_tile_map(&tk, a.k_pool, p.pool_rows, L::BN) ||
-                  !encode_pool_tile_map(&tv, a.v_pool, p.pool_rows, L::BN)))
-    return cudaErrorInvalidValue;
-  if (!encode_rows_tile_map(&tkr, a.k_resp, g.hkv, g.R, L::BN) ||
-      !encode_rows_tile_map(&tvr, a.v_resp, g.hkv, g.R, L::BN))
-    return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(tc_bwd_dq_tm_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kSmem);
-  if (e != cudaSuccess) return e;
-  const int64_t units = (int64_t)launch_parts(g) * g.hkv * p.n_mt;
-  if (units == 0) return cudaSuccess;
-  LaunchScope ls(kKTcBwdDq, s);
-  tc_bwd_dq_tm_kernel<<<(unsigned)units, kThreads, L::kSmem, s>>>(tk, tv, tkr, tvr, p);
-  return cudaGetLastError();
-}
-
-
-// ===========================================================================
-// Backward with 128-key tiles at the tensor pipe's full rate (default).
+// Backward with 128-key tiles at the tensor pipe's full rate.
 //
 // The dQ accumulator (256 columns) and dO (128 columns of bf16 pairs) leave
 // one 128-column tensor-memory area X, which S_j, dP_j and dS_j share in
@@ -915,20 +517,8 @@ cudaError_t bwd_ring(const BwdParams& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-bool use_tm_kernel() {
-  static const bool v = [] {
-    const char* e = getenv("LS_TC_BWD_VARIANT");
-    return e && e[0] == 't';
-  }();
-  return v;
-}
-
 }  // namespace
 
-// The 128-key ring kernel; LS_TC_BWD_VARIANT=tm selects the 64-key kernel
-// with three K slots for comparison.
-cudaError_t launch_tc_bwd_dq(const BwdParams& a, cudaStream_t s) {
-  return use_tm_kernel() ? bwd_tm(a, s) : bwd_ring(a, s);
-}
+cudaError_t launch_tc_bwd_dq(const BwdParams& a, cudaStream_t s) { return bwd_ring(a, s); }
 
 }  // namespace ls

@@ -1,5 +1,4 @@
-// Runs a prompt-attention backward kernel's source (tc_bwd_dq_ring_kernel with
-// LS_EMU_RING defined, else tc_bwd_dq_tm_kernel) on
+// Runs the prompt-attention backward kernel's source (tc_bwd_dq_ring_kernel) on
 // the CPU block emulator:  attn_bwd_emu <in.bin> <out.bin>
 // in.bin: int64 hq, hkv, R, P, page_size, pool_pages, num_pages, ns,
 // split_span; float32 scale; then bf16 k_pool, v_pool [pool_pages][hkv][page][256],
@@ -31,18 +30,11 @@ emu::TensorMap rows_tile_map(const void* base, int heads, int64_t rows, int box_
           {64, (uint32_t)box_rows, (uint32_t)blocks, 1}};
 }
 
-#ifdef LS_EMU_RING
 // the 128-key ring kernel: K and V chunks of [128 keys x 128 columns]
 constexpr int kBoxBlocks = 2;
 #define LS_EMU_KERNEL tc_bwd_dq_ring_kernel
 #define LS_EMU_THREADS kThreadsRing
 using EmuLayout = BwdRingLayout;
-#else
-constexpr int kBoxBlocks = 4;
-#define LS_EMU_KERNEL tc_bwd_dq_tm_kernel
-#define LS_EMU_THREADS kThreads
-using EmuLayout = BwdTmLayout;
-#endif
 
 void emulate(BwdKParams p, const void* k_pool, const void* v_pool, const void* k_resp,
              const void* v_resp) {

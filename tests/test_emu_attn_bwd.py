@@ -1,4 +1,4 @@
-"""The prompt-attention backward kernel (tc_bwd_dq_tm_kernel in
+"""The prompt-attention backward kernel (tc_bwd_dq_ring_kernel in
 csrc/ls_tc_bwd.cu), its own source compiled for the host and run on the CPU
 block emulator (tests/emu/): TMA copies and tcgen05 MMAs run asynchronously
 on engine threads with random delays, so a missing wait or an early slot
@@ -26,7 +26,6 @@ TOL_BF16 = 2e-2
 
 
 KERNELS = {  # kernel: (first line of its block, line after it)
-    "tm": ("struct BwdTmLayout", "cudaError_t bwd_tm("),
     "ring": ("struct BwdRingLayout", "cudaError_t bwd_ring("),
 }
 
@@ -42,9 +41,8 @@ def kernel_source(mutation=None, kernel="ring"):
         assert mutation[0] in body, mutation[0]
         i = body.rindex(mutation[0])
         body = body[:i] + mutation[1] + body[i + len(mutation[0]):]
-    pre = src[:src.index("// ===========================================================================\n// Backward with dO held in tensor memory")]
-    text = ("#define LS_EMU_RING 1\n" if kernel == "ring" else "") + pre + body + \
-        "}  // namespace\n}  // namespace ls\n"
+    pre = src[:src.index("// ===========================================================================\n// Backward with 128-key tiles")]
+    text = pre + body + "}  // namespace\n}  // namespace ls\n"
     text = text.replace("extern __shared__", "extern")
     ex2 = 'asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));'
     assert ex2 in text
@@ -100,7 +98,7 @@ def run_case(exe, d, P=600, R=64, seed=5, span=256):
     return out, float(np.abs(dq - want["dq"]).max() / np.abs(want["dq"]).max())
 
 
-@pytest.fixture(scope="module", params=["ring", "tm"])
+@pytest.fixture(scope="module", params=["ring"])
 def emulator(tmp_path_factory, request):
     d = tmp_path_factory.mktemp("emu_attn_bwd_" + request.param)
     return build(d, kernel=request.param), d
