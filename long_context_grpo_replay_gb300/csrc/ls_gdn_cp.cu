@@ -263,7 +263,8 @@ __global__ void __launch_bounds__(kThr, 1)
 // end, E and dU into the scratch.
 constexpr uint32_t kChT0 = 0, kChT1 = kTile, kChT2 = 2 * kTile, kChT3 = 3 * kTile;
 constexpr uint32_t kChT4 = 4 * kTile, kChT5 = 5 * kTile, kChMisc = 6 * kTile;
-constexpr uint32_t kChainSmem = kChMisc + 2048 + 1024;
+constexpr uint32_t kChRowScr = kChMisc + 2048;  // per-warp row scratch (rows_load32 / rows_store32)
+constexpr uint32_t kChainSmem = kChRowScr + kRowScrFloats * 4 + 1024;
 
 __global__ void __launch_bounds__(kThr, 1)
     gdn_cp_chain_kernel(int H, int R, int nch, const float* __restrict__ s0,
@@ -279,11 +280,14 @@ __global__ void __launch_bounds__(kThr, 1)
   float* sbt = sc + kC;
   float* swt = sbt + kC;
   float* sw = swt + 4;  // w_t (state pass) or gamma_t (gradient pass), zero past the response
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kChMisc + 1536);
+  // the barriers sit past sw (which ends at byte 1552 of the misc area)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kChMisc + 1600);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
   uint32_t* abort_s = tslot + 1;
 
   const int h = blockIdx.x, m = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+  float* wscr = reinterpret_cast<float*>(sm + kChRowScr) + warp * 32 * 33;
+  const int r0 = warp * 32;  // first row of this warp's 32 (rows of S, G, E, dU)
   {
     const int64_t tok = (int64_t)m * R * H;
     q += tok * kD, k += tok * kD, d_o += tok * kD, g += tok, beta += tok;
@@ -319,9 +323,9 @@ __global__ void __launch_bounds__(kThr, 1)
     const int nt = R - t0 < kC ? (int)(R - t0) : kC;
     float* blk = scratch_of(scr, H, nch, m, h, ch);
     {
-      float* dst = blk + (int64_t)kSstart * kTileElems + x * kD;
+      float* dst = blk + (int64_t)kSstart * kTileElems + r0 * kD;
 #pragma unroll
-      for (int c = 0; c < kD; ++c) dst[c] = st[c];
+      for (int cb = 0; cb < 4; ++cb) rows_store32(st + cb * 32, dst + cb * 32, kD, 32, wscr);
     }
     stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
     __syncthreads();
@@ -341,20 +345,22 @@ __global__ void __launch_bounds__(kThr, 1)
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
     {  // E row x = E0 row x - (ZK S^T) row x; E^T column x as bf16
-      const float* e0 = blk + (int64_t)kE0 * kTileElems + x * kD;
-      float* eo = blk + (int64_t)kEblk * kTileElems + x * kD;
+      const float* e0 = blk + (int64_t)kE0 * kTileElems + r0 * kD;
+      float* eo = blk + (int64_t)kEblk * kTileElems + r0 * kD;
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t t32[32];
+        float ev[32];
+        rows_load32(ev, e0 + cb * 32, kD, 32, wscr);
         tmem_ld32(tb + lane_off + cb * 32, t32);
         tmem_wait_ld_r(t32);
 #pragma unroll
         for (int xx = 0; xx < 32; ++xx) {
           const int i = cb * 32 + xx;
-          const float e = e0[i] - __uint_as_float(t32[xx]);
-          eo[i] = e;
-          st_shared_u16(sb + kChT3 + elem_off(i, x), bf16_of(e));
+          ev[xx] -= __uint_as_float(t32[xx]);
+          st_shared_u16(sb + kChT3 + elem_off(i, x), bf16_of(ev[xx]));
         }
+        rows_store32(ev, eo + cb * 32, kD, 32, wscr);
       }
     }
     fence_proxy_async_smem();
@@ -395,9 +401,9 @@ __global__ void __launch_bounds__(kThr, 1)
     const int nt = R - t0 < kC ? (int)(R - t0) : kC;
     float* blk = scratch_of(scr, H, nch, m, h, ch);
     {
-      float* dst = blk + (int64_t)kGend * kTileElems + x * kD;
+      float* dst = blk + (int64_t)kGend * kTileElems + r0 * kD;
 #pragma unroll
-      for (int c = 0; c < kD; ++c) dst[c] = st[c];
+      for (int cb = 0; cb < 4; ++cb) rows_store32(st + cb * 32, dst + cb * 32, kD, 32, wscr);
     }
     stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
     __syncthreads();
@@ -428,21 +434,23 @@ __global__ void __launch_bounds__(kThr, 1)
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
     {  // dU row x = dU0 row x + (ZW G^T) row x; -(gamma b dU)^T column x as bf16
-      const float* u0 = blk + (int64_t)kDU0 * kTileElems + x * kD;
-      float* uo = blk + (int64_t)kDUblk * kTileElems + x * kD;
+      const float* u0 = blk + (int64_t)kDU0 * kTileElems + r0 * kD;
+      float* uo = blk + (int64_t)kDUblk * kTileElems + r0 * kD;
       const float f = -sw[x] * sbt[x];
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t t32[32];
+        float uv[32];
+        rows_load32(uv, u0 + cb * 32, kD, 32, wscr);
         tmem_ld32(tb + lane_off + cb * 32, t32);
         tmem_wait_ld_r(t32);
 #pragma unroll
         for (int xx = 0; xx < 32; ++xx) {
           const int i = cb * 32 + xx;
-          const float du = u0[i] + __uint_as_float(t32[xx]);
-          uo[i] = du;
-          st_shared_u16(sb + kChT5 + elem_off(i, x), bf16_of(f * du));
+          uv[xx] += __uint_as_float(t32[xx]);
+          st_shared_u16(sb + kChT5 + elem_off(i, x), bf16_of(f * uv[xx]));
         }
+        rows_store32(uv, uo + cb * 32, kD, 32, wscr);
       }
     }
     fence_proxy_async_smem();
@@ -498,7 +506,8 @@ __global__ void __launch_bounds__(kThr, 1)
 //         dgamma = rowsum(dO . Q S^T) - rowsum(b . dU . K S^T),
 //         and dc_last += sum(rw) + gamma_C <G, S>.
 constexpr uint32_t kOutMisc = 6 * kTile;
-constexpr uint32_t kOutSmem = kOutMisc + 4096 + 1024;
+constexpr uint32_t kOutRowScr = kOutMisc + 4096;  // per-warp row scratch (rows_load32 / rows_store32)
+constexpr uint32_t kOutSmem = kOutRowScr + kRowScrFloats * 4 + 1024;
 
 __global__ void __launch_bounds__(kThr, 1)
     gdn_cp_out_kernel(int H, int R, int nch, const float* __restrict__ q,
@@ -526,6 +535,7 @@ __global__ void __launch_bounds__(kThr, 1)
 
   const int ch = blockIdx.x, h = blockIdx.y, m = blockIdx.z, tid = threadIdx.x, warp = tid >> 5;
   const int lane = tid & 31;
+  float* wscr = reinterpret_cast<float*>(sm + kOutRowScr) + warp * 32 * 33;
   const int64_t t0 = (int64_t)ch * kC;
   const int nt = R - t0 < kC ? (int)(R - t0) : kC;
   {
@@ -540,7 +550,6 @@ __global__ void __launch_bounds__(kThr, 1)
   const float* Eb = blk + (int64_t)kEblk * kTileElems;
   const float* dUb = blk + (int64_t)kDUblk * kTileElems;
   const float* gkb = blk + (int64_t)kGKblk * kTileElems;
-  float* Pb = blk + (int64_t)kE0 * kTileElems;  // the E0 block is free after the chain: P (fp32)
   if (tid == 0) {
     for (int i = 0; i < 5; ++i) mbar_init(smem_u32(&bars[i]), 1);
     *abort_s = 0;
@@ -557,8 +566,10 @@ __global__ void __launch_bounds__(kThr, 1)
   const volatile uint32_t* abortp = abort_s;
   const int64_t rs = (int64_t)H * kD;
   const int t = tid;  // token row in the epilogues
-  const int64_t row = ((t0 + t) * H + h) * kD;  // row t of q, k, v, d_o, o, dq, dk, dv
   const bool live = t < nt;
+  const int r0 = warp * 32;          // first row of this warp's 32
+  const int nvw = nt - r0;           // rows of the warp inside the response
+  const int64_t wrow = ((t0 + r0) * H + h) * kD;  // row r0 of q, k, v, d_o, o, dq, dk, dv
   bool ok = true;
 
   // ---- round 1: Q K^T -> T0, Q S^T -> T1, K S^T -> T2
@@ -589,37 +600,38 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
       uint32_t t32[32];
-      float f32[32];
-      // P row t (bf16 tile S5 for P E, fp32 copy for r)
+      float f32[32], ra[32], rb[32];
+      // P row t (bf16 tile S5: the A operand of P E, and read back for r)
       tmem_ld32(tb + lane_off + 0 + cb * 32, t32);
       tmem_wait_ld_r(t32);
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) {
         const int s = cb * 32 + xx;
         f32[xx] = s <= t ? expf(ct - sc[s]) * __uint_as_float(t32[xx]) : 0.f;
-        Pb[t * kD + s] = f32[xx];
       }
 #pragma unroll
       for (int gg = 0; gg < 4; ++gg) st_shared_v4(S5 + tile_off(t, cb * 4 + gg), pack8(&f32[8 * gg]));
       // Q S^T row t: dgamma, and T1 scaled by gamma_t for o = gamma Q S^T + P E
+      rows_load32(ra, d_o + wrow + cb * 32, rs, nvw, wscr);
       tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
       tmem_wait_ld_r(t32);
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) {
         const float qs = __uint_as_float(t32[xx]);
-        if (live) dgam = fmaf(d_o[row + cb * 32 + xx], qs, dgam);
+        dgam = fmaf(ra[xx], qs, dgam);  // 0 past the response
         t32[xx] = __float_as_uint(gt * qs);
       }
       tmem_st32(tb + lane_off + 128 + cb * 32, t32);
       // K S^T row t: db (dU . X) and dgamma (- b dU . K S^T)
+      rows_load32(ra, dUb + r0 * kD + cb * 32, kD, 32, wscr);
+      rows_load32(rb, v + wrow + cb * 32, rs, nvw, wscr);
       tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
       tmem_wait_ld_r(t32);
       if (live) {
 #pragma unroll
         for (int xx = 0; xx < 32; ++xx) {
-          const int i = cb * 32 + xx;
-          const float ks = __uint_as_float(t32[xx]), du = dUb[t * kD + i];
-          dbt = fmaf(du, v[row + i] - gt * ks, dbt);
+          const float ks = __uint_as_float(t32[xx]), du = ra[xx];
+          dbt = fmaf(du, rb[xx] - gt * ks, dbt);
           dgam = fmaf(-bt * du, ks, dgam);
         }
       }
@@ -649,16 +661,25 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
       uint32_t t32[32];
-      float f32[32];
+      float f32[32], rv[32];
       // o row t
       tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
       tmem_wait_ld_r(t32);
-      if (live && o) {
-        float4* op = reinterpret_cast<float4*>(o + row + cb * 32);
+      if (o) {
 #pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4)
-          op[i4] = make_float4(__uint_as_float(t32[4 * i4]), __uint_as_float(t32[4 * i4 + 1]),
-                               __uint_as_float(t32[4 * i4 + 2]), __uint_as_float(t32[4 * i4 + 3]));
+        for (int xx = 0; xx < 32; ++xx) f32[xx] = __uint_as_float(t32[xx]);
+        rows_store32(f32, o + wrow + cb * 32, rs, nvw, wscr);
+      }
+      // P row t, back from the bf16 tile S5 (before LdP overwrites the row)
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) {
+        const uint4 pk = ld_shared_v4(S5 + tile_off(t, cb * 4 + gg));
+        const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+        for (int i2 = 0; i2 < 4; ++i2) {
+          const float2 f = unpack_bf16x2(w4[i2]);
+          rv[8 * gg + 2 * i2] = f.x, rv[8 * gg + 2 * i2 + 1] = f.y;
+        }
       }
       // dP row t: LdP (tile S5, row t; and LdP^T column t into S0), r = dP . P
       tmem_ld32(tb + lane_off + 0 + cb * 32, t32);
@@ -668,9 +689,7 @@ __global__ void __launch_bounds__(kThr, 1)
         const int s = cb * 32 + xx;
         const float dp = __uint_as_float(t32[xx]);
         f32[xx] = s <= t ? expf(ct - sc[s]) * dp : 0.f;
-        const float r = dp * Pb[t * kD + s];
-        rrow += r;
-        if (r != 0.f) atomicAdd(&rcol[s], r);
+        rv[xx] *= dp;  // r = dP . P
         st_shared_u16(S0 + elem_off(s, t), bf16_of(f32[xx]));
       }
 #pragma unroll
@@ -686,9 +705,7 @@ __global__ void __launch_bounds__(kThr, 1)
           const float da = -__uint_as_float(t32[xx]);
           const float gkv = gkb[a_at(t, s)];
           dbt = fmaf(da, gkv, dbt);
-          const float r = da * bt * gkv;
-          rrow += r;
-          if (r != 0.f) atomicAdd(&rcol[s], r);
+          rv[xx] = fmaf(da * bt, gkv, rv[xx]);
           mk = da * bt * expf(ct - sc[s]);
         }
         if (s <= t) {
@@ -697,13 +714,17 @@ __global__ void __launch_bounds__(kThr, 1)
           st_shared_u16(S3 + elem_off(s, t), hb);
         }
       }
+      // row sums of r stay with the thread; column sums over the warp's rows
+      // by a shuffle exchange, then one shared add per column and warp
+#pragma unroll
+      for (int xx = 0; xx < 32; ++xx) rrow += rv[xx];
+      atomicAdd(&rcol[cb * 32 + lane], warp_colsum32(rv));
       // E G row t: rw = w . rowsum(E G . K)
+      rows_load32(f32, k + wrow + cb * 32, rs, nvw, wscr);
       tmem_ld32(tb + lane_off + 384 + cb * 32, t32);
       tmem_wait_ld_r(t32);
-      if (live) {
 #pragma unroll
-        for (int xx = 0; xx < 32; ++xx) rw = fmaf(__uint_as_float(t32[xx]), k[row + cb * 32 + xx], rw);
-      }
+      for (int xx = 0; xx < 32; ++xx) rw = fmaf(__uint_as_float(t32[xx]), f32[xx], rw);  // 0 past R
     }
     rw *= wt;
     // dO tile rows scaled by gamma for dQ; K back into S1; dV
@@ -721,8 +742,14 @@ __global__ void __launch_bounds__(kThr, 1)
         }
         st_shared_v4(ad, pack8(f8));
       }
-      if (live)
-        for (int i = 0; i < kD; ++i) dv[row + i] = bt * dUb[t * kD + i];
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        float u[32];
+        rows_load32(u, dUb + r0 * kD + cb * 32, kD, 32, wscr);
+#pragma unroll
+        for (int xx = 0; xx < 32; ++xx) u[xx] *= bt;
+        rows_store32(u, dv + wrow + cb * 32, rs, nvw, wscr);
+      }
     }
     __syncthreads();
     stage_rows(S1, k + (t0 * H + h) * kD, rs, nt, nullptr);
@@ -743,21 +770,24 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
       uint32_t t32[32];
+      float f32[32];
       tmem_ld32(tb + lane_off + 0 + cb * 32, t32);
       tmem_wait_ld_r(t32);
-      if (live)
 #pragma unroll
-        for (int xx = 0; xx < 32; ++xx) dq[row + cb * 32 + xx] = __uint_as_float(t32[xx]);
+      for (int xx = 0; xx < 32; ++xx) f32[xx] = __uint_as_float(t32[xx]);
+      rows_store32(f32, dq + wrow + cb * 32, rs, nvw, wscr);
     }
     // Q into S4, -(gamma b) dU into S5 for dK
     {
       const float f = -sgam[t] * sbt[t];
-      float f8[8];
 #pragma unroll 1
-      for (int gq = 0; gq < 16; ++gq) {
+      for (int cb = 0; cb < 4; ++cb) {
+        float u[32];
+        rows_load32(u, dUb + r0 * kD + cb * 32, kD, 32, wscr);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) f8[u] = f * dUb[t * kD + 8 * gq + u];
-        st_shared_v4(S5 + tile_off(t, gq), pack8(f8));
+        for (int xx = 0; xx < 32; ++xx) u[xx] *= f;
+#pragma unroll
+        for (int gg = 0; gg < 4; ++gg) st_shared_v4(S5 + tile_off(t, cb * 4 + gg), pack8(&u[8 * gg]));
       }
     }
     stage_rows(S4, q + (t0 * H + h) * kD, rs, nt, nullptr);
@@ -780,18 +810,25 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
       uint32_t a32[32], b32[32];
+      float f32[32];
       tmem_ld32(tb + lane_off + 256 + cb * 32, a32);
       tmem_ld32(tb + lane_off + 384 + cb * 32, b32);
       tmem_wait_ld_r(a32);
       reg_dep(b32);
-      if (live)
 #pragma unroll
-        for (int xx = 0; xx < 32; ++xx)
-          dk[row + cb * 32 + xx] = fmaf(wt, __uint_as_float(b32[xx]), __uint_as_float(a32[xx]));
+      for (int xx = 0; xx < 32; ++xx) f32[xx] = fmaf(wt, __uint_as_float(b32[xx]), __uint_as_float(a32[xx]));
+      rows_store32(f32, dk + wrow + cb * 32, rs, nvw, wscr);
     }
     // <G, S> over the block, then dc and its reverse cumulative sum
     float gs = 0.f;
-    for (int j = 0; j < kD; ++j) gs = fmaf(Gen[t * kD + j], Sst[t * kD + j], gs);
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+      float ga[32], sa[32];
+      rows_load32(ga, Gen + r0 * kD + cb * 32, kD, 32, wscr);
+      rows_load32(sa, Sst + r0 * kD + cb * 32, kD, 32, wscr);
+#pragma unroll
+      for (int xx = 0; xx < 32; ++xx) gs = fmaf(ga[xx], sa[xx], gs);
+    }
     float rws = rw;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {

@@ -71,6 +71,56 @@ __device__ __forceinline__ void mma_group(uint32_t d, uint32_t a, uint32_t b, bo
   for (int kk = 0; kk < 8; ++kk)
     mma_ss(d, kdesc(a, kk), b_mn ? mndesc(b, kk) : kdesc(b, kk), id, (acc || kk > 0) ? 1u : 0u);
 }
+// ---- thread-per-row code and coalesced global rows.  The 32 threads of a
+// warp own 32 consecutive rows; a [32 rows x 32 columns] float block moves
+// between global memory and their registers through a padded [32 x 33]
+// shared-memory scratch of the warp, so every global access is one 128-byte
+// row segment (one row per warp instruction) instead of 32 rows' scattered
+// words.  Rows at or past nvalid (relative to the block) read as 0 / are not
+// written.  base points to the block's element (0, 0); row r at base + r * stride.
+// v: 32 consecutive values of the thread's row (registers when the caller's
+// indices are compile-time constants).
+__device__ __forceinline__ void rows_load32(float* v, const float* base, int64_t stride, int nvalid,
+                                            float* scr) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll 4
+  for (int r = 0; r < 32; ++r) scr[r * 33 + lane] = r < nvalid ? base[r * stride + lane] : 0.f;
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 32; ++c) v[c] = scr[lane * 33 + c];
+  __syncwarp();
+}
+__device__ __forceinline__ void rows_store32(const float* v, float* base, int64_t stride, int nvalid,
+                                             float* scr) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) scr[lane * 33 + c] = v[c];
+  __syncwarp();
+#pragma unroll 4
+  for (int r = 0; r < 32; ++r)
+    if (r < nvalid) base[r * stride + lane] = scr[r * 33 + lane];
+  __syncwarp();
+}
+// Column sums of a [32 x 32] block held one row per lane (v[c] = column c of
+// the lane's row): after the five halving exchange rounds (31 shuffles) lane
+// l holds the sum of column l over the warp's 32 rows.  v is overwritten.
+__device__ __forceinline__ float warp_colsum32(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int c = 0; c < w; ++c) {
+      const float send = upper ? v[c] : v[c + w];
+      const float keep = upper ? v[c + w] : v[c];
+      v[c] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0];
+}
+// Words of the per-warp row scratch (32 x 33 floats per warp, four warps).
+constexpr int kRowScrFloats = 4 * 32 * 33;
+
 // fp32 [128 x 128] shared buffer, columns XOR-swizzled by the row: row
 // writes (thread = row) and column reads (thread = column) are both free of
 // bank conflicts.

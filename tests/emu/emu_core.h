@@ -205,9 +205,21 @@ inline int any_sync(int p) {
 }
 
 // ------------------------------------------------------------ mbarriers
+// An mbarrier in dynamic shared memory keeps this word in its 8 bytes for the
+// emulator's own check: a kernel store that lands on the barrier (an
+// overlapping array, say) would corrupt a real barrier's state, and here it
+// fails the next operation on it.
+constexpr uint64_t kMbarMagic = 0x6d6261725f656d75ull;
 inline Mbar& mbar_locked(Block& b, uint32_t addr) {
   for (int i = 0; i < b.n_mbars; ++i)
-    if (b.mbars[i].addr == addr) return b.mbars[i];
+    if (b.mbars[i].addr == addr) {
+      if (addr < kSmemBytes) {
+        uint64_t w;
+        std::memcpy(&w, g_smem + addr, 8);
+        if (w != kMbarMagic) die("an mbarrier in shared memory was overwritten by a store", addr);
+      }
+      return b.mbars[i];
+    }
   die("mbarrier used before mbarrier.init", addr);
 }
 inline void mbar_init(uint32_t addr, uint32_t count) {
@@ -218,6 +230,7 @@ inline void mbar_init(uint32_t addr, uint32_t count) {
   Mbar& m = b.mbars[b.n_mbars++];
   m.addr = addr, m.count = count, m.pending = (int)count, m.tx = 0;
   m.phase = 0;
+  if (addr < kSmemBytes) std::memcpy(g_smem + addr, &kMbarMagic, 8);
 }
 inline void mbar_update_locked(Mbar& m, int arrivals, int64_t tx_add) {
   m.pending -= arrivals;
