@@ -239,6 +239,26 @@ LS_API ls_status ls_replay_bwd_part(const ls_attn_desc* desc, const ls_prompt_kv
 LS_API ls_status ls_sum_parts(int32_t n_parts, int64_t n_elems, const float* parts,
                               int32_t out_dtype, void* out, void* stream);
 
+/* Staging of prompt pages kept outside HBM (the GLM path of the DeepRead
+ * summary, Method, keeps its prompt state in CPU memory and stages it per
+ * layer; on GB300 the Grace memory sits behind the coherent CPU-GPU link).
+ * Copies logical pages first_page .. first_page + n_pages - 1 of a prompt,
+ * K and V, from source pools [src_pages][Hkv][S_p][d] into staging pools
+ * [n_pages][Hkv][S_p][d], in logical order:
+ *   k_dst[i] = k_src[page_table[first_page + i]], likewise v.
+ * The GPU reads the sources directly (one kernel, no copy-engine calls), so
+ * they must be device memory or pinned host memory (pageable host memory is
+ * refused with LS_ERR_INVALID_ARGUMENT).  page_table is device memory and
+ * holds at least first_page + n_pages entries; the staging pools hold
+ * n_pages pages.  An entry outside [0, src_pages) zeroes its staging page and
+ * is reported through the status word of ws (ws may be NULL).  Pages are
+ * copied bit for bit.  0 <= n_pages <= 65535.  The interface is this
+ * library's. */
+LS_API ls_status ls_stage_pages(const ls_attn_desc* desc, const void* k_src, const void* v_src,
+                                int64_t src_pages, const int32_t* page_table, int64_t first_page,
+                                int32_t n_pages, void* k_dst, void* v_dst, void* ws,
+                                size_t ws_bytes, void* stream);
+
 /* Gated-DeltaNet state replay (the Qwen model's recurrent layers keep a
  * fixed-size state for the prompt and replay each response from it with that
  * state detached: DeepRead summary, Method, Qwen path; review sections 二,

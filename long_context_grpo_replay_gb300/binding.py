@@ -21,7 +21,8 @@ __all__ = [
     "desc_for", "prompt_from", "EXPORTED_SYMBOLS", "ls_replay_fwd_noalloc",
     "ls_replay_fwd_noalloc_scratch_bytes", "ls_prompt_prefill", "ls_prompt_prefill_workspace_size",
     "ls_replay_fwd_part", "ls_replay_bwd_part", "ls_sum_parts",
-    "GdnDesc", "LS_GDN_EXACT", "LS_GDN_TENSOR_CORE", "ls_gdn_workspace_size", "ls_gdn_replay_fwd", "ls_gdn_replay_bwd",
+    "GdnDesc", "LS_GDN_EXACT", "LS_GDN_TENSOR_CORE", "ls_gdn_workspace_size", "ls_gdn_replay_fwd",
+    "ls_gdn_replay_bwd", "ls_stage_pages",
 ]
 
 LS_DTYPE_F32 = 0
@@ -35,7 +36,7 @@ EXPORTED_SYMBOLS = [
     "ls_launch_count", "ls_uses_tensor_cores", "ls_replay_fwd_noalloc",
     "ls_replay_fwd_noalloc_scratch_bytes", "ls_prompt_prefill", "ls_prompt_prefill_workspace_size",
     "ls_replay_fwd_part", "ls_replay_bwd_part", "ls_sum_parts",
-    "ls_gdn_workspace_size", "ls_gdn_replay_fwd", "ls_gdn_replay_bwd",
+    "ls_gdn_workspace_size", "ls_gdn_replay_fwd", "ls_gdn_replay_bwd", "ls_stage_pages",
 ]
 
 
@@ -119,6 +120,7 @@ def lib() -> ctypes.CDLL:
         "ls_gdn_replay_fwd": [ctypes.POINTER(GdnDesc), P, P, P, P, P, P, I32, P, P, P],
         "ls_gdn_replay_bwd": [ctypes.POINTER(GdnDesc), P, P, P, P, P, P, P, I32, P, P, P, P, P, P,
                               SZ, P],
+        "ls_stage_pages": [ctypes.POINTER(AttnDesc), P, P, I64, P, I64, I32, P, P, P, SZ, P],
         "ls_read_device_status": [P, SZ, P],
         "ls_clear_device_status": [P, SZ, P],
         "ls_trace_enable": [I32],
@@ -317,6 +319,17 @@ def ls_gdn_replay_bwd(s0, q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta, ws, stre
                                    _ptr(v), _ptr(g), _ptr(beta), _ptr(d_o), _resp_len(q), _ptr(dq), _ptr(dk),
                                    _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(ws), _nbytes(ws),
                                    _stream(stream)))
+
+
+def ls_stage_pages(desc, k_src, v_src, page_table, first_page, n_pages, k_dst, v_dst, ws=None,
+                   stream=None):
+    """Logical pages first_page .. first_page+n_pages-1 (slots from the
+    device page_table) of pinned-host or device pools into staging pools;
+    see ls.h."""
+    _want_dtype(desc, k_src, v_src, k_dst, v_dst)
+    _check(lib().ls_stage_pages(ctypes.byref(desc), _ptr(k_src), _ptr(v_src), k_src.shape[0],
+                                _ptr(page_table), first_page, n_pages, _ptr(k_dst), _ptr(v_dst),
+                                _ptr(ws), 0 if ws is None else _nbytes(ws), _stream(stream)))
 
 
 def ls_replay_fwd_noalloc(desc, prompt, q, k_resp, v_resp, o, lse, stream=None):

@@ -63,7 +63,7 @@ cudaEvent_t take_event() {
 const char* kKernelNames[kNumKernelIds] = {
     "page_write",  "simt_fwd",   "tc_fwd",     "lse_merge", "bwd_preprocess",
     "simt_bwd_dq", "tc_bwd_dq",  "simt_dkdv",  "tc_dkdv",   "dq_reduce",
-    "gdn_fwd",     "gdn_bwd"};
+    "gdn_fwd",     "gdn_bwd",    "stage_pages"};
 
 // ------------------------------------------------------------------ devices
 int device_sms() {
@@ -653,6 +653,58 @@ ls_status ls_gdn_replay_bwd(const ls_gdn_desc* desc, const float* s0, const floa
     LS_CUDA(launch_gdn_bwd(desc->batch, desc->heads, resp_len, s0, q, k, v, g, beta, d_o, dq, dk,
                            dv, dg, dbeta, scratch, static_cast<cudaStream_t>(stream)),
             "GDN backward launch");
+  return LS_OK;
+}
+
+namespace {
+// A device-readable address for p: device or managed memory as is, pinned
+// host memory through its device mapping; NULL for memory the GPU cannot
+// read (pageable host memory), which is refused before any launch.
+const void* device_readable(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+    return nullptr;
+  }
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged: return p;
+    case cudaMemoryTypeHost: return a.devicePointer;
+    default: return nullptr;
+  }
+}
+}  // namespace
+
+ls_status ls_stage_pages(const ls_attn_desc* desc, const void* k_src, const void* v_src,
+                         int64_t src_pages, const int32_t* page_table, int64_t first_page,
+                         int32_t n_pages, void* k_dst, void* v_dst, void* ws, size_t ws_bytes,
+                         void* stream) {
+  LS_CHECK(check_desc(desc));
+  if (n_pages < 0 || n_pages > 65535 || first_page < 0 || src_pages < 1)
+    return fail(LS_ERR_INVALID_ARGUMENT,
+                "need 0 <= n_pages <= 65535, first_page >= 0 and src_pages >= 1");
+  if (n_pages == 0) return LS_OK;
+  if (!k_src || !v_src || !page_table || !k_dst || !v_dst)
+    return fail(LS_ERR_INVALID_ARGUMENT, "pools, page table and staging buffers must be non-NULL");
+  if (!aligned(k_src, 16) || !aligned(v_src, 16) || !aligned(k_dst, 16) || !aligned(v_dst, 16) ||
+      !aligned(page_table, 4))
+    return fail(LS_ERR_INVALID_ARGUMENT, "pools and staging buffers must be 16-byte aligned");
+  const void* ks = device_readable(k_src);
+  const void* vs = device_readable(v_src);
+  if (!ks || !vs)
+    return fail(LS_ERR_INVALID_ARGUMENT,
+                "source pools must be device memory or pinned host memory (the GPU cannot read "
+                "pageable host memory)");
+  uint32_t* status = nullptr;
+  if (ws) {
+    LS_CHECK(check_ws(ws, ws_bytes, kWsHeader));
+    status = reinterpret_cast<uint32_t*>(ws);
+  }
+  const int64_t page_bytes = (int64_t)desc->hkv * desc->page_size * desc->head_dim *
+                             (desc->dtype == LS_DTYPE_F32 ? 4 : 2);
+  LS_CUDA(launch_stage_pages(page_bytes, ks, vs, src_pages, page_table, first_page, n_pages, k_dst,
+                             v_dst, status, static_cast<cudaStream_t>(stream)),
+          "page staging launch");
   return LS_OK;
 }
 

@@ -40,6 +40,7 @@ enum KernelId : int32_t {
   kKDqReduce,
   kKGdnFwd,
   kKGdnBwd,
+  kKStagePages,
   kNumKernelIds
 };
 
@@ -112,6 +113,10 @@ cudaError_t launch_page_write(int dtype, int hkv, int d, int page_size, void* k_
                               const void* v, uint32_t* status, cudaStream_t s);
 cudaError_t launch_simt_fwd(int dtype, const FwdParams& p, cudaStream_t s);
 cudaError_t launch_simt_fwd_resp(int dtype, const FwdParams& p, cudaStream_t s);
+// Whole pages of a device-readable source pool into a staging pool (ls_stage_pages).
+cudaError_t launch_stage_pages(int64_t page_bytes, const void* k_src, const void* v_src,
+                               int64_t src_pages, const int32_t* pt, int64_t first, int n_pages,
+                               void* k_dst, void* v_dst, uint32_t* status, cudaStream_t s);
 cudaError_t launch_lse_merge(int n_parts, int64_t n_rows, int d, const float* o_parts,
                              const float* lse_parts, int out_dtype, void* o, float* lse,
                              cudaStream_t s);

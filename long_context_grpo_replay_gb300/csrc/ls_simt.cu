@@ -65,6 +65,38 @@ __global__ void __launch_bounds__(256) page_write_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// Staging of whole pages from a (host-resident, device-mapped) pool into a
+// compact staging pool: dst page i <- src page page_table[first + i], K for
+// blockIdx.z == 0 and V for 1.  Each thread keeps four 16-byte loads in
+// flight, since the source sits behind the CPU-GPU link with microseconds of
+// latency.  A page id outside the source pool zeroes the destination page and
+// sets the status word.
+__global__ void __launch_bounds__(256) stage_pages_kernel(
+    int64_t page_bytes, const char* __restrict__ k_src, const char* __restrict__ v_src,
+    int64_t src_pages, const int32_t* __restrict__ pt, int64_t first, char* __restrict__ k_dst,
+    char* __restrict__ v_dst, uint32_t* status) {
+  const int64_t i = blockIdx.y;
+  const int32_t slot = __ldg(pt + first + i);
+  const bool ok = slot >= 0 && slot < src_pages;
+  if (!ok && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0 && status)
+    atomicOr(status, kStatusBadPage);
+  const uint4* src = reinterpret_cast<const uint4*>((blockIdx.z ? v_src : k_src) +
+                                                    (ok ? (int64_t)slot : 0) * page_bytes);
+  uint4* dst = reinterpret_cast<uint4*>((blockIdx.z ? v_dst : k_dst) + i * page_bytes);
+  const int64_t n16 = page_bytes >> 4;
+  const int64_t step = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < n16; c += 4 * step) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      v[u] = (ok && c + u * step < n16) ? __ldcs(src + c + u * step) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (c + u * step < n16) __stcs(dst + c + u * step, v[u]);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // A4 exact LSE merge: one thread per (row, 4 columns).
 // ---------------------------------------------------------------------------
 template <typename TO>
@@ -504,6 +536,20 @@ cudaError_t launch_page_write(int dtype, int hkv, int d, int page_size, void* k_
                                          reinterpret_cast<char*>(v_pool), pool_pages, pt,
                                          start_pos, n_tok, reinterpret_cast<const char*>(k),
                                          reinterpret_cast<const char*>(v), status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stage_pages(int64_t page_bytes, const void* k_src, const void* v_src,
+                               int64_t src_pages, const int32_t* pt, int64_t first, int n_pages,
+                               void* k_dst, void* v_dst, uint32_t* status, cudaStream_t s) {
+  if (n_pages == 0) return cudaSuccess;
+  const int64_t n16 = page_bytes >> 4;
+  int64_t bx = (n16 + 4 * 256 - 1) / (4 * 256);
+  if (bx > 32) bx = 32;
+  LaunchScope ls(kKStagePages, s);
+  stage_pages_kernel<<<dim3((unsigned)bx, (unsigned)n_pages, 2), 256, 0, s>>>(
+      page_bytes, reinterpret_cast<const char*>(k_src), reinterpret_cast<const char*>(v_src),
+      src_pages, pt, first, reinterpret_cast<char*>(k_dst), reinterpret_cast<char*>(v_dst), status);
   return cudaGetLastError();
 }
 

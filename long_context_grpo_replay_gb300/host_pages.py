@@ -6,7 +6,9 @@ applied to the KV pages of the full-attention replay.  Pages live in pinned
 host memory (on GB300 the Grace memory, reached over NVLink-C2C).  For each
 pass the prompt is cut into chunks of whole logical pages.  Each chunk is
 copied into one of two device staging pools on a copy stream while the
-previous chunk computes.
+previous chunk computes; the copy is one library kernel per chunk
+(ls_stage_pages) that reads the pinned pages directly over the CPU-GPU link
+through a device copy of the page table.
 
 Every chunk is an exact share of the keys, so the result is exact:
 
@@ -17,8 +19,8 @@ Every chunk is an exact share of the keys, so the result is exact:
              first chunk.
 
 Device memory holds two chunks of pages plus one float32 partial per chunk,
-however long the prompt.  The page copies are plain transfers and every
-arithmetic step runs in the library.
+however long the prompt.  Every step, the page copies included, runs in the
+library.
 """
 from __future__ import annotations
 
@@ -66,6 +68,7 @@ class HostPagedReplay:
         self.kst = [torch.empty(shape, dtype=k_pool_host.dtype, device=device) for _ in range(2)]
         self.vst = [torch.empty(shape, dtype=v_pool_host.dtype, device=device) for _ in range(2)]
         self.local_pt = torch.arange(chunk_pages, dtype=torch.int32, device=device)
+        self.pt_dev = self.pt.to(torch.int32).to(device)  # logical page -> host pool slot
         self.copy_stream = torch.cuda.Stream(device)
         self.device = device
 
@@ -84,7 +87,7 @@ class HostPagedReplay:
         return max(ls.ls_replay_workspace_size(self.desc, self._prompt(0, c0, c1), max_resp_len)
                    for c0, c1 in {self.chunks[0], self.chunks[-1]})
 
-    def _stream_chunks(self, run_chunk):
+    def _stream_chunks(self, run_chunk, ws):
         """Stage every chunk (double-buffered) and call run_chunk(i, prompt)."""
         stream = torch.cuda.current_stream(self.device)
         if not self.chunks:
@@ -99,11 +102,8 @@ class HostPagedReplay:
             b = i & 1
             c0, c1 = self.chunks[i]
             self.copy_stream.wait_event(free[b])
-            with torch.cuda.stream(self.copy_stream):
-                for j, p in enumerate(range(c0, c1)):
-                    slot = int(self.pt[p])
-                    self.kst[b][j].copy_(self.kh[slot], non_blocking=True)
-                    self.vst[b][j].copy_(self.vh[slot], non_blocking=True)
+            ls.ls_stage_pages(self.desc, self.kh, self.vh, self.pt_dev, c0, c1 - c0, self.kst[b],
+                              self.vst[b], ws, self.copy_stream)
             copied[b].record(self.copy_stream)
 
         stage(0)
@@ -124,7 +124,7 @@ class HostPagedReplay:
         def run(i, prompt):
             ls.ls_replay_fwd_part(self.desc, prompt, q, k, v, i == 0, parts_o[i], parts_l[i], ws)
 
-        self._stream_chunks(run)
+        self._stream_chunks(run, ws)
         ls.ls_lse_merge(parts_o.view(n, R * hq, d), parts_l.view(n, R * hq), o, lse)
 
     def backward(self, q, k, v, d_o, o, lse, dq, dk, dv, ws):
@@ -140,5 +140,5 @@ class HostPagedReplay:
             ls.ls_replay_bwd_part(self.desc, prompt, q, k, v, d_o, lse, delta, first, dq_parts[i],
                                   dk if first else None, dv if first else None, ws)
 
-        self._stream_chunks(run)
+        self._stream_chunks(run, ws)
         ls.ls_sum_parts(dq_parts, dq)

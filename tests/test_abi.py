@@ -222,3 +222,21 @@ def test_noalloc_forward_validates_before_touching_the_device(ls):
     big = ls.PromptKV(1 << 24, 1 << 24, 8192, 1 << 24, 8192, 2097152)
     assert L.ls_replay_fwd_noalloc(ctypes.byref(d), ctypes.byref(big), A, A, A, 8192, A, A, None) == 3
     assert "64 MiB" in ls.ls_last_error()
+
+
+def test_stage_pages_validates_before_any_launch(ls):
+    """ls_stage_pages refuses NULL buffers, bad counts and memory the GPU
+    cannot read (pageable host memory) with a status, launching nothing."""
+    import numpy as np
+
+    L = ls.lib()
+    d = _desc(ls)
+    A = ctypes.c_void_p(1 << 24)
+    assert L.ls_stage_pages(ctypes.byref(d), A, A, 8, A, 0, 0, A, A, None, 0, None) == 0  # no-op
+    assert L.ls_stage_pages(ctypes.byref(d), None, A, 8, A, 0, 4, A, A, None, 0, None) == 1
+    assert L.ls_stage_pages(ctypes.byref(d), A, A, 8, A, 0, 70000, A, A, None, 0, None) == 1
+    assert L.ls_stage_pages(ctypes.byref(d), A, A, 8, A, -1, 4, A, A, None, 0, None) == 1
+    buf = np.zeros(1 << 16, dtype=np.uint8)  # pageable host memory
+    p = ctypes.c_void_p((buf.ctypes.data + 15) // 16 * 16)
+    assert L.ls_stage_pages(ctypes.byref(d), p, p, 8, A, 0, 4, A, A, None, 0, None) == 1
+    assert "pinned" in ls.ls_last_error()

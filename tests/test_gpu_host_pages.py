@@ -64,3 +64,42 @@ def test_sum_parts(cuda_device):
     outb = torch.empty(1000, 4, device=cuda_device, dtype=torch.bfloat16)
     ls.ls_sum_parts(parts, outb)
     assert float((outb.double() - want).abs().max() / want.abs().max()) <= 1e-2
+
+
+@pytest.mark.parametrize("where", ["pinned_host", "device"])
+def test_stage_pages_is_a_bit_exact_gather(cuda_device, where):
+    """ls_stage_pages copies logical pages first..first+n-1 of a scattered pool
+    into a compact staging pool in logical order, bit for bit, reading pinned
+    host memory directly; an entry outside the pool zeroes its staging page
+    and sets the status word."""
+    w = inputs.Workload("stage", 24, 4, 256, 256, 256 * 40, (1,), "bf16", seed=9, pool_factor=2,
+                        poison=True)
+    pr = inputs.make_prompt(w, "cpu")
+    desc = ls.desc_for(w.hq, w.hkv, w.head_dim, w.page_size, torch.bfloat16, w.scale)
+    if where == "pinned_host":
+        kp, vp = pr["k_pool"].pin_memory(), pr["v_pool"].pin_memory()
+    else:
+        kp, vp = pr["k_pool"].to(cuda_device), pr["v_pool"].to(cuda_device)
+    pt = pr["page_table"].to(torch.int32)
+    pt_dev = pt.to(cuda_device)
+    first, n = 7, 20
+    kd = torch.full((n,) + tuple(kp.shape[1:]), float("nan"), dtype=torch.bfloat16, device=cuda_device)
+    vd = kd.clone()
+    ws = torch.zeros(256, dtype=torch.uint8, device=cuda_device)
+    ls.ls_stage_pages(desc, kp, vp, pt_dev, first, n, kd, vd, ws)
+    torch.cuda.synchronize()
+    ls.ls_read_device_status(ws)
+    sel = pt[first:first + n].long()
+    want_k = pr["k_pool"][sel]
+    want_v = pr["v_pool"][sel]
+    assert torch.equal(kd.cpu().view(torch.int16), want_k.view(torch.int16))
+    assert torch.equal(vd.cpu().view(torch.int16), want_v.view(torch.int16))
+    # an out-of-pool entry: that staging page is zeroed and reported
+    bad = pt.clone()
+    bad[first + 3] = kp.shape[0] + 11
+    ls.ls_stage_pages(desc, kp, vp, bad.to(cuda_device), first, n, kd, vd, ws)
+    with pytest.raises(ls.LsError) as ei:
+        ls.ls_read_device_status(ws)
+    assert ei.value.status == 5
+    assert not (kd[3].view(torch.int16) != 0).any() and not (vd[3].view(torch.int16) != 0).any()
+    assert torch.equal(kd[4].cpu().view(torch.int16), want_k[4].view(torch.int16))
