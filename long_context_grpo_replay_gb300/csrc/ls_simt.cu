@@ -66,33 +66,45 @@ __global__ void __launch_bounds__(256) page_write_kernel(
 
 // ---------------------------------------------------------------------------
 // Staging of whole pages from a (host-resident, device-mapped) pool into a
-// compact staging pool: dst page i <- src page page_table[first + i], K for
-// blockIdx.z == 0 and V for 1.  Each thread keeps four 16-byte loads in
-// flight, since the source sits behind the CPU-GPU link with microseconds of
-// latency.  A page id outside the source pool zeroes the destination page and
-// sets the status word.
+// compact staging pool: dst page i <- src page page_table[first + i], K and
+// V.  A small grid (two blocks per SM) walks all 16-byte pieces of the chunk
+// with a grid-stride loop, each thread keeping four loads in flight: enough
+// bytes in flight for the microseconds of latency of the CPU-GPU link, while
+// leaving the SMs' thread slots to the replay kernels that run beside it on
+// another stream.  A page id outside the source pool zeroes the destination
+// page and sets the status word.
 __global__ void __launch_bounds__(256) stage_pages_kernel(
     int64_t page_bytes, const char* __restrict__ k_src, const char* __restrict__ v_src,
-    int64_t src_pages, const int32_t* __restrict__ pt, int64_t first, char* __restrict__ k_dst,
-    char* __restrict__ v_dst, uint32_t* status) {
-  const int64_t i = blockIdx.y;
-  const int32_t slot = __ldg(pt + first + i);
-  const bool ok = slot >= 0 && slot < src_pages;
-  if (!ok && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0 && status)
-    atomicOr(status, kStatusBadPage);
-  const uint4* src = reinterpret_cast<const uint4*>((blockIdx.z ? v_src : k_src) +
-                                                    (ok ? (int64_t)slot : 0) * page_bytes);
-  uint4* dst = reinterpret_cast<uint4*>((blockIdx.z ? v_dst : k_dst) + i * page_bytes);
-  const int64_t n16 = page_bytes >> 4;
+    int64_t src_pages, const int32_t* __restrict__ pt, int64_t first, int n_pages,
+    char* __restrict__ k_dst, char* __restrict__ v_dst, uint32_t* status) {
+  const int64_t n16 = page_bytes >> 4;       // pieces per page
+  const int64_t total = 2 * n_pages * n16;   // K pages, then V pages
   const int64_t step = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < n16; c += 4 * step) {
+  for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < total; c += 4 * step) {
     uint4 v[4];
+    int64_t dsti[4];
+    char* dstb[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t g = c + u * step;
+      dstb[u] = nullptr;
+      v[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (g < total) {
+        const bool isv = g >= n_pages * n16;
+        const int64_t gg = isv ? g - n_pages * n16 : g;
+        const int64_t i = gg / n16, piece = gg - i * n16;
+        const int32_t slot = __ldg(pt + first + i);
+        const bool ok = slot >= 0 && slot < src_pages;
+        if (!ok && piece == 0 && !isv && status) atomicOr(status, kStatusBadPage);
+        if (ok)
+          v[u] = __ldcs(reinterpret_cast<const uint4*>((isv ? v_src : k_src) + (int64_t)slot * page_bytes) + piece);
+        dstb[u] = isv ? v_dst : k_dst;
+        dsti[u] = gg;
+      }
+    }
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-      v[u] = (ok && c + u * step < n16) ? __ldcs(src + c + u * step) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (c + u * step < n16) __stcs(dst + c + u * step, v[u]);
+      if (dstb[u]) __stcs(reinterpret_cast<uint4*>(dstb[u]) + dsti[u], v[u]);
   }
 }
 
@@ -543,13 +555,17 @@ cudaError_t launch_stage_pages(int64_t page_bytes, const void* k_src, const void
                                int64_t src_pages, const int32_t* pt, int64_t first, int n_pages,
                                void* k_dst, void* v_dst, uint32_t* status, cudaStream_t s) {
   if (n_pages == 0) return cudaSuccess;
-  const int64_t n16 = page_bytes >> 4;
-  int64_t bx = (n16 + 4 * 256 - 1) / (4 * 256);
-  if (bx > 32) bx = 32;
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t pieces = 2 * (int64_t)n_pages * (page_bytes >> 4);
+  const int64_t want = (pieces + 4 * 256 - 1) / (4 * 256);
+  const unsigned grid = (unsigned)(want < 2 * (int64_t)sms ? want : 2 * (int64_t)sms);
   LaunchScope ls(kKStagePages, s);
-  stage_pages_kernel<<<dim3((unsigned)bx, (unsigned)n_pages, 2), 256, 0, s>>>(
-      page_bytes, reinterpret_cast<const char*>(k_src), reinterpret_cast<const char*>(v_src),
-      src_pages, pt, first, reinterpret_cast<char*>(k_dst), reinterpret_cast<char*>(v_dst), status);
+  stage_pages_kernel<<<grid, 256, 0, s>>>(page_bytes, reinterpret_cast<const char*>(k_src),
+                                          reinterpret_cast<const char*>(v_src), src_pages, pt, first,
+                                          n_pages, reinterpret_cast<char*>(k_dst),
+                                          reinterpret_cast<char*>(v_dst), status);
   return cudaGetLastError();
 }
 
