@@ -71,6 +71,11 @@ class HostPagedReplay:
         self.pt_dev = self.pt.to(torch.int32).to(device)  # logical page -> host pool slot
         self.copy_stream = torch.cuda.Stream(device)
         self.device = device
+        # passes alternate their chunk order, so that each pass starts on the
+        # chunk the previous one left in a staging pool and never waits for
+        # its first copy; held[b] is the chunk staging pool b holds
+        self.reverse = False
+        self.held = [None, None]
 
     def n_chunks(self) -> int:
         return max(1, len(self.chunks))
@@ -88,31 +93,43 @@ class HostPagedReplay:
                    for c0, c1 in {self.chunks[0], self.chunks[-1]})
 
     def _stream_chunks(self, run_chunk, ws):
-        """Stage every chunk (double-buffered) and call run_chunk(i, prompt)."""
+        """Stage every chunk (double-buffered) and call run_chunk(chunk index,
+        prompt) for each; the order alternates between passes (see __init__)."""
         stream = torch.cuda.current_stream(self.device)
         if not self.chunks:
             run_chunk(0, ls.prompt_from(None, None, None, 0))
             return
+        n = len(self.chunks)
+        order = list(range(n - 1, -1, -1)) if self.reverse else list(range(n))
+        self.reverse = not self.reverse
+        b0 = self.held.index(order[0]) if order[0] in self.held else 0
+        bufs = [b0 ^ (i & 1) for i in range(n)]
         copied = [torch.cuda.Event(), torch.cuda.Event()]
         free = [torch.cuda.Event(), torch.cuda.Event()]
         for e in free:
             e.record(stream)
+        need_copy = [True] * n
+        need_copy[0] = self.held[b0] != order[0]
 
         def stage(i):
-            b = i & 1
-            c0, c1 = self.chunks[i]
+            b, ci = bufs[i], order[i]
+            c0, c1 = self.chunks[ci]
             self.copy_stream.wait_event(free[b])
             ls.ls_stage_pages(self.desc, self.kh, self.vh, self.pt_dev, c0, c1 - c0, self.kst[b],
                               self.vst[b], ws, self.copy_stream)
             copied[b].record(self.copy_stream)
+            self.held[b] = ci
 
-        stage(0)
-        for i, (c0, c1) in enumerate(self.chunks):
-            b = i & 1
-            if i + 1 < len(self.chunks):
+        if need_copy[0]:
+            stage(0)
+        for i in range(n):
+            b, ci = bufs[i], order[i]
+            if i + 1 < n:
                 stage(i + 1)
-            stream.wait_event(copied[b])
-            run_chunk(i, self._prompt(b, c0, c1))
+            if need_copy[i]:
+                stream.wait_event(copied[b])
+            c0, c1 = self.chunks[ci]
+            run_chunk(ci, self._prompt(b, c0, c1))
             free[b].record(stream)
 
     def forward(self, q, k, v, o, lse, ws):
