@@ -39,10 +39,15 @@ __device__ __forceinline__ float* scratch_of(float* scr, int H, int nch, int m, 
 }
 
 // Cumulative log-decay and write strength of the chunk's tokens into sc[],
-// sbt[] (zero past the response); swt[4] is scan scratch.  All threads.
+// sbt[] (zero past the response); swt[4] is scan scratch.  Called by all
+// threads of the block; threads past the chunk's 128 only meet the barrier.
 __device__ __forceinline__ void stage_gates(const float* g, const float* beta, int64_t t0, int nt,
                                             int H, int h, float* sc, float* sbt, float* swt) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid >= kThr) {
+    __syncthreads();
+    return;
+  }
   float x = 0.f;
   if (tid < nt) {
     x = g[(t0 + tid) * H + h];
@@ -106,12 +111,16 @@ __device__ __forceinline__ void solve_upper(float* buf, const float* gk, const f
 }
 
 // ---------------------------------------------------------------- prep
-// One CTA per (chunk, head, member).
+// One CTA per (chunk, head, member), 256 threads: the first 128 own the
+// chunk's rows and columns (tensor-memory lanes, one column each in the
+// solves); the second 128 run the second of each pair of independent
+// triangular solves beside the first (E0 with ZK, dU0 with ZW).
 constexpr uint32_t kPrepK = 0, kPrepQ = kTile, kPrepDO = 2 * kTile, kPrepGK = 3 * kTile;
 constexpr uint32_t kPrepU = 4 * kTile, kPrepMisc = 6 * kTile;
 constexpr uint32_t kPrepSmem = kPrepMisc + 2048 + 1024;
+constexpr int kPrepThr = 2 * kThr;
 
-__global__ void __launch_bounds__(kThr, 1)
+__global__ void __launch_bounds__(kPrepThr, 1)
     gdn_cp_prep_kernel(int H, int R, int nch, const float* __restrict__ q,
                        const float* __restrict__ k, const float* __restrict__ v,
                        const float* __restrict__ g, const float* __restrict__ beta,
@@ -123,6 +132,8 @@ __global__ void __launch_bounds__(kThr, 1)
   const uint32_t sb = smem_u32(sm);
   float* gk = reinterpret_cast<float*>(sm + kPrepGK);
   float* buf = reinterpret_cast<float*>(sm + kPrepU);
+  // the second solve's buffer: the K and Q tiles, once the MMAs have read them
+  float* buf2 = reinterpret_cast<float*>(sm + kPrepK);
   float* sc = reinterpret_cast<float*>(sm + kPrepMisc);
   float* sbt = sc + kC;
   float* swt = sbt + kC;
@@ -154,9 +165,11 @@ __global__ void __launch_bounds__(kThr, 1)
   const volatile uint32_t* abortp = abort_s;
   const int64_t rs = (int64_t)H * kD;  // token stride of q, k, v, d_o
 
-  stage_rows(sb + kPrepK, k + (t0 * H + h) * kD, rs, nt, nullptr);
-  stage_rows(sb + kPrepQ, q + (t0 * H + h) * kD, rs, nt, nullptr);
-  stage_rows(sb + kPrepDO, d_o + (t0 * H + h) * kD, rs, nt, nullptr);
+  if (tid < kThr) {
+    stage_rows(sb + kPrepK, k + (t0 * H + h) * kD, rs, nt, nullptr);
+    stage_rows(sb + kPrepQ, q + (t0 * H + h) * kD, rs, nt, nullptr);
+    stage_rows(sb + kPrepDO, d_o + (t0 * H + h) * kD, rs, nt, nullptr);
+  }
   stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
   fence_proxy_async_smem();
   __syncthreads();
@@ -172,10 +185,10 @@ __global__ void __launch_bounds__(kThr, 1)
     tc_fence_after();
     // thread r: GK row r (s < r); P^T row r: P^T[r][t] = [t >= r] Gamma_tr (K_r . Q_t)
     const int r = tid;
-    const float cr = sc[r];
+    const float cr = tid < kThr ? sc[r] : 0.f;
     float* gko = out + (int64_t)kGKblk * kTileElems;
 #pragma unroll 1
-    for (int cb = 0; cb < 4; ++cb) {
+    for (int cb = 0; tid < kThr && cb < 4; ++cb) {
       uint32_t t32[32];
       tmem_ld32(tb + lane_off + 0 + cb * 32, t32);
       tmem_wait_ld_r(t32);
@@ -207,41 +220,47 @@ __global__ void __launch_bounds__(kThr, 1)
       mma_group(tb + 256, sb + kPrepQ, sb + kPrepDO, true, false);
       mma_commit(smem_u32(&bars[1]));
     }
-    // forward solves, thread x = column x: E0 from b V, ZK from b gamma K
-    const int x = tid;
-    for (int which = 0; which < 2; ++which) {
-      const float* src = which == 0 ? v : k;
-      for (int t = 0; t < kC; ++t) {
-        float val = 0.f;
-        if (t < nt) val = sbt[t] * src[(t0 + t) * rs + h * kD + x] * (which == 0 ? 1.f : expf(sc[t]));
-        buf[u_at(t, x)] = val;
-      }
-      solve_lower(buf, gk, sbt, nt8, x);
-      float* dst = out + (int64_t)(which == 0 ? kE0 : kZK) * kTileElems;
-      for (int t = 0; t < kC; ++t) dst[t * kD + x] = buf[u_at(t, x)];
-    }
+    // the second solve of each pair writes over the K and Q tiles: the
+    // P^T dO product must have read them first
     ok = mbar_wait_warp(smem_u32(&bars[1]), 0, abortp);
     if (!__syncthreads_or(!ok)) {
       tc_fence_after();
-      // backward solves: dU0 from dE0 (rows from tensor memory), ZW from w K
-#pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t t32[32];
-        tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
-        tmem_wait_ld_r(t32);
-#pragma unroll
-        for (int xx = 0; xx < 32; ++xx) buf[u_at(r, cb * 32 + xx)] = __uint_as_float(t32[xx]);
+      // forward solves, thread x = column x: E0 from b V (first 128 threads),
+      // ZK from b gamma K (second 128), side by side
+      const int x = tid & (kThr - 1), which = tid / kThr;
+      float* bw = which == 0 ? buf : buf2;
+      {
+        const float* src = which == 0 ? v : k;
+        for (int t = 0; t < kC; ++t) {
+          float val = 0.f;
+          if (t < nt) val = sbt[t] * src[(t0 + t) * rs + h * kD + x] * (which == 0 ? 1.f : expf(sc[t]));
+          bw[u_at(t, x)] = val;
+        }
+        solve_lower(bw, gk, sbt, nt8, x);
+        float* dst = out + (int64_t)(which == 0 ? kE0 : kZK) * kTileElems;
+        for (int t = 0; t < kC; ++t) dst[t * kD + x] = bw[u_at(t, x)];
       }
       __syncthreads();
-      solve_upper(buf, gk, sbt, nt8, x);
-      float* dst = out + (int64_t)kDU0 * kTileElems;
-      for (int t = 0; t < kC; ++t) dst[t * kD + x] = buf[u_at(t, x)];
-      const float clast = sc[kC - 1];
-      for (int t = 0; t < kC; ++t)
-        buf[u_at(t, x)] = t < nt ? expf(clast - sc[t]) * k[(t0 + t) * rs + h * kD + x] : 0.f;
-      solve_upper(buf, gk, sbt, nt8, x);
-      dst = out + (int64_t)kZW * kTileElems;
-      for (int t = 0; t < kC; ++t) dst[t * kD + x] = buf[u_at(t, x)];
+      // backward solves: dU0 from dE0 (rows from tensor memory, first 128
+      // threads), ZW from w K (second 128), side by side
+      if (which == 0) {
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+          uint32_t t32[32];
+          tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
+          tmem_wait_ld_r(t32);
+#pragma unroll
+          for (int xx = 0; xx < 32; ++xx) buf[u_at(r, cb * 32 + xx)] = __uint_as_float(t32[xx]);
+        }
+      } else {
+        const float clast = sc[kC - 1];
+        for (int t = 0; t < kC; ++t)
+          buf2[u_at(t, x)] = t < nt ? expf(clast - sc[t]) * k[(t0 + t) * rs + h * kD + x] : 0.f;
+      }
+      __syncthreads();
+      solve_upper(bw, gk, sbt, nt8, x);
+      float* dst = out + (int64_t)(which == 0 ? kDU0 : kZW) * kTileElems;
+      for (int t = 0; t < kC; ++t) dst[t * kD + x] = bw[u_at(t, x)];
     }
   }
   if (__syncthreads_or(!ok) && tid == 0 && status) atomicOr(status, kStatusTimeout);
@@ -901,7 +920,7 @@ cudaError_t launch_gdn_cp_bwd(int B, int H, int R, const float* s0, const float*
                                 kOutSmem)) != cudaSuccess)
     return e;
   LaunchScope ls(kKGdnBwd, st);
-  gdn_cp_prep_kernel<<<dim3(nch, H, B), kThr, kPrepSmem, st>>>(H, R, nch, q, k, v, g, beta, d_o, ws,
+  gdn_cp_prep_kernel<<<dim3(nch, H, B), kPrepThr, kPrepSmem, st>>>(H, R, nch, q, k, v, g, beta, d_o, ws,
                                                               status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gdn_cp_chain_kernel<<<dim3(H, B), kThr, kChainSmem, st>>>(H, R, nch, s0, q, k, g, beta, d_o, ws,
