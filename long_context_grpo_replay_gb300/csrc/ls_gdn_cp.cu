@@ -282,8 +282,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
 // end, E and dU into the scratch.
 constexpr uint32_t kChT0 = 0, kChT1 = kTile, kChT2 = 2 * kTile, kChT3 = 3 * kTile;
 constexpr uint32_t kChT4 = 4 * kTile, kChT5 = 5 * kTile, kChMisc = 6 * kTile;
-constexpr uint32_t kChRowScr = kChMisc + 2048;  // per-warp row scratch (rows_load32 / rows_store32)
-constexpr uint32_t kChainSmem = kChRowScr + kRowScrFloats * 4 + 1024;
+constexpr uint32_t kChainSmem = kChMisc + 2048 + 1024;
 
 __global__ void __launch_bounds__(kThr, 1)
     gdn_cp_chain_kernel(int H, int R, int nch, const float* __restrict__ s0,
@@ -305,8 +304,6 @@ __global__ void __launch_bounds__(kThr, 1)
   uint32_t* abort_s = tslot + 1;
 
   const int h = blockIdx.x, m = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
-  float* wscr = reinterpret_cast<float*>(sm + kChRowScr) + warp * 32 * 33;
-  const int r0 = warp * 32;  // first row of this warp's 32 (rows of S, G, E, dU)
   {
     const int64_t tok = (int64_t)m * R * H;
     q += tok * kD, k += tok * kD, d_o += tok * kD, g += tok, beta += tok;
@@ -342,9 +339,11 @@ __global__ void __launch_bounds__(kThr, 1)
     const int nt = R - t0 < kC ? (int)(R - t0) : kC;
     float* blk = scratch_of(scr, H, nch, m, h, ch);
     {
-      float* dst = blk + (int64_t)kSstart * kTileElems + r0 * kD;
+      // each thread's own row: the stores are not waited on, and this
+      // sequential kernel runs faster with them than with a staged transpose
+      float* dst = blk + (int64_t)kSstart * kTileElems + x * kD;
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) rows_store32(st + cb * 32, dst + cb * 32, kD, 32, wscr);
+      for (int c = 0; c < kD; ++c) dst[c] = st[c];
     }
     stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
     __syncthreads();
@@ -364,22 +363,20 @@ __global__ void __launch_bounds__(kThr, 1)
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
     {  // E row x = E0 row x - (ZK S^T) row x; E^T column x as bf16
-      const float* e0 = blk + (int64_t)kE0 * kTileElems + r0 * kD;
-      float* eo = blk + (int64_t)kEblk * kTileElems + r0 * kD;
+      const float* e0 = blk + (int64_t)kE0 * kTileElems + x * kD;
+      float* eo = blk + (int64_t)kEblk * kTileElems + x * kD;
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t t32[32];
-        float ev[32];
-        rows_load32(ev, e0 + cb * 32, kD, 32, wscr);
         tmem_ld32(tb + lane_off + cb * 32, t32);
         tmem_wait_ld_r(t32);
 #pragma unroll
         for (int xx = 0; xx < 32; ++xx) {
           const int i = cb * 32 + xx;
-          ev[xx] -= __uint_as_float(t32[xx]);
-          st_shared_u16(sb + kChT3 + elem_off(i, x), bf16_of(ev[xx]));
+          const float e = e0[i] - __uint_as_float(t32[xx]);
+          eo[i] = e;
+          st_shared_u16(sb + kChT3 + elem_off(i, x), bf16_of(e));
         }
-        rows_store32(ev, eo + cb * 32, kD, 32, wscr);
       }
     }
     fence_proxy_async_smem();
@@ -420,9 +417,9 @@ __global__ void __launch_bounds__(kThr, 1)
     const int nt = R - t0 < kC ? (int)(R - t0) : kC;
     float* blk = scratch_of(scr, H, nch, m, h, ch);
     {
-      float* dst = blk + (int64_t)kGend * kTileElems + r0 * kD;
+      float* dst = blk + (int64_t)kGend * kTileElems + x * kD;
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) rows_store32(st + cb * 32, dst + cb * 32, kD, 32, wscr);
+      for (int c = 0; c < kD; ++c) dst[c] = st[c];
     }
     stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
     __syncthreads();
@@ -453,23 +450,21 @@ __global__ void __launch_bounds__(kThr, 1)
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
     {  // dU row x = dU0 row x + (ZW G^T) row x; -(gamma b dU)^T column x as bf16
-      const float* u0 = blk + (int64_t)kDU0 * kTileElems + r0 * kD;
-      float* uo = blk + (int64_t)kDUblk * kTileElems + r0 * kD;
+      const float* u0 = blk + (int64_t)kDU0 * kTileElems + x * kD;
+      float* uo = blk + (int64_t)kDUblk * kTileElems + x * kD;
       const float f = -sw[x] * sbt[x];
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t t32[32];
-        float uv[32];
-        rows_load32(uv, u0 + cb * 32, kD, 32, wscr);
         tmem_ld32(tb + lane_off + cb * 32, t32);
         tmem_wait_ld_r(t32);
 #pragma unroll
         for (int xx = 0; xx < 32; ++xx) {
           const int i = cb * 32 + xx;
-          uv[xx] += __uint_as_float(t32[xx]);
-          st_shared_u16(sb + kChT5 + elem_off(i, x), bf16_of(f * uv[xx]));
+          const float du = u0[i] + __uint_as_float(t32[xx]);
+          uo[i] = du;
+          st_shared_u16(sb + kChT5 + elem_off(i, x), bf16_of(f * du));
         }
-        rows_store32(uv, uo + cb * 32, kD, 32, wscr);
       }
     }
     fence_proxy_async_smem();
