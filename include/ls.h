@@ -289,8 +289,9 @@ LS_API ls_status ls_stage_pages(const ls_attn_desc* desc, const void* k_src, con
  *   LS_GDN_TENSOR_CORE  the chunkwise forward and the chunk-parallel
  *                       backward on tcgen05 tensor cores with bf16 operands
  *                       and float32 accumulation; about 5e-3 relative error,
- *                       held to 2e-2 (the bf16 bar).  q, k, v, d_o and the
- *                       outputs must be 16-byte aligned (else LS_ERR_CUDA).
+ *                       held to 2e-2 (the bf16 bar).  s0, q, k, v, d_o and
+ *                       the outputs must be 16-byte aligned (else
+ *                       LS_ERR_CUDA).
  *                       If a bounded device wait gives up in the forward, o
  *                       and s_final of that (member, head) are set to NaN.
  * Float32 callers that need the 1e-5 result keep LS_GDN_EXACT.

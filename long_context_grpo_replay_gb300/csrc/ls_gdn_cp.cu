@@ -329,9 +329,12 @@ __global__ void __launch_bounds__(kThr, 1)
 
   float st[kD];  // S (state pass), then G (gradient pass): row x, fp32
   {
-    const float* src = s0 + ((int64_t)h * kD + x) * kD;
+    const float4* src = reinterpret_cast<const float4*>(s0 + ((int64_t)h * kD + x) * kD);
 #pragma unroll
-    for (int c = 0; c < kD; ++c) st[c] = src[c];
+    for (int c = 0; c < kD / 4; ++c) {
+      const float4 a4 = src[c];
+      st[4 * c] = a4.x, st[4 * c + 1] = a4.y, st[4 * c + 2] = a4.z, st[4 * c + 3] = a4.w;
+    }
   }
   // ---- state forward
   for (int ch = 0; ok && ch < nch; ++ch) {
@@ -339,11 +342,12 @@ __global__ void __launch_bounds__(kThr, 1)
     const int nt = R - t0 < kC ? (int)(R - t0) : kC;
     float* blk = scratch_of(scr, H, nch, m, h, ch);
     {
-      // each thread's own row: the stores are not waited on, and this
-      // sequential kernel runs faster with them than with a staged transpose
-      float* dst = blk + (int64_t)kSstart * kTileElems + x * kD;
+      // each thread's own row, in 16-byte pieces: the stores are not waited
+      // on, and this sequential kernel runs faster with them than with a
+      // staged transpose
+      float4* dst = reinterpret_cast<float4*>(blk + (int64_t)kSstart * kTileElems + x * kD);
 #pragma unroll
-      for (int c = 0; c < kD; ++c) dst[c] = st[c];
+      for (int c = 0; c < kD / 4; ++c) dst[c] = make_float4(st[4 * c], st[4 * c + 1], st[4 * c + 2], st[4 * c + 3]);
     }
     stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
     __syncthreads();
@@ -363,20 +367,27 @@ __global__ void __launch_bounds__(kThr, 1)
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
     {  // E row x = E0 row x - (ZK S^T) row x; E^T column x as bf16
-      const float* e0 = blk + (int64_t)kE0 * kTileElems + x * kD;
-      float* eo = blk + (int64_t)kEblk * kTileElems + x * kD;
+      const float4* e0 = reinterpret_cast<const float4*>(blk + (int64_t)kE0 * kTileElems + x * kD);
+      float4* eo = reinterpret_cast<float4*>(blk + (int64_t)kEblk * kTileElems + x * kD);
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t t32[32];
+        float e[32];
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 a4 = e0[cb * 8 + q4];
+          e[4 * q4] = a4.x, e[4 * q4 + 1] = a4.y, e[4 * q4 + 2] = a4.z, e[4 * q4 + 3] = a4.w;
+        }
         tmem_ld32(tb + lane_off + cb * 32, t32);
         tmem_wait_ld_r(t32);
 #pragma unroll
         for (int xx = 0; xx < 32; ++xx) {
-          const int i = cb * 32 + xx;
-          const float e = e0[i] - __uint_as_float(t32[xx]);
-          eo[i] = e;
-          st_shared_u16(sb + kChT3 + elem_off(i, x), bf16_of(e));
+          e[xx] -= __uint_as_float(t32[xx]);
+          st_shared_u16(sb + kChT3 + elem_off(cb * 32 + xx, x), bf16_of(e[xx]));
         }
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          eo[cb * 8 + q4] = make_float4(e[4 * q4], e[4 * q4 + 1], e[4 * q4 + 2], e[4 * q4 + 3]);
       }
     }
     fence_proxy_async_smem();
@@ -405,9 +416,9 @@ __global__ void __launch_bounds__(kThr, 1)
     __syncthreads();
   }
   if (ok && s_final) {
-    float* dst = s_final + (((int64_t)m * H + h) * kD + x) * kD;
+    float4* dst = reinterpret_cast<float4*>(s_final + (((int64_t)m * H + h) * kD + x) * kD);
 #pragma unroll
-    for (int c = 0; c < kD; ++c) dst[c] = st[c];
+    for (int c = 0; c < kD / 4; ++c) dst[c] = make_float4(st[4 * c], st[4 * c + 1], st[4 * c + 2], st[4 * c + 3]);
   }
   // ---- dL/dS backward
 #pragma unroll
@@ -417,9 +428,9 @@ __global__ void __launch_bounds__(kThr, 1)
     const int nt = R - t0 < kC ? (int)(R - t0) : kC;
     float* blk = scratch_of(scr, H, nch, m, h, ch);
     {
-      float* dst = blk + (int64_t)kGend * kTileElems + x * kD;
+      float4* dst = reinterpret_cast<float4*>(blk + (int64_t)kGend * kTileElems + x * kD);
 #pragma unroll
-      for (int c = 0; c < kD; ++c) dst[c] = st[c];
+      for (int c = 0; c < kD / 4; ++c) dst[c] = make_float4(st[4 * c], st[4 * c + 1], st[4 * c + 2], st[4 * c + 3]);
     }
     stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
     __syncthreads();
@@ -450,21 +461,28 @@ __global__ void __launch_bounds__(kThr, 1)
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
     {  // dU row x = dU0 row x + (ZW G^T) row x; -(gamma b dU)^T column x as bf16
-      const float* u0 = blk + (int64_t)kDU0 * kTileElems + x * kD;
-      float* uo = blk + (int64_t)kDUblk * kTileElems + x * kD;
+      const float4* u0 = reinterpret_cast<const float4*>(blk + (int64_t)kDU0 * kTileElems + x * kD);
+      float4* uo = reinterpret_cast<float4*>(blk + (int64_t)kDUblk * kTileElems + x * kD);
       const float f = -sw[x] * sbt[x];
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t t32[32];
+        float du[32];
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 a4 = u0[cb * 8 + q4];
+          du[4 * q4] = a4.x, du[4 * q4 + 1] = a4.y, du[4 * q4 + 2] = a4.z, du[4 * q4 + 3] = a4.w;
+        }
         tmem_ld32(tb + lane_off + cb * 32, t32);
         tmem_wait_ld_r(t32);
 #pragma unroll
         for (int xx = 0; xx < 32; ++xx) {
-          const int i = cb * 32 + xx;
-          const float du = u0[i] + __uint_as_float(t32[xx]);
-          uo[i] = du;
-          st_shared_u16(sb + kChT5 + elem_off(i, x), bf16_of(f * du));
+          du[xx] += __uint_as_float(t32[xx]);
+          st_shared_u16(sb + kChT5 + elem_off(cb * 32 + xx, x), bf16_of(f * du[xx]));
         }
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          uo[cb * 8 + q4] = make_float4(du[4 * q4], du[4 * q4 + 1], du[4 * q4 + 2], du[4 * q4 + 3]);
       }
     }
     fence_proxy_async_smem();
@@ -902,8 +920,8 @@ cudaError_t launch_gdn_cp_bwd(int B, int H, int R, const float* s0, const float*
                               uint32_t* status, cudaStream_t st) {
   if (B == 0 || H == 0 || R == 0) return cudaSuccess;
   if (H > 65535 || B > 65535) return cudaErrorInvalidValue;  // grid y and z
-  for (const void* p : {(const void*)q, (const void*)k, (const void*)v, (const void*)d_o,
-                        (const void*)dq, (const void*)dk, (const void*)ws})
+  for (const void* p : {(const void*)s0, (const void*)q, (const void*)k, (const void*)v,
+                        (const void*)d_o, (const void*)dq, (const void*)dk, (const void*)ws})
     if (reinterpret_cast<uintptr_t>(p) & 15u) return cudaErrorMisalignedAddress;
   const int nch = (R + kC - 1) / kC;
   cudaError_t e;
