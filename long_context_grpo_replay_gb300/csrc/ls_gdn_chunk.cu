@@ -14,7 +14,8 @@
 // cores, one thread per column of E.  The state stays in fp32 registers (one
 // row per thread) and is rounded to bf16 only as an MMA operand, so this path
 // carries bf16-operand rounding: about 4e-3 relative on o and on the final
-// state at 4096 tokens.
+// state at 4096 tokens.  The per-element decay factors use the fast __expf (a few
+// ulp).
 //
 // One CTA of 128 threads per (head, member).  Thread r is token row r of the
 // chunk (tensor-memory lane r) in the epilogues, state row r for the state,
@@ -194,7 +195,7 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) {
         const int s = cb * 32 + xx;
-        if (s < r) sA[a_at(r, s)] = br * expf(cr - sc[s]) * __uint_as_float(t32[xx]);
+        if (s < r) sA[a_at(r, s)] = br * __expf(cr - sc[s]) * __uint_as_float(t32[xx]);
       }
       tmem_ld32(tb + lane_off + kTmQK + cb * 32, t32);
       tmem_wait_ld_r(t32);
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) {
         const int s = cb * 32 + xx;
-        pv[xx] = s <= r ? expf(cr - sc[s]) * __uint_as_float(t32[xx]) : 0.f;
+        pv[xx] = s <= r ? __expf(cr - sc[s]) * __uint_as_float(t32[xx]) : 0.f;
       }
 #pragma unroll
       for (int gg = 0; gg < 4; ++gg)

@@ -16,7 +16,9 @@
 //         of q, k, v, g, b from S, G, E and dU of the chunk.
 // The chains carry only two 128 x 128 products per chunk; everything else is
 // parallel over chunks.  Products are tcgen05.mma on bf16 operands with fp32
-// accumulators; solves and states are fp32.
+// accumulators; solves and states are fp32.  The per-element decay
+// factors exp(c_t - c_s) use the fast __expf (a few ulp), far below the
+// bf16 rounding of the products' operands.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -196,7 +198,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
       for (int xx = 0; xx < 32; ++xx) {
         const int s = cb * 32 + xx;
         if (s < r) {
-          const float val = expf(cr - sc[s]) * __uint_as_float(t32[xx]);
+          const float val = __expf(cr - sc[s]) * __uint_as_float(t32[xx]);
           gk[a_at(r, s)] = val;
           gko[a_at(r, s)] = val;
         }
@@ -207,7 +209,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) {
         const int t = cb * 32 + xx;
-        pv[xx] = t >= r ? expf(sc[t] - cr) * __uint_as_float(t32[xx]) : 0.f;
+        pv[xx] = t >= r ? __expf(sc[t] - cr) * __uint_as_float(t32[xx]) : 0.f;
       }
 #pragma unroll
       for (int gg = 0; gg < 4; ++gg) st_shared_v4(sb + kPrepQ + tile_off(r, cb * 4 + gg), pack8(&pv[8 * gg]));
@@ -233,7 +235,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
         const float* src = which == 0 ? v : k;
         for (int t = 0; t < kC; ++t) {
           float val = 0.f;
-          if (t < nt) val = sbt[t] * src[(t0 + t) * rs + h * kD + x] * (which == 0 ? 1.f : expf(sc[t]));
+          if (t < nt) val = sbt[t] * src[(t0 + t) * rs + h * kD + x] * (which == 0 ? 1.f : __expf(sc[t]));
           bw[u_at(t, x)] = val;
         }
         solve_lower(bw, gk, sbt, nt8, x);
@@ -255,7 +257,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
       } else {
         const float clast = sc[kC - 1];
         for (int t = 0; t < kC; ++t)
-          buf2[u_at(t, x)] = t < nt ? expf(clast - sc[t]) * k[(t0 + t) * rs + h * kD + x] : 0.f;
+          buf2[u_at(t, x)] = t < nt ? __expf(clast - sc[t]) * k[(t0 + t) * rs + h * kD + x] : 0.f;
       }
       __syncthreads();
       solve_upper(bw, gk, sbt, nt8, x);
@@ -639,7 +641,7 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) {
         const int s = cb * 32 + xx;
-        f32[xx] = s <= t ? expf(ct - sc[s]) * __uint_as_float(t32[xx]) : 0.f;
+        f32[xx] = s <= t ? __expf(ct - sc[s]) * __uint_as_float(t32[xx]) : 0.f;
       }
 #pragma unroll
       for (int gg = 0; gg < 4; ++gg) st_shared_v4(S5 + tile_off(t, cb * 4 + gg), pack8(&f32[8 * gg]));
@@ -720,7 +722,7 @@ __global__ void __launch_bounds__(kThr, 1)
       for (int xx = 0; xx < 32; ++xx) {
         const int s = cb * 32 + xx;
         const float dp = __uint_as_float(t32[xx]);
-        f32[xx] = s <= t ? expf(ct - sc[s]) * dp : 0.f;
+        f32[xx] = s <= t ? __expf(ct - sc[s]) * dp : 0.f;
         rv[xx] *= dp;  // r = dP . P
         st_shared_u16(S0 + elem_off(s, t), bf16_of(f32[xx]));
       }
@@ -738,7 +740,7 @@ __global__ void __launch_bounds__(kThr, 1)
           const float gkv = gkb[a_at(t, s)];
           dbt = fmaf(da, gkv, dbt);
           rv[xx] = fmaf(da * bt, gkv, rv[xx]);
-          mk = da * bt * expf(ct - sc[s]);
+          mk = da * bt * __expf(ct - sc[s]);
         }
         if (s <= t) {
           const uint16_t hb = bf16_of(mk);

@@ -54,6 +54,7 @@ inline unsigned __float_as_uint(float f) {
   return u;
 }
 inline float __log2f(float x) { return std::log2(x); }
+inline float __expf(float x) { return std::exp(x); }
 template <class T>
 inline T __ldg(const T* p) {
   return *p;
