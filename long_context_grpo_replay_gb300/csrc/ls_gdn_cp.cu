@@ -168,9 +168,9 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   const int64_t rs = (int64_t)H * kD;  // token stride of q, k, v, d_o
 
   if (tid < kThr) {
-    stage_rows(sb + kPrepK, k + (t0 * H + h) * kD, rs, nt, nullptr);
-    stage_rows(sb + kPrepQ, q + (t0 * H + h) * kD, rs, nt, nullptr);
-    stage_rows(sb + kPrepDO, d_o + (t0 * H + h) * kD, rs, nt, nullptr);
+    stage_rows<4>(sb + kPrepK, k + (t0 * H + h) * kD, rs, nt, nullptr);
+    stage_rows<4>(sb + kPrepQ, q + (t0 * H + h) * kD, rs, nt, nullptr);
+    stage_rows<4>(sb + kPrepDO, d_o + (t0 * H + h) * kD, rs, nt, nullptr);
   }
   stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
   fence_proxy_async_smem();
@@ -356,8 +356,8 @@ __global__ void __launch_bounds__(kThr, 1)
     sw[x] = x < nt ? expf(sc[kC - 1] - sc[x]) : 0.f;
     __syncthreads();
     stage_row_regs(sb + kChT0, x, st);                                         // S (bf16)
-    stage_rows(sb + kChT1, blk + (int64_t)kZK * kTileElems, kD, kC, nullptr);  // ZK
-    stage_rows(sb + kChT2, k + (t0 * H + h) * kD, rs, nt, sw);                 // W = diag(w) K
+    stage_rows<4>(sb + kChT1, blk + (int64_t)kZK * kTileElems, kD, kC, nullptr);  // ZK
+    stage_rows<4>(sb + kChT2, k + (t0 * H + h) * kD, rs, nt, sw);                 // W = diag(w) K
     fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {  // ZK S^T -> cols 0..127
@@ -439,9 +439,9 @@ __global__ void __launch_bounds__(kThr, 1)
     sw[x] = expf(sc[x]);
     __syncthreads();
     stage_row_regs(sb + kChT0, x, st);                                         // G (bf16)
-    stage_rows(sb + kChT1, blk + (int64_t)kZW * kTileElems, kD, kC, nullptr);  // ZW
-    stage_rows(sb + kChT2, q + (t0 * H + h) * kD, rs, nt, nullptr);            // Q
-    stage_rows(sb + kChT3, k + (t0 * H + h) * kD, rs, nt, nullptr);            // K
+    stage_rows<4>(sb + kChT1, blk + (int64_t)kZW * kTileElems, kD, kC, nullptr);  // ZW
+    stage_rows<4>(sb + kChT2, q + (t0 * H + h) * kD, rs, nt, nullptr);            // Q
+    stage_rows<4>(sb + kChT3, k + (t0 * H + h) * kD, rs, nt, nullptr);            // K
 #pragma unroll 4
     for (int gq = 0; gq < 16; ++gq) {  // (gamma dO)^T row x (tokens along K)
       float f8[8];

@@ -41,22 +41,34 @@ __device__ __forceinline__ uint16_t bf16_of(float x) { return (uint16_t)(pack_bf
 
 // Rows 0..nt-1 of a float32 matrix (row r at src + r * stride, 128 columns)
 // into a tile, each row times scale[r] when scale is given; rows nt..127 zero.
-// All threads.
+// All threads.  The shared-memory stores are ordering points for the
+// compiler, so each batch of kBatch row pieces is loaded into registers
+// before any of it is stored: kBatch global loads in flight, not one.
+template <int kBatch = 8>
 __device__ __forceinline__ void stage_rows(uint32_t tile, const float* src, int64_t stride, int nt,
                                            const float* scale) {
+  static_assert(16 % kBatch == 0, "batch divides the 16 pieces per thread");
   const int tid = threadIdx.x;
-#pragma unroll 4
-  for (int it = 0; it < 16; ++it) {
-    const int item = tid + kThr * it, r = item >> 4, gq = item & 15;
-    uint4 pk = make_uint4(0u, 0u, 0u, 0u);
-    if (r < nt) {
-      const float4* p = reinterpret_cast<const float4*>(src + r * stride + gq * 8);
-      const float4 a = p[0], b = p[1];
-      const float f = scale ? scale[r] : 1.f;
-      const float x[8] = {a.x * f, a.y * f, a.z * f, a.w * f, b.x * f, b.y * f, b.z * f, b.w * f};
-      pk = pack8(x);
+#pragma unroll 1
+  for (int it0 = 0; it0 < 16; it0 += kBatch) {
+    float4 a[kBatch], b[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int item = tid + kThr * (it0 + j), r = item >> 4, gq = item & 15;
+      a[j] = b[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r < nt) {
+        const float4* p = reinterpret_cast<const float4*>(src + r * stride + gq * 8);
+        a[j] = p[0], b[j] = p[1];
+      }
     }
-    st_shared_v4(tile + tile_off(r, gq), pk);
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int item = tid + kThr * (it0 + j), r = item >> 4, gq = item & 15;
+      const float f = (scale && r < nt) ? scale[r] : 1.f;
+      const float x[8] = {a[j].x * f, a[j].y * f, a[j].z * f, a[j].w * f,
+                          b[j].x * f, b[j].y * f, b[j].z * f, b[j].w * f};
+      st_shared_v4(tile + tile_off(r, gq), pack8(x));
+    }
   }
 }
 // One row of a tile from 128 registers (thread = row).
@@ -83,8 +95,11 @@ __device__ __forceinline__ void mma_group(uint32_t d, uint32_t a, uint32_t b, bo
 __device__ __forceinline__ void rows_load32(float* v, const float* base, int64_t stride, int nvalid,
                                             float* scr) {
   const int lane = threadIdx.x & 31;
-#pragma unroll 4
-  for (int r = 0; r < 32; ++r) scr[r * 33 + lane] = r < nvalid ? base[r * stride + lane] : 0.f;
+  float tmp[32];  // all 32 loads issued before the first shared store
+#pragma unroll
+  for (int r = 0; r < 32; ++r) tmp[r] = r < nvalid ? base[r * stride + lane] : 0.f;
+#pragma unroll
+  for (int r = 0; r < 32; ++r) scr[r * 33 + lane] = tmp[r];
   __syncwarp();
 #pragma unroll
   for (int c = 0; c < 32; ++c) v[c] = scr[lane * 33 + c];
