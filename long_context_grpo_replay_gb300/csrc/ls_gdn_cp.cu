@@ -68,14 +68,22 @@ __device__ __forceinline__ void stage_gates(const float* g, const float* beta, i
   sc[tid] = x;
 }
 
-// Forward substitution (I + diag(b) GK) y = rhs on column x of the fp32
-// buffer buf (in place), rows 0..nt8-1, eight rows at a time.
-__device__ __forceinline__ void solve_lower(float* buf, const float* gk, const float* sbt, int nt8,
-                                            int x) {
-  for (int t8 = 0; t8 < nt8; t8 += 8) {
+// fp32 [128 x 128] buffer of T with rows of 129 floats: a column read by
+// consecutive threads and a row read by a whole warp are both free of bank
+// conflicts, with no index arithmetic beyond the row base.
+constexpr int kTStride = kC + 1;
+__device__ __forceinline__ int b_at(int t, int x) { return t * kTStride + x; }
+
+// Column x of the inverse of the unit lower-triangular diagonal block of
+// (I + diag(b) GK) on rows and columns r0 .. r0+63, by forward substitution
+// eight rows at a time, into buf (column x, rows r0 .. r0+63; the rows above
+// x come out zero).  x lies inside the block.
+__device__ __forceinline__ void invert_block64(float* buf, const float* gk, const float* sbt, int r0,
+                                               int x) {
+  for (int t8 = r0; t8 < r0 + 64; t8 += 8) {
     float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int s = 0; s < t8; ++s) {
-      const float e = buf[u_at(s, x)];
+    for (int s = r0; s < t8; ++s) {
+      const float e = buf[b_at(s, x)];
 #pragma unroll
       for (int u = 0; u < 8; ++u) sum[u] = fmaf(gk[a_at(t8 + u, s)], e, sum[u]);
     }
@@ -84,42 +92,33 @@ __device__ __forceinline__ void solve_lower(float* buf, const float* gk, const f
     for (int u = 0; u < 8; ++u) {
 #pragma unroll
       for (int u2 = 0; u2 < u; ++u2) sum[u] = fmaf(gk[a_at(t8 + u, t8 + u2)], ev[u2], sum[u]);
-      ev[u] = fmaf(-sbt[t8 + u], sum[u], buf[u_at(t8 + u, x)]);
+      ev[u] = fmaf(-sbt[t8 + u], sum[u], t8 + u == x ? 1.f : 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) buf[u_at(t8 + u, x)] = ev[u];
-  }
-}
-// Backward substitution (I + diag(b) GK)^T y = rhs on column x, in place.
-__device__ __forceinline__ void solve_upper(float* buf, const float* gk, const float* sbt, int nt8,
-                                            int x) {
-  for (int t8 = nt8 - 8; t8 >= 0; t8 -= 8) {
-    float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int s = t8 + 8; s < nt8; ++s) {
-      const float e = sbt[s] * buf[u_at(s, x)];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) sum[u] = fmaf(gk[a_at(s, t8 + u)], e, sum[u]);
-    }
-    float ev[8];
-#pragma unroll
-    for (int u = 7; u >= 0; --u) {
-#pragma unroll
-      for (int u2 = 7; u2 > u; --u2) sum[u] = fmaf(gk[a_at(t8 + u2, t8 + u)], sbt[t8 + u2] * ev[u2], sum[u]);
-      ev[u] = buf[u_at(t8 + u, x)] - sum[u];
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) buf[u_at(t8 + u, x)] = ev[u];
+    for (int u = 0; u < 8; ++u) buf[b_at(t8 + u, x)] = ev[u];
   }
 }
 
 // ---------------------------------------------------------------- prep
-// One CTA per (chunk, head, member), 256 threads: the first 128 own the
-// chunk's rows and columns (tensor-memory lanes, one column each in the
-// solves); the second 128 run the second of each pair of independent
-// triangular solves beside the first (E0 with ZK, dU0 with ZW).
-constexpr uint32_t kPrepK = 0, kPrepQ = kTile, kPrepDO = 2 * kTile, kPrepGK = 3 * kTile;
-constexpr uint32_t kPrepU = 4 * kTile, kPrepMisc = 6 * kTile;
-constexpr uint32_t kPrepSmem = kPrepMisc + 2048 + 1024;
+// One CTA per (chunk, head, member), 256 threads in two groups of 128.
+// T = (I + diag(b) GK)^-1 is formed explicitly in fp32 by blocks of 64
+// rows: each diagonal block by forward substitution (group A, one column per
+// thread), the off-diagonal block as T21 = -T22 (diag(b) GK21) T11 by two
+// products on the CUDA cores.  The four right-hand sides are then tensor-core
+// products with T as the A operand, split into bf16 hi + lo parts (their sum
+// is T to about 2^-17):
+//   E0 = T (b V), ZK = T (b gamma K)      (the T tile read M-major)
+//   dU0 = T^T dE0, ZW = T^T (w K)         (the same tile read K-major)
+// Group B stages the right-hand sides while group A forms T.
+// Shared memory: R0 K -> b V, R1 Q -> P^T -> b gamma K, R2 dO -> w K,
+// R3 GK (packed fp32) -> dE0, R4 + R5 (and 512 bytes more) T (fp32) -> T hi (R4),
+// T lo (R5).
+constexpr uint32_t kPrepR0 = 0, kPrepR1 = kTile, kPrepR2 = 2 * kTile, kPrepR3 = 3 * kTile;
+constexpr uint32_t kPrepR4 = 4 * kTile, kPrepR5 = 5 * kTile;
+// T in fp32 (rows of 129 floats) runs 512 bytes past R5
+constexpr uint32_t kPrepMisc = 6 * kTile + 1024;
+constexpr uint32_t kPrepSmem = kPrepMisc + 3072 + 1024;
+static_assert(kPrepR4 + kC * kTStride * 4 <= kPrepMisc, "T buffer overlaps the misc area");
 constexpr int kPrepThr = 2 * kThr;
 
 __global__ void __launch_bounds__(kPrepThr, 1)
@@ -132,27 +131,29 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(sm);
-  float* gk = reinterpret_cast<float*>(sm + kPrepGK);
-  float* buf = reinterpret_cast<float*>(sm + kPrepU);
-  // the second solve's buffer: the K and Q tiles, once the MMAs have read them
-  float* buf2 = reinterpret_cast<float*>(sm + kPrepK);
+  float* gk = reinterpret_cast<float*>(sm + kPrepR3);
+  float* buf = reinterpret_cast<float*>(sm + kPrepR4);
   float* sc = reinterpret_cast<float*>(sm + kPrepMisc);
-  float* sbt = sc + kC;
-  float* swt = sbt + kC;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kPrepMisc + 1536);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
+  float* sbt = sc + kC;    // b
+  float* sbg = sbt + kC;   // b gamma
+  float* swk = sbg + kC;   // w (zero past the response)
+  float* swt = swk + kC;   // 8 floats of scan scratch
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kPrepMisc + 2560);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 4);
   uint32_t* abort_s = tslot + 1;
 
   const int ch = blockIdx.x, h = blockIdx.y, m = blockIdx.z, tid = threadIdx.x, warp = tid >> 5;
+  const bool grpA = tid < kThr;
+  const int gt = tid & (kThr - 1);  // index within the group: row / column
   const int64_t t0 = (int64_t)ch * kC;
-  const int nt = R - t0 < kC ? (int)(R - t0) : kC, nt8 = (nt + 7) & ~7;
+  const int nt = R - t0 < kC ? (int)(R - t0) : kC;
   {
     const int64_t tok = (int64_t)m * R * H;
     q += tok * kD, k += tok * kD, v += tok * kD, d_o += tok * kD, g += tok, beta += tok;
   }
   float* out = scratch_of(scr, H, nch, m, h, ch);
   if (tid == 0) {
-    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), 1);
     *abort_s = 0;
     fence_mbar_init();
   }
@@ -163,112 +164,214 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tb = *tslot, lane_off = (uint32_t)(warp * 32) << 16;
+  const uint32_t tb = *tslot, lane_off = (uint32_t)((warp & 3) * 32) << 16;
   const volatile uint32_t* abortp = abort_s;
   const int64_t rs = (int64_t)H * kD;  // token stride of q, k, v, d_o
+  const int64_t row0 = (t0 * H + h) * kD;
 
-  if (tid < kThr) {
-    stage_rows<4>(sb + kPrepK, k + (t0 * H + h) * kD, rs, nt, nullptr);
-    stage_rows<4>(sb + kPrepQ, q + (t0 * H + h) * kD, rs, nt, nullptr);
-    stage_rows<4>(sb + kPrepDO, d_o + (t0 * H + h) * kD, rs, nt, nullptr);
+  if (grpA) {
+    stage_rows<4>(sb + kPrepR0, k + row0, rs, nt, nullptr, gt);
+    stage_rows<4>(sb + kPrepR1, q + row0, rs, nt, nullptr, gt);
+  } else {
+    stage_rows<4>(sb + kPrepR2, d_o + row0, rs, nt, nullptr, gt);
   }
   stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
   fence_proxy_async_smem();
   __syncthreads();
+  if (!grpA) {  // the right-hand sides' row scales (read after the next block barrier)
+    const float ct = sc[gt], clast = sc[kC - 1];
+    sbg[gt] = sbt[gt] * __expf(ct);
+    swk[gt] = gt < nt ? __expf(clast - ct) : 0.f;
+  }
 
   if (tid == 0) {  // K K^T -> cols 0..127, K Q^T -> 128..255
     tc_fence_after();
-    mma_group(tb + 0, sb + kPrepK, sb + kPrepK, false, false);
-    mma_group(tb + 128, sb + kPrepK, sb + kPrepQ, false, false);
+    mma_group(tb + 0, sb + kPrepR0, sb + kPrepR0, false, false);
+    mma_group(tb + 128, sb + kPrepR0, sb + kPrepR1, false, false);
     mma_commit(smem_u32(&bars[0]));
   }
   bool ok = mbar_wait_warp(smem_u32(&bars[0]), 0, abortp);
   if (!__syncthreads_or(!ok)) {
     tc_fence_after();
-    // thread r: GK row r (s < r); P^T row r: P^T[r][t] = [t >= r] Gamma_tr (K_r . Q_t)
-    const int r = tid;
-    const float cr = tid < kThr ? sc[r] : 0.f;
-    float* gko = out + (int64_t)kGKblk * kTileElems;
+    if (grpA) {
+      // thread r: GK row r (s < r); P^T row r: P^T[r][t] = [t >= r] Gamma_tr (K_r . Q_t)
+      const int r = gt;
+      const float cr = sc[r];
+      float* gko = out + (int64_t)kGKblk * kTileElems;
 #pragma unroll 1
-    for (int cb = 0; tid < kThr && cb < 4; ++cb) {
-      uint32_t t32[32];
-      tmem_ld32(tb + lane_off + 0 + cb * 32, t32);
-      tmem_wait_ld_r(t32);
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t t32[32];
+        tmem_ld32(tb + lane_off + 0 + cb * 32, t32);
+        tmem_wait_ld_r(t32);
 #pragma unroll
-      for (int xx = 0; xx < 32; ++xx) {
-        const int s = cb * 32 + xx;
-        if (s < r) {
-          const float val = __expf(cr - sc[s]) * __uint_as_float(t32[xx]);
-          gk[a_at(r, s)] = val;
-          gko[a_at(r, s)] = val;
+        for (int xx = 0; xx < 32; ++xx) {
+          const int s = cb * 32 + xx;
+          if (s < r) {
+            const float val = __expf(cr - sc[s]) * __uint_as_float(t32[xx]);
+            gk[a_at(r, s)] = val;
+            gko[a_at(r, s)] = val;
+          }
         }
-      }
-      tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
-      tmem_wait_ld_r(t32);
-      float pv[32];
+        tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
+        tmem_wait_ld_r(t32);
+        float pv[32];
 #pragma unroll
-      for (int xx = 0; xx < 32; ++xx) {
-        const int t = cb * 32 + xx;
-        pv[xx] = t >= r ? __expf(sc[t] - cr) * __uint_as_float(t32[xx]) : 0.f;
-      }
+        for (int xx = 0; xx < 32; ++xx) {
+          const int t = cb * 32 + xx;
+          pv[xx] = t >= r ? __expf(sc[t] - cr) * __uint_as_float(t32[xx]) : 0.f;
+        }
 #pragma unroll
-      for (int gg = 0; gg < 4; ++gg) st_shared_v4(sb + kPrepQ + tile_off(r, cb * 4 + gg), pack8(&pv[8 * gg]));
+        for (int gg = 0; gg < 4; ++gg) st_shared_v4(sb + kPrepR1 + tile_off(r, cb * 4 + gg), pack8(&pv[8 * gg]));
+      }
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {  // dE0 = P^T dO -> cols 256..383 (dO as an N-major B)
       tc_fence_after();
-      mma_group(tb + 256, sb + kPrepQ, sb + kPrepDO, true, false);
+      mma_group(tb + 256, sb + kPrepR1, sb + kPrepR2, true, false);
       mma_commit(smem_u32(&bars[1]));
     }
-    // the second solve of each pair writes over the K and Q tiles: the
-    // P^T dO product must have read them first
-    ok = mbar_wait_warp(smem_u32(&bars[1]), 0, abortp);
-    if (!__syncthreads_or(!ok)) {
-      tc_fence_after();
-      // forward solves, thread x = column x: E0 from b V (first 128 threads),
-      // ZK from b gamma K (second 128), side by side
-      const int x = tid & (kThr - 1), which = tid / kThr;
-      float* bw = which == 0 ? buf : buf2;
-      {
-        const float* src = which == 0 ? v : k;
-        for (int t = 0; t < kC; ++t) {
-          float val = 0.f;
-          if (t < nt) val = sbt[t] * src[(t0 + t) * rs + h * kD + x] * (which == 0 ? 1.f : __expf(sc[t]));
-          bw[u_at(t, x)] = val;
+    if (grpA) {
+      // ---- T by blocks of 64 rows.  Column x: T11 (x < 64) or T22 (x >= 64)
+      // by substitution; the rest of the column zero.
+      const int x = gt, r0 = x & 64;
+      for (int t = 0; t < kC; ++t)
+        if (t < r0 || t >= r0 + 64) buf[b_at(t, x)] = 0.f;
+      invert_block64(buf, gk, sbt, r0, x);
+      named_bar_sync(1, kThr);
+      // thread (xc, hf) owns column xc of the off-diagonal block, rows
+      // 64 + 32 hf .. 64 + 32 hf + 31
+      const int xc = x & 63, hf = x >> 6;
+      {  // Y = diag(b) GK21 T11 into the block's place (T11 does not read it)
+        float tcol[64];
+#pragma unroll
+        for (int s = 0; s < 64; ++s) tcol[s] = buf[b_at(s, xc)];
+#pragma unroll 1
+        for (int j = 0; j < 32; ++j) {
+          const int t = 64 + 32 * hf + j;
+          const float* gr = gk + a_at(t, 0);
+          float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+          for (int s = 0; s < 64; s += 4) {
+            p0 = fmaf(gr[s], tcol[s], p0);
+            p1 = fmaf(gr[s + 1], tcol[s + 1], p1);
+            p2 = fmaf(gr[s + 2], tcol[s + 2], p2);
+            p3 = fmaf(gr[s + 3], tcol[s + 3], p3);
+          }
+          buf[b_at(t, xc)] = sbt[t] * ((p0 + p1) + (p2 + p3));
         }
-        solve_lower(bw, gk, sbt, nt8, x);
-        float* dst = out + (int64_t)(which == 0 ? kE0 : kZK) * kTileElems;
-        for (int t = 0; t < kC; ++t) dst[t * kD + x] = bw[u_at(t, x)];
       }
-      __syncthreads();
-      // backward solves: dU0 from dE0 (rows from tensor memory, first 128
-      // threads), ZW from w K (second 128), side by side
-      if (which == 0) {
+      named_bar_sync(1, kThr);
+      {  // T21 = -T22 Y (T22 stored with its zero upper triangle and unit diagonal)
+        float ycol[64];
+#pragma unroll
+        for (int s = 0; s < 64; ++s) ycol[s] = buf[b_at(64 + s, xc)];
+        named_bar_sync(1, kThr);  // Y read everywhere before T21 overwrites it
+#pragma unroll 1
+        for (int j = 0; j < 32; ++j) {
+          const int t = 64 + 32 * hf + j;
+          const float* tr = buf + b_at(t, 64);
+          float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+          for (int s = 0; s < 64; s += 4) {
+            p0 = fmaf(tr[s], ycol[s], p0);
+            p1 = fmaf(tr[s + 1], ycol[s + 1], p1);
+            p2 = fmaf(tr[s + 2], ycol[s + 2], p2);
+            p3 = fmaf(tr[s + 3], ycol[s + 3], p3);
+          }
+          buf[b_at(t, xc)] = -((p0 + p1) + (p2 + p3));
+        }
+      }
+    } else {
+      // ---- group B: the right-hand sides, once P^T dO has read R1 and R2
+      ok = mbar_wait_warp(smem_u32(&bars[1]), 0, abortp);
+      if (ok) {
+        stage_rows<4>(sb + kPrepR0, v + row0, rs, nt, sbt, gt);  // b V
+        stage_rows<4>(sb + kPrepR1, k + row0, rs, nt, sbg, gt);  // b gamma K
+        stage_rows<4>(sb + kPrepR2, k + row0, rs, nt, swk, gt);  // w K
+      }
+    }
+    if (!__syncthreads_or(!ok)) {
+      float tcol[kC];
+      if (grpA) {
+#pragma unroll
+        for (int t = 0; t < kC; ++t) tcol[t] = buf[b_at(t, gt)];
+      } else {
+        // dE0 rows (bf16) over GK, which the substitution no longer needs
+        tc_fence_after();
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
           uint32_t t32[32];
           tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
           tmem_wait_ld_r(t32);
+          float f32[32];
 #pragma unroll
-          for (int xx = 0; xx < 32; ++xx) buf[u_at(r, cb * 32 + xx)] = __uint_as_float(t32[xx]);
+          for (int xx = 0; xx < 32; ++xx) f32[xx] = __uint_as_float(t32[xx]);
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg) st_shared_v4(sb + kPrepR3 + tile_off(gt, cb * 4 + gg), pack8(&f32[8 * gg]));
         }
-      } else {
-        const float clast = sc[kC - 1];
-        for (int t = 0; t < kC; ++t)
-          buf2[u_at(t, x)] = t < nt ? __expf(clast - sc[t]) * k[(t0 + t) * rs + h * kD + x] : 0.f;
       }
+      __syncthreads();  // T read from R4 / R5 before its bf16 halves overwrite them
+      if (grpA) {  // row x of the hi and lo tiles = column x of T
+#pragma unroll
+        for (int gq = 0; gq < 16; ++gq) {
+          float hi[8], lo[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint16_t hb = bf16_of(tcol[8 * gq + u]);
+            hi[u] = __uint_as_float((uint32_t)hb << 16);
+            lo[u] = tcol[8 * gq + u] - hi[u];
+          }
+          st_shared_v4(sb + kPrepR4 + tile_off(gt, gq), pack8(hi));
+          st_shared_v4(sb + kPrepR5 + tile_off(gt, gq), pack8(lo));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
       __syncthreads();
-      solve_upper(bw, gk, sbt, nt8, x);
-      float* dst = out + (int64_t)(which == 0 ? kDU0 : kZW) * kTileElems;
-      for (int t = 0; t < kC; ++t) dst[t * kD + x] = bw[u_at(t, x)];
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t th = sb + kPrepR4, tl = sb + kPrepR5;
+        mma_group_amn(tb + 0, th, sb + kPrepR0, true, false);    // E0 = T (b V)
+        mma_group_amn(tb + 0, tl, sb + kPrepR0, true, true);
+        mma_group_amn(tb + 128, th, sb + kPrepR1, true, false);  // ZK = T (b gamma K)
+        mma_group_amn(tb + 128, tl, sb + kPrepR1, true, true);
+        mma_group(tb + 256, th, sb + kPrepR3, true, false);      // dU0 = T^T dE0
+        mma_group(tb + 256, tl, sb + kPrepR3, true, true);
+        mma_group(tb + 384, th, sb + kPrepR2, true, false);      // ZW = T^T (w K)
+        mma_group(tb + 384, tl, sb + kPrepR2, true, true);
+        mma_commit(smem_u32(&bars[2]));
+      }
+      ok = mbar_wait_warp(smem_u32(&bars[2]), 0, abortp);
+      if (!__syncthreads_or(!ok)) {
+        // warps 0-3: E0 and ZK (columns 0..255); warps 4-7: dU0 and ZW
+        tc_fence_after();
+        float* wscr = reinterpret_cast<float*>(sm + kPrepR0) + warp * 32 * 33;
+        const int r0w = (warp & 3) * 32;
+#pragma unroll 1
+        for (int bi = 0; bi < 2; ++bi) {
+          const int blkid = grpA ? (bi == 0 ? kE0 : kZK) : (bi == 0 ? kDU0 : kZW);
+          const uint32_t col = (grpA ? 0 : 256) + bi * 128;
+          float* dst = out + (int64_t)blkid * kTileElems + r0w * kD;
+#pragma unroll 1
+          for (int cb = 0; cb < 4; ++cb) {
+            uint32_t t32[32];
+            tmem_ld32(tb + lane_off + col + cb * 32, t32);
+            tmem_wait_ld_r(t32);
+            float f32[32];
+#pragma unroll
+            for (int xx = 0; xx < 32; ++xx) f32[xx] = __uint_as_float(t32[xx]);
+            rows_store32(f32, dst + cb * 32, kD, 32, wscr);
+          }
+        }
+      }
     }
   }
   if (__syncthreads_or(!ok) && tid == 0 && status) atomicOr(status, kStatusTimeout);
   if (tid == 0) {  // drain before tensor memory is freed
-    mma_commit(smem_u32(&bars[2]));
-    mbar_wait(smem_u32(&bars[2]), 0, abortp);
+    mma_commit(smem_u32(&bars[3]));
+    mbar_wait(smem_u32(&bars[3]), 0, abortp);
   }
   tc_fence_before();
   __syncthreads();

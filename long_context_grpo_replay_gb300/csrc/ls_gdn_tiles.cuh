@@ -41,14 +41,14 @@ __device__ __forceinline__ uint16_t bf16_of(float x) { return (uint16_t)(pack_bf
 
 // Rows 0..nt-1 of a float32 matrix (row r at src + r * stride, 128 columns)
 // into a tile, each row times scale[r] when scale is given; rows nt..127 zero.
-// All threads.  The shared-memory stores are ordering points for the
+// 128 threads.  The shared-memory stores are ordering points for the
 // compiler, so each batch of kBatch row pieces is loaded into registers
 // before any of it is stored: kBatch global loads in flight, not one.
+// tid: the caller's index among the 128 threads that stage the tile.
 template <int kBatch = 8>
 __device__ __forceinline__ void stage_rows(uint32_t tile, const float* src, int64_t stride, int nt,
-                                           const float* scale) {
+                                           const float* scale, int tid = threadIdx.x) {
   static_assert(16 % kBatch == 0, "batch divides the 16 pieces per thread");
-  const int tid = threadIdx.x;
 #pragma unroll 1
   for (int it0 = 0; it0 < 16; it0 += kBatch) {
     float4 a[kBatch], b[kBatch];
@@ -82,6 +82,15 @@ __device__ __forceinline__ void mma_group(uint32_t d, uint32_t a, uint32_t b, bo
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
     mma_ss(d, kdesc(a, kk), b_mn ? mndesc(b, kk) : kdesc(b, kk), id, (acc || kk > 0) ? 1u : 0u);
+}
+// The same with A read M-major (a tile whose row s holds column s of A), so
+// one tile serves as A in K-major form for one product and as A^T in M-major
+// form for another.
+__device__ __forceinline__ void mma_group_amn(uint32_t d, uint32_t a, uint32_t b, bool b_mn, bool acc) {
+  const uint32_t id = idesc_bf16(128, 128, b_mn, true);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ss(d, mndesc(a, kk), b_mn ? mndesc(b, kk) : kdesc(b, kk), id, (acc || kk > 0) ? 1u : 0u);
 }
 // ---- thread-per-row code and coalesced global rows.  The 32 threads of a
 // warp own 32 consecutive rows; a [32 rows x 32 columns] float block moves

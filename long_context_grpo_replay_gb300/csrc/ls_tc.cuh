@@ -141,10 +141,11 @@ __device__ __forceinline__ void tc_fence_after() {
 // ---------------------------------------------------------------- MMA
 // Instruction descriptor, kind::f16 with bf16 A/B and f32 accumulation.
 // b_mn_major: B stored with N contiguous (else K contiguous).
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major, bool a_mn_major = false) {
   return (1u << 4)                          // D format: f32
          | (1u << 7)                        // A format: bf16
          | (1u << 10)                       // B format: bf16
+         | ((a_mn_major ? 1u : 0u) << 15)   // A major-ness
          | ((b_mn_major ? 1u : 0u) << 16)   // B major-ness
          | ((uint32_t)(N >> 3) << 17)       // N / 8
          | ((uint32_t)(M >> 4) << 24);      // M / 16

@@ -109,6 +109,8 @@ struct Block {
   std::vector<std::pair<const void*, uint32_t>> statics;
   uint32_t tmem[kTmemLanes][kTmemCols];
   bool tmem_allocated = false;
+  std::unique_ptr<std::barrier<>> named[16];  // bar.sync id, n (id 1..15), made on first use
+  uint32_t named_n[16] = {};
   Engine tensor, copy;  // declared last: destroyed (drained) first
 };
 
@@ -155,6 +157,24 @@ inline int syncthreads_or(int p) {
   return r;
 }
 inline void syncwarp() { g_block->warp_bar[t_tid >> 5]->arrive_and_wait(); }
+// A named barrier among n threads (whole warps); every use of one id must
+// name the same count.
+inline void named_bar_sync(uint32_t id, uint32_t n) {
+  Block& b = *g_block;
+  if (id == 0 || id >= 16 || n == 0 || n % 32 || (int)n > b.nthreads) die("named barrier", id, n);
+  std::barrier<>* br;
+  {
+    std::lock_guard<std::mutex> lk(b.mu);
+    if (!b.named[id]) {
+      b.named[id].reset(new std::barrier<>(n));
+      b.named_n[id] = n;
+    } else if (b.named_n[id] != n) {
+      die("named barrier used with two thread counts", id, n);
+    }
+    br = b.named[id].get();
+  }
+  br->arrive_and_wait();
+}
 inline float shfl_up(float x, int off) {
   Block& b = *g_block;
   const int w = t_tid >> 5, l = t_tid & 31;

@@ -29,8 +29,8 @@ inline void tmem_dealloc(uint32_t, uint32_t) { emu::tmem_dealloc(); }
 inline void tc_fence_before() {}
 inline void tc_fence_after() {}
 
-constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major, bool a_mn_major = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 inline uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -78,7 +78,7 @@ inline void tmem_ld1x2(uint32_t a0, uint32_t a1, uint32_t& a, uint32_t& b) {
 }
 inline void tmem_wait_ld() {}
 inline void tmem_wait_st() {}
-inline void named_bar_sync(uint32_t, uint32_t) { emu::die("named barriers are not emulated"); }
+inline void named_bar_sync(uint32_t id, uint32_t n) { emu::named_bar_sync(id, n); }
 inline void tmem_wait_ld_r(uint32_t (&)[32]) {}
 inline void reg_dep(uint32_t (&)[32]) {}
 inline uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
