@@ -7,18 +7,26 @@
 // log-decays, gamma_t = exp(c_t), Gamma_ts = exp(c_t - c_s), w_t = gamma_C /
 // gamma_t, GK = strict_lower(Gamma . K K^T), A = diag(b) GK, T = (I + A)^-1,
 // P = lower(Gamma . Q K^T), W = diag(w) K.  The replay is three stages:
-//   prep  (all chunks at once): E0 = T diag(b) V, ZK = T diag(b gamma) K,
-//         dU0 = T^T P^T dO, ZW = T^T W         (the only triangular solves)
-//   chain (per head and member, over the chunks):
-//         state forward   E = E0 - ZK S^T,  S <- gamma_C S + E^T W
-//         dL/dS backward  dU = dU0 + ZW G^T, G <- gamma_C G + (gamma dO)^T Q - (gamma b dU)^T K
-//   out   (all chunks at once): o = diag(gamma) Q S^T + P E and the gradients
-//         of q, k, v, g, b from S, G, E and dU of the chunk.
-// The chains carry only two 128 x 128 products per chunk; everything else is
+//   prep  (all chunks at once): T, then E0 = T diag(b) V, ZK = T diag(b gamma) K,
+//         dU0 = T^T P^T dO, ZW = T^T W, and the chains' per-chunk terms
+//         M = ZK^T W, F = E0^T W, M' = ZW^T diag(gamma b) K,
+//         F' = (gamma dO)^T Q - (gamma b dU0)^T K
+//   chain (per head and member, over the chunks): the affine recurrences
+//         state forward   S <- gamma_C S - S M + F     (S at each chunk's start)
+//         dL/dS backward  G <- gamma_C G - G M' + F'   (G at each chunk's end)
+//   out   (all chunks at once): E = E0 - ZK S^T, dU = dU0 + ZW G^T, then
+//         o = diag(gamma) Q S^T + P E and the gradients of q, k, v, g, b from
+//         S, G, E and dU of the chunk.
+// (S M = (ZK S^T)^T W and G M' = (diag(gamma b) ZW G^T)^T K: the recurrences
+// are the state and gradient updates S <- gamma_C S + E^T W and
+// G <- gamma_C G + (gamma dO)^T Q - (gamma b dU)^T K with E and dU expanded.)
+// The chains carry one 128 x 128 product group per chunk; everything else is
 // parallel over chunks.  Products are tcgen05.mma on bf16 operands with fp32
-// accumulators; solves and states are fp32.  The per-element decay
-// factors exp(c_t - c_s) use the fast __expf (a few ulp), far below the
-// bf16 rounding of the products' operands.
+// accumulators; where an operand carries the chain's state or its input term
+// it is split into bf16 hi + lo parts, so the recurrences lose no more than
+// one bf16 rounding of M, M' per chunk.  Solves and states are fp32.  The
+// per-element decay factors exp(c_t - c_s) use the fast __expf (a few ulp),
+// far below the bf16 rounding of the products' operands.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -31,13 +39,56 @@ namespace ls {
 namespace {
 using namespace gdn;
 
-// float32 scratch per (member, head, chunk): the [128 x 128] blocks below,
-// then the packed GK.
-enum : int { kE0 = 0, kZK, kDU0, kZW, kEblk, kDUblk, kSstart, kGend, kGKblk, kScrBlocks };
-constexpr int64_t kScrFloats = (int64_t)kScrBlocks * kTileElems;
+// float32 scratch per (member, head, chunk), in [128 x 128] blocks:
+//   kE0, kDU0       E0 and dU0 (prep)
+//   kSstart, kGend  S at the chunk's start, G = dL/dS at its end (chain)
+//   kEblk, kDUblk   E and dU (out, for its own later passes)
+//   kGKblk          the packed GK (prep); its last float holds gamma_C
+// then bf16 tile images of 32 KB in the swizzled shared-memory layout, so a
+// plain copy lands them ready for the MMAs: ZK, ZW, -M, F hi, F lo, -M',
+// F' hi, F' lo (rows as in the formulas above).
+enum : int { kE0 = 0, kDU0, kSstart, kGend, kEblk, kDUblk, kGKblk, kFloatBlocks };
+enum : int { kImZK = 0, kImZW, kImM, kImFhi, kImFlo, kImMg, kImFghi, kImFglo, kImages };
+constexpr int64_t kImgFloats = kTile / 4;
+constexpr int64_t kScrFloats = (int64_t)kFloatBlocks * kTileElems + kImages * kImgFloats;
+constexpr int64_t kGammaAt = (int64_t)kGKblk * kTileElems + kTileElems - 1;
 
 __device__ __forceinline__ float* scratch_of(float* scr, int H, int nch, int m, int h, int ch) {
   return scr + (((int64_t)m * H + h) * nch + ch) * kScrFloats;
+}
+__device__ __forceinline__ float* image_of(float* blk, int i) {
+  return blk + (int64_t)kFloatBlocks * kTileElems + i * kImgFloats;
+}
+// 16-byte groups gq0 .. gq0+ngq-1 of row r of a bf16 tile, from 8 ngq fp32
+// values: into the shared-memory tile at `tile` when to_smem, and into the
+// same place of a tile image in global memory when img is given.
+__device__ __forceinline__ void put_tile_row(bool to_smem, uint32_t tile, float* img, int r, const float* x,
+                                             int gq0, int ngq) {
+  for (int gq = gq0; gq < gq0 + ngq; ++gq) {
+    const uint4 pk = pack8(x + 8 * (gq - gq0));
+    if (to_smem) st_shared_v4(tile + tile_off(r, gq), pk);
+    if (img) *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(img) + tile_off(r, gq)) = pk;
+  }
+}
+// bf16 hi and lo parts of 8 values: hi = bf16(x), lo = bf16(x - hi).
+__device__ __forceinline__ void split8(const float* x, float* hi, float* lo) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    hi[u] = __uint_as_float((uint32_t)bf16_of(x[u]) << 16);
+    lo[u] = x[u] - hi[u];
+  }
+}
+// A 32 KB tile image from global memory into shared memory (128 threads).
+__device__ __forceinline__ void copy_image(uint32_t tile, const float* img) {
+  const uint4* src = reinterpret_cast<const uint4*>(img);
+#pragma unroll 1
+  for (int i0 = 0; i0 < 16; i0 += 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = src[threadIdx.x + kThr * (i0 + j)];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) st_shared_v4(tile + 16u * (threadIdx.x + kThr * (i0 + j)), v[j]);
+  }
 }
 
 // Cumulative log-decay and write strength of the chunk's tokens into sc[],
@@ -137,9 +188,10 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   float* sbt = sc + kC;    // b
   float* sbg = sbt + kC;   // b gamma
   float* swk = sbg + kC;   // w (zero past the response)
-  float* swt = swk + kC;   // 8 floats of scan scratch
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kPrepMisc + 2560);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 4);
+  float* sgm = swk + kC;   // gamma
+  float* swt = sgm + kC;   // 8 floats of scan scratch
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kPrepMisc + 2624);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 6);
   uint32_t* abort_s = tslot + 1;
 
   const int ch = blockIdx.x, h = blockIdx.y, m = blockIdx.z, tid = threadIdx.x, warp = tid >> 5;
@@ -153,7 +205,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   }
   float* out = scratch_of(scr, H, nch, m, h, ch);
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    for (int i = 0; i < 6; ++i) mbar_init(smem_u32(&bars[i]), 1);
     *abort_s = 0;
     fence_mbar_init();
   }
@@ -180,8 +232,10 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   __syncthreads();
   if (!grpA) {  // the right-hand sides' row scales (read after the next block barrier)
     const float ct = sc[gt], clast = sc[kC - 1];
-    sbg[gt] = sbt[gt] * __expf(ct);
+    sgm[gt] = __expf(ct);
+    sbg[gt] = sbt[gt] * sgm[gt];
     swk[gt] = gt < nt ? __expf(clast - ct) : 0.f;
+    if (gt == 0) out[kGammaAt] = expf(clast);  // gamma_C for the chains
   }
 
   if (tid == 0) {  // K K^T -> cols 0..127, K Q^T -> 128..255
@@ -345,24 +399,104 @@ __global__ void __launch_bounds__(kPrepThr, 1)
       }
       ok = mbar_wait_warp(smem_u32(&bars[2]), 0, abortp);
       if (!__syncthreads_or(!ok)) {
-        // warps 0-3: E0 and ZK (columns 0..255); warps 4-7: dU0 and ZW
+        // ---- E0, ZK (warps 0-3) and dU0, ZW (warps 4-7): E0 and dU0 to the
+        // scratch in fp32; bf16 tiles of E0 (R0), ZK (R3), -gamma b dU0 (R4)
+        // and ZW (R5) for the chains' terms, ZK and ZW also as images for out
         tc_fence_after();
-        float* wscr = reinterpret_cast<float*>(sm + kPrepR0) + warp * 32 * 33;
-        const int r0w = (warp & 3) * 32;
+        const int r = gt;  // row = token
+        float* fdst = out + (int64_t)(grpA ? kE0 : kDU0) * kTileElems + r * kD;
+        const uint32_t tA = sb + (grpA ? kPrepR0 : kPrepR4), tB = sb + (grpA ? kPrepR3 : kPrepR5);
+        float* img = image_of(out, grpA ? kImZK : kImZW);
+        const float fa = grpA ? 1.f : -sbg[r];
+        const uint32_t colA = grpA ? 0 : 256;
 #pragma unroll 1
-        for (int bi = 0; bi < 2; ++bi) {
-          const int blkid = grpA ? (bi == 0 ? kE0 : kZK) : (bi == 0 ? kDU0 : kZW);
-          const uint32_t col = (grpA ? 0 : 256) + bi * 128;
-          float* dst = out + (int64_t)blkid * kTileElems + r0w * kD;
+        for (int cb = 0; cb < 4; ++cb) {
+          uint32_t t32[32];
+          float f[32];
+          tmem_ld32(tb + lane_off + colA + cb * 32, t32);
+          tmem_wait_ld_r(t32);
+#pragma unroll
+          for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
+          float4* fd = reinterpret_cast<float4*>(fdst + cb * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) fd[q4] = make_float4(f[4 * q4], f[4 * q4 + 1], f[4 * q4 + 2], f[4 * q4 + 3]);
+#pragma unroll
+          for (int xx = 0; xx < 32; ++xx) f[xx] *= fa;
+          put_tile_row(true, tA, nullptr, r, f, cb * 4, 4);
+          tmem_ld32(tb + lane_off + colA + 128 + cb * 32, t32);
+          tmem_wait_ld_r(t32);
+#pragma unroll
+          for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
+          put_tile_row(true, tB, img, r, f, cb * 4, 4);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+          tc_fence_after();
+          mma_group_amn(tb + 0, sb + kPrepR3, sb + kPrepR2, true, false);    // M = ZK^T W
+          mma_group_amn(tb + 128, sb + kPrepR0, sb + kPrepR2, true, false);  // F = E0^T W
+          mma_group_amn(tb + 256, sb + kPrepR5, sb + kPrepR1, true, false);  // M' = ZW^T diag(b gamma) K
+          mma_commit(smem_u32(&bars[3]));
+        }
+        ok = mbar_wait_warp(smem_u32(&bars[3]), 0, abortp);
+        if (!__syncthreads_or(!ok)) {
+          // Q (R0), K (R1), gamma dO (R2) for F'; meanwhile -M, F hi / lo
+          // (group A) and -M' (group B) to their images
+          tc_fence_after();
+          if (grpA) {
+            stage_rows<4>(sb + kPrepR0, q + row0, rs, nt, nullptr, gt);
+            stage_rows<4>(sb + kPrepR1, k + row0, rs, nt, nullptr, gt);
+          } else {
+            stage_rows<4>(sb + kPrepR2, d_o + row0, rs, nt, sgm, gt);
+          }
 #pragma unroll 1
           for (int cb = 0; cb < 4; ++cb) {
             uint32_t t32[32];
-            tmem_ld32(tb + lane_off + col + cb * 32, t32);
+            float f[32], hi[32], lo[32];
+            tmem_ld32(tb + lane_off + (grpA ? 0 : 256) + cb * 32, t32);
             tmem_wait_ld_r(t32);
-            float f32[32];
 #pragma unroll
-            for (int xx = 0; xx < 32; ++xx) f32[xx] = __uint_as_float(t32[xx]);
-            rows_store32(f32, dst + cb * 32, kD, 32, wscr);
+            for (int xx = 0; xx < 32; ++xx) f[xx] = -__uint_as_float(t32[xx]);
+            put_tile_row(false, 0, image_of(out, grpA ? kImM : kImMg), r, f, cb * 4, 4);
+            if (grpA) {
+              tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
+              tmem_wait_ld_r(t32);
+#pragma unroll
+              for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
+#pragma unroll
+              for (int gg = 0; gg < 4; ++gg) split8(&f[8 * gg], &hi[8 * gg], &lo[8 * gg]);
+              put_tile_row(false, 0, image_of(out, kImFhi), r, hi, cb * 4, 4);
+              put_tile_row(false, 0, image_of(out, kImFlo), r, lo, cb * 4, 4);
+            }
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncthreads();
+          if (tid == 0) {  // F' = (gamma dO)^T Q - (gamma b dU0)^T K -> cols 384..511
+            tc_fence_after();
+            mma_group_amn(tb + 384, sb + kPrepR2, sb + kPrepR0, true, false);
+            mma_group_amn(tb + 384, sb + kPrepR4, sb + kPrepR1, true, true);
+            mma_commit(smem_u32(&bars[4]));
+          }
+          ok = mbar_wait_warp(smem_u32(&bars[4]), 0, abortp);
+          if (!__syncthreads_or(!ok)) {
+            // F' hi / lo: group A columns 0..63, group B 64..127
+            tc_fence_after();
+#pragma unroll 1
+            for (int cb = 0; cb < 2; ++cb) {
+              const int c0 = (grpA ? 0 : 64) + cb * 32;
+              uint32_t t32[32];
+              float f[32], hi[32], lo[32];
+              tmem_ld32(tb + lane_off + 384 + c0, t32);
+              tmem_wait_ld_r(t32);
+#pragma unroll
+              for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
+#pragma unroll
+              for (int gg = 0; gg < 4; ++gg) split8(&f[8 * gg], &hi[8 * gg], &lo[8 * gg]);
+              put_tile_row(false, 0, image_of(out, kImFghi), r, hi, c0 / 8, 4);
+              put_tile_row(false, 0, image_of(out, kImFglo), r, lo, c0 / 8, 4);
+            }
           }
         }
       }
@@ -370,8 +504,8 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   }
   if (__syncthreads_or(!ok) && tid == 0 && status) atomicOr(status, kStatusTimeout);
   if (tid == 0) {  // drain before tensor memory is freed
-    mma_commit(smem_u32(&bars[3]));
-    mbar_wait(smem_u32(&bars[3]), 0, abortp);
+    mma_commit(smem_u32(&bars[5]));
+    mbar_wait(smem_u32(&bars[5]), 0, abortp);
   }
   tc_fence_before();
   __syncthreads();
@@ -382,256 +516,159 @@ __global__ void __launch_bounds__(kPrepThr, 1)
 }
 
 // ---------------------------------------------------------------- chain
-// One CTA per (head, member), sequential over the chunks: the state forward,
-// then dL/dS backward.  Per chunk it writes S at the chunk's start, G at its
-// end, E and dU into the scratch.
-constexpr uint32_t kChT0 = 0, kChT1 = kTile, kChT2 = 2 * kTile, kChT3 = 3 * kTile;
-constexpr uint32_t kChT4 = 4 * kTile, kChT5 = 5 * kTile, kChMisc = 6 * kTile;
-constexpr uint32_t kChainSmem = kChMisc + 2048 + 1024;
+// One CTA per (head, member), sequential over the chunks: the state forward
+// S <- gamma_C S + D (writing S at each chunk's start), then dL/dS backward
+// G <- gamma_C G + D (writing G at each chunk's end), with one product group
+// per chunk, D = S_hi (-M) + S_lo (-M) + I F_hi + I F_lo (S split into bf16
+// hi + lo, the identity as A).  The chunk's three tiles come from prep's
+// images by bulk copy; the next chunk's copies start as soon as the current
+// chunk's products have read theirs.  256 threads: thread (x, half) keeps
+// columns 64 half .. 64 half + 63 of state row x.
+constexpr uint32_t kChI = 0, kChShi = kTile, kChSlo = 2 * kTile, kChM = 3 * kTile,
+                   kChFhi = 4 * kTile, kChFlo = 5 * kTile, kChMisc = 6 * kTile;
+constexpr uint32_t kChainSmem = kChMisc + 1024 + 1024;
+constexpr int kChThr = 2 * kThr;
 
-__global__ void __launch_bounds__(kThr, 1)
-    gdn_cp_chain_kernel(int H, int R, int nch, const float* __restrict__ s0,
-                        const float* __restrict__ q, const float* __restrict__ k,
-                        const float* __restrict__ g, const float* __restrict__ beta,
-                        const float* __restrict__ d_o, float* __restrict__ scr,
+__global__ void __launch_bounds__(kChThr, 1)
+    gdn_cp_chain_kernel(int H, int nch, const float* __restrict__ s0, float* __restrict__ scr,
                         float* __restrict__ s_final, uint32_t* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(sm);
-  float* sc = reinterpret_cast<float*>(sm + kChMisc);
-  float* sbt = sc + kC;
-  float* swt = sbt + kC;
-  float* sw = swt + 4;  // w_t (state pass) or gamma_t (gradient pass), zero past the response
-  // the barriers sit past sw (which ends at byte 1552 of the misc area)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kChMisc + 1600);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kChMisc);  // copies, products, drain
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
   uint32_t* abort_s = tslot + 1;
+  uint32_t* never_s = tslot + 2;  // stays 0: the drain's waits are bounded by time alone
 
   const int h = blockIdx.x, m = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
-  {
-    const int64_t tok = (int64_t)m * R * H;
-    q += tok * kD, k += tok * kD, d_o += tok * kD, g += tok, beta += tok;
-  }
+  const int x = tid & (kThr - 1), half = tid >> 7, c0 = 64 * half, gq0 = 8 * half;
   if (tid == 0) {
     for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&bars[i]), 1);
     *abort_s = 0;
+    *never_s = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(smem_u32(tslot), 512);
+    tmem_alloc(smem_u32(tslot), 128);
     tmem_relinquish();
+  }
+#pragma unroll 1
+  for (int gq = gq0; gq < gq0 + 8; ++gq) {  // the identity, row x
+    float e[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) e[u] = 8 * gq + u == x ? 1.f : 0.f;
+    st_shared_v4(sb + kChI + tile_off(x, gq), pack8(e));
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tb = *tslot, lane_off = (uint32_t)(warp * 32) << 16;
+  const uint32_t tb = *tslot, lane_off = (uint32_t)((warp & 3) * 32) << 16;
   const volatile uint32_t* abortp = abort_s;
-  const int64_t rs = (int64_t)H * kD;
-  const int x = tid;  // state row i / token row t / column, by phase
-  uint32_t n0 = 0, n1 = 0;  // completed phases of bars[0], bars[1]
+  uint32_t ncp = 0, nmm = 0;  // completed phases of the copy and product barriers
+  int pend = -1;              // thread 0: parity of a copy phase given up on
   bool ok = true;
 
-  float st[kD];  // S (state pass), then G (gradient pass): row x, fp32
+  // chunk visited at step i of the 2 nch steps: forward, then backward
+  auto chunk_at = [&](int i) { return i < nch ? i : 2 * nch - 1 - i; };
+  auto issue = [&](int i) {  // thread 0: the three tiles of step i
+    float* blk = scratch_of(scr, H, nch, m, h, chunk_at(i));
+    const bool bw = i >= nch;
+    const uint32_t bar = smem_u32(&bars[0]);
+    mbar_expect_tx(bar, 3 * kTile);
+    bulk_load(sb + kChM, image_of(blk, bw ? kImMg : kImM), kTile, bar);
+    bulk_load(sb + kChFhi, image_of(blk, bw ? kImFghi : kImFhi), kTile, bar);
+    bulk_load(sb + kChFlo, image_of(blk, bw ? kImFglo : kImFlo), kTile, bar);
+  };
+  if (tid == 0) issue(0);
+
+  float st[64];  // S (forward), then G (backward): row x, columns c0 .. c0+63, fp32
   {
-    const float4* src = reinterpret_cast<const float4*>(s0 + ((int64_t)h * kD + x) * kD);
+    const float4* src = reinterpret_cast<const float4*>(s0 + ((int64_t)h * kD + x) * kD + c0);
 #pragma unroll
-    for (int c = 0; c < kD / 4; ++c) {
+    for (int c = 0; c < 16; ++c) {
       const float4 a4 = src[c];
       st[4 * c] = a4.x, st[4 * c + 1] = a4.y, st[4 * c + 2] = a4.z, st[4 * c + 3] = a4.w;
     }
   }
-  // ---- state forward
-  for (int ch = 0; ok && ch < nch; ++ch) {
-    const int64_t t0 = (int64_t)ch * kC;
-    const int nt = R - t0 < kC ? (int)(R - t0) : kC;
-    float* blk = scratch_of(scr, H, nch, m, h, ch);
-    {
-      // each thread's own row, in 16-byte pieces: the stores are not waited
-      // on, and this sequential kernel runs faster with them than with a
-      // staged transpose
-      float4* dst = reinterpret_cast<float4*>(blk + (int64_t)kSstart * kTileElems + x * kD);
+  for (int i = 0; ok && i < 2 * nch; ++i) {
+    const bool bw = i >= nch;
+    if (i == nch) {
+      if (s_final) {
+        float4* dst = reinterpret_cast<float4*>(s_final + (((int64_t)m * H + h) * kD + x) * kD + c0);
 #pragma unroll
-      for (int c = 0; c < kD / 4; ++c) dst[c] = make_float4(st[4 * c], st[4 * c + 1], st[4 * c + 2], st[4 * c + 3]);
-    }
-    stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
-    __syncthreads();
-    sw[x] = x < nt ? expf(sc[kC - 1] - sc[x]) : 0.f;
-    __syncthreads();
-    stage_row_regs(sb + kChT0, x, st);                                         // S (bf16)
-    stage_rows<4>(sb + kChT1, blk + (int64_t)kZK * kTileElems, kD, kC, nullptr);  // ZK
-    stage_rows<4>(sb + kChT2, k + (t0 * H + h) * kD, rs, nt, sw);                 // W = diag(w) K
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {  // ZK S^T -> cols 0..127
-      tc_fence_after();
-      mma_group(tb + 0, sb + kChT1, sb + kChT0, false, false);
-      mma_commit(smem_u32(&bars[0]));
-    }
-    ok = mbar_wait_warp(smem_u32(&bars[0]), n0++ & 1, abortp);
-    if (__syncthreads_or(!ok)) break;
-    tc_fence_after();
-    {  // E row x = E0 row x - (ZK S^T) row x; E^T column x as bf16
-      const float4* e0 = reinterpret_cast<const float4*>(blk + (int64_t)kE0 * kTileElems + x * kD);
-      float4* eo = reinterpret_cast<float4*>(blk + (int64_t)kEblk * kTileElems + x * kD);
-#pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t t32[32];
-        float e[32];
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 a4 = e0[cb * 8 + q4];
-          e[4 * q4] = a4.x, e[4 * q4 + 1] = a4.y, e[4 * q4 + 2] = a4.z, e[4 * q4 + 3] = a4.w;
-        }
-        tmem_ld32(tb + lane_off + cb * 32, t32);
-        tmem_wait_ld_r(t32);
-#pragma unroll
-        for (int xx = 0; xx < 32; ++xx) {
-          e[xx] -= __uint_as_float(t32[xx]);
-          st_shared_u16(sb + kChT3 + elem_off(cb * 32 + xx, x), bf16_of(e[xx]));
-        }
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4)
-          eo[cb * 8 + q4] = make_float4(e[4 * q4], e[4 * q4 + 1], e[4 * q4 + 2], e[4 * q4 + 3]);
+        for (int c = 0; c < 16; ++c) dst[c] = make_float4(st[4 * c], st[4 * c + 1], st[4 * c + 2], st[4 * c + 3]);
       }
+#pragma unroll
+      for (int c = 0; c < 64; ++c) st[c] = 0.f;
+    }
+    float* blk = scratch_of(scr, H, nch, m, h, chunk_at(i));
+    const float gc = blk[kGammaAt];
+    {  // S at the chunk's start / G at its end, row x
+      float4* dst = reinterpret_cast<float4*>(blk + (int64_t)(bw ? kGend : kSstart) * kTileElems + x * kD + c0);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) dst[c] = make_float4(st[4 * c], st[4 * c + 1], st[4 * c + 2], st[4 * c + 3]);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float hi[8], lo[8];
+      split8(&st[8 * j], hi, lo);
+      st_shared_v4(sb + kChShi + tile_off(x, gq0 + j), pack8(hi));
+      st_shared_v4(sb + kChSlo + tile_off(x, gq0 + j), pack8(lo));
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {  // E^T W -> cols 128..255 (W as an N-major B)
-      tc_fence_after();
-      mma_group(tb + 128, sb + kChT3, sb + kChT2, true, false);
-      mma_commit(smem_u32(&bars[1]));
-    }
-    ok = mbar_wait_warp(smem_u32(&bars[1]), n1++ & 1, abortp);
-    if (__syncthreads_or(!ok)) break;
-    tc_fence_after();
-    {
-      const float gl = expf(sc[kC - 1]);
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t t32[32];
-        tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
-        tmem_wait_ld_r(t32);
-#pragma unroll
-        for (int xx = 0; xx < 32; ++xx) st[cb * 32 + xx] = fmaf(gl, st[cb * 32 + xx], __uint_as_float(t32[xx]));
-      }
-    }
-    tc_fence_before();
-    __syncthreads();
-  }
-  if (ok && s_final) {
-    float4* dst = reinterpret_cast<float4*>(s_final + (((int64_t)m * H + h) * kD + x) * kD);
-#pragma unroll
-    for (int c = 0; c < kD / 4; ++c) dst[c] = make_float4(st[4 * c], st[4 * c + 1], st[4 * c + 2], st[4 * c + 3]);
-  }
-  // ---- dL/dS backward
-#pragma unroll
-  for (int c = 0; c < kD; ++c) st[c] = 0.f;
-  for (int ch = nch - 1; ok && ch >= 0; --ch) {
-    const int64_t t0 = (int64_t)ch * kC;
-    const int nt = R - t0 < kC ? (int)(R - t0) : kC;
-    float* blk = scratch_of(scr, H, nch, m, h, ch);
-    {
-      float4* dst = reinterpret_cast<float4*>(blk + (int64_t)kGend * kTileElems + x * kD);
-#pragma unroll
-      for (int c = 0; c < kD / 4; ++c) dst[c] = make_float4(st[4 * c], st[4 * c + 1], st[4 * c + 2], st[4 * c + 3]);
-    }
-    stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
-    __syncthreads();
-    sw[x] = expf(sc[x]);
-    __syncthreads();
-    stage_row_regs(sb + kChT0, x, st);                                         // G (bf16)
-    stage_rows<4>(sb + kChT1, blk + (int64_t)kZW * kTileElems, kD, kC, nullptr);  // ZW
-    stage_rows<4>(sb + kChT2, q + (t0 * H + h) * kD, rs, nt, nullptr);            // Q
-    stage_rows<4>(sb + kChT3, k + (t0 * H + h) * kD, rs, nt, nullptr);            // K
-#pragma unroll 4
-    for (int gq = 0; gq < 16; ++gq) {  // (gamma dO)^T row x (tokens along K)
-      float f8[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int t = 8 * gq + u;
-        f8[u] = t < nt ? sw[t] * d_o[(t0 + t) * rs + h * kD + x] : 0.f;
-      }
-      st_shared_v4(sb + kChT4 + tile_off(x, gq), pack8(f8));
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {  // ZW G^T -> cols 0..127
-      tc_fence_after();
-      mma_group(tb + 0, sb + kChT1, sb + kChT0, false, false);
-      mma_commit(smem_u32(&bars[0]));
-    }
-    ok = mbar_wait_warp(smem_u32(&bars[0]), n0++ & 1, abortp);
-    if (__syncthreads_or(!ok)) break;
-    tc_fence_after();
-    {  // dU row x = dU0 row x + (ZW G^T) row x; -(gamma b dU)^T column x as bf16
-      const float4* u0 = reinterpret_cast<const float4*>(blk + (int64_t)kDU0 * kTileElems + x * kD);
-      float4* uo = reinterpret_cast<float4*>(blk + (int64_t)kDUblk * kTileElems + x * kD);
-      const float f = -sw[x] * sbt[x];
-#pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t t32[32];
-        float du[32];
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 a4 = u0[cb * 8 + q4];
-          du[4 * q4] = a4.x, du[4 * q4 + 1] = a4.y, du[4 * q4 + 2] = a4.z, du[4 * q4 + 3] = a4.w;
+    if (warp == 0) {
+      const bool got = mbar_wait_warp(smem_u32(&bars[0]), ncp & 1, abortp);
+      if (tid == 0) {
+        if (got) {
+          tc_fence_after();
+          mma_group(tb, sb + kChShi, sb + kChM, true, false);
+          mma_group(tb, sb + kChSlo, sb + kChM, true, true);
+          mma_group(tb, sb + kChI, sb + kChFhi, true, true);
+          mma_group(tb, sb + kChI, sb + kChFlo, true, true);
+          mma_commit(smem_u32(&bars[1]));
+        } else {
+          pend = (int)(ncp & 1);
+          *abort_s = 1u;
         }
-        tmem_ld32(tb + lane_off + cb * 32, t32);
-        tmem_wait_ld_r(t32);
-#pragma unroll
-        for (int xx = 0; xx < 32; ++xx) {
-          du[xx] += __uint_as_float(t32[xx]);
-          st_shared_u16(sb + kChT5 + elem_off(cb * 32 + xx, x), bf16_of(f * du[xx]));
-        }
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4)
-          uo[cb * 8 + q4] = make_float4(du[4 * q4], du[4 * q4 + 1], du[4 * q4 + 2], du[4 * q4 + 3]);
       }
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {  // (gamma dO)^T Q - (gamma b dU)^T K -> cols 128..255
-      tc_fence_after();
-      mma_group(tb + 128, sb + kChT4, sb + kChT2, true, false);
-      mma_group(tb + 128, sb + kChT5, sb + kChT3, true, true);
-      mma_commit(smem_u32(&bars[1]));
-    }
-    ok = mbar_wait_warp(smem_u32(&bars[1]), n1++ & 1, abortp);
+    ++ncp;
+    ok = mbar_wait_warp(smem_u32(&bars[1]), nmm++ & 1, abortp);
     if (__syncthreads_or(!ok)) break;
+    if (tid == 0 && i + 1 < 2 * nch) issue(i + 1);  // the products have read this step's tiles
     tc_fence_after();
-    {
-      const float gl = expf(sc[kC - 1]);
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t t32[32];
-        tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
-        tmem_wait_ld_r(t32);
+    for (int cb = 0; cb < 2; ++cb) {
+      uint32_t t32[32];
+      tmem_ld32(tb + lane_off + c0 + cb * 32, t32);
+      tmem_wait_ld_r(t32);
 #pragma unroll
-        for (int xx = 0; xx < 32; ++xx) st[cb * 32 + xx] = fmaf(gl, st[cb * 32 + xx], __uint_as_float(t32[xx]));
-      }
+      for (int xx = 0; xx < 32; ++xx) st[cb * 32 + xx] = fmaf(gc, st[cb * 32 + xx], __uint_as_float(t32[xx]));
     }
     tc_fence_before();
-    __syncthreads();
   }
   if (!ok && tid == 0 && status) atomicOr(status, kStatusTimeout);
-  if (tid == 0) {
+  if (tid == 0) {  // drain the products, and a copy given up on, before the CTA ends
     mma_commit(smem_u32(&bars[2]));
-    mbar_wait(smem_u32(&bars[2]), 0, abortp);
+    mbar_wait(smem_u32(&bars[2]), 0, never_s);
+    if (pend >= 0) mbar_wait(smem_u32(&bars[0]), (uint32_t)pend, never_s);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tb, 512);
+    tmem_dealloc(tb, 128);
   }
 }
 
 // ---------------------------------------------------------------- out
-// One CTA per (chunk, head, member): the output o and the gradients of the
-// chunk's q, k, v, g, b from S (start), G (end), E and dU of the chunk.
+// One CTA per (chunk, head, member): first E = E0 - ZK S^T and
+// dU = dU0 + ZW G^T of the chunk (into the scratch), then the output o and
+// the gradients of the chunk's q, k, v, g, b from S (start), G (end), E and
+// dU.
 //   o   = diag(gamma) Q S^T + P E
 //   dQ  = diag(gamma) dO S + LdP K,            LdP = lower(Gamma . dP), dP = dO E^T
 //   dK  = LdP^T Q + Msym K - diag(gamma b) dU S + diag(w) E G,
@@ -667,7 +704,7 @@ __global__ void __launch_bounds__(kThr, 1)
   float* rcol = sw + kC;
   float* swt = rcol + kC;  // 8 floats of scan and reduction scratch
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOutMisc + 3584);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 5);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 6);
   uint32_t* abort_s = tslot + 1;
 
   const int ch = blockIdx.x, h = blockIdx.y, m = blockIdx.z, tid = threadIdx.x, warp = tid >> 5;
@@ -684,11 +721,11 @@ __global__ void __launch_bounds__(kThr, 1)
   float* blk = scratch_of(scr, H, nch, m, h, ch);
   const float* Sst = blk + (int64_t)kSstart * kTileElems;
   const float* Gen = blk + (int64_t)kGend * kTileElems;
-  const float* Eb = blk + (int64_t)kEblk * kTileElems;
-  const float* dUb = blk + (int64_t)kDUblk * kTileElems;
+  float* Eb = blk + (int64_t)kEblk * kTileElems;
+  float* dUb = blk + (int64_t)kDUblk * kTileElems;
   const float* gkb = blk + (int64_t)kGKblk * kTileElems;
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    for (int i = 0; i < 6; ++i) mbar_init(smem_u32(&bars[i]), 1);
     *abort_s = 0;
     fence_mbar_init();
   }
@@ -709,10 +746,48 @@ __global__ void __launch_bounds__(kThr, 1)
   const int64_t wrow = ((t0 + r0) * H + h) * kD;  // row r0 of q, k, v, d_o, o, dq, dk, dv
   bool ok = true;
 
+  // ---- round 0: ZK S^T -> T0, ZW G^T -> T1; E and dU rows into the scratch
+  copy_image(S0, image_of(blk, kImZK));
+  copy_image(S1, image_of(blk, kImZW));
+  stage_rows(S2, Sst, kD, kD, nullptr);
+  stage_rows(S3, Gen, kD, kD, nullptr);
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    tc_fence_after();
+    mma_group(tb + 0, S0, S2, false, false);
+    mma_group(tb + 128, S1, S3, false, false);
+    mma_commit(smem_u32(&bars[5]));
+  }
+  ok = mbar_wait_warp(smem_u32(&bars[5]), 0, abortp);
+  if (!__syncthreads_or(!ok)) {
+    tc_fence_after();
+    const float* e0b = blk + (int64_t)kE0 * kTileElems;
+    const float* du0b = blk + (int64_t)kDU0 * kTileElems;
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+      uint32_t t32[32];
+      float f32[32];
+      rows_load32(f32, e0b + r0 * kD + cb * 32, kD, 32, wscr);
+      tmem_ld32(tb + lane_off + 0 + cb * 32, t32);
+      tmem_wait_ld_r(t32);
+#pragma unroll
+      for (int xx = 0; xx < 32; ++xx) f32[xx] -= __uint_as_float(t32[xx]);
+      rows_store32(f32, Eb + r0 * kD + cb * 32, kD, 32, wscr);
+      rows_load32(f32, du0b + r0 * kD + cb * 32, kD, 32, wscr);
+      tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
+      tmem_wait_ld_r(t32);
+#pragma unroll
+      for (int xx = 0; xx < 32; ++xx) f32[xx] += __uint_as_float(t32[xx]);
+      rows_store32(f32, dUb + r0 * kD + cb * 32, kD, 32, wscr);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();  // E and dU rows written before any thread reads them back
+
   // ---- round 1: Q K^T -> T0, Q S^T -> T1, K S^T -> T2
   stage_rows(S0, q + (t0 * H + h) * kD, rs, nt, nullptr);
   stage_rows(S1, k + (t0 * H + h) * kD, rs, nt, nullptr);
-  stage_rows(S2, Sst, kD, kD, nullptr);
   stage_rows(S3, Eb, kD, kC, nullptr);
   stage_rows(S4, d_o + (t0 * H + h) * kD, rs, nt, nullptr);
   stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
@@ -729,7 +804,7 @@ __global__ void __launch_bounds__(kThr, 1)
     mma_group(tb + 256, S1, S2, false, false);
     mma_commit(smem_u32(&bars[0]));
   }
-  ok = mbar_wait_warp(smem_u32(&bars[0]), 0, abortp);
+  if (ok) ok = mbar_wait_warp(smem_u32(&bars[0]), 0, abortp);
   float dgam = 0.f, dbt = 0.f, rrow = 0.f, rw = 0.f;
   if (!__syncthreads_or(!ok)) {
     tc_fence_after();
@@ -1041,8 +1116,7 @@ cudaError_t launch_gdn_cp_bwd(int B, int H, int R, const float* s0, const float*
   gdn_cp_prep_kernel<<<dim3(nch, H, B), kPrepThr, kPrepSmem, st>>>(H, R, nch, q, k, v, g, beta, d_o, ws,
                                                               status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  gdn_cp_chain_kernel<<<dim3(H, B), kThr, kChainSmem, st>>>(H, R, nch, s0, q, k, g, beta, d_o, ws,
-                                                           nullptr, status);
+  gdn_cp_chain_kernel<<<dim3(H, B), kChThr, kChainSmem, st>>>(H, nch, s0, ws, nullptr, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gdn_cp_out_kernel<<<dim3(nch, H, B), kThr, kOutSmem, st>>>(H, R, nch, q, k, v, g, beta, d_o, ws,
                                                             nullptr, dq, dk, dv, dg, dbeta, status);

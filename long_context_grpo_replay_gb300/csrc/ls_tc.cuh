@@ -116,6 +116,16 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
+// Untiled bulk copy from global to shared memory (cp.async.bulk): both
+// addresses 16-byte aligned, bytes a multiple of 16; completes `bytes` of
+// transaction on bar.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- TMEM
 // Warp-wide: allocates ncols columns (power of two >= 32) and writes the base
 // address to shared memory at dst.

@@ -441,4 +441,16 @@ inline void tma_load(uint32_t dst, const TensorMap* m, uint32_t bar, const int32
   });
 }
 
+// Untiled bulk copy (cp.async.bulk): bytes land unchanged at dst.
+inline void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  if (dst % 16 || reinterpret_cast<uintptr_t>(src) % 16 || bytes % 16 || bytes == 0)
+    die("bulk copy: addresses and size must be 16-byte multiples", dst, bytes);
+  smem_ptr(dst, 16);
+  smem_ptr(dst + bytes - 16, 16);  // the whole destination inside shared memory
+  g_block->copy.push([=] {
+    std::memcpy(smem_ptr(dst, 16), src, bytes);
+    mbar_complete_tx(bar, bytes);
+  });
+}
+
 }  // namespace emu

@@ -54,6 +54,9 @@ inline void mma_commit(uint32_t bar) { emu::mma_commit(bar); }
 inline void mbar_arrive(uint32_t bar) { emu::mbar_arrive(bar); }
 inline void mbar_expect_tx(uint32_t bar, uint32_t bytes) { emu::mbar_expect_tx(bar, bytes); }
 inline void prefetch_tmap(const CUtensorMap*) {}
+inline void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  emu::bulk_load(dst, src, bytes, bar);
+}
 inline void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t c0, int32_t c1) {
   const int32_t c[2] = {c0, c1};
   emu::tma_load(dst, m, bar, c);

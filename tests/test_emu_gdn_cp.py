@@ -19,7 +19,28 @@ EMU = Path(__file__).resolve().parent / "emu"
 CSRC = ROOT / "long_context_grpo_replay_gb300" / "csrc"
 SRC = CSRC / "ls_gdn_cp.cu"
 TOL_BF16 = 2e-2
-SCR_BLOCKS = 9  # E0, ZK, dU0, ZW, E, dU, S_start, G_end, GK
+# scratch per chunk: float32 [128 x 128] blocks E0, dU0, S_start, G_end, E,
+# dU, GK; then bf16 tile images (32 KB, the swizzled shared-memory layout)
+# ZK, ZW, -M, F hi, F lo, -M', F' hi, F' lo
+FLOAT_BLOCKS, IMAGES = 7, 8
+B_E0, B_DU0, B_SSTART, B_GEND, B_E, B_DU = range(6)
+I_ZK, I_ZW, I_M, I_FHI, I_FLO, I_MG, I_FGHI, I_FGLO = range(8)
+SCR_FLOATS = FLOAT_BLOCKS * 128 * 128 + IMAGES * 8192
+
+
+def block(chunk, i):
+    return chunk[i * 16384:(i + 1) * 16384].reshape(128, 128)
+
+
+def image(chunk, i):
+    """A bf16 tile image decoded: element (r, c) sits in 64-column box c // 64,
+    row r at 128 bytes per row, its 16-byte group XOR-ed with r mod 8."""
+    raw = chunk[FLOAT_BLOCKS * 16384 + i * 8192:FLOAT_BLOCKS * 16384 + (i + 1) * 8192]
+    u16 = raw.view(np.uint16)
+    r = np.arange(128)[:, None]
+    c = np.arange(128)[None, :]
+    off = (c // 64) * 16384 + r * 128 + ((((c % 64) // 8) ^ (r % 8)) << 4) + (c % 8) * 2
+    return (u16[off // 2].astype(np.uint32) << 16).view(np.float32)
 
 
 def build(d):
@@ -54,9 +75,9 @@ def run(exe, d, c, stage):
     assert r.returncode == 0, r.stderr[-2000:]
     nch = -(-R // 128)
     out = np.fromfile(d / "out.bin", dtype=np.float32, offset=4)
-    n_scr = B * H * nch * SCR_BLOCKS * 128 * 128
+    n_scr = B * H * nch * SCR_FLOATS
     status = int(np.fromfile(d / "out.bin", dtype=np.uint32, count=1)[0])
-    scr = out[:n_scr].reshape(B, H, nch, SCR_BLOCKS, 128, 128)
+    scr = out[:n_scr].reshape(B, H, nch, SCR_FLOATS)
     return status, scr, out[n_scr:]
 
 
@@ -70,6 +91,17 @@ def rel(a, b):
     return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-30))
 
 
+def _chain_terms(K, Q, dO, g, b, E0, ZK, dU0, ZW):
+    """The chains' per-chunk terms from the chunk-local solves (float64):
+    M = ZK^T W, F = E0^T W, M' = ZW^T diag(gamma b) K,
+    F' = (gamma dO)^T Q - (gamma b dU0)^T K."""
+    c = np.cumsum(g)
+    gam = np.exp(c)
+    W = np.exp(c[-1] - c)[:, None] * K
+    return (ZK.T @ W, E0.T @ W, ZW.T @ ((gam * b)[:, None] * K),
+            (gam[:, None] * dO).T @ Q - ((gam * b)[:, None] * dU0).T @ K)
+
+
 def test_prep_solves_match_the_reference(emulator):
     exe, d = emulator
     B, H, R = 1, 2, 200  # two chunks, the second partial
@@ -77,20 +109,30 @@ def test_prep_solves_match_the_reference(emulator):
     status, scr, _ = run(exe, d, c, "prep")
     assert status == 0
     a = {x: t.numpy().astype(np.float64) for x, t in c.items()}
-    errs = []
+    errs = {}
     for h in range(H):
         for ch, (t0, t1) in enumerate([(0, 128), (128, 200)]):
             sl = slice(t0, t1)
-            want = _cp_prep(a["k"][0, sl, h], a["q"][0, sl, h], a["v"][0, sl, h], a["d_o"][0, sl, h],
-                            a["g"][0, sl, h], a["beta"][0, sl, h])
+            args = [a[x][0, sl, h] for x in ("k", "q", "v", "d_o", "g", "beta")]
+            E0, ZK, dU0, ZW = _cp_prep(*args)
+            M, F, Mg, Fg = _chain_terms(args[0], args[1], args[3], args[4], args[5], E0, ZK, dU0, ZW)
             n = t1 - t0
-            for blk, w in zip(range(4), want):
-                got = scr[0, h, ch, blk, :n]
-                errs.append(rel(got, w))
-                assert rel(got, w) <= TOL_BF16, (h, ch, blk, rel(got, w))
-                if n < 128:
-                    assert np.abs(scr[0, h, ch, blk, n:]).max() == 0.0  # rows past the response
-    print("prep max rel err", max(errs))
+            sc = scr[0, h, ch]
+            got = {"E0": block(sc, B_E0), "dU0": block(sc, B_DU0), "ZK": image(sc, I_ZK),
+                   "ZW": image(sc, I_ZW), "M": -image(sc, I_M),
+                   "F": image(sc, I_FHI).astype(np.float64) + image(sc, I_FLO),
+                   "Mg": -image(sc, I_MG),
+                   "Fg": image(sc, I_FGHI).astype(np.float64) + image(sc, I_FGLO)}
+            want = {"E0": E0, "dU0": dU0, "ZK": ZK, "ZW": ZW, "M": M, "F": F, "Mg": Mg, "Fg": Fg}
+            for name, w in want.items():
+                gv = got[name] if name in ("M", "F", "Mg", "Fg") else got[name][:n]
+                errs[name] = max(errs.get(name, 0.0), rel(gv, w))
+                if n < 128 and name in ("E0", "dU0", "ZK", "ZW"):
+                    assert np.abs(got[name][n:]).max() == 0.0, name  # rows past the response
+    print("prep max rel errs", errs)
+    assert all(e <= TOL_BF16 for e in errs.values()), errs
+    assert abs(scr[0, 0, 1, FLOAT_BLOCKS * 16384 - 1] -
+               np.exp(a["g"][0, 128:200, 0].sum())) < 1e-5  # gamma_C of the partial chunk
 
 
 def _chains(s0, q, k, v, g, b, d_o):
@@ -118,6 +160,8 @@ def _chains(s0, q, k, v, g, b, d_o):
 
 
 def test_chains_match_the_reference(emulator):
+    """S at each chunk's start and G at its end (chain), E and dU (out), over
+    three chunks, the last partial."""
     exe, d = emulator
     B, H, R = 2, 1, 300  # three chunks, the last partial; two members share s0
     c = inputs.make_gdn_group(B, H, R, seed=32)
@@ -131,9 +175,10 @@ def test_chains_match_the_reference(emulator):
                                                a["d_o"][m, :, 0])
         for ch in range(3):
             n = min(128, R - 128 * ch)
-            for name, blk, want in (("S_start", 6, S_start[ch]), ("E", 4, E[ch][:n]),
-                                    ("G_end", 7, G_end[ch]), ("dU", 5, dU[ch][:n])):
-                got = scr[m, 0, ch, blk] if name in ("S_start", "G_end") else scr[m, 0, ch, blk, :n]
+            for name, blk, want in (("S_start", B_SSTART, S_start[ch]), ("E", B_E, E[ch][:n]),
+                                    ("G_end", B_GEND, G_end[ch]), ("dU", B_DU, dU[ch][:n])):
+                got = block(scr[m, 0, ch], blk)
+                got = got if name in ("S_start", "G_end") else got[:n]
                 if np.abs(want).max() == 0:
                     assert np.abs(got).max() == 0, name
                     continue

@@ -272,32 +272,55 @@ def _cp_prep(K, Q, V, dO, g, b):
             np.linalg.solve(IA.T, Pt @ dO), np.linalg.solve(IA.T, W))
 
 
-def _chunk_parallel(s0, q, k, v, g, b, d_o, C):
+def _chunk_parallel(s0, q, k, v, g, b, d_o, C, chains="explicit"):
     """The replay and its gradients in three stages: chunk-local solves (all
     chunks independent), then the two linear chains over the chunks (the state
     forward, E = E0 - ZK S^T, S <- gamma_C S + E^T W; dL/dS backward,
     dU = dU0 + ZW G^T, G <- gamma_C G + (gamma dO)^T Q - (gamma b dU)^T K),
     then every output chunk by chunk from its starting state, its final dL/dS,
-    E and dU (independent again)."""
+    E and dU (independent again).  chains="affine" runs the same chains with
+    E and dU expanded into per-chunk terms formed beforehand:
+    S <- gamma_C S - S M + F, G <- gamma_C G - G M' + F', with M = ZK^T W,
+    F = E0^T W, M' = ZW^T diag(gamma b) K, F' = (gamma dO)^T Q - (gamma b dU0)^T K;
+    E and dU then come from S and G chunk by chunk."""
     R = len(g)
     chunks = [(a, min(R, a + C)) for a in range(0, R, C)]
     pre = [_cp_prep(k[a:e], q[a:e], v[a:e], d_o[a:e], g[a:e], b[a:e]) for a, e in chunks]
     S, S_start, E = s0.copy(), [], []
-    for (a, e), (E0, ZK, _, _) in zip(chunks, pre):
-        S_start.append(S)
-        c = np.cumsum(g[a:e])
-        E.append(E0 - ZK @ S.T)
-        S = np.exp(c[-1]) * S + E[-1].T @ (np.exp(c[-1] - c)[:, None] * k[a:e])
-    out = {"s_final": S}
-    G, G_end, dU = np.zeros_like(S), [None] * len(chunks), [None] * len(chunks)
-    for ci in reversed(range(len(chunks))):
-        a, e = chunks[ci]
-        G_end[ci] = G
-        c = np.cumsum(g[a:e])
-        gam = np.exp(c)
-        dU[ci] = pre[ci][2] + pre[ci][3] @ G.T
-        G = np.exp(c[-1]) * G + (gam[:, None] * d_o[a:e]).T @ q[a:e] - \
-            ((gam * b[a:e])[:, None] * dU[ci]).T @ k[a:e]
+    G, G_end, dU = np.zeros_like(s0), [None] * len(chunks), [None] * len(chunks)
+    if chains == "affine":
+        terms = []
+        for (a, e), (E0, ZK, dU0, ZW) in zip(chunks, pre):
+            c = np.cumsum(g[a:e])
+            gam, W = np.exp(c), np.exp(c[-1] - c)[:, None] * k[a:e]
+            gb = (gam * b[a:e])[:, None]
+            terms.append((np.exp(c[-1]), ZK.T @ W, E0.T @ W, ZW.T @ (gb * k[a:e]),
+                          (gam[:, None] * d_o[a:e]).T @ q[a:e] - (gb * dU0).T @ k[a:e]))
+        for (a, e), (E0, ZK, _, _), (gc, M, F, _, _) in zip(chunks, pre, terms):
+            S_start.append(S)
+            E.append(E0 - ZK @ S.T)
+            S = gc * S - S @ M + F
+        out = {"s_final": S}
+        for ci in reversed(range(len(chunks))):
+            gc, _, _, Mg, Fg = terms[ci]
+            G_end[ci] = G
+            dU[ci] = pre[ci][2] + pre[ci][3] @ G.T
+            G = gc * G - G @ Mg + Fg
+    else:
+        for (a, e), (E0, ZK, _, _) in zip(chunks, pre):
+            S_start.append(S)
+            c = np.cumsum(g[a:e])
+            E.append(E0 - ZK @ S.T)
+            S = np.exp(c[-1]) * S + E[-1].T @ (np.exp(c[-1] - c)[:, None] * k[a:e])
+        out = {"s_final": S}
+        for ci in reversed(range(len(chunks))):
+            a, e = chunks[ci]
+            G_end[ci] = G
+            c = np.cumsum(g[a:e])
+            gam = np.exp(c)
+            dU[ci] = pre[ci][2] + pre[ci][3] @ G.T
+            G = np.exp(c[-1]) * G + (gam[:, None] * d_o[a:e]).T @ q[a:e] - \
+                ((gam * b[a:e])[:, None] * dU[ci]).T @ k[a:e]
     res = {x: np.zeros_like(t) for x, t in (("o", v), ("dq", q), ("dk", k), ("dv", v),
                                              ("dg", g), ("dbeta", b))}
     for ci, (a, e) in enumerate(chunks):
@@ -330,11 +353,12 @@ def _chunk_parallel(s0, q, k, v, g, b, d_o, C):
     return out
 
 
+@pytest.mark.parametrize("chains", ["explicit", "affine"])
 @pytest.mark.parametrize("C", [1, 4, 8, 23])
-def test_chunk_parallel_form_equals_the_oracle(C):
+def test_chunk_parallel_form_equals_the_oracle(C, chains):
     s0, q, k, v, g, b, d_o = _case(H=1, dk=6, dv=5, R=23, seed=2, unit_k=False)
     want = gdn_replay(s0, q, k, v, g, b, d_o)
-    got = _chunk_parallel(s0[0], q[:, 0], k[:, 0], v[:, 0], g[:, 0], b[:, 0], d_o[:, 0], C)
+    got = _chunk_parallel(s0[0], q[:, 0], k[:, 0], v[:, 0], g[:, 0], b[:, 0], d_o[:, 0], C, chains)
     for x in ("o", "dq", "dk", "dv", "dg", "dbeta"):
         np.testing.assert_allclose(got[x], want[x][:, 0], atol=1e-10, err_msg=x)
     np.testing.assert_allclose(got["s_final"], want["s_final"][0], atol=1e-10)
