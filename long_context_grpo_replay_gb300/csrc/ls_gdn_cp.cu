@@ -78,17 +78,33 @@ __device__ __forceinline__ void split8(const float* x, float* hi, float* lo) {
     lo[u] = x[u] - hi[u];
   }
 }
-// A 32 KB tile image from global memory into shared memory (128 threads).
-__device__ __forceinline__ void copy_image(uint32_t tile, const float* img) {
+// A 32 KB tile image from global memory into shared memory, by the 128
+// threads whose index among them is tid.
+__device__ __forceinline__ void copy_image(uint32_t tile, const float* img, int tid) {
   const uint4* src = reinterpret_cast<const uint4*>(img);
 #pragma unroll 1
   for (int i0 = 0; i0 < 16; i0 += 8) {
     uint4 v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = src[threadIdx.x + kThr * (i0 + j)];
+    for (int j = 0; j < 8; ++j) v[j] = src[tid + kThr * (i0 + j)];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) st_shared_v4(tile + 16u * (threadIdx.x + kThr * (i0 + j)), v[j]);
+    for (int j = 0; j < 8; ++j) st_shared_v4(tile + 16u * (tid + kThr * (i0 + j)), v[j]);
   }
+}
+// 32 consecutive floats of one row, 16-byte pieces (zeros when !valid).
+__device__ __forceinline__ void row_ld32(float* v, const float* p, bool valid) {
+  const float4* p4 = reinterpret_cast<const float4*>(p);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 a = valid ? p4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[4 * i] = a.x, v[4 * i + 1] = a.y, v[4 * i + 2] = a.z, v[4 * i + 3] = a.w;
+  }
+}
+__device__ __forceinline__ void row_st32(const float* v, float* p, bool valid) {
+  if (!valid) return;
+  float4* p4 = reinterpret_cast<float4*>(p);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) p4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
 // Cumulative log-decay and write strength of the chunk's tokens into sc[],
@@ -220,6 +236,10 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   const volatile uint32_t* abortp = abort_s;
   const int64_t rs = (int64_t)H * kD;  // token stride of q, k, v, d_o
   const int64_t row0 = (t0 * H + h) * kD;
+  if (gt < nt) {  // the chunk's rows, asked into L2 up front (q and k are read twice)
+    prefetch_l2((grpA ? k : v) + row0 + gt * rs, kD * 4);
+    prefetch_l2((grpA ? q : d_o) + row0 + gt * rs, kD * 4);
+  }
 
   if (grpA) {
     stage_rows<4>(sb + kPrepR0, k + row0, rs, nt, nullptr, gt);
@@ -680,10 +700,13 @@ __global__ void __launch_bounds__(kChThr, 1)
 //         dgamma = rowsum(dO . Q S^T) - rowsum(b . dU . K S^T),
 //         and dc_last += sum(rw) + gamma_C <G, S>.
 constexpr uint32_t kOutMisc = 6 * kTile;
-constexpr uint32_t kOutRowScr = kOutMisc + 4096;  // per-warp row scratch (rows_load32 / rows_store32)
-constexpr uint32_t kOutSmem = kOutRowScr + kRowScrFloats * 4 + 1024;
+constexpr uint32_t kOutSmem = kOutMisc + 6144 + 1024;
+constexpr int kOutThr = 2 * kThr;
 
-__global__ void __launch_bounds__(kThr, 1)
+// 256 threads: thread (t, hf) owns token row t and the column half
+// 64 hf .. 64 hf + 63 (column blocks cb = 2 hf, 2 hf + 1) in every epilogue;
+// the row sums of the two halves meet in shared memory at the end.
+__global__ void __launch_bounds__(kOutThr, 1)
     gdn_cp_out_kernel(int H, int R, int nch, const float* __restrict__ q,
                       const float* __restrict__ k, const float* __restrict__ v,
                       const float* __restrict__ g, const float* __restrict__ beta,
@@ -702,14 +725,15 @@ __global__ void __launch_bounds__(kThr, 1)
   float* sgam = sbt + kC;
   float* sw = sgam + kC;
   float* rcol = sw + kC;
-  float* swt = rcol + kC;  // 8 floats of scan and reduction scratch
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOutMisc + 3584);
+  float* part = rcol + kC;     // [5][128] row sums of the second column half
+  float* swt = part + 5 * kC;  // 8 floats of scan and reduction scratch
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOutMisc + 5184);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 6);
   uint32_t* abort_s = tslot + 1;
 
   const int ch = blockIdx.x, h = blockIdx.y, m = blockIdx.z, tid = threadIdx.x, warp = tid >> 5;
   const int lane = tid & 31;
-  float* wscr = reinterpret_cast<float*>(sm + kOutRowScr) + warp * 32 * 33;
+  const int t = tid & (kThr - 1), hf = tid >> 7, cb0 = 2 * hf;  // row, column half
   const int64_t t0 = (int64_t)ch * kC;
   const int nt = R - t0 < kC ? (int)(R - t0) : kC;
   {
@@ -736,21 +760,29 @@ __global__ void __launch_bounds__(kThr, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tb = *tslot, lane_off = (uint32_t)(warp * 32) << 16;
+  const uint32_t tb = *tslot, lane_off = (uint32_t)((warp & 3) * 32) << 16;
   const volatile uint32_t* abortp = abort_s;
   const int64_t rs = (int64_t)H * kD;
-  const int t = tid;  // token row in the epilogues
   const bool live = t < nt;
-  const int r0 = warp * 32;          // first row of this warp's 32
-  const int nvw = nt - r0;           // rows of the warp inside the response
-  const int64_t wrow = ((t0 + r0) * H + h) * kD;  // row r0 of q, k, v, d_o, o, dq, dk, dv
+  const int r0 = (warp & 3) * 32;  // first row of this warp's 32
+  const int64_t row0 = (t0 * H + h) * kD;
+  const int64_t rowt = ((t0 + t) * H + h) * kD;  // row t of q, k, v, d_o, o, dq, dk, dv
   bool ok = true;
 
+  // everything this CTA reads, asked into L2 up front: rows of q, k, v, dO
+  // and the chunk's scratch blocks
+  if (live) {
+    prefetch_l2((hf ? v : q) + rowt, kD * 4);
+    prefetch_l2((hf ? d_o : k) + rowt, kD * 4);
+  }
+  if (tid == 0) {
+    prefetch_l2(blk, 4 * kTileElems * 4);                             // E0, dU0, S, G
+    prefetch_l2(blk + (int64_t)kGKblk * kTileElems, kTileElems * 4);  // GK
+    prefetch_l2(image_of(blk, kImZK), 2 * kTile);                      // ZK, ZW
+  }
   // ---- round 0: ZK S^T -> T0, ZW G^T -> T1; E and dU rows into the scratch
-  copy_image(S0, image_of(blk, kImZK));
-  copy_image(S1, image_of(blk, kImZW));
-  stage_rows(S2, Sst, kD, kD, nullptr);
-  stage_rows(S3, Gen, kD, kD, nullptr);
+  copy_image(hf ? S1 : S0, image_of(blk, hf ? kImZW : kImZK), t);
+  stage_rows<4>(hf ? S3 : S2, hf ? Gen : Sst, kD, kD, nullptr, t);
   fence_proxy_async_smem();
   __syncthreads();
   if (tid == 0) {
@@ -762,39 +794,44 @@ __global__ void __launch_bounds__(kThr, 1)
   ok = mbar_wait_warp(smem_u32(&bars[5]), 0, abortp);
   if (!__syncthreads_or(!ok)) {
     tc_fence_after();
-    const float* e0b = blk + (int64_t)kE0 * kTileElems;
-    const float* du0b = blk + (int64_t)kDU0 * kTileElems;
+    const float* e0r = blk + (int64_t)kE0 * kTileElems + t * kD;
+    const float* du0r = blk + (int64_t)kDU0 * kTileElems + t * kD;
 #pragma unroll 1
-    for (int cb = 0; cb < 4; ++cb) {
+    for (int cb = cb0; cb < cb0 + 2; ++cb) {
       uint32_t t32[32];
       float f32[32];
-      rows_load32(f32, e0b + r0 * kD + cb * 32, kD, 32, wscr);
+      row_ld32(f32, e0r + cb * 32, true);
       tmem_ld32(tb + lane_off + 0 + cb * 32, t32);
       tmem_wait_ld_r(t32);
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) f32[xx] -= __uint_as_float(t32[xx]);
-      rows_store32(f32, Eb + r0 * kD + cb * 32, kD, 32, wscr);
-      rows_load32(f32, du0b + r0 * kD + cb * 32, kD, 32, wscr);
+      row_st32(f32, Eb + t * kD + cb * 32, true);
+      row_ld32(f32, du0r + cb * 32, true);
       tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
       tmem_wait_ld_r(t32);
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) f32[xx] += __uint_as_float(t32[xx]);
-      rows_store32(f32, dUb + r0 * kD + cb * 32, kD, 32, wscr);
+      row_st32(f32, dUb + t * kD + cb * 32, true);
     }
   }
   tc_fence_before();
   __syncthreads();  // E and dU rows written before any thread reads them back
 
   // ---- round 1: Q K^T -> T0, Q S^T -> T1, K S^T -> T2
-  stage_rows(S0, q + (t0 * H + h) * kD, rs, nt, nullptr);
-  stage_rows(S1, k + (t0 * H + h) * kD, rs, nt, nullptr);
-  stage_rows(S3, Eb, kD, kC, nullptr);
-  stage_rows(S4, d_o + (t0 * H + h) * kD, rs, nt, nullptr);
+  if (hf == 0) {
+    stage_rows<4>(S0, q + row0, rs, nt, nullptr, t);
+    stage_rows<4>(S1, k + row0, rs, nt, nullptr, t);
+  } else {
+    stage_rows<4>(S3, Eb, kD, kC, nullptr, t);
+    stage_rows<4>(S4, d_o + row0, rs, nt, nullptr, t);
+  }
   stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
   __syncthreads();
-  sgam[t] = expf(sc[t]);
-  sw[t] = live ? expf(sc[kC - 1] - sc[t]) : 0.f;
-  rcol[t] = 0.f;
+  if (hf == 0) {
+    sgam[t] = expf(sc[t]);
+    sw[t] = live ? expf(sc[kC - 1] - sc[t]) : 0.f;
+    rcol[t] = 0.f;
+  }
   fence_proxy_async_smem();
   __syncthreads();
   if (tid == 0) {
@@ -805,12 +842,12 @@ __global__ void __launch_bounds__(kThr, 1)
     mma_commit(smem_u32(&bars[0]));
   }
   if (ok) ok = mbar_wait_warp(smem_u32(&bars[0]), 0, abortp);
-  float dgam = 0.f, dbt = 0.f, rrow = 0.f, rw = 0.f;
+  float dgam = 0.f, dbt = 0.f, rrow = 0.f, rw = 0.f;  // this half's parts of the row sums
   if (!__syncthreads_or(!ok)) {
     tc_fence_after();
     const float ct = sc[t], gt = sgam[t], bt = sbt[t];
 #pragma unroll 1
-    for (int cb = 0; cb < 4; ++cb) {
+    for (int cb = cb0; cb < cb0 + 2; ++cb) {
       uint32_t t32[32];
       float f32[32], ra[32], rb[32];
       // P row t (bf16 tile S5: the A operand of P E, and read back for r)
@@ -824,7 +861,7 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
       for (int gg = 0; gg < 4; ++gg) st_shared_v4(S5 + tile_off(t, cb * 4 + gg), pack8(&f32[8 * gg]));
       // Q S^T row t: dgamma, and T1 scaled by gamma_t for o = gamma Q S^T + P E
-      rows_load32(ra, d_o + wrow + cb * 32, rs, nvw, wscr);
+      row_ld32(ra, d_o + rowt + cb * 32, live);
       tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
       tmem_wait_ld_r(t32);
 #pragma unroll
@@ -835,8 +872,8 @@ __global__ void __launch_bounds__(kThr, 1)
       }
       tmem_st32(tb + lane_off + 128 + cb * 32, t32);
       // K S^T row t: db (dU . X) and dgamma (- b dU . K S^T)
-      rows_load32(ra, dUb + r0 * kD + cb * 32, kD, 32, wscr);
-      rows_load32(rb, v + wrow + cb * 32, rs, nvw, wscr);
+      row_ld32(ra, dUb + t * kD + cb * 32, true);
+      row_ld32(rb, v + rowt + cb * 32, live);
       tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
       tmem_wait_ld_r(t32);
       if (live) {
@@ -853,8 +890,7 @@ __global__ void __launch_bounds__(kThr, 1)
     tc_fence_before();
     __syncthreads();
     // ---- round 2: P E -> T1 (onto gamma Q S^T), dO E^T -> T0, dU E^T -> T2, E G -> T3
-    stage_rows(S0, dUb, kD, kC, nullptr);
-    stage_rows(S1, Gen, kD, kD, nullptr);
+    stage_rows<4>(hf ? S1 : S0, hf ? Gen : dUb, kD, kC, nullptr, t);
     fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {
@@ -871,7 +907,7 @@ __global__ void __launch_bounds__(kThr, 1)
     tc_fence_after();
     const float ct = sc[t], bt = sbt[t], gt = sgam[t], wt = sw[t];
 #pragma unroll 1
-    for (int cb = 0; cb < 4; ++cb) {
+    for (int cb = cb0; cb < cb0 + 2; ++cb) {
       uint32_t t32[32];
       float f32[32], rv[32];
       // o row t
@@ -880,7 +916,7 @@ __global__ void __launch_bounds__(kThr, 1)
       if (o) {
 #pragma unroll
         for (int xx = 0; xx < 32; ++xx) f32[xx] = __uint_as_float(t32[xx]);
-        rows_store32(f32, o + wrow + cb * 32, rs, nvw, wscr);
+        row_st32(f32, o + rowt + cb * 32, live);
       }
       // P row t, back from the bf16 tile S5 (before LdP overwrites the row)
 #pragma unroll
@@ -907,6 +943,7 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
       for (int gg = 0; gg < 4; ++gg) st_shared_v4(S5 + tile_off(t, cb * 4 + gg), pack8(&f32[8 * gg]));
       // dA row t = -strict_lower(dU E^T): db, r, and Msym (both triangles) into S3
+      const float* gkr = gkb + a_at(t, cb * 32);  // GK row t from column cb*32 (used where s < t)
       tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
       tmem_wait_ld_r(t32);
 #pragma unroll
@@ -915,7 +952,7 @@ __global__ void __launch_bounds__(kThr, 1)
         float mk = 0.f;
         if (s < t) {
           const float da = -__uint_as_float(t32[xx]);
-          const float gkv = gkb[a_at(t, s)];
+          const float gkv = gkr[xx];
           dbt = fmaf(da, gkv, dbt);
           rv[xx] = fmaf(da * bt, gkv, rv[xx]);
           mk = da * bt * __expf(ct - sc[s]);
@@ -932,39 +969,37 @@ __global__ void __launch_bounds__(kThr, 1)
       for (int xx = 0; xx < 32; ++xx) rrow += rv[xx];
       atomicAdd(&rcol[cb * 32 + lane], warp_colsum32(rv));
       // E G row t: rw = w . rowsum(E G . K)
-      rows_load32(f32, k + wrow + cb * 32, rs, nvw, wscr);
+      row_ld32(f32, k + rowt + cb * 32, live);
       tmem_ld32(tb + lane_off + 384 + cb * 32, t32);
       tmem_wait_ld_r(t32);
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) rw = fmaf(__uint_as_float(t32[xx]), f32[xx], rw);  // 0 past R
     }
     rw *= wt;
-    // dO tile rows scaled by gamma for dQ; K back into S1; dV
-    {
+    // dO tile rows scaled by gamma for dQ; dV
 #pragma unroll
-      for (int gq = 0; gq < 16; ++gq) {
-        const uint32_t ad = S4 + tile_off(t, gq);
-        const uint4 pk = ld_shared_v4(ad);
-        const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
-        float f8[8];
+    for (int gq = 8 * hf; gq < 8 * hf + 8; ++gq) {
+      const uint32_t ad = S4 + tile_off(t, gq);
+      const uint4 pk = ld_shared_v4(ad);
+      const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
+      float f8[8];
 #pragma unroll
-        for (int i2 = 0; i2 < 4; ++i2) {
-          const float2 f = unpack_bf16x2(w4[i2]);
-          f8[2 * i2] = f.x * gt, f8[2 * i2 + 1] = f.y * gt;
-        }
-        st_shared_v4(ad, pack8(f8));
+      for (int i2 = 0; i2 < 4; ++i2) {
+        const float2 f = unpack_bf16x2(w4[i2]);
+        f8[2 * i2] = f.x * gt, f8[2 * i2 + 1] = f.y * gt;
       }
+      st_shared_v4(ad, pack8(f8));
+    }
 #pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
-        float u[32];
-        rows_load32(u, dUb + r0 * kD + cb * 32, kD, 32, wscr);
+    for (int cb = cb0; cb < cb0 + 2; ++cb) {
+      float u[32];
+      row_ld32(u, dUb + t * kD + cb * 32, true);
 #pragma unroll
-        for (int xx = 0; xx < 32; ++xx) u[xx] *= bt;
-        rows_store32(u, dv + wrow + cb * 32, rs, nvw, wscr);
-      }
+      for (int xx = 0; xx < 32; ++xx) u[xx] *= bt;
+      row_st32(u, dv + rowt + cb * 32, live);
     }
     __syncthreads();
-    stage_rows(S1, k + (t0 * H + h) * kD, rs, nt, nullptr);
+    stage_rows<4, kOutThr>(S1, k + row0, rs, nt, nullptr, tid);  // K back into S1
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -979,30 +1014,25 @@ __global__ void __launch_bounds__(kThr, 1)
   }
   if (!__syncthreads_or(!ok)) {
     tc_fence_after();
+    const float f = -sgam[t] * sbt[t];
 #pragma unroll 1
-    for (int cb = 0; cb < 4; ++cb) {
+    for (int cb = cb0; cb < cb0 + 2; ++cb) {
       uint32_t t32[32];
       float f32[32];
       tmem_ld32(tb + lane_off + 0 + cb * 32, t32);
       tmem_wait_ld_r(t32);
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) f32[xx] = __uint_as_float(t32[xx]);
-      rows_store32(f32, dq + wrow + cb * 32, rs, nvw, wscr);
-    }
-    // Q into S4, -(gamma b) dU into S5 for dK
-    {
-      const float f = -sgam[t] * sbt[t];
-#pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
-        float u[32];
-        rows_load32(u, dUb + r0 * kD + cb * 32, kD, 32, wscr);
+      row_st32(f32, dq + rowt + cb * 32, live);
+      // -(gamma b) dU into S5 for dK
+      row_ld32(f32, dUb + t * kD + cb * 32, true);
 #pragma unroll
-        for (int xx = 0; xx < 32; ++xx) u[xx] *= f;
+      for (int xx = 0; xx < 32; ++xx) f32[xx] *= f;
 #pragma unroll
-        for (int gg = 0; gg < 4; ++gg) st_shared_v4(S5 + tile_off(t, cb * 4 + gg), pack8(&u[8 * gg]));
-      }
+      for (int gg = 0; gg < 4; ++gg) st_shared_v4(S5 + tile_off(t, cb * 4 + gg), pack8(&f32[8 * gg]));
     }
-    stage_rows(S4, q + (t0 * H + h) * kD, rs, nt, nullptr);
+    __syncthreads();  // S5 rows of both halves written; dQ read out of T0
+    stage_rows<4, kOutThr>(S4, q + row0, rs, nt, nullptr, tid);  // Q into S4
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -1019,8 +1049,9 @@ __global__ void __launch_bounds__(kThr, 1)
   if (!__syncthreads_or(!ok)) {
     tc_fence_after();
     const float wt = sw[t];
+    float gs = 0.f;  // this half's part of <G, S> over row t
 #pragma unroll 1
-    for (int cb = 0; cb < 4; ++cb) {
+    for (int cb = cb0; cb < cb0 + 2; ++cb) {
       uint32_t a32[32], b32[32];
       float f32[32];
       tmem_ld32(tb + lane_off + 256 + cb * 32, a32);
@@ -1029,46 +1060,63 @@ __global__ void __launch_bounds__(kThr, 1)
       reg_dep(b32);
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) f32[xx] = fmaf(wt, __uint_as_float(b32[xx]), __uint_as_float(a32[xx]));
-      rows_store32(f32, dk + wrow + cb * 32, rs, nvw, wscr);
-    }
-    // <G, S> over the block, then dc and its reverse cumulative sum
-    float gs = 0.f;
-#pragma unroll 1
-    for (int cb = 0; cb < 4; ++cb) {
+      row_st32(f32, dk + rowt + cb * 32, live);
       float ga[32], sa[32];
-      rows_load32(ga, Gen + r0 * kD + cb * 32, kD, 32, wscr);
-      rows_load32(sa, Sst + r0 * kD + cb * 32, kD, 32, wscr);
+      row_ld32(ga, Gen + t * kD + cb * 32, true);
+      row_ld32(sa, Sst + t * kD + cb * 32, true);
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) gs = fmaf(ga[xx], sa[xx], gs);
     }
-    float rws = rw;
+    // the second half's row sums to the first
+    if (hf) {
+      part[0 * kC + t] = dgam;
+      part[1 * kC + t] = dbt;
+      part[2 * kC + t] = rrow;
+      part[3 * kC + t] = rw;
+      part[4 * kC + t] = gs;
+    }
+    __syncthreads();
+    float rws = 0.f;
+    if (!hf) {
+      dgam += part[0 * kC + t];
+      dbt += part[1 * kC + t];
+      rrow += part[2 * kC + t];
+      rw += part[3 * kC + t];
+      gs += part[4 * kC + t];
+      rws = rw;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      gs += __shfl_xor_sync(0xffffffffu, gs, off);
-      rws += __shfl_xor_sync(0xffffffffu, rws, off);
+      for (int off = 16; off > 0; off >>= 1) {
+        gs += __shfl_xor_sync(0xffffffffu, gs, off);
+        rws += __shfl_xor_sync(0xffffffffu, rws, off);
+      }
+      if (lane == 0) {
+        swt[warp] = gs;
+        swt[4 + warp] = rws;
+      }
     }
     __syncthreads();
-    if (lane == 0) {
-      swt[warp] = gs;
-      swt[4 + warp] = rws;
-    }
-    __syncthreads();
-    float dc = dgam * sgam[t] + rrow - rcol[t] - rw;
-    if (t == kC - 1)
-      dc += (swt[4] + swt[5] + swt[6] + swt[7]) + sgam[kC - 1] * (swt[0] + swt[1] + swt[2] + swt[3]);
-    float x = dc;  // suffix sum within the warp
+    // dc and its reverse cumulative sum over the chunk (first half: one thread per row)
+    float x = 0.f;
+    if (!hf) {
+      float dc = dgam * sgam[t] + rrow - rcol[t] - rw;
+      if (t == kC - 1)
+        dc += (swt[4] + swt[5] + swt[6] + swt[7]) + sgam[kC - 1] * (swt[0] + swt[1] + swt[2] + swt[3]);
+      x = dc;  // suffix sum within the warp
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float y = __shfl_down_sync(0xffffffffu, x, off);
-      if (lane + off < 32) x += y;
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_down_sync(0xffffffffu, x, off);
+        if (lane + off < 32) x += y;
+      }
     }
     __syncthreads();
-    if (lane == 0) swt[warp] = x;  // the warp's total
+    if (!hf && lane == 0) swt[warp] = x;  // the warp's total
     __syncthreads();
-    for (int w = warp + 1; w < 4; ++w) x += swt[w];
-    if (live) {
-      dg[(t0 + t) * H + h] = x;
-      dbeta[(t0 + t) * H + h] = dbt;
+    if (!hf) {
+      for (int w = warp + 1; w < 4; ++w) x += swt[w];
+      if (live) {
+        dg[(t0 + t) * H + h] = x;
+        dbeta[(t0 + t) * H + h] = dbt;
+      }
     }
   }
   if (!ok && tid == 0 && status) atomicOr(status, kStatusTimeout);
@@ -1101,7 +1149,8 @@ cudaError_t launch_gdn_cp_bwd(int B, int H, int R, const float* s0, const float*
   if (B == 0 || H == 0 || R == 0) return cudaSuccess;
   if (H > 65535 || B > 65535) return cudaErrorInvalidValue;  // grid y and z
   for (const void* p : {(const void*)s0, (const void*)q, (const void*)k, (const void*)v,
-                        (const void*)d_o, (const void*)dq, (const void*)dk, (const void*)ws})
+                        (const void*)d_o, (const void*)dq, (const void*)dk, (const void*)dv,
+                        (const void*)ws})
     if (reinterpret_cast<uintptr_t>(p) & 15u) return cudaErrorMisalignedAddress;
   const int nch = (R + kC - 1) / kC;
   cudaError_t e;
@@ -1118,7 +1167,7 @@ cudaError_t launch_gdn_cp_bwd(int B, int H, int R, const float* s0, const float*
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gdn_cp_chain_kernel<<<dim3(H, B), kChThr, kChainSmem, st>>>(H, nch, s0, ws, nullptr, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  gdn_cp_out_kernel<<<dim3(nch, H, B), kThr, kOutSmem, st>>>(H, R, nch, q, k, v, g, beta, d_o, ws,
+  gdn_cp_out_kernel<<<dim3(nch, H, B), kOutThr, kOutSmem, st>>>(H, R, nch, q, k, v, g, beta, d_o, ws,
                                                             nullptr, dq, dk, dv, dg, dbeta, status);
   return cudaGetLastError();
 }

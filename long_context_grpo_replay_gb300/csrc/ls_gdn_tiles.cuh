@@ -44,17 +44,18 @@ __device__ __forceinline__ uint16_t bf16_of(float x) { return (uint16_t)(pack_bf
 // 128 threads.  The shared-memory stores are ordering points for the
 // compiler, so each batch of kBatch row pieces is loaded into registers
 // before any of it is stored: kBatch global loads in flight, not one.
-// tid: the caller's index among the 128 threads that stage the tile.
-template <int kBatch = 8>
+// tid: the caller's index among the kWorkers threads that stage the tile.
+template <int kBatch = 8, int kWorkers = kThr>
 __device__ __forceinline__ void stage_rows(uint32_t tile, const float* src, int64_t stride, int nt,
                                            const float* scale, int tid = threadIdx.x) {
-  static_assert(16 % kBatch == 0, "batch divides the 16 pieces per thread");
+  constexpr int kPer = 2048 / kWorkers;  // 16-byte pieces per thread
+  static_assert(kPer % kBatch == 0, "batch divides the pieces per thread");
 #pragma unroll 1
-  for (int it0 = 0; it0 < 16; it0 += kBatch) {
+  for (int it0 = 0; it0 < kPer; it0 += kBatch) {
     float4 a[kBatch], b[kBatch];
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
-      const int item = tid + kThr * (it0 + j), r = item >> 4, gq = item & 15;
+      const int item = tid + kWorkers * (it0 + j), r = item >> 4, gq = item & 15;
       a[j] = b[j] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (r < nt) {
         const float4* p = reinterpret_cast<const float4*>(src + r * stride + gq * 8);
@@ -63,7 +64,7 @@ __device__ __forceinline__ void stage_rows(uint32_t tile, const float* src, int6
     }
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
-      const int item = tid + kThr * (it0 + j), r = item >> 4, gq = item & 15;
+      const int item = tid + kWorkers * (it0 + j), r = item >> 4, gq = item & 15;
       const float f = (scale && r < nt) ? scale[r] : 1.f;
       const float x[8] = {a[j].x * f, a[j].y * f, a[j].z * f, a[j].w * f,
                           b[j].x * f, b[j].y * f, b[j].z * f, b[j].w * f};
@@ -123,6 +124,23 @@ __device__ __forceinline__ void rows_store32(const float* v, float* base, int64_
 #pragma unroll 4
   for (int r = 0; r < 32; ++r)
     if (r < nvalid) base[r * stride + lane] = scr[r * 33 + lane];
+  __syncwarp();
+}
+// The same for rows r0 .. r0+31 of a packed strict lower triangle (row t at
+// t (t - 1) / 2), columns c0 .. c0+31: v[c] = element (r0 + lane, c0 + c).
+// Entries on or above the diagonal come out as whatever the packing holds
+// there (the caller masks them); every read stays below row 128's start.
+__device__ __forceinline__ void rows_load32_packed(float* v, const float* packed, int r0, int c0,
+                                                   float* scr) {
+  const int lane = threadIdx.x & 31;
+  float tmp[32];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) tmp[r] = packed[(r0 + r) * (r0 + r - 1) / 2 + c0 + lane];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) scr[r * 33 + lane] = tmp[r];
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 32; ++c) v[c] = scr[lane * 33 + c];
   __syncwarp();
 }
 // Column sums of a [32 x 32] block held one row per lane (v[c] = column c of

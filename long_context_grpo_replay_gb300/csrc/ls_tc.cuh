@@ -126,6 +126,14 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// Asks for bytes (a multiple of 16) of global memory at p (16-byte aligned)
+// to be brought into L2 (cp.async.bulk.prefetch): a hint with no completion
+// to wait for and no registers held.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- TMEM
 // Warp-wide: allocates ncols columns (power of two >= 32) and writes the base
 // address to shared memory at dst.

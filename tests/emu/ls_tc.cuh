@@ -57,6 +57,9 @@ inline void prefetch_tmap(const CUtensorMap*) {}
 inline void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   emu::bulk_load(dst, src, bytes, bar);
 }
+inline void prefetch_l2(const void* p, uint32_t bytes) {  // a hint: only its arguments are checked
+  if (reinterpret_cast<uintptr_t>(p) % 16 || bytes % 16 || bytes == 0) emu::die("L2 prefetch arguments", bytes);
+}
 inline void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t c0, int32_t c1) {
   const int32_t c[2] = {c0, c1};
   emu::tma_load(dst, m, bar, c);
