@@ -939,7 +939,7 @@ def run_gdn(args):
     stream = torch.cuda.current_stream(dev)
 
     def step(x):
-        ls.ls_gdn_replay_fwd(x["s0"], x["q"], x["k"], x["v"], x["g"], x["beta"], o, s_final, stream,
+        ls.ls_gdn_replay_fwd(x["s0"], x["q"], x["k"], x["v"], x["g"], x["beta"], o, s_final, ws, stream,
                              precision=prec)
         ls.ls_gdn_replay_bwd(x["s0"], x["q"], x["k"], x["v"], x["g"], x["beta"], x["d_o"],
                              gr["dq"], gr["dk"], gr["dv"], gr["dg"], gr["dbeta"], ws, stream,

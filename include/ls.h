@@ -275,25 +275,26 @@ LS_API ls_status ls_stage_pages(const ls_attn_desc* desc, const void* k_src, con
  * ls_gdn_replay_fwd writes o and, if s_final is non-NULL, the state after the
  * last token.  ls_gdn_replay_bwd returns the gradient of sum(d_o * o) for q,
  * k, v, g and beta (same shapes); none is formed for s0 (the detached prompt
- * state).  It needs ls_gdn_workspace_size() bytes of workspace (256-byte
- * aligned, owned by the caller).  The workspace starts with the same 256-byte
- * device status word as the attention workspace: a bounded device wait that
- * ran out in the tensor-core path sets it, and ls_read_device_status(ws)
- * reports it.  resp_len == 0 or batch == 0 is a no-op (the forward still
+ * state).  The backward, and the forward with LS_GDN_TENSOR_CORE, need
+ * ls_gdn_workspace_size() bytes of workspace (256-byte aligned, owned by the
+ * caller; the forward with LS_GDN_EXACT takes ws = NULL, ws_bytes = 0, and
+ * ignores a workspace it is given).  The workspace starts with the same
+ * 256-byte device status word as the attention workspace: a bounded device
+ * wait that ran out in the tensor-core path sets it, and
+ * ls_read_device_status(ws) reports it (the outputs of that call are then
+ * not to be used).  resp_len == 0 or batch == 0 is a no-op (the forward still
  * copies s0 to s_final when R = 0).
  *
  * precision selects the kernels (a zeroed desc selects the exact path):
  *   LS_GDN_EXACT        float32 recurrence, one token at a time; about 1e-7
  *                       relative error, held to 1e-5 against the float64
  *                       oracle.
- *   LS_GDN_TENSOR_CORE  the chunkwise forward and the chunk-parallel
- *                       backward on tcgen05 tensor cores with bf16 operands
- *                       and float32 accumulation; about 5e-3 relative error,
- *                       held to 2e-2 (the bf16 bar).  s0, q, k, v, d_o and
- *                       the outputs must be 16-byte aligned (else
- *                       LS_ERR_CUDA).
- *                       If a bounded device wait gives up in the forward, o
- *                       and s_final of that (member, head) are set to NaN.
+ *   LS_GDN_TENSOR_CORE  the chunk-parallel forward and backward (chunks of
+ *                       128 tokens) on tcgen05 tensor cores with bf16
+ *                       operands and float32 accumulation; about 5e-3
+ *                       relative error, held to 2e-2 (the bf16 bar).  s0, q,
+ *                       k, v, d_o and the outputs must be 16-byte aligned
+ *                       (else LS_ERR_CUDA).
  * Float32 callers that need the 1e-5 result keep LS_GDN_EXACT.
  * Errors: LS_ERR_UNSUPPORTED for other dk/dv, LS_ERR_INVALID_ARGUMENT for
  * NULL buffers, negative sizes or an unknown precision,
@@ -312,7 +313,7 @@ LS_API ls_status ls_gdn_workspace_size(const ls_gdn_desc* desc, int32_t resp_len
 LS_API ls_status ls_gdn_replay_fwd(const ls_gdn_desc* desc, const float* s0, const float* q,
                                    const float* k, const float* v, const float* g,
                                    const float* beta, int32_t resp_len, float* o, float* s_final,
-                                   void* stream);
+                                   void* ws, size_t ws_bytes, void* stream);
 LS_API ls_status ls_gdn_replay_bwd(const ls_gdn_desc* desc, const float* s0, const float* q,
                                    const float* k, const float* v, const float* g,
                                    const float* beta, const float* d_o, int32_t resp_len,

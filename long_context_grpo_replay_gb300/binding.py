@@ -117,7 +117,7 @@ def lib() -> ctypes.CDLL:
         "ls_replay_bwd_part": [ctypes.POINTER(AttnDesc), ctypes.POINTER(PromptKV), P, P, P, P, P, P,
                                I32, I32, P, P, P, P, SZ, P],
         "ls_gdn_workspace_size": [ctypes.POINTER(GdnDesc), I32, ctypes.POINTER(SZ)],
-        "ls_gdn_replay_fwd": [ctypes.POINTER(GdnDesc), P, P, P, P, P, P, I32, P, P, P],
+        "ls_gdn_replay_fwd": [ctypes.POINTER(GdnDesc), P, P, P, P, P, P, I32, P, P, P, SZ, P],
         "ls_gdn_replay_bwd": [ctypes.POINTER(GdnDesc), P, P, P, P, P, P, P, I32, P, P, P, P, P, P,
                               SZ, P],
         "ls_stage_pages": [ctypes.POINTER(AttnDesc), P, P, I64, P, I64, I32, P, P, P, SZ, P],
@@ -301,14 +301,16 @@ def ls_gdn_workspace_size(desc, resp_len) -> int:
     return out.value
 
 
-def ls_gdn_replay_fwd(s0, q, k, v, g, beta, o, s_final=None, stream=None, precision=LS_GDN_EXACT):
+def ls_gdn_replay_fwd(s0, q, k, v, g, beta, o, s_final=None, ws=None, stream=None,
+                      precision=LS_GDN_EXACT):
     """Gated-DeltaNet replay from the captured state s0 [H, dv, dk] of one
     member (q [R, H, dk]) or a group (q [B, R, H, dk]); see ls.h.  float32
-    buffers; precision LS_GDN_EXACT or LS_GDN_TENSOR_CORE."""
+    buffers; precision LS_GDN_EXACT (ws may be None) or LS_GDN_TENSOR_CORE
+    (ws of ls_gdn_workspace_size bytes)."""
     _want_f32(s0, q, k, v, g, beta, o, s_final)
     _check(lib().ls_gdn_replay_fwd(ctypes.byref(_gdn_desc(s0, q, precision)), _ptr(s0), _ptr(q), _ptr(k),
                                    _ptr(v), _ptr(g), _ptr(beta), _resp_len(q), _ptr(o), _ptr(s_final),
-                                   _stream(stream)))
+                                   _ptr(ws), 0 if ws is None else _nbytes(ws), _stream(stream)))
 
 
 def ls_gdn_replay_bwd(s0, q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta, ws, stream=None,

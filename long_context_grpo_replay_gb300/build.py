@@ -20,7 +20,7 @@ INCLUDE = HERE.parent / "include"
 LIBDIR = HERE / "_lib"
 LIB = LIBDIR / "libls.so"
 SOURCES = ["ls_api.cu", "ls_simt.cu", "ls_tc_fwd.cu", "ls_tc_bwd.cu", "ls_tc_dkdv.cu", "ls_noalloc.cu",
-           "ls_gdn.cu", "ls_gdn_chunk.cu", "ls_gdn_cp.cu"]
+           "ls_gdn.cu", "ls_gdn_cp.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

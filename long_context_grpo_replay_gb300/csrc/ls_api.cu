@@ -616,16 +616,20 @@ ls_status ls_gdn_workspace_size(const ls_gdn_desc* desc, int32_t resp_len, size_
 
 ls_status ls_gdn_replay_fwd(const ls_gdn_desc* desc, const float* s0, const float* q,
                             const float* k, const float* v, const float* g, const float* beta,
-                            int32_t resp_len, float* o, float* s_final, void* stream) {
+                            int32_t resp_len, float* o, float* s_final, void* ws, size_t ws_bytes,
+                            void* stream) {
   LS_CHECK(check_gdn(desc));
   if (resp_len < 0) return fail(LS_ERR_INVALID_ARGUMENT, "resp_len < 0");
   if (desc->batch == 0 || desc->heads == 0 || (resp_len == 0 && !s_final)) return LS_OK;
   if (!s0 || (resp_len > 0 && (!q || !k || !v || !g || !beta || !o)))
     return fail(LS_ERR_INVALID_ARGUMENT, "state and token buffers must be non-NULL");
-  if (desc->precision == LS_GDN_TENSOR_CORE)
-    LS_CUDA(launch_gdn_chunk_fwd(desc->batch, desc->heads, resp_len, s0, q, k, v, g, beta, o,
-                                 s_final, static_cast<cudaStream_t>(stream)),
-            "GDN chunk forward launch");
+  const bool tc = desc->precision == LS_GDN_TENSOR_CORE && resp_len > 0;
+  if (tc) LS_CHECK(check_ws(ws, ws_bytes, gdn_ws_need(*desc, resp_len)));
+  if (tc)
+    LS_CUDA(launch_gdn_cp_fwd(desc->batch, desc->heads, resp_len, s0, q, k, v, g, beta, o, s_final,
+                              reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader),
+                              static_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream)),
+            "GDN chunk-parallel forward launch");
   else
     LS_CUDA(launch_gdn_fwd(desc->batch, desc->heads, resp_len, s0, q, k, v, g, beta, o, s_final,
                            static_cast<cudaStream_t>(stream)),

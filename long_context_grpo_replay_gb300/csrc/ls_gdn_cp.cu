@@ -31,6 +31,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <initializer_list>
 
 #include "ls_gdn_tiles.cuh"
 #include "ls_internal.h"
@@ -188,6 +189,8 @@ constexpr uint32_t kPrepSmem = kPrepMisc + 3072 + 1024;
 static_assert(kPrepR4 + kC * kTStride * 4 <= kPrepMisc, "T buffer overlaps the misc area");
 constexpr int kPrepThr = 2 * kThr;
 
+// kBwd = false: the forward's share only (E0, ZK, M, F, gamma_C; no dO).
+template <bool kBwd>
 __global__ void __launch_bounds__(kPrepThr, 1)
     gdn_cp_prep_kernel(int H, int R, int nch, const float* __restrict__ q,
                        const float* __restrict__ k, const float* __restrict__ v,
@@ -217,7 +220,8 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   const int nt = R - t0 < kC ? (int)(R - t0) : kC;
   {
     const int64_t tok = (int64_t)m * R * H;
-    q += tok * kD, k += tok * kD, v += tok * kD, d_o += tok * kD, g += tok, beta += tok;
+    q += tok * kD, k += tok * kD, v += tok * kD, g += tok, beta += tok;
+    if (kBwd) d_o += tok * kD;
   }
   float* out = scratch_of(scr, H, nch, m, h, ch);
   if (tid == 0) {
@@ -238,13 +242,13 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   const int64_t row0 = (t0 * H + h) * kD;
   if (gt < nt) {  // the chunk's rows, asked into L2 up front (q and k are read twice)
     prefetch_l2((grpA ? k : v) + row0 + gt * rs, kD * 4);
-    prefetch_l2((grpA ? q : d_o) + row0 + gt * rs, kD * 4);
+    if (kBwd) prefetch_l2((grpA ? q : d_o) + row0 + gt * rs, kD * 4);
   }
 
   if (grpA) {
     stage_rows<4>(sb + kPrepR0, k + row0, rs, nt, nullptr, gt);
-    stage_rows<4>(sb + kPrepR1, q + row0, rs, nt, nullptr, gt);
-  } else {
+    if (kBwd) stage_rows<4>(sb + kPrepR1, q + row0, rs, nt, nullptr, gt);
+  } else if (kBwd) {
     stage_rows<4>(sb + kPrepR2, d_o + row0, rs, nt, nullptr, gt);
   }
   stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
@@ -261,7 +265,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   if (tid == 0) {  // K K^T -> cols 0..127, K Q^T -> 128..255
     tc_fence_after();
     mma_group(tb + 0, sb + kPrepR0, sb + kPrepR0, false, false);
-    mma_group(tb + 128, sb + kPrepR0, sb + kPrepR1, false, false);
+    if (kBwd) mma_group(tb + 128, sb + kPrepR0, sb + kPrepR1, false, false);
     mma_commit(smem_u32(&bars[0]));
   }
   bool ok = mbar_wait_warp(smem_u32(&bars[0]), 0, abortp);
@@ -286,22 +290,24 @@ __global__ void __launch_bounds__(kPrepThr, 1)
             gko[a_at(r, s)] = val;
           }
         }
-        tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
-        tmem_wait_ld_r(t32);
-        float pv[32];
+        if (kBwd) {
+          tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
+          tmem_wait_ld_r(t32);
+          float pv[32];
 #pragma unroll
-        for (int xx = 0; xx < 32; ++xx) {
-          const int t = cb * 32 + xx;
-          pv[xx] = t >= r ? __expf(sc[t] - cr) * __uint_as_float(t32[xx]) : 0.f;
+          for (int xx = 0; xx < 32; ++xx) {
+            const int t = cb * 32 + xx;
+            pv[xx] = t >= r ? __expf(sc[t] - cr) * __uint_as_float(t32[xx]) : 0.f;
+          }
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg) st_shared_v4(sb + kPrepR1 + tile_off(r, cb * 4 + gg), pack8(&pv[8 * gg]));
         }
-#pragma unroll
-        for (int gg = 0; gg < 4; ++gg) st_shared_v4(sb + kPrepR1 + tile_off(r, cb * 4 + gg), pack8(&pv[8 * gg]));
       }
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {  // dE0 = P^T dO -> cols 256..383 (dO as an N-major B)
+    if (kBwd && tid == 0) {  // dE0 = P^T dO -> cols 256..383 (dO as an N-major B)
       tc_fence_after();
       mma_group(tb + 256, sb + kPrepR1, sb + kPrepR2, true, false);
       mma_commit(smem_u32(&bars[1]));
@@ -359,7 +365,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
       }
     } else {
       // ---- group B: the right-hand sides, once P^T dO has read R1 and R2
-      ok = mbar_wait_warp(smem_u32(&bars[1]), 0, abortp);
+      if (kBwd) ok = mbar_wait_warp(smem_u32(&bars[1]), 0, abortp);
       if (ok) {
         stage_rows<4>(sb + kPrepR0, v + row0, rs, nt, sbt, gt);  // b V
         stage_rows<4>(sb + kPrepR1, k + row0, rs, nt, sbg, gt);  // b gamma K
@@ -371,7 +377,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
       if (grpA) {
 #pragma unroll
         for (int t = 0; t < kC; ++t) tcol[t] = buf[b_at(t, gt)];
-      } else {
+      } else if (kBwd) {
         // dE0 rows (bf16) over GK, which the substitution no longer needs
         tc_fence_after();
 #pragma unroll 1
@@ -411,10 +417,12 @@ __global__ void __launch_bounds__(kPrepThr, 1)
         mma_group_amn(tb + 0, tl, sb + kPrepR0, true, true);
         mma_group_amn(tb + 128, th, sb + kPrepR1, true, false);  // ZK = T (b gamma K)
         mma_group_amn(tb + 128, tl, sb + kPrepR1, true, true);
-        mma_group(tb + 256, th, sb + kPrepR3, true, false);      // dU0 = T^T dE0
-        mma_group(tb + 256, tl, sb + kPrepR3, true, true);
-        mma_group(tb + 384, th, sb + kPrepR2, true, false);      // ZW = T^T (w K)
-        mma_group(tb + 384, tl, sb + kPrepR2, true, true);
+        if (kBwd) {
+          mma_group(tb + 256, th, sb + kPrepR3, true, false);    // dU0 = T^T dE0
+          mma_group(tb + 256, tl, sb + kPrepR3, true, true);
+          mma_group(tb + 384, th, sb + kPrepR2, true, false);    // ZW = T^T (w K)
+          mma_group(tb + 384, tl, sb + kPrepR2, true, true);
+        }
         mma_commit(smem_u32(&bars[2]));
       }
       ok = mbar_wait_warp(smem_u32(&bars[2]), 0, abortp);
@@ -430,7 +438,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
         const float fa = grpA ? 1.f : -sbg[r];
         const uint32_t colA = grpA ? 0 : 256;
 #pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {
+        for (int cb = 0; (grpA || kBwd) && cb < 4; ++cb) {
           uint32_t t32[32];
           float f[32];
           tmem_ld32(tb + lane_off + colA + cb * 32, t32);
@@ -456,7 +464,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
           tc_fence_after();
           mma_group_amn(tb + 0, sb + kPrepR3, sb + kPrepR2, true, false);    // M = ZK^T W
           mma_group_amn(tb + 128, sb + kPrepR0, sb + kPrepR2, true, false);  // F = E0^T W
-          mma_group_amn(tb + 256, sb + kPrepR5, sb + kPrepR1, true, false);  // M' = ZW^T diag(b gamma) K
+          if (kBwd) mma_group_amn(tb + 256, sb + kPrepR5, sb + kPrepR1, true, false);  // M' = ZW^T diag(b gamma) K
           mma_commit(smem_u32(&bars[3]));
         }
         ok = mbar_wait_warp(smem_u32(&bars[3]), 0, abortp);
@@ -464,14 +472,15 @@ __global__ void __launch_bounds__(kPrepThr, 1)
           // Q (R0), K (R1), gamma dO (R2) for F'; meanwhile -M, F hi / lo
           // (group A) and -M' (group B) to their images
           tc_fence_after();
-          if (grpA) {
+          if (!kBwd) {
+          } else if (grpA) {
             stage_rows<4>(sb + kPrepR0, q + row0, rs, nt, nullptr, gt);
             stage_rows<4>(sb + kPrepR1, k + row0, rs, nt, nullptr, gt);
           } else {
             stage_rows<4>(sb + kPrepR2, d_o + row0, rs, nt, sgm, gt);
           }
 #pragma unroll 1
-          for (int cb = 0; cb < 4; ++cb) {
+          for (int cb = 0; (grpA || kBwd) && cb < 4; ++cb) {
             uint32_t t32[32];
             float f[32], hi[32], lo[32];
             tmem_ld32(tb + lane_off + (grpA ? 0 : 256) + cb * 32, t32);
@@ -490,32 +499,34 @@ __global__ void __launch_bounds__(kPrepThr, 1)
               put_tile_row(false, 0, image_of(out, kImFlo), r, lo, cb * 4, 4);
             }
           }
-          fence_proxy_async_smem();
-          tc_fence_before();
-          __syncthreads();
-          if (tid == 0) {  // F' = (gamma dO)^T Q - (gamma b dU0)^T K -> cols 384..511
-            tc_fence_after();
-            mma_group_amn(tb + 384, sb + kPrepR2, sb + kPrepR0, true, false);
-            mma_group_amn(tb + 384, sb + kPrepR4, sb + kPrepR1, true, true);
-            mma_commit(smem_u32(&bars[4]));
-          }
-          ok = mbar_wait_warp(smem_u32(&bars[4]), 0, abortp);
-          if (!__syncthreads_or(!ok)) {
-            // F' hi / lo: group A columns 0..63, group B 64..127
-            tc_fence_after();
+          if (kBwd) {
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            if (tid == 0) {  // F' = (gamma dO)^T Q - (gamma b dU0)^T K -> cols 384..511
+              tc_fence_after();
+              mma_group_amn(tb + 384, sb + kPrepR2, sb + kPrepR0, true, false);
+              mma_group_amn(tb + 384, sb + kPrepR4, sb + kPrepR1, true, true);
+              mma_commit(smem_u32(&bars[4]));
+            }
+            ok = mbar_wait_warp(smem_u32(&bars[4]), 0, abortp);
+            if (!__syncthreads_or(!ok)) {
+              // F' hi / lo: group A columns 0..63, group B 64..127
+              tc_fence_after();
 #pragma unroll 1
-            for (int cb = 0; cb < 2; ++cb) {
-              const int c0 = (grpA ? 0 : 64) + cb * 32;
-              uint32_t t32[32];
-              float f[32], hi[32], lo[32];
-              tmem_ld32(tb + lane_off + 384 + c0, t32);
-              tmem_wait_ld_r(t32);
+              for (int cb = 0; cb < 2; ++cb) {
+                const int c0 = (grpA ? 0 : 64) + cb * 32;
+                uint32_t t32[32];
+                float f[32], hi[32], lo[32];
+                tmem_ld32(tb + lane_off + 384 + c0, t32);
+                tmem_wait_ld_r(t32);
 #pragma unroll
-              for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
+                for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
 #pragma unroll
-              for (int gg = 0; gg < 4; ++gg) split8(&f[8 * gg], &hi[8 * gg], &lo[8 * gg]);
-              put_tile_row(false, 0, image_of(out, kImFghi), r, hi, c0 / 8, 4);
-              put_tile_row(false, 0, image_of(out, kImFglo), r, lo, c0 / 8, 4);
+                for (int gg = 0; gg < 4; ++gg) split8(&f[8 * gg], &hi[8 * gg], &lo[8 * gg]);
+                put_tile_row(false, 0, image_of(out, kImFghi), r, hi, c0 / 8, 4);
+                put_tile_row(false, 0, image_of(out, kImFglo), r, lo, c0 / 8, 4);
+              }
             }
           }
         }
@@ -549,8 +560,9 @@ constexpr uint32_t kChI = 0, kChShi = kTile, kChSlo = 2 * kTile, kChM = 3 * kTil
 constexpr uint32_t kChainSmem = kChMisc + 1024 + 1024;
 constexpr int kChThr = 2 * kThr;
 
+// passes = 1: the state forward alone (the replay's forward), writing s_final.
 __global__ void __launch_bounds__(kChThr, 1)
-    gdn_cp_chain_kernel(int H, int nch, const float* __restrict__ s0, float* __restrict__ scr,
+    gdn_cp_chain_kernel(int H, int nch, int passes, const float* __restrict__ s0, float* __restrict__ scr,
                         float* __restrict__ s_final, uint32_t* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -611,7 +623,8 @@ __global__ void __launch_bounds__(kChThr, 1)
       st[4 * c] = a4.x, st[4 * c + 1] = a4.y, st[4 * c + 2] = a4.z, st[4 * c + 3] = a4.w;
     }
   }
-  for (int i = 0; ok && i < 2 * nch; ++i) {
+  const int steps = passes * nch;
+  for (int i = 0; ok && i <= steps; ++i) {
     const bool bw = i >= nch;
     if (i == nch) {
       if (s_final) {
@@ -622,6 +635,7 @@ __global__ void __launch_bounds__(kChThr, 1)
 #pragma unroll
       for (int c = 0; c < 64; ++c) st[c] = 0.f;
     }
+    if (i == steps) break;
     float* blk = scratch_of(scr, H, nch, m, h, chunk_at(i));
     const float gc = blk[kGammaAt];
     {  // S at the chunk's start / G at its end, row x
@@ -658,7 +672,7 @@ __global__ void __launch_bounds__(kChThr, 1)
     ++ncp;
     ok = mbar_wait_warp(smem_u32(&bars[1]), nmm++ & 1, abortp);
     if (__syncthreads_or(!ok)) break;
-    if (tid == 0 && i + 1 < 2 * nch) issue(i + 1);  // the products have read this step's tiles
+    if (tid == 0 && i + 1 < steps) issue(i + 1);  // the products have read this step's tiles
     tc_fence_after();
 #pragma unroll
     for (int cb = 0; cb < 2; ++cb) {
@@ -1132,11 +1146,198 @@ __global__ void __launch_bounds__(kOutThr, 1)
   }
 }
 
+// ---------------------------------------------------------------- forward out
+// The replay's forward output, one CTA per (chunk, head, member), 256
+// threads (row t, column half hf): E = E0 - ZK S^T, then
+// o = diag(gamma) Q S^T + P E with P = lower(Gamma . Q K^T).
+// Shared memory: F0 Q -> P, F1 K -> E, F2 S (start), F3 ZK.
+constexpr uint32_t kFoMisc = 4 * kTile;
+constexpr uint32_t kFoSmem = kFoMisc + 2048 + 1024;
+
+__global__ void __launch_bounds__(kOutThr, 1)
+    gdn_cp_fwd_out_kernel(int H, int R, int nch, const float* __restrict__ q,
+                          const float* __restrict__ k, const float* __restrict__ g,
+                          const float* __restrict__ beta, float* __restrict__ scr,
+                          float* __restrict__ o, uint32_t* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(sm);
+  const uint32_t F0 = sb, F1 = sb + kTile, F2 = sb + 2 * kTile, F3 = sb + 3 * kTile;
+  float* sc = reinterpret_cast<float*>(sm + kFoMisc);
+  float* sbt = sc + kC;
+  float* swt = sbt + kC;  // 8 floats of scan scratch
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kFoMisc + 1088);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
+  uint32_t* abort_s = tslot + 1;
+
+  const int ch = blockIdx.x, h = blockIdx.y, m = blockIdx.z, tid = threadIdx.x, warp = tid >> 5;
+  const int t = tid & (kThr - 1), hf = tid >> 7, cb0 = 2 * hf;
+  const int64_t t0 = (int64_t)ch * kC;
+  const int nt = R - t0 < kC ? (int)(R - t0) : kC;
+  {
+    const int64_t tok = (int64_t)m * R * H;
+    q += tok * kD, k += tok * kD, g += tok, beta += tok, o += tok * kD;
+  }
+  float* blk = scratch_of(scr, H, nch, m, h, ch);
+  if (tid == 0) {
+    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    *abort_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tslot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = *tslot, lane_off = (uint32_t)((warp & 3) * 32) << 16;
+  const volatile uint32_t* abortp = abort_s;
+  const int64_t rs = (int64_t)H * kD;
+  const bool live = t < nt;
+  const int64_t row0 = (t0 * H + h) * kD, rowt = ((t0 + t) * H + h) * kD;
+  if (tid == 0) prefetch_l2(blk + (int64_t)kE0 * kTileElems, kTileElems * 4);  // E0
+
+  if (hf == 0) {
+    stage_rows<4>(F0, q + row0, rs, nt, nullptr, t);
+    stage_rows<4>(F2, blk + (int64_t)kSstart * kTileElems, kD, kD, nullptr, t);
+  } else {
+    stage_rows<4>(F1, k + row0, rs, nt, nullptr, t);
+    copy_image(F3, image_of(blk, kImZK), t);
+  }
+  stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0) {  // Q K^T -> 0, Q S^T -> 128, ZK S^T -> 256
+    tc_fence_after();
+    mma_group(tb + 0, F0, F1, false, false);
+    mma_group(tb + 128, F0, F2, false, false);
+    mma_group(tb + 256, F3, F2, false, false);
+    mma_commit(smem_u32(&bars[0]));
+  }
+  bool ok = mbar_wait_warp(smem_u32(&bars[0]), 0, abortp);
+  if (!__syncthreads_or(!ok)) {
+    tc_fence_after();
+    const float ct = sc[t], gt = expf(ct);
+    const float* e0r = blk + (int64_t)kE0 * kTileElems + t * kD;
+#pragma unroll 1
+    for (int cb = cb0; cb < cb0 + 2; ++cb) {
+      uint32_t t32[32];
+      float f32[32];
+      // P row t over Q (F0)
+      tmem_ld32(tb + lane_off + 0 + cb * 32, t32);
+      tmem_wait_ld_r(t32);
+#pragma unroll
+      for (int xx = 0; xx < 32; ++xx) {
+        const int s = cb * 32 + xx;
+        f32[xx] = s <= t ? __expf(ct - sc[s]) * __uint_as_float(t32[xx]) : 0.f;
+      }
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) st_shared_v4(F0 + tile_off(t, cb * 4 + gg), pack8(&f32[8 * gg]));
+      // E row t = E0 - ZK S^T over K (F1)
+      row_ld32(f32, e0r + cb * 32, true);
+      tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
+      tmem_wait_ld_r(t32);
+#pragma unroll
+      for (int xx = 0; xx < 32; ++xx) f32[xx] -= __uint_as_float(t32[xx]);
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) st_shared_v4(F1 + tile_off(t, cb * 4 + gg), pack8(&f32[8 * gg]));
+      // gamma_t Q S^T, back into its columns for o = gamma Q S^T + P E
+      tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
+      tmem_wait_ld_r(t32);
+#pragma unroll
+      for (int xx = 0; xx < 32; ++xx) t32[xx] = __float_as_uint(gt * __uint_as_float(t32[xx]));
+      tmem_st32(tb + lane_off + 128 + cb * 32, t32);
+    }
+    tmem_wait_st();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {  // + P E -> 128 (E as an N-major B)
+      tc_fence_after();
+      mma_group(tb + 128, F0, F1, true, true);
+      mma_commit(smem_u32(&bars[1]));
+    }
+    ok = mbar_wait_warp(smem_u32(&bars[1]), 0, abortp);
+    if (!__syncthreads_or(!ok)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int cb = cb0; cb < cb0 + 2; ++cb) {
+        uint32_t t32[32];
+        float f32[32];
+        tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
+        tmem_wait_ld_r(t32);
+#pragma unroll
+        for (int xx = 0; xx < 32; ++xx) f32[xx] = __uint_as_float(t32[xx]);
+        row_st32(f32, o + rowt + cb * 32, live);
+      }
+    }
+  }
+  if (!ok && tid == 0 && status) atomicOr(status, kStatusTimeout);
+  if (tid == 0) {
+    mma_commit(smem_u32(&bars[2]));
+    mbar_wait(smem_u32(&bars[2]), 0, abortp);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tb, 512);
+  }
+}
+
 }  // namespace
 
 size_t gdn_cp_workspace_bytes(int B, int H, int R) {
   const int64_t nch = (R + kC - 1) / kC;
   return (size_t)B * H * nch * kScrFloats * sizeof(float);
+}
+
+namespace {
+cudaError_t set_smem_attributes() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(gdn_cp_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kPrepSmem)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(gdn_cp_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kPrepSmem)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(gdn_cp_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kChainSmem)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(gdn_cp_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kOutSmem)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(gdn_cp_fwd_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kFoSmem)) != cudaSuccess)
+    return e;
+  return cudaSuccess;
+}
+bool misaligned(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (reinterpret_cast<uintptr_t>(p) & 15u) return true;
+  return false;
+}
+}  // namespace
+
+// The forward in chunk-parallel form: prep's forward share over all chunks,
+// the state chain per (head, member), then o over all chunks.  ws holds the
+// scratch (gdn_cp_workspace_bytes); s0, q, k, v, o and s_final 16-byte aligned.
+cudaError_t launch_gdn_cp_fwd(int B, int H, int R, const float* s0, const float* q, const float* k,
+                              const float* v, const float* g, const float* beta, float* o,
+                              float* s_final, float* ws, uint32_t* status, cudaStream_t st) {
+  if (B == 0 || H == 0 || R == 0) return cudaSuccess;
+  if (H > 65535 || B > 65535) return cudaErrorInvalidValue;  // grid y and z
+  if (misaligned({s0, q, k, v, o, s_final, ws})) return cudaErrorMisalignedAddress;
+  const int nch = (R + kC - 1) / kC;
+  cudaError_t e;
+  if ((e = set_smem_attributes()) != cudaSuccess) return e;
+  LaunchScope ls(kKGdnFwd, st);
+  gdn_cp_prep_kernel<false><<<dim3(nch, H, B), kPrepThr, kPrepSmem, st>>>(H, R, nch, q, k, v, g, beta,
+                                                                        nullptr, ws, status);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  gdn_cp_chain_kernel<<<dim3(H, B), kChThr, kChainSmem, st>>>(H, nch, 1, s0, ws, s_final, status);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  gdn_cp_fwd_out_kernel<<<dim3(nch, H, B), kOutThr, kFoSmem, st>>>(H, R, nch, q, k, g, beta, ws, o,
+                                                                  status);
+  return cudaGetLastError();
 }
 
 // The backward in chunk-parallel form: prep over all chunks, the two chains
@@ -1148,27 +1349,18 @@ cudaError_t launch_gdn_cp_bwd(int B, int H, int R, const float* s0, const float*
                               uint32_t* status, cudaStream_t st) {
   if (B == 0 || H == 0 || R == 0) return cudaSuccess;
   if (H > 65535 || B > 65535) return cudaErrorInvalidValue;  // grid y and z
-  for (const void* p : {(const void*)s0, (const void*)q, (const void*)k, (const void*)v,
-                        (const void*)d_o, (const void*)dq, (const void*)dk, (const void*)dv,
-                        (const void*)ws})
-    if (reinterpret_cast<uintptr_t>(p) & 15u) return cudaErrorMisalignedAddress;
+  if (misaligned({s0, q, k, v, d_o, dq, dk, dv, ws})) return cudaErrorMisalignedAddress;
   const int nch = (R + kC - 1) / kC;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(gdn_cp_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kPrepSmem)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(gdn_cp_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kChainSmem)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(gdn_cp_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kOutSmem)) != cudaSuccess)
-    return e;
+  if ((e = set_smem_attributes()) != cudaSuccess) return e;
   LaunchScope ls(kKGdnBwd, st);
-  gdn_cp_prep_kernel<<<dim3(nch, H, B), kPrepThr, kPrepSmem, st>>>(H, R, nch, q, k, v, g, beta, d_o, ws,
-                                                              status);
+  gdn_cp_prep_kernel<true><<<dim3(nch, H, B), kPrepThr, kPrepSmem, st>>>(H, R, nch, q, k, v, g, beta, d_o,
+                                                                       ws, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  gdn_cp_chain_kernel<<<dim3(H, B), kChThr, kChainSmem, st>>>(H, nch, s0, ws, nullptr, status);
+  gdn_cp_chain_kernel<<<dim3(H, B), kChThr, kChainSmem, st>>>(H, nch, 2, s0, ws, nullptr, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gdn_cp_out_kernel<<<dim3(nch, H, B), kOutThr, kOutSmem, st>>>(H, R, nch, q, k, v, g, beta, d_o, ws,
-                                                            nullptr, dq, dk, dv, dg, dbeta, status);
+                                                               nullptr, dq, dk, dv, dg, dbeta, status);
   return cudaGetLastError();
 }
 

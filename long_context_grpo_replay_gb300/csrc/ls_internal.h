@@ -160,13 +160,13 @@ size_t gdn_workspace_bytes(int B, int H, int R);
 cudaError_t launch_gdn_fwd(int B, int H, int R, const float* s0, const float* q, const float* k,
                            const float* v, const float* g, const float* beta, float* o,
                            float* s_final, cudaStream_t st);
-// Chunkwise tensor-core forward (ls_gdn_chunk.cu), precision LS_GDN_TENSOR_CORE.
-cudaError_t launch_gdn_chunk_fwd(int B, int H, int R, const float* s0, const float* q,
-                                 const float* k, const float* v, const float* g, const float* beta,
-                                 float* o, float* s_final, cudaStream_t st);
-// Chunk-parallel tensor-core backward (ls_gdn_cp.cu), selected with the chunkwise forward.
+// Chunk-parallel tensor-core forward and backward (ls_gdn_cp.cu), precision
+// LS_GDN_TENSOR_CORE; both use gdn_cp_workspace_bytes of scratch.
 size_t gdn_cp_workspace_bytes(int B, int H, int R);
 // status: the workspace status word a wait that gives up sets.
+cudaError_t launch_gdn_cp_fwd(int B, int H, int R, const float* s0, const float* q, const float* k,
+                              const float* v, const float* g, const float* beta, float* o,
+                              float* s_final, float* ws, uint32_t* status, cudaStream_t st);
 cudaError_t launch_gdn_cp_bwd(int B, int H, int R, const float* s0, const float* q, const float* k,
                               const float* v, const float* g, const float* beta, const float* d_o,
                               float* dq, float* dk, float* dv, float* dg, float* dbeta, float* ws,

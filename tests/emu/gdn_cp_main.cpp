@@ -1,8 +1,8 @@
 // Runs the chunk-parallel GDN kernels' source on the CPU block emulator:
-//   gdn_cp_emu <stage> <in.bin> <out.bin>      stage: prep | all
+//   gdn_cp_emu <stage> <in.bin> <out.bin>      stage: prep | all | fwd
 // in.bin: int32 B, H, R; float32 s0 [H][128][128], q, k, v, d_o [B][R][H][128],
-// g, beta [B][R][H].  out.bin: uint32 status; the float32 scratch; then (all)
-// o, s_final, dq, dk, dv, dg, dbeta.
+// g, beta [B][R][H].  out.bin: uint32 status; the float32 scratch; then (all,
+// fwd) o, s_final, dq, dk, dv, dg, dbeta (the gradients zero after fwd).
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -19,7 +19,7 @@ alignas(1024) unsigned char smem_raw[emu::kSmemBytes];
 
 int main(int argc, char** argv) {
   if (argc != 4) return 2;
-  const bool all = std::strcmp(argv[1], "all") == 0;
+  const int mode = std::strcmp(argv[1], "all") == 0 ? 1 : std::strcmp(argv[1], "fwd") == 0 ? 2 : 0;
   FILE* f = std::fopen(argv[2], "rb");
   if (!f) return 3;
   int32_t hdr[3];
@@ -34,14 +34,14 @@ int main(int argc, char** argv) {
   std::vector<float> scr((size_t)B * H * nch * ls::kScrFloats, 0.f);
   std::vector<float> o(nt), s_final((size_t)B * ns), dq(nt), dk(nt), dv(nt), dg(nsc), dbeta(nsc);
   uint32_t status = 0;
-  ls::emu_run(all, B, H, R, s0.data(), q.data(), k.data(), v.data(), g.data(), beta.data(),
+  ls::emu_run(mode, B, H, R, s0.data(), q.data(), k.data(), v.data(), g.data(), beta.data(),
               d_o.data(), scr.data(), o.data(), s_final.data(), dq.data(), dk.data(), dv.data(),
               dg.data(), dbeta.data(), &status);
   f = std::fopen(argv[3], "wb");
   if (!f) return 6;
   std::fwrite(&status, 4, 1, f);
   std::fwrite(scr.data(), 4, scr.size(), f);
-  if (all)
+  if (mode != 0)
     for (auto* x : {&o, &s_final, &dq, &dk, &dv, &dg, &dbeta}) std::fwrite(x->data(), 4, x->size(), f);
   std::fclose(f);
   return 0;

@@ -182,10 +182,10 @@ def test_gdn_workspace_and_argument_checks(ls):
     tc = ls.GdnDesc(8, 32, 128, 128, ls.LS_GDN_TENSOR_CORE)
     # the 256-byte status header, then the precision's own scratch: per (member,
     # head) the recurrent backward keeps one 128x128 float32 state per 8-token
-    # checkpoint plus a segment of 8 states; the chunk-parallel one keeps nine
-    # 128x128 float32 blocks per 128-token chunk
+    # checkpoint plus a segment of 8 states; the chunk-parallel one keeps, per
+    # 128-token chunk, seven 128x128 float32 blocks and eight 32 KB bf16 tiles
     rec = [256 + 8 * 32 * (n + 8) * 128 * 128 * 4 for n in (1, 8, 9, 512)]
-    cp = [256 + 8 * 32 * -(-R // 128) * 9 * 128 * 128 * 4 for R in (1, 64, 65, 4096)]
+    cp = [256 + 8 * 32 * -(-R // 128) * (7 * 128 * 128 * 4 + 8 * 32768) for R in (1, 64, 65, 4096)]
     assert [ls.ls_gdn_workspace_size(d, r) for r in (1, 64, 65, 4096)] == rec
     assert [ls.ls_gdn_workspace_size(tc, r) for r in (1, 64, 65, 4096)] == cp
     out = ctypes.c_size_t(0)
@@ -197,8 +197,15 @@ def test_gdn_workspace_and_argument_checks(ls):
     assert "precision" in ls.ls_last_error()
     assert L.ls_gdn_workspace_size(ctypes.byref(d), -1, ctypes.byref(out)) == 1
     args = [None] * 6
-    assert L.ls_gdn_replay_fwd(ctypes.byref(d), *args, 0, None, None, None) == 0  # no-op
-    assert L.ls_gdn_replay_fwd(ctypes.byref(d), *args, 8, None, None, None) == 1  # NULL buffers
+    assert L.ls_gdn_replay_fwd(ctypes.byref(d), *args, 0, None, None, None, 0, None) == 0  # no-op
+    assert L.ls_gdn_replay_fwd(ctypes.byref(d), *args, 8, None, None, None, 0, None) == 1  # NULL buffers
+    # the tensor-core forward needs the workspace, refused before any launch
+    fw = [ctypes.c_void_p(256)] * 6
+    st = L.ls_gdn_replay_fwd(ctypes.byref(tc), *fw, 8, ctypes.c_void_p(256), None, None, 0, None)
+    assert st == 1 and "workspace" in ls.ls_last_error()
+    st = L.ls_gdn_replay_fwd(ctypes.byref(tc), *fw, 8, ctypes.c_void_p(256), None, ctypes.c_void_p(256),
+                             100, None)
+    assert st == 3 and "workspace" in ls.ls_last_error()  # LS_ERR_WORKSPACE_TOO_SMALL
     bw = [ctypes.c_void_p(256)] * 7
     st = L.ls_gdn_replay_bwd(ctypes.byref(d), *bw, 8, *([ctypes.c_void_p(256)] * 5), None, 0, None)
     assert st == 1 and "workspace" in ls.ls_last_error()

@@ -1,8 +1,9 @@
 """The chunk-parallel GDN kernels (csrc/ls_gdn_cp.cu), their own source
 compiled for the host and run on the CPU block emulator (tests/emu/), stage
 by stage against the float64 chunk-parallel reference of
-tests/test_oracle_gdn.py (itself pinned to the oracle), at the bf16
-tolerance of their tensor-core products."""
+tests/test_oracle_gdn.py (itself pinned to the oracle), and the forward and
+backward replays whole against the oracle, at the bf16 tolerance of their
+tensor-core products."""
 import shutil
 import subprocess
 from pathlib import Path
@@ -43,10 +44,13 @@ def image(chunk, i):
     return (u16[off // 2].astype(np.uint32) << 16).view(np.float32)
 
 
-def build(d):
+def build(d, mutation=None):
     if shutil.which("g++") is None:
         pytest.skip("no host C++ compiler")
     src = SRC.read_text()
+    if mutation:
+        assert src.count(mutation[0]) == 1, mutation[0]
+        src = src.replace(mutation[0], mutation[1])
     # the kernels, up to the end of their anonymous namespace; launchers stay out
     end = src.index("\n}  // namespace\n\nsize_t gdn_cp_workspace_bytes") + len("\n}  // namespace\n")
     text = src[:end] + "}  // namespace ls\n" + (EMU / "gdn_cp_run.inc").read_text()
@@ -260,3 +264,61 @@ def test_bench_length_matches_the_oracle(emulator):
     want = gdn_replay(a["s0"], a["q"][0], a["k"][0], a["v"][0], a["g"][0], a["beta"][0], a["d_o"][0])
     errs = {n: rel(got[n].reshape(want[n].shape), want[n]) for n in got}
     assert all(e <= TOL_BF16 for e in errs.values()), errs
+
+
+def _replay_outputs(rest, B, H, R):
+    nt, ns, nsc = B * R * H * 128, B * H * 128 * 128, B * R * H
+    got, i = {}, 0
+    for name, n in (("o", nt), ("s_final", ns), ("dq", nt), ("dk", nt), ("dv", nt), ("dg", nsc),
+                    ("dbeta", nsc)):
+        got[name] = rest[i:i + n]
+        i += n
+    return got
+
+
+def _forward_errors(exe, d, B, H, R, seed):
+    from oracle.gdn import gdn_replay
+
+    c = inputs.make_gdn_group(B, H, R, seed=seed)
+    status, _, rest = run(exe, d, c, "fwd")
+    assert status == 0
+    got = _replay_outputs(rest, B, H, R)
+    a = {x: t.numpy() for x, t in c.items()}
+    errs = {}
+    for m in range(B):
+        want = gdn_replay(a["s0"], a["q"][m], a["k"][m], a["v"][m], a["g"][m], a["beta"][m],
+                          a["d_o"][m])
+        for name in ("o", "s_final"):
+            gm = got[name].reshape((B,) + want[name].shape)[m]
+            errs[name] = max(errs.get(name, 0.0), rel(gm, want[name]))
+    return errs
+
+
+@pytest.mark.parametrize("B,H,R", [(2, 1, 300), (1, 2, 1), (1, 1, 128), (1, 1, 129), (1, 1, 4096)],
+                         ids=["three_chunks_two_members", "one_token_two_heads", "one_exact_chunk",
+                              "one_token_past_a_chunk", "bench_length"])
+def test_forward_matches_the_oracle(emulator, B, H, R):
+    """The chunk-parallel forward (prep's forward share, the state chain, the
+    forward output): o and the final state against the float64 oracle."""
+    exe, d = emulator
+    errs = _forward_errors(exe, d, B, H, R, seed=50 + R)
+    print("forward max rel errs", errs)
+    assert all(e <= TOL_BF16 for e in errs.values()), errs
+
+
+@pytest.mark.parametrize("mutation", [
+    ("        f32[xx] = s <= t ? __expf(ct - sc[s]) * __uint_as_float(t32[xx]) : 0.f;\n      }\n"
+     "#pragma unroll\n      for (int gg = 0; gg < 4; ++gg) st_shared_v4(F0",
+     "        f32[xx] = s < t ? __expf(ct - sc[s]) * __uint_as_float(t32[xx]) : 0.f;\n      }\n"
+     "#pragma unroll\n      for (int gg = 0; gg < 4; ++gg) st_shared_v4(F0"),
+    ("mma_group_amn(tb + 0, sb + kPrepR3, sb + kPrepR2, true, false);    // M = ZK^T W",
+     "mma_group(tb + 0, sb + kPrepR3, sb + kPrepR2, true, false);    // M = ZK^T W"),
+    ("st[cb * 32 + xx] = fmaf(gc, st[cb * 32 + xx], __uint_as_float(t32[xx]));",
+     "st[cb * 32 + xx] = fmaf(1.f, st[cb * 32 + xx], __uint_as_float(t32[xx]));"),
+], ids=["P_without_its_diagonal", "M_with_ZK_read_K_major", "chain_without_the_decay"])
+def test_emulator_rejects_planted_kernel_mistakes(tmp_path, mutation):
+    """A mistake planted in a copy of the kernel source must fail the
+    forward comparison."""
+    exe = build(tmp_path, mutation)
+    errs = _forward_errors(exe, tmp_path, 1, 1, 300, seed=61)
+    assert not all(e <= TOL_BF16 for e in errs.values()), errs

@@ -32,7 +32,7 @@ def _run(c):
     B, R, H, _ = q.shape
     o = torch.empty_like(c["v"])
     s_final = torch.empty((B,) + tuple(s0.shape), device=q.device, dtype=torch.float32)
-    ls.ls_gdn_replay_fwd(s0, q, c["k"], c["v"], c["g"], c["beta"], o, s_final)
+    ls.ls_gdn_replay_fwd(s0, q, c["k"], c["v"], c["g"], c["beta"], o, s_final)  # exact path: no workspace
     grads = {n: torch.empty_like(c[x]) for n, x in
              (("dq", "q"), ("dk", "k"), ("dv", "v"), ("dg", "g"), ("dbeta", "beta"))}
     ws = torch.empty(ls.ls_gdn_workspace_size(ls.GdnDesc(B, H, 128, 128), R), dtype=torch.uint8,

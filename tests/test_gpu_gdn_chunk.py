@@ -30,9 +30,13 @@ def _fwd(c):
     B, R, H, _ = c["q"].shape
     o = torch.full_like(c["v"], float("nan"))
     s_final = torch.empty((B, H, 128, 128), device=c["q"].device)
-    ls.ls_gdn_replay_fwd(c["s0"], c["q"], c["k"], c["v"], c["g"], c["beta"], o, s_final,
+    ws = torch.empty(max(1, ls.ls_gdn_workspace_size(ls.GdnDesc(B, H, 128, 128, TC), R)),
+                     dtype=torch.uint8, device=c["q"].device)
+    ls.ls_clear_device_status(ws)
+    ls.ls_gdn_replay_fwd(c["s0"], c["q"], c["k"], c["v"], c["g"], c["beta"], o, s_final, ws,
                          precision=TC)
     torch.cuda.synchronize()
+    ls.ls_read_device_status(ws)  # raises if a bounded device wait ran out
     return o, s_final
 
 
