@@ -906,13 +906,15 @@ def gdn_config(workload: str, world: int) -> dict:
     B, H, R, prec = GDN_WORKLOADS[workload]
     return {"workload": workload, "group": B, "heads": H, "resp_len": R, "dk": 128, "dv": 128,
             "precision": "LS_GDN_EXACT" if prec == 0 else "LS_GDN_TENSOR_CORE",
+            "bwd_reuses_forward": prec != 0,  # LS_GDN_BWD_REUSES_FORWARD: one forward per backward
             "parallelism": f"replicas x{world}",
             "l2": "inputs larger than L2 (%.1f GiB of q/k/v/dO)" % (4 * B * R * H * 128 * 4 / 2**30)}
 
 
 def run_gdn(args):
     """Gated-DeltaNet replay of one layer for a group: ls_gdn_replay_fwd (with
-    the final state) and ls_gdn_replay_bwd, float32, dk = dv = 128."""
+    the final state) and ls_gdn_replay_bwd, float32, dk = dv = 128; on the
+    tensor-core path the backward reuses the forward's workspace terms."""
     import torch
     import torch.distributed as dist
 
@@ -943,7 +945,7 @@ def run_gdn(args):
                              precision=prec)
         ls.ls_gdn_replay_bwd(x["s0"], x["q"], x["k"], x["v"], x["g"], x["beta"], x["d_o"],
                              gr["dq"], gr["dk"], gr["dv"], gr["dg"], gr["dbeta"], ws, stream,
-                             precision=prec)
+                             precision=prec, reuse_forward=prec == ls.LS_GDN_TENSOR_CORE)
 
     for _ in range(args.warmup):
         step(c)

@@ -297,9 +297,20 @@ LS_API ls_status ls_stage_pages(const ls_attn_desc* desc, const void* k_src, con
  *                       (else LS_ERR_CUDA).
  * Float32 callers that need the 1e-5 result keep LS_GDN_EXACT.
  * Errors: LS_ERR_UNSUPPORTED for other dk/dv, LS_ERR_INVALID_ARGUMENT for
- * NULL buffers, negative sizes or an unknown precision,
+ * NULL buffers, negative sizes, an unknown precision or unknown flags,
  * LS_ERR_WORKSPACE_TOO_SMALL; all before any launch. */
 typedef enum { LS_GDN_EXACT = 0, LS_GDN_TENSOR_CORE = 1 } ls_gdn_precision;
+
+/* flags (0 by default):
+ *   LS_GDN_BWD_REUSES_FORWARD  with LS_GDN_TENSOR_CORE, the backward takes the
+ *       forward's per-chunk terms and states from ws instead of forming them
+ *       again: the caller promises that ws was last written by
+ *       ls_gdn_replay_fwd with the same desc precision, buffers and resp_len
+ *       (the inputs unchanged since).  The results are then the ones the
+ *       backward forms without the flag, bit for bit; if the promise is
+ *       broken they are wrong (every access still stays inside ws).  Ignored
+ *       by LS_GDN_EXACT. */
+enum { LS_GDN_BWD_REUSES_FORWARD = 1 };
 
 typedef struct {
   int32_t batch;
@@ -307,6 +318,7 @@ typedef struct {
   int32_t dk;
   int32_t dv;
   int32_t precision; /* ls_gdn_precision */
+  int32_t flags;     /* LS_GDN_BWD_REUSES_FORWARD or 0 */
 } ls_gdn_desc;
 
 LS_API ls_status ls_gdn_workspace_size(const ls_gdn_desc* desc, int32_t resp_len, size_t* bytes);

@@ -21,7 +21,7 @@ __all__ = [
     "desc_for", "prompt_from", "EXPORTED_SYMBOLS", "ls_replay_fwd_noalloc",
     "ls_replay_fwd_noalloc_scratch_bytes", "ls_prompt_prefill", "ls_prompt_prefill_workspace_size",
     "ls_replay_fwd_part", "ls_replay_bwd_part", "ls_sum_parts",
-    "GdnDesc", "LS_GDN_EXACT", "LS_GDN_TENSOR_CORE", "ls_gdn_workspace_size", "ls_gdn_replay_fwd",
+    "GdnDesc", "LS_GDN_EXACT", "LS_GDN_TENSOR_CORE", "LS_GDN_BWD_REUSES_FORWARD", "ls_gdn_workspace_size", "ls_gdn_replay_fwd",
     "ls_gdn_replay_bwd", "ls_stage_pages",
 ]
 
@@ -69,11 +69,12 @@ class Member(ctypes.Structure):
 
 LS_GDN_EXACT = 0
 LS_GDN_TENSOR_CORE = 1
+LS_GDN_BWD_REUSES_FORWARD = 1  # ls_gdn_desc.flags
 
 
 class GdnDesc(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("heads", ctypes.c_int32), ("dk", ctypes.c_int32),
-                ("dv", ctypes.c_int32), ("precision", ctypes.c_int32)]
+                ("dv", ctypes.c_int32), ("precision", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 def library_path() -> Path:
@@ -284,10 +285,10 @@ def ls_sum_parts(parts, out, stream=None):
                               _stream(stream)))
 
 
-def _gdn_desc(s0, q, precision):
+def _gdn_desc(s0, q, precision, flags=0):
     """q [B, R, H, dk] (a group) or [R, H, dk] (one member)."""
     return GdnDesc(q.shape[0] if q.dim() == 4 else 1, s0.shape[0], s0.shape[2], s0.shape[1],
-                   precision)
+                   precision, flags)
 
 
 def _resp_len(q):
@@ -314,10 +315,13 @@ def ls_gdn_replay_fwd(s0, q, k, v, g, beta, o, s_final=None, ws=None, stream=Non
 
 
 def ls_gdn_replay_bwd(s0, q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta, ws, stream=None,
-                      precision=LS_GDN_EXACT):
-    """Gradients of the replay for q, k, v, g, beta (none for s0; see ls.h)."""
+                      precision=LS_GDN_EXACT, reuse_forward=False):
+    """Gradients of the replay for q, k, v, g, beta (none for s0; see ls.h).
+    reuse_forward: ws holds the scratch of ls_gdn_replay_fwd on these same
+    inputs (LS_GDN_BWD_REUSES_FORWARD)."""
     _want_f32(s0, q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta)
-    _check(lib().ls_gdn_replay_bwd(ctypes.byref(_gdn_desc(s0, q, precision)), _ptr(s0), _ptr(q), _ptr(k),
+    desc = _gdn_desc(s0, q, precision, LS_GDN_BWD_REUSES_FORWARD if reuse_forward else 0)
+    _check(lib().ls_gdn_replay_bwd(ctypes.byref(desc), _ptr(s0), _ptr(q), _ptr(k),
                                    _ptr(v), _ptr(g), _ptr(beta), _ptr(d_o), _resp_len(q), _ptr(dq), _ptr(dk),
                                    _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(ws), _nbytes(ws),
                                    _stream(stream)))

@@ -594,6 +594,8 @@ ls_status check_gdn(const ls_gdn_desc* d) {
   if (d->precision != LS_GDN_EXACT && d->precision != LS_GDN_TENSOR_CORE)
     return fail(LS_ERR_INVALID_ARGUMENT, "precision %d is not LS_GDN_EXACT or LS_GDN_TENSOR_CORE",
                 d->precision);
+  if (d->flags & ~LS_GDN_BWD_REUSES_FORWARD)
+    return fail(LS_ERR_INVALID_ARGUMENT, "unknown flags 0x%x", (unsigned)d->flags);
   if (!gdn_supported(d->dk, d->dv))
     return fail(LS_ERR_UNSUPPORTED, "dk=%d dv=%d: supported is dk = dv = 128", d->dk, d->dv);
   return LS_OK;
@@ -651,7 +653,8 @@ ls_status ls_gdn_replay_bwd(const ls_gdn_desc* desc, const float* s0, const floa
   float* scratch = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
   if (desc->precision == LS_GDN_TENSOR_CORE)
     LS_CUDA(launch_gdn_cp_bwd(desc->batch, desc->heads, resp_len, s0, q, k, v, g, beta, d_o, dq, dk,
-                              dv, dg, dbeta, scratch, status, static_cast<cudaStream_t>(stream)),
+                              dv, dg, dbeta, scratch, (desc->flags & LS_GDN_BWD_REUSES_FORWARD) != 0,
+                              status, static_cast<cudaStream_t>(stream)),
             "GDN chunk-parallel backward launch");
   else
     LS_CUDA(launch_gdn_bwd(desc->batch, desc->heads, resp_len, s0, q, k, v, g, beta, d_o, dq, dk,

@@ -47,9 +47,10 @@ using namespace gdn;
 //   kGKblk          the packed GK (prep); its last float holds gamma_C
 // then bf16 tile images of 32 KB in the swizzled shared-memory layout, so a
 // plain copy lands them ready for the MMAs: ZK, ZW, -M, F hi, F lo, -M',
-// F' hi, F' lo (rows as in the formulas above).
+// F' hi, F' lo (rows as in the formulas above), and T hi, T lo (row x =
+// column x of T).
 enum : int { kE0 = 0, kDU0, kSstart, kGend, kEblk, kDUblk, kGKblk, kFloatBlocks };
-enum : int { kImZK = 0, kImZW, kImM, kImFhi, kImFlo, kImMg, kImFghi, kImFglo, kImages };
+enum : int { kImZK = 0, kImZW, kImM, kImFhi, kImFlo, kImMg, kImFghi, kImFglo, kImThi, kImTlo, kImages };
 constexpr int64_t kImgFloats = kTile / 4;
 constexpr int64_t kScrFloats = (int64_t)kFloatBlocks * kTileElems + kImages * kImgFloats;
 constexpr int64_t kGammaAt = (int64_t)kGKblk * kTileElems + kTileElems - 1;
@@ -168,19 +169,18 @@ __device__ __forceinline__ void invert_block64(float* buf, const float* gk, cons
 }
 
 // ---------------------------------------------------------------- prep
-// One CTA per (chunk, head, member), 256 threads in two groups of 128.
-// T = (I + diag(b) GK)^-1 is formed explicitly in fp32 by blocks of 64
-// rows: each diagonal block by forward substitution (group A, one column per
-// thread), the off-diagonal block as T21 = -T22 (diag(b) GK21) T11 by two
-// products on the CUDA cores.  The four right-hand sides are then tensor-core
-// products with T as the A operand, split into bf16 hi + lo parts (their sum
-// is T to about 2^-17):
-//   E0 = T (b V), ZK = T (b gamma K)      (the T tile read M-major)
-//   dU0 = T^T dE0, ZW = T^T (w K)         (the same tile read K-major)
-// Group B stages the right-hand sides while group A forms T.
-// Shared memory: R0 K -> b V, R1 Q -> P^T -> b gamma K, R2 dO -> w K,
-// R3 GK (packed fp32) -> dE0, R4 + R5 (and 512 bytes more) T (fp32) -> T hi (R4),
-// T lo (R5).
+// The forward's share of each chunk, one CTA per (chunk, head, member), 256
+// threads in two groups of 128.  T = (I + diag(b) GK)^-1 is formed
+// explicitly in fp32 by blocks of 64 rows: each diagonal block by forward
+// substitution (group A, one column per thread), the off-diagonal block as
+// T21 = -T22 (diag(b) GK21) T11 by two products on the CUDA cores, while
+// group B stages the right-hand sides.  With T split into bf16 hi + lo parts
+// (their sum is T to about 2^-17) as the A operand (its tile read M-major):
+// E0 = T (b V), ZK = T (b gamma K); then the state chain's terms M = ZK^T W
+// and F = E0^T W.  Written to the scratch: E0, GK, gamma_C, and the images of
+// ZK, -M, F hi / lo and T hi / lo (the last for the backward's own terms).
+// Shared memory: R0 K -> b V -> E0, R1 b gamma K, R2 w K, R3 GK (packed
+// fp32) -> ZK, R4 + R5 (and 512 bytes more) T (fp32) -> T hi (R4), T lo (R5).
 constexpr uint32_t kPrepR0 = 0, kPrepR1 = kTile, kPrepR2 = 2 * kTile, kPrepR3 = 3 * kTile;
 constexpr uint32_t kPrepR4 = 4 * kTile, kPrepR5 = 5 * kTile;
 // T in fp32 (rows of 129 floats) runs 512 bytes past R5
@@ -189,13 +189,10 @@ constexpr uint32_t kPrepSmem = kPrepMisc + 3072 + 1024;
 static_assert(kPrepR4 + kC * kTStride * 4 <= kPrepMisc, "T buffer overlaps the misc area");
 constexpr int kPrepThr = 2 * kThr;
 
-// kBwd = false: the forward's share only (E0, ZK, M, F, gamma_C; no dO).
-template <bool kBwd>
 __global__ void __launch_bounds__(kPrepThr, 1)
-    gdn_cp_prep_kernel(int H, int R, int nch, const float* __restrict__ q,
-                       const float* __restrict__ k, const float* __restrict__ v,
-                       const float* __restrict__ g, const float* __restrict__ beta,
-                       const float* __restrict__ d_o, float* __restrict__ scr,
+    gdn_cp_prep_kernel(int H, int R, int nch, const float* __restrict__ k,
+                       const float* __restrict__ v, const float* __restrict__ g,
+                       const float* __restrict__ beta, float* __restrict__ scr,
                        uint32_t* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -220,8 +217,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   const int nt = R - t0 < kC ? (int)(R - t0) : kC;
   {
     const int64_t tok = (int64_t)m * R * H;
-    q += tok * kD, k += tok * kD, v += tok * kD, g += tok, beta += tok;
-    if (kBwd) d_o += tok * kD;
+    k += tok * kD, v += tok * kD, g += tok, beta += tok;
   }
   float* out = scratch_of(scr, H, nch, m, h, ch);
   if (tid == 0) {
@@ -240,17 +236,9 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   const volatile uint32_t* abortp = abort_s;
   const int64_t rs = (int64_t)H * kD;  // token stride of q, k, v, d_o
   const int64_t row0 = (t0 * H + h) * kD;
-  if (gt < nt) {  // the chunk's rows, asked into L2 up front (q and k are read twice)
-    prefetch_l2((grpA ? k : v) + row0 + gt * rs, kD * 4);
-    if (kBwd) prefetch_l2((grpA ? q : d_o) + row0 + gt * rs, kD * 4);
-  }
+  if (gt < nt) prefetch_l2((grpA ? k : v) + row0 + gt * rs, kD * 4);  // the chunk's rows into L2
 
-  if (grpA) {
-    stage_rows<4>(sb + kPrepR0, k + row0, rs, nt, nullptr, gt);
-    if (kBwd) stage_rows<4>(sb + kPrepR1, q + row0, rs, nt, nullptr, gt);
-  } else if (kBwd) {
-    stage_rows<4>(sb + kPrepR2, d_o + row0, rs, nt, nullptr, gt);
-  }
+  if (grpA) stage_rows<4>(sb + kPrepR0, k + row0, rs, nt, nullptr, gt);
   stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
   fence_proxy_async_smem();
   __syncthreads();
@@ -262,17 +250,16 @@ __global__ void __launch_bounds__(kPrepThr, 1)
     if (gt == 0) out[kGammaAt] = expf(clast);  // gamma_C for the chains
   }
 
-  if (tid == 0) {  // K K^T -> cols 0..127, K Q^T -> 128..255
+  if (tid == 0) {  // K K^T -> cols 0..127
     tc_fence_after();
     mma_group(tb + 0, sb + kPrepR0, sb + kPrepR0, false, false);
-    if (kBwd) mma_group(tb + 128, sb + kPrepR0, sb + kPrepR1, false, false);
     mma_commit(smem_u32(&bars[0]));
   }
   bool ok = mbar_wait_warp(smem_u32(&bars[0]), 0, abortp);
   if (!__syncthreads_or(!ok)) {
     tc_fence_after();
     if (grpA) {
-      // thread r: GK row r (s < r); P^T row r: P^T[r][t] = [t >= r] Gamma_tr (K_r . Q_t)
+      // thread r: GK row r (s < r)
       const int r = gt;
       const float cr = sc[r];
       float* gko = out + (int64_t)kGKblk * kTileElems;
@@ -290,28 +277,9 @@ __global__ void __launch_bounds__(kPrepThr, 1)
             gko[a_at(r, s)] = val;
           }
         }
-        if (kBwd) {
-          tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
-          tmem_wait_ld_r(t32);
-          float pv[32];
-#pragma unroll
-          for (int xx = 0; xx < 32; ++xx) {
-            const int t = cb * 32 + xx;
-            pv[xx] = t >= r ? __expf(sc[t] - cr) * __uint_as_float(t32[xx]) : 0.f;
-          }
-#pragma unroll
-          for (int gg = 0; gg < 4; ++gg) st_shared_v4(sb + kPrepR1 + tile_off(r, cb * 4 + gg), pack8(&pv[8 * gg]));
-        }
       }
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
     __syncthreads();
-    if (kBwd && tid == 0) {  // dE0 = P^T dO -> cols 256..383 (dO as an N-major B)
-      tc_fence_after();
-      mma_group(tb + 256, sb + kPrepR1, sb + kPrepR2, true, false);
-      mma_commit(smem_u32(&bars[1]));
-    }
     if (grpA) {
       // ---- T by blocks of 64 rows.  Column x: T11 (x < 64) or T22 (x >= 64)
       // by substitution; the rest of the column zero.
@@ -364,47 +332,27 @@ __global__ void __launch_bounds__(kPrepThr, 1)
         }
       }
     } else {
-      // ---- group B: the right-hand sides, once P^T dO has read R1 and R2
-      if (kBwd) ok = mbar_wait_warp(smem_u32(&bars[1]), 0, abortp);
-      if (ok) {
-        stage_rows<4>(sb + kPrepR0, v + row0, rs, nt, sbt, gt);  // b V
-        stage_rows<4>(sb + kPrepR1, k + row0, rs, nt, sbg, gt);  // b gamma K
-        stage_rows<4>(sb + kPrepR2, k + row0, rs, nt, swk, gt);  // w K
-      }
+      // ---- group B: the right-hand sides (K K^T has read R0)
+      stage_rows<4>(sb + kPrepR0, v + row0, rs, nt, sbt, gt);  // b V
+      stage_rows<4>(sb + kPrepR1, k + row0, rs, nt, sbg, gt);  // b gamma K
+      stage_rows<4>(sb + kPrepR2, k + row0, rs, nt, swk, gt);  // w K
     }
     if (!__syncthreads_or(!ok)) {
       float tcol[kC];
       if (grpA) {
 #pragma unroll
         for (int t = 0; t < kC; ++t) tcol[t] = buf[b_at(t, gt)];
-      } else if (kBwd) {
-        // dE0 rows (bf16) over GK, which the substitution no longer needs
-        tc_fence_after();
-#pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {
-          uint32_t t32[32];
-          tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
-          tmem_wait_ld_r(t32);
-          float f32[32];
-#pragma unroll
-          for (int xx = 0; xx < 32; ++xx) f32[xx] = __uint_as_float(t32[xx]);
-#pragma unroll
-          for (int gg = 0; gg < 4; ++gg) st_shared_v4(sb + kPrepR3 + tile_off(gt, cb * 4 + gg), pack8(&f32[8 * gg]));
-        }
       }
       __syncthreads();  // T read from R4 / R5 before its bf16 halves overwrite them
-      if (grpA) {  // row x of the hi and lo tiles = column x of T
+      if (grpA) {  // row x of the hi and lo tiles = column x of T; also their images
+        float* ih = image_of(out, kImThi);
+        float* il = image_of(out, kImTlo);
 #pragma unroll
         for (int gq = 0; gq < 16; ++gq) {
           float hi[8], lo[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint16_t hb = bf16_of(tcol[8 * gq + u]);
-            hi[u] = __uint_as_float((uint32_t)hb << 16);
-            lo[u] = tcol[8 * gq + u] - hi[u];
-          }
-          st_shared_v4(sb + kPrepR4 + tile_off(gt, gq), pack8(hi));
-          st_shared_v4(sb + kPrepR5 + tile_off(gt, gq), pack8(lo));
+          split8(&tcol[8 * gq], hi, lo);
+          put_tile_row(true, sb + kPrepR4, ih, gt, hi, gq, 1);
+          put_tile_row(true, sb + kPrepR5, il, gt, lo, gq, 1);
         }
       }
       fence_proxy_async_smem();
@@ -417,45 +365,33 @@ __global__ void __launch_bounds__(kPrepThr, 1)
         mma_group_amn(tb + 0, tl, sb + kPrepR0, true, true);
         mma_group_amn(tb + 128, th, sb + kPrepR1, true, false);  // ZK = T (b gamma K)
         mma_group_amn(tb + 128, tl, sb + kPrepR1, true, true);
-        if (kBwd) {
-          mma_group(tb + 256, th, sb + kPrepR3, true, false);    // dU0 = T^T dE0
-          mma_group(tb + 256, tl, sb + kPrepR3, true, true);
-          mma_group(tb + 384, th, sb + kPrepR2, true, false);    // ZW = T^T (w K)
-          mma_group(tb + 384, tl, sb + kPrepR2, true, true);
-        }
         mma_commit(smem_u32(&bars[2]));
       }
       ok = mbar_wait_warp(smem_u32(&bars[2]), 0, abortp);
       if (!__syncthreads_or(!ok)) {
-        // ---- E0, ZK (warps 0-3) and dU0, ZW (warps 4-7): E0 and dU0 to the
-        // scratch in fp32; bf16 tiles of E0 (R0), ZK (R3), -gamma b dU0 (R4)
-        // and ZW (R5) for the chains' terms, ZK and ZW also as images for out
+        // ---- E0 and ZK (warps 0-3): E0 to the scratch in fp32; bf16 tiles of
+        // E0 (R0) and ZK (R3) for M and F, ZK also as an image for out
         tc_fence_after();
         const int r = gt;  // row = token
-        float* fdst = out + (int64_t)(grpA ? kE0 : kDU0) * kTileElems + r * kD;
-        const uint32_t tA = sb + (grpA ? kPrepR0 : kPrepR4), tB = sb + (grpA ? kPrepR3 : kPrepR5);
-        float* img = image_of(out, grpA ? kImZK : kImZW);
-        const float fa = grpA ? 1.f : -sbg[r];
-        const uint32_t colA = grpA ? 0 : 256;
+        float* fdst = out + (int64_t)kE0 * kTileElems + r * kD;
+        float* img = image_of(out, kImZK);
 #pragma unroll 1
-        for (int cb = 0; (grpA || kBwd) && cb < 4; ++cb) {
+        for (int cb = 0; grpA && cb < 4; ++cb) {
           uint32_t t32[32];
           float f[32];
-          tmem_ld32(tb + lane_off + colA + cb * 32, t32);
+          tmem_ld32(tb + lane_off + cb * 32, t32);
           tmem_wait_ld_r(t32);
 #pragma unroll
           for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
           float4* fd = reinterpret_cast<float4*>(fdst + cb * 32);
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) fd[q4] = make_float4(f[4 * q4], f[4 * q4 + 1], f[4 * q4 + 2], f[4 * q4 + 3]);
-#pragma unroll
-          for (int xx = 0; xx < 32; ++xx) f[xx] *= fa;
-          put_tile_row(true, tA, nullptr, r, f, cb * 4, 4);
-          tmem_ld32(tb + lane_off + colA + 128 + cb * 32, t32);
+          put_tile_row(true, sb + kPrepR0, nullptr, r, f, cb * 4, 4);
+          tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
           tmem_wait_ld_r(t32);
 #pragma unroll
           for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
-          put_tile_row(true, tB, img, r, f, cb * 4, 4);
+          put_tile_row(true, sb + kPrepR3, img, r, f, cb * 4, 4);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -464,70 +400,29 @@ __global__ void __launch_bounds__(kPrepThr, 1)
           tc_fence_after();
           mma_group_amn(tb + 0, sb + kPrepR3, sb + kPrepR2, true, false);    // M = ZK^T W
           mma_group_amn(tb + 128, sb + kPrepR0, sb + kPrepR2, true, false);  // F = E0^T W
-          if (kBwd) mma_group_amn(tb + 256, sb + kPrepR5, sb + kPrepR1, true, false);  // M' = ZW^T diag(b gamma) K
           mma_commit(smem_u32(&bars[3]));
         }
         ok = mbar_wait_warp(smem_u32(&bars[3]), 0, abortp);
         if (!__syncthreads_or(!ok)) {
-          // Q (R0), K (R1), gamma dO (R2) for F'; meanwhile -M, F hi / lo
-          // (group A) and -M' (group B) to their images
+          // -M and F hi / lo to their images (group A)
           tc_fence_after();
-          if (!kBwd) {
-          } else if (grpA) {
-            stage_rows<4>(sb + kPrepR0, q + row0, rs, nt, nullptr, gt);
-            stage_rows<4>(sb + kPrepR1, k + row0, rs, nt, nullptr, gt);
-          } else {
-            stage_rows<4>(sb + kPrepR2, d_o + row0, rs, nt, sgm, gt);
-          }
 #pragma unroll 1
-          for (int cb = 0; (grpA || kBwd) && cb < 4; ++cb) {
+          for (int cb = 0; grpA && cb < 4; ++cb) {
             uint32_t t32[32];
             float f[32], hi[32], lo[32];
-            tmem_ld32(tb + lane_off + (grpA ? 0 : 256) + cb * 32, t32);
+            tmem_ld32(tb + lane_off + cb * 32, t32);
             tmem_wait_ld_r(t32);
 #pragma unroll
             for (int xx = 0; xx < 32; ++xx) f[xx] = -__uint_as_float(t32[xx]);
-            put_tile_row(false, 0, image_of(out, grpA ? kImM : kImMg), r, f, cb * 4, 4);
-            if (grpA) {
-              tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
-              tmem_wait_ld_r(t32);
+            put_tile_row(false, 0, image_of(out, kImM), r, f, cb * 4, 4);
+            tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
+            tmem_wait_ld_r(t32);
 #pragma unroll
-              for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
+            for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
 #pragma unroll
-              for (int gg = 0; gg < 4; ++gg) split8(&f[8 * gg], &hi[8 * gg], &lo[8 * gg]);
-              put_tile_row(false, 0, image_of(out, kImFhi), r, hi, cb * 4, 4);
-              put_tile_row(false, 0, image_of(out, kImFlo), r, lo, cb * 4, 4);
-            }
-          }
-          if (kBwd) {
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            if (tid == 0) {  // F' = (gamma dO)^T Q - (gamma b dU0)^T K -> cols 384..511
-              tc_fence_after();
-              mma_group_amn(tb + 384, sb + kPrepR2, sb + kPrepR0, true, false);
-              mma_group_amn(tb + 384, sb + kPrepR4, sb + kPrepR1, true, true);
-              mma_commit(smem_u32(&bars[4]));
-            }
-            ok = mbar_wait_warp(smem_u32(&bars[4]), 0, abortp);
-            if (!__syncthreads_or(!ok)) {
-              // F' hi / lo: group A columns 0..63, group B 64..127
-              tc_fence_after();
-#pragma unroll 1
-              for (int cb = 0; cb < 2; ++cb) {
-                const int c0 = (grpA ? 0 : 64) + cb * 32;
-                uint32_t t32[32];
-                float f[32], hi[32], lo[32];
-                tmem_ld32(tb + lane_off + 384 + c0, t32);
-                tmem_wait_ld_r(t32);
-#pragma unroll
-                for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
-#pragma unroll
-                for (int gg = 0; gg < 4; ++gg) split8(&f[8 * gg], &hi[8 * gg], &lo[8 * gg]);
-                put_tile_row(false, 0, image_of(out, kImFghi), r, hi, c0 / 8, 4);
-                put_tile_row(false, 0, image_of(out, kImFglo), r, lo, c0 / 8, 4);
-              }
-            }
+            for (int gg = 0; gg < 4; ++gg) split8(&f[8 * gg], &hi[8 * gg], &lo[8 * gg]);
+            put_tile_row(false, 0, image_of(out, kImFhi), r, hi, cb * 4, 4);
+            put_tile_row(false, 0, image_of(out, kImFlo), r, lo, cb * 4, 4);
           }
         }
       }
@@ -537,6 +432,250 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   if (tid == 0) {  // drain before tensor memory is freed
     mma_commit(smem_u32(&bars[5]));
     mbar_wait(smem_u32(&bars[5]), 0, abortp);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tb, 512);
+  }
+}
+
+// ---------------------------------------------------------------- prep (backward's terms)
+// The backward's own terms of each chunk from the T that the forward share
+// left in the scratch (its hi and lo images, brought in by bulk copy): one
+// CTA per (chunk, head, member), 256 threads in two groups of 128.
+//   dE0 = P^T dO (P^T from a K Q^T product), dU0 = T^T dE0, ZW = T^T W,
+//   M' = ZW^T diag(gamma b) K, F' = (gamma dO)^T Q - (gamma b dU0)^T K.
+// Written to the scratch: dU0, and the images of ZW, -M', F' hi / lo.
+// Shared memory: G0 K, G1 Q -> P^T -> b gamma K, G2 dO -> w K -> Q,
+// G3 dE0 -> -gamma b dU0, G4 T hi -> gamma dO, G5 T lo -> ZW.
+constexpr uint32_t kGr0 = 0, kGr1 = kTile, kGr2 = 2 * kTile, kGr3 = 3 * kTile, kGr4 = 4 * kTile,
+                   kGr5 = 5 * kTile, kGrMisc = 6 * kTile;
+constexpr uint32_t kGrSmem = kGrMisc + 3072 + 1024;
+
+__global__ void __launch_bounds__(kPrepThr, 1)
+    gdn_cp_prep_grad_kernel(int H, int R, int nch, const float* __restrict__ q,
+                            const float* __restrict__ k, const float* __restrict__ g,
+                            const float* __restrict__ beta, const float* __restrict__ d_o,
+                            float* __restrict__ scr, uint32_t* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(sm);
+  float* sc = reinterpret_cast<float*>(sm + kGrMisc);
+  float* sbt = sc + kC;    // b
+  float* sbg = sbt + kC;   // b gamma
+  float* swk = sbg + kC;   // w (zero past the response)
+  float* sgm = swk + kC;   // gamma
+  float* swt = sgm + kC;   // 8 floats of scan scratch
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kGrMisc + 2624);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 6);
+  uint32_t* abort_s = tslot + 1;
+  uint32_t* never_s = tslot + 2;  // stays 0: the drain's waits are bounded by time alone
+
+  const int ch = blockIdx.x, h = blockIdx.y, m = blockIdx.z, tid = threadIdx.x, warp = tid >> 5;
+  const bool grpA = tid < kThr;
+  const int gt = tid & (kThr - 1);  // index within the group: row
+  const int64_t t0 = (int64_t)ch * kC;
+  const int nt = R - t0 < kC ? (int)(R - t0) : kC;
+  {
+    const int64_t tok = (int64_t)m * R * H;
+    q += tok * kD, k += tok * kD, d_o += tok * kD, g += tok, beta += tok;
+  }
+  float* out = scratch_of(scr, H, nch, m, h, ch);
+  if (tid == 0) {
+    for (int i = 0; i < 6; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    *abort_s = 0;
+    *never_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tslot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = *tslot, lane_off = (uint32_t)((warp & 3) * 32) << 16;
+  const volatile uint32_t* abortp = abort_s;
+  const int64_t rs = (int64_t)H * kD;
+  const int64_t row0 = (t0 * H + h) * kD;
+  if (tid == 0) {  // T hi, T lo
+    const uint32_t bar = smem_u32(&bars[2]);
+    mbar_expect_tx(bar, 2 * kTile);
+    bulk_load(sb + kGr4, image_of(out, kImThi), kTile, bar);
+    bulk_load(sb + kGr5, image_of(out, kImTlo), kTile, bar);
+  }
+  if (gt < nt) {  // the chunk's rows into L2 (k and q are read twice)
+    prefetch_l2((grpA ? k : d_o) + row0 + gt * rs, kD * 4);
+    if (grpA) prefetch_l2(q + row0 + gt * rs, kD * 4);
+  }
+  if (grpA) {
+    stage_rows<4>(sb + kGr0, k + row0, rs, nt, nullptr, gt);
+    stage_rows<4>(sb + kGr1, q + row0, rs, nt, nullptr, gt);
+  } else {
+    stage_rows<4>(sb + kGr2, d_o + row0, rs, nt, nullptr, gt);
+  }
+  stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (!grpA) {  // row scales (read after the next block barrier)
+    const float ct = sc[gt], clast = sc[kC - 1];
+    sgm[gt] = __expf(ct);
+    sbg[gt] = sbt[gt] * sgm[gt];
+    swk[gt] = gt < nt ? __expf(clast - ct) : 0.f;
+  }
+  if (tid == 0) {  // K Q^T -> cols 0..127
+    tc_fence_after();
+    mma_group(tb + 0, sb + kGr0, sb + kGr1, false, false);
+    mma_commit(smem_u32(&bars[0]));
+  }
+  bool ok = mbar_wait_warp(smem_u32(&bars[0]), 0, abortp);
+  bool copied = false;  // thread 0: the T copies were waited for
+  if (!__syncthreads_or(!ok)) {
+    tc_fence_after();
+    if (grpA) {  // P^T row r: P^T[r][t] = [t >= r] Gamma_tr (K_r . Q_t), over Q (G1)
+      const int r = gt;
+      const float cr = sc[r];
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t t32[32];
+        float pv[32];
+        tmem_ld32(tb + lane_off + cb * 32, t32);
+        tmem_wait_ld_r(t32);
+#pragma unroll
+        for (int xx = 0; xx < 32; ++xx) {
+          const int t = cb * 32 + xx;
+          pv[xx] = t >= r ? __expf(sc[t] - cr) * __uint_as_float(t32[xx]) : 0.f;
+        }
+        put_tile_row(true, sb + kGr1, nullptr, r, pv, cb * 4, 4);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {  // dE0 = P^T dO -> cols 128..255 (dO as an N-major B)
+      tc_fence_after();
+      mma_group(tb + 128, sb + kGr1, sb + kGr2, true, false);
+      mma_commit(smem_u32(&bars[1]));
+    }
+    ok = mbar_wait_warp(smem_u32(&bars[1]), 0, abortp);
+    if (!__syncthreads_or(!ok)) {
+      tc_fence_after();
+      if (grpA) {  // dE0 rows (bf16) into G3
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+          uint32_t t32[32];
+          float f[32];
+          tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
+          tmem_wait_ld_r(t32);
+#pragma unroll
+          for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
+          put_tile_row(true, sb + kGr3, nullptr, gt, f, cb * 4, 4);
+        }
+      } else {  // the products have read P^T (G1) and dO (G2)
+        stage_rows<4>(sb + kGr2, k + row0, rs, nt, swk, gt);  // w K
+        stage_rows<4>(sb + kGr1, k + row0, rs, nt, sbg, gt);  // b gamma K
+      }
+      if (warp == 0) {
+        ok = mbar_wait_warp(smem_u32(&bars[2]), 0, abortp);  // T hi, T lo landed
+        if (tid == 0) copied = ok;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      if (!__syncthreads_or(!ok)) {
+        if (tid == 0) {
+          tc_fence_after();
+          mma_group(tb + 256, sb + kGr4, sb + kGr3, true, false);  // dU0 = T^T dE0
+          mma_group(tb + 256, sb + kGr5, sb + kGr3, true, true);
+          mma_group(tb + 384, sb + kGr4, sb + kGr2, true, false);  // ZW = T^T (w K)
+          mma_group(tb + 384, sb + kGr5, sb + kGr2, true, true);
+          mma_commit(smem_u32(&bars[3]));
+        }
+        ok = mbar_wait_warp(smem_u32(&bars[3]), 0, abortp);
+        if (!__syncthreads_or(!ok)) {
+          // group A: dU0 rows to the scratch (fp32) and -gamma b dU0 into G3,
+          // then Q into G2; group B: ZW rows into G5 and its image, then
+          // gamma dO into G4
+          tc_fence_after();
+          const int r = gt;
+          if (grpA) {
+            float* fdst = out + (int64_t)kDU0 * kTileElems + r * kD;
+            const float fa = -sbg[r];
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {
+              uint32_t t32[32];
+              float f[32];
+              tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
+              tmem_wait_ld_r(t32);
+#pragma unroll
+              for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
+              float4* fd = reinterpret_cast<float4*>(fdst + cb * 32);
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4) fd[q4] = make_float4(f[4 * q4], f[4 * q4 + 1], f[4 * q4 + 2], f[4 * q4 + 3]);
+#pragma unroll
+              for (int xx = 0; xx < 32; ++xx) f[xx] *= fa;
+              put_tile_row(true, sb + kGr3, nullptr, r, f, cb * 4, 4);
+            }
+            stage_rows<4>(sb + kGr2, q + row0, rs, nt, nullptr, gt);
+          } else {
+            float* img = image_of(out, kImZW);
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {
+              uint32_t t32[32];
+              float f[32];
+              tmem_ld32(tb + lane_off + 384 + cb * 32, t32);
+              tmem_wait_ld_r(t32);
+#pragma unroll
+              for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
+              put_tile_row(true, sb + kGr5, img, r, f, cb * 4, 4);
+            }
+            stage_rows<4>(sb + kGr4, d_o + row0, rs, nt, sgm, gt);
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncthreads();
+          if (tid == 0) {
+            tc_fence_after();
+            mma_group_amn(tb + 0, sb + kGr5, sb + kGr1, true, false);    // M' = ZW^T diag(b gamma) K
+            mma_group_amn(tb + 128, sb + kGr4, sb + kGr2, true, false);  // F' = (gamma dO)^T Q
+            mma_group_amn(tb + 128, sb + kGr3, sb + kGr0, true, true);   //      - (gamma b dU0)^T K
+            mma_commit(smem_u32(&bars[4]));
+          }
+          ok = mbar_wait_warp(smem_u32(&bars[4]), 0, abortp);
+          if (!__syncthreads_or(!ok)) {
+            // -M' (group A) and F' hi / lo (group B) to their images
+            tc_fence_after();
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {
+              uint32_t t32[32];
+              float f[32], hi[32], lo[32];
+              tmem_ld32(tb + lane_off + (grpA ? 0 : 128) + cb * 32, t32);
+              tmem_wait_ld_r(t32);
+              if (grpA) {
+#pragma unroll
+                for (int xx = 0; xx < 32; ++xx) f[xx] = -__uint_as_float(t32[xx]);
+                put_tile_row(false, 0, image_of(out, kImMg), r, f, cb * 4, 4);
+              } else {
+#pragma unroll
+                for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
+#pragma unroll
+                for (int gg = 0; gg < 4; ++gg) split8(&f[8 * gg], &hi[8 * gg], &lo[8 * gg]);
+                put_tile_row(false, 0, image_of(out, kImFghi), r, hi, cb * 4, 4);
+                put_tile_row(false, 0, image_of(out, kImFglo), r, lo, cb * 4, 4);
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+  if (__syncthreads_or(!ok) && tid == 0 && status) atomicOr(status, kStatusTimeout);
+  if (tid == 0) {  // drain: the products, and the T copies if nobody waited for them
+    mma_commit(smem_u32(&bars[5]));
+    mbar_wait(smem_u32(&bars[5]), 0, never_s);
+    if (!copied) mbar_wait(smem_u32(&bars[2]), 0, never_s);
   }
   tc_fence_before();
   __syncthreads();
@@ -560,10 +699,13 @@ constexpr uint32_t kChI = 0, kChShi = kTile, kChSlo = 2 * kTile, kChM = 3 * kTil
 constexpr uint32_t kChainSmem = kChMisc + 1024 + 1024;
 constexpr int kChThr = 2 * kThr;
 
-// passes = 1: the state forward alone (the replay's forward), writing s_final.
+// Steps i0 .. i1-1 of the 2 nch steps (forward over the chunks, then backward):
+// [0, nch) the replay's forward (writing s_final), [nch, 2 nch) the backward
+// alone (the forward's S already in the scratch), [0, 2 nch) both.
 __global__ void __launch_bounds__(kChThr, 1)
-    gdn_cp_chain_kernel(int H, int nch, int passes, const float* __restrict__ s0, float* __restrict__ scr,
-                        float* __restrict__ s_final, uint32_t* __restrict__ status) {
+    gdn_cp_chain_kernel(int H, int nch, int i0, int i1, const float* __restrict__ s0,
+                        float* __restrict__ scr, float* __restrict__ s_final,
+                        uint32_t* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -612,21 +754,21 @@ __global__ void __launch_bounds__(kChThr, 1)
     bulk_load(sb + kChFhi, image_of(blk, bw ? kImFghi : kImFhi), kTile, bar);
     bulk_load(sb + kChFlo, image_of(blk, bw ? kImFglo : kImFlo), kTile, bar);
   };
-  if (tid == 0) issue(0);
+  if (tid == 0 && i0 < i1) issue(i0);
 
   float st[64];  // S (forward), then G (backward): row x, columns c0 .. c0+63, fp32
   {
     const float4* src = reinterpret_cast<const float4*>(s0 + ((int64_t)h * kD + x) * kD + c0);
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-      const float4 a4 = src[c];
+      const float4 a4 = i0 < nch ? src[c] : make_float4(0.f, 0.f, 0.f, 0.f);
       st[4 * c] = a4.x, st[4 * c + 1] = a4.y, st[4 * c + 2] = a4.z, st[4 * c + 3] = a4.w;
     }
   }
-  const int steps = passes * nch;
-  for (int i = 0; ok && i <= steps; ++i) {
+  const int steps = i1;
+  for (int i = i0; ok && i <= steps; ++i) {
     const bool bw = i >= nch;
-    if (i == nch) {
+    if (i == nch && i0 < nch) {
       if (s_final) {
         float4* dst = reinterpret_cast<float4*>(s_final + (((int64_t)m * H + h) * kD + x) * kD + c0);
 #pragma unroll
@@ -714,7 +856,7 @@ __global__ void __launch_bounds__(kChThr, 1)
 //         dgamma = rowsum(dO . Q S^T) - rowsum(b . dU . K S^T),
 //         and dc_last += sum(rw) + gamma_C <G, S>.
 constexpr uint32_t kOutMisc = 6 * kTile;
-constexpr uint32_t kOutSmem = kOutMisc + 6144 + 1024;
+constexpr uint32_t kOutSmem = kOutMisc + 8192 + 1024;
 constexpr int kOutThr = 2 * kThr;
 
 // 256 threads: thread (t, hf) owns token row t and the column half
@@ -742,6 +884,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
   float* part = rcol + kC;     // [5][128] row sums of the second column half
   float* swt = part + 5 * kC;  // 8 floats of scan and reduction scratch
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOutMisc + 5184);
+  float* colpart = reinterpret_cast<float*>(sm + kOutMisc + 5376);  // [4][128] column sums of r per row quarter
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 6);
   uint32_t* abort_s = tslot + 1;
 
@@ -844,7 +987,6 @@ __global__ void __launch_bounds__(kOutThr, 1)
   if (hf == 0) {
     sgam[t] = expf(sc[t]);
     sw[t] = live ? expf(sc[kC - 1] - sc[t]) : 0.f;
-    rcol[t] = 0.f;
   }
   fence_proxy_async_smem();
   __syncthreads();
@@ -978,10 +1120,11 @@ __global__ void __launch_bounds__(kOutThr, 1)
         }
       }
       // row sums of r stay with the thread; column sums over the warp's rows
-      // by a shuffle exchange, then one shared add per column and warp
+      // by a shuffle exchange, one slot per (row quarter, column): summed in
+      // a fixed order later, so the result does not depend on warp timing
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) rrow += rv[xx];
-      atomicAdd(&rcol[cb * 32 + lane], warp_colsum32(rv));
+      colpart[(warp & 3) * kC + cb * 32 + lane] = warp_colsum32(rv);
       // E G row t: rw = w . rowsum(E G . K)
       row_ld32(f32, k + rowt + cb * 32, live);
       tmem_ld32(tb + lane_off + 384 + cb * 32, t32);
@@ -1081,7 +1224,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) gs = fmaf(ga[xx], sa[xx], gs);
     }
-    // the second half's row sums to the first
+    // the second half's row sums to the first; the column sums of r
     if (hf) {
       part[0 * kC + t] = dgam;
       part[1 * kC + t] = dbt;
@@ -1092,6 +1235,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
     __syncthreads();
     float rws = 0.f;
     if (!hf) {
+      rcol[t] = ((colpart[t] + colpart[kC + t]) + colpart[2 * kC + t]) + colpart[3 * kC + t];
       dgam += part[0 * kC + t];
       dbt += part[1 * kC + t];
       rrow += part[2 * kC + t];
@@ -1297,10 +1441,10 @@ size_t gdn_cp_workspace_bytes(int B, int H, int R) {
 namespace {
 cudaError_t set_smem_attributes() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(gdn_cp_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if ((e = cudaFuncSetAttribute(gdn_cp_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kPrepSmem)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(gdn_cp_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kPrepSmem)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(gdn_cp_prep_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kGrSmem)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(gdn_cp_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kChainSmem)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(gdn_cp_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1317,8 +1461,8 @@ bool misaligned(std::initializer_list<const void*> ps) {
 }
 }  // namespace
 
-// The forward in chunk-parallel form: prep's forward share over all chunks,
-// the state chain per (head, member), then o over all chunks.  ws holds the
+// The forward in chunk-parallel form: the forward share of every chunk, the
+// state chain per (head, member), then o over all chunks.  ws holds the
 // scratch (gdn_cp_workspace_bytes); s0, q, k, v, o and s_final 16-byte aligned.
 cudaError_t launch_gdn_cp_fwd(int B, int H, int R, const float* s0, const float* q, const float* k,
                               const float* v, const float* g, const float* beta, float* o,
@@ -1330,23 +1474,24 @@ cudaError_t launch_gdn_cp_fwd(int B, int H, int R, const float* s0, const float*
   cudaError_t e;
   if ((e = set_smem_attributes()) != cudaSuccess) return e;
   LaunchScope ls(kKGdnFwd, st);
-  gdn_cp_prep_kernel<false><<<dim3(nch, H, B), kPrepThr, kPrepSmem, st>>>(H, R, nch, q, k, v, g, beta,
-                                                                        nullptr, ws, status);
+  gdn_cp_prep_kernel<<<dim3(nch, H, B), kPrepThr, kPrepSmem, st>>>(H, R, nch, k, v, g, beta, ws, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  gdn_cp_chain_kernel<<<dim3(H, B), kChThr, kChainSmem, st>>>(H, nch, 1, s0, ws, s_final, status);
+  gdn_cp_chain_kernel<<<dim3(H, B), kChThr, kChainSmem, st>>>(H, nch, 0, nch, s0, ws, s_final, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gdn_cp_fwd_out_kernel<<<dim3(nch, H, B), kOutThr, kFoSmem, st>>>(H, R, nch, q, k, g, beta, ws, o,
                                                                   status);
   return cudaGetLastError();
 }
 
-// The backward in chunk-parallel form: prep over all chunks, the two chains
-// per (head, member), then the outputs over all chunks.  ws holds the
-// scratch (gdn_cp_workspace_bytes); q, k, v and d_o must be 16-byte aligned.
+// The backward in chunk-parallel form: the forward share of every chunk
+// (unless reuse_forward: the scratch already holds it, from the forward on
+// the same inputs), the backward's own terms, the chains (the backward one
+// alone under reuse_forward), then the outputs over all chunks.  ws holds
+// the scratch; s0, q, k, v, d_o, dq, dk, dv 16-byte aligned.
 cudaError_t launch_gdn_cp_bwd(int B, int H, int R, const float* s0, const float* q, const float* k,
                               const float* v, const float* g, const float* beta, const float* d_o,
                               float* dq, float* dk, float* dv, float* dg, float* dbeta, float* ws,
-                              uint32_t* status, cudaStream_t st) {
+                              bool reuse_forward, uint32_t* status, cudaStream_t st) {
   if (B == 0 || H == 0 || R == 0) return cudaSuccess;
   if (H > 65535 || B > 65535) return cudaErrorInvalidValue;  // grid y and z
   if (misaligned({s0, q, k, v, d_o, dq, dk, dv, ws})) return cudaErrorMisalignedAddress;
@@ -1354,10 +1499,16 @@ cudaError_t launch_gdn_cp_bwd(int B, int H, int R, const float* s0, const float*
   cudaError_t e;
   if ((e = set_smem_attributes()) != cudaSuccess) return e;
   LaunchScope ls(kKGdnBwd, st);
-  gdn_cp_prep_kernel<true><<<dim3(nch, H, B), kPrepThr, kPrepSmem, st>>>(H, R, nch, q, k, v, g, beta, d_o,
-                                                                       ws, status);
+  if (!reuse_forward) {
+    gdn_cp_prep_kernel<<<dim3(nch, H, B), kPrepThr, kPrepSmem, st>>>(H, R, nch, k, v, g, beta, ws,
+                                                                    status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  gdn_cp_prep_grad_kernel<<<dim3(nch, H, B), kPrepThr, kGrSmem, st>>>(H, R, nch, q, k, g, beta, d_o, ws,
+                                                                     status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  gdn_cp_chain_kernel<<<dim3(H, B), kChThr, kChainSmem, st>>>(H, nch, 2, s0, ws, nullptr, status);
+  gdn_cp_chain_kernel<<<dim3(H, B), kChThr, kChainSmem, st>>>(H, nch, reuse_forward ? nch : 0, 2 * nch,
+                                                             s0, ws, nullptr, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gdn_cp_out_kernel<<<dim3(nch, H, B), kOutThr, kOutSmem, st>>>(H, R, nch, q, k, v, g, beta, d_o, ws,
                                                                nullptr, dq, dk, dv, dg, dbeta, status);

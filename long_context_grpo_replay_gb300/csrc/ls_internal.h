@@ -167,10 +167,11 @@ size_t gdn_cp_workspace_bytes(int B, int H, int R);
 cudaError_t launch_gdn_cp_fwd(int B, int H, int R, const float* s0, const float* q, const float* k,
                               const float* v, const float* g, const float* beta, float* o,
                               float* s_final, float* ws, uint32_t* status, cudaStream_t st);
+// reuse_forward: ws holds the scratch of launch_gdn_cp_fwd on the same inputs.
 cudaError_t launch_gdn_cp_bwd(int B, int H, int R, const float* s0, const float* q, const float* k,
                               const float* v, const float* g, const float* beta, const float* d_o,
                               float* dq, float* dk, float* dv, float* dg, float* dbeta, float* ws,
-                              uint32_t* status, cudaStream_t st);
+                              bool reuse_forward, uint32_t* status, cudaStream_t st);
 cudaError_t launch_gdn_bwd(int B, int H, int R, const float* s0, const float* q, const float* k,
                            const float* v, const float* g, const float* beta, const float* d_o,
                            float* dq, float* dk, float* dv, float* dg, float* dbeta, float* ws,

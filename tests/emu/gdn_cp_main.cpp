@@ -1,8 +1,8 @@
 // Runs the chunk-parallel GDN kernels' source on the CPU block emulator:
-//   gdn_cp_emu <stage> <in.bin> <out.bin>      stage: prep | all | fwd
+//   gdn_cp_emu <stage> <in.bin> <out.bin>      stage: prep | all | fwd | fwd_bwd
 // in.bin: int32 B, H, R; float32 s0 [H][128][128], q, k, v, d_o [B][R][H][128],
 // g, beta [B][R][H].  out.bin: uint32 status; the float32 scratch; then (all,
-// fwd) o, s_final, dq, dk, dv, dg, dbeta (the gradients zero after fwd).
+// fwd, fwd_bwd) o, s_final, dq, dk, dv, dg, dbeta (the gradients zero after fwd).
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -19,7 +19,10 @@ alignas(1024) unsigned char smem_raw[emu::kSmemBytes];
 
 int main(int argc, char** argv) {
   if (argc != 4) return 2;
-  const int mode = std::strcmp(argv[1], "all") == 0 ? 1 : std::strcmp(argv[1], "fwd") == 0 ? 2 : 0;
+  const int mode = std::strcmp(argv[1], "all") == 0       ? 1
+                   : std::strcmp(argv[1], "fwd") == 0     ? 2
+                   : std::strcmp(argv[1], "fwd_bwd") == 0 ? 3
+                                                          : 0;
   FILE* f = std::fopen(argv[2], "rb");
   if (!f) return 3;
   int32_t hdr[3];

@@ -22,10 +22,10 @@ SRC = CSRC / "ls_gdn_cp.cu"
 TOL_BF16 = 2e-2
 # scratch per chunk: float32 [128 x 128] blocks E0, dU0, S_start, G_end, E,
 # dU, GK; then bf16 tile images (32 KB, the swizzled shared-memory layout)
-# ZK, ZW, -M, F hi, F lo, -M', F' hi, F' lo
-FLOAT_BLOCKS, IMAGES = 7, 8
+# ZK, ZW, -M, F hi, F lo, -M', F' hi, F' lo, T hi, T lo
+FLOAT_BLOCKS, IMAGES = 7, 10
 B_E0, B_DU0, B_SSTART, B_GEND, B_E, B_DU = range(6)
-I_ZK, I_ZW, I_M, I_FHI, I_FLO, I_MG, I_FGHI, I_FGLO = range(8)
+I_ZK, I_ZW, I_M, I_FHI, I_FLO, I_MG, I_FGHI, I_FGLO, I_THI, I_TLO = range(10)
 SCR_FLOATS = FLOAT_BLOCKS * 128 * 128 + IMAGES * 8192
 
 
@@ -122,6 +122,14 @@ def test_prep_solves_match_the_reference(emulator):
             M, F, Mg, Fg = _chain_terms(args[0], args[1], args[3], args[4], args[5], E0, ZK, dU0, ZW)
             n = t1 - t0
             sc = scr[0, h, ch]
+            # T = (I + diag(b) GK)^-1, stored as its transpose's rows (row x = column x)
+            n_ = t1 - t0
+            kk, gg, bb = args[0], args[4], args[5]
+            cc = np.cumsum(gg)
+            A = bb[:, None] * np.tril(np.exp(cc[:, None] - cc[None, :]) * (kk @ kk.T), -1)
+            Tn = np.linalg.inv(np.eye(n_) + A)
+            Tt = image(sc, I_THI).astype(np.float64) + image(sc, I_TLO)
+            errs["T"] = max(errs.get("T", 0.0), rel(Tt[:n_, :n_].T, Tn))
             got = {"E0": block(sc, B_E0), "dU0": block(sc, B_DU0), "ZK": image(sc, I_ZK),
                    "ZW": image(sc, I_ZW), "M": -image(sc, I_M),
                    "F": image(sc, I_FHI).astype(np.float64) + image(sc, I_FLO),
@@ -322,3 +330,20 @@ def test_emulator_rejects_planted_kernel_mistakes(tmp_path, mutation):
     exe = build(tmp_path, mutation)
     errs = _forward_errors(exe, tmp_path, 1, 1, 300, seed=61)
     assert not all(e <= TOL_BF16 for e in errs.values()), errs
+
+
+def test_backward_reusing_the_forward_scratch_is_bit_identical(emulator):
+    """The forward, then the backward with the forward's scratch (its terms
+    and states not formed again), gives the gradients of the backward that
+    forms everything itself, bit for bit."""
+    exe, d = emulator
+    B, H, R = 2, 1, 300
+    c = inputs.make_gdn_group(B, H, R, seed=71)
+    st1, _, full = run(exe, d, c, "all")
+    st2, _, reuse = run(exe, d, c, "fwd_bwd")
+    assert st1 == 0 and st2 == 0
+    g1, g2 = _replay_outputs(full, B, H, R), _replay_outputs(reuse, B, H, R)
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert np.array_equal(g1[name], g2[name]), name
+    for name in ("o", "s_final"):  # the reusing run's o and s_final come from the forward
+        assert np.array_equal(g1[name], g2[name]), name

@@ -89,3 +89,30 @@ def test_chunk_path_at_bench_size_sampled(cuda_device):
     assert torch.isfinite(o).all() and torch.isfinite(s_final).all()
     assert all(torch.isfinite(t).all() for t in grads.values())
     _check(c, o, s_final, 6, (1, 30), grads)
+
+
+@pytest.mark.parametrize("B,H,R", [(2, 3, 300), (8, 32, 4096)], ids=["three_chunks", "bench_size"])
+def test_backward_reusing_the_forward_is_bit_identical(cuda_device, B, H, R):
+    """ls_gdn_replay_fwd, then ls_gdn_replay_bwd with LS_GDN_BWD_REUSES_FORWARD on
+    the same workspace: the gradients equal, bit for bit, those of a backward
+    that forms every term itself (the column sums of the output kernel are
+    summed in a fixed order, so both runs are deterministic)."""
+    c = inputs.make_gdn_group(B, H, R, seed=90 + R, device=cuda_device)
+    want = _bwd(c)
+    ws = torch.empty(ls.ls_gdn_workspace_size(ls.GdnDesc(B, H, 128, 128, TC), R), dtype=torch.uint8,
+                     device=cuda_device)
+    ls.ls_clear_device_status(ws)
+    o = torch.empty_like(c["v"])
+    s_final = torch.empty((B, H, 128, 128), device=cuda_device)
+    ls.ls_gdn_replay_fwd(c["s0"], c["q"], c["k"], c["v"], c["g"], c["beta"], o, s_final, ws, precision=TC)
+    got = {n: torch.empty_like(c[x]) for n, x in
+           (("dq", "q"), ("dk", "k"), ("dv", "v"), ("dg", "g"), ("dbeta", "beta"))}
+    ls.ls_gdn_replay_bwd(c["s0"], c["q"], c["k"], c["v"], c["g"], c["beta"], c["d_o"], got["dq"], got["dk"],
+                         got["dv"], got["dg"], got["dbeta"], ws, precision=TC, reuse_forward=True)
+    torch.cuda.synchronize()
+    ls.ls_read_device_status(ws)
+    for name in want:
+        assert torch.equal(got[name], want[name]), name
+    if R <= 300:
+        for b in range(B):
+            _check(c, o, s_final, b, range(H), got)
