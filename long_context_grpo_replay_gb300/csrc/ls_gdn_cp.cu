@@ -40,20 +40,23 @@ namespace ls {
 namespace {
 using namespace gdn;
 
-// float32 scratch per (member, head, chunk), in [128 x 128] blocks:
+// float32 scratch per (member, head, chunk), in [128 x 128] blocks stored
+// column-group interleaved (element (r, c) at ((c / 4) * 128 + r) * 4 + c % 4:
+// the 32 threads of a warp, holding 32 consecutive rows, touch 512
+// contiguous bytes with each 16-byte access):
 //   kE0, kDU0       E0 and dU0 (prep)
 //   kSstart, kGend  S at the chunk's start, G = dL/dS at its end (chain)
 //   kEblk, kDUblk   E and dU (out, for its own later passes)
-//   kGKblk          the packed GK (prep); its last float holds gamma_C
+//   kGKblk          GK (prep; zero on and above the diagonal)
 // then bf16 tile images of 32 KB in the swizzled shared-memory layout, so a
 // plain copy lands them ready for the MMAs: ZK, ZW, -M, F hi, F lo, -M',
 // F' hi, F' lo (rows as in the formulas above), and T hi, T lo (row x =
-// column x of T).
+// column x of T); then 16 floats, the first gamma_C.
 enum : int { kE0 = 0, kDU0, kSstart, kGend, kEblk, kDUblk, kGKblk, kFloatBlocks };
 enum : int { kImZK = 0, kImZW, kImM, kImFhi, kImFlo, kImMg, kImFghi, kImFglo, kImThi, kImTlo, kImages };
 constexpr int64_t kImgFloats = kTile / 4;
-constexpr int64_t kScrFloats = (int64_t)kFloatBlocks * kTileElems + kImages * kImgFloats;
-constexpr int64_t kGammaAt = (int64_t)kGKblk * kTileElems + kTileElems - 1;
+constexpr int64_t kGammaAt = (int64_t)kFloatBlocks * kTileElems + kImages * kImgFloats;
+constexpr int64_t kScrFloats = kGammaAt + 16;
 
 __device__ __forceinline__ float* scratch_of(float* scr, int H, int nch, int m, int h, int ch) {
   return scr + (((int64_t)m * H + h) * nch + ch) * kScrFloats;
@@ -91,6 +94,34 @@ __device__ __forceinline__ void copy_image(uint32_t tile, const float* img, int 
     for (int j = 0; j < 8; ++j) v[j] = src[tid + kThr * (i0 + j)];
 #pragma unroll
     for (int j = 0; j < 8; ++j) st_shared_v4(tile + 16u * (tid + kThr * (i0 + j)), v[j]);
+  }
+}
+// Row r, columns c0 .. c0+31 of an interleaved scratch block.
+__device__ __forceinline__ float4* blk4(float* b, int r, int c4) {
+  return reinterpret_cast<float4*>(b) + c4 * kC + r;
+}
+__device__ __forceinline__ const float4* blk4(const float* b, int r, int c4) {
+  return reinterpret_cast<const float4*>(b) + c4 * kC + r;
+}
+__device__ __forceinline__ void blk_ld32(float* v, const float* b, int r, int c0) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 a = *blk4(b, r, c0 / 4 + i);
+    v[4 * i] = a.x, v[4 * i + 1] = a.y, v[4 * i + 2] = a.z, v[4 * i + 3] = a.w;
+  }
+}
+__device__ __forceinline__ void blk_st32(const float* v, float* b, int r, int c0) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) *blk4(b, r, c0 / 4 + i) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+// Row r of an interleaved scratch block into row r of a bf16 tile.
+__device__ __forceinline__ void stage_row_blk(uint32_t tile, const float* b, int r) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < kD; c0 += 32) {
+    float v[32];
+    blk_ld32(v, b, r, c0);
+#pragma unroll
+    for (int gg = 0; gg < 4; ++gg) st_shared_v4(tile + tile_off(r, c0 / 8 + gg), pack8(&v[8 * gg]));
   }
 }
 // 32 consecutive floats of one row, 16-byte pieces (zeros when !valid).
@@ -266,17 +297,20 @@ __global__ void __launch_bounds__(kPrepThr, 1)
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t t32[32];
+        float row[32];
         tmem_ld32(tb + lane_off + 0 + cb * 32, t32);
         tmem_wait_ld_r(t32);
 #pragma unroll
         for (int xx = 0; xx < 32; ++xx) {
           const int s = cb * 32 + xx;
+          row[xx] = 0.f;
           if (s < r) {
             const float val = __expf(cr - sc[s]) * __uint_as_float(t32[xx]);
             gk[a_at(r, s)] = val;
-            gko[a_at(r, s)] = val;
+            row[xx] = val;
           }
         }
+        blk_st32(row, gko, r, cb * 32);
       }
     }
     __syncthreads();
@@ -373,7 +407,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
         // E0 (R0) and ZK (R3) for M and F, ZK also as an image for out
         tc_fence_after();
         const int r = gt;  // row = token
-        float* fdst = out + (int64_t)kE0 * kTileElems + r * kD;
+        float* fdst = out + (int64_t)kE0 * kTileElems;
         float* img = image_of(out, kImZK);
 #pragma unroll 1
         for (int cb = 0; grpA && cb < 4; ++cb) {
@@ -383,9 +417,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
           tmem_wait_ld_r(t32);
 #pragma unroll
           for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
-          float4* fd = reinterpret_cast<float4*>(fdst + cb * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) fd[q4] = make_float4(f[4 * q4], f[4 * q4 + 1], f[4 * q4 + 2], f[4 * q4 + 3]);
+          blk_st32(f, fdst, r, cb * 32);
           put_tile_row(true, sb + kPrepR0, nullptr, r, f, cb * 4, 4);
           tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
           tmem_wait_ld_r(t32);
@@ -601,7 +633,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
           tc_fence_after();
           const int r = gt;
           if (grpA) {
-            float* fdst = out + (int64_t)kDU0 * kTileElems + r * kD;
+            float* fdst = out + (int64_t)kDU0 * kTileElems;
             const float fa = -sbg[r];
 #pragma unroll 1
             for (int cb = 0; cb < 4; ++cb) {
@@ -611,9 +643,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
               tmem_wait_ld_r(t32);
 #pragma unroll
               for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
-              float4* fd = reinterpret_cast<float4*>(fdst + cb * 32);
-#pragma unroll
-              for (int q4 = 0; q4 < 8; ++q4) fd[q4] = make_float4(f[4 * q4], f[4 * q4 + 1], f[4 * q4 + 2], f[4 * q4 + 3]);
+              blk_st32(f, fdst, r, cb * 32);
 #pragma unroll
               for (int xx = 0; xx < 32; ++xx) f[xx] *= fa;
               put_tile_row(true, sb + kGr3, nullptr, r, f, cb * 4, 4);
@@ -781,9 +811,9 @@ __global__ void __launch_bounds__(kChThr, 1)
     float* blk = scratch_of(scr, H, nch, m, h, chunk_at(i));
     const float gc = blk[kGammaAt];
     {  // S at the chunk's start / G at its end, row x
-      float4* dst = reinterpret_cast<float4*>(blk + (int64_t)(bw ? kGend : kSstart) * kTileElems + x * kD + c0);
+      float* dst = blk + (int64_t)(bw ? kGend : kSstart) * kTileElems;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) dst[c] = make_float4(st[4 * c], st[4 * c + 1], st[4 * c + 2], st[4 * c + 3]);
+      for (int c = 0; c < 16; ++c) *blk4(dst, x, c0 / 4 + c) = make_float4(st[4 * c], st[4 * c + 1], st[4 * c + 2], st[4 * c + 3]);
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -939,7 +969,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
   }
   // ---- round 0: ZK S^T -> T0, ZW G^T -> T1; E and dU rows into the scratch
   copy_image(hf ? S1 : S0, image_of(blk, hf ? kImZW : kImZK), t);
-  stage_rows<4>(hf ? S3 : S2, hf ? Gen : Sst, kD, kD, nullptr, t);
+  stage_row_blk(hf ? S3 : S2, hf ? Gen : Sst, t);
   fence_proxy_async_smem();
   __syncthreads();
   if (tid == 0) {
@@ -951,24 +981,24 @@ __global__ void __launch_bounds__(kOutThr, 1)
   ok = mbar_wait_warp(smem_u32(&bars[5]), 0, abortp);
   if (!__syncthreads_or(!ok)) {
     tc_fence_after();
-    const float* e0r = blk + (int64_t)kE0 * kTileElems + t * kD;
-    const float* du0r = blk + (int64_t)kDU0 * kTileElems + t * kD;
+    const float* e0b = blk + (int64_t)kE0 * kTileElems;
+    const float* du0b = blk + (int64_t)kDU0 * kTileElems;
 #pragma unroll 1
     for (int cb = cb0; cb < cb0 + 2; ++cb) {
       uint32_t t32[32];
       float f32[32];
-      row_ld32(f32, e0r + cb * 32, true);
+      blk_ld32(f32, e0b, t, cb * 32);
       tmem_ld32(tb + lane_off + 0 + cb * 32, t32);
       tmem_wait_ld_r(t32);
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) f32[xx] -= __uint_as_float(t32[xx]);
-      row_st32(f32, Eb + t * kD + cb * 32, true);
-      row_ld32(f32, du0r + cb * 32, true);
+      blk_st32(f32, Eb, t, cb * 32);
+      blk_ld32(f32, du0b, t, cb * 32);
       tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
       tmem_wait_ld_r(t32);
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) f32[xx] += __uint_as_float(t32[xx]);
-      row_st32(f32, dUb + t * kD + cb * 32, true);
+      blk_st32(f32, dUb, t, cb * 32);
     }
   }
   tc_fence_before();
@@ -979,7 +1009,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
     stage_rows<4>(S0, q + row0, rs, nt, nullptr, t);
     stage_rows<4>(S1, k + row0, rs, nt, nullptr, t);
   } else {
-    stage_rows<4>(S3, Eb, kD, kC, nullptr, t);
+    stage_row_blk(S3, Eb, t);
     stage_rows<4>(S4, d_o + row0, rs, nt, nullptr, t);
   }
   stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
@@ -1028,7 +1058,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
       }
       tmem_st32(tb + lane_off + 128 + cb * 32, t32);
       // K S^T row t: db (dU . X) and dgamma (- b dU . K S^T)
-      row_ld32(ra, dUb + t * kD + cb * 32, true);
+      blk_ld32(ra, dUb, t, cb * 32);
       row_ld32(rb, v + rowt + cb * 32, live);
       tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
       tmem_wait_ld_r(t32);
@@ -1046,7 +1076,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
     tc_fence_before();
     __syncthreads();
     // ---- round 2: P E -> T1 (onto gamma Q S^T), dO E^T -> T0, dU E^T -> T2, E G -> T3
-    stage_rows<4>(hf ? S1 : S0, hf ? Gen : dUb, kD, kC, nullptr, t);
+    stage_row_blk(hf ? S1 : S0, hf ? Gen : dUb, t);
     fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {
@@ -1099,7 +1129,8 @@ __global__ void __launch_bounds__(kOutThr, 1)
 #pragma unroll
       for (int gg = 0; gg < 4; ++gg) st_shared_v4(S5 + tile_off(t, cb * 4 + gg), pack8(&f32[8 * gg]));
       // dA row t = -strict_lower(dU E^T): db, r, and Msym (both triangles) into S3
-      const float* gkr = gkb + a_at(t, cb * 32);  // GK row t from column cb*32 (used where s < t)
+      float gkr[32];  // GK row t, columns cb*32 ..
+      if (cb * 32 < r0 + 32) blk_ld32(gkr, gkb, t, cb * 32);
       tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
       tmem_wait_ld_r(t32);
 #pragma unroll
@@ -1150,7 +1181,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
 #pragma unroll 1
     for (int cb = cb0; cb < cb0 + 2; ++cb) {
       float u[32];
-      row_ld32(u, dUb + t * kD + cb * 32, true);
+      blk_ld32(u, dUb, t, cb * 32);
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) u[xx] *= bt;
       row_st32(u, dv + rowt + cb * 32, live);
@@ -1182,7 +1213,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
       for (int xx = 0; xx < 32; ++xx) f32[xx] = __uint_as_float(t32[xx]);
       row_st32(f32, dq + rowt + cb * 32, live);
       // -(gamma b) dU into S5 for dK
-      row_ld32(f32, dUb + t * kD + cb * 32, true);
+      blk_ld32(f32, dUb, t, cb * 32);
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) f32[xx] *= f;
 #pragma unroll
@@ -1219,8 +1250,8 @@ __global__ void __launch_bounds__(kOutThr, 1)
       for (int xx = 0; xx < 32; ++xx) f32[xx] = fmaf(wt, __uint_as_float(b32[xx]), __uint_as_float(a32[xx]));
       row_st32(f32, dk + rowt + cb * 32, live);
       float ga[32], sa[32];
-      row_ld32(ga, Gen + t * kD + cb * 32, true);
-      row_ld32(sa, Sst + t * kD + cb * 32, true);
+      blk_ld32(ga, Gen, t, cb * 32);
+      blk_ld32(sa, Sst, t, cb * 32);
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) gs = fmaf(ga[xx], sa[xx], gs);
     }
@@ -1345,7 +1376,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
 
   if (hf == 0) {
     stage_rows<4>(F0, q + row0, rs, nt, nullptr, t);
-    stage_rows<4>(F2, blk + (int64_t)kSstart * kTileElems, kD, kD, nullptr, t);
+    stage_row_blk(F2, blk + (int64_t)kSstart * kTileElems, t);
   } else {
     stage_rows<4>(F1, k + row0, rs, nt, nullptr, t);
     copy_image(F3, image_of(blk, kImZK), t);
@@ -1364,7 +1395,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
   if (!__syncthreads_or(!ok)) {
     tc_fence_after();
     const float ct = sc[t], gt = expf(ct);
-    const float* e0r = blk + (int64_t)kE0 * kTileElems + t * kD;
+    const float* e0b = blk + (int64_t)kE0 * kTileElems;
 #pragma unroll 1
     for (int cb = cb0; cb < cb0 + 2; ++cb) {
       uint32_t t32[32];
@@ -1380,7 +1411,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
 #pragma unroll
       for (int gg = 0; gg < 4; ++gg) st_shared_v4(F0 + tile_off(t, cb * 4 + gg), pack8(&f32[8 * gg]));
       // E row t = E0 - ZK S^T over K (F1)
-      row_ld32(f32, e0r + cb * 32, true);
+      blk_ld32(f32, e0b, t, cb * 32);
       tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
       tmem_wait_ld_r(t32);
 #pragma unroll

@@ -26,11 +26,13 @@ TOL_BF16 = 2e-2
 FLOAT_BLOCKS, IMAGES = 7, 10
 B_E0, B_DU0, B_SSTART, B_GEND, B_E, B_DU = range(6)
 I_ZK, I_ZW, I_M, I_FHI, I_FLO, I_MG, I_FGHI, I_FGLO, I_THI, I_TLO = range(10)
-SCR_FLOATS = FLOAT_BLOCKS * 128 * 128 + IMAGES * 8192
+SCR_FLOATS = FLOAT_BLOCKS * 128 * 128 + IMAGES * 8192 + 16  # then gamma_C and padding
+GAMMA_AT = FLOAT_BLOCKS * 128 * 128 + IMAGES * 8192
 
 
 def block(chunk, i):
-    return chunk[i * 16384:(i + 1) * 16384].reshape(128, 128)
+    """A float32 block decoded: element (r, c) at ((c // 4) * 128 + r) * 4 + c % 4."""
+    return chunk[i * 16384:(i + 1) * 16384].reshape(32, 128, 4).transpose(1, 0, 2).reshape(128, 128)
 
 
 def image(chunk, i):
@@ -143,8 +145,7 @@ def test_prep_solves_match_the_reference(emulator):
                     assert np.abs(got[name][n:]).max() == 0.0, name  # rows past the response
     print("prep max rel errs", errs)
     assert all(e <= TOL_BF16 for e in errs.values()), errs
-    assert abs(scr[0, 0, 1, FLOAT_BLOCKS * 16384 - 1] -
-               np.exp(a["g"][0, 128:200, 0].sum())) < 1e-5  # gamma_C of the partial chunk
+    assert abs(scr[0, 0, 1, GAMMA_AT] - np.exp(a["g"][0, 128:200, 0].sum())) < 1e-5  # gamma_C, partial chunk
 
 
 def _chains(s0, q, k, v, g, b, d_o):
