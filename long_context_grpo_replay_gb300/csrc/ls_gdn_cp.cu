@@ -174,24 +174,50 @@ __device__ __forceinline__ void stage_gates(const float* g, const float* beta, i
 constexpr int kTStride = kC + 1;
 __device__ __forceinline__ int b_at(int t, int x) { return t * kTStride + x; }
 
+// GK in shared memory by blocks of eight rows: the part of rows 8j .. 8j+7
+// left of column 8j at gk + 32 j (j - 1), element (8j + u, s) at s * 8 + u
+// (one column's eight coefficients in two 16-byte loads); the strict lower
+// triangles of the diagonal 8 x 8 blocks apart, in gkd, element
+// (8j + u, 8j + u2) at j * 64 + u * 8 + u2.
+__device__ __forceinline__ int gk_base(int j) { return 32 * j * (j - 1); }
+constexpr int kGkFloats = 32 * 16 * 15;  // blocks 0 .. 15
+constexpr int kGkdFloats = 16 * 64;
+
 // Column x of the inverse of the unit lower-triangular diagonal block of
 // (I + diag(b) GK) on rows and columns r0 .. r0+63, by forward substitution
 // eight rows at a time, into buf (column x, rows r0 .. r0+63; the rows above
 // x come out zero).  x lies inside the block.
-__device__ __forceinline__ void invert_block64(float* buf, const float* gk, const float* sbt, int r0,
-                                               int x) {
+__device__ __forceinline__ void invert_block64(float* buf, const float* gk, const float* gkd,
+                                               const float* sbt, int r0, int x) {
   for (int t8 = r0; t8 < r0 + 64; t8 += 8) {
+    const int j = t8 >> 3;
+    const float* gb = gk + gk_base(j);
     float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int s = r0; s < t8; ++s) {
-      const float e = buf[b_at(s, x)];
+    // eight columns s at a time (t8 - r0 is a multiple of 8): the inner loop
+    // has a fixed length, so all of its 24 loads issue ahead of the FMAs
+#pragma unroll 1
+    for (int s8 = r0; s8 < t8; s8 += 8) {
+      float e[8];
+      float4 a[8], c[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) sum[u] = fmaf(gk[a_at(t8 + u, s)], e, sum[u]);
+      for (int i = 0; i < 8; ++i) {
+        e[i] = buf[b_at(s8 + i, x)];
+        a[i] = *reinterpret_cast<const float4*>(gb + (s8 + i) * 8);
+        c[i] = *reinterpret_cast<const float4*>(gb + (s8 + i) * 8 + 4);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        sum[0] = fmaf(a[i].x, e[i], sum[0]), sum[1] = fmaf(a[i].y, e[i], sum[1]);
+        sum[2] = fmaf(a[i].z, e[i], sum[2]), sum[3] = fmaf(a[i].w, e[i], sum[3]);
+        sum[4] = fmaf(c[i].x, e[i], sum[4]), sum[5] = fmaf(c[i].y, e[i], sum[5]);
+        sum[6] = fmaf(c[i].z, e[i], sum[6]), sum[7] = fmaf(c[i].w, e[i], sum[7]);
+      }
     }
     float ev[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
 #pragma unroll
-      for (int u2 = 0; u2 < u; ++u2) sum[u] = fmaf(gk[a_at(t8 + u, t8 + u2)], ev[u2], sum[u]);
+      for (int u2 = 0; u2 < u; ++u2) sum[u] = fmaf(gkd[j * 64 + u * 8 + u2], ev[u2], sum[u]);
       ev[u] = fmaf(-sbt[t8 + u], sum[u], t8 + u == x ? 1.f : 0.f);
     }
 #pragma unroll
@@ -216,7 +242,9 @@ constexpr uint32_t kPrepR0 = 0, kPrepR1 = kTile, kPrepR2 = 2 * kTile, kPrepR3 = 
 constexpr uint32_t kPrepR4 = 4 * kTile, kPrepR5 = 5 * kTile;
 // T in fp32 (rows of 129 floats) runs 512 bytes past R5
 constexpr uint32_t kPrepMisc = 6 * kTile + 1024;
-constexpr uint32_t kPrepSmem = kPrepMisc + 3072 + 1024;
+constexpr uint32_t kPrepGkd = kPrepMisc + 3072;  // GK's diagonal blocks
+constexpr uint32_t kPrepSmem = kPrepGkd + kGkdFloats * 4 + 1024;
+static_assert(kGkFloats * 4 <= kTile, "GK's blocks fit in R3");
 static_assert(kPrepR4 + kC * kTStride * 4 <= kPrepMisc, "T buffer overlaps the misc area");
 constexpr int kPrepThr = 2 * kThr;
 
@@ -230,6 +258,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
                                            ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(sm);
   float* gk = reinterpret_cast<float*>(sm + kPrepR3);
+  float* gkd = reinterpret_cast<float*>(sm + kPrepGkd);
   float* buf = reinterpret_cast<float*>(sm + kPrepR4);
   float* sc = reinterpret_cast<float*>(sm + kPrepMisc);
   float* sbt = sc + kC;    // b
@@ -306,7 +335,10 @@ __global__ void __launch_bounds__(kPrepThr, 1)
           row[xx] = 0.f;
           if (s < r) {
             const float val = __expf(cr - sc[s]) * __uint_as_float(t32[xx]);
-            gk[a_at(r, s)] = val;
+            if (s < (r & ~7))
+              gk[gk_base(r >> 3) + s * 8 + (r & 7)] = val;
+            else
+              gkd[(r >> 3) * 64 + (r & 7) * 8 + (s & 7)] = val;
             row[xx] = val;
           }
         }
@@ -320,7 +352,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
       const int x = gt, r0 = x & 64;
       for (int t = 0; t < kC; ++t)
         if (t < r0 || t >= r0 + 64) buf[b_at(t, x)] = 0.f;
-      invert_block64(buf, gk, sbt, r0, x);
+      invert_block64(buf, gk, gkd, sbt, r0, x);
       named_bar_sync(1, kThr);
       // thread (xc, hf) owns column xc of the off-diagonal block, rows
       // 64 + 32 hf .. 64 + 32 hf + 31
@@ -332,14 +364,14 @@ __global__ void __launch_bounds__(kPrepThr, 1)
 #pragma unroll 1
         for (int j = 0; j < 32; ++j) {
           const int t = 64 + 32 * hf + j;
-          const float* gr = gk + a_at(t, 0);
+          const float* gr = gk + gk_base(t >> 3) + (t & 7);  // element s at gr[8 s]
           float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
 #pragma unroll
           for (int s = 0; s < 64; s += 4) {
-            p0 = fmaf(gr[s], tcol[s], p0);
-            p1 = fmaf(gr[s + 1], tcol[s + 1], p1);
-            p2 = fmaf(gr[s + 2], tcol[s + 2], p2);
-            p3 = fmaf(gr[s + 3], tcol[s + 3], p3);
+            p0 = fmaf(gr[8 * s], tcol[s], p0);
+            p1 = fmaf(gr[8 * (s + 1)], tcol[s + 1], p1);
+            p2 = fmaf(gr[8 * (s + 2)], tcol[s + 2], p2);
+            p3 = fmaf(gr[8 * (s + 3)], tcol[s + 3], p3);
           }
           buf[b_at(t, xc)] = sbt[t] * ((p0 + p1) + (p2 + p3));
         }
