@@ -354,47 +354,56 @@ __global__ void __launch_bounds__(kPrepThr, 1)
         if (t < r0 || t >= r0 + 64) buf[b_at(t, x)] = 0.f;
       invert_block64(buf, gk, gkd, sbt, r0, x);
       named_bar_sync(1, kThr);
-      // thread (xc, hf) owns column xc of the off-diagonal block, rows
-      // 64 + 32 hf .. 64 + 32 hf + 31
-      const int xc = x & 63, hf = x >> 6;
+      // thread (xc, rq) owns columns xc and xc + 32 of the off-diagonal block,
+      // rows 64 + 16 rq .. 64 + 16 rq + 15: the 16 rows' coefficients of one
+      // column are shared by the warp and serve two columns per thread
+      const int xc = x & 31, rq = x >> 5, t0r = 64 + 16 * rq;
+      float acc[2][16];
       {  // Y = diag(b) GK21 T11 into the block's place (T11 does not read it)
-        float tcol[64];
 #pragma unroll
-        for (int s = 0; s < 64; ++s) tcol[s] = buf[b_at(s, xc)];
-#pragma unroll 1
-        for (int j = 0; j < 32; ++j) {
-          const int t = 64 + 32 * hf + j;
-          const float* gr = gk + gk_base(t >> 3) + (t & 7);  // element s at gr[8 s]
-          float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+        for (int i = 0; i < 16; ++i) acc[0][i] = acc[1][i] = 0.f;
+        const float* g0 = gk + gk_base(t0r >> 3);      // rows t0r .. t0r+7
+        const float* g1 = gk + gk_base((t0r >> 3) + 1);  // rows t0r+8 .. t0r+15
+#pragma unroll 4
+        for (int s = 0; s < 64; ++s) {
+          const float e0 = buf[b_at(s, xc)], e1 = buf[b_at(s, xc + 32)];
+          const float4 a0 = *reinterpret_cast<const float4*>(g0 + s * 8);
+          const float4 a1 = *reinterpret_cast<const float4*>(g0 + s * 8 + 4);
+          const float4 a2 = *reinterpret_cast<const float4*>(g1 + s * 8);
+          const float4 a3 = *reinterpret_cast<const float4*>(g1 + s * 8 + 4);
+          const float gcoef[16] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w,
+                                   a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
 #pragma unroll
-          for (int s = 0; s < 64; s += 4) {
-            p0 = fmaf(gr[8 * s], tcol[s], p0);
-            p1 = fmaf(gr[8 * (s + 1)], tcol[s + 1], p1);
-            p2 = fmaf(gr[8 * (s + 2)], tcol[s + 2], p2);
-            p3 = fmaf(gr[8 * (s + 3)], tcol[s + 3], p3);
+          for (int i = 0; i < 16; ++i) {
+            acc[0][i] = fmaf(gcoef[i], e0, acc[0][i]);
+            acc[1][i] = fmaf(gcoef[i], e1, acc[1][i]);
           }
-          buf[b_at(t, xc)] = sbt[t] * ((p0 + p1) + (p2 + p3));
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          buf[b_at(t0r + i, xc)] = sbt[t0r + i] * acc[0][i];
+          buf[b_at(t0r + i, xc + 32)] = sbt[t0r + i] * acc[1][i];
         }
       }
       named_bar_sync(1, kThr);
       {  // T21 = -T22 Y (T22 stored with its zero upper triangle and unit diagonal)
-        float ycol[64];
 #pragma unroll
-        for (int s = 0; s < 64; ++s) ycol[s] = buf[b_at(64 + s, xc)];
-        named_bar_sync(1, kThr);  // Y read everywhere before T21 overwrites it
-#pragma unroll 1
-        for (int j = 0; j < 32; ++j) {
-          const int t = 64 + 32 * hf + j;
-          const float* tr = buf + b_at(t, 64);
-          float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+        for (int i = 0; i < 16; ++i) acc[0][i] = acc[1][i] = 0.f;
+#pragma unroll 4
+        for (int s = 0; s < 64; ++s) {
+          const float y0 = buf[b_at(64 + s, xc)], y1 = buf[b_at(64 + s, xc + 32)];
 #pragma unroll
-          for (int s = 0; s < 64; s += 4) {
-            p0 = fmaf(tr[s], ycol[s], p0);
-            p1 = fmaf(tr[s + 1], ycol[s + 1], p1);
-            p2 = fmaf(tr[s + 2], ycol[s + 2], p2);
-            p3 = fmaf(tr[s + 3], ycol[s + 3], p3);
+          for (int i = 0; i < 16; ++i) {
+            const float tc = buf[b_at(t0r + i, 64 + s)];
+            acc[0][i] = fmaf(tc, y0, acc[0][i]);
+            acc[1][i] = fmaf(tc, y1, acc[1][i]);
           }
-          buf[b_at(t, xc)] = -((p0 + p1) + (p2 + p3));
+        }
+        named_bar_sync(1, kThr);  // Y read everywhere before T21 overwrites it
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          buf[b_at(t0r + i, xc)] = -acc[0][i];
+          buf[b_at(t0r + i, xc + 32)] = -acc[1][i];
         }
       }
     } else {
