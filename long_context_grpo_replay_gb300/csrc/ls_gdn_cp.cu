@@ -46,14 +46,19 @@ using namespace gdn;
 // contiguous bytes with each 16-byte access):
 //   kE0, kDU0       E0 and dU0 (prep)
 //   kSstart, kGend  S at the chunk's start, G = dL/dS at its end (chain)
-//   kEblk, kDUblk   E and dU (out, for its own later passes)
+//   kDUblk          dU (out, for its own later passes)
 //   kGKblk          GK (prep; zero on and above the diagonal)
 // then bf16 tile images of 32 KB in the swizzled shared-memory layout, so a
 // plain copy lands them ready for the MMAs: ZK, ZW, -M, F hi, F lo, -M',
-// F' hi, F' lo (rows as in the formulas above), and T hi, T lo (row x =
-// column x of T); then 16 floats, the first gamma_C.
-enum : int { kE0 = 0, kDU0, kSstart, kGend, kEblk, kDUblk, kGKblk, kFloatBlocks };
-enum : int { kImZK = 0, kImZW, kImM, kImFhi, kImFlo, kImMg, kImFghi, kImFglo, kImThi, kImTlo, kImages };
+// F' hi, F' lo (rows as in the formulas above), T hi, T lo (row x = column x
+// of T), and the tiles of K, Q, dO (token rows; prep), S at the chunk's start
+// and G at its end (state rows; chain) for the output kernels; then 16
+// floats, the first gamma_C.
+enum : int { kE0 = 0, kDU0, kSstart, kGend, kDUblk, kGKblk, kFloatBlocks };
+enum : int {
+  kImZK = 0, kImZW, kImM, kImFhi, kImFlo, kImMg, kImFghi, kImFglo, kImThi, kImTlo,
+  kImK, kImQ, kImDO, kImS, kImG, kImages
+};
 constexpr int64_t kImgFloats = kTile / 4;
 constexpr int64_t kGammaAt = (int64_t)kFloatBlocks * kTileElems + kImages * kImgFloats;
 constexpr int64_t kScrFloats = kGammaAt + 16;
@@ -95,6 +100,12 @@ __device__ __forceinline__ void copy_image(uint32_t tile, const float* img, int 
 #pragma unroll
     for (int j = 0; j < 8; ++j) st_shared_v4(tile + 16u * (tid + kThr * (i0 + j)), v[j]);
   }
+}
+// Bulk copies of n tile images into shared-memory tiles, completing on bar
+// (thread 0 of the CTA; the tiles' previous readers must be done).
+__device__ __forceinline__ void copy_tiles(uint32_t bar, int n, const uint32_t* dst, const float* const* src) {
+  mbar_expect_tx(bar, (uint32_t)n * kTile);
+  for (int i = 0; i < n; ++i) bulk_load(dst[i], src[i], kTile, bar);
 }
 // Row r, columns c0 .. c0+31 of an interleaved scratch block.
 __device__ __forceinline__ float4* blk4(float* b, int r, int c4) {
@@ -298,7 +309,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   const int64_t row0 = (t0 * H + h) * kD;
   if (gt < nt) prefetch_l2((grpA ? k : v) + row0 + gt * rs, kD * 4);  // the chunk's rows into L2
 
-  if (grpA) stage_rows<4>(sb + kPrepR0, k + row0, rs, nt, nullptr, gt);
+  if (grpA) stage_rows<4>(sb + kPrepR0, k + row0, rs, nt, nullptr, gt, image_of(out, kImK));
   stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
   fence_proxy_async_smem();
   __syncthreads();
@@ -586,9 +597,9 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   }
   if (grpA) {
     stage_rows<4>(sb + kGr0, k + row0, rs, nt, nullptr, gt);
-    stage_rows<4>(sb + kGr1, q + row0, rs, nt, nullptr, gt);
+    stage_rows<4>(sb + kGr1, q + row0, rs, nt, nullptr, gt, image_of(out, kImQ));
   } else {
-    stage_rows<4>(sb + kGr2, d_o + row0, rs, nt, nullptr, gt);
+    stage_rows<4>(sb + kGr2, d_o + row0, rs, nt, nullptr, gt, image_of(out, kImDO));
   }
   stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
   fence_proxy_async_smem();
@@ -856,12 +867,15 @@ __global__ void __launch_bounds__(kChThr, 1)
 #pragma unroll
       for (int c = 0; c < 16; ++c) *blk4(dst, x, c0 / 4 + c) = make_float4(st[4 * c], st[4 * c + 1], st[4 * c + 2], st[4 * c + 3]);
     }
+    uint8_t* simg = reinterpret_cast<uint8_t*>(image_of(blk, bw ? kImG : kImS));  // bf16 S (or G) for the output kernels
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       float hi[8], lo[8];
       split8(&st[8 * j], hi, lo);
-      st_shared_v4(sb + kChShi + tile_off(x, gq0 + j), pack8(hi));
+      const uint4 ph = pack8(hi);
+      st_shared_v4(sb + kChShi + tile_off(x, gq0 + j), ph);
       st_shared_v4(sb + kChSlo + tile_off(x, gq0 + j), pack8(lo));
+      *reinterpret_cast<uint4*>(simg + tile_off(x, gq0 + j)) = ph;
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -956,8 +970,9 @@ __global__ void __launch_bounds__(kOutThr, 1)
   float* swt = part + 5 * kC;  // 8 floats of scan and reduction scratch
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOutMisc + 5184);
   float* colpart = reinterpret_cast<float*>(sm + kOutMisc + 5376);  // [4][128] column sums of r per row quarter
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 6);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 7);
   uint32_t* abort_s = tslot + 1;
+  uint32_t* never_s = tslot + 2;  // stays 0: the drain's waits are bounded by time alone
 
   const int ch = blockIdx.x, h = blockIdx.y, m = blockIdx.z, tid = threadIdx.x, warp = tid >> 5;
   const int lane = tid & 31;
@@ -973,12 +988,12 @@ __global__ void __launch_bounds__(kOutThr, 1)
   float* blk = scratch_of(scr, H, nch, m, h, ch);
   const float* Sst = blk + (int64_t)kSstart * kTileElems;
   const float* Gen = blk + (int64_t)kGend * kTileElems;
-  float* Eb = blk + (int64_t)kEblk * kTileElems;
   float* dUb = blk + (int64_t)kDUblk * kTileElems;
   const float* gkb = blk + (int64_t)kGKblk * kTileElems;
   if (tid == 0) {
-    for (int i = 0; i < 6; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    for (int i = 0; i < 7; ++i) mbar_init(smem_u32(&bars[i]), 1);
     *abort_s = 0;
+    *never_s = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -990,37 +1005,51 @@ __global__ void __launch_bounds__(kOutThr, 1)
   tc_fence_after();
   const uint32_t tb = *tslot, lane_off = (uint32_t)((warp & 3) * 32) << 16;
   const volatile uint32_t* abortp = abort_s;
+  const uint32_t cbar = smem_u32(&bars[6]);  // the tile images' bulk copies, one phase per round
+  uint32_t ncp = 0, nwt = 0;  // copy phases issued, and waited for (every thread keeps both)
+  int pend = -1;              // thread 0: parity of a copy phase whose wait gave up
   const int64_t rs = (int64_t)H * kD;
   const bool live = t < nt;
   const int r0 = (warp & 3) * 32;  // first row of this warp's 32
-  const int64_t row0 = (t0 * H + h) * kD;
   const int64_t rowt = ((t0 + t) * H + h) * kD;  // row t of q, k, v, d_o, o, dq, dk, dv
   bool ok = true;
+  auto wait_copies = [&]() {  // every warp: the current copy phase has landed
+    const bool got = mbar_wait_warp(cbar, nwt & 1, abortp);
+    if (!got && tid == 0) pend = (int)(nwt & 1);
+    ++nwt;
+    return got;
+  };
 
-  // everything this CTA reads, asked into L2 up front: rows of q, k, v, dO
-  // and the chunk's scratch blocks
-  if (live) {
-    prefetch_l2((hf ? v : q) + rowt, kD * 4);
-    prefetch_l2((hf ? d_o : k) + rowt, kD * 4);
-  }
+  // everything this CTA reads, asked into L2 up front: rows of v and dO (the
+  // tiles come from images) and the chunk's scratch blocks
+  if (live) prefetch_l2((hf ? v : d_o) + rowt, kD * 4);
   if (tid == 0) {
     prefetch_l2(blk, 4 * kTileElems * 4);                             // E0, dU0, S, G
     prefetch_l2(blk + (int64_t)kGKblk * kTileElems, kTileElems * 4);  // GK
-    prefetch_l2(image_of(blk, kImZK), 2 * kTile);                      // ZK, ZW
+    const uint32_t dst[4] = {S0, S1, S2, S3};  // ---- round 0 tiles: ZK, ZW, S, G
+    const float* src[4] = {image_of(blk, kImZK), image_of(blk, kImZW), image_of(blk, kImS),
+                           image_of(blk, kImG)};
+    copy_tiles(cbar, 4, dst, src);
   }
-  // ---- round 0: ZK S^T -> T0, ZW G^T -> T1; E and dU rows into the scratch
-  copy_image(hf ? S1 : S0, image_of(blk, hf ? kImZW : kImZK), t);
-  stage_row_blk(hf ? S3 : S2, hf ? Gen : Sst, t);
-  fence_proxy_async_smem();
-  __syncthreads();
-  if (tid == 0) {
-    tc_fence_after();
-    mma_group(tb + 0, S0, S2, false, false);
-    mma_group(tb + 128, S1, S3, false, false);
-    mma_commit(smem_u32(&bars[5]));
-  }
-  ok = mbar_wait_warp(smem_u32(&bars[5]), 0, abortp);
+  ++ncp;
+  // ---- round 0: ZK S^T -> T0, ZW G^T -> T1; E into S3 (bf16) and dU rows into the scratch
+  ok = wait_copies();
   if (!__syncthreads_or(!ok)) {
+    if (tid == 0) {
+      tc_fence_after();
+      mma_group(tb + 0, S0, S2, false, false);
+      mma_group(tb + 128, S1, S3, false, false);
+      mma_commit(smem_u32(&bars[5]));
+    }
+    ok = mbar_wait_warp(smem_u32(&bars[5]), 0, abortp);
+  }
+  if (!__syncthreads_or(!ok)) {
+    if (tid == 0) {  // round 1 tiles: Q, K, dO (the round-0 products are done with S0, S1)
+      const uint32_t dst[3] = {S0, S1, S4};
+      const float* src[3] = {image_of(blk, kImQ), image_of(blk, kImK), image_of(blk, kImDO)};
+      copy_tiles(cbar, 3, dst, src);
+    }
+    ++ncp;
     tc_fence_after();
     const float* e0b = blk + (int64_t)kE0 * kTileElems;
     const float* du0b = blk + (int64_t)kDU0 * kTileElems;
@@ -1033,7 +1062,8 @@ __global__ void __launch_bounds__(kOutThr, 1)
       tmem_wait_ld_r(t32);
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) f32[xx] -= __uint_as_float(t32[xx]);
-      blk_st32(f32, Eb, t, cb * 32);
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) st_shared_v4(S3 + tile_off(t, cb * 4 + gg), pack8(&f32[8 * gg]));
       blk_ld32(f32, du0b, t, cb * 32);
       tmem_ld32(tb + lane_off + 128 + cb * 32, t32);
       tmem_wait_ld_r(t32);
@@ -1043,25 +1073,19 @@ __global__ void __launch_bounds__(kOutThr, 1)
     }
   }
   tc_fence_before();
-  __syncthreads();  // E and dU rows written before any thread reads them back
+  __syncthreads();  // dU rows written before any thread reads them back
 
   // ---- round 1: Q K^T -> T0, Q S^T -> T1, K S^T -> T2
-  if (hf == 0) {
-    stage_rows<4>(S0, q + row0, rs, nt, nullptr, t);
-    stage_rows<4>(S1, k + row0, rs, nt, nullptr, t);
-  } else {
-    stage_row_blk(S3, Eb, t);
-    stage_rows<4>(S4, d_o + row0, rs, nt, nullptr, t);
-  }
   stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
   __syncthreads();
   if (hf == 0) {
     sgam[t] = expf(sc[t]);
     sw[t] = live ? expf(sc[kC - 1] - sc[t]) : 0.f;
   }
+  if (ok) ok = wait_copies();
   fence_proxy_async_smem();
-  __syncthreads();
-  if (tid == 0) {
+  if (__syncthreads_or(!ok)) ok = false;
+  if (ok && tid == 0) {
     tc_fence_after();
     mma_group(tb + 0, S0, S1, false, false);
     mma_group(tb + 128, S0, S2, false, false);
@@ -1071,6 +1095,12 @@ __global__ void __launch_bounds__(kOutThr, 1)
   if (ok) ok = mbar_wait_warp(smem_u32(&bars[0]), 0, abortp);
   float dgam = 0.f, dbt = 0.f, rrow = 0.f, rw = 0.f;  // this half's parts of the row sums
   if (!__syncthreads_or(!ok)) {
+    if (tid == 0) {  // round 2's G (the round-1 products are done with S1)
+      const uint32_t dst[1] = {S1};
+      const float* src[1] = {image_of(blk, kImG)};
+      copy_tiles(cbar, 1, dst, src);
+    }
+    ++ncp;
     tc_fence_after();
     const float ct = sc[t], gt = sgam[t], bt = sbt[t];
 #pragma unroll 1
@@ -1117,10 +1147,11 @@ __global__ void __launch_bounds__(kOutThr, 1)
     tc_fence_before();
     __syncthreads();
     // ---- round 2: P E -> T1 (onto gamma Q S^T), dO E^T -> T0, dU E^T -> T2, E G -> T3
-    stage_row_blk(hf ? S1 : S0, hf ? Gen : dUb, t);
+    if (hf == 0) stage_row_blk(S0, dUb, t);
+    ok = wait_copies();
     fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
+    if (__syncthreads_or(!ok)) ok = false;
+    if (ok && tid == 0) {
       tc_fence_after();
       mma_group(tb + 128, S5, S3, true, true);
       mma_group(tb + 0, S4, S3, false, false);
@@ -1128,9 +1159,15 @@ __global__ void __launch_bounds__(kOutThr, 1)
       mma_group(tb + 384, S3, S1, true, false);
       mma_commit(smem_u32(&bars[1]));
     }
-    ok = mbar_wait_warp(smem_u32(&bars[1]), 0, abortp);
+    if (ok) ok = mbar_wait_warp(smem_u32(&bars[1]), 0, abortp);
   }
   if (!__syncthreads_or(!ok)) {
+    if (tid == 0) {  // round 3a's K (the round-2 products are done with S1)
+      const uint32_t dst[1] = {S1};
+      const float* src[1] = {image_of(blk, kImK)};
+      copy_tiles(cbar, 1, dst, src);
+    }
+    ++ncp;
     tc_fence_after();
     const float ct = sc[t], bt = sbt[t], gt = sgam[t], wt = sw[t];
 #pragma unroll 1
@@ -1227,21 +1264,26 @@ __global__ void __launch_bounds__(kOutThr, 1)
       for (int xx = 0; xx < 32; ++xx) u[xx] *= bt;
       row_st32(u, dv + rowt + cb * 32, live);
     }
-    __syncthreads();
-    stage_rows<4, kOutThr>(S1, k + row0, rs, nt, nullptr, tid);  // K back into S1
+    ok = wait_copies();  // K back in S1
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    if (__syncthreads_or(!ok)) ok = false;
     // ---- round 3a: dQ = (gamma dO) S + LdP K -> T0
-    if (tid == 0) {
+    if (ok && tid == 0) {
       tc_fence_after();
       mma_group(tb + 0, S4, S2, true, false);
       mma_group(tb + 0, S5, S1, true, true);
       mma_commit(smem_u32(&bars[2]));
     }
-    ok = mbar_wait_warp(smem_u32(&bars[2]), 0, abortp);
+    if (ok) ok = mbar_wait_warp(smem_u32(&bars[2]), 0, abortp);
   }
   if (!__syncthreads_or(!ok)) {
+    if (tid == 0) {  // round 3b's Q (the round-3a products are done with S4)
+      const uint32_t dst[1] = {S4};
+      const float* src[1] = {image_of(blk, kImQ)};
+      copy_tiles(cbar, 1, dst, src);
+    }
+    ++ncp;
     tc_fence_after();
     const float f = -sgam[t] * sbt[t];
 #pragma unroll 1
@@ -1260,20 +1302,19 @@ __global__ void __launch_bounds__(kOutThr, 1)
 #pragma unroll
       for (int gg = 0; gg < 4; ++gg) st_shared_v4(S5 + tile_off(t, cb * 4 + gg), pack8(&f32[8 * gg]));
     }
-    __syncthreads();  // S5 rows of both halves written; dQ read out of T0
-    stage_rows<4, kOutThr>(S4, q + row0, rs, nt, nullptr, tid);  // Q into S4
+    ok = wait_copies();  // Q in S4
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    if (__syncthreads_or(!ok)) ok = false;  // S5 rows of both halves written; dQ read out of T0
     // ---- round 3b: dK = LdP^T Q + Msym K - (gamma b dU) S -> T2 (+ w E G from T3)
-    if (tid == 0) {
+    if (ok && tid == 0) {
       tc_fence_after();
       mma_group(tb + 256, S0, S4, true, false);
       mma_group(tb + 256, S3, S1, true, true);
       mma_group(tb + 256, S5, S2, true, true);
       mma_commit(smem_u32(&bars[3]));
     }
-    ok = mbar_wait_warp(smem_u32(&bars[3]), 0, abortp);
+    if (ok) ok = mbar_wait_warp(smem_u32(&bars[3]), 0, abortp);
   }
   if (!__syncthreads_or(!ok)) {
     tc_fence_after();
@@ -1350,9 +1391,11 @@ __global__ void __launch_bounds__(kOutThr, 1)
     }
   }
   if (!ok && tid == 0 && status) atomicOr(status, kStatusTimeout);
-  if (tid == 0) {
+  if (tid == 0) {  // drain: the products, and a copy phase nobody waited for
     mma_commit(smem_u32(&bars[4]));
-    mbar_wait(smem_u32(&bars[4]), 0, abortp);
+    mbar_wait(smem_u32(&bars[4]), 0, never_s);
+    if (nwt < ncp) mbar_wait(cbar, (ncp - 1) & 1, never_s);
+    else if (pend >= 0) mbar_wait(cbar, (uint32_t)pend, never_s);
   }
   tc_fence_before();
   __syncthreads();
@@ -1384,8 +1427,9 @@ __global__ void __launch_bounds__(kOutThr, 1)
   float* sbt = sc + kC;
   float* swt = sbt + kC;  // 8 floats of scan scratch
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kFoMisc + 1088);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 4);
   uint32_t* abort_s = tslot + 1;
+  uint32_t* never_s = tslot + 2;  // stays 0: the drain's waits are bounded by time alone
 
   const int ch = blockIdx.x, h = blockIdx.y, m = blockIdx.z, tid = threadIdx.x, warp = tid >> 5;
   const int t = tid & (kThr - 1), hf = tid >> 7, cb0 = 2 * hf;
@@ -1397,8 +1441,9 @@ __global__ void __launch_bounds__(kOutThr, 1)
   }
   float* blk = scratch_of(scr, H, nch, m, h, ch);
   if (tid == 0) {
-    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), 1);
     *abort_s = 0;
+    *never_s = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -1415,24 +1460,26 @@ __global__ void __launch_bounds__(kOutThr, 1)
   const int64_t row0 = (t0 * H + h) * kD, rowt = ((t0 + t) * H + h) * kD;
   if (tid == 0) prefetch_l2(blk + (int64_t)kE0 * kTileElems, kTileElems * 4);  // E0
 
-  if (hf == 0) {
-    stage_rows<4>(F0, q + row0, rs, nt, nullptr, t);
-    stage_row_blk(F2, blk + (int64_t)kSstart * kTileElems, t);
-  } else {
-    stage_rows<4>(F1, k + row0, rs, nt, nullptr, t);
-    copy_image(F3, image_of(blk, kImZK), t);
+  const uint32_t cbar = smem_u32(&bars[3]);
+  if (tid == 0) {  // K, S and ZK from their images
+    const uint32_t dst[3] = {F1, F2, F3};
+    const float* src[3] = {image_of(blk, kImK), image_of(blk, kImS), image_of(blk, kImZK)};
+    copy_tiles(cbar, 3, dst, src);
   }
+  if (hf == 0) stage_rows<4>(F0, q + row0, rs, nt, nullptr, t);
   stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
+  bool ok = mbar_wait_warp(cbar, 0, abortp);
+  const bool copied = ok;  // thread 0: the copies landed (else the drain waits for them)
   fence_proxy_async_smem();
-  __syncthreads();
-  if (tid == 0) {  // Q K^T -> 0, Q S^T -> 128, ZK S^T -> 256
+  if (__syncthreads_or(!ok)) ok = false;
+  if (ok && tid == 0) {  // Q K^T -> 0, Q S^T -> 128, ZK S^T -> 256
     tc_fence_after();
     mma_group(tb + 0, F0, F1, false, false);
     mma_group(tb + 128, F0, F2, false, false);
     mma_group(tb + 256, F3, F2, false, false);
     mma_commit(smem_u32(&bars[0]));
   }
-  bool ok = mbar_wait_warp(smem_u32(&bars[0]), 0, abortp);
+  if (ok) ok = mbar_wait_warp(smem_u32(&bars[0]), 0, abortp);
   if (!__syncthreads_or(!ok)) {
     tc_fence_after();
     const float ct = sc[t], gt = expf(ct);
@@ -1491,9 +1538,10 @@ __global__ void __launch_bounds__(kOutThr, 1)
     }
   }
   if (!ok && tid == 0 && status) atomicOr(status, kStatusTimeout);
-  if (tid == 0) {
+  if (tid == 0) {  // drain: the products, and the copies if their wait gave up
     mma_commit(smem_u32(&bars[2]));
-    mbar_wait(smem_u32(&bars[2]), 0, abortp);
+    mbar_wait(smem_u32(&bars[2]), 0, never_s);
+    if (!copied) mbar_wait(cbar, 0, never_s);
   }
   tc_fence_before();
   __syncthreads();

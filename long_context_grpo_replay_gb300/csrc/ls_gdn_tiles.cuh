@@ -45,9 +45,12 @@ __device__ __forceinline__ uint16_t bf16_of(float x) { return (uint16_t)(pack_bf
 // compiler, so each batch of kBatch row pieces is loaded into registers
 // before any of it is stored: kBatch global loads in flight, not one.
 // tid: the caller's index among the kWorkers threads that stage the tile.
+// img, when given, receives the same bytes as the tile (a 32 KB image of it
+// in global memory, 16-byte aligned), for a later bulk copy.
 template <int kBatch = 8, int kWorkers = kThr>
 __device__ __forceinline__ void stage_rows(uint32_t tile, const float* src, int64_t stride, int nt,
-                                           const float* scale, int tid = threadIdx.x) {
+                                           const float* scale, int tid = threadIdx.x,
+                                           void* img = nullptr) {
   constexpr int kPer = 2048 / kWorkers;  // 16-byte pieces per thread
   static_assert(kPer % kBatch == 0, "batch divides the pieces per thread");
 #pragma unroll 1
@@ -68,7 +71,9 @@ __device__ __forceinline__ void stage_rows(uint32_t tile, const float* src, int6
       const float f = (scale && r < nt) ? scale[r] : 1.f;
       const float x[8] = {a[j].x * f, a[j].y * f, a[j].z * f, a[j].w * f,
                           b[j].x * f, b[j].y * f, b[j].z * f, b[j].w * f};
-      st_shared_v4(tile + tile_off(r, gq), pack8(x));
+      const uint4 pk = pack8(x);
+      st_shared_v4(tile + tile_off(r, gq), pk);
+      if (img) *reinterpret_cast<uint4*>(static_cast<uint8_t*>(img) + tile_off(r, gq)) = pk;
     }
   }
 }

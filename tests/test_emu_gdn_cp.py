@@ -20,12 +20,13 @@ EMU = Path(__file__).resolve().parent / "emu"
 CSRC = ROOT / "long_context_grpo_replay_gb300" / "csrc"
 SRC = CSRC / "ls_gdn_cp.cu"
 TOL_BF16 = 2e-2
-# scratch per chunk: float32 [128 x 128] blocks E0, dU0, S_start, G_end, E,
-# dU, GK; then bf16 tile images (32 KB, the swizzled shared-memory layout)
-# ZK, ZW, -M, F hi, F lo, -M', F' hi, F' lo, T hi, T lo
-FLOAT_BLOCKS, IMAGES = 7, 10
-B_E0, B_DU0, B_SSTART, B_GEND, B_E, B_DU = range(6)
-I_ZK, I_ZW, I_M, I_FHI, I_FLO, I_MG, I_FGHI, I_FGLO, I_THI, I_TLO = range(10)
+# scratch per chunk: float32 [128 x 128] blocks E0, dU0, S_start, G_end, dU,
+# GK; then bf16 tile images (32 KB, the swizzled shared-memory layout) ZK,
+# ZW, -M, F hi, F lo, -M', F' hi, F' lo, T hi, T lo, K, Q, dO, S, G
+FLOAT_BLOCKS, IMAGES = 6, 15
+B_E0, B_DU0, B_SSTART, B_GEND, B_DU = range(5)
+(I_ZK, I_ZW, I_M, I_FHI, I_FLO, I_MG, I_FGHI, I_FGLO, I_THI, I_TLO, I_K, I_Q, I_DO, I_S,
+ I_G) = range(15)
 SCR_FLOATS = FLOAT_BLOCKS * 128 * 128 + IMAGES * 8192 + 16  # then gamma_C and padding
 GAMMA_AT = FLOAT_BLOCKS * 128 * 128 + IMAGES * 8192
 
@@ -173,8 +174,8 @@ def _chains(s0, q, k, v, g, b, d_o):
 
 
 def test_chains_match_the_reference(emulator):
-    """S at each chunk's start and G at its end (chain), E and dU (out), over
-    three chunks, the last partial."""
+    """S at each chunk's start and G at its end (chain: fp32 and their bf16
+    images) and dU (out), over three chunks, the last partial."""
     exe, d = emulator
     B, H, R = 2, 1, 300  # three chunks, the last partial; two members share s0
     c = inputs.make_gdn_group(B, H, R, seed=32)
@@ -188,10 +189,12 @@ def test_chains_match_the_reference(emulator):
                                                a["d_o"][m, :, 0])
         for ch in range(3):
             n = min(128, R - 128 * ch)
-            for name, blk, want in (("S_start", B_SSTART, S_start[ch]), ("E", B_E, E[ch][:n]),
-                                    ("G_end", B_GEND, G_end[ch]), ("dU", B_DU, dU[ch][:n])):
-                got = block(scr[m, 0, ch], blk)
-                got = got if name in ("S_start", "G_end") else got[:n]
+            sc = scr[m, 0, ch]
+            for name, got, want in (("S_start", block(sc, B_SSTART), S_start[ch]),
+                                    ("S image", image(sc, I_S), S_start[ch]),
+                                    ("G_end", block(sc, B_GEND), G_end[ch]),
+                                    ("G image", image(sc, I_G), G_end[ch]),
+                                    ("dU", block(sc, B_DU)[:n], dU[ch][:n])):
                 if np.abs(want).max() == 0:
                     assert np.abs(got).max() == 0, name
                     continue
