@@ -351,3 +351,44 @@ def test_backward_reusing_the_forward_scratch_is_bit_identical(emulator):
         assert np.array_equal(g1[name], g2[name]), name
     for name in ("o", "s_final"):  # the reusing run's o and s_final come from the forward
         assert np.array_equal(g1[name], g2[name]), name
+
+
+def _backward_errors(exe, d, B, H, R, seed):
+    from oracle.gdn import gdn_replay
+
+    c = inputs.make_gdn_group(B, H, R, seed=seed)
+    status, _, rest = run(exe, d, c, "fwd_bwd")
+    assert status == 0
+    got = _replay_outputs(rest, B, H, R)
+    a = {x: t.numpy() for x, t in c.items()}
+    errs = {}
+    for m in range(B):
+        want = gdn_replay(a["s0"], a["q"][m], a["k"][m], a["v"][m], a["g"][m], a["beta"][m],
+                          a["d_o"][m])
+        for name in ("dq", "dk", "dv", "dg", "dbeta"):
+            gm = got[name].reshape((B,) + want[name].shape)[m]
+            errs[name] = max(errs.get(name, 0.0), rel(gm, want[name]))
+    return errs
+
+
+def test_backward_reusing_the_forward_matches_the_oracle(emulator):
+    exe, d = emulator
+    errs = _backward_errors(exe, d, 2, 1, 300, seed=62)
+    print("backward (reusing the forward) max rel errs", errs)
+    assert all(e <= TOL_BF16 for e in errs.values()), errs
+
+
+@pytest.mark.parametrize("mutation", [
+    ("f32[xx] = s <= t ? __expf(ct - sc[s]) * dp : 0.f;",
+     "f32[xx] = s < t ? __expf(ct - sc[s]) * dp : 0.f;"),
+    ("mma_group(tb + 384, sb + kGr4, sb + kGr2, true, false);  // ZW = T^T (w K)",
+     "mma_group_amn(tb + 384, sb + kGr4, sb + kGr2, true, false);  // ZW = T^T (w K)"),
+    ("      for (int xx = 0; xx < 32; ++xx) f32[xx] += __uint_as_float(t32[xx]);",
+     "      for (int xx = 0; xx < 32; ++xx) f32[xx] -= __uint_as_float(t32[xx]);"),
+], ids=["LdP_without_its_diagonal", "ZW_with_T_read_M_major", "dU_with_ZW_G_subtracted"])
+def test_emulator_rejects_planted_backward_mistakes(tmp_path, mutation):
+    """A mistake planted in a copy of the backward kernels' source must fail
+    the gradients' comparison."""
+    exe = build(tmp_path, mutation)
+    errs = _backward_errors(exe, tmp_path, 1, 1, 300, seed=63)
+    assert not all(e <= TOL_BF16 for e in errs.values()), errs
