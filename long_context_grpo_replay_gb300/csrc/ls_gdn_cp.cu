@@ -526,14 +526,16 @@ __global__ void __launch_bounds__(kPrepThr, 1)
 }
 
 // ---------------------------------------------------------------- prep (backward's terms)
-// The backward's own terms of each chunk from the T that the forward share
-// left in the scratch (its hi and lo images, brought in by bulk copy): one
-// CTA per (chunk, head, member), 256 threads in two groups of 128.
+// The backward's own terms of each chunk from what the forward share left in
+// the scratch (T as its hi and lo images and K's tile, brought in by bulk
+// copy): one CTA per (chunk, head, member), 256 threads in two groups of 128.
 //   dE0 = P^T dO (P^T from a K Q^T product), dU0 = T^T dE0, ZW = T^T W,
-//   M' = ZW^T diag(gamma b) K, F' = (gamma dO)^T Q - (gamma b dU0)^T K.
-// Written to the scratch: dU0, and the images of ZW, -M', F' hi / lo.
-// Shared memory: G0 K, G1 Q -> P^T -> b gamma K, G2 dO -> w K -> Q,
-// G3 dE0 -> -gamma b dU0, G4 T hi -> gamma dO, G5 T lo -> ZW.
+//   M' = (diag(gamma b) ZW)^T K, F' = dO^T (diag(gamma) Q) - (gamma b dU0)^T K.
+// The row scales sit on tiles formed here (ZW's rows, Q's rows), so K and
+// dO serve unscaled.  Written to the scratch: dU0, and the images of Q, dO,
+// ZW, -M', F' hi / lo.
+// Shared memory: G0 K, G1 Q -> P^T -> w K, G2 dO, G3 dE0 -> -gamma b dU0,
+// G4 T hi -> gamma Q, G5 T lo -> gamma b ZW.
 constexpr uint32_t kGr0 = 0, kGr1 = kTile, kGr2 = 2 * kTile, kGr3 = 3 * kTile, kGr4 = 4 * kTile,
                    kGr5 = 5 * kTile, kGrMisc = 6 * kTile;
 constexpr uint32_t kGrSmem = kGrMisc + 3072 + 1024;
@@ -585,22 +587,16 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   const volatile uint32_t* abortp = abort_s;
   const int64_t rs = (int64_t)H * kD;
   const int64_t row0 = (t0 * H + h) * kD;
-  if (tid == 0) {  // T hi, T lo
-    const uint32_t bar = smem_u32(&bars[2]);
-    mbar_expect_tx(bar, 2 * kTile);
-    bulk_load(sb + kGr4, image_of(out, kImThi), kTile, bar);
-    bulk_load(sb + kGr5, image_of(out, kImTlo), kTile, bar);
+  if (tid == 0) {  // K, T hi, T lo
+    const uint32_t dst[3] = {sb + kGr0, sb + kGr4, sb + kGr5};
+    const float* src[3] = {image_of(out, kImK), image_of(out, kImThi), image_of(out, kImTlo)};
+    copy_tiles(smem_u32(&bars[2]), 3, dst, src);
   }
-  if (gt < nt) {  // the chunk's rows into L2 (k and q are read twice)
-    prefetch_l2((grpA ? k : d_o) + row0 + gt * rs, kD * 4);
-    if (grpA) prefetch_l2(q + row0 + gt * rs, kD * 4);
-  }
-  if (grpA) {
-    stage_rows<4>(sb + kGr0, k + row0, rs, nt, nullptr, gt);
+  if (gt < nt) prefetch_l2((grpA ? q : k) + row0 + gt * rs, kD * 4);  // q, k are read twice
+  if (grpA)
     stage_rows<4>(sb + kGr1, q + row0, rs, nt, nullptr, gt, image_of(out, kImQ));
-  } else {
+  else
     stage_rows<4>(sb + kGr2, d_o + row0, rs, nt, nullptr, gt, image_of(out, kImDO));
-  }
   stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
   fence_proxy_async_smem();
   __syncthreads();
@@ -610,13 +606,19 @@ __global__ void __launch_bounds__(kPrepThr, 1)
     sbg[gt] = sbt[gt] * sgm[gt];
     swk[gt] = gt < nt ? __expf(clast - ct) : 0.f;
   }
-  if (tid == 0) {  // K Q^T -> cols 0..127
-    tc_fence_after();
-    mma_group(tb + 0, sb + kGr0, sb + kGr1, false, false);
-    mma_commit(smem_u32(&bars[0]));
+  bool ok = true, copied = false;  // copied (thread 0): the copies were waited for
+  if (warp == 0) {
+    ok = mbar_wait_warp(smem_u32(&bars[2]), 0, abortp);  // K, T hi, T lo landed
+    if (tid == 0) copied = ok;
   }
-  bool ok = mbar_wait_warp(smem_u32(&bars[0]), 0, abortp);
-  bool copied = false;  // thread 0: the T copies were waited for
+  if (!__syncthreads_or(!ok)) {
+    if (tid == 0) {  // K Q^T -> cols 0..127
+      tc_fence_after();
+      mma_group(tb + 0, sb + kGr0, sb + kGr1, false, false);
+      mma_commit(smem_u32(&bars[0]));
+    }
+    ok = mbar_wait_warp(smem_u32(&bars[0]), 0, abortp);
+  }
   if (!__syncthreads_or(!ok)) {
     tc_fence_after();
     if (grpA) {  // P^T row r: P^T[r][t] = [t >= r] Gamma_tr (K_r . Q_t), over Q (G1)
@@ -658,95 +660,92 @@ __global__ void __launch_bounds__(kPrepThr, 1)
           for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
           put_tile_row(true, sb + kGr3, nullptr, gt, f, cb * 4, 4);
         }
-      } else {  // the products have read P^T (G1) and dO (G2)
-        stage_rows<4>(sb + kGr2, k + row0, rs, nt, swk, gt);  // w K
-        stage_rows<4>(sb + kGr1, k + row0, rs, nt, sbg, gt);  // b gamma K
-      }
-      if (warp == 0) {
-        ok = mbar_wait_warp(smem_u32(&bars[2]), 0, abortp);  // T hi, T lo landed
-        if (tid == 0) copied = ok;
+      } else {  // w K over P^T (G1), which dE0 has read
+        stage_rows<4>(sb + kGr1, k + row0, rs, nt, swk, gt);
       }
       fence_proxy_async_smem();
       tc_fence_before();
+      __syncthreads();
+      if (tid == 0) {
+        tc_fence_after();
+        mma_group(tb + 256, sb + kGr4, sb + kGr3, true, false);  // dU0 = T^T dE0
+        mma_group(tb + 256, sb + kGr5, sb + kGr3, true, true);
+        mma_group(tb + 384, sb + kGr4, sb + kGr1, true, false);  // ZW = T^T (w K)
+        mma_group(tb + 384, sb + kGr5, sb + kGr1, true, true);
+        mma_commit(smem_u32(&bars[3]));
+      }
+      ok = mbar_wait_warp(smem_u32(&bars[3]), 0, abortp);
       if (!__syncthreads_or(!ok)) {
+        // group A: dU0 rows to the scratch (fp32) and -gamma b dU0 into G3,
+        // then gamma Q into G4; group B: ZW rows to their image and, times
+        // gamma b, into G5
+        tc_fence_after();
+        const int r = gt;
+        if (grpA) {
+          float* fdst = out + (int64_t)kDU0 * kTileElems;
+          const float fa = -sbg[r];
+#pragma unroll 1
+          for (int cb = 0; cb < 4; ++cb) {
+            uint32_t t32[32];
+            float f[32];
+            tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
+            tmem_wait_ld_r(t32);
+#pragma unroll
+            for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
+            blk_st32(f, fdst, r, cb * 32);
+#pragma unroll
+            for (int xx = 0; xx < 32; ++xx) f[xx] *= fa;
+            put_tile_row(true, sb + kGr3, nullptr, r, f, cb * 4, 4);
+          }
+          stage_rows<4>(sb + kGr4, q + row0, rs, nt, sgm, gt);
+        } else {
+          float* img = image_of(out, kImZW);
+          const float fb = sbg[r];
+#pragma unroll 1
+          for (int cb = 0; cb < 4; ++cb) {
+            uint32_t t32[32];
+            float f[32];
+            tmem_ld32(tb + lane_off + 384 + cb * 32, t32);
+            tmem_wait_ld_r(t32);
+#pragma unroll
+            for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
+            put_tile_row(false, 0, img, r, f, cb * 4, 4);
+#pragma unroll
+            for (int xx = 0; xx < 32; ++xx) f[xx] *= fb;
+            put_tile_row(true, sb + kGr5, nullptr, r, f, cb * 4, 4);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
         if (tid == 0) {
           tc_fence_after();
-          mma_group(tb + 256, sb + kGr4, sb + kGr3, true, false);  // dU0 = T^T dE0
-          mma_group(tb + 256, sb + kGr5, sb + kGr3, true, true);
-          mma_group(tb + 384, sb + kGr4, sb + kGr2, true, false);  // ZW = T^T (w K)
-          mma_group(tb + 384, sb + kGr5, sb + kGr2, true, true);
-          mma_commit(smem_u32(&bars[3]));
+          mma_group_amn(tb + 0, sb + kGr5, sb + kGr0, true, false);    // M' = (gamma b ZW)^T K
+          mma_group_amn(tb + 128, sb + kGr2, sb + kGr4, true, false);  // F' = dO^T (gamma Q)
+          mma_group_amn(tb + 128, sb + kGr3, sb + kGr0, true, true);   //      - (gamma b dU0)^T K
+          mma_commit(smem_u32(&bars[4]));
         }
-        ok = mbar_wait_warp(smem_u32(&bars[3]), 0, abortp);
+        ok = mbar_wait_warp(smem_u32(&bars[4]), 0, abortp);
         if (!__syncthreads_or(!ok)) {
-          // group A: dU0 rows to the scratch (fp32) and -gamma b dU0 into G3,
-          // then Q into G2; group B: ZW rows into G5 and its image, then
-          // gamma dO into G4
+          // -M' (group A) and F' hi / lo (group B) to their images
           tc_fence_after();
-          const int r = gt;
-          if (grpA) {
-            float* fdst = out + (int64_t)kDU0 * kTileElems;
-            const float fa = -sbg[r];
 #pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-              uint32_t t32[32];
-              float f[32];
-              tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
-              tmem_wait_ld_r(t32);
+          for (int cb = 0; cb < 4; ++cb) {
+            uint32_t t32[32];
+            float f[32], hi[32], lo[32];
+            tmem_ld32(tb + lane_off + (grpA ? 0 : 128) + cb * 32, t32);
+            tmem_wait_ld_r(t32);
+            if (grpA) {
+#pragma unroll
+              for (int xx = 0; xx < 32; ++xx) f[xx] = -__uint_as_float(t32[xx]);
+              put_tile_row(false, 0, image_of(out, kImMg), r, f, cb * 4, 4);
+            } else {
 #pragma unroll
               for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
-              blk_st32(f, fdst, r, cb * 32);
 #pragma unroll
-              for (int xx = 0; xx < 32; ++xx) f[xx] *= fa;
-              put_tile_row(true, sb + kGr3, nullptr, r, f, cb * 4, 4);
-            }
-            stage_rows<4>(sb + kGr2, q + row0, rs, nt, nullptr, gt);
-          } else {
-            float* img = image_of(out, kImZW);
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-              uint32_t t32[32];
-              float f[32];
-              tmem_ld32(tb + lane_off + 384 + cb * 32, t32);
-              tmem_wait_ld_r(t32);
-#pragma unroll
-              for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
-              put_tile_row(true, sb + kGr5, img, r, f, cb * 4, 4);
-            }
-            stage_rows<4>(sb + kGr4, d_o + row0, rs, nt, sgm, gt);
-          }
-          fence_proxy_async_smem();
-          tc_fence_before();
-          __syncthreads();
-          if (tid == 0) {
-            tc_fence_after();
-            mma_group_amn(tb + 0, sb + kGr5, sb + kGr1, true, false);    // M' = ZW^T diag(b gamma) K
-            mma_group_amn(tb + 128, sb + kGr4, sb + kGr2, true, false);  // F' = (gamma dO)^T Q
-            mma_group_amn(tb + 128, sb + kGr3, sb + kGr0, true, true);   //      - (gamma b dU0)^T K
-            mma_commit(smem_u32(&bars[4]));
-          }
-          ok = mbar_wait_warp(smem_u32(&bars[4]), 0, abortp);
-          if (!__syncthreads_or(!ok)) {
-            // -M' (group A) and F' hi / lo (group B) to their images
-            tc_fence_after();
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-              uint32_t t32[32];
-              float f[32], hi[32], lo[32];
-              tmem_ld32(tb + lane_off + (grpA ? 0 : 128) + cb * 32, t32);
-              tmem_wait_ld_r(t32);
-              if (grpA) {
-#pragma unroll
-                for (int xx = 0; xx < 32; ++xx) f[xx] = -__uint_as_float(t32[xx]);
-                put_tile_row(false, 0, image_of(out, kImMg), r, f, cb * 4, 4);
-              } else {
-#pragma unroll
-                for (int xx = 0; xx < 32; ++xx) f[xx] = __uint_as_float(t32[xx]);
-#pragma unroll
-                for (int gg = 0; gg < 4; ++gg) split8(&f[8 * gg], &hi[8 * gg], &lo[8 * gg]);
-                put_tile_row(false, 0, image_of(out, kImFghi), r, hi, cb * 4, 4);
-                put_tile_row(false, 0, image_of(out, kImFglo), r, lo, cb * 4, 4);
-              }
+              for (int gg = 0; gg < 4; ++gg) split8(&f[8 * gg], &hi[8 * gg], &lo[8 * gg]);
+              put_tile_row(false, 0, image_of(out, kImFghi), r, hi, cb * 4, 4);
+              put_tile_row(false, 0, image_of(out, kImFglo), r, lo, cb * 4, 4);
             }
           }
         }
@@ -754,7 +753,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
     }
   }
   if (__syncthreads_or(!ok) && tid == 0 && status) atomicOr(status, kStatusTimeout);
-  if (tid == 0) {  // drain: the products, and the T copies if nobody waited for them
+  if (tid == 0) {  // drain: the products, and the copies if nobody waited for them
     mma_commit(smem_u32(&bars[5]));
     mbar_wait(smem_u32(&bars[5]), 0, never_s);
     if (!copied) mbar_wait(smem_u32(&bars[2]), 0, never_s);

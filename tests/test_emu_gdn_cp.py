@@ -381,8 +381,8 @@ def test_backward_reusing_the_forward_matches_the_oracle(emulator):
 @pytest.mark.parametrize("mutation", [
     ("f32[xx] = s <= t ? __expf(ct - sc[s]) * dp : 0.f;",
      "f32[xx] = s < t ? __expf(ct - sc[s]) * dp : 0.f;"),
-    ("mma_group(tb + 384, sb + kGr4, sb + kGr2, true, false);  // ZW = T^T (w K)",
-     "mma_group_amn(tb + 384, sb + kGr4, sb + kGr2, true, false);  // ZW = T^T (w K)"),
+    ("mma_group(tb + 384, sb + kGr4, sb + kGr1, true, false);  // ZW = T^T (w K)",
+     "mma_group_amn(tb + 384, sb + kGr4, sb + kGr1, true, false);  // ZW = T^T (w K)"),
     ("      for (int xx = 0; xx < 32; ++xx) f32[xx] += __uint_as_float(t32[xx]);",
      "      for (int xx = 0; xx < 32; ++xx) f32[xx] -= __uint_as_float(t32[xx]);"),
 ], ids=["LdP_without_its_diagonal", "ZW_with_T_read_M_major", "dU_with_ZW_G_subtracted"])
