@@ -140,14 +140,16 @@ def max_over_ranks(ms: float, device) -> float:
     return float(t.item())
 
 
-def replay_config(workload: str, w, world: int, host_pages: int = 0) -> dict:
+def replay_config(workload: str, w, world: int, host_pages: int = 0, member_major: bool = False) -> dict:
     """The config object of a replay line; both arms print the same one."""
     kv_bytes_pass = w.prompt_len * w.hkv * w.head_dim * 2 * (2 if w.dtype == "bf16" else 4)
+    order = ("one member at a time" if member_major else
+             "chunk-major: each pass streams the prompt once for the group")
     return {"workload": workload, "prompt_len": w.prompt_len, "resp_lens": list(w.resp_lens),
             "group": w.group, "hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim,
             "page_size": w.page_size, "parallelism": f"replicas x{world}",
             "pages": ("HBM" if host_pages <= 0 else
-                      f"pinned host memory, streamed in chunks of {host_pages} pages "
+                      f"pinned host memory, streamed in chunks of {host_pages} pages, {order} "
                       "(capture outside the timed steps)"),
             "l2": "inputs larger than L2 (prompt K/V %.1f GiB per pass)" % (kv_bytes_pass / 2**30)}
 
@@ -231,11 +233,16 @@ def run_ours(args):
         ws = torch.empty(host.workspace_bytes(max(w.resp_lens)), dtype=torch.uint8, device=dev)
         ls.ls_clear_device_status(ws)
 
-        def step():
-            for m in members:
-                host.forward(m["q"], m["k"], m["v"], m["o"], m["lse"], ws)
-                host.backward(m["q"], m["k"], m["v"], m["d_o"], m["o"], m["lse"], m["dq"],
-                              m["dk"], m["dv"], ws)
+        if args.host_pages_member_major:
+            def step():
+                for m in members:
+                    host.forward(m["q"], m["k"], m["v"], m["o"], m["lse"], ws)
+                    host.backward(m["q"], m["k"], m["v"], m["d_o"], m["o"], m["lse"], m["dq"],
+                                  m["dk"], m["dv"], ws)
+        else:
+            def step():  # chunk-major: each pass streams the prompt once for the group
+                host.forward_group(members, ws)
+                host.backward_group(members, ws)
 
     for _ in range(args.warmup):
         step()
@@ -337,7 +344,8 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic (seeded N(0,1)/sqrt(d) Q/K/V, N(0,1) dO, random page table)",
             "config": replay_config(args.workload, w, world,
-                                    args.host_pages if host is not None else 0),
+                                    args.host_pages if host is not None else 0,
+                                    args.host_pages_member_major),
             "prompt_kv_gbs": round(kv_gbs, 1),
             "replays_per_s": round(G * world / (ms_step * 1e-3), 4),
             "roofline": roof,
@@ -639,7 +647,7 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": replay_config(args.workload, w, world, args.host_pages),
+        "config": replay_config(args.workload, w, world, args.host_pages, args.host_pages_member_major),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -1078,6 +1086,9 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the short-response leg and the G=2/G=8 memory check")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--host-pages-member-major", action="store_true",
+                    help="with --host-pages: one member at a time (the prompt streamed once per "
+                         "member and pass) instead of chunk-major over the group")
     ap.add_argument("--host-pages", type=int, default=0,
                     help="keep the prompt pages in pinned host memory, streamed in chunks of "
                          "this many pages (0: pages in HBM)")

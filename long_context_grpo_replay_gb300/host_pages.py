@@ -21,6 +21,13 @@ Every chunk is an exact share of the keys, so the result is exact:
 Device memory holds two chunks of pages plus one float32 partial per chunk,
 however long the prompt.  Every step, the page copies included, runs in the
 library.
+
+A group can run chunk-major instead (forward_group, backward_group): each
+pass stages every chunk once and runs all members' shares over it before
+the next chunk, so the prompt crosses the CPU-GPU link once per pass for the
+whole group rather than once per member.  The price is that every member's
+chunk partials are live at once (float32 [chunks, R, Hq, d] per member)
+instead of one member's.
 """
 from __future__ import annotations
 
@@ -159,3 +166,44 @@ class HostPagedReplay:
 
         self._stream_chunks(run, ws)
         ls.ls_sum_parts(dq_parts, dq)
+
+    def forward_group(self, members, ws):
+        """Chunk-major forward of a group: members are dicts with q, k, v, o,
+        lse (o and lse written)."""
+        n = self.n_chunks()
+        parts = []
+        for m in members:
+            R, hq, d = m["q"].shape
+            parts.append((torch.empty((n, R, hq, d), dtype=torch.float32, device=m["q"].device),
+                          torch.empty((n, R, hq), dtype=torch.float32, device=m["q"].device)))
+
+        def run(i, prompt):
+            for m, (po, pl) in zip(members, parts):
+                ls.ls_replay_fwd_part(self.desc, prompt, m["q"], m["k"], m["v"], i == 0, po[i], pl[i], ws)
+
+        self._stream_chunks(run, ws)
+        for m, (po, pl) in zip(members, parts):
+            R, hq, d = m["q"].shape
+            ls.ls_lse_merge(po.view(n, R * hq, d), pl.view(n, R * hq), m["o"], m["lse"])
+
+    def backward_group(self, members, ws):
+        """Chunk-major backward of a group: members also carry d_o, and dq,
+        dk, dv (written)."""
+        n = self.n_chunks()
+        state = []
+        for m in members:
+            R, hq, d = m["q"].shape
+            delta = torch.empty((R, hq), dtype=torch.float32, device=m["q"].device)
+            ls.ls_replay_bwd_preprocess(self.desc, m["o"], m["d_o"], delta)
+            state.append((delta, torch.empty((n, R, hq, d), dtype=torch.float32, device=m["q"].device)))
+
+        def run(i, prompt):
+            first = i == 0
+            for m, (delta, dqp) in zip(members, state):
+                ls.ls_replay_bwd_part(self.desc, prompt, m["q"], m["k"], m["v"], m["d_o"], m["lse"], delta,
+                                      first, dqp[i], m["dk"] if first else None,
+                                      m["dv"] if first else None, ws)
+
+        self._stream_chunks(run, ws)
+        for m, (_, dqp) in zip(members, state):
+            ls.ls_sum_parts(dqp, m["dq"])

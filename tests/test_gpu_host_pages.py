@@ -54,6 +54,38 @@ def test_host_paged_replay_matches_the_oracle(cuda_device, P, chunk):
     assert all(e <= tol for e in errs.values()) and e_l <= LSE_TOL, (P, chunk, errs, e_l)
 
 
+def test_host_paged_group_chunk_major_matches_the_oracle(cuda_device):
+    """Two members of different lengths, chunk-major (every chunk staged
+    once for both): each member's O, LSE, dQ, dK, dV against the oracle."""
+    dev = cuda_device
+    P, chunk = 5000, 3
+    w = inputs.Workload("hostgroup", 24, 4, 256, 256, P, (300, 77), "bf16", seed=29, pool_factor=2,
+                        poison=True)
+    pr = inputs.make_prompt(w, "cpu")
+    kh, vh = pr["k_pool"].pin_memory(), pr["v_pool"].pin_memory()
+    desc = ls.desc_for(w.hq, w.hkv, w.head_dim, w.page_size, torch.bfloat16, w.scale)
+    rep = HostPagedReplay(desc, kh, vh, pr["page_table"], P, chunk, dev)
+    cpu_members = [inputs.make_member(w, g, "cpu") for g in range(2)]
+    members = []
+    for m in cpu_members:
+        q, k, v, d_o = (m[x].to(dev) for x in ("q", "k", "v", "d_o"))
+        R = q.shape[0]
+        members.append({"q": q, "k": k, "v": v, "d_o": d_o, "o": torch.empty_like(q),
+                        "lse": torch.empty(R, w.hq, device=dev, dtype=torch.float32),
+                        "dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v)})
+    ws = torch.empty(rep.workspace_bytes(max(w.resp_lens)), dtype=torch.uint8, device=dev)
+    ls.ls_clear_device_status(ws)
+    rep.forward_group(members, ws)
+    rep.backward_group(members, ws)
+    ls.ls_read_device_status(ws)
+    for m, mc in zip(members, cpu_members):
+        want = ref.replay_member(pr["k_pool"], pr["v_pool"], pr["page_table"], P, mc["q"], mc["k"],
+                                 mc["v"], mc["d_o"], scale=w.scale)
+        errs = {key: rel_err(m[key].double().cpu().numpy(), want[key]) for key in ("o", "dq", "dk", "dv")}
+        e_l = float(np.abs(m["lse"].double().cpu().numpy() - want["lse"]).max())
+        assert all(e <= TOL["bf16"] for e in errs.values()) and e_l <= LSE_TOL, (errs, e_l)
+
+
 def test_sum_parts(cuda_device):
     g = torch.Generator(device=cuda_device).manual_seed(3)
     parts = torch.randn(5, 1000, 4, device=cuda_device, generator=g)
