@@ -1007,7 +1007,6 @@ __global__ void __launch_bounds__(kOutThr, 1)
   const uint32_t cbar = smem_u32(&bars[6]);  // the tile images' bulk copies, one phase per round
   uint32_t ncp = 0, nwt = 0;  // copy phases issued, and waited for (every thread keeps both)
   int pend = -1;              // thread 0: parity of a copy phase whose wait gave up
-  const int64_t rs = (int64_t)H * kD;
   const bool live = t < nt;
   const int r0 = (warp & 3) * 32;  // first row of this warp's 32
   const int64_t rowt = ((t0 + t) * H + h) * kD;  // row t of q, k, v, d_o, o, dq, dk, dv
