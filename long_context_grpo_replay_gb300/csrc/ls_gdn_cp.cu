@@ -1220,10 +1220,21 @@ __global__ void __launch_bounds__(kOutThr, 1)
           rv[xx] = fmaf(da * bt, gkv, rv[xx]);
           mk = da * bt * __expf(ct - sc[s]);
         }
-        if (s <= t) {
-          const uint16_t hb = bf16_of(mk);
-          st_shared_u16(S3 + elem_off(t, s), hb);
-          st_shared_u16(S3 + elem_off(s, t), hb);
+        gkr[xx] = mk;  // M row t, column s (zero on and right of the diagonal)
+        if (s <= t) st_shared_u16(S3 + elem_off(s, t), bf16_of(mk));  // M^T: column t, row s
+      }
+      // M row t: whole 16-byte pieces left of the diagonal, single elements
+      // in the piece that holds it (only thread t writes row t at or left of
+      // column t; the rest of the row belongs to the other rows' M^T)
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) {
+        const int s0 = cb * 32 + 8 * gg;
+        if (s0 + 7 <= t) {
+          st_shared_v4(S3 + tile_off(t, cb * 4 + gg), pack8(&gkr[8 * gg]));
+        } else if (s0 <= t) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (s0 + u <= t) st_shared_u16(S3 + elem_off(t, s0 + u), bf16_of(gkr[8 * gg + u]));
         }
       }
       // row sums of r stay with the thread; column sums over the warp's rows
