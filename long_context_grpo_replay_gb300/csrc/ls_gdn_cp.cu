@@ -88,19 +88,6 @@ __device__ __forceinline__ void split8(const float* x, float* hi, float* lo) {
     lo[u] = x[u] - hi[u];
   }
 }
-// A 32 KB tile image from global memory into shared memory, by the 128
-// threads whose index among them is tid.
-__device__ __forceinline__ void copy_image(uint32_t tile, const float* img, int tid) {
-  const uint4* src = reinterpret_cast<const uint4*>(img);
-#pragma unroll 1
-  for (int i0 = 0; i0 < 16; i0 += 8) {
-    uint4 v[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = src[tid + kThr * (i0 + j)];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) st_shared_v4(tile + 16u * (tid + kThr * (i0 + j)), v[j]);
-  }
-}
 // Bulk copies of n tile images into shared-memory tiles, completing on bar
 // (thread 0 of the CTA; the tiles' previous readers must be done).
 __device__ __forceinline__ void copy_tiles(uint32_t bar, int n, const uint32_t* dst, const float* const* src) {

@@ -77,11 +77,6 @@ __device__ __forceinline__ void stage_rows(uint32_t tile, const float* src, int6
     }
   }
 }
-// One row of a tile from 128 registers (thread = row).
-__device__ __forceinline__ void stage_row_regs(uint32_t tile, int r, const float (&x)[kD]) {
-#pragma unroll
-  for (int gq = 0; gq < 16; ++gq) st_shared_v4(tile + tile_off(r, gq), pack8(&x[8 * gq]));
-}
 // D[tmem] (+)= A B^T over K = 128 (eight K steps); B K-major or N-major.
 __device__ __forceinline__ void mma_group(uint32_t d, uint32_t a, uint32_t b, bool b_mn, bool acc) {
   const uint32_t id = idesc_bf16(128, 128, b_mn);
@@ -97,56 +92,6 @@ __device__ __forceinline__ void mma_group_amn(uint32_t d, uint32_t a, uint32_t b
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
     mma_ss(d, mndesc(a, kk), b_mn ? mndesc(b, kk) : kdesc(b, kk), id, (acc || kk > 0) ? 1u : 0u);
-}
-// ---- thread-per-row code and coalesced global rows.  The 32 threads of a
-// warp own 32 consecutive rows; a [32 rows x 32 columns] float block moves
-// between global memory and their registers through a padded [32 x 33]
-// shared-memory scratch of the warp, so every global access is one 128-byte
-// row segment (one row per warp instruction) instead of 32 rows' scattered
-// words.  Rows at or past nvalid (relative to the block) read as 0 / are not
-// written.  base points to the block's element (0, 0); row r at base + r * stride.
-// v: 32 consecutive values of the thread's row (registers when the caller's
-// indices are compile-time constants).
-__device__ __forceinline__ void rows_load32(float* v, const float* base, int64_t stride, int nvalid,
-                                            float* scr) {
-  const int lane = threadIdx.x & 31;
-  float tmp[32];  // all 32 loads issued before the first shared store
-#pragma unroll
-  for (int r = 0; r < 32; ++r) tmp[r] = r < nvalid ? base[r * stride + lane] : 0.f;
-#pragma unroll
-  for (int r = 0; r < 32; ++r) scr[r * 33 + lane] = tmp[r];
-  __syncwarp();
-#pragma unroll
-  for (int c = 0; c < 32; ++c) v[c] = scr[lane * 33 + c];
-  __syncwarp();
-}
-__device__ __forceinline__ void rows_store32(const float* v, float* base, int64_t stride, int nvalid,
-                                             float* scr) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int c = 0; c < 32; ++c) scr[lane * 33 + c] = v[c];
-  __syncwarp();
-#pragma unroll 4
-  for (int r = 0; r < 32; ++r)
-    if (r < nvalid) base[r * stride + lane] = scr[r * 33 + lane];
-  __syncwarp();
-}
-// The same for rows r0 .. r0+31 of a packed strict lower triangle (row t at
-// t (t - 1) / 2), columns c0 .. c0+31: v[c] = element (r0 + lane, c0 + c).
-// Entries on or above the diagonal come out as whatever the packing holds
-// there (the caller masks them); every read stays below row 128's start.
-__device__ __forceinline__ void rows_load32_packed(float* v, const float* packed, int r0, int c0,
-                                                   float* scr) {
-  const int lane = threadIdx.x & 31;
-  float tmp[32];
-#pragma unroll
-  for (int r = 0; r < 32; ++r) tmp[r] = packed[(r0 + r) * (r0 + r - 1) / 2 + c0 + lane];
-#pragma unroll
-  for (int r = 0; r < 32; ++r) scr[r * 33 + lane] = tmp[r];
-  __syncwarp();
-#pragma unroll
-  for (int c = 0; c < 32; ++c) v[c] = scr[lane * 33 + c];
-  __syncwarp();
 }
 // Column sums of a [32 x 32] block held one row per lane (v[c] = column c of
 // the lane's row): after the five halving exchange rounds (31 shuffles) lane
@@ -165,15 +110,5 @@ __device__ __forceinline__ float warp_colsum32(float (&v)[32]) {
   }
   return v[0];
 }
-// Words of the per-warp row scratch (32 x 33 floats per warp, four warps).
-constexpr int kRowScrFloats = 4 * 32 * 33;
-
-// fp32 [128 x 128] shared buffer, columns XOR-swizzled by the row: row
-// writes (thread = row) and column reads (thread = column) are both free of
-// bank conflicts.
-__device__ __forceinline__ int u_at(int t, int j) { return t * kD + (j ^ (t & 31)); }
-// packed strict lower triangle
-__device__ __forceinline__ int a_at(int t, int s) { return t * (t - 1) / 2 + s; }
-
 }  // namespace gdn
 }  // namespace ls
