@@ -39,3 +39,26 @@ def compile_harness(main_cpp: str, include_dir: Path, exe: Path):
                        timeout=900)
     assert r.returncode == 0, r.stderr[-3000:]
     return exe
+
+
+class EmulatorFault(AssertionError):
+    """The emulated kernel stopped on one of the emulator's own checks (a
+    barrier protocol or shared-memory rule broken, an AddressSanitizer
+    report) instead of finishing."""
+
+
+def check_run(r):
+    """Raise EmulatorFault with the emulator's message when its run failed."""
+    if r.returncode != 0:
+        raise EmulatorFault(r.stderr[-2000:])
+
+
+def rejected(run):
+    """For a planted mistake: True when run() raises EmulatorFault from one of
+    the emulator's checks, else run()'s own verdict (a result outside the
+    tolerance must be reported as True by run)."""
+    try:
+        return run()
+    except EmulatorFault as e:
+        msg = str(e)
+        return "emulator:" in msg or "AddressSanitizer" in msg

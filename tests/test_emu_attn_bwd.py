@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle.ref as ref
-from emu_support import compile_harness
+from emu_support import check_run, compile_harness, rejected
 from long_context_grpo_replay_gb300 import inputs
 
 ROOT = Path(__file__).resolve().parents[1]
@@ -91,7 +91,7 @@ def run_case(exe, d, P=600, R=64, seed=5, span=256):
         f.write(want["delta"].astype(np.float32).tobytes())
     r = subprocess.run([str(exe), str(d / "in.bin"), str(d / "out.bin")], capture_output=True,
                        text=True, timeout=900)
-    assert r.returncode == 0, r.stderr[-2000:]
+    check_run(r)
     out = np.fromfile(d / "out.bin", dtype=np.uint32, count=2)
     parts = np.fromfile(d / "out.bin", dtype=np.float32, offset=8).reshape(ns + 1, R, w.hq, 256)
     dq = parts.astype(np.float64).sum(0) * w.scale
@@ -131,7 +131,12 @@ def test_emulated_backward_over_many_tiles(emulator):
 def test_emulator_rejects_planted_kernel_mistakes(tmp_path, mutation):
     """A wrong operand layout, a missing wait, a lost accumulation and a
     misplaced operand, each planted in a copy of the ring kernel's source,
-    must fail the comparison."""
+    must fail the comparison (or stop the emulated kernel on one of the
+    emulator's checks, which a missing wait may do)."""
     exe = build(tmp_path, mutation)
-    status, err = run_case(exe, tmp_path)
-    assert not err <= TOL_BF16, err  # also true for NaN
+
+    def wrong():
+        status, err = run_case(exe, tmp_path)
+        return not err <= TOL_BF16  # also true for NaN
+
+    assert rejected(wrong)

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import oracle.ref as ref
-from emu_support import compile_harness
+from emu_support import check_run, compile_harness
 from long_context_grpo_replay_gb300 import inputs
 
 ROOT = Path(__file__).resolve().parents[1]
@@ -65,7 +65,7 @@ def test_emulated_dkdv_matches_the_oracle(tmp_path):
         f.write(want["delta"].astype(np.float32).tobytes())
     r = subprocess.run([str(exe), str(tmp_path / "in.bin"), str(tmp_path / "out.bin")],
                        capture_output=True, text=True, timeout=900)
-    assert r.returncode == 0, r.stderr[-2000:]
+    check_run(r)
     status = np.fromfile(tmp_path / "out.bin", dtype=np.uint32, count=2)
     assert status[0] == 0, status
     raw = np.fromfile(tmp_path / "out.bin", dtype=np.uint16, offset=8)

@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle.ref as ref
-from emu_support import compile_harness
+from emu_support import check_run, compile_harness, rejected
 from long_context_grpo_replay_gb300 import inputs
 
 ROOT = Path(__file__).resolve().parents[1]
@@ -83,7 +83,7 @@ def run_case(exe, d, P=600, R=64, seed=6, span=256):
             f.write(_bf16_bytes(m[x]))
     r = subprocess.run([str(exe), str(d / "in.bin"), str(d / "out.bin")], capture_output=True,
                        text=True, timeout=900)
-    assert r.returncode == 0, r.stderr[-2000:]
+    check_run(r)
     status = np.fromfile(d / "out.bin", dtype=np.uint32, count=2)
     n = (ns + 1) * R * w.hq
     vals = np.fromfile(d / "out.bin", dtype=np.float32, offset=8)
@@ -127,7 +127,12 @@ def test_emulated_forward_over_many_tiles(emulator):
 def test_emulator_rejects_planted_kernel_mistakes(tmp_path, mutation):
     """V read as a K-major operand in P V, or a K chunk's slot refilled
     before the S that reads it is complete, planted in a copy of the kernel
-    source, must fail the comparison."""
+    source, must fail the comparison (or stop the emulated kernel on one of
+    the emulator's checks, which a missing wait may do)."""
     exe = build(tmp_path, mutation)
-    status, e_o, e_l = run_case(exe, tmp_path, P=1500, R=40, seed=7, span=1536)
-    assert not (e_o <= TOL_BF16 and e_l <= LSE_TOL), (e_o, e_l)
+
+    def wrong():
+        status, e_o, e_l = run_case(exe, tmp_path, P=1500, R=40, seed=7, span=1536)
+        return not (e_o <= TOL_BF16 and e_l <= LSE_TOL)
+
+    assert rejected(wrong)

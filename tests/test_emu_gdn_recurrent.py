@@ -12,7 +12,7 @@ from pathlib import Path
 import numpy as np
 import pytest
 
-from emu_support import compile_harness
+from emu_support import check_run, compile_harness
 from long_context_grpo_replay_gb300 import inputs
 from oracle.gdn import gdn_replay
 
@@ -49,7 +49,7 @@ def run_case(exe, d, B=2, H=1, R=20, seed=13):
             c[x].numpy().astype(np.float32).tofile(f)
     r = subprocess.run([str(exe), str(d / "in.bin"), str(d / "out.bin")], capture_output=True,
                        text=True, timeout=900)
-    assert r.returncode == 0, r.stderr[-2000:]
+    check_run(r)
     out = np.fromfile(d / "out.bin", dtype=np.float32)
     nt, ns, nsc = B * R * H * 128, B * H * 128 * 128, B * R * H
     sizes = [("o", nt), ("s_final", ns), ("dq", nt), ("dk", nt), ("dv", nt), ("dg", nsc),
