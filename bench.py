@@ -373,7 +373,9 @@ def short_response_leg(args, desc, prompt, ws, stream, dev, pk, clocks):
     prompt pages already written, timed (steps x group replay, after the
     warm-up) with CUDA events on the stream.  Reports the forward's and the
     backward's prompt-K/V GB/s and their fractions of the HBM and tensor
-    peaks, next to the ceiling the arithmetic intensity allows: at R = 64 a
+    peaks (with each kernel's DRAM bytes per launch when an ncu capture of
+    the current source is recorded), next to the ceiling the arithmetic
+    intensity allows: at R = 64 a
     prompt-K/V byte carries 384 flop in the forward and 576 in the backward,
     above the ridge of the measured peaks, so the tensor pipe, not HBM, is the
     first limit."""
@@ -436,7 +438,10 @@ def short_response_leg(args, desc, prompt, ws, stream, dev, pk, clocks):
                      "tflops": round(fl / (lms * 1e-3) / 1e12, 1),
                      "tensor_frac": round(fl / (lms * 1e-3) / 1e12 / peak_t, 4),
                      "flop_per_byte": round(intensity, 1),
-                     "hbm_frac_ceiling": round(min(1.0, ridge / intensity), 4)}
+                     "hbm_frac_ceiling": round(min(1.0, ridge / intensity), 4),
+                     "traffic": recorded_traffic(kern, SHORT_WORKLOAD,
+                                                 ROOT / "long_context_grpo_replay_gb300" / "csrc" /
+                                                 ("ls_tc_fwd.cu" if name == "fwd" else "ls_tc_bwd.cu"))}
     if "fwd" in legs and "bwd" in legs:
         gbs = 2 * kv / ((legs["fwd"] + legs["bwd"]) * 1e-3) / 1e9
         inten = 10.0 * R * P * d * hq / (2 * kv)

@@ -86,6 +86,10 @@ WORKLOADS = {
     # bf16 P=2M, G=8 x R=64: the short-response KV-streaming variant
     "bf16_p2m_r64_g8": Workload("bf16_p2m_r64_g8", 24, 4, 256, 256, 2097152,
                                 (64,) * 8, "bf16", 4),
+    # bf16 P=256K, G=8 x R=64: the short-response case at a size an ncu capture
+    # of every counter pass can hold (prompt K/V still larger than L2)
+    "bf16_p256k_r64_g8": Workload("bf16_p256k_r64_g8", 24, 4, 256, 256, 262144,
+                                  (64,) * 8, "bf16", 4),
     # bf16 stress: P=4,456,448 scattered over a 2x pool (unused slots NaN), ragged R
     "bf16_p4m_ragged_g8": Workload("bf16_p4m_ragged_g8", 24, 4, 256, 256, 4456448,
                                    _stress_lens(5, 8), "bf16", 5, pool_factor=2, poison=True),
