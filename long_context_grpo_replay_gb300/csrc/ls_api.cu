@@ -355,6 +355,8 @@ LaunchScope::LaunchScope(int32_t k, cudaStream_t s) : kid(k), stream(s), ev0(nul
   if (e && cudaEventRecord(e, s) == cudaSuccess) ev0 = e;
 }
 
+void LaunchScope::more_kernels(int n) { g_launch_count.fetch_add(n, std::memory_order_relaxed); }
+
 namespace {
 // LS_DEBUG_SYNC=1: synchronise after every launch and log it to stderr, so
 // that a stall or an error names its kernel.

@@ -1596,6 +1596,7 @@ cudaError_t launch_gdn_cp_fwd(int B, int H, int R, const float* s0, const float*
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gdn_cp_fwd_out_kernel<<<dim3(nch, H, B), kOutThr, kFoSmem, st>>>(H, R, nch, q, k, g, beta, ws, o,
                                                                   status);
+  ls.more_kernels(2);
   return cudaGetLastError();
 }
 
@@ -1628,6 +1629,7 @@ cudaError_t launch_gdn_cp_bwd(int B, int H, int R, const float* s0, const float*
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gdn_cp_out_kernel<<<dim3(nch, H, B), kOutThr, kOutSmem, st>>>(H, R, nch, q, k, v, g, beta, d_o, ws,
                                                                nullptr, dq, dk, dv, dg, dbeta, status);
+  ls.more_kernels(reuse_forward ? 2 : 3);
   return cudaGetLastError();
 }
 

@@ -49,6 +49,9 @@ enum KernelId : int32_t {
 struct LaunchScope {
   LaunchScope(int32_t kid, cudaStream_t s);
   ~LaunchScope();
+  // A scope counts as one kernel launch; a launcher that runs n kernels
+  // under one scope (one trace entry) adds the other n - 1 here.
+  void more_kernels(int n);
   int32_t kid;
   cudaStream_t stream;
   void* ev0;

@@ -116,3 +116,29 @@ def test_backward_reusing_the_forward_is_bit_identical(cuda_device, B, H, R):
     if R <= 300:
         for b in range(B):
             _check(c, o, s_final, b, range(H), got)
+
+
+def test_every_kernel_launch_is_counted(cuda_device):
+    """ls_launch_count counts kernels, not calls: the forward runs three
+    (prep, chain, output), the backward three when it reuses the forward's
+    terms and four when it forms them itself."""
+    B, H, R = 1, 2, 200
+    c = inputs.make_gdn_group(B, H, R, seed=5, device=cuda_device)
+    ws = torch.empty(ls.ls_gdn_workspace_size(ls.GdnDesc(B, H, 128, 128, TC), R), dtype=torch.uint8,
+                     device=cuda_device)
+    ls.ls_clear_device_status(ws)
+    o = torch.empty_like(c["v"])
+    s_final = torch.empty((B, H, 128, 128), device=cuda_device)
+    grads = [torch.empty_like(c[x]) for x in ("q", "k", "v", "g", "beta")]
+    n0 = ls.ls_launch_count()
+    ls.ls_gdn_replay_fwd(c["s0"], c["q"], c["k"], c["v"], c["g"], c["beta"], o, s_final, ws, precision=TC)
+    n1 = ls.ls_launch_count()
+    ls.ls_gdn_replay_bwd(c["s0"], c["q"], c["k"], c["v"], c["g"], c["beta"], c["d_o"], *grads, ws,
+                         precision=TC, reuse_forward=True)
+    n2 = ls.ls_launch_count()
+    ls.ls_gdn_replay_bwd(c["s0"], c["q"], c["k"], c["v"], c["g"], c["beta"], c["d_o"], *grads, ws,
+                         precision=TC)
+    n3 = ls.ls_launch_count()
+    torch.cuda.synchronize()
+    ls.ls_read_device_status(ws)
+    assert (n1 - n0, n2 - n1, n3 - n2) == (3, 3, 4)
