@@ -45,22 +45,24 @@ using namespace gdn;
 // the 32 threads of a warp, holding 32 consecutive rows, touch 512
 // contiguous bytes with each 16-byte access):
 //   kE0, kDU0       E0 and dU0 (prep)
-//   kSstart, kGend  S at the chunk's start, G = dL/dS at its end (chain)
+//   kSstart         S at the chunk's start (chain)
 //   kDUblk          dU (out, for its own later passes)
 //   kGKblk          GK (prep; zero on and above the diagonal)
 // then bf16 tile images of 32 KB in the swizzled shared-memory layout, so a
 // plain copy lands them ready for the MMAs: ZK, ZW, -M, F hi, F lo, -M',
 // F' hi, F' lo (rows as in the formulas above), T hi, T lo (row x = column x
 // of T), and the tiles of K, Q, dO (token rows; prep), S at the chunk's start
-// and G at its end (state rows; chain) for the output kernels; then 16
-// floats, the first gamma_C.
-enum : int { kE0 = 0, kDU0, kSstart, kGend, kDUblk, kGKblk, kFloatBlocks };
+// and G = dL/dS at its end (state rows; chain) for the output kernels; then
+// 16 floats: gamma_C (prep), then <G, S> of G at the chunk's end and S at its
+// start (the backward chain).
+enum : int { kE0 = 0, kDU0, kSstart, kDUblk, kGKblk, kFloatBlocks };
 enum : int {
   kImZK = 0, kImZW, kImM, kImFhi, kImFlo, kImMg, kImFghi, kImFglo, kImThi, kImTlo,
   kImK, kImQ, kImDO, kImS, kImG, kImages
 };
 constexpr int64_t kImgFloats = kTile / 4;
 constexpr int64_t kGammaAt = (int64_t)kFloatBlocks * kTileElems + kImages * kImgFloats;
+constexpr int64_t kGsAt = kGammaAt + 1;
 constexpr int64_t kScrFloats = kGammaAt + 16;
 
 __device__ __forceinline__ float* scratch_of(float* scr, int H, int nch, int m, int h, int ch) {
@@ -761,7 +763,10 @@ __global__ void __launch_bounds__(kPrepThr, 1)
 // hi + lo, the identity as A).  The chunk's three tiles come from prep's
 // images by bulk copy; the next chunk's copies start as soon as the current
 // chunk's products have read theirs.  256 threads: thread (x, half) keeps
-// columns 64 half .. 64 half + 63 of state row x.
+// columns 64 half .. 64 half + 63 of state row x.  A backward step also
+// forms <G, S> of the chunk (G at its end, S at its start, both fp32) while
+// its products run, for the output kernel's dg; the eight warps' partial
+// sums meet in a fixed order, so the sum does not depend on timing.
 constexpr uint32_t kChI = 0, kChShi = kTile, kChSlo = 2 * kTile, kChM = 3 * kTile,
                    kChFhi = 4 * kTile, kChFlo = 5 * kTile, kChMisc = 6 * kTile;
 constexpr uint32_t kChainSmem = kChMisc + 1024 + 1024;
@@ -780,6 +785,7 @@ __global__ void __launch_bounds__(kChThr, 1)
   const uint32_t sb = smem_u32(sm);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kChMisc);  // copies, products, drain
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
+  float* gsw = reinterpret_cast<float*>(sm + kChMisc + 64);  // <G, S>: one partial per warp
   uint32_t* abort_s = tslot + 1;
   uint32_t* never_s = tslot + 2;  // stays 0: the drain's waits are bounded by time alone
 
@@ -821,6 +827,7 @@ __global__ void __launch_bounds__(kChThr, 1)
     bulk_load(sb + kChM, image_of(blk, bw ? kImMg : kImM), kTile, bar);
     bulk_load(sb + kChFhi, image_of(blk, bw ? kImFghi : kImFhi), kTile, bar);
     bulk_load(sb + kChFlo, image_of(blk, bw ? kImFglo : kImFlo), kTile, bar);
+    if (bw) prefetch_l2(blk + (int64_t)kSstart * kTileElems, kTileElems * 4);  // for <G, S>
   };
   if (tid == 0 && i0 < i1) issue(i0);
 
@@ -848,10 +855,10 @@ __global__ void __launch_bounds__(kChThr, 1)
     if (i == steps) break;
     float* blk = scratch_of(scr, H, nch, m, h, chunk_at(i));
     const float gc = blk[kGammaAt];
-    {  // S at the chunk's start / G at its end, row x
-      float* dst = blk + (int64_t)(bw ? kGend : kSstart) * kTileElems;
+    float* sst = blk + (int64_t)kSstart * kTileElems;
+    if (!bw) {  // S at the chunk's start, row x
 #pragma unroll
-      for (int c = 0; c < 16; ++c) *blk4(dst, x, c0 / 4 + c) = make_float4(st[4 * c], st[4 * c + 1], st[4 * c + 2], st[4 * c + 3]);
+      for (int c = 0; c < 16; ++c) *blk4(sst, x, c0 / 4 + c) = make_float4(st[4 * c], st[4 * c + 1], st[4 * c + 2], st[4 * c + 3]);
     }
     uint8_t* simg = reinterpret_cast<uint8_t*>(image_of(blk, bw ? kImG : kImS));  // bf16 S (or G) for the output kernels
 #pragma unroll
@@ -883,9 +890,28 @@ __global__ void __launch_bounds__(kChThr, 1)
       }
     }
     ++ncp;
+    if (bw) {  // <G, S> of this chunk, row x (S read back as this thread wrote it)
+      float gs = 0.f;
+#pragma unroll
+      for (int c4 = 0; c4 < 16; c4 += 4) {
+        float4 a4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) a4[u] = *blk4(sst, x, c0 / 4 + c4 + u);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float* sv = &st[4 * (c4 + u)];
+          gs = fmaf(sv[0], a4[u].x, fmaf(sv[1], a4[u].y, fmaf(sv[2], a4[u].z, fmaf(sv[3], a4[u].w, gs))));
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, off);
+      if ((tid & 31) == 0) gsw[warp] = gs;
+    }
     ok = mbar_wait_warp(smem_u32(&bars[1]), nmm++ & 1, abortp);
     if (__syncthreads_or(!ok)) break;
     if (tid == 0 && i + 1 < steps) issue(i + 1);  // the products have read this step's tiles
+    if (bw && tid == 32)  // the next step's partials come after its next barrier
+      blk[kGsAt] = ((gsw[0] + gsw[1]) + (gsw[2] + gsw[3])) + ((gsw[4] + gsw[5]) + (gsw[6] + gsw[7]));
     tc_fence_after();
 #pragma unroll
     for (int cb = 0; cb < 2; ++cb) {
@@ -952,8 +978,8 @@ __global__ void __launch_bounds__(kOutThr, 1)
   float* sgam = sbt + kC;
   float* sw = sgam + kC;
   float* rcol = sw + kC;
-  float* part = rcol + kC;     // [5][128] row sums of the second column half
-  float* swt = part + 5 * kC;  // 8 floats of scan and reduction scratch
+  float* part = rcol + kC;     // [4][128] row sums of the second column half
+  float* swt = part + 4 * kC;  // 8 floats of scan and reduction scratch
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOutMisc + 5184);
   float* colpart = reinterpret_cast<float*>(sm + kOutMisc + 5376);  // [4][128] column sums of r per row quarter
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 7);
@@ -972,8 +998,6 @@ __global__ void __launch_bounds__(kOutThr, 1)
     dq += tok * kD, dk += tok * kD, dv += tok * kD, dg += tok, dbeta += tok;
   }
   float* blk = scratch_of(scr, H, nch, m, h, ch);
-  const float* Sst = blk + (int64_t)kSstart * kTileElems;
-  const float* Gen = blk + (int64_t)kGend * kTileElems;
   float* dUb = blk + (int64_t)kDUblk * kTileElems;
   const float* gkb = blk + (int64_t)kGKblk * kTileElems;
   if (tid == 0) {
@@ -1009,7 +1033,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
   // tiles come from images) and the chunk's scratch blocks
   if (live) prefetch_l2((hf ? v : d_o) + rowt, kD * 4);
   if (tid == 0) {
-    prefetch_l2(blk, 4 * kTileElems * 4);                             // E0, dU0, S, G
+    prefetch_l2(blk, 2 * kTileElems * 4);                             // E0, dU0
     prefetch_l2(blk + (int64_t)kGKblk * kTileElems, kTileElems * 4);  // GK
     const uint32_t dst[4] = {S0, S1, S2, S3};  // ---- round 0 tiles: ZK, ZW, S, G
     const float* src[4] = {image_of(blk, kImZK), image_of(blk, kImZW), image_of(blk, kImS),
@@ -1315,7 +1339,6 @@ __global__ void __launch_bounds__(kOutThr, 1)
   if (!__syncthreads_or(!ok)) {
     tc_fence_after();
     const float wt = sw[t];
-    float gs = 0.f;  // this half's part of <G, S> over row t
 #pragma unroll 1
     for (int cb = cb0; cb < cb0 + 2; ++cb) {
       uint32_t a32[32], b32[32];
@@ -1327,11 +1350,6 @@ __global__ void __launch_bounds__(kOutThr, 1)
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) f32[xx] = fmaf(wt, __uint_as_float(b32[xx]), __uint_as_float(a32[xx]));
       row_st32(f32, dk + rowt + cb * 32, live);
-      float ga[32], sa[32];
-      blk_ld32(ga, Gen, t, cb * 32);
-      blk_ld32(sa, Sst, t, cb * 32);
-#pragma unroll
-      for (int xx = 0; xx < 32; ++xx) gs = fmaf(ga[xx], sa[xx], gs);
     }
     // the second half's row sums to the first; the column sums of r
     if (hf) {
@@ -1339,7 +1357,6 @@ __global__ void __launch_bounds__(kOutThr, 1)
       part[1 * kC + t] = dbt;
       part[2 * kC + t] = rrow;
       part[3 * kC + t] = rw;
-      part[4 * kC + t] = gs;
     }
     __syncthreads();
     float rws = 0.f;
@@ -1349,17 +1366,10 @@ __global__ void __launch_bounds__(kOutThr, 1)
       dbt += part[1 * kC + t];
       rrow += part[2 * kC + t];
       rw += part[3 * kC + t];
-      gs += part[4 * kC + t];
       rws = rw;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        gs += __shfl_xor_sync(0xffffffffu, gs, off);
-        rws += __shfl_xor_sync(0xffffffffu, rws, off);
-      }
-      if (lane == 0) {
-        swt[warp] = gs;
-        swt[4 + warp] = rws;
-      }
+      for (int off = 16; off > 0; off >>= 1) rws += __shfl_xor_sync(0xffffffffu, rws, off);
+      if (lane == 0) swt[4 + warp] = rws;
     }
     __syncthreads();
     // dc and its reverse cumulative sum over the chunk (first half: one thread per row)
@@ -1367,7 +1377,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
     if (!hf) {
       float dc = dgam * sgam[t] + rrow - rcol[t] - rw;
       if (t == kC - 1)
-        dc += (swt[4] + swt[5] + swt[6] + swt[7]) + sgam[kC - 1] * (swt[0] + swt[1] + swt[2] + swt[3]);
+        dc += (swt[4] + swt[5] + swt[6] + swt[7]) + sgam[kC - 1] * blk[kGsAt];
       x = dc;  // suffix sum within the warp
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {

@@ -183,10 +183,10 @@ def test_gdn_workspace_and_argument_checks(ls):
     # the 256-byte status header, then the precision's own scratch: per (member,
     # head) the recurrent backward keeps one 128x128 float32 state per 8-token
     # checkpoint plus a segment of 8 states; the chunk-parallel one keeps, per
-    # 128-token chunk, six 128x128 float32 blocks, fifteen 32 KB bf16 tiles
+    # 128-token chunk, five 128x128 float32 blocks, fifteen 32 KB bf16 tiles
     # and 16 floats
     rec = [256 + 8 * 32 * (n + 8) * 128 * 128 * 4 for n in (1, 8, 9, 512)]
-    cp = [256 + 8 * 32 * -(-R // 128) * (6 * 128 * 128 * 4 + 15 * 32768 + 64) for R in (1, 64, 65, 4096)]
+    cp = [256 + 8 * 32 * -(-R // 128) * (5 * 128 * 128 * 4 + 15 * 32768 + 64) for R in (1, 64, 65, 4096)]
     assert [ls.ls_gdn_workspace_size(d, r) for r in (1, 64, 65, 4096)] == rec
     assert [ls.ls_gdn_workspace_size(tc, r) for r in (1, 64, 65, 4096)] == cp
     out = ctypes.c_size_t(0)

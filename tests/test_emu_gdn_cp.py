@@ -20,15 +20,17 @@ EMU = Path(__file__).resolve().parent / "emu"
 CSRC = ROOT / "long_context_grpo_replay_gb300" / "csrc"
 SRC = CSRC / "ls_gdn_cp.cu"
 TOL_BF16 = 2e-2
-# scratch per chunk: float32 [128 x 128] blocks E0, dU0, S_start, G_end, dU,
-# GK; then bf16 tile images (32 KB, the swizzled shared-memory layout) ZK,
-# ZW, -M, F hi, F lo, -M', F' hi, F' lo, T hi, T lo, K, Q, dO, S, G
-FLOAT_BLOCKS, IMAGES = 6, 15
-B_E0, B_DU0, B_SSTART, B_GEND, B_DU = range(5)
+# scratch per chunk: float32 [128 x 128] blocks E0, dU0, S_start, dU, GK;
+# then bf16 tile images (32 KB, the swizzled shared-memory layout) ZK, ZW,
+# -M, F hi, F lo, -M', F' hi, F' lo, T hi, T lo, K, Q, dO, S, G; then
+# gamma_C, <G_end, S_start> and padding
+FLOAT_BLOCKS, IMAGES = 5, 15
+B_E0, B_DU0, B_SSTART, B_DU = range(4)
 (I_ZK, I_ZW, I_M, I_FHI, I_FLO, I_MG, I_FGHI, I_FGLO, I_THI, I_TLO, I_K, I_Q, I_DO, I_S,
  I_G) = range(15)
-SCR_FLOATS = FLOAT_BLOCKS * 128 * 128 + IMAGES * 8192 + 16  # then gamma_C and padding
+SCR_FLOATS = FLOAT_BLOCKS * 128 * 128 + IMAGES * 8192 + 16
 GAMMA_AT = FLOAT_BLOCKS * 128 * 128 + IMAGES * 8192
+GS_AT = GAMMA_AT + 1
 
 
 def block(chunk, i):
@@ -174,8 +176,9 @@ def _chains(s0, q, k, v, g, b, d_o):
 
 
 def test_chains_match_the_reference(emulator):
-    """S at each chunk's start and G at its end (chain: fp32 and their bf16
-    images) and dU (out), over three chunks, the last partial."""
+    """S at each chunk's start (chain: fp32 and its bf16 image), G at its end
+    (the bf16 image) and their inner product <G, S> (the backward chain), and
+    dU (out), over three chunks, the last partial."""
     exe, d = emulator
     B, H, R = 2, 1, 300  # three chunks, the last partial; two members share s0
     c = inputs.make_gdn_group(B, H, R, seed=32)
@@ -192,13 +195,17 @@ def test_chains_match_the_reference(emulator):
             sc = scr[m, 0, ch]
             for name, got, want in (("S_start", block(sc, B_SSTART), S_start[ch]),
                                     ("S image", image(sc, I_S), S_start[ch]),
-                                    ("G_end", block(sc, B_GEND), G_end[ch]),
                                     ("G image", image(sc, I_G), G_end[ch]),
                                     ("dU", block(sc, B_DU)[:n], dU[ch][:n])):
                 if np.abs(want).max() == 0:
                     assert np.abs(got).max() == 0, name
                     continue
                 errs[name] = max(errs.get(name, 0.0), rel(got, want))
+            # <G, S>: against the product of the two norms (the sum cancels)
+            gs = float((G_end[ch] * S_start[ch]).sum())
+            scale = np.linalg.norm(G_end[ch]) * np.linalg.norm(S_start[ch])
+            errs["<G,S>"] = max(errs.get("<G,S>", 0.0),
+                                abs(float(sc[GS_AT]) - gs) / scale if scale else abs(float(sc[GS_AT])))
     print("chain max rel errs", errs)
     assert all(e <= TOL_BF16 for e in errs.values()), errs
 
