@@ -606,12 +606,16 @@ def cpu_baseline(w, k_pool, v_pool, pt, members, budget_s=20.0):
     R = m0["q"].shape[0]
     rows = np.array([R - 1])
     dt, fl = _oracle_sample(w, kp, vp, ptc, m0, rows)
+    n_rows = len(rows) * (w.hq // w.hkv)  # query-head rows the sample replays
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
             "kind": "oracle",
             "sample": f"member 0, response row {R - 1} of the {w.hq // w.hkv} query heads of KV "
                       f"head 0, forward+backward over all {w.prompt_len} prompt keys "
                       f"(float64 numpy; {dt:.1f} s)",
-            "seconds": round(dt, 2)}
+            "seconds": round(dt, 2),
+            "rows_per_s": round(n_rows / dt, 3),
+            # the member's algorithmic flops at the sample's rate
+            "extrapolated_s_per_member": round(replay_flops(w.prompt_len, R, w.hq, w.head_dim) / (fl / dt), 1)}
 
 
 def run_reference(args):
