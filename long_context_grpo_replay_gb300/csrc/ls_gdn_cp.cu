@@ -140,32 +140,42 @@ __device__ __forceinline__ void row_st32(const float* v, float* p, bool valid) {
   for (int i = 0; i < 8; ++i) p4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
-// Cumulative log-decay and write strength of the chunk's tokens into sc[],
-// sbt[] (zero past the response); swt[4] is scan scratch.  Called by all
-// threads of the block; threads past the chunk's 128 only meet the barrier.
-__device__ __forceinline__ void stage_gates(const float* g, const float* beta, int64_t t0, int nt,
-                                            int H, int h, float* sc, float* sbt, float* swt) {
+// Cumulative log-decay and write strength of the chunk's tokens, in two
+// steps so that the loads' latency hides behind other work: load_gates
+// (threads 0..127: token tid's g and b, zero past the response) early, then
+// scan_gates (every thread of the block, which meets one barrier inside; the
+// threads past the chunk's 128 only meet it) into sc[] (running log-decay)
+// and sbt[] (b); swt[4] is scan scratch.
+struct Gates {
+  float g, b;
+};
+__device__ __forceinline__ Gates load_gates(const float* g, const float* beta, int64_t t0, int nt, int H,
+                                            int h) {
+  const int tid = threadIdx.x;
+  Gates x{0.f, 0.f};
+  if (tid < kThr && tid < nt) {
+    x.g = g[(t0 + tid) * H + h];
+    x.b = beta[(t0 + tid) * H + h];
+  }
+  return x;
+}
+__device__ __forceinline__ void scan_gates(Gates x, float* sc, float* sbt, float* swt) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid >= kThr) {
     __syncthreads();
     return;
   }
-  float x = 0.f;
-  if (tid < nt) {
-    x = g[(t0 + tid) * H + h];
-    sbt[tid] = beta[(t0 + tid) * H + h];
-  } else {
-    sbt[tid] = 0.f;
-  }
+  sbt[tid] = x.b;
+  float c = x.g;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const float y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
+    const float y = __shfl_up_sync(0xffffffffu, c, off);
+    if (lane >= off) c += y;
   }
-  if (lane == 31) swt[warp] = x;
+  if (lane == 31) swt[warp] = c;
   __syncthreads();
-  for (int w = 0; w < warp; ++w) x += swt[w];
-  sc[tid] = x;
+  for (int w = 0; w < warp; ++w) c += swt[w];
+  sc[tid] = c;
 }
 
 // fp32 [128 x 128] buffer of T with rows of 129 floats: a column read by
@@ -279,6 +289,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
     const int64_t tok = (int64_t)m * R * H;
     k += tok * kD, v += tok * kD, g += tok, beta += tok;
   }
+  const Gates gates = load_gates(g, beta, t0, nt, H, h);  // scanned later
   float* out = scratch_of(scr, H, nch, m, h, ch);
   if (tid == 0) {
     for (int i = 0; i < 6; ++i) mbar_init(smem_u32(&bars[i]), 1);
@@ -299,7 +310,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   if (gt < nt) prefetch_l2((grpA ? k : v) + row0 + gt * rs, kD * 4);  // the chunk's rows into L2
 
   if (grpA) stage_rows<4>(sb + kPrepR0, k + row0, rs, nt, nullptr, gt, image_of(out, kImK));
-  stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
+  scan_gates(gates, sc, sbt, swt);
   fence_proxy_async_smem();
   __syncthreads();
   if (!grpA) {  // the right-hand sides' row scales (read after the next block barrier)
@@ -558,6 +569,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
     const int64_t tok = (int64_t)m * R * H;
     q += tok * kD, k += tok * kD, d_o += tok * kD, g += tok, beta += tok;
   }
+  const Gates gates = load_gates(g, beta, t0, nt, H, h);  // scanned later
   float* out = scratch_of(scr, H, nch, m, h, ch);
   if (tid == 0) {
     for (int i = 0; i < 6; ++i) mbar_init(smem_u32(&bars[i]), 1);
@@ -586,7 +598,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
     stage_rows<4>(sb + kGr1, q + row0, rs, nt, nullptr, gt, image_of(out, kImQ));
   else
     stage_rows<4>(sb + kGr2, d_o + row0, rs, nt, nullptr, gt, image_of(out, kImDO));
-  stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
+  scan_gates(gates, sc, sbt, swt);
   fence_proxy_async_smem();
   __syncthreads();
   if (!grpA) {  // row scales (read after the next block barrier)
@@ -997,6 +1009,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
     if (o) o += tok * kD;
     dq += tok * kD, dk += tok * kD, dv += tok * kD, dg += tok, dbeta += tok;
   }
+  const Gates gates = load_gates(g, beta, t0, nt, H, h);  // scanned later
   float* blk = scratch_of(scr, H, nch, m, h, ch);
   float* dUb = blk + (int64_t)kDUblk * kTileElems;
   const float* gkb = blk + (int64_t)kGKblk * kTileElems;
@@ -1041,7 +1054,15 @@ __global__ void __launch_bounds__(kOutThr, 1)
     copy_tiles(cbar, 4, dst, src);
   }
   ++ncp;
-  // ---- round 0: ZK S^T -> T0, ZW G^T -> T1; E into S3 (bf16) and dU rows into the scratch
+  // the gates while the copies land
+  scan_gates(gates, sc, sbt, swt);
+  __syncthreads();
+  if (hf == 0) {
+    sgam[t] = expf(sc[t]);
+    sw[t] = live ? expf(sc[kC - 1] - sc[t]) : 0.f;
+  }
+  // ---- round 0: ZK S^T -> T0, ZW G^T -> T1; E into S3 (bf16), dU rows into
+  // the scratch, and dV = diag(b) dU
   ok = wait_copies();
   if (!__syncthreads_or(!ok)) {
     if (tid == 0) {
@@ -1079,18 +1100,16 @@ __global__ void __launch_bounds__(kOutThr, 1)
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) f32[xx] += __uint_as_float(t32[xx]);
       blk_st32(f32, dUb, t, cb * 32);
+      const float bt = sbt[t];
+#pragma unroll
+      for (int xx = 0; xx < 32; ++xx) f32[xx] *= bt;
+      row_st32(f32, dv + rowt + cb * 32, live);
     }
   }
   tc_fence_before();
   __syncthreads();  // dU rows written before any thread reads them back
 
   // ---- round 1: Q K^T -> T0, Q S^T -> T1, K S^T -> T2
-  stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
-  __syncthreads();
-  if (hf == 0) {
-    sgam[t] = expf(sc[t]);
-    sw[t] = live ? expf(sc[kC - 1] - sc[t]) : 0.f;
-  }
   if (ok) ok = wait_copies();
   fence_proxy_async_smem();
   if (__syncthreads_or(!ok)) ok = false;
@@ -1262,7 +1281,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
       for (int xx = 0; xx < 32; ++xx) rw = fmaf(__uint_as_float(t32[xx]), f32[xx], rw);  // 0 past R
     }
     rw *= wt;
-    // dO tile rows scaled by gamma for dQ; dV
+    // dO tile rows scaled by gamma for dQ
 #pragma unroll
     for (int gq = 8 * hf; gq < 8 * hf + 8; ++gq) {
       const uint32_t ad = S4 + tile_off(t, gq);
@@ -1275,14 +1294,6 @@ __global__ void __launch_bounds__(kOutThr, 1)
         f8[2 * i2] = f.x * gt, f8[2 * i2 + 1] = f.y * gt;
       }
       st_shared_v4(ad, pack8(f8));
-    }
-#pragma unroll 1
-    for (int cb = cb0; cb < cb0 + 2; ++cb) {
-      float u[32];
-      blk_ld32(u, dUb, t, cb * 32);
-#pragma unroll
-      for (int xx = 0; xx < 32; ++xx) u[xx] *= bt;
-      row_st32(u, dv + rowt + cb * 32, live);
     }
     ok = wait_copies();  // K back in S1
     fence_proxy_async_smem();
@@ -1445,6 +1456,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
     const int64_t tok = (int64_t)m * R * H;
     q += tok * kD, k += tok * kD, g += tok, beta += tok, o += tok * kD;
   }
+  const Gates gates = load_gates(g, beta, t0, nt, H, h);  // scanned later
   float* blk = scratch_of(scr, H, nch, m, h, ch);
   if (tid == 0) {
     for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), 1);
@@ -1473,7 +1485,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
     copy_tiles(cbar, 3, dst, src);
   }
   if (hf == 0) stage_rows<4>(F0, q + row0, rs, nt, nullptr, t);
-  stage_gates(g, beta, t0, nt, H, h, sc, sbt, swt);
+  scan_gates(gates, sc, sbt, swt);
   bool ok = mbar_wait_warp(cbar, 0, abortp);
   const bool copied = ok;  // thread 0: the copies landed (else the drain waits for them)
   fence_proxy_async_smem();
