@@ -1221,7 +1221,8 @@ __global__ void __launch_bounds__(kOutThr, 1)
           rv[8 * gg + 2 * i2] = f.x, rv[8 * gg + 2 * i2 + 1] = f.y;
         }
       }
-      // dP row t: LdP (tile S5, row t; and LdP^T column t into S0), r = dP . P
+      // dP row t: LdP (tile S5, row t; LdP^T is the same tile read M-major),
+      // r = dP . P
       tmem_ld32(tb + lane_off + 0 + cb * 32, t32);
       tmem_wait_ld_r(t32);
 #pragma unroll
@@ -1230,42 +1231,31 @@ __global__ void __launch_bounds__(kOutThr, 1)
         const float dp = __uint_as_float(t32[xx]);
         f32[xx] = s <= t ? __expf(ct - sc[s]) * dp : 0.f;
         rv[xx] *= dp;  // r = dP . P
-        st_shared_u16(S0 + elem_off(s, t), bf16_of(f32[xx]));
       }
 #pragma unroll
       for (int gg = 0; gg < 4; ++gg) st_shared_v4(S5 + tile_off(t, cb * 4 + gg), pack8(&f32[8 * gg]));
-      // dA row t = -strict_lower(dU E^T): db, r, and Msym (both triangles) into S3
+      // dA row t = -strict_lower(dU E^T): db, r, and M row t into S3 (Msym K is
+      // M K plus the same tile read M-major)
       float gkr[32];  // GK row t, columns cb*32 ..
       if (cb * 32 < r0 + 32) blk_ld32(gkr, gkb, t, cb * 32);
       tmem_ld32(tb + lane_off + 256 + cb * 32, t32);
       tmem_wait_ld_r(t32);
 #pragma unroll
-      for (int xx = 0; xx < 32; ++xx) {
-        const int s = cb * 32 + xx;
-        float mk = 0.f;
-        if (s < t) {
-          const float da = -__uint_as_float(t32[xx]);
-          const float gkv = gkr[xx];
-          dbt = fmaf(da, gkv, dbt);
-          rv[xx] = fmaf(da * bt, gkv, rv[xx]);
-          mk = da * bt * __expf(ct - sc[s]);
-        }
-        gkr[xx] = mk;  // M row t, column s (zero on and right of the diagonal)
-        if (s <= t) st_shared_u16(S3 + elem_off(s, t), bf16_of(mk));  // M^T: column t, row s
-      }
-      // M row t: whole 16-byte pieces left of the diagonal, single elements
-      // in the piece that holds it (only thread t writes row t at or left of
-      // column t; the rest of the row belongs to the other rows' M^T)
-#pragma unroll
       for (int gg = 0; gg < 4; ++gg) {
-        const int s0 = cb * 32 + 8 * gg;
-        if (s0 + 7 <= t) {
-          st_shared_v4(S3 + tile_off(t, cb * 4 + gg), pack8(&gkr[8 * gg]));
-        } else if (s0 <= t) {
+        float mk[8];  // M row t, columns 8 gg .. (zero on and right of the diagonal)
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (s0 + u <= t) st_shared_u16(S3 + elem_off(t, s0 + u), bf16_of(gkr[8 * gg + u]));
+        for (int u = 0; u < 8; ++u) {
+          const int xx = 8 * gg + u, s = cb * 32 + xx;
+          mk[u] = 0.f;
+          if (s < t) {
+            const float da = -__uint_as_float(t32[xx]);
+            const float gkv = gkr[xx];
+            dbt = fmaf(da, gkv, dbt);
+            rv[xx] = fmaf(da * bt, gkv, rv[xx]);
+            mk[u] = da * bt * __expf(ct - sc[s]);
+          }
         }
+        st_shared_v4(S3 + tile_off(t, cb * 4 + gg), pack8(mk));
       }
       // row sums of r stay with the thread; column sums over the warp's rows
       // by a shuffle exchange, one slot per (row quarter, column): summed in
@@ -1326,23 +1316,24 @@ __global__ void __launch_bounds__(kOutThr, 1)
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) f32[xx] = __uint_as_float(t32[xx]);
       row_st32(f32, dq + rowt + cb * 32, live);
-      // -(gamma b) dU into S5 for dK
+      // -(gamma b) dU into S0 for dK (LdP stays in S5)
       blk_ld32(f32, dUb, t, cb * 32);
 #pragma unroll
       for (int xx = 0; xx < 32; ++xx) f32[xx] *= f;
 #pragma unroll
-      for (int gg = 0; gg < 4; ++gg) st_shared_v4(S5 + tile_off(t, cb * 4 + gg), pack8(&f32[8 * gg]));
+      for (int gg = 0; gg < 4; ++gg) st_shared_v4(S0 + tile_off(t, cb * 4 + gg), pack8(&f32[8 * gg]));
     }
     ok = wait_copies();  // Q in S4
     fence_proxy_async_smem();
     tc_fence_before();
-    if (__syncthreads_or(!ok)) ok = false;  // S5 rows of both halves written; dQ read out of T0
-    // ---- round 3b: dK = LdP^T Q + Msym K - (gamma b dU) S -> T2 (+ w E G from T3)
+    if (__syncthreads_or(!ok)) ok = false;  // S0 rows of both halves written; dQ read out of T0
+    // ---- round 3b: dK = LdP^T Q + (M + M^T) K - (gamma b dU) S -> T2 (+ w E G from T3)
     if (ok && tid == 0) {
       tc_fence_after();
-      mma_group(tb + 256, S0, S4, true, false);
+      mma_group_amn(tb + 256, S5, S4, true, false);
       mma_group(tb + 256, S3, S1, true, true);
-      mma_group(tb + 256, S5, S2, true, true);
+      mma_group_amn(tb + 256, S3, S1, true, true);
+      mma_group(tb + 256, S0, S2, true, true);
       mma_commit(smem_u32(&bars[3]));
     }
     if (ok) ok = mbar_wait_warp(smem_u32(&bars[3]), 0, abortp);
