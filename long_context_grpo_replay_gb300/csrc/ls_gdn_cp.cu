@@ -419,9 +419,8 @@ __global__ void __launch_bounds__(kPrepThr, 1)
       }
     } else {
       // ---- group B: the right-hand sides (K K^T has read R0)
-      stage_rows<4>(sb + kPrepR0, v + row0, rs, nt, sbt, gt);  // b V
-      stage_rows<4>(sb + kPrepR1, k + row0, rs, nt, sbg, gt);  // b gamma K
-      stage_rows<4>(sb + kPrepR2, k + row0, rs, nt, swk, gt);  // w K
+      stage_rows<8>(sb + kPrepR0, v + row0, rs, nt, sbt, gt);                   // b V
+      stage_rows_pair<8>(sb + kPrepR1, sbg, sb + kPrepR2, swk, k + row0, rs, nt, gt);  // b gamma K, w K
     }
     if (!__syncthreads_or(!ok)) {
       float tcol[kC];

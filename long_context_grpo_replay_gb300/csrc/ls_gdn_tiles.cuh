@@ -77,6 +77,40 @@ __device__ __forceinline__ void stage_rows(uint32_t tile, const float* src, int6
     }
   }
 }
+// The same rows staged into two tiles at once, row r times scale_a[r] into
+// tile_a and times scale_b[r] into tile_b (both scales given): one pass of
+// global loads for two scaled copies.
+template <int kBatch = 8, int kWorkers = kThr>
+__device__ __forceinline__ void stage_rows_pair(uint32_t tile_a, const float* scale_a, uint32_t tile_b,
+                                                const float* scale_b, const float* src, int64_t stride,
+                                                int nt, int tid = threadIdx.x) {
+  constexpr int kPer = 2048 / kWorkers;  // 16-byte pieces per thread
+  static_assert(kPer % kBatch == 0, "batch divides the pieces per thread");
+#pragma unroll 1
+  for (int it0 = 0; it0 < kPer; it0 += kBatch) {
+    float4 a[kBatch], b[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int item = tid + kWorkers * (it0 + j), r = item >> 4, gq = item & 15;
+      a[j] = b[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r < nt) {
+        const float4* p = reinterpret_cast<const float4*>(src + r * stride + gq * 8);
+        a[j] = p[0], b[j] = p[1];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int item = tid + kWorkers * (it0 + j), r = item >> 4, gq = item & 15;
+      const float fa = r < nt ? scale_a[r] : 0.f, fb = r < nt ? scale_b[r] : 0.f;
+      const float xa[8] = {a[j].x * fa, a[j].y * fa, a[j].z * fa, a[j].w * fa,
+                           b[j].x * fa, b[j].y * fa, b[j].z * fa, b[j].w * fa};
+      const float xb[8] = {a[j].x * fb, a[j].y * fb, a[j].z * fb, a[j].w * fb,
+                           b[j].x * fb, b[j].y * fb, b[j].z * fb, b[j].w * fb};
+      st_shared_v4(tile_a + tile_off(r, gq), pack8(xa));
+      st_shared_v4(tile_b + tile_off(r, gq), pack8(xb));
+    }
+  }
+}
 // D[tmem] (+)= A B^T over K = 128 (eight K steps); B K-major or N-major.
 __device__ __forceinline__ void mma_group(uint32_t d, uint32_t a, uint32_t b, bool b_mn, bool acc) {
   const uint32_t id = idesc_bf16(128, 128, b_mn);
