@@ -1027,7 +1027,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
   tc_fence_after();
   const uint32_t tb = *tslot, lane_off = (uint32_t)((warp & 3) * 32) << 16;
   const volatile uint32_t* abortp = abort_s;
-  const uint32_t cbar = smem_u32(&bars[6]);  // the tile images' bulk copies, one phase per round
+  const uint32_t cbar = smem_u32(&bars[6]);  // the tile images' bulk copies, one phase per product step
   uint32_t ncp = 0, nwt = 0;  // copy phases issued, and waited for (every thread keeps both)
   int pend = -1;              // thread 0: parity of a copy phase whose wait gave up
   const bool live = t < nt;
@@ -1047,7 +1047,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
   if (tid == 0) {
     prefetch_l2(blk, 2 * kTileElems * 4);                             // E0, dU0
     prefetch_l2(blk + (int64_t)kGKblk * kTileElems, kTileElems * 4);  // GK
-    const uint32_t dst[4] = {S0, S1, S2, S3};  // ---- round 0 tiles: ZK, ZW, S, G
+    const uint32_t dst[4] = {S0, S1, S2, S3};  // ---- step 0 tiles: ZK, ZW, S, G
     const float* src[4] = {image_of(blk, kImZK), image_of(blk, kImZW), image_of(blk, kImS),
                            image_of(blk, kImG)};
     copy_tiles(cbar, 4, dst, src);
@@ -1060,7 +1060,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
     sgam[t] = expf(sc[t]);
     sw[t] = live ? expf(sc[kC - 1] - sc[t]) : 0.f;
   }
-  // ---- round 0: ZK S^T -> T0, ZW G^T -> T1; E into S3 (bf16), dU rows into
+  // ---- step 0: ZK S^T -> T0, ZW G^T -> T1; E into S3 (bf16), dU rows into
   // the scratch, and dV = diag(b) dU
   ok = wait_copies();
   if (!__syncthreads_or(!ok)) {
@@ -1073,7 +1073,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
     ok = mbar_wait_warp(smem_u32(&bars[5]), 0, abortp);
   }
   if (!__syncthreads_or(!ok)) {
-    if (tid == 0) {  // round 1 tiles: Q, K, dO (the round-0 products are done with S0, S1)
+    if (tid == 0) {  // step 1 tiles: Q, K, dO (the step-0 products are done with S0, S1)
       const uint32_t dst[3] = {S0, S1, S4};
       const float* src[3] = {image_of(blk, kImQ), image_of(blk, kImK), image_of(blk, kImDO)};
       copy_tiles(cbar, 3, dst, src);
@@ -1108,7 +1108,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
   tc_fence_before();
   __syncthreads();  // dU rows written before any thread reads them back
 
-  // ---- round 1: Q K^T -> T0, Q S^T -> T1, K S^T -> T2
+  // ---- step 1: Q K^T -> T0, Q S^T -> T1, K S^T -> T2
   if (ok) ok = wait_copies();
   fence_proxy_async_smem();
   if (__syncthreads_or(!ok)) ok = false;
@@ -1122,7 +1122,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
   if (ok) ok = mbar_wait_warp(smem_u32(&bars[0]), 0, abortp);
   float dgam = 0.f, dbt = 0.f, rrow = 0.f, rw = 0.f;  // this half's parts of the row sums
   if (!__syncthreads_or(!ok)) {
-    if (tid == 0) {  // round 2's G (the round-1 products are done with S1)
+    if (tid == 0) {  // step 2's G (the step-1 products are done with S1)
       const uint32_t dst[1] = {S1};
       const float* src[1] = {image_of(blk, kImG)};
       copy_tiles(cbar, 1, dst, src);
@@ -1173,7 +1173,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    // ---- round 2: P E -> T1 (onto gamma Q S^T), dO E^T -> T0, dU E^T -> T2, E G -> T3
+    // ---- step 2: P E -> T1 (onto gamma Q S^T), dO E^T -> T0, dU E^T -> T2, E G -> T3
     if (hf == 0) stage_row_blk(S0, dUb, t);
     ok = wait_copies();
     fence_proxy_async_smem();
@@ -1189,7 +1189,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
     if (ok) ok = mbar_wait_warp(smem_u32(&bars[1]), 0, abortp);
   }
   if (!__syncthreads_or(!ok)) {
-    if (tid == 0) {  // round 3a's K (the round-2 products are done with S1)
+    if (tid == 0) {  // step 3a's K (the step-2 products are done with S1)
       const uint32_t dst[1] = {S1};
       const float* src[1] = {image_of(blk, kImK)};
       copy_tiles(cbar, 1, dst, src);
@@ -1288,7 +1288,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
     fence_proxy_async_smem();
     tc_fence_before();
     if (__syncthreads_or(!ok)) ok = false;
-    // ---- round 3a: dQ = (gamma dO) S + LdP K -> T0
+    // ---- step 3a: dQ = (gamma dO) S + LdP K -> T0
     if (ok && tid == 0) {
       tc_fence_after();
       mma_group(tb + 0, S4, S2, true, false);
@@ -1298,7 +1298,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
     if (ok) ok = mbar_wait_warp(smem_u32(&bars[2]), 0, abortp);
   }
   if (!__syncthreads_or(!ok)) {
-    if (tid == 0) {  // round 3b's Q (the round-3a products are done with S4)
+    if (tid == 0) {  // step 3b's Q (the step-3a products are done with S4)
       const uint32_t dst[1] = {S4};
       const float* src[1] = {image_of(blk, kImQ)};
       copy_tiles(cbar, 1, dst, src);
@@ -1326,7 +1326,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
     fence_proxy_async_smem();
     tc_fence_before();
     if (__syncthreads_or(!ok)) ok = false;  // S0 rows of both halves written; dQ read out of T0
-    // ---- round 3b: dK = LdP^T Q + (M + M^T) K - (gamma b dU) S -> T2 (+ w E G from T3)
+    // ---- step 3b: dK = LdP^T Q + (M + M^T) K - (gamma b dU) S -> T2 (+ w E G from T3)
     if (ok && tid == 0) {
       tc_fence_after();
       mma_group_amn(tb + 256, S5, S4, true, false);
