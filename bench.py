@@ -256,18 +256,19 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
+    # one event between consecutive steps as well, for the per-step median
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     with ClockSampler(local) as clk:
-        e0.record(stream)
-        for _ in range(args.steps):
+        ev[0].record(stream)
+        for i in range(args.steps):
             step()
-        e1.record(stream)
+            ev[i + 1].record(stream)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     launches = ls.ls_launch_count() - launches0
-    ms_total = e0.elapsed_time(e1)
+    ms_total = ev[0].elapsed_time(ev[-1])
+    ms_median = statistics.median(ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps))
     trace = ls.kernel_trace()
     ls.ls_trace_enable(False)
     ls.ls_read_device_status(ws)
@@ -279,11 +280,18 @@ def run_ours(args):
                                / G / 2**30, 3),
     }
     ms_total = max_over_ranks(ms_total, dev)
+    ms_median = max_over_ranks(ms_median, dev)
     ms_step = ms_total / args.steps
     flops_step = sum(replay_flops(P, R, hq, d) for R in w.resp_lens)
     value = job_throughput(flops_step, world, ms_step)
     kv_bytes_pass = P * hkv * d * 2 * (2 if tdt == torch.bfloat16 else 4)
     kv_gbs = 2 * G * kv_bytes_pass * world / (ms_step * 1e-3) / 1e9
+    # the same with each member's own tensors counted once per pass that
+    # touches them: forward Q, K_r, V_r in, O and LSE out; preprocess O, dO in,
+    # D out; backward Q, K_r, V_r, dO, LSE, D in, dQ, dK, dV out
+    esz = 2 if tdt == torch.bfloat16 else 4
+    io_member = sum((7 * R * hq * d + 6 * R * hkv * d) * esz + 4 * R * hq * 4 for R in w.resp_lens)
+    kv_io_gbs = (2 * G * kv_bytes_pass + io_member) * world / (ms_step * 1e-3) / 1e9
 
     # ---- roofline of the dominant kernel (time from the traced events)
     pk, pk_src = peaks()
@@ -347,7 +355,9 @@ def run_ours(args):
                                     args.host_pages if host is not None else 0,
                                     args.host_pages_member_major),
             "prompt_kv_gbs": round(kv_gbs, 1),
+            "prompt_kv_and_member_io_gbs": round(kv_io_gbs, 1),
             "replays_per_s": round(G * world / (ms_step * 1e-3), 4),
+            "replays_per_s_median_step": round(G * world / (ms_median * 1e-3), 4),
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
