@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   const int64_t row0 = (t0 * H + h) * kD;
   if (gt < nt) prefetch_l2((grpA ? k : v) + row0 + gt * rs, kD * 4);  // the chunk's rows into L2
 
-  if (grpA) stage_rows<4>(sb + kPrepR0, k + row0, rs, nt, nullptr, gt, image_of(out, kImK));
+  if (grpA) stage_rows<16>(sb + kPrepR0, k + row0, rs, nt, nullptr, gt, image_of(out, kImK));
   scan_gates(gates, sc, sbt, swt);
   fence_proxy_async_smem();
   __syncthreads();
@@ -419,8 +419,8 @@ __global__ void __launch_bounds__(kPrepThr, 1)
       }
     } else {
       // ---- group B: the right-hand sides (K K^T has read R0)
-      stage_rows<8>(sb + kPrepR0, v + row0, rs, nt, sbt, gt);                   // b V
-      stage_rows_pair<8>(sb + kPrepR1, sbg, sb + kPrepR2, swk, k + row0, rs, nt, gt);  // b gamma K, w K
+      stage_rows<16>(sb + kPrepR0, v + row0, rs, nt, sbt, gt);                   // b V
+      stage_rows_pair<16>(sb + kPrepR1, sbg, sb + kPrepR2, swk, k + row0, rs, nt, gt);  // b gamma K, w K
     }
     if (!__syncthreads_or(!ok)) {
       float tcol[kC];
@@ -594,9 +594,9 @@ __global__ void __launch_bounds__(kPrepThr, 1)
   }
   if (gt < nt) prefetch_l2((grpA ? q : k) + row0 + gt * rs, kD * 4);  // q, k are read twice
   if (grpA)
-    stage_rows<4>(sb + kGr1, q + row0, rs, nt, nullptr, gt, image_of(out, kImQ));
+    stage_rows<16>(sb + kGr1, q + row0, rs, nt, nullptr, gt, image_of(out, kImQ));
   else
-    stage_rows<4>(sb + kGr2, d_o + row0, rs, nt, nullptr, gt, image_of(out, kImDO));
+    stage_rows<16>(sb + kGr2, d_o + row0, rs, nt, nullptr, gt, image_of(out, kImDO));
   scan_gates(gates, sc, sbt, swt);
   fence_proxy_async_smem();
   __syncthreads();
@@ -661,7 +661,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
           put_tile_row(true, sb + kGr3, nullptr, gt, f, cb * 4, 4);
         }
       } else {  // w K over P^T (G1), which dE0 has read
-        stage_rows<4>(sb + kGr1, k + row0, rs, nt, swk, gt);
+        stage_rows<16>(sb + kGr1, k + row0, rs, nt, swk, gt);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -697,7 +697,7 @@ __global__ void __launch_bounds__(kPrepThr, 1)
             for (int xx = 0; xx < 32; ++xx) f[xx] *= fa;
             put_tile_row(true, sb + kGr3, nullptr, r, f, cb * 4, 4);
           }
-          stage_rows<4>(sb + kGr4, q + row0, rs, nt, sgm, gt);
+          stage_rows<16>(sb + kGr4, q + row0, rs, nt, sgm, gt);
         } else {
           float* img = image_of(out, kImZW);
           const float fb = sbg[r];
@@ -1474,7 +1474,7 @@ __global__ void __launch_bounds__(kOutThr, 1)
     const float* src[3] = {image_of(blk, kImK), image_of(blk, kImS), image_of(blk, kImZK)};
     copy_tiles(cbar, 3, dst, src);
   }
-  if (hf == 0) stage_rows<4>(F0, q + row0, rs, nt, nullptr, t);
+  if (hf == 0) stage_rows<16>(F0, q + row0, rs, nt, nullptr, t);
   scan_gates(gates, sc, sbt, swt);
   bool ok = mbar_wait_warp(cbar, 0, abortp);
   const bool copied = ok;  // thread 0: the copies landed (else the drain waits for them)
