@@ -389,8 +389,14 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
       tc_fence_before();
       warp_arrive(smem_u32(&bar_sfree));  // dP_j may now overwrite X
       if (full) {
+        const uint64_t sc2 = f2(p.scale_log2, p.scale_log2), nl2 = f2(-lse2, -lse2);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pv[c] = ex2(fmaf(pv[c], p.scale_log2, -lse2));
+        for (int c = 0; c < 32; c += 2) {
+          float x0, x1;
+          f2_split(f2_fma(f2(pv[c], pv[c + 1]), sc2, nl2), x0, x1);
+          pv[c] = ex2(x0);
+          pv[c + 1] = ex2(x1);
+        }
       } else {
 #pragma unroll
         for (int c = 0; c < 32; ++c) pv[c] = c < nv ? ex2(fmaf(pv[c], p.scale_log2, -lse2)) : 0.f;
@@ -403,10 +409,16 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
         tmem_ld32(tX, rp);
         tmem_wait_ld_r(rp);
         if (full) {
+          // dS = P (dP - D), two keys per packed instruction
+          const uint64_t nd2 = f2(-dl, -dl);
 #pragma unroll
-          for (int c = 0; c < 32; c += 2)
-            ds_pk[c >> 1] = pack_bf16x2(pv[c] * (__uint_as_float(rp[c]) - dl),
-                                        pv[c + 1] * (__uint_as_float(rp[c + 1]) - dl));
+          for (int c = 0; c < 32; c += 2) {
+            float d0, d1;
+            f2_split(f2_mul(f2(pv[c], pv[c + 1]),
+                            f2_add(f2(__uint_as_float(rp[c]), __uint_as_float(rp[c + 1])), nd2)),
+                     d0, d1);
+            ds_pk[c >> 1] = pack_bf16x2(d0, d1);
+          }
         } else {
           // masked keys give dS = 0 exactly, whatever dP holds (NaN included)
 #pragma unroll

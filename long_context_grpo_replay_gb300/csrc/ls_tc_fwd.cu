@@ -443,14 +443,20 @@ __global__ void __launch_bounds__(kThreadsRing, 1)
       uint32_t pk[32];
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
       if (m_run != -CUDART_INF_F) {
-        const float nm = -m_run;
+        // the exponents' arguments and the row sums two keys per packed
+        // instruction
+        const uint64_t sc2 = f2(p.scale_log2, p.scale_log2), nm2 = f2(-m_run, -m_run);
+        uint64_t acc[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
-          const float p0 = ex2(fmaf(s[c], p.scale_log2, nm));
-          const float p1 = ex2(fmaf(s[c + 1], p.scale_log2, nm));
-          ps[(c >> 1) & 3] += p0 + p1;
+          float x0, x1;
+          f2_split(f2_fma(f2(s[c], s[c + 1]), sc2, nm2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          acc[(c >> 1) & 1] = f2_add(acc[(c >> 1) & 1], f2(p0, p1));
           pk[c >> 1] = pack_bf16x2(p0, p1);
         }
+        f2_split(acc[0], ps[0], ps[1]);
+        f2_split(acc[1], ps[2], ps[3]);
       } else {
 #pragma unroll
         for (int c = 0; c < 32; ++c) pk[c] = 0u;

@@ -94,6 +94,28 @@ inline uint32_t pack_bf16x2(float lo, float hi) {
   return emu::bf16_bits(lo) | (emu::bf16_bits(hi) << 16);
 }
 inline float2 unpack_bf16x2(uint32_t u) { return {emu::bf16_float(u), emu::bf16_float(u >> 16)}; }
+// packed float32 pairs: lane 0 in the low word, each lane rounded as the
+// scalar operation
+inline uint64_t f2(float lo, float hi) { return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32); }
+inline void f2_split(uint64_t r, float& lo, float& hi) {
+  lo = __uint_as_float((uint32_t)r);
+  hi = __uint_as_float((uint32_t)(r >> 32));
+}
+inline uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  float a0, a1, b0, b1, c0, c1;
+  f2_split(a, a0, a1), f2_split(b, b0, b1), f2_split(c, c0, c1);
+  return f2(std::fma(a0, b0, c0), std::fma(a1, b1, c1));
+}
+inline uint64_t f2_add(uint64_t a, uint64_t b) {
+  float a0, a1, b0, b1;
+  f2_split(a, a0, a1), f2_split(b, b0, b1);
+  return f2(a0 + b0, a1 + b1);
+}
+inline uint64_t f2_mul(uint64_t a, uint64_t b) {
+  float a0, a1, b0, b1;
+  f2_split(a, a0, a1), f2_split(b, b0, b1);
+  return f2(a0 * b0, a1 * b1);
+}
 inline uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   std::memcpy(&v, emu::smem_ptr(addr, 16), 16);
