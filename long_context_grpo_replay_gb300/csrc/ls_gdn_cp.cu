@@ -202,7 +202,8 @@ __device__ __forceinline__ void invert_block64(float* buf, const float* gk, cons
   for (int t8 = r0; t8 < r0 + 64; t8 += 8) {
     const int j = t8 >> 3;
     const float* gb = gk + gk_base(j);
-    float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    // the eight rows' sums in packed pairs (rows u, u+1 per 64-bit register)
+    uint64_t sp[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
     // eight columns s at a time (t8 - r0 is a multiple of 8): the inner loop
     // has a fixed length, so all of its 24 loads issue ahead of the FMAs
 #pragma unroll 1
@@ -217,12 +218,16 @@ __device__ __forceinline__ void invert_block64(float* buf, const float* gk, cons
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        sum[0] = fmaf(a[i].x, e[i], sum[0]), sum[1] = fmaf(a[i].y, e[i], sum[1]);
-        sum[2] = fmaf(a[i].z, e[i], sum[2]), sum[3] = fmaf(a[i].w, e[i], sum[3]);
-        sum[4] = fmaf(c[i].x, e[i], sum[4]), sum[5] = fmaf(c[i].y, e[i], sum[5]);
-        sum[6] = fmaf(c[i].z, e[i], sum[6]), sum[7] = fmaf(c[i].w, e[i], sum[7]);
+        const uint64_t ee = f2(e[i], e[i]);
+        sp[0] = f2_fma(f2(a[i].x, a[i].y), ee, sp[0]);
+        sp[1] = f2_fma(f2(a[i].z, a[i].w), ee, sp[1]);
+        sp[2] = f2_fma(f2(c[i].x, c[i].y), ee, sp[2]);
+        sp[3] = f2_fma(f2(c[i].z, c[i].w), ee, sp[3]);
       }
     }
+    float sum[8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) f2_split(sp[u], sum[2 * u], sum[2 * u + 1]);
     float ev[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -369,15 +374,16 @@ __global__ void __launch_bounds__(kPrepThr, 1)
       // rows 64 + 16 rq .. 64 + 16 rq + 15: the 16 rows' coefficients of one
       // column are shared by the warp and serve two columns per thread
       const int xc = x & 31, rq = x >> 5, t0r = 64 + 16 * rq;
-      float acc[2][16];
+      // acc[i]: rows t0r + i of columns xc and xc + 32, as one packed pair
+      uint64_t acc[16];
       {  // Y = diag(b) GK21 T11 into the block's place (T11 does not read it)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[0][i] = acc[1][i] = 0.f;
+        for (int i = 0; i < 16; ++i) acc[i] = f2(0.f, 0.f);
         const float* g0 = gk + gk_base(t0r >> 3);      // rows t0r .. t0r+7
         const float* g1 = gk + gk_base((t0r >> 3) + 1);  // rows t0r+8 .. t0r+15
 #pragma unroll 4
         for (int s = 0; s < 64; ++s) {
-          const float e0 = buf[b_at(s, xc)], e1 = buf[b_at(s, xc + 32)];
+          const uint64_t ee = f2(buf[b_at(s, xc)], buf[b_at(s, xc + 32)]);
           const float4 a0 = *reinterpret_cast<const float4*>(g0 + s * 8);
           const float4 a1 = *reinterpret_cast<const float4*>(g0 + s * 8 + 4);
           const float4 a2 = *reinterpret_cast<const float4*>(g1 + s * 8);
@@ -385,36 +391,36 @@ __global__ void __launch_bounds__(kPrepThr, 1)
           const float gcoef[16] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w,
                                    a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            acc[0][i] = fmaf(gcoef[i], e0, acc[0][i]);
-            acc[1][i] = fmaf(gcoef[i], e1, acc[1][i]);
-          }
+          for (int i = 0; i < 16; ++i) acc[i] = f2_fma(f2(gcoef[i], gcoef[i]), ee, acc[i]);
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          buf[b_at(t0r + i, xc)] = sbt[t0r + i] * acc[0][i];
-          buf[b_at(t0r + i, xc + 32)] = sbt[t0r + i] * acc[1][i];
+          float y0, y1;
+          f2_split(acc[i], y0, y1);
+          buf[b_at(t0r + i, xc)] = sbt[t0r + i] * y0;
+          buf[b_at(t0r + i, xc + 32)] = sbt[t0r + i] * y1;
         }
       }
       named_bar_sync(1, kThr);
       {  // T21 = -T22 Y (T22 stored with its zero upper triangle and unit diagonal)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[0][i] = acc[1][i] = 0.f;
+        for (int i = 0; i < 16; ++i) acc[i] = f2(0.f, 0.f);
 #pragma unroll 4
         for (int s = 0; s < 64; ++s) {
-          const float y0 = buf[b_at(64 + s, xc)], y1 = buf[b_at(64 + s, xc + 32)];
+          const uint64_t yy = f2(buf[b_at(64 + s, xc)], buf[b_at(64 + s, xc + 32)]);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float tc = buf[b_at(t0r + i, 64 + s)];
-            acc[0][i] = fmaf(tc, y0, acc[0][i]);
-            acc[1][i] = fmaf(tc, y1, acc[1][i]);
+            acc[i] = f2_fma(f2(tc, tc), yy, acc[i]);
           }
         }
         named_bar_sync(1, kThr);  // Y read everywhere before T21 overwrites it
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          buf[b_at(t0r + i, xc)] = -acc[0][i];
-          buf[b_at(t0r + i, xc + 32)] = -acc[1][i];
+          float t0v, t1v;
+          f2_split(acc[i], t0v, t1v);
+          buf[b_at(t0r + i, xc)] = -t0v;
+          buf[b_at(t0r + i, xc + 32)] = -t1v;
         }
       }
     } else {
